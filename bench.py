@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""SSD forward + backward throughput (tokens/s) on GB300.
+
+One step = ssd_fwd + ssd_bwd over one batch of the Mamba-2 layer workload
+(batch 4, seqlen 4096, 24 heads, headdim 64, d_state 128, 1 group, chunk 256,
+bf16 inputs, fp32 outputs and gradients), i.e. every step of the chunked scan
+and its backward.  Inputs are seeded synthetic data resident in HBM before the
+timed region; L2 (129 MB) is flushed by writing a 512 MB buffer before every
+timed step, outside the step's CUDA events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own batch (weak scaling, no
+collective on the data path); the reported time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "layer_fwdbwd_bf16"
+METRIC = "SSD fwd+bwd tokens/sec on 1 GB300; % tensor-pipe peak and HBM GB/s per kernel"
+UNIT = "tokens/s"
+FP32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x FMA x max clock
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_config(name, scaling_note):
+    from state_space_model_sm_gb300.inputs import WORKLOADS
+    shape, dtype, init_std, seed, _ = WORKLOADS[name]
+    return {"workload": f"{name}: SSD fwd+bwd batch={shape.batch} seqlen={shape.seqlen} "
+                        f"nheads={shape.nheads} headdim={shape.headdim} dstate={shape.dstate} "
+                        f"ngroups={shape.ngroups} chunk_size={shape.chunk_size}",
+            "batch": shape.batch, "seqlen": shape.seqlen, "nheads": shape.nheads,
+            "headdim": shape.headdim, "dstate": shape.dstate, "ngroups": shape.ngroups,
+            "chunk_size": shape.chunk_size, "input_dtype": dtype, "grad_dtype": "f32",
+            "seed": seed, "l2": scaling_note, "parallelism": "replicas (weak)"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# -------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import state_space_model_sm_gb300 as ssd
+    from state_space_model_sm_gb300 import roofline
+    from state_space_model_sm_gb300.inputs import WORKLOADS, make_inputs, to_torch
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ssd.build()
+    ssd.load_library()
+    shape, dtype, init_std, seed, _ = WORKLOADS[args.workload]
+    inp = make_inputs(shape, seed=seed + 1000 * rank, dtype=dtype, init_std=init_std,
+                      with_dy=True)
+    t = to_torch(inp, dev)
+    Bt, T, H, P, N, G, L = (shape.batch, shape.seqlen, shape.nheads, shape.headdim,
+                            shape.dstate, shape.ngroups, shape.chunk_size)
+    f32 = dict(dtype=torch.float32, device=dev)
+    y = torch.empty((Bt, T, H, P), **f32)
+    final = torch.empty((Bt, H, P, N), **f32)
+    grads = dict(dx=torch.empty((Bt, T, H, P), **f32), ddt=torch.empty((Bt, T, H), **f32),
+                 dA=torch.empty((H,), **f32), dB=torch.empty((Bt, T, G, N), **f32),
+                 dC=torch.empty((Bt, T, G, N), **f32), dD=torch.empty((H,), **f32),
+                 ddt_bias=torch.empty((H,), **f32))
+    if t["init"] is not None:
+        grads["dinit_states"] = torch.empty((Bt, H, P, N), **f32)
+    sh = ssd.make_shape(Bt, T, H, P, N, G, L, ssd.SSD_BF16 if dtype == "bf16" else ssd.SSD_F32,
+                        ssd.SSD_F32)
+    ws = torch.empty(max(ssd.fwd_workspace_bytes(sh), ssd.bwd_workspace_bytes(sh)),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def step(tt):
+        ssd.ssd_fwd(tt["x"], tt["dt"], tt["dt_bias"], tt["A"], tt["B"], tt["C"], tt["D"],
+                    chunk_size=L, init_states=tt["init"], workspace=ws, y=y, final_states=final)
+        ssd.ssd_bwd(tt["x"], tt["dt"], tt["dt_bias"], tt["A"], tt["B"], tt["C"], tt["D"], L,
+                    tt["init"], tt["dy"], None, workspace=ws, out=grads)
+
+    for _ in range(args.warmup):
+        step(t)
+    torch.cuda.synchronize()
+    if ssd.device_status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    stream = torch.cuda.current_stream(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    launches0 = ssd.launch_count()
+    ssd.profile_enable(True)
+    with ClockSampler(local) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            step(t)
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    launches = ssd.launch_count() - launches0
+    prof = ssd.profile_read()
+    ssd.profile_enable(False)
+    if ssd.device_status() != 0:
+        raise RuntimeError("device status word set during the timed region")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = float(sum(step_ms))
+    if world > 1:
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    tokens = Bt * T * world * args.steps
+    value = tokens / (total_ms / 1e3)
+
+    # dominant kernel and its roofline
+    rd = roofline.Dims(Bt, T, H, P, N, G, L, ib=2 if dtype == "bf16" else 4, ob=4)
+    per_kernel = {k: {"ms_total": v[0], "launches": v[1], "us_per_launch": 1e3 * v[0] / v[1]}
+                  for k, v in prof.items() if v[1] > 0}
+    dom = max(per_kernel, key=lambda k: per_kernel[k]["ms_total"])
+    peaks = load_peaks()
+    roof = kernel_roofline(dom, per_kernel[dom], rd, peaks, roofline)
+    kernels_out = {}
+    for k, v in per_kernel.items():
+        r = kernel_roofline(k, v, rd, peaks, roofline)
+        kernels_out[k] = {"us": round(v["us_per_launch"], 2), "launches_per_step":
+                          v["launches"] / args.steps, "share": round(v["ms_total"] / sum(
+                              x["ms_total"] for x in per_kernel.values()), 4),
+                          "hbm_GBps": round(r["hbm_GBps"], 1), "bound": r["bound"],
+                          "frac": round(r["frac"], 4)}
+
+    # end to end: host (pinned) buffers through the same C-ABI calls
+    e2e = None
+    if rank == 0 or world > 1:
+        e2e = run_e2e(args, inp, t, step, y, final, grads, dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample(args.workload)
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in / f32 accum+grads",
+            "data": "synthetic (seeded PCG64, workload distributions)",
+            "config": workload_config(args.workload, "flushed (512 MB write) before every step"),
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clk.summary(), "kernels": kernels_out, "path": ssd.last_path(),
+            "gpu": torch.cuda.get_device_name(dev),
+            "step_flops_algorithmic": roofline.step_flops(rd),
+        }
+        print(json.dumps(out))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm": float(p.get("hbm_gbs")), "bf16": float(p.get("bf16_tflops")),
+                "bf16_sustained": float(p.get("bf16_tflops_sustained", p.get("bf16_tflops"))),
+                "source": "measured"}
+    return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_roofline(name, v, rd, peaks, roofline):
+    sec = v["us_per_launch"] / 1e6
+    nbytes = roofline.kernel_bytes(name, rd)
+    gbs = nbytes / sec / 1e9
+    try:
+        flops = roofline.kernel_flops(name, rd)
+    except KeyError:
+        flops = None
+    path_tc = False
+    try:
+        import state_space_model_sm_gb300 as ssd
+        path_tc = ssd.last_path() == 1
+    except Exception:
+        pass
+    if flops is not None and not path_tc:
+        # generic SIMT contraction: bounded by the fp32 ALUs
+        ach = flops / sec / 1e12
+        return {"kernel": name, "bound": "alu", "achieved": round(ach, 3),
+                "peak": round(FP32_ALU_PEAK_TFLOPS, 1), "unit": "TFLOP/s",
+                "frac": ach / FP32_ALU_PEAK_TFLOPS, "traffic": None, "hbm_GBps": gbs,
+                "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2070 MHz"}
+    return {"kernel": name, "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"],
+            "unit": "GB/s", "frac": gbs / peaks["hbm"], "traffic": None, "hbm_GBps": gbs,
+            "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+            "peak_source": peaks["source"]}
+
+
+def run_e2e(args, inp, t, step, y, final, grads, dev):
+    """Same step through the public API with pinned host buffers: every step
+    copies its inputs host->device and reads y, final and all gradients back."""
+    import torch
+    names_in = [k for k in ("x", "dt", "dt_bias", "A", "B", "C", "D", "init", "dy")
+                if t[k] is not None]
+    host_in = {k: t[k].cpu().pin_memory() for k in names_in}
+    dev_in = {k: torch.empty_like(t[k]) for k in names_in}
+    outs = [y, final] + list(grads.values())
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    tt = {k: None for k in t}
+    tt.update(dev_in)
+    stream = torch.cuda.current_stream(dev)
+    n = max(3, min(args.steps, 10))
+    for i in range(n + 2):
+        if i == 2:
+            torch.cuda.synchronize()
+            s = torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+        for k in names_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        step(tt)
+        for o, h in zip(outs, host_out):
+            h.copy_(o, non_blocking=True)
+    e = torch.cuda.Event(enable_timing=True)
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    tokens = inp.shape.batch * inp.shape.seqlen
+    return {"value": round(tokens / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------------ CPU oracle
+def cpu_baseline_sample(workload, min_seconds=10.0):
+    """The CPU oracle (fp64 recurrence, forward + reverse sweep, as it stands)
+    on batch rows of the same workload, repeated until >= min_seconds."""
+    import numpy as np
+
+    import oracle
+    from state_space_model_sm_gb300.inputs import WORKLOADS, SSDShape, make_inputs
+    shape, dtype, init_std, seed, _ = WORKLOADS[workload]
+    one = SSDShape(1, shape.seqlen, shape.nheads, shape.headdim, shape.dstate, shape.ngroups,
+                   shape.chunk_size)
+    inp = make_inputs(one, seed=seed, dtype=dtype, init_std=init_std, with_dy=True)
+    args = oracle.from_inputs(inp)
+    dy = inp.dy.astype(np.float64)
+    cores = oracle.hardware_threads()
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.ssd_fwd(*args, nthreads=cores)
+        oracle.ssd_bwd(*args, dy, None, nthreads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= 50:
+            break
+    tokens = reps * one.seqlen
+    return {"value": round(tokens / el, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{reps} x (batch row 0 of {workload}: seqlen {one.seqlen}, "
+                      f"{one.nheads} heads), fp64 forward + backward, {el:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the CPU oracle as it stands on the host cores, on a
+    bounded sample (one batch row) of the same workload per step."""
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from state_space_model_sm_gb300.inputs import WORKLOADS, SSDShape, make_inputs
+    shape, dtype, init_std, seed, _ = WORKLOADS[args.workload]
+    one = SSDShape(1, shape.seqlen, shape.nheads, shape.headdim, shape.dstate, shape.ngroups,
+                   shape.chunk_size)
+    inp = make_inputs(one, seed=seed, dtype=dtype, init_std=init_std, with_dy=True)
+    a = oracle.from_inputs(inp)
+    dy = inp.dy.astype(np.float64)
+    cores = oracle.hardware_threads()
+
+    def step():
+        oracle.ssd_fwd(*a, nthreads=cores)
+        oracle.ssd_bwd(*a, dy, None, nthreads=cores)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = args.steps * one.seqlen / el
+    sample = (f"per step: batch row 0 of {args.workload} (seqlen {one.seqlen}, "
+              f"{one.nheads} heads), fp64 forward + backward")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * el / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args.workload, "n/a (host)"),
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}))
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

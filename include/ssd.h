@@ -1,0 +1,132 @@
+/*
+ * ssd.h -- C ABI of libssd: the Mamba-2 SSD chunked selective scan on one
+ * GB300 (sm_103a).
+ *
+ * The operation (forward): for every batch b and head h, with g(h) = h/(H/G)
+ *     delta_t = softplus(dt[b,t,h] + dt_bias[h])          (softplus(v) = v for v > 20)
+ *     h_t     = exp(delta_t * A[h]) * h_{t-1} + delta_t * x_t (outer) B_t[g(h)]
+ *     y_t     = C_t[g(h)] . h_t + D[h] * x_t,     h_{-1} = init,  final = h_{T-1}
+ * computed by the chunked algorithm of the pages: chunk_cumsum, chunk_state,
+ * state_passing and chunk_scan ("Optimizing Mamba-2 kernels for the B200",
+ * Stage 1 kernel table, fwd_2 / fwd_3 / fwd_5; "Mamba-2 offers a different
+ * scaling path": chunk_cumsum, fwd_pass_state, compute_out).  The backward
+ * returns the gradients of L = <dy, y> + <dfinal, final> with respect to every
+ * input (same kernel table, bwd_5 .. bwd_16; the forward states are recomputed
+ * inside ssd_bwd, as bwd_5 and bwd_6 do on the pages).
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are dense, row-major, caller-owned DEVICE memory on the
+ *     current CUDA device.  The library never allocates, frees or keeps a
+ *     pointer after the call returns (asynchronously, on `stream`).
+ *   - Shapes (B = batch, T = seqlen, H = nheads, P = headdim, N = dstate,
+ *     G = ngroups):
+ *         x, y, dy, dx         (B, T, H, P)     dtype in_dtype / out_dtype / in_dtype / f32
+ *         dt, ddt              (B, T, H)        in_dtype / f32
+ *         B, C, dB, dC         (B, T, G, N)     in_dtype / f32
+ *         dt_bias, A, D, dA, dD, ddt_bias   (H) f32
+ *         init, final, dfinal, dinit        (B, H, P, N) f32
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     launch goes to that stream; no call synchronises the host.
+ *   - Every pointer must be aligned to its element size; the tensor-core fast
+ *     path additionally needs 16-byte alignment of x, B, C, dy, y (it is only
+ *     chosen when that holds).
+ *   - Errors: a host-side check that fails returns before anything is
+ *     launched.  A failed launch returns SSD_ERR_CUDA.  Kernels never trap:
+ *     a bounded wait that times out on the device records SSD_ERR_TIMEOUT in a
+ *     device status word, which ssd_get_device_status() reads and clears.
+ *   - No entry point throws or exits; all are thread-safe.
+ */
+#ifndef SSD_H_
+#define SSD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SSD_OK = 0,
+  SSD_ERR_INVALID_ARG = 1, /* bad shape, NULL required pointer, misalignment */
+  SSD_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement   */
+  SSD_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than the size query   */
+  SSD_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed            */
+  SSD_ERR_TIMEOUT = 5      /* a device-side bounded wait expired              */
+} ssd_status;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+/* Problem description.  Limits: every extent >= 1; nheads % ngroups == 0;
+ * 1 <= chunk_size <= 256; headdim * dstate <= 16384.  seqlen need not be a
+ * multiple of chunk_size (the last chunk is partial). */
+typedef struct {
+  int64_t batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size;
+  int32_t in_dtype;  /* ssd_dtype of x, dt, B, C (and dy in ssd_bwd) */
+  int32_t out_dtype; /* ssd_dtype of y                                */
+} ssd_shape;
+
+/* Byte offsets, inside the ssd_fwd workspace, of the intermediates the
+ * forward leaves there (all f32; nc = ceil(seqlen / chunk_size)):
+ *   delta     (B, H, nc, L)       softplus(dt + dt_bias), 0 on the padded tail
+ *   dA_cumsum (B, H, nc, L)       in-chunk inclusive cumsum of delta * A
+ *   states    (B, nc, H, P, N)    chunk_state output S_c
+ *   hprev     (B, nc, H, P, N)    state entering chunk c (state_passing output)
+ * They stay valid until the workspace is reused. */
+typedef struct {
+  size_t delta, dA_cumsum, states, hprev, total;
+} ssd_fwd_layout;
+
+/* Workspace bytes needed by ssd_fwd / ssd_bwd for this shape (0 if the shape
+ * is invalid).  The workspace is caller-owned device memory, 256-byte aligned. */
+size_t ssd_fwd_workspace_size(const ssd_shape* shape);
+size_t ssd_bwd_workspace_size(const ssd_shape* shape);
+int ssd_fwd_workspace_layout(const ssd_shape* shape, ssd_fwd_layout* out);
+
+/* Forward.  dt_bias, D, init and final_states may be NULL (zero bias, no skip
+ * term, zero initial state, final state not written). */
+int ssd_fwd(const ssd_shape* shape, const void* x, const void* dt, const float* dt_bias,
+            const float* A, const void* B, const void* C, const float* D,
+            const float* init_states, void* y, float* final_states, void* workspace,
+            size_t workspace_bytes, void* stream);
+
+/* Backward.  Takes the forward inputs (not saved states) plus dy and an
+ * optional dfinal_states (NULL = 0).  Writes dx, ddt (w.r.t. the raw dt
+ * input), dA, dB and dC (summed over the heads of each group); dD, ddt_bias
+ * and dinit_states may be NULL (not written).  Reductions are deterministic:
+ * repeated calls give bit-identical results. */
+int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* dt_bias,
+            const float* A, const void* B, const void* C, const float* D,
+            const float* init_states, const void* dy, const float* dfinal_states, float* dx,
+            float* ddt, float* dA, float* dB, float* dC, float* dD, float* ddt_bias,
+            float* dinit_states, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, returns the device status word of the current
+ * device (SSD_OK or SSD_ERR_TIMEOUT) and clears it. */
+int ssd_get_device_status(void* stream);
+
+/* Which kernel family the last ssd_fwd / ssd_bwd on this host thread used:
+ * 0 = generic SIMT path, 1 = tcgen05 tensor-core path. */
+int ssd_last_path(void);
+
+/* Optional per-kernel timing.  ssd_profile_enable(1) clears the counters and
+ * brackets every later kernel launch of this library with two CUDA events on
+ * its launch stream; ssd_profile_enable(0) stops.  ssd_profile_read waits for
+ * the recorded events and writes, for up to max_kernels kernel names, the name
+ * (64 bytes each, NUL-terminated, into `names`), the summed device time in ms
+ * and the number of launches; it returns the number of entries (or
+ * -SSD_ERR_CUDA).  Any output pointer may be NULL. */
+int ssd_profile_enable(int on);
+int ssd_profile_read(int max_kernels, char* names, double* ms, int64_t* launches);
+
+/* Number of kernels this library has launched in this process. */
+int64_t ssd_launch_count(void);
+
+/* Static description of a status code. */
+const char* ssd_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_H_ */

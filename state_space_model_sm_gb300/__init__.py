@@ -1,1 +1,223 @@
-"""Mamba-2 SSD chunked selective scan for GB300 (sm_103a)."""
+"""Mamba-2 SSD chunked selective scan for GB300 (sm_103a).
+
+Thin binding over the C ABI in ``include/ssd.h``: it checks torch tensors,
+allocates outputs and workspace with torch's caching allocator, and passes
+raw device pointers plus the current CUDA stream to libssd.  Every step of
+the computation runs in the library's CUDA kernels; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+from . import _native
+from ._native import build  # noqa: F401
+
+SSD_F32, SSD_BF16 = 0, 1
+
+
+class SSDError(RuntimeError):
+    def __init__(self, fn, status):
+        lib = _native.load()
+        super().__init__(f"{fn} failed: status {status} ({lib.ssd_strerror(status).decode()})")
+        self.status = status
+
+
+def load_library():
+    return _native.load()
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t == torch.float32:
+        return SSD_F32
+    if t == torch.bfloat16:
+        return SSD_BF16
+    raise TypeError(f"unsupported dtype {t}; use float32 or bfloat16")
+
+
+def make_shape(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, in_dtype=SSD_BF16,
+               out_dtype=SSD_F32) -> _native.Shape:
+    return _native.Shape(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, in_dtype,
+                         out_dtype)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, name, shape, dtype, device):
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: expected device {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def _shape_from(x, B, chunk_size, out_dtype):
+    Bt, T, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    return make_shape(Bt, T, H, P, N, G, chunk_size, _dtype_code(x.dtype), _dtype_code(out_dtype))
+
+
+def _validate(x, dt, dt_bias, A, B, C, D, init_states):
+    torch = _torch()
+    if x.dim() != 4 or B.dim() != 4:
+        raise ValueError("x must be (batch, seqlen, nheads, headdim), B/C (batch, seqlen, ngroups, dstate)")
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("tensors must live on a CUDA device")
+    Bt, T, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    _check(x, "x", (Bt, T, H, P), x.dtype, dev)
+    _check(dt, "dt", (Bt, T, H), x.dtype, dev)
+    _check(B, "B", (Bt, T, G, N), x.dtype, dev)
+    _check(C, "C", (Bt, T, G, N), x.dtype, dev)
+    _check(A, "A", (H,), torch.float32, dev)
+    _check(dt_bias, "dt_bias", (H,), torch.float32, dev)
+    _check(D, "D", (H,), torch.float32, dev)
+    _check(init_states, "init_states", (Bt, H, P, N), torch.float32, dev)
+    return Bt, T, H, P, N, G
+
+
+def fwd_workspace_bytes(shape) -> int:
+    return int(_native.load().ssd_fwd_workspace_size(ctypes.byref(shape)))
+
+
+def bwd_workspace_bytes(shape) -> int:
+    return int(_native.load().ssd_bwd_workspace_size(ctypes.byref(shape)))
+
+
+def fwd_workspace_layout(shape) -> dict:
+    lay = _native.FwdLayout()
+    st = _native.load().ssd_fwd_workspace_layout(ctypes.byref(shape), ctypes.byref(lay))
+    if st != 0:
+        raise SSDError("ssd_fwd_workspace_layout", st)
+    return dict(delta=lay.delta, dA_cumsum=lay.dA_cumsum, states=lay.states, hprev=lay.hprev,
+                total=lay.total)
+
+
+def _workspace(nbytes, device, workspace):
+    torch = _torch()
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return workspace
+    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+
+
+def ssd_fwd(x, dt, dt_bias, A, B, C, D=None, chunk_size: int = 256, init_states=None,
+            out_dtype=None, return_final_states: bool = True, workspace=None, y=None,
+            final_states=None):
+    """y, final_states = SSD(x, dt, A, B, C, D, init_states) by the chunked scan.
+
+    x (b, t, h, p), dt (b, t, h), B/C (b, t, g, n) in float32 or bfloat16 (one
+    dtype for all four); dt_bias, A, D (h,) and init_states (b, h, p, n) float32.
+    y is float32 by default (``out_dtype=torch.bfloat16`` for bf16)."""
+    torch = _torch()
+    lib = _native.load()
+    Bt, T, H, P, N, G = _validate(x, dt, dt_bias, A, B, C, D, init_states)
+    out_dtype = torch.float32 if out_dtype is None else out_dtype
+    shape = _shape_from(x, B, chunk_size, out_dtype)
+    if y is None:
+        y = torch.empty((Bt, T, H, P), dtype=out_dtype, device=x.device)
+    _check(y, "y", (Bt, T, H, P), out_dtype, x.device)
+    if return_final_states and final_states is None:
+        final_states = torch.empty((Bt, H, P, N), dtype=torch.float32, device=x.device)
+    ws_bytes = lib.ssd_fwd_workspace_size(ctypes.byref(shape))
+    if ws_bytes == 0:
+        raise ValueError("invalid SSD shape")
+    ws = _workspace(ws_bytes, x.device, workspace)
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    st = lib.ssd_fwd(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B),
+                     _ptr(C), _ptr(D), _ptr(init_states), _ptr(y),
+                     _ptr(final_states) if return_final_states else None, _ptr(ws),
+                     ctypes.c_size_t(ws.numel()), ctypes.c_void_p(stream))
+    if st != 0:
+        raise SSDError("ssd_fwd", st)
+    return y, (final_states if return_final_states else None)
+
+
+def ssd_bwd(x, dt, dt_bias, A, B, C, D, chunk_size: int, init_states, dy, dfinal_states=None,
+            workspace=None, out=None):
+    """Gradients of <dy, y> + <dfinal, final> w.r.t. every input of ssd_fwd.
+
+    Returns a dict with dx, ddt, dA, dB, dC (float32, shapes of the inputs)
+    and dD, ddt_bias, dinit_states (when D / init_states are given; dD and
+    ddt_bias are always returned)."""
+    torch = _torch()
+    lib = _native.load()
+    Bt, T, H, P, N, G = _validate(x, dt, dt_bias, A, B, C, D, init_states)
+    _check(dy, "dy", (Bt, T, H, P), x.dtype, x.device)
+    _check(dfinal_states, "dfinal_states", (Bt, H, P, N), torch.float32, x.device)
+    shape = _shape_from(x, B, chunk_size, torch.float32)
+    f32 = dict(dtype=torch.float32, device=x.device)
+    if out is None:
+        out = dict(dx=torch.empty((Bt, T, H, P), **f32), ddt=torch.empty((Bt, T, H), **f32),
+                   dA=torch.empty((H,), **f32), dB=torch.empty((Bt, T, G, N), **f32),
+                   dC=torch.empty((Bt, T, G, N), **f32), dD=torch.empty((H,), **f32),
+                   ddt_bias=torch.empty((H,), **f32))
+        if init_states is not None:
+            out["dinit_states"] = torch.empty((Bt, H, P, N), **f32)
+    ws_bytes = lib.ssd_bwd_workspace_size(ctypes.byref(shape))
+    if ws_bytes == 0:
+        raise ValueError("invalid SSD shape")
+    ws = _workspace(ws_bytes, x.device, workspace)
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    st = lib.ssd_bwd(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B),
+                     _ptr(C), _ptr(D), _ptr(init_states), _ptr(dy), _ptr(dfinal_states),
+                     _ptr(out["dx"]), _ptr(out["ddt"]), _ptr(out["dA"]), _ptr(out["dB"]),
+                     _ptr(out["dC"]), _ptr(out.get("dD")), _ptr(out.get("ddt_bias")),
+                     _ptr(out.get("dinit_states")), _ptr(ws), ctypes.c_size_t(ws.numel()),
+                     ctypes.c_void_p(stream))
+    if st != 0:
+        raise SSDError("ssd_bwd", st)
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronise and read/clear the library's device status word."""
+    torch = _torch()
+    s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+    return int(_native.load().ssd_get_device_status(ctypes.c_void_p(s)))
+
+
+def last_path() -> int:
+    """0 = generic SIMT kernels, 1 = tcgen05 tensor-core kernels (last call, this thread)."""
+    return int(_native.load().ssd_last_path())
+
+
+def profile_enable(on: bool = True) -> None:
+    """Start (clearing previous totals) or stop per-kernel CUDA-event timing."""
+    _native.load().ssd_profile_enable(1 if on else 0)
+
+
+def profile_read(max_kernels: int = 64) -> dict:
+    """{kernel name: (total device ms, launches)} since profile_enable(True)."""
+    lib = _native.load()
+    names = ctypes.create_string_buffer(64 * max_kernels)
+    ms = (ctypes.c_double * max_kernels)()
+    cnt = (ctypes.c_int64 * max_kernels)()
+    n = lib.ssd_profile_read(max_kernels, names, ms, cnt)
+    if n < 0:
+        raise SSDError("ssd_profile_read", -n)
+    out = {}
+    for i in range(n):
+        nm = names.raw[64 * i:64 * (i + 1)].split(b"\0", 1)[0].decode()
+        out[nm] = (ms[i], cnt[i])
+    return out
+
+
+def launch_count() -> int:
+    """Kernels launched by libssd in this process so far."""
+    return int(_native.load().ssd_launch_count())

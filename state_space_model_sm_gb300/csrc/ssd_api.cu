@@ -1,0 +1,256 @@
+// C ABI of libssd (declared in include/ssd.h): argument checks, workspace
+// carving and dispatch to the kernel families.
+#include <cstring>
+
+#include "ssd_internal.h"
+
+namespace ssd {
+
+__device__ int g_device_status = 0;
+
+int* device_status_ptr() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
+
+namespace {
+
+thread_local int t_last_path = 0;
+
+constexpr size_t kAlign = 256;
+
+bool valid_dtype(int32_t v) { return v == SSD_F32 || v == SSD_BF16; }
+
+int make_dims(const ssd_shape* s, Dims* d) {
+  if (!s) return SSD_ERR_INVALID_ARG;
+  if (s->batch < 1 || s->seqlen < 1 || s->nheads < 1 || s->headdim < 1 || s->dstate < 1 ||
+      s->ngroups < 1 || s->chunk_size < 1)
+    return SSD_ERR_INVALID_ARG;
+  if (s->nheads % s->ngroups != 0) return SSD_ERR_INVALID_ARG;
+  if (!valid_dtype(s->in_dtype) || !valid_dtype(s->out_dtype)) return SSD_ERR_INVALID_ARG;
+  if (s->chunk_size > 256) return SSD_ERR_UNSUPPORTED;
+  if (s->headdim * s->dstate > 16384) return SSD_ERR_UNSUPPORTED;
+  // Keep every tensor's element count within int64 and every per-dimension
+  // index within int32 (the kernels index a dimension with int).
+  const int64_t lim = (int64_t)1 << 31;
+  if (s->batch >= lim || s->seqlen >= lim || s->nheads >= 65536 || s->batch >= 65536)
+    return SSD_ERR_UNSUPPORTED;
+  const int64_t nc = (s->seqlen + s->chunk_size - 1) / s->chunk_size;
+  if (nc >= lim) return SSD_ERR_UNSUPPORTED;
+  d->B = (int)s->batch;
+  d->T = (int)s->seqlen;
+  d->H = (int)s->nheads;
+  d->P = (int)s->headdim;
+  d->N = (int)s->dstate;
+  d->G = (int)s->ngroups;
+  d->L = (int)s->chunk_size;
+  d->nc = (int)nc;
+  d->in_bf16 = s->in_dtype == SSD_BF16;
+  d->out_bf16 = s->out_dtype == SSD_BF16;
+  return SSD_OK;
+}
+
+struct Carver {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, kAlign);
+    return o;
+  }
+};
+
+struct FwdOffsets {
+  size_t delta, acs, S, Hprev, CB, total;
+};
+
+FwdOffsets fwd_offsets(const Dims& d) {
+  Carver c;
+  const size_t vec = (size_t)d.B * d.H * d.nc * d.L * sizeof(float);
+  const size_t st = (size_t)d.B * d.nc * d.H * d.P * d.N * sizeof(float);
+  FwdOffsets o;
+  o.delta = c.take(vec);
+  o.acs = c.take(vec);
+  o.S = c.take(st);
+  o.Hprev = c.take(st);
+  o.CB = c.take((size_t)d.B * d.nc * d.G * d.L * d.L * sizeof(float));
+  o.total = c.off;
+  return o;
+}
+
+struct BwdOffsets {
+  FwdOffsets f;
+  size_t dHs, dS, dlast, dyx, qrow, ddir, ycs, dBh, dCh, part, total;
+};
+
+BwdOffsets bwd_offsets(const Dims& d) {
+  BwdOffsets o;
+  o.f = fwd_offsets(d);
+  Carver c;
+  c.off = o.f.total;
+  const size_t vec = (size_t)d.B * d.H * d.nc * d.L * sizeof(float);
+  const size_t st = (size_t)d.B * d.nc * d.H * d.P * d.N * sizeof(float);
+  const size_t ph = (size_t)d.B * d.T * d.H * d.N * sizeof(float);
+  o.dHs = c.take(st);
+  o.dS = c.take(st);
+  o.dlast = c.take((size_t)d.B * d.H * d.nc * sizeof(float));
+  o.dyx = c.take((size_t)d.B * d.nc * d.H * d.L * d.L * sizeof(float));
+  o.qrow = c.take(vec);
+  o.ddir = c.take(vec);
+  o.ycs = c.take(vec);
+  o.dBh = c.take(ph);
+  o.dCh = c.take(ph);
+  o.part = c.take((size_t)d.B * d.H * d.nc * 3 * sizeof(float));
+  o.total = c.off;
+  return o;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int check_fwd_ptrs(const Dims& d, const FwdArgs& a) {
+  if (!a.x || !a.dt || !a.A || !a.B || !a.C) return SSD_ERR_INVALID_ARG;
+  const size_t in = d.in_bf16 ? 2 : 4;
+  if (!aligned(a.x, in) || !aligned(a.dt, in) || !aligned(a.B, in) || !aligned(a.C, in))
+    return SSD_ERR_INVALID_ARG;
+  const float* fp[] = {a.dt_bias, a.A, a.D, a.init, a.final_state};
+  for (const float* p : fp)
+    if (p && !aligned(p, 4)) return SSD_ERR_INVALID_ARG;
+  return SSD_OK;
+}
+
+FwdWs carve_fwd(char* base, const FwdOffsets& o) {
+  FwdWs w;
+  w.delta = reinterpret_cast<float*>(base + o.delta);
+  w.acs = reinterpret_cast<float*>(base + o.acs);
+  w.S = reinterpret_cast<float*>(base + o.S);
+  w.Hprev = reinterpret_cast<float*>(base + o.Hprev);
+  w.CB = reinterpret_cast<float*>(base + o.CB);
+  return w;
+}
+
+}  // namespace
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" {
+
+size_t ssd_fwd_workspace_size(const ssd_shape* shape) {
+  Dims d;
+  if (make_dims(shape, &d) != SSD_OK) return 0;
+  return fwd_offsets(d).total;
+}
+
+size_t ssd_bwd_workspace_size(const ssd_shape* shape) {
+  Dims d;
+  if (make_dims(shape, &d) != SSD_OK) return 0;
+  return bwd_offsets(d).total;
+}
+
+int ssd_fwd_workspace_layout(const ssd_shape* shape, ssd_fwd_layout* out) {
+  Dims d;
+  const int st = make_dims(shape, &d);
+  if (st != SSD_OK) return st;
+  if (!out) return SSD_ERR_INVALID_ARG;
+  const FwdOffsets o = fwd_offsets(d);
+  out->delta = o.delta;
+  out->dA_cumsum = o.acs;
+  out->states = o.S;
+  out->hprev = o.Hprev;
+  out->total = o.total;
+  return SSD_OK;
+}
+
+int ssd_fwd(const ssd_shape* shape, const void* x, const void* dt, const float* dt_bias,
+            const float* A, const void* B, const void* C, const float* D,
+            const float* init_states, void* y, float* final_states, void* workspace,
+            size_t workspace_bytes, void* stream) {
+  Dims d;
+  int st = make_dims(shape, &d);
+  if (st != SSD_OK) return st;
+  FwdArgs a{x, dt, dt_bias, A, B, C, D, init_states, y, final_states};
+  st = check_fwd_ptrs(d, a);
+  if (st != SSD_OK) return st;
+  if (!y || !aligned(y, d.out_bf16 ? 2 : 4)) return SSD_ERR_INVALID_ARG;
+  const FwdOffsets o = fwd_offsets(d);
+  if (!workspace || workspace_bytes < o.total || !aligned(workspace, kAlign))
+    return SSD_ERR_WORKSPACE;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const FwdWs w = carve_fwd(static_cast<char*>(workspace), o);
+  t_last_path = 0;
+  return simt_forward(d, a, w, s) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* dt_bias,
+            const float* A, const void* B, const void* C, const float* D,
+            const float* init_states, const void* dy, const float* dfinal_states, float* dx,
+            float* ddt, float* dA, float* dB, float* dC, float* dD, float* ddt_bias,
+            float* dinit_states, void* workspace, size_t workspace_bytes, void* stream) {
+  Dims d;
+  int st = make_dims(shape, &d);
+  if (st != SSD_OK) return st;
+  BwdArgs a;
+  a.f = FwdArgs{x, dt, dt_bias, A, B, C, D, init_states, nullptr, nullptr};
+  st = check_fwd_ptrs(d, a.f);
+  if (st != SSD_OK) return st;
+  a.dy = dy;
+  a.dfinal = dfinal_states;
+  a.dx = dx;
+  a.ddt = ddt;
+  a.dA = dA;
+  a.dB = dB;
+  a.dC = dC;
+  a.dD = dD;
+  a.ddt_bias = ddt_bias;
+  a.dinit = dinit_states;
+  if (!dy || !dx || !ddt || !dA || !dB || !dC) return SSD_ERR_INVALID_ARG;
+  if (!aligned(dy, d.in_bf16 ? 2 : 4)) return SSD_ERR_INVALID_ARG;
+  const float* fp[] = {dfinal_states, dx, ddt, dA, dB, dC, dD, ddt_bias, dinit_states};
+  for (const float* p : fp)
+    if (p && !aligned(p, 4)) return SSD_ERR_INVALID_ARG;
+  const BwdOffsets o = bwd_offsets(d);
+  if (!workspace || workspace_bytes < o.total || !aligned(workspace, kAlign))
+    return SSD_ERR_WORKSPACE;
+  char* base = static_cast<char*>(workspace);
+  BwdWs w;
+  w.f = carve_fwd(base, o.f);
+  w.dHs = reinterpret_cast<float*>(base + o.dHs);
+  w.dS = reinterpret_cast<float*>(base + o.dS);
+  w.dlast = reinterpret_cast<float*>(base + o.dlast);
+  w.dyx = reinterpret_cast<float*>(base + o.dyx);
+  w.qrow = reinterpret_cast<float*>(base + o.qrow);
+  w.ddir = reinterpret_cast<float*>(base + o.ddir);
+  w.ycs = reinterpret_cast<float*>(base + o.ycs);
+  w.dBh = reinterpret_cast<float*>(base + o.dBh);
+  w.dCh = reinterpret_cast<float*>(base + o.dCh);
+  w.part = reinterpret_cast<float*>(base + o.part);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  t_last_path = 0;
+  return simt_backward(d, a, w, s) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+int ssd_get_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SSD_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return SSD_ERR_CUDA;
+  const int zero = 0;
+  if (v != 0 && cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess)
+    return SSD_ERR_CUDA;
+  return v;
+}
+
+int ssd_last_path(void) { return t_last_path; }
+
+const char* ssd_strerror(int status) {
+  switch (status) {
+    case SSD_OK: return "ok";
+    case SSD_ERR_INVALID_ARG: return "invalid argument (shape, NULL pointer or alignment)";
+    case SSD_ERR_UNSUPPORTED: return "shape outside what the kernels implement";
+    case SSD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SSD_ERR_CUDA: return "CUDA runtime or launch error";
+    case SSD_ERR_TIMEOUT: return "device-side bounded wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,100 @@
+// Internal declarations shared by the translation units of libssd.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ssd.h"
+
+namespace ssd {
+
+// Problem dimensions after host validation.
+struct Dims {
+  int B, T, H, P, N, G, L, nc;
+  int in_bf16, out_bf16;
+};
+
+// Device address of the status word of the current device (defined in
+// ssd_api.cu).  Kernels whose bounded waits expire store SSD_ERR_TIMEOUT there.
+int* device_status_ptr();
+
+// Brackets one kernel launch: counts it and, when profiling is enabled,
+// records CUDA events around it on the launch stream (ssd_profile.cu).
+class LaunchScope {
+ public:
+  LaunchScope(const char* name, cudaStream_t s);
+  ~LaunchScope();
+  LaunchScope(const LaunchScope&) = delete;
+  LaunchScope& operator=(const LaunchScope&) = delete;
+
+ private:
+  const char* name_;
+  cudaStream_t s_;
+  cudaEvent_t start_ = nullptr;
+};
+
+#define SSD_LAUNCH(name, stream, ...)                  \
+  do {                                                 \
+    ::ssd::LaunchScope ssd_scope_(name, stream);       \
+    __VA_ARGS__;                                       \
+  } while (0)
+
+// ---------------------------------------------------------------- pointers
+struct FwdArgs {
+  const void* x;
+  const void* dt;
+  const float* dt_bias;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const float* init;
+  void* y;
+  float* final_state;
+};
+
+struct BwdArgs {
+  FwdArgs f;
+  const void* dy;
+  const float* dfinal;
+  float* dx;
+  float* ddt;
+  float* dA;
+  float* dB;
+  float* dC;
+  float* dD;
+  float* ddt_bias;
+  float* dinit;
+};
+
+// Workspace carving for the generic path.
+struct FwdWs {
+  float* delta;  // (B, H, nc, L)
+  float* acs;    // (B, H, nc, L)
+  float* S;      // (B, nc, H, P, N)
+  float* Hprev;  // (B, nc, H, P, N)
+  float* CB;     // (B, nc, G, L, L)
+};
+
+struct BwdWs {
+  FwdWs f;
+  float* dHs;    // (B, nc, H, P, N)
+  float* dS;     // (B, nc, H, P, N)
+  float* dlast;  // (B, H, nc)
+  float* dyx;    // (B, nc, H, L, L)
+  float* qrow;   // (B, H, nc, L)  delta_s <x_s, state part of u_s>
+  float* ddir;   // (B, H, nc, L)  <x_s, u_s>
+  float* ycs;    // (B, H, nc, L)  exp(a_l) <dy_l, H_c C_l>
+  float* dBh;    // (B, T, H, N)
+  float* dCh;    // (B, T, H, N)
+  float* part;   // (B, H, nc, 3)  per-chunk partial sums of dA, ddt_bias, dD
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Generic SIMT path (ssd_simt.cu).  Return cudaGetLastError() of the launches.
+cudaError_t simt_forward(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s);
+cudaError_t simt_backward(const Dims& d, const BwdArgs& a, const BwdWs& w, cudaStream_t s);
+
+}  // namespace ssd

@@ -123,3 +123,17 @@ WORKLOADS = {
 def make_workload(name: str) -> SSDInputs:
     shape, dtype, init_std, seed, bwd = WORKLOADS[name]
     return make_inputs(shape, seed=seed, dtype=dtype, init_std=init_std, with_dy=bwd)
+
+
+def to_torch(inp: SSDInputs, device="cuda") -> dict:
+    """Copy an input bundle to torch tensors (bf16 or fp32 storage as drawn)."""
+    import torch
+    tdt = torch.bfloat16 if inp.dtype == "bf16" else torch.float32
+
+    def cv(a, dt=tdt):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(
+            device=device, dtype=dt)
+    f32 = torch.float32
+    return dict(x=cv(inp.x), dt=cv(inp.dt), dt_bias=cv(inp.dt_bias, f32), A=cv(inp.A, f32),
+                B=cv(inp.B), C=cv(inp.C), D=cv(inp.D, f32), init=cv(inp.init, f32),
+                dy=cv(inp.dy), dfinal=cv(inp.dfinal, f32))

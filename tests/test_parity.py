@@ -1,0 +1,152 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Small cases (several tiles, ragged tails, edge shapes) are compared element by
+element, intermediates included; the full-size workloads are compared in full
+(the oracle finishes them in seconds on the host cores).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import chunked
+from parity_util import assert_close, stats, to_np
+from state_space_model_sm_gb300.inputs import SSDShape, make_inputs, make_workload, to_torch
+
+pytestmark = pytest.mark.gpu
+
+
+def run_fwd(ssd, inp, out_dtype=None):
+    import torch
+    t = to_torch(inp)
+    y, final = ssd.ssd_fwd(t["x"], t["dt"], t["dt_bias"], t["A"], t["B"], t["C"], t["D"],
+                           chunk_size=inp.shape.chunk_size, init_states=t["init"],
+                           out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert ssd.device_status() == 0
+    return y, final
+
+
+def run_bwd(ssd, inp):
+    import torch
+    t = to_torch(inp)
+    g = ssd.ssd_bwd(t["x"], t["dt"], t["dt_bias"], t["A"], t["B"], t["C"], t["D"],
+                    inp.shape.chunk_size, t["init"], t["dy"], t["dfinal"])
+    torch.cuda.synchronize()
+    assert ssd.device_status() == 0
+    return {k: to_np(v) for k, v in g.items()}
+
+
+def oracle_fwd(inp):
+    return oracle.ssd_fwd(*oracle.from_inputs(inp))
+
+
+def oracle_bwd(inp):
+    args = oracle.from_inputs(inp)
+    return oracle.ssd_bwd(*args, np.asarray(inp.dy, np.float64),
+                          None if inp.dfinal is None else np.asarray(inp.dfinal, np.float64))
+
+
+SMALL = [
+    # (name, shape, dtype, init_std)
+    ("tiny_f32", SSDShape(1, 256, 4, 16, 16, 1, 64), "f32", 0.0),
+    ("tail_f32", SSDShape(2, 250, 4, 16, 8, 2, 64), "f32", 0.5),
+    ("odd_f32", SSDShape(1, 77, 3, 5, 7, 1, 16), "f32", 0.3),
+    ("tail_bf16", SSDShape(2, 300, 4, 64, 128, 2, 128), "bf16", 0.1),
+    ("multi_bf16", SSDShape(2, 1024, 8, 64, 128, 1, 256), "bf16", 0.0),
+    ("g_eq_h_bf16", SSDShape(1, 512, 4, 64, 64, 4, 64), "bf16", 0.2),
+    ("single_token", SSDShape(1, 1, 2, 16, 16, 1, 64), "f32", 0.5),
+    ("chunk1_f32", SSDShape(1, 20, 2, 4, 4, 1, 1), "f32", 0.5),
+]
+
+
+@pytest.mark.parametrize("name,shape,dtype,init_std", SMALL, ids=[s[0] for s in SMALL])
+def test_forward_small(cuda_lib, name, shape, dtype, init_std):
+    inp = make_inputs(shape, seed=11, dtype=dtype, init_std=init_std)
+    y, final = run_fwd(cuda_lib, inp)
+    y_ref, f_ref = oracle_fwd(inp)
+    assert_close("y", to_np(y), y_ref, dtype)
+    assert_close("final", to_np(final), f_ref, dtype)
+
+
+@pytest.mark.parametrize("name,shape,dtype,init_std", SMALL, ids=[s[0] for s in SMALL])
+def test_backward_small(cuda_lib, name, shape, dtype, init_std):
+    inp = make_inputs(shape, seed=12, dtype=dtype, init_std=init_std, with_dy=True,
+                      dfinal_std=0.5)
+    g = run_bwd(cuda_lib, inp)
+    ref = oracle_bwd(inp)
+    keys = ["dx", "ddt", "dA", "dB", "dC", "dD", "ddt_bias"]
+    if inp.init is not None:
+        keys.append("dinit")
+    for k in keys:
+        got = g["dinit_states"] if k == "dinit" else g[k]
+        assert_close(k, got, ref[k], dtype)
+
+
+def test_forward_intermediates_match_chunked_reference(cuda_lib):
+    """Per-kernel parity: delta, dA_cumsum (chunk_cumsum), states (chunk_state)
+    and hprev (state_passing), read from the documented workspace layout."""
+    import torch
+    inp = make_inputs(SSDShape(2, 300, 4, 64, 128, 2, 128), seed=5, dtype="bf16", init_std=0.1)
+    t = to_torch(inp)
+    Bt, T, H, P, N, G, L = 2, 300, 4, 64, 128, 2, 128
+    nc = 3
+    shape = cuda_lib.make_shape(Bt, T, H, P, N, G, L, cuda_lib.SSD_BF16, cuda_lib.SSD_F32)
+    lay = cuda_lib.fwd_workspace_layout(shape)
+    ws = torch.zeros(lay["total"], dtype=torch.uint8, device="cuda")
+    cuda_lib.ssd_fwd(t["x"], t["dt"], t["dt_bias"], t["A"], t["B"], t["C"], t["D"],
+                     chunk_size=L, init_states=t["init"], workspace=ws)
+    torch.cuda.synchronize()
+
+    def view(off, shp):
+        n = int(np.prod(shp))
+        return to_np(ws[off:off + 4 * n].view(torch.float32).reshape(shp))
+    ref = chunked.ssd_chunked_fwd(*oracle.from_inputs(inp), L)
+    s = stats(view(lay["delta"], (Bt, H, nc, L)), ref["delta"])
+    assert s["rel_l2"] < 1e-6, s
+    s = stats(view(lay["dA_cumsum"], (Bt, H, nc, L)), ref["a"])
+    assert s["rel_l2"] < 1e-5, s
+    s = stats(view(lay["states"], (Bt, nc, H, P, N)), ref["S"])
+    assert s["rel_l2"] < 1e-3, s
+    s = stats(view(lay["hprev"], (Bt, nc, H, P, N)), ref["Hprev"])
+    assert s["rel_l2"] < 1e-3, s
+
+
+def test_backward_is_deterministic(cuda_lib):
+    inp = make_inputs(SSDShape(2, 512, 8, 64, 128, 2, 128), seed=3, dtype="bf16", with_dy=True)
+    g1 = run_bwd(cuda_lib, inp)
+    g2 = run_bwd(cuda_lib, inp)
+    for k in g1:
+        assert np.array_equal(g1[k], g2[k]), k
+
+
+def test_bf16_output_mode(cuda_lib):
+    import torch
+    inp = make_inputs(SSDShape(2, 512, 8, 64, 128, 1, 256), seed=4, dtype="bf16")
+    y, _ = run_fwd(cuda_lib, inp, out_dtype=torch.bfloat16)
+    y_ref, _ = oracle_fwd(inp)
+    s = stats(to_np(y), y_ref)
+    assert s["page_ok"] and s["rel_l2"] < 1e-2, s
+
+
+# ------------------------------------------------------------ full workloads
+
+@pytest.mark.parametrize("name", ["tiny_f32", "layer_bf16", "hybrid_bf16", "long_bf16"])
+def test_forward_workload(cuda_lib, name):
+    inp = make_workload(name)
+    y, final = run_fwd(cuda_lib, inp)
+    y_ref, f_ref = oracle_fwd(inp)
+    s = assert_close("y", to_np(y), y_ref, inp.dtype)
+    assert_close("final", to_np(final), f_ref, inp.dtype)
+    print(name, s)
+
+
+def test_forward_backward_workload(cuda_lib):
+    inp = make_workload("layer_fwdbwd_bf16")
+    y, final = run_fwd(cuda_lib, inp)
+    y_ref, f_ref = oracle_fwd(inp)
+    assert_close("y", to_np(y), y_ref, "bf16")
+    g = run_bwd(cuda_lib, inp)
+    ref = oracle_bwd(inp)
+    for k in ["dx", "ddt", "dA", "dB", "dC", "dD", "ddt_bias"]:
+        s = assert_close(k, g[k], ref[k], "bf16")
+        print(k, s)
