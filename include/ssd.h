@@ -122,6 +122,30 @@ int ssd_profile_read(int max_kernels, char* names, double* ms, int64_t* launches
 /* Number of kernels this library has launched in this process. */
 int64_t ssd_launch_count(void);
 
+/* Forward pass for callers that cannot allocate device memory (no workspace
+ * argument).  The pages have no counterpart: this is a convenience of this
+ * library.  Callers such as a host runtime whose memory pool already owns the
+ * device, a plugin that is handed only its tensors, or a latency-critical loop
+ * that cannot afford cudaMalloc (which may synchronise the device) use it
+ * instead of ssd_fwd.
+ *   - Scratch: a fixed array of ssd_noalloc_scratch_bytes() bytes (64 MiB) of
+ *     device memory inside the library, held on every GPU that loads the
+ *     library until the process exits.  Shapes whose ssd_fwd_workspace_size()
+ *     exceeds it return SSD_ERR_WORKSPACE; nothing is launched.
+ *   - Inputs, outputs, results and errors are those of ssd_fwd.  It calls no
+ *     cudaMalloc, cudaFree or other allocating routine.
+ *   - The first call on each device looks up the scratch's device address
+ *     (with that device current) and caches it; make that first call before
+ *     any stream capture.
+ *   - Every call on a device shares the one scratch array and leaves the last
+ *     call's intermediates in it: calls that overlap on the GPU (different
+ *     streams, or host threads without ordering between them) race and give
+ *     wrong results.  Order them, e.g. on one stream. */
+int ssd_fwd_noalloc(const ssd_shape* shape, const void* x, const void* dt, const float* dt_bias,
+                    const float* A, const void* B, const void* C, const float* D,
+                    const float* init_states, void* y, float* final_states, void* stream);
+size_t ssd_noalloc_scratch_bytes(void);
+
 /* Static description of a status code. */
 const char* ssd_strerror(int status);
 
