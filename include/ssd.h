@@ -146,6 +146,16 @@ int ssd_fwd_noalloc(const ssd_shape* shape, const void* x, const void* dt, const
                     const float* init_states, void* y, float* final_states, void* stream);
 size_t ssd_noalloc_scratch_bytes(void);
 
+/* Diagnostic: one tcgen05 tile product on the current device,
+ * D[128][nn] = A[128][k] * B[nn][k]^T (A, B bf16 row-major, D f32 row-major,
+ * all device memory), with A and B staged in shared memory K-major (0) or
+ * MN-major (1) in the 128-byte-swizzle layout of the tensor-core kernels;
+ * swap_mn_offsets exchanges the two byte offsets of MN-major descriptors.
+ * 16 <= nn <= 256, nn % 16 == 0 (nn % 64 == 0 when b_mn); 16 <= k <= 128,
+ * k % 16 == 0; A and B 16-byte aligned.  Asynchronous on `stream`. */
+int ssd_selftest_mma(int a_mn, int b_mn, int swap_mn_offsets, int nn, int k, const void* A,
+                     const void* B, float* D, void* stream);
+
 /* Static description of a status code. */
 const char* ssd_strerror(int status);
 
