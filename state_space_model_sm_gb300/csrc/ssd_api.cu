@@ -1,5 +1,6 @@
 // C ABI of libssd (declared in include/ssd.h): argument checks, workspace
 // carving and dispatch to the kernel families.
+#include <cstdlib>
 #include <cstring>
 
 #include "ssd_internal.h"
@@ -107,6 +108,12 @@ BwdOffsets bwd_offsets(const Dims& d) {
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
+// SSD_FORCE_SIMT=1 in the environment keeps every call on the generic kernels.
+bool force_simt() {
+  const char* v = std::getenv("SSD_FORCE_SIMT");
+  return v && v[0] == '1';
+}
+
 int check_fwd_ptrs(const Dims& d, const FwdArgs& a) {
   if (!a.x || !a.dt || !a.A || !a.B || !a.C) return SSD_ERR_INVALID_ARG;
   const size_t in = d.in_bf16 ? 2 : 4;
@@ -177,8 +184,11 @@ int ssd_fwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
     return SSD_ERR_WORKSPACE;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const FwdWs w = carve_fwd(static_cast<char*>(workspace), o);
-  t_last_path = 0;
-  return simt_forward(d, a, w, s) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+  const bool tc = !force_simt() && tc_forward_supported(d) && aligned(x, 16) && aligned(B, 16) &&
+                  aligned(C, 16) && aligned(y, 16);
+  t_last_path = tc ? 1 : 0;
+  const cudaError_t e = tc ? tc_forward(d, a, w, s) : simt_forward(d, a, w, s);
+  return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
 int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* dt_bias,

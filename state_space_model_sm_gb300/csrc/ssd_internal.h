@@ -96,5 +96,14 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Generic SIMT path (ssd_simt.cu).  Return cudaGetLastError() of the launches.
 cudaError_t simt_forward(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s);
 cudaError_t simt_backward(const Dims& d, const BwdArgs& a, const BwdWs& w, cudaStream_t s);
+// The bandwidth-bound steps shared by both paths: chunk_cumsum (delta, a)
+// and state_passing (Hprev, final) on the generic kernels.
+void simt_cumsum(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s);
+void simt_state_passing(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s);
+
+// tcgen05 path (ssd_tc.cu): bf16 inputs, headdim 64, d_state 64 / 128,
+// chunk 128 / 256, an even number of heads per group.
+bool tc_forward_supported(const Dims& d);
+cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s);
 
 }  // namespace ssd

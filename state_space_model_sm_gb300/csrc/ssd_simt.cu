@@ -696,18 +696,26 @@ __global__ void k_param_grads(const float* __restrict__ part, float* __restrict_
 }
 
 template <typename Tin>
-void launch_forward_front(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
-  const Tin* dt = static_cast<const Tin*>(a.dt);
+void launch_cumsum(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
   SSD_LAUNCH("k_chunk_cumsum", s, k_chunk_cumsum<Tin><<<dim3(d.nc, d.B, (d.H + 31) / 32), kThreads, 0, s>>>(
-      dt, a.dt_bias, a.A, w.delta, w.acs, d.T, d.H, d.L, d.nc));
+      static_cast<const Tin*>(a.dt), a.dt_bias, a.A, w.delta, w.acs, d.T, d.H, d.L, d.nc));
+}
+
+void launch_state_passing(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
+  const int PN = d.P * d.N;
+  SSD_LAUNCH("k_state_passing", s, k_state_passing<<<dim3((PN + kThreads - 1) / kThreads, d.H, d.B), kThreads, 0, s>>>(
+      w.S, w.acs, a.init, w.Hprev, a.final_state, d.H, PN, d.L, d.nc));
+}
+
+template <typename Tin>
+void launch_forward_front(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
+  launch_cumsum<Tin>(d, a, w, s);
   SSD_LAUNCH("k_bmm_cb", s, k_bmm_cb<Tin><<<dim3(d.nc, d.G, d.B), kThreads, 0, s>>>(
       static_cast<const Tin*>(a.B), static_cast<const Tin*>(a.C), w.CB, d.T, d.G, d.N, d.L, d.nc));
   SSD_LAUNCH("k_chunk_state", s, k_chunk_state<Tin, 0><<<dim3(d.nc, d.H, d.B), kThreads, 0, s>>>(
       static_cast<const Tin*>(a.x), static_cast<const Tin*>(a.B), w.delta, w.acs, w.S, d.T, d.H,
       d.G, d.P, d.N, d.L, d.nc));
-  const int PN = d.P * d.N;
-  SSD_LAUNCH("k_state_passing", s, k_state_passing<<<dim3((PN + kThreads - 1) / kThreads, d.H, d.B), kThreads, 0, s>>>(
-      w.S, w.acs, a.init, w.Hprev, a.final_state, d.H, PN, d.L, d.nc));
+  launch_state_passing(d, a, w, s);
 }
 
 template <typename Tin, typename Tout>
@@ -764,6 +772,15 @@ cudaError_t simt_forward(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaSt
     else launch_forward<float, float>(d, a, w, s);
   }
   return cudaGetLastError();
+}
+
+void simt_cumsum(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
+  if (d.in_bf16) launch_cumsum<__nv_bfloat16>(d, a, w, s);
+  else launch_cumsum<float>(d, a, w, s);
+}
+
+void simt_state_passing(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
+  launch_state_passing(d, a, w, s);
 }
 
 cudaError_t simt_backward(const Dims& d, const BwdArgs& a, const BwdWs& w, cudaStream_t s) {

@@ -150,3 +150,42 @@ def test_forward_backward_workload(cuda_lib):
     for k in ["dx", "ddt", "dA", "dB", "dC", "dD", "ddt_bias"]:
         s = assert_close(k, g[k], ref[k], "bf16")
         print(k, s)
+
+
+# ------------------------------------------------- tensor-core vs generic path
+
+TC_CASES = [
+    ("tc_n128_l256", SSDShape(2, 1024, 8, 64, 128, 1, 256), 0.0),
+    ("tc_n128_l128_tail", SSDShape(2, 700, 8, 64, 128, 2, 128), 0.2),
+    ("tc_n64_l128_tail", SSDShape(1, 333, 6, 64, 64, 3, 128), 0.1),
+    ("tc_n64_l256", SSDShape(3, 512, 4, 64, 64, 1, 256), 0.0),
+    ("tc_partial_second_tile", SSDShape(1, 300, 2, 64, 128, 1, 256), 0.0),
+]
+
+
+@pytest.mark.parametrize("name,shape,init_std", TC_CASES, ids=[c[0] for c in TC_CASES])
+def test_tensor_core_forward_against_oracle_and_generic(cuda_lib, monkeypatch, name, shape,
+                                                       init_std):
+    inp = make_inputs(shape, seed=31, dtype="bf16", init_std=init_std)
+    y, final = run_fwd(cuda_lib, inp)
+    assert cuda_lib.last_path() == 1, "bf16 headdim-64 problem did not take the tcgen05 path"
+    y_ref, f_ref = oracle_fwd(inp)
+    s = assert_close("y", to_np(y), y_ref, "bf16")
+    assert s["rel_l2"] < 1e-4, s      # split-bf16 operands keep ~fp32 accuracy
+    assert_close("final", to_np(final), f_ref, "bf16")
+    monkeypatch.setenv("SSD_FORCE_SIMT", "1")
+    y2, f2 = run_fwd(cuda_lib, inp)
+    assert cuda_lib.last_path() == 0
+    s2 = stats(to_np(y), to_np(y2))
+    assert s2["rel_l2"] < 1e-4, s2
+
+
+def test_workloads_take_tensor_core_path(cuda_lib):
+    for name in ("layer_bf16", "hybrid_bf16"):
+        inp = make_workload(name)
+        inp.x, inp.B = inp.x[:, :512], inp.B[:, :512]
+        inp.C, inp.dt = inp.C[:, :512], inp.dt[:, :512]
+        inp.shape = SSDShape(inp.shape.batch, 512, inp.shape.nheads, inp.shape.headdim,
+                             inp.shape.dstate, inp.shape.ngroups, inp.shape.chunk_size)
+        run_fwd(cuda_lib, inp)
+        assert cuda_lib.last_path() == 1, name
