@@ -94,13 +94,44 @@ BwdOffsets bwd_offsets(const Dims& d) {
   const size_t ph = (size_t)d.B * d.T * d.H * d.N * sizeof(float);
   o.dHs = c.take(st);
   o.dS = c.take(st);
-  o.dlast = c.take((size_t)d.B * d.H * d.nc * sizeof(float));
+  o.dlast = c.take((size_t)d.B * d.H * d.nc * 16 * sizeof(float));  // <= 16 partials each
   o.dyx = c.take((size_t)d.B * d.nc * d.H * d.L * d.L * sizeof(float));
   o.qrow = c.take(vec);
   o.ddir = c.take(vec);
   o.ycs = c.take(vec);
   o.dBh = c.take(ph);
   o.dCh = c.take(ph);
+  o.part = c.take((size_t)d.B * d.H * d.nc * 3 * sizeof(float));
+  o.total = c.off;
+  return o;
+}
+
+struct TcBwdOffsets {
+  size_t delta, acs, S, Hprev, dHs, dS, dlast, rowsum, colsum, ycs, qrow, ddir, ddiag, dBp, dCp,
+      part, total;
+};
+
+TcBwdOffsets tc_bwd_offsets(const Dims& d) {
+  Carver c;
+  const size_t vec = (size_t)d.B * d.H * d.nc * d.L * sizeof(float);
+  const size_t st = (size_t)d.B * d.nc * d.H * d.P * d.N * sizeof(float);
+  const size_t bp = (size_t)d.B * d.T * d.G * tc_bwd_nblk(d) * d.N * sizeof(float);
+  TcBwdOffsets o;
+  o.delta = c.take(vec);
+  o.acs = c.take(vec);
+  o.S = c.take(st);
+  o.Hprev = c.take(st);
+  o.dHs = c.take(st);
+  o.dS = c.take(st);
+  o.dlast = c.take((size_t)d.B * d.H * d.nc * 16 * sizeof(float));
+  o.rowsum = c.take(vec);
+  o.colsum = c.take(vec);
+  o.ycs = c.take(vec);
+  o.qrow = c.take(vec);
+  o.ddir = c.take(vec);
+  o.ddiag = c.take(vec);
+  o.dBp = c.take(bp);
+  o.dCp = c.take(bp);
   o.part = c.take((size_t)d.B * d.H * d.nc * 3 * sizeof(float));
   o.total = c.off;
   return o;
@@ -151,7 +182,12 @@ size_t ssd_fwd_workspace_size(const ssd_shape* shape) {
 size_t ssd_bwd_workspace_size(const ssd_shape* shape) {
   Dims d;
   if (make_dims(shape, &d) != SSD_OK) return 0;
-  return bwd_offsets(d).total;
+  size_t total = bwd_offsets(d).total;
+  if (tc_forward_supported(d)) {
+    const size_t t = tc_bwd_offsets(d).total;
+    if (t > total) total = t;
+  }
+  return total;
 }
 
 int ssd_fwd_workspace_layout(const ssd_shape* shape, ssd_fwd_layout* out) {
@@ -218,10 +254,38 @@ int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
   const float* fp[] = {dfinal_states, dx, ddt, dA, dB, dC, dD, ddt_bias, dinit_states};
   for (const float* p : fp)
     if (p && !aligned(p, 4)) return SSD_ERR_INVALID_ARG;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(workspace);
+  const bool tc = !force_simt() && tc_forward_supported(d) && aligned(x, 16) && aligned(B, 16) &&
+                  aligned(C, 16) && aligned(dy, 16) && aligned(dx, 16) && aligned(dB, 16) &&
+                  aligned(dC, 16);
+  if (tc) {
+    const TcBwdOffsets o = tc_bwd_offsets(d);
+    if (!workspace || workspace_bytes < o.total || !aligned(workspace, kAlign))
+      return SSD_ERR_WORKSPACE;
+    TcBwdWs w;
+    w.delta = reinterpret_cast<float*>(base + o.delta);
+    w.acs = reinterpret_cast<float*>(base + o.acs);
+    w.S = reinterpret_cast<float*>(base + o.S);
+    w.Hprev = reinterpret_cast<float*>(base + o.Hprev);
+    w.dHs = reinterpret_cast<float*>(base + o.dHs);
+    w.dS = reinterpret_cast<float*>(base + o.dS);
+    w.dlast = reinterpret_cast<float*>(base + o.dlast);
+    w.rowsum = reinterpret_cast<float*>(base + o.rowsum);
+    w.colsum = reinterpret_cast<float*>(base + o.colsum);
+    w.ycs = reinterpret_cast<float*>(base + o.ycs);
+    w.qrow = reinterpret_cast<float*>(base + o.qrow);
+    w.ddir = reinterpret_cast<float*>(base + o.ddir);
+    w.ddiag = reinterpret_cast<float*>(base + o.ddiag);
+    w.dBp = reinterpret_cast<float*>(base + o.dBp);
+    w.dCp = reinterpret_cast<float*>(base + o.dCp);
+    w.part = reinterpret_cast<float*>(base + o.part);
+    t_last_path = 1;
+    return tc_backward(d, a, w, s) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+  }
   const BwdOffsets o = bwd_offsets(d);
   if (!workspace || workspace_bytes < o.total || !aligned(workspace, kAlign))
     return SSD_ERR_WORKSPACE;
-  char* base = static_cast<char*>(workspace);
   BwdWs w;
   w.f = carve_fwd(base, o.f);
   w.dHs = reinterpret_cast<float*>(base + o.dHs);
@@ -234,7 +298,6 @@ int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
   w.dBh = reinterpret_cast<float*>(base + o.dBh);
   w.dCh = reinterpret_cast<float*>(base + o.dCh);
   w.part = reinterpret_cast<float*>(base + o.part);
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
   t_last_path = 0;
   return simt_backward(d, a, w, s) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }

@@ -81,7 +81,7 @@ struct BwdWs {
   FwdWs f;
   float* dHs;    // (B, nc, H, P, N)
   float* dS;     // (B, nc, H, P, N)
-  float* dlast;  // (B, H, nc)
+  float* dlast;  // (B, H, nc, nsplit) partial sums of dlast
   float* dyx;    // (B, nc, H, L, L)
   float* qrow;   // (B, H, nc, L)  delta_s <x_s, state part of u_s>
   float* ddir;   // (B, H, nc, L)  <x_s, u_s>
@@ -101,9 +101,39 @@ cudaError_t simt_backward(const Dims& d, const BwdArgs& a, const BwdWs& w, cudaS
 void simt_cumsum(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s);
 void simt_state_passing(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s);
 
+int simt_state_passing_bwd(const Dims& d, const float* dHs, const float* acs, const float* Hprev,
+                           const float* dfinal, float* dS, float* dlast, float* dinit,
+                           cudaStream_t s);  // returns the dlast partials per chunk
+void simt_param_grads(const Dims& d, const float* part, float* dA, float* ddt_bias, float* dD,
+                      cudaStream_t s);
+
+// Workspace of the tensor-core backward.
+struct TcBwdWs {
+  float* delta;   // (B, H, nc, L)
+  float* acs;     // (B, H, nc, L)
+  float* S;       // (B, nc, H, P, N)
+  float* Hprev;   // (B, nc, H, P, N)
+  float* dHs;     // (B, nc, H, P, N)
+  float* dS;      // (B, nc, H, P, N)
+  float* dlast;   // (B, H, nc, <= 16) partials
+  float* rowsum;  // (B, H, nc, L) strict row sums of M (dC kernel)
+  float* colsum;  // (B, H, nc, L) strict column sums of M (dB kernel)
+  float* ycs;     // (B, H, nc, L)
+  float* qrow;    // (B, H, nc, L)
+  float* ddir;    // (B, H, nc, L)
+  float* ddiag;   // (B, H, nc, L)  <dy_t, x_t>
+  float* dBp;     // (B, T, G, nblk, N) head-block partials of dB
+  float* dCp;     // (B, T, G, nblk, N)
+  float* part;    // (B, H, nc, 3)
+};
+
 // tcgen05 path (ssd_tc.cu): bf16 inputs, headdim 64, d_state 64 / 128,
 // chunk 128 / 256, an even number of heads per group.
 bool tc_forward_supported(const Dims& d);
 cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s);
+// Head blocks per group of the dB / dC kernels (a function of the shape only,
+// so the workspace size and the launch always agree).
+int tc_bwd_nblk(const Dims& d);
+cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w, cudaStream_t s);
 
 }  // namespace ssd

@@ -259,6 +259,98 @@ __global__ void __launch_bounds__(kThreads)
   if (final_state) final_state[((int64_t)b * H + h) * PN + e] = cur;
 }
 
+// Vectorised state_passing: grid (ceil(P*N/1024), H, B); each thread carries 4
+// consecutive state elements (float4) through the chunk recurrence.  The
+// loads of S_c do not depend on the recurrence, so they are issued kPrefetch
+// chunks ahead to keep enough bytes in flight per SM.
+constexpr int kPrefetch = 8;
+
+__global__ void __launch_bounds__(kThreads)
+    k_state_passing_v4(const float4* __restrict__ S, const float* __restrict__ acs,
+                       const float4* __restrict__ init, float4* __restrict__ Hprev,
+                       float4* __restrict__ final_state, int H, int PN4, int L, int nc) {
+  const int e = blockIdx.x * kThreads + threadIdx.x, h = blockIdx.y, b = blockIdx.z;
+  if (e >= PN4) return;
+  const int64_t step = (int64_t)H * PN4;
+  const int64_t base = ((int64_t)b * nc * H + h) * PN4 + e;
+  const float* ab = acs + ((int64_t)b * H + h) * (int64_t)nc * L + (L - 1);
+  float4 cur = init ? init[((int64_t)b * H + h) * PN4 + e] : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = 0; c0 < nc; c0 += kPrefetch) {
+    float4 sv[kPrefetch];
+    float dec[kPrefetch];
+#pragma unroll
+    for (int k = 0; k < kPrefetch; ++k)
+      if (c0 + k < nc) {
+        sv[k] = S[base + (c0 + k) * step];
+        dec[k] = __expf(ab[(int64_t)(c0 + k) * L]);
+      }
+#pragma unroll
+    for (int k = 0; k < kPrefetch; ++k)
+      if (c0 + k < nc) {
+        Hprev[base + (c0 + k) * step] = cur;
+        cur.x = fmaf(dec[k], cur.x, sv[k].x);
+        cur.y = fmaf(dec[k], cur.y, sv[k].y);
+        cur.z = fmaf(dec[k], cur.z, sv[k].z);
+        cur.w = fmaf(dec[k], cur.w, sv[k].w);
+      }
+  }
+  if (final_state) final_state[((int64_t)b * H + h) * PN4 + e] = cur;
+}
+
+// Vectorised state_passing backward: grid (nsplit = ceil(P*N/1024), H, B).
+// Each block owns 1024 state elements of one (b, h) and walks the chunks in
+// reverse; the partial dot products <H_c, G_{c+1}> of its slice go to
+// dlast_part[((b*H + h)*nc + c)*nsplit + split] (summed in a fixed order later).
+__global__ void __launch_bounds__(kThreads)
+    k_state_passing_bwd_v4(const float4* __restrict__ dHs, const float* __restrict__ acs,
+                           const float4* __restrict__ Hprev, const float4* __restrict__ dfinal,
+                           float4* __restrict__ dS, float* __restrict__ dlast_part,
+                           float4* __restrict__ dinit, int H, int PN4, int L, int nc) {
+  __shared__ float red[kThreads / 32];
+  const int split = blockIdx.x, nsplit = gridDim.x, h = blockIdx.y, b = blockIdx.z;
+  const int e = split * kThreads + threadIdx.x;
+  const bool live = e < PN4;
+  const int64_t step = (int64_t)H * PN4;
+  const int64_t base = ((int64_t)b * nc * H + h) * PN4 + e;
+  const float* ab = acs + ((int64_t)b * H + h) * (int64_t)nc * L + (L - 1);
+  float4 G = (live && dfinal) ? dfinal[((int64_t)b * H + h) * PN4 + e]
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int kPf = 4;
+  for (int c1 = nc - 1; c1 >= 0; c1 -= kPf) {
+    float4 hv[kPf], gv[kPf];
+    float dec[kPf];
+#pragma unroll
+    for (int k = 0; k < kPf; ++k) {
+      const int c = c1 - k;
+      if (c >= 0) {
+        dec[k] = __expf(ab[(int64_t)c * L]);
+        if (live) {
+          hv[k] = Hprev[base + c * step];
+          gv[k] = dHs[base + c * step];
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPf; ++k) {
+      const int c = c1 - k;
+      if (c < 0) break;
+      float part = 0.f;
+      if (live) {
+        dS[base + c * step] = G;
+        part = hv[k].x * G.x + hv[k].y * G.y + hv[k].z * G.z + hv[k].w * G.w;
+        G.x = fmaf(dec[k], G.x, gv[k].x);
+        G.y = fmaf(dec[k], G.y, gv[k].y);
+        G.z = fmaf(dec[k], G.z, gv[k].z);
+        G.w = fmaf(dec[k], G.w, gv[k].w);
+      }
+      const float tot = block_sum(part, red);
+      if (threadIdx.x == 0)
+        dlast_part[(((int64_t)b * H + h) * nc + c) * nsplit + split] = dec[k] * tot;
+    }
+  }
+  if (live && dinit) dinit[((int64_t)b * H + h) * PN4 + e] = G;
+}
+
 // ------------------------------------------------------------- chunk_scan
 // grid (nc, H, B).  y_l = sum_{s<=l} CB[l,s] exp(a_l - a_s) delta_s x_s
 //                        + exp(a_l) H_c C_l + D x_l
@@ -599,8 +691,8 @@ __global__ void __launch_bounds__(kThreads)
               const float* __restrict__ dyx, const float* __restrict__ delta,
               const float* __restrict__ acs, const float* __restrict__ ddir,
               const float* __restrict__ qrow, const float* __restrict__ ycs,
-              const float* __restrict__ dlast, float* __restrict__ ddt, float* __restrict__ part,
-              int T, int H, int G, int L, int nc) {
+              const float* __restrict__ dlast, int nsplit, float* __restrict__ ddt,
+              float* __restrict__ part, int T, int H, int G, int L, int nc) {
   __shared__ float sa[256], sd[256], dr[256], sdd[256], red[kThreads / 32];
   const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, g = h / (H / G);
   const int Lv = min(L, T - c * L);
@@ -625,7 +717,8 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   if (threadIdx.x == 0) {
     // sequential prefix / suffix sums (L <= 256) in a fixed order
-    const float dl = dlast[((int64_t)b * H + h) * nc + c];
+    float dl = 0.f;
+    for (int k = 0; k < nsplit; ++k) dl += dlast[(((int64_t)b * H + h) * nc + c) * nsplit + k];
     float pre = 0.f, qpre = 0.f;
     for (int r = 0; r < Lv; ++r) {
       sdd[r] = pre + qpre + dl;
@@ -701,8 +794,18 @@ void launch_cumsum(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t
       static_cast<const Tin*>(a.dt), a.dt_bias, a.A, w.delta, w.acs, d.T, d.H, d.L, d.nc));
 }
 
+bool vec4_ok(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
 void launch_state_passing(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
   const int PN = d.P * d.N;
+  if (PN % 4 == 0 && vec4_ok(a.init) && vec4_ok(a.final_state)) {
+    const int PN4 = PN / 4;
+    SSD_LAUNCH("k_state_passing", s, k_state_passing_v4<<<dim3((PN4 + kThreads - 1) / kThreads, d.H, d.B), kThreads, 0, s>>>(
+        reinterpret_cast<const float4*>(w.S), w.acs, reinterpret_cast<const float4*>(a.init),
+        reinterpret_cast<float4*>(w.Hprev), reinterpret_cast<float4*>(a.final_state), d.H, PN4,
+        d.L, d.nc));
+    return;
+  }
   SSD_LAUNCH("k_state_passing", s, k_state_passing<<<dim3((PN + kThreads - 1) / kThreads, d.H, d.B), kThreads, 0, s>>>(
       w.S, w.acs, a.init, w.Hprev, a.final_state, d.H, PN, d.L, d.nc));
 }
@@ -726,6 +829,22 @@ void launch_forward(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_
       a.D, static_cast<Tout*>(a.y), d.T, d.H, d.G, d.P, d.N, d.L, d.nc));
 }
 
+// Returns the number of dlast partials per (b, h, c) it wrote.
+int launch_state_passing_bwd(const Dims& d, const BwdArgs& a, const BwdWs& w, cudaStream_t s) {
+  const int PN = d.P * d.N;
+  if (PN % 4 == 0 && vec4_ok(a.dfinal) && vec4_ok(a.dinit)) {
+    const int PN4 = PN / 4, nsplit = (PN4 + kThreads - 1) / kThreads;
+    SSD_LAUNCH("k_state_passing_bwd", s, k_state_passing_bwd_v4<<<dim3(nsplit, d.H, d.B), kThreads, 0, s>>>(
+        reinterpret_cast<const float4*>(w.dHs), w.f.acs, reinterpret_cast<const float4*>(w.f.Hprev),
+        reinterpret_cast<const float4*>(a.dfinal), reinterpret_cast<float4*>(w.dS), w.dlast,
+        reinterpret_cast<float4*>(a.dinit), d.H, PN4, d.L, d.nc));
+    return nsplit;
+  }
+  SSD_LAUNCH("k_state_passing_bwd", s, k_state_passing_bwd<<<d.B * d.H, kThreads, 0, s>>>(
+      w.dHs, w.f.acs, w.f.Hprev, a.dfinal, w.dS, w.dlast, a.dinit, d.H, PN, d.L, d.nc));
+  return 1;
+}
+
 template <typename Tin>
 void launch_backward(const Dims& d, const BwdArgs& a, const BwdWs& w, cudaStream_t s) {
   FwdArgs f = a.f;
@@ -739,8 +858,7 @@ void launch_backward(const Dims& d, const BwdArgs& a, const BwdWs& w, cudaStream
   SSD_LAUNCH("k_chunk_state", s, k_chunk_state<Tin, 1><<<grid, kThreads, 0, s>>>(dy, Cm, w.f.delta, w.f.acs, w.dHs, d.T, d.H,
                                                   d.G, d.P, d.N, d.L, d.nc));
   const int PN = d.P * d.N;
-  SSD_LAUNCH("k_state_passing_bwd", s, k_state_passing_bwd<<<d.B * d.H, kThreads, 0, s>>>(w.dHs, w.f.acs, w.f.Hprev, a.dfinal, w.dS,
-                                                     w.dlast, a.dinit, d.H, PN, d.L, d.nc));
+  const int nsplit = launch_state_passing_bwd(d, a, w, s);
   SSD_LAUNCH("k_dyx", s, k_dyx<Tin><<<grid, kThreads, 0, s>>>(x, dy, w.dyx, d.T, d.H, d.P, d.L, d.nc));
   SSD_LAUNCH("k_bwd_dx", s, k_bwd_dx<Tin><<<grid, kThreads, 0, s>>>(x, Bm, dy, w.f.CB, w.f.delta, w.f.acs, w.dS, a.f.D,
                                           a.dx, w.ddir, w.qrow, d.T, d.H, d.G, d.P, d.N, d.L,
@@ -751,7 +869,7 @@ void launch_backward(const Dims& d, const BwdArgs& a, const BwdWs& w, cudaStream
                                           d.H, d.G, d.P, d.N, d.L, d.nc));
   SSD_LAUNCH("k_bwd_ddA", s, k_bwd_ddA<Tin><<<grid, kThreads, 0, s>>>(static_cast<const Tin*>(a.f.dt), a.f.dt_bias, a.f.A,
                                            w.f.CB, w.dyx, w.f.delta, w.f.acs, w.ddir, w.qrow,
-                                           w.ycs, w.dlast, a.ddt, w.part, d.T, d.H, d.G, d.L,
+                                           w.ycs, w.dlast, nsplit, a.ddt, w.part, d.T, d.H, d.G, d.L,
                                            d.nc));
   const int64_t BT = (int64_t)d.B * d.T;
   const int64_t nred = BT * d.G * d.N;
@@ -781,6 +899,26 @@ void simt_cumsum(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s
 
 void simt_state_passing(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
   launch_state_passing(d, a, w, s);
+}
+
+int simt_state_passing_bwd(const Dims& d, const float* dHs, const float* acs, const float* Hprev,
+                           const float* dfinal, float* dS, float* dlast, float* dinit,
+                           cudaStream_t s) {
+  BwdArgs a{};
+  a.dfinal = dfinal;
+  a.dinit = dinit;
+  BwdWs w{};
+  w.dHs = const_cast<float*>(dHs);
+  w.f.acs = const_cast<float*>(acs);
+  w.f.Hprev = const_cast<float*>(Hprev);
+  w.dS = dS;
+  w.dlast = dlast;
+  return launch_state_passing_bwd(d, a, w, s);
+}
+
+void simt_param_grads(const Dims& d, const float* part, float* dA, float* ddt_bias, float* dD,
+                      cudaStream_t s) {
+  SSD_LAUNCH("k_param_grads", s, k_param_grads<<<d.H, 32, 0, s>>>(part, dA, ddt_bias, dD, d.B, d.H, d.nc));
 }
 
 cudaError_t simt_backward(const Dims& d, const BwdArgs& a, const BwdWs& w, cudaStream_t s) {

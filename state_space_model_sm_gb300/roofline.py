@@ -49,10 +49,31 @@ def _terms(d: Dims):
     return dict(x=x, xf=xf, bc=bc, bcf=bcf, dtb=dtb, vec=vec, st=st, fin=fin, cb=cb, y=y)
 
 
+def tc_bwd_nblk(d: Dims) -> int:
+    """Head blocks per group of the tensor-core dB / dC kernels (same rule as
+    the library: fewest blocks giving >= 2 x 152 CTAs)."""
+    hpg = d.H // d.G
+    units = d.B * d.nc * (d.L // 128) * d.G
+    for nb in range(1, hpg + 1):
+        if hpg % nb == 0 and units * nb >= 2 * 152:
+            return nb
+    return hpg
+
+
 def kernel_bytes(name: str, d: Dims) -> int:
     """Algorithmic DRAM bytes of one launch of the kernel `name`."""
     t = _terms(d)
+    nb = tc_bwd_nblk(d)
     table = {
+        # tensor-core path
+        "k_state_tc": t["x"] + t["bc"] + 2 * t["vec"] + t["st"],
+        "k_dstates_tc": t["x"] + t["bc"] + t["vec"] + t["st"],
+        "k_scan_tc": t["x"] + 2 * t["bc"] + 2 * t["vec"] + t["st"] + t["y"],
+        "k_scan_tc_dx": 2 * t["x"] + 2 * t["bc"] + 5 * t["vec"] + t["st"] + t["xf"],
+        "k_bwd_dc_tc": 2 * t["x"] + 2 * t["bc"] + 4 * t["vec"] + t["st"] + t["bcf"] * nb,
+        "k_bwd_db_tc": 2 * t["x"] + 2 * t["bc"] + 3 * t["vec"] + t["st"] + t["bcf"] * nb,
+        "k_bwd_finalize_tc": t["dtb"] + 7 * t["vec"] + d.B * d.T * d.H * 4,
+        "k_block_reduce": t["bcf"] * nb + t["bcf"],
         # forward
         "k_chunk_cumsum": t["dtb"] + 2 * t["vec"],
         "k_bmm_cb": 2 * t["bc"] + t["cb"],
@@ -77,7 +98,14 @@ def kernel_bytes(name: str, d: Dims) -> int:
 def kernel_flops(name: str, d: Dims) -> int:
     """Algorithmic FLOPs (2 per multiply-add) of one launch of `name`."""
     tri = d.L * (d.L + 1)               # 2 x the causal (s <= l) pairs of a chunk
+    if name in ("k_scan_tc", "k_scan_tc_dx"):
+        return int(d.B * d.nc * d.G * tri * d.N + d.B * d.nc * d.H * (tri * d.P + 2 * d.L * d.N * d.P))
+    if name in ("k_bwd_dc_tc", "k_bwd_db_tc"):
+        return int(d.B * d.nc * d.G * tri * d.N
+                   + d.B * d.nc * d.H * (tri * d.P + tri * d.N + 2 * d.L * d.P * d.N))
     per_chunk_head = {
+        "k_state_tc": 2 * d.L * d.P * d.N,
+        "k_dstates_tc": 2 * d.L * d.P * d.N,
         "k_chunk_state": 2 * d.L * d.P * d.N,
         "k_chunk_scan": tri * d.P + 2 * d.L * d.N * d.P,
         "k_dyx": tri * d.P,

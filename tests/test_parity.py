@@ -189,3 +189,36 @@ def test_workloads_take_tensor_core_path(cuda_lib):
                              inp.shape.dstate, inp.shape.ngroups, inp.shape.chunk_size)
         run_fwd(cuda_lib, inp)
         assert cuda_lib.last_path() == 1, name
+
+
+TC_BWD_CASES = [
+    ("tcb_n128_l256", SSDShape(2, 1024, 8, 64, 128, 1, 256), 0.0, 0.0),
+    ("tcb_n128_l128_tail_init", SSDShape(2, 700, 8, 64, 128, 2, 128), 0.2, 0.5),
+    ("tcb_n64_l128_tail", SSDShape(1, 333, 6, 64, 64, 3, 128), 0.1, 0.3),
+    ("tcb_n64_l256_heads", SSDShape(2, 512, 12, 64, 64, 1, 256), 0.0, 0.0),
+    ("tcb_partial_tile", SSDShape(1, 300, 2, 64, 128, 1, 256), 0.3, 0.2),
+]
+
+
+@pytest.mark.parametrize("name,shape,init_std,dfinal_std", TC_BWD_CASES,
+                         ids=[c[0] for c in TC_BWD_CASES])
+def test_tensor_core_backward_against_oracle_and_generic(cuda_lib, monkeypatch, name, shape,
+                                                        init_std, dfinal_std):
+    inp = make_inputs(shape, seed=41, dtype="bf16", init_std=init_std, with_dy=True,
+                      dfinal_std=dfinal_std)
+    g = run_bwd(cuda_lib, inp)
+    assert cuda_lib.last_path() == 1
+    ref = oracle_bwd(inp)
+    keys = ["dx", "ddt", "dA", "dB", "dC", "dD", "ddt_bias"]
+    for k in keys:
+        s = assert_close(k, g[k], ref[k], "bf16")
+        assert s["rel_l2"] < 1e-4, (k, s)
+    if inp.init is not None:
+        s = assert_close("dinit", g["dinit_states"], ref["dinit"], "bf16")
+        assert s["rel_l2"] < 1e-4, s
+    monkeypatch.setenv("SSD_FORCE_SIMT", "1")
+    g2 = run_bwd(cuda_lib, inp)
+    assert cuda_lib.last_path() == 0
+    for k in keys:
+        s = stats(g[k], g2[k])
+        assert s["rel_l2"] < 1e-4, (k, s)
