@@ -118,54 +118,53 @@ __device__ __forceinline__ int64_t chunk_vec(int b, int h, int c, int H, int nc,
 }
 
 // ------------------------------------------------------------ chunk_cumsum
-// grid (nc, B, ceil(H/32)).  delta = softplus(dt + dt_bias) (0 past seqlen),
-// a = inclusive in-chunk cumsum of delta * A.
+// delta = softplus(dt + dt_bias) (0 past seqlen), a = inclusive in-chunk
+// cumsum of delta * A, both laid out (B, H, nc, L).
+// Warp-per-chunk variant: grid ceil(B*nc*H / 8) blocks of 8 warps; warp w
+// handles (b, c, h) = unravel(w); lane k the E = ceil(L/32) consecutive
+// positions starting at k*E.  All dt loads of a lane are issued together.
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
-    k_chunk_cumsum(const Tin* __restrict__ dt, const float* __restrict__ dt_bias,
-                   const float* __restrict__ A, float* __restrict__ delta,
-                   float* __restrict__ acs, int T, int H, int L, int nc) {
-  __shared__ float sv[256][33];
-  const int c = blockIdx.x, b = blockIdx.y, h0 = blockIdx.z * 32;
-  for (int i = threadIdx.x; i < L * 32; i += kThreads) {
-    const int l = i >> 5, hh = i & 31, t = c * L + l, h = h0 + hh;
-    float v = 0.f;
-    if (t < T && h < H) {
-      const float raw = ldf(dt + ((int64_t)b * T + t) * H + h) + (dt_bias ? dt_bias[h] : 0.f);
-      v = softplus_f(raw);
-    }
-    sv[l][hh] = v;
-  }
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    k_chunk_cumsum_warp(const Tin* __restrict__ dt, const float* __restrict__ dt_bias,
+                        const float* __restrict__ A, float* __restrict__ delta,
+                        float* __restrict__ acs, int B, int T, int H, int L, int nc) {
+  const int64_t wid = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= (int64_t)B * nc * H) return;
+  const int h = (int)(wid % H);
+  const int64_t bc = wid / H;
+  const int c = (int)(bc % nc), b = (int)(bc / nc);
   const int E = (L + 31) / 32;
-  for (int hh = warp; hh < 32; hh += kThreads / 32) {
-    const int h = h0 + hh;
-    if (h >= H) break;
-    const float Ah = A[h];
-    float vals[8];
-    float run = 0.f;
+  const float bias = dt_bias ? dt_bias[h] : 0.f, Ah = A[h];
+  float dv[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int l = lane * E + e;
-      if (e < E && l < L) run += sv[l][hh] * Ah;
-      vals[e] = run;
-    }
-    float tot = run;
+  for (int e = 0; e < 8; ++e) {
+    const int l = lane * E + e, t = c * L + l;
+    dv[e] = (e < E && l < L && t < T) ? ldf(dt + ((int64_t)b * T + t) * H + h) : 0.f;
+  }
+  float run = 0.f, vals[8];
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float o = __shfl_up_sync(0xffffffffu, tot, off);
-      if (lane >= off) tot += o;
-    }
-    const float excl = tot - run;
-    const int64_t base = chunk_vec(b, h, c, H, nc, L);
+  for (int e = 0; e < 8; ++e) {
+    const int l = lane * E + e, t = c * L + l;
+    const float d = (e < E && l < L && t < T) ? softplus_f(dv[e] + bias) : 0.f;
+    dv[e] = d;
+    run += d * Ah;
+    vals[e] = run;
+  }
+  float tot = run;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int l = lane * E + e;
-      if (e < E && l < L) {
-        delta[base + l] = sv[l][hh];
-        acs[base + l] = excl + vals[e];
-      }
+  for (int off = 1; off < 32; off <<= 1) {
+    const float o = __shfl_up_sync(0xffffffffu, tot, off);
+    if (lane >= off) tot += o;
+  }
+  const float excl = tot - run;
+  const int64_t base = chunk_vec(b, h, c, H, nc, L);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int l = lane * E + e;
+    if (e < E && l < L) {
+      delta[base + l] = dv[e];
+      acs[base + l] = excl + vals[e];
     }
   }
 }
@@ -769,29 +768,39 @@ __global__ void k_group_reduce(const float* __restrict__ perhead, float* __restr
   out[i] = s;
 }
 
-// grid (H).  Per-head parameter gradients from the per-chunk partials.
+// grid (H), 32 threads.  Per-head parameter gradients from the per-chunk
+// partials: lane k sums the chunks k, k+32, ... in order, then a fixed
+// xor-tree combines the lanes (bit-reproducible).
 __global__ void k_param_grads(const float* __restrict__ part, float* __restrict__ dA,
                               float* __restrict__ ddt_bias, float* __restrict__ dD, int B, int H,
                               int nc) {
-  if (threadIdx.x != 0) return;
-  const int h = blockIdx.x;
+  const int h = blockIdx.x, lane = threadIdx.x;
   float a = 0.f, bb = 0.f, dd = 0.f;
-  for (int b = 0; b < B; ++b)
-    for (int c = 0; c < nc; ++c) {
-      const float* o = part + (((int64_t)b * H + h) * nc + c) * 3;
-      a += o[0];
-      bb += o[1];
-      dd += o[2];
-    }
-  dA[h] = a;
-  if (ddt_bias) ddt_bias[h] = bb;
-  if (dD) dD[h] = dd;
+  for (int i = lane; i < B * nc; i += 32) {
+    const int b = i / nc, c = i % nc;
+    const float* o = part + (((int64_t)b * H + h) * nc + c) * 3;
+    a += o[0];
+    bb += o[1];
+    dd += o[2];
+  }
+  for (int off = 16; off > 0; off >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, off);
+    bb += __shfl_xor_sync(0xffffffffu, bb, off);
+    dd += __shfl_xor_sync(0xffffffffu, dd, off);
+  }
+  if (lane == 0) {
+    dA[h] = a;
+    if (ddt_bias) ddt_bias[h] = bb;
+    if (dD) dD[h] = dd;
+  }
 }
 
 template <typename Tin>
 void launch_cumsum(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
-  SSD_LAUNCH("k_chunk_cumsum", s, k_chunk_cumsum<Tin><<<dim3(d.nc, d.B, (d.H + 31) / 32), kThreads, 0, s>>>(
-      static_cast<const Tin*>(a.dt), a.dt_bias, a.A, w.delta, w.acs, d.T, d.H, d.L, d.nc));
+  const int64_t warps = (int64_t)d.B * d.nc * d.H;
+  const int blocks = (int)((warps + kThreads / 32 - 1) / (kThreads / 32));
+  SSD_LAUNCH("k_chunk_cumsum", s, k_chunk_cumsum_warp<Tin><<<blocks, kThreads, 0, s>>>(
+      static_cast<const Tin*>(a.dt), a.dt_bias, a.A, w.delta, w.acs, d.B, d.T, d.H, d.L, d.nc));
 }
 
 bool vec4_ok(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0; }

@@ -31,13 +31,7 @@ __device__ __forceinline__ void store_split8(unsigned char* hi, unsigned char* l
                                              const float (&v)[8]) {
   uint32_t h[4], l[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float h0, l0, h1, l1;
-    split_bf16(v[2 * i], h0, l0);
-    split_bf16(v[2 * i + 1], h1, l1);
-    h[i] = pack_bf16(h0, h1);
-    l[i] = pack_bf16(l0, l1);
-  }
+  for (int i = 0; i < 4; ++i) split2_bf16(v[2 * i], v[2 * i + 1], h[i], l[i]);
   *reinterpret_cast<uint4*>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
   if (lo) *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
 }
@@ -51,6 +45,45 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&v)[8]) {
   }
 }
 
+// Copies rows [0, rows) of 8*nchunk bf16 each into 128-byte-swizzle panels
+// (chunk j of row r -> dst + (j/8)*panel + sw128(r, j%8)) with cp.async;
+// rows >= valid are zero-filled (their source is not read).  The caller
+// commits and waits.
+template <class RowPtr>
+__device__ __forceinline__ void stage_rows_async(unsigned char* dst, int rows, int nchunk,
+                                                 uint32_t panel, int valid, const bf16* safe,
+                                                 RowPtr rowptr) {
+  for (int i = threadIdx.x; i < rows * nchunk; i += 256) {
+    const int r = i / nchunk, j = i % nchunk;
+    const bool v = r < valid;
+    cp_async16(dst + (j / 8) * panel + sw128(r, j % 8), v ? rowptr(r) + j * 8 : safe, v);
+  }
+}
+
+// A 64 x N fp32 state block (row-major, rows p) as hi / lo bf16 panels of 64
+// columns (chunk j of row p -> (j/8)*8 KB + sw128(p, j%8)); all global loads
+// of a thread are issued before any conversion.
+template <int N>
+__device__ __forceinline__ void stage_state_split(unsigned char* hi, unsigned char* lo,
+                                                  const float* __restrict__ src) {
+  constexpr int kPer = 64 * (N / 8) / 256;
+  float4 u[kPer][2];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = threadIdx.x + k * 256, p = i / (N / 8), j = i % (N / 8);
+    u[k][0] = *reinterpret_cast<const float4*>(src + p * N + j * 8);
+    u[k][1] = *reinterpret_cast<const float4*>(src + p * N + j * 8 + 4);
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = threadIdx.x + k * 256, p = i / (N / 8), j = i % (N / 8);
+    const float v[8] = {u[k][0].x, u[k][0].y, u[k][0].z, u[k][0].w,
+                        u[k][1].x, u[k][1].y, u[k][1].z, u[k][1].w};
+    const uint32_t off = (j / 8) * (64 * 128) + sw128(p, j % 8);
+    store_split8(hi + off, lo + off, v);
+  }
+}
+
 // =============================================================== chunk_state
 // grid (nc, B, ceil(H / (2 * pairs))), 256 threads.  For a head pair (h, h+1)
 // of one group and chunk c:
@@ -61,28 +94,32 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&v)[8]) {
 // B = the chunk's Y rows as an MN-major operand (rows l, N columns).
 template <int N, int L>
 struct StateSmem {
-  static constexpr int kPanelB = L * 128;        // bytes of one 64-column panel of L rows
-  static constexpr int kB = (N / 64) * kPanelB;  // B tile
-  static constexpr int kX = 2 * kPanelB;         // w x for a head pair (hi or lo)
-  static constexpr int kBytes = kB + 2 * kX + 2 * L * 4 + 1024;
+  static constexpr int kKB = 64;                    // rows of l per pipeline stage
+  static constexpr int kPanel = kKB * 128;          // one 64-column panel of a stage
+  static constexpr int kB = (N / 64) * kPanel;      // Y rows of the stage
+  static constexpr int kX = 2 * kPanel;             // w X of the head pair (hi or lo)
+  static constexpr int kStage = kB + 2 * kX;
+  static constexpr int kBytes = 2 * kStage + 2 * L * 4 + 1024;
 };
 
+// grid (nc, B, ceil(H / (2 * pairs))), 256 threads, two CTAs per SM.  The
+// chunk's rows stream through a two-stage ring of 64-row blocks: the
+// threads stage block k+1 (Y rows by cp.async, w X split hi / lo) while the
+// tensor core accumulates block k.
 template <int N, int L, int MODE>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(256, 2)
     k_state_tc(const bf16* __restrict__ x, const bf16* __restrict__ Bm,
                const float* __restrict__ delta, const float* __restrict__ acs,
                float* __restrict__ S, int T, int H, int G, int nc, int pairs_per_cta,
                int* status) {
   using SM = StateSmem<N, L>;
+  constexpr int KB = SM::kKB, NKB = L / KB;
   extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t bar;
+  __shared__ uint64_t bar_stage[2], bar_done;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   unsigned char* base = align1024(smem_raw);
-  unsigned char* sB = base;
-  unsigned char* sXh = sB + SM::kB;
-  unsigned char* sXl = sXh + SM::kX;
-  float* sw = reinterpret_cast<float*>(sXl + SM::kX);  // [2][L]
+  float* sw = reinterpret_cast<float*>(base + 2 * SM::kStage);  // [2][L]
 
   const int c = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -95,25 +132,18 @@ __global__ void __launch_bounds__(256, 1)
 
   if (tid == 0) {
     abort_flag = 0;
-    mbar_init(&bar, 1);
+    mbar_init(&bar_stage[0], 1);
+    mbar_init(&bar_stage[1], 1);
+    mbar_init(&bar_done, 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&tmem_base, 128);
-
-  // B rows of the chunk: N/8 chunks of 16 bytes per row, zero past seqlen.
-  constexpr int kBC = N / 8;
-  for (int i = tid; i < L * kBC; i += 256) {
-    const int l = i / kBC, j = i % kBC;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (l < Lv)
-      v = *reinterpret_cast<const uint4*>(Bm + ((((int64_t)b * T + t0 + l) * G + g) * N) + j * 8);
-    *reinterpret_cast<uint4*>(sB + (j / 8) * SM::kPanelB + sw128(l, j % 8)) = v;
-  }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tm = tmem_base;
   constexpr uint32_t idesc = idesc_bf16(128, N, 1, 1);
+  uint32_t n_stage0 = 0, n_stage1 = 0, n_done = 0;
 
   for (int ip = 0; ip < npairs; ++ip) {
     const int h = 2 * (pair0 + ip);
@@ -123,39 +153,61 @@ __global__ void __launch_bounds__(256, 1)
       sw[i] = MODE == 0 ? __expf(acs[cv + L - 1] - acs[cv + l]) * delta[cv + l]
                         : __expf(acs[cv + l]);
     }
-    __syncthreads();
-    // w x for both heads: a row l holds x[l, h:h+2, 0:64] (256 contiguous bytes)
-    for (int i = tid; i < L * 16; i += 256) {
-      const int l = i >> 4, j = i & 15, hh = j >> 3;
-      float v[8];
-      if (l < Lv) {
-        const uint4 u =
-            *reinterpret_cast<const uint4*>(x + (((int64_t)b * T + t0 + l) * H + h) * kP + j * 8);
-        unpack8(u, v);
-        const float wl = sw[hh * L + l];
+    for (int kb = 0; kb < NKB; ++kb) {
+      const int st = kb & 1;
+      unsigned char* sB = base + st * SM::kStage;
+      unsigned char* sXh = sB + SM::kB;
+      unsigned char* sXl = sXh + SM::kX;
+      const int l0 = kb * KB;
+      // the stage is free once the MMAs that read it (two blocks ago) are done
+      const uint32_t ns = st ? n_stage1 : n_stage0;
+      if (ns > 0) mbar_wait(&bar_stage[st], (ns - 1) & 1, status, &abort_flag);
+      stage_rows_async(sB, KB, N / 8, SM::kPanel, Lv - l0, Bm, [&](int l) {
+        return Bm + (((int64_t)b * T + t0 + l0 + l) * G + g) * N;
+      });
+      cp_async_commit();
+      // X rows of both heads (256 contiguous bytes per row): loads first
+      constexpr int kPer = KB * 16 / 256;
+      uint4 u[kPer];
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = tid + k * 256, l = l0 + (i >> 4), j = i & 15;
+        u[k] = l < Lv ? *reinterpret_cast<const uint4*>(x + (((int64_t)b * T + t0 + l) * H + h) *
+                                                                kP + j * 8)
+                      : make_uint4(0, 0, 0, 0);
+      }
+      if (kb == 0) __syncthreads();  // sw ready
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = tid + k * 256, lr = i >> 4, j = i & 15, hh = j >> 3;
+        float v[8];
+        unpack8(u[k], v);
+        const float wl = sw[hh * L + l0 + lr];
 #pragma unroll
         for (int q = 0; q < 8; ++q) v[q] *= wl;
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = 0.f;
+        const uint32_t off = hh * SM::kPanel + sw128(lr, j & 7);
+        store_split8(sXh + off, sXl + off, v);
       }
-      const uint32_t off = hh * SM::kPanelB + sw128(l, j & 7);
-      store_split8(sXh + off, sXl + off, v);
-    }
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-      fence_after_sync();
-      for (int ks = 0; ks < L / 16; ++ks) {
-        const uint64_t bd = sdesc(smem_u32(sB) + ks * 2048, SM::kPanelB, 1024);
-        mma_bf16(tm, sdesc(smem_u32(sXh) + ks * 2048, SM::kPanelB, 1024), bd, idesc,
-                 ks > 0 ? 1u : 0u);
-        mma_bf16(tm, sdesc(smem_u32(sXl) + ks * 2048, SM::kPanelB, 1024), bd, idesc, 1u);
+      cp_async_wait<0>();
+      fence_async_smem();
+      fence_before_sync();
+      __syncthreads();
+      if (tid == 0) {
+        fence_after_sync();
+        for (int ks = 0; ks < KB / 16; ++ks) {
+          const uint64_t bd = sdesc(smem_u32(sB) + ks * 2048, SM::kPanel, 1024);
+          const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
+          mma_bf16(tm, sdesc(smem_u32(sXh) + ks * 2048, SM::kPanel, 1024), bd, idesc, acc);
+          mma_bf16(tm, sdesc(smem_u32(sXl) + ks * 2048, SM::kPanel, 1024), bd, idesc, 1u);
+        }
+        mma_commit(&bar_stage[st]);
+        if (kb == NKB - 1) mma_commit(&bar_done);
       }
-      mma_commit(&bar);
+      if (st) ++n_stage1;
+      else ++n_stage0;
     }
-    const bool ok = mbar_wait(&bar, ip & 1, status, &abort_flag);
+    ++n_done;
+    const bool ok = mbar_wait(&bar_done, (n_done - 1) & 1, status, &abort_flag);
     fence_after_sync();
     if (ok) {
       // lanes 32 q .. 32 q + 31 = rows m; warps q and q + 4 split the N columns
@@ -174,7 +226,7 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
     fence_before_sync();
-    __syncthreads();
+    __syncthreads();  // accumulator and sw are reused by the next pair
   }
   if (warp == 0) tmem_dealloc(tm, 128);
 }
@@ -191,20 +243,28 @@ __global__ void __launch_bounds__(256, 1)
 //     per head: Y  = sum_l P[s, l] dy_l,  P = CBT e^{a_l - a_s} [l >= s]
 //               ST = B_s . dS_c[p, :]
 //               u_s = Y + e^{a_last - a_s} ST;  dx_s = delta_s u_s + D dy_s
-//               ddir_s = <x_s, u_s>,  qrow_s = delta_s <x_s, e^{a_last - a_s} ST>
+//               ddir_s = <x_s, u_s>,  qrow_s = delta_s <x_s, e^{a_last - a_s} ST>,
+//               ddiag_s = <x_s, dy_s>
 // grid (nc * L/128, B, ceil(H / heads_per_cta)), 256 threads; the heads of a
-// CTA belong to one group.
+// CTA belong to one group.  After the shared score tile, the two warpgroups
+// run independent pipelines on alternate heads (own TMEM accumulators, P
+// buffer, operand rows and mbarriers), so one group's loads and waits overlap
+// the other's work.
 template <int N, int L>
 struct ScanSmem {
   static constexpr int kLT = 128;
   static constexpr int kC = (N / 64) * kLT * 128;           // row-operand rows of the tile
   static constexpr int kBrows = (N / 64) * L * 128;         // column-operand rows
-  static constexpr int kPbuf = 2 * kLT * 128;               // one P panel, hi + lo
-  static constexpr int kBP = kBrows > 2 * kPbuf ? kBrows : 2 * kPbuf;
-  static constexpr int kX = L * 128;                        // x or dy rows, one MN panel
-  static constexpr int kHhalf = (N / 64) * 64 * 128;        // H or dS (hi or lo), K-major
-  static constexpr int kBytes = kC + kBP + kX + 2 * kHhalf + (2 * L + 3 * 128) * 4 + 1024;
+  static constexpr int kPw = 2 * kLT * 128;                 // per group: P panel hi + lo
+  static constexpr int kBP = kBrows > 2 * kPw ? kBrows : 2 * kPw;
+  static constexpr int kX = L * 128;                        // per group: x or dy rows
+  static constexpr int kHlo = (N / 64) * 64 * 128;          // offset of the state's lo part
+  static constexpr int kBytes = kC + kBP + 2 * kX + 4 * L * 4 + 1024;
 };
+
+__device__ __forceinline__ void group_sync(int id) {
+  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
+}
 
 template <int N, int L, typename Tout, bool REV>
 __global__ void __launch_bounds__(256, 1)
@@ -217,20 +277,15 @@ __global__ void __launch_bounds__(256, 1)
               int* status) {
   using SM = ScanSmem<N, L>;
   constexpr int LT = SM::kLT, NLT = L / LT;
-  constexpr uint32_t kColY = 256, kColST = 320;
   extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t bar_cb, bar_done, bar_p[2];
+  __shared__ uint64_t bar_cb, bar_p[2], bar_st[2], bar_done[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   unsigned char* base = align1024(smem_raw);
   unsigned char* sR = base;               // row operand: C (fwd) or B (rev) rows of the tile
-  unsigned char* sBP = sR + SM::kC;       // column operand rows, later the P panels
-  unsigned char* sX = sBP + SM::kBP;      // x (fwd) or dy (rev) rows of the columns
-  unsigned char* sHh = sX + SM::kX;
-  unsigned char* sHl = sHh + SM::kHhalf;
-  float* sa = reinterpret_cast<float*>(sHl + SM::kHhalf);
-  float* sd = sa + L;
-  float* sred = sd + L;                   // [3][128] half-row partial sums (rev)
+  unsigned char* sBP = sR + SM::kC;       // column operand rows, later the groups' P buffers
+  unsigned char* sXall = sBP + SM::kBP;   // per group: x (fwd) or dy (rev) rows
+  float* sAall = reinterpret_cast<float*>(sXall + 2 * SM::kX);  // per group: a [L], delta [L]
 
   const int c = blockIdx.x / NLT, tile = blockIdx.x % NLT, b = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -244,37 +299,29 @@ __global__ void __launch_bounds__(256, 1)
   const int nsp = ncol / 64;
   const int64_t t0 = (int64_t)c * L;
   const int Lv = min(L, T - (int)t0);
-  const bf16* rowsrc = REV ? Bm : Cm;             // row operand of the score tile
-  const bf16* colsrc = REV ? Cm : Bm;             // column operand
-  const bf16* opsrc = REV ? dy : x;               // second MMA operand (per head)
+  const bf16* rowsrc = REV ? Bm : Cm;
+  const bf16* colsrc = REV ? Cm : Bm;
+  const bf16* opsrc = REV ? dy : x;
 
   if (tid == 0) {
     abort_flag = 0;
     mbar_init(&bar_cb, 1);
-    mbar_init(&bar_done, 1);
-    mbar_init(&bar_p[0], 1);
-    mbar_init(&bar_p[1], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_p[i], 1);
+      mbar_init(&bar_st[i], 1);
+      mbar_init(&bar_done[i], 1);
+    }
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&tmem_base, 512);
-
-  constexpr int kRC = N / 8;
-  for (int i = tid; i < LT * kRC; i += 256) {
-    const int rr = i / kRC, j = i % kRC, row = r0 + rr;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (row < Lv)
-      v = *reinterpret_cast<const uint4*>(rowsrc + ((((int64_t)b * T + t0 + row) * G + g) * N) +
-                                          j * 8);
-    *reinterpret_cast<uint4*>(sR + (j / 8) * (LT * 128) + sw128(rr, j % 8)) = v;
-  }
-  for (int i = tid; i < ncol * kRC; i += 256) {
-    const int cc = i / kRC, j = i % kRC, col = col0 + cc;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (col < Lv)
-      v = *reinterpret_cast<const uint4*>(colsrc + ((((int64_t)b * T + t0 + col) * G + g) * N) +
-                                          j * 8);
-    *reinterpret_cast<uint4*>(sBP + (j / 8) * (L * 128) + sw128(cc, j % 8)) = v;
-  }
+  stage_rows_async(sR, LT, N / 8, LT * 128, Lv - r0, rowsrc, [&](int rr2) {
+    return rowsrc + (((int64_t)b * T + t0 + r0 + rr2) * G + g) * N;
+  });
+  stage_rows_async(sBP, ncol, N / 8, L * 128, Lv - col0, colsrc, [&](int cc) {
+    return colsrc + (((int64_t)b * T + t0 + col0 + cc) * G + g) * N;
+  });
+  cp_async_commit();
+  cp_async_wait<0>();
   fence_async_smem();
   fence_before_sync();
   __syncthreads();
@@ -291,166 +338,184 @@ __global__ void __launch_bounds__(256, 1)
   }
   mbar_wait(&bar_cb, 0, status, &abort_flag);
   fence_after_sync();
+  // sBP (the column operand) is free from here on: it becomes the P buffers.
+  __syncthreads();
 
-  const int q = warp & 3, half = warp >> 2;
+  const int wg = tid >> 7, wtid = tid & 127, q = warp & 3;
   const int rr = 32 * q + lane, r = r0 + rr;  // this thread's row (TMEM lane)
   const uint32_t tlane = tm + ((uint32_t)(32 * q) << 16);
-  unsigned char* Phi[2] = {sBP, sBP + SM::kPbuf};
-  uint32_t ncommit[2] = {0, 0};
+  const uint32_t colY = 256 + 128 * wg, colST = colY + 64;
+  unsigned char* Pw = sBP + wg * SM::kPw;
+  unsigned char* sX = sXall + wg * SM::kX;
+  float* sa2 = sAall + wg * 2 * L;  // a * log2(e)
+  float* sx = sa2 + L;              // fwd: a*log2e - log2(delta)  (+inf where delta = 0); rev: delta
+  const int gbar = 1 + wg;
+  uint32_t n_p = 0, n_st = 0, n_done = 0;
   constexpr uint32_t id_py = idesc_bf16(128, kP, 0, 1);
   constexpr uint32_t id_st = idesc_bf16(128, kP, 0, 0);
 
-  for (int h = h_begin, it = 0; h < h_end; ++h, ++it) {
+  for (int h = h_begin + wg; h < h_end; h += 2) {
     const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
-    for (int i = tid; i < L; i += 256) {
-      sa[i] = acs[cv + i];
-      sd[i] = delta[cv + i];
-    }
-    // second operand rows (columns of the score tile): one MN-major panel
-    for (int i = tid; i < ncol * 8; i += 256) {
+    // second operand rows of this head (columns of the score tile)
+    for (int i = wtid; i < ncol * 8; i += 128) {
       const int cc = i >> 3, j = i & 7, col = col0 + cc;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (col < Lv)
-        v = *reinterpret_cast<const uint4*>(opsrc + (((int64_t)b * T + t0 + col) * H + h) * kP +
-                                            j * 8);
-      *reinterpret_cast<uint4*>(sX + sw128(cc, j)) = v;
+      const bool v = col < Lv;
+      cp_async16(sX + sw128(cc, j),
+                 v ? opsrc + (((int64_t)b * T + t0 + col) * H + h) * kP + j * 8 : opsrc, v);
     }
-    // inter-chunk state (H_c forward, dS_c backward), fp32 64 x N -> hi / lo
-    const float* Sc = state + (((int64_t)b * nc + c) * H + h) * kP * N;
-    for (int i = tid; i < kP * (N / 8); i += 256) {
-      const int p = i / (N / 8), j = i % (N / 8);
-      const float4 u0 = *reinterpret_cast<const float4*>(Sc + p * N + j * 8);
-      const float4 u1 = *reinterpret_cast<const float4*>(Sc + p * N + j * 8 + 4);
-      const float v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-      const uint32_t off = (j / 8) * (64 * 128) + sw128(p, j % 8);
-      store_split8(sHh + off, sHl + off, v);
+    cp_async_commit();
+    for (int i = wtid; i < L; i += 128) {
+      const float a2 = acs[cv + i] * kLog2e, dl = delta[cv + i];
+      sa2[i] = a2;
+      sx[i] = REV ? dl : (dl > 0.f ? a2 - lg2_approx(dl) : __int_as_float(0x7f800000));
     }
+    // the group's P buffer is free once its previous MMAs have completed
+    if (n_p > 0) mbar_wait(&bar_p[wg], (n_p - 1) & 1, status, &abort_flag);
+    {
+      // inter-chunk state (H_c / dS_c), fp32 64 x N -> hi / lo into the P buffer
+      const float* src = state + (((int64_t)b * nc + c) * H + h) * kP * N;
+      constexpr int kPer = 64 * (N / 8) / 128;
+      float4 u[kPer][2];
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = wtid + k * 128, p = i / (N / 8), j = i % (N / 8);
+        u[k][0] = *reinterpret_cast<const float4*>(src + p * N + j * 8);
+        u[k][1] = *reinterpret_cast<const float4*>(src + p * N + j * 8 + 4);
+      }
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = wtid + k * 128, p = i / (N / 8), j = i % (N / 8);
+        const float v[8] = {u[k][0].x, u[k][0].y, u[k][0].z, u[k][0].w,
+                            u[k][1].x, u[k][1].y, u[k][1].z, u[k][1].w};
+        const uint32_t off = (j / 8) * (64 * 128) + sw128(p, j % 8);
+        store_split8(Pw + off, Pw + SM::kHlo + off, v);
+      }
+    }
+    cp_async_wait<0>();
     fence_async_smem();
     fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
+    group_sync(gbar);
+    if (wtid == 0) {
       fence_after_sync();
       for (int ks = 0; ks < N / 16; ++ks) {
         const uint32_t kp = ks / 4, ko = (ks % 4) * 32;
         const uint64_t ad = sdesc(smem_u32(sR) + kp * (LT * 128) + ko, 16, 1024);
-        mma_bf16(tm + kColST, ad, sdesc(smem_u32(sHh) + kp * (64 * 128) + ko, 16, 1024), id_st,
+        mma_bf16(tm + colST, ad, sdesc(smem_u32(Pw) + kp * (64 * 128) + ko, 16, 1024), id_st,
                  ks > 0 ? 1u : 0u);
-        mma_bf16(tm + kColST, ad, sdesc(smem_u32(sHl) + kp * (64 * 128) + ko, 16, 1024), id_st,
-                 1u);
+        mma_bf16(tm + colST, ad, sdesc(smem_u32(Pw) + SM::kHlo + kp * (64 * 128) + ko, 16, 1024),
+                 id_st, 1u);
       }
+      mma_commit(&bar_st[wg]);
     }
-    const float ar = sa[r];
+    ++n_st;
+    mbar_wait(&bar_st[wg], (n_st - 1) & 1, status, &abort_flag);  // P buffer free again
+    fence_after_sync();
+    const float ar2 = sa2[r];
     for (int j = 0; j < nsp; ++j) {
-      const int buf = j & 1;
-      if (ncommit[buf] > 0) mbar_wait(&bar_p[buf], (ncommit[buf] - 1) & 1, status, &abort_flag);
-      unsigned char* ph = Phi[buf];
-      unsigned char* pl = ph + LT * 128;
-      float cb[32];
-      tmem_ld16(tlane + 64 * j + 32 * half, *reinterpret_cast<float(*)[16]>(cb));
-      tmem_ld16(tlane + 64 * j + 32 * half + 16, *reinterpret_cast<float(*)[16]>(cb + 16));
-      tmem_wait_ld();
+      if (j > 0) mbar_wait(&bar_p[wg], (n_p - 1) & 1, status, &abort_flag);
+      const float* colv = (REV ? sa2 : sx) + col0 + 64 * j;  // per-column log2 terms
 #pragma unroll
-      for (int k8 = 0; k8 < 4; ++k8) {
-        float v[8];
+      for (int hf = 0; hf < 2; ++hf) {
+        float cb[32];
+        tmem_ld16(tlane + 64 * j + 32 * hf, *reinterpret_cast<float(*)[16]>(cb));
+        tmem_ld16(tlane + 64 * j + 32 * hf + 16, *reinterpret_cast<float(*)[16]>(cb + 16));
+        tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int cl = col0 + 64 * j + 32 * half + 8 * k8 + e;  // chunk-local column
-          if constexpr (REV)
-            v[e] = cl >= r ? cb[8 * k8 + e] * __expf(sa[cl] - ar) : 0.f;
-          else
-            v[e] = cl <= r ? cb[8 * k8 + e] * __expf(ar - sa[cl]) * sd[cl] : 0.f;
+        for (int k8 = 0; k8 < 4; ++k8) {
+          const int c8 = 32 * hf + 8 * k8;  // panel-local column of the chunk
+          const float4 w0 = *reinterpret_cast<const float4*>(colv + c8);
+          const float4 w1 = *reinterpret_cast<const float4*>(colv + c8 + 4);
+          const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int cl = col0 + 64 * j + c8 + e;  // chunk-local column
+            const float f = REV ? ex2_approx(wv[e] - ar2) : ex2_approx(ar2 - wv[e]);
+            v[e] = (REV ? cl >= r : cl <= r) ? cb[8 * k8 + e] * f : 0.f;
+          }
+          const uint32_t off = sw128(rr, c8 / 8);
+          store_split8(Pw + off, Pw + LT * 128 + off, v);
         }
-        const uint32_t off = sw128(rr, 4 * half + k8);
-        store_split8(ph + off, pl + off, v);
       }
       fence_async_smem();
       fence_before_sync();
-      __syncthreads();
-      if (tid == 0) {
+      group_sync(gbar);
+      if (wtid == 0) {
         fence_after_sync();
         for (int ks = 0; ks < 4; ++ks) {
           const uint64_t bd = sdesc(smem_u32(sX) + (64 * j + 16 * ks) * 128, L * 128, 1024);
-          mma_bf16(tm + kColY, sdesc(smem_u32(ph) + ks * 32, 16, 1024), bd, id_py,
+          mma_bf16(tm + colY, sdesc(smem_u32(Pw) + ks * 32, 16, 1024), bd, id_py,
                    (j > 0 || ks > 0) ? 1u : 0u);
-          mma_bf16(tm + kColY, sdesc(smem_u32(pl) + ks * 32, 16, 1024), bd, id_py, 1u);
+          mma_bf16(tm + colY, sdesc(smem_u32(Pw) + LT * 128 + ks * 32, 16, 1024), bd, id_py, 1u);
         }
-        mma_commit(&bar_p[buf]);
+        mma_commit(&bar_p[wg]);
+        if (j == nsp - 1) mma_commit(&bar_done[wg]);  // one phase per head
       }
-      ncommit[buf]++;
+      ++n_p;
     }
-    if (tid == 0) mma_commit(&bar_done);
-    const bool ok = mbar_wait(&bar_done, it & 1, status, &abort_flag);
+    ++n_done;
+    const bool ok = mbar_wait(&bar_done[wg], (n_done - 1) & 1, status, &abort_flag);
     fence_after_sync();
-    float pd = 0.f, pq = 0.f, pdd = 0.f;  // rev: partial <x, u>, <x, state part>, <x, dy>
     if (ok) {
-      float yv[32], st[32];
-      tmem_ld16(tlane + kColY + 32 * half, *reinterpret_cast<float(*)[16]>(yv));
-      tmem_ld16(tlane + kColY + 32 * half + 16, *reinterpret_cast<float(*)[16]>(yv + 16));
-      tmem_ld16(tlane + kColST + 32 * half, *reinterpret_cast<float(*)[16]>(st));
-      tmem_ld16(tlane + kColST + 32 * half + 16, *reinterpret_cast<float(*)[16]>(st + 16));
-      tmem_wait_ld();
-      if (r < Lv) {
-        const float Dh = D ? D[h] : 0.f;
-        const int64_t rowoff = (((int64_t)b * T + t0 + r) * H + h) * kP + 32 * half;
-        if constexpr (!REV) {
-          const float ea = __expf(ar);
+      const float Dh = D ? D[h] : 0.f;
+      const int64_t rowoff = (((int64_t)b * T + t0 + r) * H + h) * kP;
+      const float ea = ex2_approx(ar2), es = ex2_approx(sa2[L - 1] - ar2);
+      const float dr = REV ? sx[r] : 0.f;
+      float pd = 0.f, pq = 0.f, pdd = 0.f;
 #pragma unroll
-          for (int k8 = 0; k8 < 4; ++k8) {
-            float xv[8], o[8];
-            unpack8(*reinterpret_cast<const uint4*>(sX + sw128(rr + r0 - col0, 4 * half + k8)),
-                    xv);
+      for (int c16 = 0; c16 < 4; ++c16) {
+        float yv[16], st[16];
+        tmem_ld16(tlane + colY + 16 * c16, yv);
+        tmem_ld16(tlane + colST + 16 * c16, st);
+        tmem_wait_ld();
+        if (r < Lv) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = yv[8 * k8 + e] + ea * st[8 * k8 + e] + Dh * xv[e];
+          for (int k8 = 0; k8 < 2; ++k8) {
+            float ov[8], o[8];
+            unpack8(*reinterpret_cast<const uint4*>(sX + sw128(r - col0, 2 * c16 + k8)), ov);
+            if constexpr (!REV) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                o[e] = yv[8 * k8 + e] + ea * st[8 * k8 + e] + Dh * ov[e];
+            } else {
+              float xv[8];
+              unpack8(*reinterpret_cast<const uint4*>(x + rowoff + 16 * c16 + 8 * k8), xv);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float us = es * st[8 * k8 + e];
+                const float u = yv[8 * k8 + e] + us;
+                o[e] = fmaf(dr, u, Dh * ov[e]);
+                pd = fmaf(xv[e], u, pd);
+                pq = fmaf(xv[e], us, pq);
+                pdd = fmaf(xv[e], ov[e], pdd);
+              }
+            }
+            Tout* op = out + rowoff + 16 * c16 + 8 * k8;
             if constexpr (sizeof(Tout) == 4) {
-              float* of = reinterpret_cast<float*>(out + rowoff) + 8 * k8;
+              float* of = reinterpret_cast<float*>(op);
               *reinterpret_cast<float4*>(of) = make_float4(o[0], o[1], o[2], o[3]);
               *reinterpret_cast<float4*>(of + 4) = make_float4(o[4], o[5], o[6], o[7]);
             } else {
-              *reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(out + rowoff) + 8 * k8) =
+              *reinterpret_cast<uint4*>(op) =
                   make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
                              pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
             }
           }
-        } else {
-          const float es = __expf(sa[L - 1] - ar), dr = sd[r];
-#pragma unroll
-          for (int k8 = 0; k8 < 4; ++k8) {
-            float dyv[8], xv[8], o[8];
-            unpack8(*reinterpret_cast<const uint4*>(sX + sw128(rr + r0 - col0, 4 * half + k8)),
-                    dyv);
-            unpack8(*reinterpret_cast<const uint4*>(x + rowoff + 8 * k8), xv);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float us = es * st[8 * k8 + e];
-              const float u = yv[8 * k8 + e] + us;
-              o[e] = fmaf(dr, u, Dh * dyv[e]);
-              pd = fmaf(xv[e], u, pd);
-              pq = fmaf(xv[e], us, pq);
-              pdd = fmaf(xv[e], dyv[e], pdd);
-            }
-            float* of = reinterpret_cast<float*>(out + rowoff) + 8 * k8;
-            *reinterpret_cast<float4*>(of) = make_float4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<float4*>(of + 4) = make_float4(o[4], o[5], o[6], o[7]);
-          }
+        }
+      }
+      if constexpr (REV) {
+        if (r < Lv) {
+          ddir[cv + r] = pd;
+          qrow[cv + r] = dr * pq;
+          ddiag[cv + r] = pdd;
         }
       }
     }
-    if constexpr (REV) {
-      if (half == 1) {
-        sred[rr] = pd;
-        sred[128 + rr] = pq;
-        sred[256 + rr] = pdd;
-      }
-      __syncthreads();
-      if (half == 0 && r < Lv) {
-        ddir[cv + r] = pd + sred[rr];
-        qrow[cv + r] = sd[r] * (pq + sred[128 + rr]);
-        ddiag[cv + r] = pdd + sred[256 + rr];
-      }
-    }
     fence_before_sync();
-    __syncthreads();
+    group_sync(gbar);  // sX, sa, sd and the accumulators are reused by the next head
   }
+  fence_before_sync();
+  __syncthreads();
   if (warp == 0) tmem_dealloc(tm, 512);
 }
 
@@ -503,9 +568,9 @@ __global__ void __launch_bounds__(256, 1)
   unsigned char* sHR = sGC + SM::kGC;
   unsigned char* sHC = sHR + SM::kHR;
   unsigned char* sP = sHC + SM::kHC;
-  float* sa = reinterpret_cast<float*>(sP + SM::kPP);
-  float* sd = sa + L;
-  float* sred = sd + L;  // [4][128]
+  float* sa2 = reinterpret_cast<float*>(sP + SM::kPP);  // a * log2(e)
+  float* sx = sa2 + L;   // dC: a*log2e - log2(delta) (+inf at delta = 0); dB: log2(delta) (-inf)
+  float* sred = sx + L;  // [4][128]
 
   const int c = blockIdx.x / NLT, tile = blockIdx.x % NLT, b = blockIdx.y;
   const int nblk = gridDim.z / G, g = blockIdx.z / nblk, kb = blockIdx.z % nblk;
@@ -528,24 +593,19 @@ __global__ void __launch_bounds__(256, 1)
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&tmem_base, 512);
-  constexpr int kRC = N / 8;
-  for (int i = tid; i < LT * kRC; i += 256) {
-    const int rr = i / kRC, j = i % kRC, row = r0 + rr;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (row < Lv)
-      v = *reinterpret_cast<const uint4*>(grow + ((((int64_t)b * T + t0 + row) * G + g) * N) +
-                                          j * 8);
-    *reinterpret_cast<uint4*>(sGR + (j / 8) * (LT * 128) + sw128(rr, j % 8)) = v;
-  }
-  for (int i = tid; i < ncol * kRC; i += 256) {
-    const int cc = i / kRC, j = i % kRC, col = col0 + cc;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (col < Lv)
-      v = *reinterpret_cast<const uint4*>(gcol + ((((int64_t)b * T + t0 + col) * G + g) * N) +
-                                          j * 8);
-    *reinterpret_cast<uint4*>(sGC + (j / 8) * (L * 128) + sw128(cc, j % 8)) = v;
-  }
-  fence_async_smem();
+  stage_rows_async(sGR, LT, N / 8, LT * 128, Lv - r0, grow, [&](int rr2) {
+    return grow + (((int64_t)b * T + t0 + r0 + rr2) * G + g) * N;
+  });
+  stage_rows_async(sGC, ncol, N / 8, L * 128, Lv - col0, gcol, [&](int cc) {
+    return gcol + (((int64_t)b * T + t0 + col0 + cc) * G + g) * N;
+  });
+  auto stage_hc = [&](int hh) {
+    stage_rows_async(sHC, ncol, 8, 0, Lv - col0, hcol, [&](int cc) {
+      return hcol + (((int64_t)b * T + t0 + col0 + cc) * H + hh) * kP;
+    });
+  };
+  stage_hc(h_begin);
+  cp_async_commit();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
@@ -566,29 +626,22 @@ __global__ void __launch_bounds__(256, 1)
   for (int h = h_begin; h < h_end; ++h) {
     const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
     for (int i = tid; i < L; i += 256) {
-      sa[i] = acs[cv + i];
-      sd[i] = delta[cv + i];
+      const float a2 = acs[cv + i] * kLog2e, dl = delta[cv + i];
+      const float l2 = dl > 0.f ? lg2_approx(dl) : -__int_as_float(0x7f800000);
+      sa2[i] = a2;
+      sx[i] = REV ? l2 : a2 - l2;
     }
-    for (int i = tid; i < LT * 8; i += 256) {
-      const int r2 = i >> 3, j = i & 7, row = r0 + r2;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (row < Lv)
-        v = *reinterpret_cast<const uint4*>(hrow + (((int64_t)b * T + t0 + row) * H + h) * kP +
-                                            j * 8);
-      *reinterpret_cast<uint4*>(sHR + sw128(r2, j)) = v;
-    }
-    for (int i = tid; i < ncol * 8; i += 256) {
-      const int cc = i >> 3, j = i & 7, col = col0 + cc;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (col < Lv)
-        v = *reinterpret_cast<const uint4*>(hcol + (((int64_t)b * T + t0 + col) * H + h) * kP +
-                                            j * 8);
-      *reinterpret_cast<uint4*>(sHC + sw128(cc, j)) = v;
-    }
+    // this head's row operand; its column operand was prefetched
+    stage_rows_async(sHR, LT, 8, 0, Lv - r0, hrow, [&](int r2) {
+      return hrow + (((int64_t)b * T + t0 + r0 + r2) * H + h) * kP;
+    });
+    cp_async_commit();
+    cp_async_wait<0>();
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
-    const float ar = sa[r], dr = sd[r];
+    // row constant of the decay exponent (dB folds delta_s of the row in)
+    const float arow = REV ? sa2[r] - sx[r] : sa2[r];
     float mpart = 0.f;
     for (int k = 0; k < npan; ++k) {
       if (tid == 0) {
@@ -620,19 +673,18 @@ __global__ void __launch_bounds__(256, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int k8 = 0; k8 < 4; ++k8) {
+          const float* colv = (REV ? sa2 : sx) + col0 + 128 * k + cb + 8 * k8;
+          const float4 w0 = *reinterpret_cast<const float4*>(colv);
+          const float4 w1 = *reinterpret_cast<const float4*>(colv + 4);
+          const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
           float v[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int cl = col0 + 128 * k + cb + 8 * k8 + e;  // chunk-local column
-            float p2;
-            bool strict;
-            if constexpr (REV) {
-              p2 = cl >= r ? __expf(sa[cl] - ar) * dr * s1[8 * k8 + e] : 0.f;
-              strict = cl > r;
-            } else {
-              p2 = cl <= r ? __expf(ar - sa[cl]) * sd[cl] * s1[8 * k8 + e] : 0.f;
-              strict = cl < r;
-            }
+            const float f = REV ? ex2_approx(wv[e] - arow) : ex2_approx(arow - wv[e]);
+            const bool keep = REV ? cl >= r : cl <= r;
+            const bool strict = REV ? cl > r : cl < r;
+            const float p2 = keep ? f * s1[8 * k8 + e] : 0.f;
             if (strict) mpart = fmaf(s0[8 * k8 + e], p2, mpart);
             v[e] = p2;
           }
@@ -659,26 +711,20 @@ __global__ void __launch_bounds__(256, 1)
       }
       ++n_acc;
     }
-    // state term of this head
+    // state term of this head; the column operand is free: fetch the next head's
     mbar_wait(&bar_acc, (n_acc - 1) & 1, status, &abort_flag);
+    if (h + 1 < h_end) stage_hc(h + 1);
+    cp_async_commit();
     for (int i = tid; i < LT * 8; i += 256) {
       const int r2 = i >> 3, j = i & 7, row = r0 + r2;
       float v[8];
       unpack8(*reinterpret_cast<const uint4*>(sHR + sw128(r2, j)), v);
-      const float sc = REV ? sd[row] * __expf(sa[L - 1] - sa[row]) : __expf(sa[row]);
+      const float sc = REV ? ex2_approx(sa2[L - 1] - sa2[row] + sx[row]) : ex2_approx(sa2[row]);
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[e] *= sc;
       store_split8(sAh + sw128(r2, j), sAl + sw128(r2, j), v);
     }
-    const float* Sc = state + (((int64_t)b * nc + c) * H + h) * kP * N;
-    for (int i = tid; i < kP * (N / 8); i += 256) {
-      const int p = i / (N / 8), j = i % (N / 8);
-      const float4 u0 = *reinterpret_cast<const float4*>(Sc + p * N + j * 8);
-      const float4 u1 = *reinterpret_cast<const float4*>(Sc + p * N + j * 8 + 4);
-      const float v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-      const uint32_t off = (j / 8) * (64 * 128) + sw128(p, j % 8);
-      store_split8(sBh + off, sBl + off, v);
-    }
+    stage_state_split<N>(sBh, sBl, state + (((int64_t)b * nc + c) * H + h) * kP * N);
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -722,7 +768,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) ypart = fmaf(dv[e], st[8 * k8 + e], ypart);
         }
-        ypart *= __expf(ar);
+        ypart *= ex2_approx(sa2[r]);
       }
     }
     if (half == 1) {
@@ -762,6 +808,23 @@ __global__ void __launch_bounds__(256, 1)
 // (dC kernel) and column sums (dB kernel) of M:
 //   ddA_r = sum_{j<r} (colsum_j - rowsum_j) + sum_{l>=r} ycs_l + sum_{s<r} qrow_s + dlast_c
 //   ddt_r = (ddir_r + A ddA_r) softplus'(dt_r + dt_bias);  partials of dA, ddt_bias, dD.
+__device__ __forceinline__ float block_exclusive_scan256(float v, float* warp_tot) {
+  // exclusive prefix of v over the 256 threads of the block, in thread order
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  __syncthreads();
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  float before = 0.f;
+  for (int w = 0; w < warp; ++w) before += warp_tot[w];
+  return before + incl - v;
+}
+
 __global__ void __launch_bounds__(256)
     k_bwd_finalize_tc(const bf16* __restrict__ dt, const float* __restrict__ dt_bias,
                       const float* __restrict__ A, const float* __restrict__ delta,
@@ -770,36 +833,36 @@ __global__ void __launch_bounds__(256)
                       const float* __restrict__ ddir, const float* __restrict__ ddiag,
                       const float* __restrict__ dlast, int nsplit, float* __restrict__ ddt,
                       float* __restrict__ part, int T, int H, int L, int nc) {
-  __shared__ float sdd[256], red[8];
-  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  __shared__ float wt[8], red[8];
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, r = threadIdx.x;
   const int Lv = min(L, T - c * L);
   const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
-  if (tid == 0) {
-    float dl = 0.f;
-    for (int k = 0; k < nsplit; ++k) dl += dlast[(((int64_t)b * H + h) * nc + c) * nsplit + k];
-    float pre = 0.f;
-    for (int r = 0; r < Lv; ++r) {
-      sdd[r] = pre + dl;
-      pre += colsum[cv + r] - rowsum[cv + r] + qrow[cv + r];
-    }
-    float suf = 0.f;
-    for (int r = Lv - 1; r >= 0; --r) {
-      suf += ycs[cv + r];
-      sdd[r] += suf;
-    }
-  }
+  const bool live = r < Lv;
+  const int64_t ti = ((int64_t)b * T + (int64_t)c * L + r) * H + h;
+  const float vdt = live ? __bfloat162float(dt[ti]) : 0.f;
+  const float jump = live ? colsum[cv + r] - rowsum[cv + r] + qrow[cv + r] : 0.f;
+  const float y = live ? ycs[cv + r] : 0.f;
+  const float dirr = live ? ddir[cv + r] : 0.f, dg = live ? ddiag[cv + r] : 0.f;
+  const float dlt = live ? delta[cv + r] : 0.f;
+  float dl = 0.f;
+  for (int k = 0; k < nsplit; ++k) dl += dlast[(((int64_t)b * H + h) * nc + c) * nsplit + k];
+  // ddA_r = prefix_{j<r}(jump_j) + dlast + suffix_{l>=r}(ycs_l)
+  const float pre = block_exclusive_scan256(jump, wt);
+  const float ypre = block_exclusive_scan256(y, wt);   // sum_{l<r} ycs
   __syncthreads();
-  const float Ah = A[h], bias = dt_bias ? dt_bias[h] : 0.f;
+  if ((r & 31) == 31) red[r >> 5] = ypre + y;
+  __syncthreads();
+  const float ytot = red[7];
+  const float dd = pre + dl + (ytot - ypre);
   float pA = 0.f, pB = 0.f, pD = 0.f;
-  for (int r = tid; r < Lv; r += 256) {
-    const int64_t ti = ((int64_t)b * T + (int64_t)c * L + r) * H + h;
-    const float v = __bfloat162float(dt[ti]) + bias;
+  if (live) {
+    const float v = vdt + (dt_bias ? dt_bias[h] : 0.f);
     const float sg = v > 20.f ? 1.f : 1.f / (1.f + __expf(-v));
-    const float gv = fmaf(Ah, sdd[r], ddir[cv + r]) * sg;
+    const float gv = fmaf(A[h], dd, dirr) * sg;
     ddt[ti] = gv;
-    pA = fmaf(delta[cv + r], sdd[r], pA);
-    pB += gv;
-    pD += ddiag[cv + r];
+    pA = dlt * dd;
+    pB = gv;
+    pD = dg;
   }
   float vals[3] = {pA, pB, pD};
 #pragma unroll
@@ -807,9 +870,9 @@ __global__ void __launch_bounds__(256)
     float v = vals[k];
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     __syncthreads();
-    if ((tid & 31) == 0) red[tid >> 5] = v;
+    if ((r & 31) == 0) red[r >> 5] = v;
     __syncthreads();
-    if (tid == 0) {
+    if (r == 0) {
       float t = 0.f;
       for (int i = 0; i < 8; ++i) t += red[i];
       part[(((int64_t)b * H + h) * nc + c) * 3 + k] = t;
@@ -817,19 +880,36 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// out[i, :] = sum_k in[i, k, :] over the nblk head-block partials, in order.
-__global__ void k_block_reduce(const float* __restrict__ in, float* __restrict__ out,
-                               int64_t rows, int nblk, int N) {
+// out[i, :] = sum_k in[i, k, :] over the nblk head-block partials, in order
+// (float4 per thread; N % 4 == 0).
+__global__ void k_block_reduce(const float4* __restrict__ in, float4* __restrict__ out,
+                               int64_t rows, int nblk, int N4) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= rows * N) return;
-  const int64_t row = i / N;
-  const int n = (int)(i % N);
-  float s = 0.f;
-  for (int k = 0; k < nblk; ++k) s += in[(row * nblk + k) * N + n];
+  if (i >= rows * N4) return;
+  const int64_t row = i / N4;
+  const int n = (int)(i % N4);
+  float4 s = in[(row * nblk) * N4 + n];
+  for (int k = 1; k < nblk; ++k) {
+    const float4 v = in[(row * nblk + k) * N4 + n];
+    s.x += v.x;
+    s.y += v.y;
+    s.z += v.z;
+    s.w += v.w;
+  }
   out[i] = s;
 }
 
 // ------------------------------------------------------------------ launch
+// Heads per CTA for the two-pipeline scan kernels: an even divisor of hpg
+// (both warpgroups busy) giving >= target_waves * sms CTAs, else the generic rule.
+int pick_heads_even(int hpg, int units, int sms, int target_waves) {
+  int best = 0;
+  for (int d = 2; d <= hpg; d += 2)
+    if (hpg % d == 0 && (int64_t)units * (hpg / d) >= (int64_t)target_waves * sms) best = d;
+  if (best == 0) best = hpg % 2 == 0 ? 2 : 1;
+  return best;
+}
+
 int pick_heads_per_cta(int hpg, int units, int sms, int target_waves) {
   // largest divisor of hpg that still gives >= target_waves * sms CTAs
   int best = 1;
@@ -859,7 +939,7 @@ cudaError_t launch_tc_forward_t(const Dims& d, const FwdArgs& a, const FwdWs& w,
     using SM = ScanSmem<N, L>;
     auto kern = k_scan_tc<N, L, Tout, false>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
-    const int hpc = pick_heads_per_cta(d.H / d.G, d.B * d.nc * (L / 128) * d.G, sms, 4);
+    const int hpc = pick_heads_even(d.H / d.G, d.B * d.nc * (L / 128) * d.G, sms, 4);
     const dim3 grid(d.nc * (L / 128), d.B, (d.H + hpc - 1) / hpc);
     SSD_LAUNCH("k_scan_tc", s,
                kern<<<grid, 256, SM::kBytes, s>>>(
@@ -911,7 +991,7 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     using SM = ScanSmem<N, L>;
     auto kern = k_scan_tc<N, L, float, true>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
-    const int hpc = pick_heads_per_cta(d.H / d.G, d.B * d.nc * (L / 128) * d.G, sms, 4);
+    const int hpc = pick_heads_even(d.H / d.G, d.B * d.nc * (L / 128) * d.G, sms, 4);
     const dim3 grid(d.nc * (L / 128), d.B, (d.H + hpc - 1) / hpc);
     SSD_LAUNCH("k_scan_tc_dx", s, kern<<<grid, 256, SM::kBytes, s>>>(
         x, Bm, Cm, dy, w.delta, w.acs, w.dS, a.f.D, a.dx, w.ddir, w.qrow, w.ddiag, d.T, d.H,
@@ -942,9 +1022,12 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
       w.qrow, w.ddir, w.ddiag, w.dlast, nsplit, a.ddt, w.part, d.T, d.H, d.L, d.nc));
   if (nblk > 1) {
     const int64_t rows = (int64_t)d.B * d.T * d.G;
-    const int blocks = (int)((rows * d.N + 255) / 256);
-    SSD_LAUNCH("k_block_reduce", s, k_block_reduce<<<blocks, 256, 0, s>>>(w.dCp, a.dC, rows, nblk, d.N));
-    SSD_LAUNCH("k_block_reduce", s, k_block_reduce<<<blocks, 256, 0, s>>>(w.dBp, a.dB, rows, nblk, d.N));
+    const int N4 = d.N / 4;
+    const int blocks = (int)((rows * N4 + 255) / 256);
+    SSD_LAUNCH("k_block_reduce", s, k_block_reduce<<<blocks, 256, 0, s>>>(
+        reinterpret_cast<const float4*>(w.dCp), reinterpret_cast<float4*>(a.dC), rows, nblk, N4));
+    SSD_LAUNCH("k_block_reduce", s, k_block_reduce<<<blocks, 256, 0, s>>>(
+        reinterpret_cast<const float4*>(w.dBp), reinterpret_cast<float4*>(a.dB), rows, nblk, N4));
   }
   simt_param_grads(d, w.part, a.dA, a.ddt_bias, a.dD, s);
   return cudaGetLastError();

@@ -154,10 +154,47 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       : "memory");
 }
 
+// ---------------------------------------------------------------- cp.async
+// 16-byte global -> shared copy; valid == false writes 16 zero bytes (the
+// source is not read).  Completion: cp_async_commit + cp_async_wait<n>.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // --------------------------------------------------------------- bf16 pack
 __device__ __forceinline__ uint32_t pack_bf16(float lo_elem, float hi_elem) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo_elem, hi_elem);
   return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Hardware base-2 exponential / logarithm (MUFU, flush-to-zero); the SSD
+// kernels keep cumulative decays in log2 units so each decay factor is one
+// subtraction and one ex2.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Two fp32 values -> packed bf16 pairs hi = rn(v), lo = rn(v - hi).
+__device__ __forceinline__ void split2_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(a, b);
+  lo = pack_bf16(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xFFFF0000u));
 }
 
 // Split v into two bf16 whose sum carries ~16 significant bits: hi = rn(v),
