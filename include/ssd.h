@@ -72,7 +72,12 @@ typedef struct {
  *   dA_cumsum (B, H, nc, L)       in-chunk inclusive cumsum of delta * A
  *   states    (B, nc, H, P, N)    chunk_state output S_c
  *   hprev     (B, nc, H, P, N)    state entering chunk c (state_passing output)
- * They stay valid until the workspace is reused. */
+ * They stay valid until the workspace is reused.  When the call took the
+ * tensor-core path (ssd_last_path() == 1), the hprev bytes hold each state
+ * (P = 64 rows x N) split into bf16 hi = rn(v) and lo = rn(v - hi) in the
+ * kernels' shared-memory layout instead of f32: per (b, c, h) N/64 "hi"
+ * panels then N/64 "lo" panels, each 64 rows of 128 bytes (64 bf16 of one
+ * row p); the 16-byte chunk j of row p is stored at chunk j ^ (p % 8). */
 typedef struct {
   size_t delta, dA_cumsum, states, hprev, total;
 } ssd_fwd_layout;

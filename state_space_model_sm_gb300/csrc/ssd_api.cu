@@ -107,8 +107,8 @@ BwdOffsets bwd_offsets(const Dims& d) {
 }
 
 struct TcBwdOffsets {
-  size_t delta, acs, S, Hprev, dHs, dS, dlast, rowsum, colsum, ycs, qrow, ddir, ddiag, dBp, dCp,
-      part, total;
+  size_t delta, acs, S, Himg, dHs, dSimg, dlast, rowsum, colsum, ycs, qrow, ddir, ddiag, dBp,
+      dCp, part, total;
 };
 
 TcBwdOffsets tc_bwd_offsets(const Dims& d) {
@@ -120,9 +120,9 @@ TcBwdOffsets tc_bwd_offsets(const Dims& d) {
   o.delta = c.take(vec);
   o.acs = c.take(vec);
   o.S = c.take(st);
-  o.Hprev = c.take(st);
+  o.Himg = c.take(st);
   o.dHs = c.take(st);
-  o.dS = c.take(st);
+  o.dSimg = c.take(st);
   o.dlast = c.take((size_t)d.B * d.H * d.nc * 16 * sizeof(float));
   o.rowsum = c.take(vec);
   o.colsum = c.take(vec);
@@ -163,6 +163,7 @@ FwdWs carve_fwd(char* base, const FwdOffsets& o) {
   w.S = reinterpret_cast<float*>(base + o.S);
   w.Hprev = reinterpret_cast<float*>(base + o.Hprev);
   w.CB = reinterpret_cast<float*>(base + o.CB);
+  w.Himg = nullptr;
   return w;
 }
 
@@ -219,9 +220,16 @@ int ssd_fwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
   if (!workspace || workspace_bytes < o.total || !aligned(workspace, kAlign))
     return SSD_ERR_WORKSPACE;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const FwdWs w = carve_fwd(static_cast<char*>(workspace), o);
+  FwdWs w = carve_fwd(static_cast<char*>(workspace), o);
   const bool tc = !force_simt() && tc_forward_supported(d) && aligned(x, 16) && aligned(B, 16) &&
-                  aligned(C, 16) && aligned(y, 16);
+                  aligned(C, 16) && aligned(y, 16) && aligned(init_states, 16) &&
+                  aligned(final_states, 16);
+  if (tc) {
+    // the tensor-core kernels read the states as split-bf16 images, written in
+    // place of the fp32 states (same bytes; see ssd_fwd_layout)
+    w.Himg = w.Hprev;
+    w.Hprev = nullptr;
+  }
   t_last_path = tc ? 1 : 0;
   const cudaError_t e = tc ? tc_forward(d, a, w, s) : simt_forward(d, a, w, s);
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
@@ -258,7 +266,8 @@ int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
   char* base = static_cast<char*>(workspace);
   const bool tc = !force_simt() && tc_forward_supported(d) && aligned(x, 16) && aligned(B, 16) &&
                   aligned(C, 16) && aligned(dy, 16) && aligned(dx, 16) && aligned(dB, 16) &&
-                  aligned(dC, 16);
+                  aligned(dC, 16) && aligned(init_states, 16) && aligned(dfinal_states, 16) &&
+                  aligned(dinit_states, 16);
   if (tc) {
     const TcBwdOffsets o = tc_bwd_offsets(d);
     if (!workspace || workspace_bytes < o.total || !aligned(workspace, kAlign))
@@ -267,9 +276,9 @@ int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
     w.delta = reinterpret_cast<float*>(base + o.delta);
     w.acs = reinterpret_cast<float*>(base + o.acs);
     w.S = reinterpret_cast<float*>(base + o.S);
-    w.Hprev = reinterpret_cast<float*>(base + o.Hprev);
+    w.Himg = base + o.Himg;
     w.dHs = reinterpret_cast<float*>(base + o.dHs);
-    w.dS = reinterpret_cast<float*>(base + o.dS);
+    w.dSimg = base + o.dSimg;
     w.dlast = reinterpret_cast<float*>(base + o.dlast);
     w.rowsum = reinterpret_cast<float*>(base + o.rowsum);
     w.colsum = reinterpret_cast<float*>(base + o.colsum);
@@ -288,6 +297,7 @@ int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
     return SSD_ERR_WORKSPACE;
   BwdWs w;
   w.f = carve_fwd(base, o.f);
+  w.f.Himg = nullptr;
   w.dHs = reinterpret_cast<float*>(base + o.dHs);
   w.dS = reinterpret_cast<float*>(base + o.dS);
   w.dlast = reinterpret_cast<float*>(base + o.dlast);

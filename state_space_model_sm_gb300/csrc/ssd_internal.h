@@ -75,6 +75,7 @@ struct FwdWs {
   float* S;      // (B, nc, H, P, N)
   float* Hprev;  // (B, nc, H, P, N)
   float* CB;     // (B, nc, G, L, L)
+  void* Himg = nullptr;  // optional (B, nc, H) bf16 hi/lo images of Hprev (tensor-core path)
 };
 
 struct BwdWs {
@@ -89,6 +90,7 @@ struct BwdWs {
   float* dBh;    // (B, T, H, N)
   float* dCh;    // (B, T, H, N)
   float* part;   // (B, H, nc, 3)  per-chunk partial sums of dA, ddt_bias, dD
+  void* dSimg = nullptr;  // optional bf16 hi/lo images of dS (tensor-core path)
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -103,6 +105,7 @@ void simt_state_passing(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStr
 
 int simt_state_passing_bwd(const Dims& d, const float* dHs, const float* acs, const float* Hprev,
                            const float* dfinal, float* dS, float* dlast, float* dinit,
+                           void* dSimg, const void* Himg,
                            cudaStream_t s);  // returns the dlast partials per chunk
 void simt_param_grads(const Dims& d, const float* part, float* dA, float* ddt_bias, float* dD,
                       cudaStream_t s);
@@ -112,9 +115,9 @@ struct TcBwdWs {
   float* delta;   // (B, H, nc, L)
   float* acs;     // (B, H, nc, L)
   float* S;       // (B, nc, H, P, N)
-  float* Hprev;   // (B, nc, H, P, N)
   float* dHs;     // (B, nc, H, P, N)
-  float* dS;      // (B, nc, H, P, N)
+  void* Himg;     // (B, nc, H) split-bf16 shared-memory images of Hprev
+  void* dSimg;    // (B, nc, H) split-bf16 shared-memory images of dS
   float* dlast;   // (B, H, nc, <= 16) partials
   float* rowsum;  // (B, H, nc, L) strict row sums of M (dC kernel)
   float* colsum;  // (B, H, nc, L) strict column sums of M (dB kernel)

@@ -296,6 +296,147 @@ __global__ void __launch_bounds__(kThreads)
   if (final_state) final_state[((int64_t)b * H + h) * PN4 + e] = cur;
 }
 
+// Image-mode state passing (tensor-core path, headdim 64, N % 64 == 0):
+// grid (P*N/2048, H, B); a thread carries 8 consecutive elements of one state
+// row through the recurrence and writes each H_c as one 16-byte hi chunk and
+// one 16-byte lo chunk of the state image.
+__device__ __forceinline__ uint32_t image_chunk_off(int e8, int N) {
+  const int n = (e8 * 8) % N, p = (e8 * 8) / N;
+  return (n >> 6) * 8192u + p * 128u + ((((n & 63) >> 3) ^ (p & 7)) << 4);
+}
+
+__device__ __forceinline__ void split8_store(unsigned char* hi, unsigned char* lo,
+                                             const float4& a, const float4& b) {
+  const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 hb = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    const float2 hf = __bfloat1622float2(hb);
+    const __nv_bfloat162 lb = __floats2bfloat162_rn(v[2 * i] - hf.x, v[2 * i + 1] - hf.y);
+    h[i] = *reinterpret_cast<const uint32_t*>(&hb);
+    l[i] = *reinterpret_cast<const uint32_t*>(&lb);
+  }
+  *reinterpret_cast<uint4*>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__device__ __forceinline__ void image_load8(const unsigned char* hi, const unsigned char* lo,
+                                            float4& a, float4& b) {
+  const uint4 h = *reinterpret_cast<const uint4*>(hi);
+  const uint4 l = *reinterpret_cast<const uint4*>(lo);
+  a.x = __uint_as_float(h.x << 16) + __uint_as_float(l.x << 16);
+  a.y = __uint_as_float(h.x & 0xFFFF0000u) + __uint_as_float(l.x & 0xFFFF0000u);
+  a.z = __uint_as_float(h.y << 16) + __uint_as_float(l.y << 16);
+  a.w = __uint_as_float(h.y & 0xFFFF0000u) + __uint_as_float(l.y & 0xFFFF0000u);
+  b.x = __uint_as_float(h.z << 16) + __uint_as_float(l.z << 16);
+  b.y = __uint_as_float(h.z & 0xFFFF0000u) + __uint_as_float(l.z & 0xFFFF0000u);
+  b.z = __uint_as_float(h.w << 16) + __uint_as_float(l.w << 16);
+  b.w = __uint_as_float(h.w & 0xFFFF0000u) + __uint_as_float(l.w & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ float4 fma4(float d, const float4& c, const float4& s) {
+  return make_float4(fmaf(d, c.x, s.x), fmaf(d, c.y, s.y), fmaf(d, c.z, s.z), fmaf(d, c.w, s.w));
+}
+
+__global__ void __launch_bounds__(kThreads)
+    k_state_passing_img(const float4* __restrict__ S, const float* __restrict__ acs,
+                        const float4* __restrict__ init, unsigned char* __restrict__ img,
+                        float4* __restrict__ final_state, int N, int H, int PN8, int L, int nc) {
+  const int e = blockIdx.x * kThreads + threadIdx.x, h = blockIdx.y, b = blockIdx.z;
+  if (e >= PN8) return;
+  const int64_t step = (int64_t)H * PN8 * 2;             // float4 units between chunks
+  const int64_t base = ((int64_t)b * nc * H + h) * PN8 * 2;  // (b, c=0, h) state, float4 units
+  const uint32_t off = image_chunk_off(e, N), lo_off = (N / 64) * 8192u;
+  const float* ab = acs + ((int64_t)b * H + h) * (int64_t)nc * L + (L - 1);
+  const int64_t sb = ((int64_t)b * H + h) * PN8 * 2 + 2 * e;
+  float4 c0 = init ? init[sb] : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 c1 = init ? init[sb + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < nc; k0 += kPrefetch) {
+    float4 s0[kPrefetch], s1[kPrefetch];
+    float dec[kPrefetch];
+#pragma unroll
+    for (int k = 0; k < kPrefetch; ++k)
+      if (k0 + k < nc) {
+        s0[k] = S[base + (k0 + k) * step + 2 * e];
+        s1[k] = S[base + (k0 + k) * step + 2 * e + 1];
+        dec[k] = __expf(ab[(int64_t)(k0 + k) * L]);
+      }
+#pragma unroll
+    for (int k = 0; k < kPrefetch; ++k)
+      if (k0 + k < nc) {
+        unsigned char* dst = img + (base + (k0 + k) * step) * 16;
+        split8_store(dst + off, dst + off + lo_off, c0, c1);
+        c0 = fma4(dec[k], c0, s0[k]);
+        c1 = fma4(dec[k], c1, s1[k]);
+      }
+  }
+  if (final_state) {
+    final_state[sb] = c0;
+    final_state[sb + 1] = c1;
+  }
+}
+
+// Image-mode state passing backward: grid (nsplit = P*N/2048, H, B); reads the
+// H_c images, writes the dS_c images; dlast partials as in the float4 kernel.
+__global__ void __launch_bounds__(kThreads)
+    k_state_passing_bwd_img(const float4* __restrict__ dHs, const float* __restrict__ acs,
+                            const unsigned char* __restrict__ himg,
+                            const float4* __restrict__ dfinal, unsigned char* __restrict__ dsimg,
+                            float* __restrict__ dlast_part, float4* __restrict__ dinit, int N,
+                            int H, int PN8, int L, int nc) {
+  __shared__ float red[kThreads / 32];
+  const int split = blockIdx.x, nsplit = gridDim.x, h = blockIdx.y, b = blockIdx.z;
+  const int e = split * kThreads + threadIdx.x;
+  const bool live = e < PN8;
+  const int64_t step = (int64_t)H * PN8 * 2;
+  const int64_t base = ((int64_t)b * nc * H + h) * PN8 * 2;
+  const uint32_t off = live ? image_chunk_off(e, N) : 0u, lo_off = (N / 64) * 8192u;
+  const float* ab = acs + ((int64_t)b * H + h) * (int64_t)nc * L + (L - 1);
+  const int64_t sb = ((int64_t)b * H + h) * PN8 * 2 + 2 * e;
+  float4 g0 = (live && dfinal) ? dfinal[sb] : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 g1 = (live && dfinal) ? dfinal[sb + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int kPf = 4;
+  for (int c1 = nc - 1; c1 >= 0; c1 -= kPf) {
+    float4 h0[kPf], h1[kPf], d0[kPf], d1[kPf];
+    float dec[kPf];
+#pragma unroll
+    for (int k = 0; k < kPf; ++k) {
+      const int c = c1 - k;
+      if (c >= 0) {
+        dec[k] = __expf(ab[(int64_t)c * L]);
+        if (live) {
+          const unsigned char* src = himg + (base + c * step) * 16;
+          image_load8(src + off, src + off + lo_off, h0[k], h1[k]);
+          d0[k] = dHs[base + c * step + 2 * e];
+          d1[k] = dHs[base + c * step + 2 * e + 1];
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPf; ++k) {
+      const int c = c1 - k;
+      if (c < 0) break;
+      float part = 0.f;
+      if (live) {
+        unsigned char* dst = dsimg + (base + c * step) * 16;
+        split8_store(dst + off, dst + off + lo_off, g0, g1);
+        part = h0[k].x * g0.x + h0[k].y * g0.y + h0[k].z * g0.z + h0[k].w * g0.w +
+               h1[k].x * g1.x + h1[k].y * g1.y + h1[k].z * g1.z + h1[k].w * g1.w;
+        g0 = fma4(dec[k], g0, d0[k]);
+        g1 = fma4(dec[k], g1, d1[k]);
+      }
+      const float tot = block_sum(part, red);
+      if (threadIdx.x == 0)
+        dlast_part[(((int64_t)b * H + h) * nc + c) * nsplit + split] = dec[k] * tot;
+    }
+  }
+  if (live && dinit) {
+    dinit[sb] = g0;
+    dinit[sb + 1] = g1;
+  }
+}
+
 // Vectorised state_passing backward: grid (nsplit = ceil(P*N/1024), H, B).
 // Each block owns 1024 state elements of one (b, h) and walks the chunks in
 // reverse; the partial dot products <H_c, G_{c+1}> of its slice go to
@@ -807,6 +948,14 @@ bool vec4_ok(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t
 
 void launch_state_passing(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
   const int PN = d.P * d.N;
+  if (w.Himg) {  // tensor-core path: states as split-bf16 images only
+    const int PN8 = PN / 8;
+    SSD_LAUNCH("k_state_passing", s, k_state_passing_img<<<dim3((PN8 + kThreads - 1) / kThreads, d.H, d.B), kThreads, 0, s>>>(
+        reinterpret_cast<const float4*>(w.S), w.acs, reinterpret_cast<const float4*>(a.init),
+        static_cast<unsigned char*>(w.Himg), reinterpret_cast<float4*>(a.final_state), d.N, d.H,
+        PN8, d.L, d.nc));
+    return;
+  }
   if (PN % 4 == 0 && vec4_ok(a.init) && vec4_ok(a.final_state)) {
     const int PN4 = PN / 4;
     SSD_LAUNCH("k_state_passing", s, k_state_passing_v4<<<dim3((PN4 + kThreads - 1) / kThreads, d.H, d.B), kThreads, 0, s>>>(
@@ -841,6 +990,15 @@ void launch_forward(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_
 // Returns the number of dlast partials per (b, h, c) it wrote.
 int launch_state_passing_bwd(const Dims& d, const BwdArgs& a, const BwdWs& w, cudaStream_t s) {
   const int PN = d.P * d.N;
+  if (w.f.Himg && w.dSimg) {  // tensor-core path
+    const int PN8 = PN / 8, nsplit = (PN8 + kThreads - 1) / kThreads;
+    SSD_LAUNCH("k_state_passing_bwd", s, k_state_passing_bwd_img<<<dim3(nsplit, d.H, d.B), kThreads, 0, s>>>(
+        reinterpret_cast<const float4*>(w.dHs), w.f.acs,
+        static_cast<const unsigned char*>(w.f.Himg), reinterpret_cast<const float4*>(a.dfinal),
+        static_cast<unsigned char*>(w.dSimg), w.dlast, reinterpret_cast<float4*>(a.dinit), d.N,
+        d.H, PN8, d.L, d.nc));
+    return nsplit;
+  }
   if (PN % 4 == 0 && vec4_ok(a.dfinal) && vec4_ok(a.dinit)) {
     const int PN4 = PN / 4, nsplit = (PN4 + kThreads - 1) / kThreads;
     SSD_LAUNCH("k_state_passing_bwd", s, k_state_passing_bwd_v4<<<dim3(nsplit, d.H, d.B), kThreads, 0, s>>>(
@@ -912,11 +1070,13 @@ void simt_state_passing(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStr
 
 int simt_state_passing_bwd(const Dims& d, const float* dHs, const float* acs, const float* Hprev,
                            const float* dfinal, float* dS, float* dlast, float* dinit,
-                           cudaStream_t s) {
+                           void* dSimg, const void* Himg, cudaStream_t s) {
   BwdArgs a{};
   a.dfinal = dfinal;
   a.dinit = dinit;
   BwdWs w{};
+  w.dSimg = dSimg;
+  w.f.Himg = const_cast<void*>(Himg);
   w.dHs = const_cast<float*>(dHs);
   w.f.acs = const_cast<float*>(acs);
   w.f.Hprev = const_cast<float*>(Hprev);

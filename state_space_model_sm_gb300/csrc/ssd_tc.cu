@@ -259,7 +259,8 @@ struct ScanSmem {
   static constexpr int kBP = kBrows > 2 * kPw ? kBrows : 2 * kPw;
   static constexpr int kX = L * 128;                        // per group: x or dy rows
   static constexpr int kHlo = (N / 64) * 64 * 128;          // offset of the state's lo part
-  static constexpr int kBytes = kC + kBP + 2 * kX + 4 * L * 4 + 1024;
+  static constexpr int kImg = 2 * kHlo;                     // bytes of one state image
+  static constexpr int kBytes = kC + kBP + 2 * kX + 8 * L * 4 + 1024;
 };
 
 __device__ __forceinline__ void group_sync(int id) {
@@ -271,7 +272,7 @@ __global__ void __launch_bounds__(256, 1)
     k_scan_tc(const bf16* __restrict__ x, const bf16* __restrict__ Bm,
               const bf16* __restrict__ Cm, const bf16* __restrict__ dy,
               const float* __restrict__ delta, const float* __restrict__ acs,
-              const float* __restrict__ state, const float* __restrict__ D,
+              const unsigned char* __restrict__ simg, const float* __restrict__ D,
               Tout* __restrict__ out, float* __restrict__ ddir, float* __restrict__ qrow,
               float* __restrict__ ddiag, int T, int H, int G, int nc, int heads_per_cta,
               int* status) {
@@ -347,51 +348,44 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t colY = 256 + 128 * wg, colST = colY + 64;
   unsigned char* Pw = sBP + wg * SM::kPw;
   unsigned char* sX = sXall + wg * SM::kX;
-  float* sa2 = sAall + wg * 2 * L;  // a * log2(e)
+  float* sa2 = sAall + wg * 4 * L;  // a * log2(e)
   float* sx = sa2 + L;              // fwd: a*log2e - log2(delta)  (+inf where delta = 0); rev: delta
+  float* sraw = sx + L;             // prefetched a [L], delta [L] of the next head
   const int gbar = 1 + wg;
   uint32_t n_p = 0, n_st = 0, n_done = 0;
   constexpr uint32_t id_py = idesc_bf16(128, kP, 0, 1);
   constexpr uint32_t id_st = idesc_bf16(128, kP, 0, 0);
 
-  for (int h = h_begin + wg; h < h_end; h += 2) {
-    const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
-    // second operand rows of this head (columns of the score tile)
+  // cp.async of everything a head needs: its second-operand rows (sX), its
+  // inter-chunk state image (into the P buffer) and its raw a / delta.
+  auto prefetch = [&](int hh) {
     for (int i = wtid; i < ncol * 8; i += 128) {
       const int cc = i >> 3, j = i & 7, col = col0 + cc;
       const bool v = col < Lv;
       cp_async16(sX + sw128(cc, j),
-                 v ? opsrc + (((int64_t)b * T + t0 + col) * H + h) * kP + j * 8 : opsrc, v);
+                 v ? opsrc + (((int64_t)b * T + t0 + col) * H + hh) * kP + j * 8 : opsrc, v);
     }
-    cp_async_commit();
+    const unsigned char* img = simg + ((((int64_t)b * nc + c) * H + hh) * (int64_t)SM::kImg);
+    for (int i = wtid; i < SM::kImg / 16; i += 128) cp_async16(Pw + 16 * i, img + 16 * i, true);
+    const int64_t cvh = (((int64_t)b * H + hh) * nc + c) * L;
+    for (int i = wtid; i < L / 4; i += 128) {
+      cp_async16(sraw + 4 * i, acs + cvh + 4 * i, true);
+      cp_async16(sraw + L + 4 * i, delta + cvh + 4 * i, true);
+    }
+  };
+  if (h_begin + wg < h_end) prefetch(h_begin + wg);
+  cp_async_commit();
+
+  for (int h = h_begin + wg; h < h_end; h += 2) {
+    const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
+    const float Dh = D ? D[h] : 0.f;
+    cp_async_wait<0>();
+    group_sync(gbar);  // the raw vectors were copied by other threads of the group
     for (int i = wtid; i < L; i += 128) {
-      const float a2 = acs[cv + i] * kLog2e, dl = delta[cv + i];
+      const float a2 = sraw[i] * kLog2e, dl = sraw[L + i];
       sa2[i] = a2;
       sx[i] = REV ? dl : (dl > 0.f ? a2 - lg2_approx(dl) : __int_as_float(0x7f800000));
     }
-    // the group's P buffer is free once its previous MMAs have completed
-    if (n_p > 0) mbar_wait(&bar_p[wg], (n_p - 1) & 1, status, &abort_flag);
-    {
-      // inter-chunk state (H_c / dS_c), fp32 64 x N -> hi / lo into the P buffer
-      const float* src = state + (((int64_t)b * nc + c) * H + h) * kP * N;
-      constexpr int kPer = 64 * (N / 8) / 128;
-      float4 u[kPer][2];
-#pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int i = wtid + k * 128, p = i / (N / 8), j = i % (N / 8);
-        u[k][0] = *reinterpret_cast<const float4*>(src + p * N + j * 8);
-        u[k][1] = *reinterpret_cast<const float4*>(src + p * N + j * 8 + 4);
-      }
-#pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int i = wtid + k * 128, p = i / (N / 8), j = i % (N / 8);
-        const float v[8] = {u[k][0].x, u[k][0].y, u[k][0].z, u[k][0].w,
-                            u[k][1].x, u[k][1].y, u[k][1].z, u[k][1].w};
-        const uint32_t off = (j / 8) * (64 * 128) + sw128(p, j % 8);
-        store_split8(Pw + off, Pw + SM::kHlo + off, v);
-      }
-    }
-    cp_async_wait<0>();
     fence_async_smem();
     fence_before_sync();
     group_sync(gbar);
@@ -456,30 +450,42 @@ __global__ void __launch_bounds__(256, 1)
     ++n_done;
     const bool ok = mbar_wait(&bar_done[wg], (n_done - 1) & 1, status, &abort_flag);
     fence_after_sync();
+    // this head's MMAs are done: sX and the P buffer take the next head's data
+    if (h + 2 < h_end) prefetch(h + 2);
+    cp_async_commit();
     if (ok) {
-      const float Dh = D ? D[h] : 0.f;
       const int64_t rowoff = (((int64_t)b * T + t0 + r) * H + h) * kP;
       const float ea = ex2_approx(ar2), es = ex2_approx(sa2[L - 1] - ar2);
       const float dr = REV ? sx[r] : 0.f;
       float pd = 0.f, pq = 0.f, pdd = 0.f;
+      const bool live = r < Lv;
+      uint4 orow[8], xrow[8];  // this row's second operand (x or dy) and, rev, x
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        orow[k] = live ? *reinterpret_cast<const uint4*>(opsrc + rowoff + 8 * k)
+                       : make_uint4(0, 0, 0, 0);
+        if constexpr (REV)
+          xrow[k] = live ? *reinterpret_cast<const uint4*>(x + rowoff + 8 * k)
+                         : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
       for (int c16 = 0; c16 < 4; ++c16) {
         float yv[16], st[16];
         tmem_ld16(tlane + colY + 16 * c16, yv);
         tmem_ld16(tlane + colST + 16 * c16, st);
         tmem_wait_ld();
-        if (r < Lv) {
+        if (live) {
 #pragma unroll
           for (int k8 = 0; k8 < 2; ++k8) {
             float ov[8], o[8];
-            unpack8(*reinterpret_cast<const uint4*>(sX + sw128(r - col0, 2 * c16 + k8)), ov);
+            unpack8(orow[2 * c16 + k8], ov);
             if constexpr (!REV) {
 #pragma unroll
               for (int e = 0; e < 8; ++e)
                 o[e] = yv[8 * k8 + e] + ea * st[8 * k8 + e] + Dh * ov[e];
             } else {
               float xv[8];
-              unpack8(*reinterpret_cast<const uint4*>(x + rowoff + 16 * c16 + 8 * k8), xv);
+              unpack8(xrow[2 * c16 + k8], xv);
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
                 const float us = es * st[8 * k8 + e];
@@ -504,7 +510,7 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
       if constexpr (REV) {
-        if (r < Lv) {
+        if (live) {
           ddir[cv + r] = pd;
           qrow[cv + r] = dr * pq;
           ddiag[cv + r] = pdd;
@@ -544,7 +550,7 @@ struct BcSmem {
   static constexpr int kHR = kLT * 128;
   static constexpr int kHC = L * 128;
   static constexpr int kPP = 4 * kLT * 128;  // P2 panel (2 x 64 columns, hi + lo); state operands later
-  static constexpr int kBytes = kGR + kGC + kHR + kHC + kPP + (2 * L + 4 * 128) * 4 + 1024;
+  static constexpr int kBytes = kGR + kGC + kHR + kHC + kPP + (4 * L + 4 * 128) * 4 + 1024;
 };
 
 template <int N, int L, bool REV>
@@ -552,7 +558,7 @@ __global__ void __launch_bounds__(256, 1)
     k_bwd_bc_tc(const bf16* __restrict__ x, const bf16* __restrict__ Bm,
                 const bf16* __restrict__ Cm, const bf16* __restrict__ dy,
                 const float* __restrict__ delta, const float* __restrict__ acs,
-                const float* __restrict__ state, float* __restrict__ out,
+                const unsigned char* __restrict__ simg, float* __restrict__ out,
                 float* __restrict__ msum, float* __restrict__ ycs, int T, int H, int G, int nc,
                 int hb, int* status) {
   using SM = BcSmem<N, L>;
@@ -571,6 +577,7 @@ __global__ void __launch_bounds__(256, 1)
   float* sa2 = reinterpret_cast<float*>(sP + SM::kPP);  // a * log2(e)
   float* sx = sa2 + L;   // dC: a*log2e - log2(delta) (+inf at delta = 0); dB: log2(delta) (-inf)
   float* sred = sx + L;  // [4][128]
+  float* sraw = sred + 4 * 128;  // prefetched a [L], delta [L] of the next head
 
   const int c = blockIdx.x / NLT, tile = blockIdx.x % NLT, b = blockIdx.y;
   const int nblk = gridDim.z / G, g = blockIdx.z / nblk, kb = blockIdx.z % nblk;
@@ -603,6 +610,11 @@ __global__ void __launch_bounds__(256, 1)
     stage_rows_async(sHC, ncol, 8, 0, Lv - col0, hcol, [&](int cc) {
       return hcol + (((int64_t)b * T + t0 + col0 + cc) * H + hh) * kP;
     });
+    const int64_t cvh = (((int64_t)b * H + hh) * nc + c) * L;
+    for (int i = tid; i < L / 4; i += 256) {
+      cp_async16(sraw + 4 * i, acs + cvh + 4 * i, true);
+      cp_async16(sraw + L + 4 * i, delta + cvh + 4 * i, true);
+    }
   };
   stage_hc(h_begin);
   cp_async_commit();
@@ -625,18 +637,19 @@ __global__ void __launch_bounds__(256, 1)
 
   for (int h = h_begin; h < h_end; ++h) {
     const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
-    for (int i = tid; i < L; i += 256) {
-      const float a2 = acs[cv + i] * kLog2e, dl = delta[cv + i];
-      const float l2 = dl > 0.f ? lg2_approx(dl) : -__int_as_float(0x7f800000);
-      sa2[i] = a2;
-      sx[i] = REV ? l2 : a2 - l2;
-    }
-    // this head's row operand; its column operand was prefetched
+    // this head's row operand; its column operand and a / delta were prefetched
     stage_rows_async(sHR, LT, 8, 0, Lv - r0, hrow, [&](int r2) {
       return hrow + (((int64_t)b * T + t0 + r0 + r2) * H + h) * kP;
     });
     cp_async_commit();
     cp_async_wait<0>();
+    __syncthreads();  // raw vectors copied by other threads
+    for (int i = tid; i < L; i += 256) {
+      const float a2 = sraw[i] * kLog2e, dl = sraw[L + i];
+      const float l2 = dl > 0.f ? lg2_approx(dl) : -__int_as_float(0x7f800000);
+      sa2[i] = a2;
+      sx[i] = REV ? l2 : a2 - l2;
+    }
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -713,6 +726,12 @@ __global__ void __launch_bounds__(256, 1)
     }
     // state term of this head; the column operand is free: fetch the next head's
     mbar_wait(&bar_acc, (n_acc - 1) & 1, status, &abort_flag);
+    {
+      // the head's state image (hi / lo panels) into the free P buffer
+      const unsigned char* img = simg + ((((int64_t)b * nc + c) * H + h) * (int64_t)(2 * NKP * 8192));
+      for (int i = tid; i < 2 * NKP * 8192 / 16; i += 256) cp_async16(sBh + 16 * i, img + 16 * i, true);
+      cp_async_commit();
+    }
     if (h + 1 < h_end) stage_hc(h + 1);
     cp_async_commit();
     for (int i = tid; i < LT * 8; i += 256) {
@@ -724,7 +743,7 @@ __global__ void __launch_bounds__(256, 1)
       for (int e = 0; e < 8; ++e) v[e] *= sc;
       store_split8(sAh + sw128(r2, j), sAl + sw128(r2, j), v);
     }
-    stage_state_split<N>(sBh, sBl, state + (((int64_t)b * nc + c) * H + h) * kP * N);
+    cp_async_wait<1>();  // the state image (the next head's prefetch may still fly)
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -944,7 +963,8 @@ cudaError_t launch_tc_forward_t(const Dims& d, const FwdArgs& a, const FwdWs& w,
     SSD_LAUNCH("k_scan_tc", s,
                kern<<<grid, 256, SM::kBytes, s>>>(
                    static_cast<const bf16*>(a.x), static_cast<const bf16*>(a.B),
-                   static_cast<const bf16*>(a.C), nullptr, w.delta, w.acs, w.Hprev, a.D,
+                   static_cast<const bf16*>(a.C), nullptr, w.delta, w.acs,
+                   static_cast<const unsigned char*>(w.Himg), a.D,
                    static_cast<Tout*>(a.y), nullptr, nullptr, nullptr, d.T, d.H, d.G, d.nc, hpc,
                    status));
   }
@@ -967,7 +987,7 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
   const bf16* dy = static_cast<const bf16*>(a.dy);
   FwdArgs f = a.f;
   f.final_state = nullptr;
-  FwdWs fw{w.delta, w.acs, w.S, w.Hprev, nullptr};
+  FwdWs fw{w.delta, w.acs, w.S, nullptr, nullptr, w.Himg};
   simt_cumsum(d, f, fw, s);
   using SS = StateSmem<N, L>;
   const int ppc = pick_heads_per_cta((d.H / d.G) / 2, d.B * d.nc * d.G, sms, 4);
@@ -985,8 +1005,8 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     SSD_LAUNCH("k_dstates_tc", s, kern<<<sgrid, 256, SS::kBytes, s>>>(
         dy, Cm, w.delta, w.acs, w.dHs, d.T, d.H, d.G, d.nc, ppc, status));
   }
-  const int nsplit = simt_state_passing_bwd(d, w.dHs, w.acs, w.Hprev, a.dfinal, w.dS, w.dlast,
-                                            a.dinit, s);
+  const int nsplit = simt_state_passing_bwd(d, w.dHs, w.acs, nullptr, a.dfinal, nullptr, w.dlast,
+                                            a.dinit, w.dSimg, w.Himg, s);
   {
     using SM = ScanSmem<N, L>;
     auto kern = k_scan_tc<N, L, float, true>;
@@ -994,7 +1014,8 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     const int hpc = pick_heads_even(d.H / d.G, d.B * d.nc * (L / 128) * d.G, sms, 4);
     const dim3 grid(d.nc * (L / 128), d.B, (d.H + hpc - 1) / hpc);
     SSD_LAUNCH("k_scan_tc_dx", s, kern<<<grid, 256, SM::kBytes, s>>>(
-        x, Bm, Cm, dy, w.delta, w.acs, w.dS, a.f.D, a.dx, w.ddir, w.qrow, w.ddiag, d.T, d.H,
+        x, Bm, Cm, dy, w.delta, w.acs, static_cast<const unsigned char*>(w.dSimg), a.f.D, a.dx,
+        w.ddir, w.qrow, w.ddiag, d.T, d.H,
         d.G, d.nc, hpc, status));
   }
   const int nblk = tc_bwd_nblk(d), hb = (d.H / d.G) / nblk;
@@ -1006,7 +1027,8 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     auto kern = k_bwd_bc_tc<N, L, false>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
     SSD_LAUNCH("k_bwd_dc_tc", s, kern<<<bgrid, 256, SM::kBytes, s>>>(
-        x, Bm, Cm, dy, w.delta, w.acs, w.Hprev, dCout, w.rowsum, w.ycs, d.T, d.H, d.G, d.nc, hb,
+        x, Bm, Cm, dy, w.delta, w.acs, static_cast<const unsigned char*>(w.Himg), dCout,
+        w.rowsum, w.ycs, d.T, d.H, d.G, d.nc, hb,
         status));
   }
   {
@@ -1014,7 +1036,8 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     auto kern = k_bwd_bc_tc<N, L, true>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
     SSD_LAUNCH("k_bwd_db_tc", s, kern<<<bgrid, 256, SM::kBytes, s>>>(
-        x, Bm, Cm, dy, w.delta, w.acs, w.dS, dBout, w.colsum, nullptr, d.T, d.H, d.G, d.nc, hb,
+        x, Bm, Cm, dy, w.delta, w.acs, static_cast<const unsigned char*>(w.dSimg), dBout,
+        w.colsum, nullptr, d.T, d.H, d.G, d.nc, hb,
         status));
   }
   SSD_LAUNCH("k_bwd_finalize_tc", s, k_bwd_finalize_tc<<<dim3(d.nc, d.H, d.B), 256, 0, s>>>(
