@@ -123,7 +123,7 @@ TcBwdOffsets tc_bwd_offsets(const Dims& d) {
   o.Himg = c.take(st);
   o.dHs = c.take(st);
   o.dSimg = c.take(st);
-  o.dlast = c.take((size_t)d.B * d.H * d.nc * 16 * sizeof(float));
+  o.dlast = c.take((size_t)d.B * d.H * d.nc * 64 * sizeof(float));  // <= 64 partials each
   o.rowsum = c.take(vec);
   o.colsum = c.take(vec);
   o.ycs = c.take(vec);

@@ -385,7 +385,6 @@ __global__ void __launch_bounds__(kThreads)
                             const float4* __restrict__ dfinal, unsigned char* __restrict__ dsimg,
                             float* __restrict__ dlast_part, float4* __restrict__ dinit, int N,
                             int H, int PN8, int L, int nc) {
-  __shared__ float red[kThreads / 32];
   const int split = blockIdx.x, nsplit = gridDim.x, h = blockIdx.y, b = blockIdx.z;
   const int e = split * kThreads + threadIdx.x;
   const bool live = e < PN8;
@@ -426,9 +425,12 @@ __global__ void __launch_bounds__(kThreads)
         g0 = fma4(dec[k], g0, d0[k]);
         g1 = fma4(dec[k], g1, d1[k]);
       }
-      const float tot = block_sum(part, red);
-      if (threadIdx.x == 0)
-        dlast_part[(((int64_t)b * H + h) * nc + c) * nsplit + split] = dec[k] * tot;
+      // one partial per warp (fixed-order sums later, no block barrier here)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      if ((threadIdx.x & 31) == 0)
+        dlast_part[((((int64_t)b * H + h) * nc + c) * nsplit + split) * (kThreads / 32) +
+                   (threadIdx.x >> 5)] = dec[k] * part;
     }
   }
   if (live && dinit) {
@@ -997,7 +999,7 @@ int launch_state_passing_bwd(const Dims& d, const BwdArgs& a, const BwdWs& w, cu
         static_cast<const unsigned char*>(w.f.Himg), reinterpret_cast<const float4*>(a.dfinal),
         static_cast<unsigned char*>(w.dSimg), w.dlast, reinterpret_cast<float4*>(a.dinit), d.N,
         d.H, PN8, d.L, d.nc));
-    return nsplit;
+    return nsplit * (kThreads / 32);  // one partial per warp
   }
   if (PN % 4 == 0 && vec4_ok(a.dfinal) && vec4_ok(a.dinit)) {
     const int PN4 = PN / 4, nsplit = (PN4 + kThreads - 1) / kThreads;

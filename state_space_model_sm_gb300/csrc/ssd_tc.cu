@@ -145,6 +145,22 @@ __global__ void __launch_bounds__(256, 2)
   constexpr uint32_t idesc = idesc_bf16(128, N, 1, 1);
   uint32_t n_stage0 = 0, n_stage1 = 0, n_done = 0;
 
+  // X rows (both heads of a pair, 256 contiguous bytes per row) of a 64-row
+  // block go through registers; the next block's rows are loaded while the
+  // current block is scaled, split and multiplied.
+  constexpr int kPer = KB * 16 / 256;
+  auto load_block = [&](uint4 (&u)[kPer], int hp, int l0) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = tid + k * 256, l = l0 + (i >> 4), j = i & 15;
+      u[k] = l < Lv ? *reinterpret_cast<const uint4*>(x + (((int64_t)b * T + t0 + l) * H + hp) *
+                                                              kP + j * 8)
+                    : make_uint4(0, 0, 0, 0);
+    }
+  };
+  uint4 u[kPer], un[kPer];
+  if (npairs > 0) load_block(u, 2 * pair0, 0);
+
   for (int ip = 0; ip < npairs; ++ip) {
     const int h = 2 * (pair0 + ip);
     for (int i = tid; i < 2 * L; i += 256) {
@@ -159,6 +175,9 @@ __global__ void __launch_bounds__(256, 2)
       unsigned char* sXh = sB + SM::kB;
       unsigned char* sXl = sXh + SM::kX;
       const int l0 = kb * KB;
+      // next block's X rows (or the next pair's first block) start loading now
+      if (kb + 1 < NKB) load_block(un, h, l0 + KB);
+      else if (ip + 1 < npairs) load_block(un, h + 2, 0);
       // the stage is free once the MMAs that read it (two blocks ago) are done
       const uint32_t ns = st ? n_stage1 : n_stage0;
       if (ns > 0) mbar_wait(&bar_stage[st], (ns - 1) & 1, status, &abort_flag);
@@ -166,16 +185,6 @@ __global__ void __launch_bounds__(256, 2)
         return Bm + (((int64_t)b * T + t0 + l0 + l) * G + g) * N;
       });
       cp_async_commit();
-      // X rows of both heads (256 contiguous bytes per row): loads first
-      constexpr int kPer = KB * 16 / 256;
-      uint4 u[kPer];
-#pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int i = tid + k * 256, l = l0 + (i >> 4), j = i & 15;
-        u[k] = l < Lv ? *reinterpret_cast<const uint4*>(x + (((int64_t)b * T + t0 + l) * H + h) *
-                                                                kP + j * 8)
-                      : make_uint4(0, 0, 0, 0);
-      }
       if (kb == 0) __syncthreads();  // sw ready
 #pragma unroll
       for (int k = 0; k < kPer; ++k) {
@@ -188,6 +197,8 @@ __global__ void __launch_bounds__(256, 2)
         const uint32_t off = hh * SM::kPanel + sw128(lr, j & 7);
         store_split8(sXh + off, sXl + off, v);
       }
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) u[k] = un[k];
       cp_async_wait<0>();
       fence_async_smem();
       fence_before_sync();
@@ -408,15 +419,19 @@ __global__ void __launch_bounds__(256, 1)
     for (int j = 0; j < nsp; ++j) {
       if (j > 0) mbar_wait(&bar_p[wg], (n_p - 1) & 1, status, &abort_flag);
       const float* colv = (REV ? sa2 : sx) + col0 + 64 * j;  // per-column log2 terms
+      // 16-column groups; the TMEM load of group q+1 is in flight while group q
+      // is formed (wait::ld covers every earlier load, so it is issued first)
+      float cbA[16], cbB[16];
+      tmem_ld16(tlane + 64 * j, cbA);
+      tmem_wait_ld();
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float cb[32];
-        tmem_ld16(tlane + 64 * j + 32 * hf, *reinterpret_cast<float(*)[16]>(cb));
-        tmem_ld16(tlane + 64 * j + 32 * hf + 16, *reinterpret_cast<float(*)[16]>(cb + 16));
-        tmem_wait_ld();
+      for (int q = 0; q < 4; ++q) {
+        float(&cur)[16] = (q & 1) ? cbB : cbA;
+        float(&nxt)[16] = (q & 1) ? cbA : cbB;
+        if (q < 3) tmem_ld16(tlane + 64 * j + 16 * (q + 1), nxt);
 #pragma unroll
-        for (int k8 = 0; k8 < 4; ++k8) {
-          const int c8 = 32 * hf + 8 * k8;  // panel-local column of the chunk
+        for (int k8 = 0; k8 < 2; ++k8) {
+          const int c8 = 16 * q + 8 * k8;  // panel-local column of the chunk
           const float4 w0 = *reinterpret_cast<const float4*>(colv + c8);
           const float4 w1 = *reinterpret_cast<const float4*>(colv + c8 + 4);
           const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -425,11 +440,12 @@ __global__ void __launch_bounds__(256, 1)
           for (int e = 0; e < 8; ++e) {
             const int cl = col0 + 64 * j + c8 + e;  // chunk-local column
             const float f = REV ? ex2_approx(wv[e] - ar2) : ex2_approx(ar2 - wv[e]);
-            v[e] = (REV ? cl >= r : cl <= r) ? cb[8 * k8 + e] * f : 0.f;
+            v[e] = (REV ? cl >= r : cl <= r) ? cur[8 * k8 + e] * f : 0.f;
           }
           const uint32_t off = sw128(rr, c8 / 8);
           store_split8(Pw + off, Pw + LT * 128 + off, v);
         }
+        if (q < 3) tmem_wait_ld();
       }
       fence_async_smem();
       fence_before_sync();
@@ -675,17 +691,24 @@ __global__ void __launch_bounds__(256, 1)
       mbar_wait(&bar_s, (n_s - 1) & 1, status, &abort_flag);
       if (n_acc > 0) mbar_wait(&bar_acc, (n_acc - 1) & 1, status, &abort_flag);
       fence_after_sync();
+      // 16-column groups of S0 and S1; group q+1's TMEM loads fly while q is formed
+      float a0[16], a1[16], b0[16], b1[16];
+      tmem_ld16(tlane + kColS0 + 64 * half, a0);
+      tmem_ld16(tlane + kColS1 + 64 * half, a1);
+      tmem_wait_ld();
 #pragma unroll
-      for (int g32 = 0; g32 < 2; ++g32) {
-        float s0[32], s1[32];
-        const uint32_t cb = 64 * half + 32 * g32;
-        tmem_ld16(tlane + kColS0 + cb, *reinterpret_cast<float(*)[16]>(s0));
-        tmem_ld16(tlane + kColS0 + cb + 16, *reinterpret_cast<float(*)[16]>(s0 + 16));
-        tmem_ld16(tlane + kColS1 + cb, *reinterpret_cast<float(*)[16]>(s1));
-        tmem_ld16(tlane + kColS1 + cb + 16, *reinterpret_cast<float(*)[16]>(s1 + 16));
-        tmem_wait_ld();
+      for (int qg = 0; qg < 4; ++qg) {
+        float(&s0)[16] = (qg & 1) ? b0 : a0;
+        float(&s1)[16] = (qg & 1) ? b1 : a1;
+        float(&n0)[16] = (qg & 1) ? a0 : b0;
+        float(&n1)[16] = (qg & 1) ? a1 : b1;
+        const uint32_t cb = 64 * half + 16 * qg;
+        if (qg < 3) {
+          tmem_ld16(tlane + kColS0 + cb + 16, n0);
+          tmem_ld16(tlane + kColS1 + cb + 16, n1);
+        }
 #pragma unroll
-        for (int k8 = 0; k8 < 4; ++k8) {
+        for (int k8 = 0; k8 < 2; ++k8) {
           const float* colv = (REV ? sa2 : sx) + col0 + 128 * k + cb + 8 * k8;
           const float4 w0 = *reinterpret_cast<const float4*>(colv);
           const float4 w1 = *reinterpret_cast<const float4*>(colv + 4);
@@ -701,9 +724,10 @@ __global__ void __launch_bounds__(256, 1)
             if (strict) mpart = fmaf(s0[8 * k8 + e], p2, mpart);
             v[e] = p2;
           }
-          const uint32_t off = half * (LT * 128) + sw128(rr, 4 * g32 + k8);
+          const uint32_t off = half * (LT * 128) + sw128(rr, (16 * qg + 8 * k8) / 8);
           store_split8(sP + off, sP + 2 * LT * 128 + off, v);
         }
+        if (qg < 3) tmem_wait_ld();
       }
       fence_async_smem();
       fence_before_sync();
