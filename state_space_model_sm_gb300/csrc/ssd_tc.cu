@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(256, 1)
               const float* __restrict__ delta, const float* __restrict__ acs,
               const unsigned char* __restrict__ simg, const float* __restrict__ D,
               Tout* __restrict__ out, float* __restrict__ ddir, float* __restrict__ qrow,
-              float* __restrict__ ddiag, int T, int H, int G, int nc, int heads_per_cta,
+              float* __restrict__ ddiag, int B_, int T, int H, int G, int nc, int items_per_cta,
               int* status) {
   using SM = ScanSmem<N, L>;
   constexpr int LT = SM::kLT, NLT = L / LT;
@@ -299,18 +299,11 @@ __global__ void __launch_bounds__(256, 1)
   unsigned char* sXall = sBP + SM::kBP;   // per group: x (fwd) or dy (rev) rows
   float* sAall = reinterpret_cast<float*>(sXall + 2 * SM::kX);  // per group: a [L], delta [L]
 
-  const int c = blockIdx.x / NLT, tile = blockIdx.x % NLT, b = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hpg = H / G;
-  const int h_begin = blockIdx.z * heads_per_cta;
-  const int h_end = min(H, h_begin + heads_per_cta);
-  const int g = h_begin / hpg;
-  const int r0 = tile * LT;                       // first row (chunk-local)
-  const int col0 = REV ? r0 : 0;                  // first column
-  const int ncol = REV ? L - r0 : r0 + LT;        // number of columns
-  const int nsp = ncol / 64;
-  const int64_t t0 = (int64_t)c * L;
-  const int Lv = min(L, T - (int)t0);
+  const int64_t n_items = (int64_t)B_ * nc * NLT * H;  // (batch, chunk, tile, group) x head
+  const int64_t it_begin = (int64_t)blockIdx.x * items_per_cta;
+  const int64_t it_end = min(n_items, it_begin + items_per_cta);
   const bf16* rowsrc = REV ? Bm : Cm;
   const bf16* colsrc = REV ? Cm : Bm;
   const bf16* opsrc = REV ? dy : x;
@@ -326,44 +319,70 @@ __global__ void __launch_bounds__(256, 1)
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&tmem_base, 512);
-  stage_rows_async(sR, LT, N / 8, LT * 128, Lv - r0, rowsrc, [&](int rr2) {
-    return rowsrc + (((int64_t)b * T + t0 + r0 + rr2) * G + g) * N;
-  });
-  stage_rows_async(sBP, ncol, N / 8, L * 128, Lv - col0, colsrc, [&](int cc) {
-    return colsrc + (((int64_t)b * T + t0 + col0 + cc) * G + g) * N;
-  });
-  cp_async_commit();
-  cp_async_wait<0>();
-  fence_async_smem();
+  // TMEM and the per-group state live across the CTA's whole item range
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tm = tmem_base;
-  if (tid == 0) {
-    const uint32_t id = idesc_bf16(128, ncol, 0, 0);
-    for (int ks = 0; ks < N / 16; ++ks) {
-      const uint32_t kp = ks / 4, ko = (ks % 4) * 32;
-      mma_bf16(tm, sdesc(smem_u32(sR) + kp * (LT * 128) + ko, 16, 1024),
-               sdesc(smem_u32(sBP) + kp * (L * 128) + ko, 16, 1024), id, ks > 0 ? 1u : 0u);
-    }
-    mma_commit(&bar_cb);
-  }
-  mbar_wait(&bar_cb, 0, status, &abort_flag);
-  fence_after_sync();
-  // sBP (the column operand) is free from here on: it becomes the P buffers.
-  __syncthreads();
-
   const int wg = tid >> 7, wtid = tid & 127, q = warp & 3;
-  const int rr = 32 * q + lane, r = r0 + rr;  // this thread's row (TMEM lane)
+  const int rr = 32 * q + lane;
   const uint32_t tlane = tm + ((uint32_t)(32 * q) << 16);
   const uint32_t colY = 256 + 128 * wg, colST = colY + 64;
+  const int gbar = 1 + wg;
+  uint32_t n_p = 0, n_st = 0, n_done = 0, n_units = 0;
+
+  for (int64_t item = it_begin; item < it_end;) {
+    // one unit = (batch, chunk, row tile, group); this CTA's heads of it
+    const int64_t unit = item / hpg;
+    const int j0 = (int)(item % hpg);
+    const int j1 = (int)min((int64_t)hpg, j0 + (it_end - item));
+    item += j1 - j0;
+    const int g = (int)(unit % G);
+    const int64_t bct = unit / G;
+    const int tile = (int)(bct % NLT);
+    const int64_t bc = bct / NLT;
+    const int c = (int)(bc % nc), b = (int)(bc / nc);
+    const int h_begin = g * hpg + j0, h_end = g * hpg + j1;
+    const int r0 = tile * LT;                       // first row (chunk-local)
+    const int col0 = REV ? r0 : 0;                  // first column
+    const int ncol = REV ? L - r0 : r0 + LT;        // number of columns
+    const int nsp = ncol / 64;
+    const int64_t t0 = (int64_t)c * L;
+    const int Lv = min(L, T - (int)t0);
+    const int r = r0 + rr;                          // this thread's row (TMEM lane)
+
+  stage_rows_async(sR, LT, N / 8, LT * 128, Lv - r0, rowsrc, [&](int rr2) {
+      return rowsrc + (((int64_t)b * T + t0 + r0 + rr2) * G + g) * N;
+    });
+    stage_rows_async(sBP, ncol, N / 8, L * 128, Lv - col0, colsrc, [&](int cc) {
+      return colsrc + (((int64_t)b * T + t0 + col0 + cc) * G + g) * N;
+    });
+    cp_async_commit();
+    cp_async_wait<0>();
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      const uint32_t id = idesc_bf16(128, ncol, 0, 0);
+      for (int ks = 0; ks < N / 16; ++ks) {
+        const uint32_t kp = ks / 4, ko = (ks % 4) * 32;
+        mma_bf16(tm, sdesc(smem_u32(sR) + kp * (LT * 128) + ko, 16, 1024),
+                 sdesc(smem_u32(sBP) + kp * (L * 128) + ko, 16, 1024), id, ks > 0 ? 1u : 0u);
+      }
+      mma_commit(&bar_cb);
+    }
+    mbar_wait(&bar_cb, n_units & 1, status, &abort_flag);
+    ++n_units;
+    fence_after_sync();
+    // sBP (the column operand) is free from here on: it becomes the P buffers.
+    __syncthreads();
+
   unsigned char* Pw = sBP + wg * SM::kPw;
   unsigned char* sX = sXall + wg * SM::kX;
   float* sa2 = sAall + wg * 4 * L;  // a * log2(e)
   float* sx = sa2 + L;              // fwd: a*log2e - log2(delta)  (+inf where delta = 0); rev: delta
   float* sraw = sx + L;             // prefetched a [L], delta [L] of the next head
-  const int gbar = 1 + wg;
-  uint32_t n_p = 0, n_st = 0, n_done = 0;
   constexpr uint32_t id_py = idesc_bf16(128, kP, 0, 1);
   constexpr uint32_t id_st = idesc_bf16(128, kP, 0, 0);
 
@@ -535,6 +554,10 @@ __global__ void __launch_bounds__(256, 1)
     }
     fence_before_sync();
     group_sync(gbar);  // sX, sa, sd and the accumulators are reused by the next head
+  }
+    // both groups are done with this unit's C.B^T tile and buffers
+    fence_before_sync();
+    __syncthreads();
   }
   fence_before_sync();
   __syncthreads();
@@ -943,14 +966,14 @@ __global__ void k_block_reduce(const float4* __restrict__ in, float4* __restrict
 }
 
 // ------------------------------------------------------------------ launch
-// Heads per CTA for the two-pipeline scan kernels: an even divisor of hpg
-// (both warpgroups busy) giving >= target_waves * sms CTAs, else the generic rule.
-int pick_heads_even(int hpg, int units, int sms, int target_waves) {
-  int best = 0;
-  for (int d = 2; d <= hpg; d += 2)
-    if (hpg % d == 0 && (int64_t)units * (hpg / d) >= (int64_t)target_waves * sms) best = d;
-  if (best == 0) best = hpg % 2 == 0 ? 2 : 1;
-  return best;
+// Persistent scan kernels: one CTA per SM, each taking a contiguous range of
+// the (batch, chunk, row tile, group) x head items, so every SM gets the same
+// number of heads (+-1) whatever the shape.
+void scan_partition(const Dims& d, int sms, int* grid, int* per) {
+  const int64_t items = (int64_t)d.B * d.nc * (d.L / 128) * d.H;
+  const int64_t g = items < sms ? items : sms;
+  *per = (int)((items + g - 1) / g);
+  *grid = (int)((items + *per - 1) / *per);
 }
 
 int pick_heads_per_cta(int hpg, int units, int sms, int target_waves) {
@@ -982,15 +1005,15 @@ cudaError_t launch_tc_forward_t(const Dims& d, const FwdArgs& a, const FwdWs& w,
     using SM = ScanSmem<N, L>;
     auto kern = k_scan_tc<N, L, Tout, false>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
-    const int hpc = pick_heads_even(d.H / d.G, d.B * d.nc * (L / 128) * d.G, sms, 4);
-    const dim3 grid(d.nc * (L / 128), d.B, (d.H + hpc - 1) / hpc);
+    int grid, per;
+    scan_partition(d, sms, &grid, &per);
     SSD_LAUNCH("k_scan_tc", s,
                kern<<<grid, 256, SM::kBytes, s>>>(
                    static_cast<const bf16*>(a.x), static_cast<const bf16*>(a.B),
                    static_cast<const bf16*>(a.C), nullptr, w.delta, w.acs,
                    static_cast<const unsigned char*>(w.Himg), a.D,
-                   static_cast<Tout*>(a.y), nullptr, nullptr, nullptr, d.T, d.H, d.G, d.nc, hpc,
-                   status));
+                   static_cast<Tout*>(a.y), nullptr, nullptr, nullptr, d.B, d.T, d.H, d.G, d.nc,
+                   per, status));
   }
   return cudaGetLastError();
 }
@@ -1035,12 +1058,11 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     using SM = ScanSmem<N, L>;
     auto kern = k_scan_tc<N, L, float, true>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
-    const int hpc = pick_heads_even(d.H / d.G, d.B * d.nc * (L / 128) * d.G, sms, 4);
-    const dim3 grid(d.nc * (L / 128), d.B, (d.H + hpc - 1) / hpc);
+    int grid, per;
+    scan_partition(d, sms, &grid, &per);
     SSD_LAUNCH("k_scan_tc_dx", s, kern<<<grid, 256, SM::kBytes, s>>>(
         x, Bm, Cm, dy, w.delta, w.acs, static_cast<const unsigned char*>(w.dSimg), a.f.D, a.dx,
-        w.ddir, w.qrow, w.ddiag, d.T, d.H,
-        d.G, d.nc, hpc, status));
+        w.ddir, w.qrow, w.ddiag, d.B, d.T, d.H, d.G, d.nc, per, status));
   }
   const int nblk = tc_bwd_nblk(d), hb = (d.H / d.G) / nblk;
   const dim3 bgrid(d.nc * (L / 128), d.B, d.G * nblk);
