@@ -161,6 +161,13 @@ size_t ssd_noalloc_scratch_bytes(void);
 int ssd_selftest_mma(int a_mn, int b_mn, int swap_mn_offsets, int nn, int k, const void* A,
                      const void* B, float* D, void* stream);
 
+/* Diagnostic: launches one kernel whose only work is a wait on a barrier
+ * that nothing completes.  The library's bounded wait gives up after about one
+ * second, records SSD_ERR_TIMEOUT in the device status word and the kernel
+ * returns; the CUDA context stays usable.  Lets callers check their handling
+ * of ssd_get_device_status() without any GPU fault.  Asynchronous. */
+int ssd_selftest_timeout(void* stream);
+
 /* Static description of a status code. */
 const char* ssd_strerror(int status);
 

@@ -129,3 +129,32 @@ extern "C" int ssd_selftest_mma(int a_mn, int b_mn, int swap_mn_offsets, int nn,
                  nn, k, a_mn, b_mn, swap_mn_offsets, status));
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
+
+namespace ssd {
+namespace {
+
+// One warp waits on an mbarrier that no one arrives on.  The wait is the
+// library's bounded wait: after its time limit it records SSD_ERR_TIMEOUT in
+// the status word and the kernel returns normally.
+__global__ void k_selftest_timeout(int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait(&bar, 0, status, &abort_flag);
+}
+
+}  // namespace
+}  // namespace ssd
+
+extern "C" int ssd_selftest_timeout(void* stream) {
+  int* status = ssd::device_status_ptr();
+  if (!status) return SSD_ERR_CUDA;
+  SSD_LAUNCH("k_selftest_timeout", static_cast<cudaStream_t>(stream),
+             ssd::k_selftest_timeout<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status));
+  return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}

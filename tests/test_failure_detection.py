@@ -1,0 +1,33 @@
+"""Failure detection without a GPU fault: a bounded device-side wait that
+nothing completes must expire, record SSD_ERR_TIMEOUT in the status word and
+leave the context usable for the next call."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+from parity_util import assert_close, to_np
+from state_space_model_sm_gb300 import _native
+from state_space_model_sm_gb300.inputs import SSDShape, make_inputs, to_torch
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(cuda_lib):
+    import torch
+    lib = _native.load()
+    assert cuda_lib.device_status() == 0
+    stream = torch.cuda.current_stream().cuda_stream
+    assert lib.ssd_selftest_timeout(ctypes.c_void_p(stream)) == 0
+    assert cuda_lib.device_status() == 5           # SSD_ERR_TIMEOUT, read and cleared
+    assert cuda_lib.device_status() == 0
+    # the context still runs kernels correctly
+    inp = make_inputs(SSDShape(1, 300, 4, 64, 128, 1, 256), seed=8, dtype="bf16")
+    t = to_torch(inp)
+    y, _ = cuda_lib.ssd_fwd(t["x"], t["dt"], t["dt_bias"], t["A"], t["B"], t["C"], t["D"],
+                            chunk_size=256)
+    torch.cuda.synchronize()
+    y_ref, _ = oracle.ssd_fwd(*oracle.from_inputs(inp))
+    assert_close("y", to_np(y), y_ref, "bf16")
+    assert cuda_lib.device_status() == 0
