@@ -53,34 +53,10 @@ template <class RowPtr>
 __device__ __forceinline__ void stage_rows_async(unsigned char* dst, int rows, int nchunk,
                                                  uint32_t panel, int valid, const bf16* safe,
                                                  RowPtr rowptr) {
-  for (int i = threadIdx.x; i < rows * nchunk; i += 256) {
+  for (int i = threadIdx.x; i < rows * nchunk; i += blockDim.x) {
     const int r = i / nchunk, j = i % nchunk;
     const bool v = r < valid;
     cp_async16(dst + (j / 8) * panel + sw128(r, j % 8), v ? rowptr(r) + j * 8 : safe, v);
-  }
-}
-
-// A 64 x N fp32 state block (row-major, rows p) as hi / lo bf16 panels of 64
-// columns (chunk j of row p -> (j/8)*8 KB + sw128(p, j%8)); all global loads
-// of a thread are issued before any conversion.
-template <int N>
-__device__ __forceinline__ void stage_state_split(unsigned char* hi, unsigned char* lo,
-                                                  const float* __restrict__ src) {
-  constexpr int kPer = 64 * (N / 8) / 256;
-  float4 u[kPer][2];
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int i = threadIdx.x + k * 256, p = i / (N / 8), j = i % (N / 8);
-    u[k][0] = *reinterpret_cast<const float4*>(src + p * N + j * 8);
-    u[k][1] = *reinterpret_cast<const float4*>(src + p * N + j * 8 + 4);
-  }
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int i = threadIdx.x + k * 256, p = i / (N / 8), j = i % (N / 8);
-    const float v[8] = {u[k][0].x, u[k][0].y, u[k][0].z, u[k][0].w,
-                        u[k][1].x, u[k][1].y, u[k][1].z, u[k][1].w};
-    const uint32_t off = (j / 8) * (64 * 128) + sw128(p, j % 8);
-    store_split8(hi + off, lo + off, v);
   }
 }
 
@@ -271,15 +247,15 @@ struct ScanSmem {
   static constexpr int kX = L * 128;                        // per group: x or dy rows
   static constexpr int kHlo = (N / 64) * 64 * 128;          // offset of the state's lo part
   static constexpr int kImg = 2 * kHlo;                     // bytes of one state image
-  static constexpr int kBytes = kC + kBP + 2 * kX + 8 * L * 4 + 1024;
+  static constexpr int kBytes = kC + kBP + 2 * kX + (8 * L + 6 * 128) * 4 + 1024;
 };
 
 __device__ __forceinline__ void group_sync(int id) {
-  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
+  asm volatile("bar.sync %0, 256;" ::"r"(id) : "memory");
 }
 
 template <int N, int L, typename Tout, bool REV>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(512, 1)
     k_scan_tc(const bf16* __restrict__ x, const bf16* __restrict__ Bm,
               const bf16* __restrict__ Cm, const bf16* __restrict__ dy,
               const float* __restrict__ delta, const float* __restrict__ acs,
@@ -324,11 +300,14 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   fence_after_sync();
   const uint32_t tm = tmem_base;
-  const int wg = tid >> 7, wtid = tid & 127, q = warp & 3;
+  // two pipelines of 8 warps; a TMEM row is shared by the warps q and q + 4
+  // of a pipeline, each taking 32 of a panel's 64 columns
+  const int wg = tid >> 8, wtid = tid & 255, wq = wtid >> 5, q = wq & 3, half = wq >> 2;
   const int rr = 32 * q + lane;
   const uint32_t tlane = tm + ((uint32_t)(32 * q) << 16);
   const uint32_t colY = 256 + 128 * wg, colST = colY + 64;
   const int gbar = 1 + wg;
+  float* sred = sAall + 8 * L + wg * 3 * 128;  // [3][128] per pipeline: half-row partial sums
   uint32_t n_p = 0, n_st = 0, n_done = 0, n_units = 0;
 
   for (int64_t item = it_begin; item < it_end;) {
@@ -389,16 +368,16 @@ __global__ void __launch_bounds__(256, 1)
   // cp.async of everything a head needs: its second-operand rows (sX), its
   // inter-chunk state image (into the P buffer) and its raw a / delta.
   auto prefetch = [&](int hh) {
-    for (int i = wtid; i < ncol * 8; i += 128) {
+    for (int i = wtid; i < ncol * 8; i += 256) {
       const int cc = i >> 3, j = i & 7, col = col0 + cc;
       const bool v = col < Lv;
       cp_async16(sX + sw128(cc, j),
                  v ? opsrc + (((int64_t)b * T + t0 + col) * H + hh) * kP + j * 8 : opsrc, v);
     }
     const unsigned char* img = simg + ((((int64_t)b * nc + c) * H + hh) * (int64_t)SM::kImg);
-    for (int i = wtid; i < SM::kImg / 16; i += 128) cp_async16(Pw + 16 * i, img + 16 * i, true);
+    for (int i = wtid; i < SM::kImg / 16; i += 256) cp_async16(Pw + 16 * i, img + 16 * i, true);
     const int64_t cvh = (((int64_t)b * H + hh) * nc + c) * L;
-    for (int i = wtid; i < L / 4; i += 128) {
+    for (int i = wtid; i < L / 4; i += 256) {
       cp_async16(sraw + 4 * i, acs + cvh + 4 * i, true);
       cp_async16(sraw + L + 4 * i, delta + cvh + 4 * i, true);
     }
@@ -411,7 +390,7 @@ __global__ void __launch_bounds__(256, 1)
     const float Dh = D ? D[h] : 0.f;
     cp_async_wait<0>();
     group_sync(gbar);  // the raw vectors were copied by other threads of the group
-    for (int i = wtid; i < L; i += 128) {
+    for (int i = wtid; i < L; i += 256) {
       const float a2 = sraw[i] * kLog2e, dl = sraw[L + i];
       sa2[i] = a2;
       sx[i] = REV ? dl : (dl > 0.f ? a2 - lg2_approx(dl) : __int_as_float(0x7f800000));
@@ -438,19 +417,18 @@ __global__ void __launch_bounds__(256, 1)
     for (int j = 0; j < nsp; ++j) {
       if (j > 0) mbar_wait(&bar_p[wg], (n_p - 1) & 1, status, &abort_flag);
       const float* colv = (REV ? sa2 : sx) + col0 + 64 * j;  // per-column log2 terms
-      // 16-column groups; the TMEM load of group q+1 is in flight while group q
-      // is formed (wait::ld covers every earlier load, so it is issued first)
+      // the thread's 32 columns as two 16-column groups; the second group's
+      // TMEM load is in flight while the first is formed
       float cbA[16], cbB[16];
-      tmem_ld16(tlane + 64 * j, cbA);
+      tmem_ld16(tlane + 64 * j + 32 * half, cbA);
       tmem_wait_ld();
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float(&cur)[16] = (q & 1) ? cbB : cbA;
-        float(&nxt)[16] = (q & 1) ? cbA : cbB;
-        if (q < 3) tmem_ld16(tlane + 64 * j + 16 * (q + 1), nxt);
+      for (int qg = 0; qg < 2; ++qg) {
+        float(&cur)[16] = qg ? cbB : cbA;
+        if (qg == 0) tmem_ld16(tlane + 64 * j + 32 * half + 16, cbB);
 #pragma unroll
         for (int k8 = 0; k8 < 2; ++k8) {
-          const int c8 = 16 * q + 8 * k8;  // panel-local column of the chunk
+          const int c8 = 32 * half + 16 * qg + 8 * k8;  // panel-local column of the chunk
           const float4 w0 = *reinterpret_cast<const float4*>(colv + c8);
           const float4 w1 = *reinterpret_cast<const float4*>(colv + c8 + 4);
           const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -464,7 +442,7 @@ __global__ void __launch_bounds__(256, 1)
           const uint32_t off = sw128(rr, c8 / 8);
           store_split8(Pw + off, Pw + LT * 128 + off, v);
         }
-        if (q < 3) tmem_wait_ld();
+        if (qg == 0) tmem_wait_ld();
       }
       fence_async_smem();
       fence_before_sync();
@@ -482,32 +460,34 @@ __global__ void __launch_bounds__(256, 1)
       }
       ++n_p;
     }
+    // this thread's 32 columns of its row of the second operand (x or dy) and,
+    // rev, of x: loaded now, so the latency overlaps the last MMAs
+    const int64_t rowoff = (((int64_t)b * T + t0 + r) * H + h) * kP;
+    const bool live = r < Lv;
+    uint4 orow[4], xrow[4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      orow[kk] = live ? *reinterpret_cast<const uint4*>(opsrc + rowoff + 32 * half + 8 * kk)
+                      : make_uint4(0, 0, 0, 0);
+      if constexpr (REV)
+        xrow[kk] = live ? *reinterpret_cast<const uint4*>(x + rowoff + 32 * half + 8 * kk)
+                        : make_uint4(0, 0, 0, 0);
+    }
     ++n_done;
     const bool ok = mbar_wait(&bar_done[wg], (n_done - 1) & 1, status, &abort_flag);
     fence_after_sync();
     // this head's MMAs are done: sX and the P buffer take the next head's data
     if (h + 2 < h_end) prefetch(h + 2);
     cp_async_commit();
+    float pd = 0.f, pq = 0.f, pdd = 0.f;  // rev: partial <x, u>, <x, state part>, <x, dy>
     if (ok) {
-      const int64_t rowoff = (((int64_t)b * T + t0 + r) * H + h) * kP;
       const float ea = ex2_approx(ar2), es = ex2_approx(sa2[L - 1] - ar2);
       const float dr = REV ? sx[r] : 0.f;
-      float pd = 0.f, pq = 0.f, pdd = 0.f;
-      const bool live = r < Lv;
-      uint4 orow[8], xrow[8];  // this row's second operand (x or dy) and, rev, x
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        orow[k] = live ? *reinterpret_cast<const uint4*>(opsrc + rowoff + 8 * k)
-                       : make_uint4(0, 0, 0, 0);
-        if constexpr (REV)
-          xrow[k] = live ? *reinterpret_cast<const uint4*>(x + rowoff + 8 * k)
-                         : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int c16 = 0; c16 < 4; ++c16) {
+      for (int c16 = 0; c16 < 2; ++c16) {
         float yv[16], st[16];
-        tmem_ld16(tlane + colY + 16 * c16, yv);
-        tmem_ld16(tlane + colST + 16 * c16, st);
+        tmem_ld16(tlane + colY + 32 * half + 16 * c16, yv);
+        tmem_ld16(tlane + colST + 32 * half + 16 * c16, st);
         tmem_wait_ld();
         if (live) {
 #pragma unroll
@@ -531,7 +511,7 @@ __global__ void __launch_bounds__(256, 1)
                 pdd = fmaf(xv[e], ov[e], pdd);
               }
             }
-            Tout* op = out + rowoff + 16 * c16 + 8 * k8;
+            Tout* op = out + rowoff + 32 * half + 16 * c16 + 8 * k8;
             if constexpr (sizeof(Tout) == 4) {
               float* of = reinterpret_cast<float*>(op);
               *reinterpret_cast<float4*>(of) = make_float4(o[0], o[1], o[2], o[3]);
@@ -544,12 +524,19 @@ __global__ void __launch_bounds__(256, 1)
           }
         }
       }
-      if constexpr (REV) {
-        if (live) {
-          ddir[cv + r] = pd;
-          qrow[cv + r] = dr * pq;
-          ddiag[cv + r] = pdd;
-        }
+    }
+    if constexpr (REV) {
+      // combine the two half-rows (pipeline-local barrier)
+      if (half == 1) {
+        sred[rr] = pd;
+        sred[128 + rr] = pq;
+        sred[256 + rr] = pdd;
+      }
+      group_sync(gbar);
+      if (half == 0 && r < Lv) {
+        ddir[cv + r] = pd + sred[rr];
+        qrow[cv + r] = sx[r] * (pq + sred[128 + rr]);
+        ddiag[cv + r] = pdd + sred[256 + rr];
       }
     }
     fence_before_sync();
@@ -1008,7 +995,7 @@ cudaError_t launch_tc_forward_t(const Dims& d, const FwdArgs& a, const FwdWs& w,
     int grid, per;
     scan_partition(d, sms, &grid, &per);
     SSD_LAUNCH("k_scan_tc", s,
-               kern<<<grid, 256, SM::kBytes, s>>>(
+               kern<<<grid, 512, SM::kBytes, s>>>(
                    static_cast<const bf16*>(a.x), static_cast<const bf16*>(a.B),
                    static_cast<const bf16*>(a.C), nullptr, w.delta, w.acs,
                    static_cast<const unsigned char*>(w.Himg), a.D,
@@ -1060,7 +1047,7 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
     int grid, per;
     scan_partition(d, sms, &grid, &per);
-    SSD_LAUNCH("k_scan_tc_dx", s, kern<<<grid, 256, SM::kBytes, s>>>(
+    SSD_LAUNCH("k_scan_tc_dx", s, kern<<<grid, 512, SM::kBytes, s>>>(
         x, Bm, Cm, dy, w.delta, w.acs, static_cast<const unsigned char*>(w.dSimg), a.f.D, a.dx,
         w.ddir, w.qrow, w.ddiag, d.B, d.T, d.H, d.G, d.nc, per, status));
   }
