@@ -207,6 +207,7 @@ def run_ours(args, world, rank, local):
     dom = max(per_kernel, key=lambda k: per_kernel[k]["ms_total"])
     peaks = load_peaks()
     roof = kernel_roofline(dom, per_kernel[dom], rd, peaks, roofline)
+    roof["traffic"] = measured_traffic(dom, args.workload)
     kernels_out = {}
     for k, v in per_kernel.items():
         r = kernel_roofline(k, v, rd, peaks, roofline)
@@ -253,6 +254,25 @@ def load_peaks():
                 "bf16_sustained": float(p.get("bf16_tflops_sustained", p.get("bf16_tflops"))),
                 "source": "measured"}
     return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def measured_traffic(name, workload):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
+    one ncu capture of this kernel on this workload, from profiles/; None when
+    no capture exists or the kernel sources changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        entry = json.load(f).get(name)
+    if not entry or entry.get("workload") != workload:
+        return None
+    h = hashlib.sha256()
+    for src in entry["sources"]:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return int(entry["bytes_per_launch"]) if h.hexdigest() == entry["sources_sha256"] else None
 
 
 def kernel_roofline(name, v, rd, peaks, roofline):
