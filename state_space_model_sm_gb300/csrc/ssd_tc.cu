@@ -552,22 +552,31 @@ __global__ void __launch_bounds__(512, 1)
 }
 
 // ================================================================ dB and dC
-// grid (nc * L/128, B, G * nblk), 256 threads.  CTA = a 128-row tile of chunk
+// grid (nc * L/128, B, G * nblk), 288 threads.  CTA = a 128-row tile of chunk
 // c and one block of hb consecutive heads of group g (blockIdx.z = g*nblk + k);
 // its accumulator sums the block's heads, so out holds one partial per block.
 // REV = false -> dC (rows l, columns s in [0, l0 + 128)):
-//   per head and 128-column panel: S0 = C_l . B_s (K = N), S1 = dy_l . x_s (K = P)
+//   per head and 64-column panel: S1 = dy_l . x_s (K = P),
 //     P2[l,s] = e^{a_l - a_s} delta_s S1 [s <= l];  ACC += P2 . B  (K = s)
-//     msum_l += sum_{s < l} S0 P2
-//   then ACC += (e^{a_l} dy_l) . H_c (K = p);  ST = C_l . H_c^T (K = n)
-//     ycs_l = e^{a_l} <dy_l, ST_l>
+//   then ACC += (e^{a_l} dy_l) . H_c (K = p)
 // REV = true -> dB (rows s, columns l in [s0, L)):
-//   S0 = B_s . C_l, S1 = x_s . dy_l
-//     P2[s,l] = e^{a_l - a_s} delta_s S1 [l >= s];  ACC += P2 . C  (K = l)
-//     msum_s += sum_{l > s} S0 P2
+//   S1 = x_s . dy_l,  P2[s,l] = e^{a_l - a_s} delta_s S1 [l >= s];  ACC += P2 . C
 //   then ACC += (delta_s e^{a_last - a_s} x_s) . dS_c (K = p)
-// msum holds the strict row (dC) or column (dB) sums of
-// M[l,s] = C_l.B_s e^{a_l - a_s} delta_s <dy_l, x_s> for the ddA gradient.
+// The ddA terms come from the accumulator itself.  Each head accumulates
+// into its own TMEM region HD (started from zero), folded into the block's
+// total TOT by the conversion threads.  With R the tile's row operand of the
+// contraction HD feeds (C_l for dC, B_s for dB), x1 = R_r . HD_r after the
+// head's panels and x2 = R_r . HD_r after its state term:
+//   msum_r = x1 - P2[r,r] (R_r . G_r)   (strict row / column sum of
+//            M[l,s] = C_l.B_s e^{a_l - a_s} delta_s <dy_l, x_s>; G = the other operand)
+//   ycs_l  = x2 - x1 = e^{a_l} <dy_l, C_l . H_c^T>                  (dC only)
+// so no C.B^T or C.H^T product is formed.
+//
+// Warps 0-15 form P2 (rows split over the four TMEM lane quarters, columns
+// over four groups); warp 16 issues every MMA.  S1 panels alternate between two
+// TMEM buffers and P2 panels between two shared-memory buffers, handed over
+// with full / empty mbarriers, so the tensor core forms panel k+1 and
+// accumulates panel k-1 while panel k is converted.
 template <int N, int L>
 struct BcSmem {
   static constexpr int kLT = 128;
@@ -575,12 +584,34 @@ struct BcSmem {
   static constexpr int kGC = (N / 64) * L * 128;
   static constexpr int kHR = kLT * 128;
   static constexpr int kHC = L * 128;
-  static constexpr int kPP = 4 * kLT * 128;  // P2 panel (2 x 64 columns, hi + lo); state operands later
-  static constexpr int kBytes = kGR + kGC + kHR + kHC + kPP + (4 * L + 4 * 128) * 4 + 1024;
+  static constexpr int kPB = 2 * kLT * 128;  // one P buffer: 64-column panel, hi + lo
+  static constexpr int kBytes = kGR + kGC + kHR + kHC + 2 * kPB + (4 * L + 8 * 128) * 4 + 1024;
+  static_assert(2 * (N / 64) * 8192 <= kPB, "state image fits one P buffer");
 };
 
+constexpr int kBcEpiWarps = 16;                // conversion warps: 4 lane quarters x 4 column groups
+constexpr int kBcEpi = 32 * kBcEpiWarps;        // conversion threads
+constexpr int kBcThreads = kBcEpi + 32;         // + the MMA warp
+
+// rows [0, rows) of 8*nchunk bf16 into 128-byte-swizzle panels by the
+// conversion threads (t in [0, kBcEpi)); rows >= valid are zero-filled.
+template <class RowPtr>
+__device__ __forceinline__ void stage_rows_epi(unsigned char* dst, int rows, int nchunk,
+                                               uint32_t panel, int valid, const bf16* safe,
+                                               RowPtr rowptr, int t) {
+  for (int i = t; i < rows * nchunk; i += kBcEpi) {
+    const int r = i / nchunk, j = i % nchunk;
+    const bool v = r < valid;
+    cp_async16(dst + (j / 8) * panel + sw128(r, j % 8), v ? rowptr(r) + j * 8 : safe, v);
+  }
+}
+
+__device__ __forceinline__ void epi_sync() {  // the conversion threads
+  asm volatile("bar.sync 1, %0;" ::"n"(kBcEpi) : "memory");
+}
+
 template <int N, int L, bool REV>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kBcThreads, 1)
     k_bwd_bc_tc(const bf16* __restrict__ x, const bf16* __restrict__ Bm,
                 const bf16* __restrict__ Cm, const bf16* __restrict__ dy,
                 const float* __restrict__ delta, const float* __restrict__ acs,
@@ -589,9 +620,10 @@ __global__ void __launch_bounds__(256, 1)
                 int hb, int* status) {
   using SM = BcSmem<N, L>;
   constexpr int LT = SM::kLT, NLT = L / LT, NKP = N / 64;
-  constexpr uint32_t kColS0 = 0, kColS1 = 128, kColAcc = 256, kColST = 384;
+  constexpr uint32_t kColAcc = 128, kColTot = 256;  // HD, TOT; S1 buffers at columns 0 and 64
   extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t bar_s, bar_acc, bar_st;
+  __shared__ uint64_t bar_sfull[2], bar_sempty[2], bar_pfull[2], bar_pempty[2];
+  __shared__ uint64_t bar_ops, bar_stready, bar_sdone;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   unsigned char* base = align1024(smem_raw);
@@ -599,18 +631,18 @@ __global__ void __launch_bounds__(256, 1)
   unsigned char* sGC = sGR + SM::kGR;
   unsigned char* sHR = sGC + SM::kGC;
   unsigned char* sHC = sHR + SM::kHR;
-  unsigned char* sP = sHC + SM::kHC;
-  float* sa2 = reinterpret_cast<float*>(sP + SM::kPP);  // a * log2(e)
+  unsigned char* sP = sHC + SM::kHC;  // P buffers 0 and 1
+  float* sa2 = reinterpret_cast<float*>(sP + 2 * SM::kPB);  // a * log2(e)
   float* sx = sa2 + L;   // dC: a*log2e - log2(delta) (+inf at delta = 0); dB: log2(delta) (-inf)
-  float* sred = sx + L;  // [4][128]
-  float* sraw = sred + 4 * 128;  // prefetched a [L], delta [L] of the next head
+  float* sred = sx + L;  // [2][4][128]: per column group, msum and ycs partials
+  float* sraw = sred + 8 * 128;  // prefetched a [L], delta [L] of the next head
 
   const int c = blockIdx.x / NLT, tile = blockIdx.x % NLT, b = blockIdx.y;
   const int nblk = gridDim.z / G, g = blockIdx.z / nblk, kb = blockIdx.z % nblk;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h_begin = g * (H / G) + kb * hb, h_end = h_begin + hb;
   const int r0 = tile * LT, col0 = REV ? r0 : 0, ncol = REV ? L - r0 : r0 + LT;
-  const int npan = ncol / 128;
+  const int npan = ncol / 64;
   const int64_t t0 = (int64_t)c * L;
   const int Lv = min(L, T - (int)t0);
   const bf16* grow = REV ? Bm : Cm;
@@ -620,235 +652,304 @@ __global__ void __launch_bounds__(256, 1)
 
   if (tid == 0) {
     abort_flag = 0;
-    mbar_init(&bar_s, 1);
-    mbar_init(&bar_acc, 1);
-    mbar_init(&bar_st, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_sfull[i], 1);
+      mbar_init(&bar_sempty[i], kBcEpiWarps);
+      mbar_init(&bar_pfull[i], kBcEpiWarps);
+      mbar_init(&bar_pempty[i], 1);
+    }
+    mbar_init(&bar_ops, kBcEpi);
+    mbar_init(&bar_stready, kBcEpi);
+    mbar_init(&bar_sdone, 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&tmem_base, 512);
-  stage_rows_async(sGR, LT, N / 8, LT * 128, Lv - r0, grow, [&](int rr2) {
-    return grow + (((int64_t)b * T + t0 + r0 + rr2) * G + g) * N;
-  });
-  stage_rows_async(sGC, ncol, N / 8, L * 128, Lv - col0, gcol, [&](int cc) {
-    return gcol + (((int64_t)b * T + t0 + col0 + cc) * G + g) * N;
-  });
-  auto stage_hc = [&](int hh) {
-    stage_rows_async(sHC, ncol, 8, 0, Lv - col0, hcol, [&](int cc) {
-      return hcol + (((int64_t)b * T + t0 + col0 + cc) * H + hh) * kP;
-    });
-    const int64_t cvh = (((int64_t)b * H + hh) * nc + c) * L;
-    for (int i = tid; i < L / 4; i += 256) {
-      cp_async16(sraw + 4 * i, acs + cvh + 4 * i, true);
-      cp_async16(sraw + L + 4 * i, delta + cvh + 4 * i, true);
-    }
-  };
-  stage_hc(h_begin);
-  cp_async_commit();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tm = tmem_base;
-  const int q = warp & 3, half = warp >> 2;
-  const int rr = 32 * q + lane, r = r0 + rr;
-  const uint32_t tlane = tm + ((uint32_t)(32 * q) << 16);
-  uint32_t n_s = 0, n_acc = 0, n_st = 0;
-  bool acc_started = false;  // meaningful in thread 0 only
-  constexpr uint32_t id_sc0 = idesc_bf16(128, 128, 0, 0);
+  constexpr uint32_t id_s = idesc_bf16(128, 64, 0, 0);
   constexpr uint32_t id_acc = idesc_bf16(128, N, 0, 1);
-  constexpr uint32_t id_st = idesc_bf16(128, kP, 0, 0);
-  unsigned char* sAh = sP;                      // state A operand hi / lo (128 x 64)
-  unsigned char* sAl = sP + LT * 128;
-  unsigned char* sBh = sP + 2 * LT * 128;       // state B operand hi / lo (64 x N)
-  unsigned char* sBl = sBh + NKP * 64 * 128;
 
-  for (int h = h_begin; h < h_end; ++h) {
-    const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
-    // this head's row operand; its column operand and a / delta were prefetched
-    stage_rows_async(sHR, LT, 8, 0, Lv - r0, hrow, [&](int r2) {
-      return hrow + (((int64_t)b * T + t0 + r0 + r2) * H + h) * kP;
-    });
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();  // raw vectors copied by other threads
-    for (int i = tid; i < L; i += 256) {
-      const float a2 = sraw[i] * kLog2e, dl = sraw[L + i];
-      const float l2 = dl > 0.f ? lg2_approx(dl) : -__int_as_float(0x7f800000);
-      sa2[i] = a2;
-      sx[i] = REV ? l2 : a2 - l2;
-    }
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    // row constant of the decay exponent (dB folds delta_s of the row in)
-    const float arow = REV ? sa2[r] - sx[r] : sa2[r];
-    float mpart = 0.f;
-    for (int k = 0; k < npan; ++k) {
-      if (tid == 0) {
-        fence_after_sync();
-        for (int ks = 0; ks < N / 16; ++ks) {
-          const uint32_t kp = ks / 4, ko = (ks % 4) * 32;
-          mma_bf16(tm + kColS0, sdesc(smem_u32(sGR) + kp * (LT * 128) + ko, 16, 1024),
-                   sdesc(smem_u32(sGC) + kp * (L * 128) + k * 128 * 128 + ko, 16, 1024), id_sc0,
-                   ks > 0 ? 1u : 0u);
-        }
-        for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tm + kColS1, sdesc(smem_u32(sHR) + ks * 32, 16, 1024),
-                   sdesc(smem_u32(sHC) + k * 128 * 128 + ks * 32, 16, 1024), id_sc0,
-                   ks > 0 ? 1u : 0u);
-        mma_commit(&bar_s);
-      }
-      ++n_s;
-      mbar_wait(&bar_s, (n_s - 1) & 1, status, &abort_flag);
-      if (n_acc > 0) mbar_wait(&bar_acc, (n_acc - 1) & 1, status, &abort_flag);
+  if (warp == kBcEpiWarps) {
+    // ------------------------------------------------------------ MMA warp
+    const uint32_t leader = elect_one();
+    const uint64_t dHR = sdesc(smem_u32(sHR), 16, 1024), dHC = sdesc(smem_u32(sHC), 16, 1024);
+    const uint64_t dGC = sdesc(smem_u32(sGC), L * 128, 1024), dP = sdesc(smem_u32(sP), 16, 1024);
+    const uint64_t dIm = sdesc(smem_u32(sP + SM::kPB), 64 * 128, 1024);
+    constexpr uint32_t kLo = NKP * 64 * 128;  // lo panels of the state image
+    uint32_t ph_se = 0, ph_pf = 0;  // per-buffer parity bits of the next wait
+    uint32_t n_head = 0, gp = 0;
+    auto issue_s1 = [&](int j, uint32_t bs) {
+      mbar_wait(&bar_sempty[bs], ((ph_se >> bs) & 1u) ^ 1u, status, &abort_flag);
+      ph_se ^= 1u << bs;
       fence_after_sync();
-      // 16-column groups of S0 and S1; group q+1's TMEM loads fly while q is formed
-      float a0[16], a1[16], b0[16], b1[16];
-      tmem_ld16(tlane + kColS0 + 64 * half, a0);
-      tmem_ld16(tlane + kColS1 + 64 * half, a1);
-      tmem_wait_ld();
 #pragma unroll
-      for (int qg = 0; qg < 4; ++qg) {
-        float(&s0)[16] = (qg & 1) ? b0 : a0;
-        float(&s1)[16] = (qg & 1) ? b1 : a1;
-        float(&n0)[16] = (qg & 1) ? a0 : b0;
-        float(&n1)[16] = (qg & 1) ? a1 : b1;
-        const uint32_t cb = 64 * half + 16 * qg;
-        if (qg < 3) {
-          tmem_ld16(tlane + kColS0 + cb + 16, n0);
-          tmem_ld16(tlane + kColS1 + cb + 16, n1);
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16_if(tm + 64 * bs, desc_add(dHR, ks * 32), desc_add(dHC, j * 64 * 128 + ks * 32),
+                    id_s, ks > 0 ? 1u : 0u, leader);
+      mma_commit_if(&bar_sfull[bs], leader);
+    };
+    for (int h = h_begin; h < h_end; ++h, ++n_head) {
+      mbar_wait(&bar_ops, n_head & 1u, status, &abort_flag);  // HR, HC of this head staged
+      fence_after_sync();
+      issue_s1(0, gp & 1u);
+      for (int j = 0; j < npan; ++j) {
+        const uint32_t bs = (gp + j) & 1u;
+        if (j + 1 < npan) issue_s1(j + 1, bs ^ 1u);
+        mbar_wait(&bar_pfull[bs], (ph_pf >> bs) & 1u, status, &abort_flag);
+        ph_pf ^= 1u << bs;
+        fence_after_sync();
+        const uint64_t dp = desc_add(dP, bs * SM::kPB);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t bd = desc_add(dGC, (j * 64 + ks * 16) * 128);
+          mma_bf16_if(tm + kColAcc, desc_add(dp, ks * 32), bd, id_acc, (j > 0 || ks > 0) ? 1u : 0u,
+                      leader);
+          mma_bf16_if(tm + kColAcc, desc_add(dp, LT * 128 + ks * 32), bd, id_acc, 1u, leader);
+        }
+        mma_commit_if(&bar_pempty[bs], leader);
+      }
+      gp += npan;
+      // state term: A operand (hi / lo) in P buffer 0, the state image in P buffer 1
+      mbar_wait(&bar_stready, n_head & 1u, status, &abort_flag);
+      fence_after_sync();
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const uint64_t ah = desc_add(dP, ks * 32), al = desc_add(dP, LT * 128 + ks * 32);
+        const uint64_t bh = desc_add(dIm, ks * 2048), bl = desc_add(dIm, kLo + ks * 2048);
+        mma_bf16_if(tm + kColAcc, ah, bh, id_acc, 1u, leader);
+        mma_bf16_if(tm + kColAcc, ah, bl, id_acc, 1u, leader);
+        mma_bf16_if(tm + kColAcc, al, bh, id_acc, 1u, leader);
+      }
+      mma_commit_if(&bar_sdone, leader);
+    }
+  } else {
+    // ----------------------------------------------------- conversion warps
+    constexpr int NC = N / 4;  // accumulator columns of one column group
+    const int q = warp & 3, cq = warp >> 2;
+    const int rr = 32 * q + lane, r = r0 + rr;
+    const uint32_t tlane = tm + ((uint32_t)(32 * q) << 16);
+    unsigned char* sAh = sP;  // state A operand hi / lo (128 x 64)
+    unsigned char* sAl = sP + LT * 128;
+    auto stage_hr = [&](int hh) {
+      stage_rows_epi(sHR, LT, 8, 0, Lv - r0, hrow, [&](int r2) {
+        return hrow + (((int64_t)b * T + t0 + r0 + r2) * H + hh) * kP;
+      }, tid);
+    };
+    auto stage_hc = [&](int hh) {
+      stage_rows_epi(sHC, ncol, 8, 0, Lv - col0, hcol, [&](int cc) {
+        return hcol + (((int64_t)b * T + t0 + col0 + cc) * H + hh) * kP;
+      }, tid);
+      const int64_t cvh = (((int64_t)b * H + hh) * nc + c) * L;
+      for (int i = tid; i < L / 4; i += kBcEpi) {
+        cp_async16(sraw + 4 * i, acs + cvh + 4 * i, true);
+        cp_async16(sraw + L + 4 * i, delta + cvh + 4 * i, true);
+      }
+    };
+    stage_rows_epi(sGR, LT, N / 8, LT * 128, Lv - r0, grow, [&](int rr2) {
+      return grow + (((int64_t)b * T + t0 + r0 + rr2) * G + g) * N;
+    }, tid);
+    stage_rows_epi(sGC, ncol, N / 8, L * 128, Lv - col0, gcol, [&](int cc) {
+      return gcol + (((int64_t)b * T + t0 + col0 + cc) * G + g) * N;
+    }, tid);
+    stage_hc(h_begin);
+    stage_hr(h_begin);
+    cp_async_commit();
+
+    // R_r . HD_r over this thread's column group; fold != 0 also adds HD into
+    // TOT (first == true: TOT = HD)
+    auto acc_dot = [&](bool fold, bool first) {
+      float s = 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < NC; c0 += 16) {
+        float v[16];
+        const uint32_t col = cq * NC + c0;
+        tmem_ld16(tlane + kColAcc + col, v);
+        tmem_wait_ld();
+        if (fold) {
+          float t[16];
+          if (!first) {
+            tmem_ld16(tlane + kColTot + col, t);
+            tmem_wait_ld();
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) t[e] = first ? v[e] : t[e] + v[e];
+          tmem_st16(tlane + kColTot + col, t);
         }
 #pragma unroll
         for (int k8 = 0; k8 < 2; ++k8) {
-          const float* colv = (REV ? sa2 : sx) + col0 + 128 * k + cb + 8 * k8;
-          const float4 w0 = *reinterpret_cast<const float4*>(colv);
-          const float4 w1 = *reinterpret_cast<const float4*>(colv + 4);
-          const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-          float v[8];
+          const int cc = cq * NC + c0 + 8 * k8;  // first of 8 columns
+          float rv[8];
+          unpack8(*reinterpret_cast<const uint4*>(sGR + (cc / 64) * (LT * 128) +
+                                                  sw128(rr, (cc % 64) / 8)), rv);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int cl = col0 + 128 * k + cb + 8 * k8 + e;  // chunk-local column
-            const float f = REV ? ex2_approx(wv[e] - arow) : ex2_approx(arow - wv[e]);
-            const bool keep = REV ? cl >= r : cl <= r;
-            const bool strict = REV ? cl > r : cl < r;
-            const float p2 = keep ? f * s1[8 * k8 + e] : 0.f;
-            if (strict) mpart = fmaf(s0[8 * k8 + e], p2, mpart);
-            v[e] = p2;
-          }
-          const uint32_t off = half * (LT * 128) + sw128(rr, (16 * qg + 8 * k8) / 8);
-          store_split8(sP + off, sP + 2 * LT * 128 + off, v);
+          for (int e = 0; e < 8; ++e) s = fmaf(rv[e], v[8 * k8 + e], s);
         }
-        if (qg < 3) tmem_wait_ld();
+      }
+      if (fold) tmem_wait_st();
+      return s;
+    };
+
+    // per-buffer parity bits: S1 full waits, and the number of panels written
+    // into each P buffer (mod 2); CTA-uniform
+    uint32_t ph_sf = 0, ph_pe = 0, n_head = 0, gp = 0;
+    float cbdot = 0.f;  // R_r . G_r (the diagonal's M factor)
+    for (int h = h_begin; h < h_end; ++h, ++n_head) {
+      const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
+      cp_async_wait<0>();  // HR, HC and a / delta of this head (and GR, GC the first time)
+      epi_sync();
+      if (h == h_begin) {
+        const int rc = r - col0;  // the row of the column operand at the diagonal
+        float s = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < N; cc += 8) {
+          float u[8], w[8];
+          unpack8(*reinterpret_cast<const uint4*>(sGR + (cc / 64) * (LT * 128) +
+                                                  sw128(rr, (cc % 64) / 8)), u);
+          unpack8(*reinterpret_cast<const uint4*>(sGC + (cc / 64) * (L * 128) +
+                                                  sw128(rc, (cc % 64) / 8)), w);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) s = fmaf(u[e], w[e], s);
+        }
+        cbdot = s;
+      }
+      for (int i = tid; i < L; i += kBcEpi) {
+        const float a2 = sraw[i] * kLog2e, dl = sraw[L + i];
+        const float l2 = dl > 0.f ? lg2_approx(dl) : -__int_as_float(0x7f800000);
+        sa2[i] = a2;
+        sx[i] = REV ? l2 : a2 - l2;
       }
       fence_async_smem();
-      fence_before_sync();
-      __syncthreads();
-      if (tid == 0) {
+      mbar_arrive(&bar_ops);  // this thread's staged operands are visible to the MMAs
+      epi_sync();             // sa2 / sx complete
+      const float arow = REV ? sa2[r] - sx[r] : sa2[r];
+      float pdiag = 0.f;  // P2 at the diagonal (this thread's row), if its columns hold it
+      for (int j = 0; j < npan; ++j) {
+        const uint32_t bs = (gp + j) & 1u;
+        mbar_wait(&bar_sfull[bs], (ph_sf >> bs) & 1u, status, &abort_flag);
+        ph_sf ^= 1u << bs;
         fence_after_sync();
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t sub = ks / 4, ko = (ks % 4) * 32;
-          const uint64_t bd = sdesc(smem_u32(sGC) + (k * 128 + ks * 16) * 128, L * 128, 1024);
-          mma_bf16(tm + kColAcc, sdesc(smem_u32(sP) + sub * (LT * 128) + ko, 16, 1024), bd, id_acc,
-                   acc_started ? 1u : 0u);
-          acc_started = true;
-          mma_bf16(tm + kColAcc,
-                   sdesc(smem_u32(sP) + 2 * LT * 128 + sub * (LT * 128) + ko, 16, 1024), bd,
-                   id_acc, 1u);
-        }
-        mma_commit(&bar_acc);
-      }
-      ++n_acc;
-    }
-    // state term of this head; the column operand is free: fetch the next head's
-    mbar_wait(&bar_acc, (n_acc - 1) & 1, status, &abort_flag);
-    {
-      // the head's state image (hi / lo panels) into the free P buffer
-      const unsigned char* img = simg + ((((int64_t)b * nc + c) * H + h) * (int64_t)(2 * NKP * 8192));
-      for (int i = tid; i < 2 * NKP * 8192 / 16; i += 256) cp_async16(sBh + 16 * i, img + 16 * i, true);
-      cp_async_commit();
-    }
-    if (h + 1 < h_end) stage_hc(h + 1);
-    cp_async_commit();
-    for (int i = tid; i < LT * 8; i += 256) {
-      const int r2 = i >> 3, j = i & 7, row = r0 + r2;
-      float v[8];
-      unpack8(*reinterpret_cast<const uint4*>(sHR + sw128(r2, j)), v);
-      const float sc = REV ? ex2_approx(sa2[L - 1] - sa2[row] + sx[row]) : ex2_approx(sa2[row]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] *= sc;
-      store_split8(sAh + sw128(r2, j), sAl + sw128(r2, j), v);
-    }
-    cp_async_wait<1>();  // the state image (the next head's prefetch may still fly)
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-      fence_after_sync();
-      for (int ks = 0; ks < 4; ++ks) {
-        const uint64_t ah = sdesc(smem_u32(sAh) + ks * 32, 16, 1024);
-        const uint64_t al = sdesc(smem_u32(sAl) + ks * 32, 16, 1024);
-        const uint64_t bh = sdesc(smem_u32(sBh) + ks * 2048, 64 * 128, 1024);
-        const uint64_t bl = sdesc(smem_u32(sBl) + ks * 2048, 64 * 128, 1024);
-        mma_bf16(tm + kColAcc, ah, bh, id_acc, 1u);
-        mma_bf16(tm + kColAcc, ah, bl, id_acc, 1u);
-        mma_bf16(tm + kColAcc, al, bh, id_acc, 1u);
-      }
-      if constexpr (!REV) {
-        for (int ks = 0; ks < N / 16; ++ks) {
-          const uint32_t kp = ks / 4, ko = (ks % 4) * 32;
-          const uint64_t ad = sdesc(smem_u32(sGR) + kp * (LT * 128) + ko, 16, 1024);
-          mma_bf16(tm + kColST, ad, sdesc(smem_u32(sBh) + kp * (64 * 128) + ko, 16, 1024), id_st,
-                   ks > 0 ? 1u : 0u);
-          mma_bf16(tm + kColST, ad, sdesc(smem_u32(sBl) + kp * (64 * 128) + ko, 16, 1024), id_st,
-                   1u);
-        }
-      }
-      mma_commit(&bar_st);
-    }
-    ++n_st;
-    const bool ok = mbar_wait(&bar_st, (n_st - 1) & 1, status, &abort_flag);
-    fence_after_sync();
-    float ypart = 0.f;
-    if constexpr (!REV) {
-      if (ok) {
-        float st[32];
-        tmem_ld16(tlane + kColST + 32 * half, *reinterpret_cast<float(*)[16]>(st));
-        tmem_ld16(tlane + kColST + 32 * half + 16, *reinterpret_cast<float(*)[16]>(st + 16));
+        float s1[16];
+        tmem_ld16(tlane + 64 * bs + 16 * cq, s1);
         tmem_wait_ld();
-#pragma unroll
-        for (int k8 = 0; k8 < 4; ++k8) {
-          float dv[8];
-          unpack8(*reinterpret_cast<const uint4*>(sHR + sw128(rr, 4 * half + k8)), dv);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) ypart = fmaf(dv[e], st[8 * k8 + e], ypart);
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_sempty[bs]);
+        if (j == npan - 1 && h + 1 < h_end) {
+          stage_hc(h + 1);  // the head's last S1 product is done with the column operand
+          cp_async_commit();
         }
-        ypart *= ex2_approx(sa2[r]);
+        // P buffer bs: the accumulate of its previous panel must be done with it
+        mbar_wait(&bar_pempty[bs], ((ph_pe >> bs) & 1u) ^ 1u, status, &abort_flag);
+        ph_pe ^= 1u << bs;
+        unsigned char* pb = sP + bs * SM::kPB;
+        {
+          // the warp's 32 rows [rw, rw + 32) against its 16 columns [cg, cg + 16):
+          // outside the causal triangle, strictly inside it, or across the diagonal
+          const int cg = col0 + 64 * j + 16 * cq, rw = r0 + 32 * q;
+          const bool outside = REV ? cg + 15 < rw : cg > rw + 31;
+          const bool inside = REV ? cg > rw + 31 : cg + 15 < rw;
+#pragma unroll
+          for (int k8 = 0; k8 < 2; ++k8) {
+            const int cb = 16 * cq + 8 * k8;  // column within the panel
+            const uint32_t off = sw128(rr, cb / 8);
+            if (outside) {
+              *reinterpret_cast<uint4*>(pb + off) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(pb + LT * 128 + off) = make_uint4(0, 0, 0, 0);
+              continue;
+            }
+            const float* colv = (REV ? sa2 : sx) + col0 + 64 * j + cb;
+            const float4 w0 = *reinterpret_cast<const float4*>(colv);
+            const float4 w1 = *reinterpret_cast<const float4*>(colv + 4);
+            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float f = REV ? ex2_approx(wv[e] - arow) : ex2_approx(arow - wv[e]);
+              v[e] = f * s1[8 * k8 + e];
+            }
+            if (!inside) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int cl = col0 + 64 * j + cb + e;  // chunk-local column
+                if (cl == r) pdiag = v[e];
+                if (REV ? cl < r : cl > r) v[e] = 0.f;
+              }
+            }
+            store_split8(pb + off, pb + LT * 128 + off, v);
+          }
+        }
+        fence_async_smem();
+        fence_before_sync();  // HD reads of the previous head precede its next accumulate
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_pfull[bs]);
       }
-    }
-    if (half == 1) {
-      sred[rr] = mpart;
-      sred[128 + rr] = ypart;
-    }
-    __syncthreads();
-    if (half == 0 && r < Lv) {
-      msum[cv + r] = mpart + sred[rr];
-      if constexpr (!REV) ycs[cv + r] = ypart + sred[128 + rr];
-    }
-    fence_before_sync();
-    __syncthreads();
-  }
-  // the block's accumulated dB / dC rows
-  if (!abort_flag) {  // CTA-uniform: the TMEM loads below are warp-collective
-    float* o = out + (((((int64_t)b * T + t0 + r) * G + g) * nblk + kb) * N) + half * (N / 2);
+      // every accumulate of the head done (a commit covers all earlier MMAs)
+      {
+        const uint32_t bl = (gp + npan - 1) & 1u;
+        mbar_wait(&bar_pempty[bl], ((ph_pe >> bl) & 1u) ^ 1u, status, &abort_flag);
+      }
+      gp += npan;
+      fence_after_sync();
+      const float x1 = acc_dot(false, false);
+      // state term operands: the head's state image (hi / lo panels) into P buffer 1
+      {
+        const unsigned char* img =
+            simg + ((((int64_t)b * nc + c) * H + h) * (int64_t)(2 * NKP * 8192));
+        unsigned char* dst = sP + SM::kPB;
+        for (int i = tid; i < 2 * NKP * 8192 / 16; i += kBcEpi)
+          cp_async16(dst + 16 * i, img + 16 * i, true);
+        cp_async_commit();
+      }
+      for (int i = tid; i < LT * 8; i += kBcEpi) {
+        const int r2 = i >> 3, jj = i & 7, row = r0 + r2;
+        float v[8];
+        unpack8(*reinterpret_cast<const uint4*>(sHR + sw128(r2, jj)), v);
+        const float sc = REV ? ex2_approx(sa2[L - 1] - sa2[row] + sx[row]) : ex2_approx(sa2[row]);
 #pragma unroll
-    for (int c0 = 0; c0 < N / 2; c0 += 16) {
-      float v[16];
-      tmem_ld16(tlane + kColAcc + half * (N / 2) + c0, v);
-      tmem_wait_ld();
-      if (r < Lv) {
+        for (int e = 0; e < 8; ++e) v[e] *= sc;
+        store_split8(sAh + sw128(r2, jj), sAl + sw128(r2, jj), v);
+      }
+      cp_async_wait<0>();  // the state image (and the next head's column operand)
+      fence_async_smem();
+      fence_before_sync();  // the HD reads above precede the state term's accumulate
+      mbar_arrive(&bar_stready);
+      epi_sync();  // every thread is done with the row operand
+      if (h + 1 < h_end) {
+        stage_hr(h + 1);
+        cp_async_commit();
+      }
+      // warp-uniform: the TMEM accesses below are warp-collective
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_sdone, n_head & 1u, status, &abort_flag));
+      fence_after_sync();
+      const float x2 = ok ? acc_dot(true, h == h_begin) : x1;
+      const float mpart = x1 - pdiag * cbdot;
+      const float ypart = x2 - x1;
+      sred[cq * 128 + rr] = mpart;
+      sred[512 + cq * 128 + rr] = ypart;
+      epi_sync();
+      if (cq == 0 && r < Lv) {
+        msum[cv + r] = sred[rr] + sred[128 + rr] + sred[256 + rr] + sred[384 + rr];
+        if constexpr (!REV)
+          ycs[cv + r] = sred[512 + rr] + sred[640 + rr] + sred[768 + rr] + sred[896 + rr];
+      }
+      epi_sync();  // sred reused by the next head
+    }
+    // the block's accumulated dB / dC rows
+    if (!abort_flag) {  // CTA-uniform: the TMEM loads below are warp-collective
+      float* o = out + (((((int64_t)b * T + t0 + r) * G + g) * nblk + kb) * N) + cq * NC;
 #pragma unroll
-        for (int k4 = 0; k4 < 16; k4 += 4)
-          *reinterpret_cast<float4*>(o + c0 + k4) =
-              make_float4(v[k4], v[k4 + 1], v[k4 + 2], v[k4 + 3]);
+      for (int c0 = 0; c0 < NC; c0 += 16) {
+        float v[16];
+        tmem_ld16(tlane + kColTot + cq * NC + c0, v);
+        tmem_wait_ld();
+        if (r < Lv) {
+#pragma unroll
+          for (int k4 = 0; k4 < 16; k4 += 4)
+            *reinterpret_cast<float4*>(o + c0 + k4) =
+                make_float4(v[k4], v[k4 + 1], v[k4 + 2], v[k4 + 3]);
+        }
       }
     }
   }
@@ -1059,7 +1160,7 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     using SM = BcSmem<N, L>;
     auto kern = k_bwd_bc_tc<N, L, false>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
-    SSD_LAUNCH("k_bwd_dc_tc", s, kern<<<bgrid, 256, SM::kBytes, s>>>(
+    SSD_LAUNCH("k_bwd_dc_tc", s, kern<<<bgrid, kBcThreads, SM::kBytes, s>>>(
         x, Bm, Cm, dy, w.delta, w.acs, static_cast<const unsigned char*>(w.Himg), dCout,
         w.rowsum, w.ycs, d.T, d.H, d.G, d.nc, hb,
         status));
@@ -1068,7 +1169,7 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     using SM = BcSmem<N, L>;
     auto kern = k_bwd_bc_tc<N, L, true>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
-    SSD_LAUNCH("k_bwd_db_tc", s, kern<<<bgrid, 256, SM::kBytes, s>>>(
+    SSD_LAUNCH("k_bwd_db_tc", s, kern<<<bgrid, kBcThreads, SM::kBytes, s>>>(
         x, Bm, Cm, dy, w.delta, w.acs, static_cast<const unsigned char*>(w.dSimg), dBout,
         w.colsum, nullptr, d.T, d.H, d.G, d.nc, hb,
         status));
