@@ -552,8 +552,9 @@ __global__ void __launch_bounds__(512, 1)
 }
 
 // ================================================================ dB and dC
-// grid (nc * L/128, B, G * nblk), 288 threads.  CTA = a 128-row tile of chunk
-// c and one block of hb consecutive heads of group g (blockIdx.z = g*nblk + k);
+// grid (nc, B, L/128 * G * nblk), 288 threads.  CTA = a 128-row tile of chunk
+// c and one block of hb consecutive heads of group g (blockIdx.z = (tile order)
+// * G * nblk + g * nblk + k);
 // its accumulator sums the block's heads, so out holds one partial per block.
 // REV = false -> dC (rows l, columns s in [0, l0 + 128)):
 //   per head and 64-column panel: S1 = dy_l . x_s (K = P),
@@ -572,8 +573,8 @@ __global__ void __launch_bounds__(512, 1)
 //   ycs_l  = x2 - x1 = e^{a_l} <dy_l, C_l . H_c^T>                  (dC only)
 // so no C.B^T or C.H^T product is formed.
 //
-// Warps 0-15 form P2 (rows split over the four TMEM lane quarters, columns
-// over four groups); warp 16 issues every MMA.  S1 panels alternate between two
+// Warps 0-7 form P2 (rows split over the four TMEM lane quarters, columns
+// over two groups); warp 8 issues every MMA.  S1 panels alternate between two
 // TMEM buffers and P2 panels between two shared-memory buffers, handed over
 // with full / empty mbarriers, so the tensor core forms panel k+1 and
 // accumulates panel k-1 while panel k is converted.
@@ -589,7 +590,8 @@ struct BcSmem {
   static_assert(2 * (N / 64) * 8192 <= kPB, "state image fits one P buffer");
 };
 
-constexpr int kBcEpiWarps = 16;                // conversion warps: 4 lane quarters x 4 column groups
+constexpr int kBcEpiWarps = 8;                 // conversion warps: 4 lane quarters x 2 column groups
+constexpr int kBcGroups = kBcEpiWarps / 4;      // column groups (1, 2 or 4)
 constexpr int kBcEpi = 32 * kBcEpiWarps;        // conversion threads
 constexpr int kBcThreads = kBcEpi + 32;         // + the MMA warp
 
@@ -634,11 +636,13 @@ __global__ void __launch_bounds__(kBcThreads, 1)
   unsigned char* sP = sHC + SM::kHC;  // P buffers 0 and 1
   float* sa2 = reinterpret_cast<float*>(sP + 2 * SM::kPB);  // a * log2(e)
   float* sx = sa2 + L;   // dC: a*log2e - log2(delta) (+inf at delta = 0); dB: log2(delta) (-inf)
-  float* sred = sx + L;  // [2][4][128]: per column group, msum and ycs partials
+  float* sred = sx + L;  // [2][4][128]: per column group (up to 4), msum and ycs partials
   float* sraw = sred + 8 * 128;  // prefetched a [L], delta [L] of the next head
 
-  const int c = blockIdx.x / NLT, tile = blockIdx.x % NLT, b = blockIdx.y;
-  const int nblk = gridDim.z / G, g = blockIdx.z / nblk, kb = blockIdx.z % nblk;
+  // row tiles with the most columns (dC: the last, dB: the first) are launched first
+  const int gz = gridDim.z / NLT, zt = blockIdx.z / gz, zr = blockIdx.z % gz;
+  const int c = blockIdx.x, b = blockIdx.y, tile = REV ? zt : NLT - 1 - zt;
+  const int nblk = gz / G, g = zr / nblk, kb = zr % nblk;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h_begin = g * (H / G) + kb * hb, h_end = h_begin + hb;
   const int r0 = tile * LT, col0 = REV ? r0 : 0, ncol = REV ? L - r0 : r0 + LT;
@@ -676,7 +680,7 @@ __global__ void __launch_bounds__(kBcThreads, 1)
     const uint32_t leader = elect_one();
     const uint64_t dHR = sdesc(smem_u32(sHR), 16, 1024), dHC = sdesc(smem_u32(sHC), 16, 1024);
     const uint64_t dGC = sdesc(smem_u32(sGC), L * 128, 1024), dP = sdesc(smem_u32(sP), 16, 1024);
-    const uint64_t dIm = sdesc(smem_u32(sP + SM::kPB), 64 * 128, 1024);
+    const uint64_t dIm0 = sdesc(smem_u32(sP), 64 * 128, 1024);
     constexpr uint32_t kLo = NKP * 64 * 128;  // lo panels of the state image
     uint32_t ph_se = 0, ph_pf = 0;  // per-buffer parity bits of the next wait
     uint32_t n_head = 0, gp = 0;
@@ -711,12 +715,15 @@ __global__ void __launch_bounds__(kBcThreads, 1)
         mma_commit_if(&bar_pempty[bs], leader);
       }
       gp += npan;
-      // state term: A operand (hi / lo) in P buffer 0, the state image in P buffer 1
+      // state term: A operand (hi / lo) in the last panel's P buffer, the state
+      // image in the other one
       mbar_wait(&bar_stready, n_head & 1u, status, &abort_flag);
       fence_after_sync();
+      const uint32_t pl = (gp - 1) & 1u;
+      const uint64_t dA = desc_add(dP, pl * SM::kPB), dIm = desc_add(dIm0, (pl ^ 1u) * SM::kPB);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        const uint64_t ah = desc_add(dP, ks * 32), al = desc_add(dP, LT * 128 + ks * 32);
+        const uint64_t ah = desc_add(dA, ks * 32), al = desc_add(dA, LT * 128 + ks * 32);
         const uint64_t bh = desc_add(dIm, ks * 2048), bl = desc_add(dIm, kLo + ks * 2048);
         mma_bf16_if(tm + kColAcc, ah, bh, id_acc, 1u, leader);
         mma_bf16_if(tm + kColAcc, ah, bl, id_acc, 1u, leader);
@@ -726,12 +733,11 @@ __global__ void __launch_bounds__(kBcThreads, 1)
     }
   } else {
     // ----------------------------------------------------- conversion warps
-    constexpr int NC = N / 4;  // accumulator columns of one column group
+    constexpr int NC = N / kBcGroups;   // accumulator columns of one column group
+    constexpr int PC = 64 / kBcGroups;  // columns of a 64-column panel per thread
     const int q = warp & 3, cq = warp >> 2;
     const int rr = 32 * q + lane, r = r0 + rr;
     const uint32_t tlane = tm + ((uint32_t)(32 * q) << 16);
-    unsigned char* sAh = sP;  // state A operand hi / lo (128 x 64)
-    unsigned char* sAl = sP + LT * 128;
     auto stage_hr = [&](int hh) {
       stage_rows_epi(sHR, LT, 8, 0, Lv - r0, hrow, [&](int r2) {
         return hrow + (((int64_t)b * T + t0 + r0 + r2) * H + hh) * kP;
@@ -795,6 +801,33 @@ __global__ void __launch_bounds__(kBcThreads, 1)
     // into each P buffer (mod 2); CTA-uniform
     uint32_t ph_sf = 0, ph_pe = 0, n_head = 0, gp = 0;
     float cbdot = 0.f;  // R_r . G_r (the diagonal's M factor)
+    // The end of a head (its state term's x2, the TOT fold, msum / ycs) runs
+    // once the next head's operands are staged, so the state-term MMAs overlap
+    // the next head's start.  The pending head's values:
+    int64_t pv_cv = 0;
+    float pv_x1 = 0.f, pv_pdiag = 0.f;
+    auto finish_head = [&](uint32_t nh, bool first) {
+      // warp-uniform: the TMEM accesses below are warp-collective
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_sdone, nh & 1u, status, &abort_flag));
+      fence_after_sync();
+      const float x2 = ok ? acc_dot(true, first) : pv_x1;
+      const float mpart = pv_x1 - pv_pdiag * cbdot;
+      const float ypart = x2 - pv_x1;
+      sred[cq * 128 + rr] = mpart;
+      sred[512 + cq * 128 + rr] = ypart;
+      epi_sync();
+      if (cq == 0 && r < Lv) {
+        float ms = 0.f, ys = 0.f;
+#pragma unroll
+        for (int k = 0; k < kBcGroups; ++k) {
+          ms += sred[k * 128 + rr];
+          ys += sred[512 + k * 128 + rr];
+        }
+        msum[pv_cv + r] = ms;
+        if constexpr (!REV) ycs[pv_cv + r] = ys;
+      }
+      epi_sync();  // sred reused
+    };
     for (int h = h_begin; h < h_end; ++h, ++n_head) {
       const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
       cp_async_wait<0>();  // HR, HC and a / delta of this head (and GR, GC the first time)
@@ -823,6 +856,9 @@ __global__ void __launch_bounds__(kBcThreads, 1)
       fence_async_smem();
       mbar_arrive(&bar_ops);  // this thread's staged operands are visible to the MMAs
       epi_sync();             // sa2 / sx complete
+      // the previous head's end, before this head's first P2 reaches a buffer
+      // its state term reads and before this head's first accumulate restarts HD
+      if (h > h_begin) finish_head(n_head - 1, h - 1 == h_begin);
       const float arow = REV ? sa2[r] - sx[r] : sa2[r];
       float pdiag = 0.f;  // P2 at the diagonal (this thread's row), if its columns hold it
       for (int j = 0; j < npan; ++j) {
@@ -830,8 +866,10 @@ __global__ void __launch_bounds__(kBcThreads, 1)
         mbar_wait(&bar_sfull[bs], (ph_sf >> bs) & 1u, status, &abort_flag);
         ph_sf ^= 1u << bs;
         fence_after_sync();
-        float s1[16];
-        tmem_ld16(tlane + 64 * bs + 16 * cq, s1);
+        float s1[PC];
+#pragma unroll
+        for (int k = 0; k < PC / 16; ++k)
+          tmem_ld16(tlane + 64 * bs + PC * cq + 16 * k, *reinterpret_cast<float(*)[16]>(s1 + 16 * k));
         tmem_wait_ld();
         fence_before_sync();
         __syncwarp();
@@ -840,19 +878,21 @@ __global__ void __launch_bounds__(kBcThreads, 1)
           stage_hc(h + 1);  // the head's last S1 product is done with the column operand
           cp_async_commit();
         }
+
         // P buffer bs: the accumulate of its previous panel must be done with it
         mbar_wait(&bar_pempty[bs], ((ph_pe >> bs) & 1u) ^ 1u, status, &abort_flag);
         ph_pe ^= 1u << bs;
         unsigned char* pb = sP + bs * SM::kPB;
-        {
-          // the warp's 32 rows [rw, rw + 32) against its 16 columns [cg, cg + 16):
+#pragma unroll
+        for (int qg = 0; qg < PC / 16; ++qg) {
+          // the warp's 32 rows [rw, rw + 32) against 16 columns [cg, cg + 16):
           // outside the causal triangle, strictly inside it, or across the diagonal
-          const int cg = col0 + 64 * j + 16 * cq, rw = r0 + 32 * q;
+          const int cg = col0 + 64 * j + PC * cq + 16 * qg, rw = r0 + 32 * q;
           const bool outside = REV ? cg + 15 < rw : cg > rw + 31;
           const bool inside = REV ? cg > rw + 31 : cg + 15 < rw;
 #pragma unroll
           for (int k8 = 0; k8 < 2; ++k8) {
-            const int cb = 16 * cq + 8 * k8;  // column within the panel
+            const int cb = PC * cq + 16 * qg + 8 * k8;  // column within the panel
             const uint32_t off = sw128(rr, cb / 8);
             if (outside) {
               *reinterpret_cast<uint4*>(pb + off) = make_uint4(0, 0, 0, 0);
@@ -867,7 +907,7 @@ __global__ void __launch_bounds__(kBcThreads, 1)
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const float f = REV ? ex2_approx(wv[e] - arow) : ex2_approx(arow - wv[e]);
-              v[e] = f * s1[8 * k8 + e];
+              v[e] = f * s1[16 * qg + 8 * k8 + e];
             }
             if (!inside) {
 #pragma unroll
@@ -885,23 +925,26 @@ __global__ void __launch_bounds__(kBcThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_pfull[bs]);
       }
-      // every accumulate of the head done (a commit covers all earlier MMAs)
-      {
-        const uint32_t bl = (gp + npan - 1) & 1u;
-        mbar_wait(&bar_pempty[bl], ((ph_pe >> bl) & 1u) ^ 1u, status, &abort_flag);
-      }
       gp += npan;
-      fence_after_sync();
-      const float x1 = acc_dot(false, false);
-      // state term operands: the head's state image (hi / lo panels) into P buffer 1
+      // state term operands: the head's state image (hi / lo panels) goes to the
+      // second-to-last panel's buffer as soon as its accumulate is done, the A
+      // operand to the last panel's buffer
+      const uint32_t pl = (gp - 1) & 1u, po = pl ^ 1u;
+      mbar_wait(&bar_pempty[po], ((ph_pe >> po) & 1u) ^ 1u, status, &abort_flag);
       {
         const unsigned char* img =
             simg + ((((int64_t)b * nc + c) * H + h) * (int64_t)(2 * NKP * 8192));
-        unsigned char* dst = sP + SM::kPB;
+        unsigned char* dst = sP + po * SM::kPB;
         for (int i = tid; i < 2 * NKP * 8192 / 16; i += kBcEpi)
           cp_async16(dst + 16 * i, img + 16 * i, true);
         cp_async_commit();
       }
+      // every accumulate of the head done (a commit covers all earlier MMAs)
+      mbar_wait(&bar_pempty[pl], ((ph_pe >> pl) & 1u) ^ 1u, status, &abort_flag);
+      fence_after_sync();
+      const float x1 = acc_dot(false, false);
+      unsigned char* sAh = sP + pl * SM::kPB;  // state A operand hi / lo (128 x 64)
+      unsigned char* sAl = sAh + LT * 128;
       for (int i = tid; i < LT * 8; i += kBcEpi) {
         const int r2 = i >> 3, jj = i & 7, row = r0 + r2;
         float v[8];
@@ -920,22 +963,11 @@ __global__ void __launch_bounds__(kBcThreads, 1)
         stage_hr(h + 1);
         cp_async_commit();
       }
-      // warp-uniform: the TMEM accesses below are warp-collective
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_sdone, n_head & 1u, status, &abort_flag));
-      fence_after_sync();
-      const float x2 = ok ? acc_dot(true, h == h_begin) : x1;
-      const float mpart = x1 - pdiag * cbdot;
-      const float ypart = x2 - x1;
-      sred[cq * 128 + rr] = mpart;
-      sred[512 + cq * 128 + rr] = ypart;
-      epi_sync();
-      if (cq == 0 && r < Lv) {
-        msum[cv + r] = sred[rr] + sred[128 + rr] + sred[256 + rr] + sred[384 + rr];
-        if constexpr (!REV)
-          ycs[cv + r] = sred[512 + rr] + sred[640 + rr] + sred[768 + rr] + sred[896 + rr];
-      }
-      epi_sync();  // sred reused by the next head
+      pv_cv = cv;
+      pv_x1 = x1;
+      pv_pdiag = pdiag;
     }
+    if (hb > 0) finish_head(n_head - 1, hb == 1);
     // the block's accumulated dB / dC rows
     if (!abort_flag) {  // CTA-uniform: the TMEM loads below are warp-collective
       float* o = out + (((((int64_t)b * T + t0 + r) * G + g) * nblk + kb) * N) + cq * NC;
@@ -1153,7 +1185,7 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
         w.ddir, w.qrow, w.ddiag, d.B, d.T, d.H, d.G, d.nc, per, status));
   }
   const int nblk = tc_bwd_nblk(d), hb = (d.H / d.G) / nblk;
-  const dim3 bgrid(d.nc * (L / 128), d.B, d.G * nblk);
+  const dim3 bgrid(d.nc, d.B, (L / 128) * d.G * nblk);
   float* dCout = nblk == 1 ? a.dC : w.dCp;
   float* dBout = nblk == 1 ? a.dB : w.dBp;
   {
