@@ -50,6 +50,21 @@ def dist_setup(args):
     return world, rank, local
 
 
+def aggregate_over_ranks(ms, tokens_per_rank, world, device=None):
+    """Whole-job throughput of a timed region: the slowest rank's time (max
+    over ranks) and the tokens every rank processed in it.  Returns
+    (max_ms, tokens_per_second).  With world > 1 it takes part in one
+    all-reduce on the default process group (device: where the reduced tensor
+    lives, a CUDA device under NCCL, None for CPU under gloo)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, tokens_per_rank * world / (ms / 1e3)
+
+
 def workload_config(name, scaling_note):
     from state_space_model_sm_gb300.inputs import WORKLOADS
     shape, dtype, init_std, seed, _ = WORKLOADS[name]
@@ -192,13 +207,7 @@ def run_ours(args, world, rank, local):
     if ssd.device_status() != 0:
         raise RuntimeError("device status word set during the timed region")
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = float(sum(step_ms))
-    if world > 1:
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
-    tokens = Bt * T * world * args.steps
-    value = tokens / (total_ms / 1e3)
+    total_ms, value = aggregate_over_ranks(float(sum(step_ms)), Bt * T * args.steps, world, dev)
 
     # dominant kernel and its roofline
     rd = roofline.Dims(Bt, T, H, P, N, G, L, ib=2 if dtype == "bf16" else 4, ob=4)
@@ -221,9 +230,7 @@ def run_ours(args, world, rank, local):
             kernels_out[k]["tensor_frac"] = round(r["tensor_frac"], 4)
 
     # end to end: host (pinned) buffers through the same C-ABI calls
-    e2e = None
-    if rank == 0 or world > 1:
-        e2e = run_e2e(args, inp, t, step, y, final, grads, dev)
+    e2e = run_e2e(args, inp, t, step, y, final, grads, dev, world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -309,9 +316,10 @@ def kernel_roofline(name, v, rd, peaks, roofline):
     return out
 
 
-def run_e2e(args, inp, t, step, y, final, grads, dev):
+def run_e2e(args, inp, t, step, y, final, grads, dev, world):
     """Same step through the public API with pinned host buffers: every step
-    copies its inputs host->device and reads y, final and all gradients back."""
+    copies its inputs host->device and reads y, final and all gradients back.
+    Every rank runs it; the value is whole-job tokens/s (max time over ranks)."""
     import torch
     names_in = [k for k in ("x", "dt", "dt_bias", "A", "B", "C", "D", "init", "dy")
                 if t[k] is not None]
@@ -338,9 +346,9 @@ def run_e2e(args, inp, t, step, y, final, grads, dev):
     e = torch.cuda.Event(enable_timing=True)
     e.record(stream)
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / n
-    tokens = inp.shape.batch * inp.shape.seqlen
-    return {"value": round(tokens / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+    ms, value = aggregate_over_ranks(s.elapsed_time(e) / n, inp.shape.batch * inp.shape.seqlen,
+                                     world, dev)
+    return {"value": round(value, 1), "unit": UNIT, "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
