@@ -339,7 +339,10 @@ __device__ __forceinline__ float4 fma4(float d, const float4& c, const float4& s
   return make_float4(fmaf(d, c.x, s.x), fmaf(d, c.y, s.y), fmaf(d, c.z, s.z), fmaf(d, c.w, s.w));
 }
 
-__global__ void __launch_bounds__(kThreads)
+// Three blocks per SM (registers capped) put the whole grid of the
+// workloads here in one wave; four chunks in flight per thread.
+constexpr int kPrefetchImg = 4;
+__global__ void __launch_bounds__(kThreads, 3)
     k_state_passing_img(const float4* __restrict__ S, const float* __restrict__ acs,
                         const float4* __restrict__ init, unsigned char* __restrict__ img,
                         float4* __restrict__ final_state, int N, int H, int PN8, int L, int nc) {
@@ -352,18 +355,18 @@ __global__ void __launch_bounds__(kThreads)
   const int64_t sb = ((int64_t)b * H + h) * PN8 * 2 + 2 * e;
   float4 c0 = init ? init[sb] : make_float4(0.f, 0.f, 0.f, 0.f);
   float4 c1 = init ? init[sb + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k0 = 0; k0 < nc; k0 += kPrefetch) {
-    float4 s0[kPrefetch], s1[kPrefetch];
-    float dec[kPrefetch];
+  for (int k0 = 0; k0 < nc; k0 += kPrefetchImg) {
+    float4 s0[kPrefetchImg], s1[kPrefetchImg];
+    float dec[kPrefetchImg];
 #pragma unroll
-    for (int k = 0; k < kPrefetch; ++k)
+    for (int k = 0; k < kPrefetchImg; ++k)
       if (k0 + k < nc) {
         s0[k] = S[base + (k0 + k) * step + 2 * e];
         s1[k] = S[base + (k0 + k) * step + 2 * e + 1];
         dec[k] = __expf(ab[(int64_t)(k0 + k) * L]);
       }
 #pragma unroll
-    for (int k = 0; k < kPrefetch; ++k)
+    for (int k = 0; k < kPrefetchImg; ++k)
       if (k0 + k < nc) {
         unsigned char* dst = img + (base + (k0 + k) * step) * 16;
         split8_store(dst + off, dst + off + lo_off, c0, c1);
@@ -379,7 +382,7 @@ __global__ void __launch_bounds__(kThreads)
 
 // Image-mode state passing backward: grid (nsplit = P*N/2048, H, B); reads the
 // H_c images, writes the dS_c images; dlast partials as in the float4 kernel.
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
     k_state_passing_bwd_img(const float4* __restrict__ dHs, const float* __restrict__ acs,
                             const unsigned char* __restrict__ himg,
                             const float4* __restrict__ dfinal, unsigned char* __restrict__ dsimg,
@@ -395,7 +398,7 @@ __global__ void __launch_bounds__(kThreads)
   const int64_t sb = ((int64_t)b * H + h) * PN8 * 2 + 2 * e;
   float4 g0 = (live && dfinal) ? dfinal[sb] : make_float4(0.f, 0.f, 0.f, 0.f);
   float4 g1 = (live && dfinal) ? dfinal[sb + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
-  constexpr int kPf = 4;
+  constexpr int kPf = 3;
   for (int c1 = nc - 1; c1 >= 0; c1 -= kPf) {
     float4 h0[kPf], h1[kPf], d0[kPf], d1[kPf];
     float dec[kPf];
