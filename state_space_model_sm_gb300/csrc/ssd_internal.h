@@ -41,6 +41,10 @@ class LaunchScope {
   } while (0)
 
 // ---------------------------------------------------------------- pointers
+// delta = softplus(dt + dt_bias): the linear branch above 20, where
+// log(1 + e^v) equals v in fp32.
+__device__ __forceinline__ float dt_softplus(float v) { return v > 20.f ? v : log1pf(expf(v)); }
+
 struct FwdArgs {
   const void* x;
   const void* dt;

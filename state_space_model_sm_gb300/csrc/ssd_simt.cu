@@ -36,7 +36,7 @@ __device__ __forceinline__ void stf<__nv_bfloat16>(__nv_bfloat16* p, float v) {
   *p = __float2bfloat16_rn(v);
 }
 
-__device__ __forceinline__ float softplus_f(float v) { return v > 20.f ? v : log1pf(expf(v)); }
+__device__ __forceinline__ float softplus_f(float v) { return dt_softplus(v); }
 __device__ __forceinline__ float softplus_grad_f(float v) {
   return v > 20.f ? 1.f : 1.f / (1.f + expf(-v));
 }

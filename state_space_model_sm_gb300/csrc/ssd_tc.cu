@@ -85,7 +85,8 @@ struct StateSmem {
 template <int N, int L, int MODE>
 __global__ void __launch_bounds__(256, 2)
     k_state_tc(const bf16* __restrict__ x, const bf16* __restrict__ Bm,
-               const float* __restrict__ delta, const float* __restrict__ acs,
+               const bf16* __restrict__ dt, const float* __restrict__ dt_bias,
+               const float* __restrict__ A, float* __restrict__ delta, float* __restrict__ acs,
                float* __restrict__ S, int T, int H, int G, int nc, int pairs_per_cta,
                int* status) {
   using SM = StateSmem<N, L>;
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(256, 2)
   __shared__ uint64_t bar_stage[2], bar_done;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
+  __shared__ float s_scan[8 + 2];  // per-warp totals, then a[L-1] of each head
   unsigned char* base = align1024(smem_raw);
   float* sw = reinterpret_cast<float*>(base + 2 * SM::kStage);  // [2][L]
 
@@ -139,11 +141,52 @@ __global__ void __launch_bounds__(256, 2)
 
   for (int ip = 0; ip < npairs; ++ip) {
     const int h = 2 * (pair0 + ip);
-    for (int i = tid; i < 2 * L; i += 256) {
-      const int hh = i / L, l = i % L;
-      const int64_t cv = (((int64_t)b * H + h + hh) * nc + c) * L;
-      sw[i] = MODE == 0 ? __expf(acs[cv + L - 1] - acs[cv + l]) * delta[cv + l]
-                        : __expf(acs[cv + l]);
+    if constexpr (MODE == 0) {
+      // chunk_cumsum of the pair's two heads, 128 threads per head, L/128
+      // consecutive positions per thread: delta = softplus(dt + dt_bias) (0
+      // past seqlen), a = in-chunk inclusive cumsum of delta * A; both are
+      // written for the later kernels
+      constexpr int E2 = L / 128;
+      const int hh = tid >> 7, tl = tid & 127, hd = h + hh;
+      const float bias = dt_bias ? dt_bias[hd] : 0.f, Ah = A[hd];
+      float dl[E2], al[E2], run = 0.f;
+#pragma unroll
+      for (int e = 0; e < E2; ++e) {
+        const int l = tl * E2 + e;
+        dl[e] = l < Lv ? dt_softplus(__bfloat162float(dt[((int64_t)b * T + t0 + l) * H + hd]) + bias)
+                       : 0.f;
+        run += dl[e] * Ah;
+        al[e] = run;
+      }
+      float incl = run;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (lane == 31) s_scan[warp] = incl;
+      __syncthreads();
+      float pre = incl - run;  // exclusive prefix within the warp
+      for (int k = 0; k < (warp & 3); ++k) pre += s_scan[4 * hh + k];
+      const int64_t cv = (((int64_t)b * H + hd) * nc + c) * L;
+#pragma unroll
+      for (int e = 0; e < E2; ++e) {
+        const int l = tl * E2 + e;
+        al[e] += pre;
+        delta[cv + l] = dl[e];
+        acs[cv + l] = al[e];
+      }
+      if (tl == 127) s_scan[8 + hh] = al[E2 - 1];  // a[L-1] as written
+      __syncthreads();
+      const float alast = s_scan[8 + hh];
+#pragma unroll
+      for (int e = 0; e < E2; ++e) sw[hh * L + tl * E2 + e] = __expf(alast - al[e]) * dl[e];
+    } else {
+      for (int i = tid; i < 2 * L; i += 256) {
+        const int hh = i / L, l = i % L;
+        const int64_t cv = (((int64_t)b * H + h + hh) * nc + c) * L;
+        sw[i] = __expf(acs[cv + l]);
+      }
     }
     for (int kb = 0; kb < NKB; ++kb) {
       const int st = kb & 1;
@@ -1107,8 +1150,8 @@ int pick_heads_per_cta(int hpg, int units, int sms, int target_waves) {
 template <int N, int L, typename Tout>
 cudaError_t launch_tc_forward_t(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s,
                                 int* status, int sms) {
-  simt_cumsum(d, a, w, s);
   {
+    // chunk_cumsum runs inside the chunk_state kernel
     using SM = StateSmem<N, L>;
     auto kern = k_state_tc<N, L, 0>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
@@ -1117,8 +1160,9 @@ cudaError_t launch_tc_forward_t(const Dims& d, const FwdArgs& a, const FwdWs& w,
     const dim3 grid(d.nc, d.B, (pairs_total + ppc - 1) / ppc);
     SSD_LAUNCH("k_state_tc", s,
                kern<<<grid, 256, SM::kBytes, s>>>(
-                   static_cast<const bf16*>(a.x), static_cast<const bf16*>(a.B), w.delta, w.acs,
-                   w.S, d.T, d.H, d.G, d.nc, ppc, status));
+                   static_cast<const bf16*>(a.x), static_cast<const bf16*>(a.B),
+                   static_cast<const bf16*>(a.dt), a.dt_bias, a.A, w.delta, w.acs, w.S, d.T, d.H,
+                   d.G, d.nc, ppc, status));
   }
   simt_state_passing(d, a, w, s);
   {
@@ -1155,7 +1199,6 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
   FwdArgs f = a.f;
   f.final_state = nullptr;
   FwdWs fw{w.delta, w.acs, w.S, nullptr, nullptr, w.Himg};
-  simt_cumsum(d, f, fw, s);
   using SS = StateSmem<N, L>;
   const int ppc = pick_heads_per_cta((d.H / d.G) / 2, d.B * d.nc * d.G, sms, 4);
   const dim3 sgrid(d.nc, d.B, (d.H / 2 + ppc - 1) / ppc);
@@ -1163,14 +1206,16 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     auto kern = k_state_tc<N, L, 0>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::kBytes);
     SSD_LAUNCH("k_state_tc", s, kern<<<sgrid, 256, SS::kBytes, s>>>(
-        x, Bm, w.delta, w.acs, w.S, d.T, d.H, d.G, d.nc, ppc, status));
+        x, Bm, static_cast<const bf16*>(f.dt), f.dt_bias, f.A, w.delta, w.acs, w.S, d.T, d.H,
+        d.G, d.nc, ppc, status));  // with chunk_cumsum
   }
   simt_state_passing(d, f, fw, s);
   {
     auto kern = k_state_tc<N, L, 1>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::kBytes);
     SSD_LAUNCH("k_dstates_tc", s, kern<<<sgrid, 256, SS::kBytes, s>>>(
-        dy, Cm, w.delta, w.acs, w.dHs, d.T, d.H, d.G, d.nc, ppc, status));
+        dy, Cm, nullptr, nullptr, nullptr, w.delta, w.acs, w.dHs, d.T, d.H, d.G, d.nc, ppc,
+        status));
   }
   const int nsplit = simt_state_passing_bwd(d, w.dHs, w.acs, nullptr, a.dfinal, nullptr, w.dlast,
                                             a.dinit, w.dSimg, w.Himg, s);

@@ -66,7 +66,8 @@ def kernel_bytes(name: str, d: Dims) -> int:
     nb = tc_bwd_nblk(d)
     table = {
         # tensor-core path
-        "k_state_tc": t["x"] + t["bc"] + 2 * t["vec"] + t["st"],
+        # chunk_state with chunk_cumsum inside: reads dt, writes delta and dA_cumsum
+        "k_state_tc": t["x"] + t["bc"] + t["dtb"] + 2 * t["vec"] + t["st"],
         "k_dstates_tc": t["x"] + t["bc"] + t["vec"] + t["st"],
         "k_scan_tc": t["x"] + 2 * t["bc"] + 2 * t["vec"] + t["st"] + t["y"],
         "k_scan_tc_dx": 2 * t["x"] + 2 * t["bc"] + 5 * t["vec"] + t["st"] + t["xf"],
