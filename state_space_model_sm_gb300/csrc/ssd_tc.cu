@@ -629,7 +629,7 @@ struct BcSmem {
   static constexpr int kHR = kLT * 128;
   static constexpr int kHC = L * 128;
   static constexpr int kPB = 2 * kLT * 128;  // one P buffer: 64-column panel, hi + lo
-  static constexpr int kBytes = kGR + kGC + kHR + kHC + 2 * kPB + (4 * L + 8 * 128) * 4 + 1024;
+  static constexpr int kBytes = kGR + kGC + kHR + kHC + 2 * kPB + (5 * L + 8 * 128) * 4 + 1024;
   static_assert(2 * (N / 64) * 8192 <= kPB, "state image fits one P buffer");
 };
 
@@ -681,6 +681,7 @@ __global__ void __launch_bounds__(kBcThreads, 1)
   float* sx = sa2 + L;   // dC: a*log2e - log2(delta) (+inf at delta = 0); dB: log2(delta) (-inf)
   float* sred = sx + L;  // [2][4][128]: per column group (up to 4), msum and ycs partials
   float* sraw = sred + 8 * 128;  // prefetched a [L], delta [L] of the next head
+  float* scf = sraw + 2 * L;     // column factors of the decay against 16-column group edges
 
   // row tiles with the most columns (dC: the last, dB: the first) are launched first
   const int gz = gridDim.z / NLT, zt = blockIdx.z / gz, zr = blockIdx.z % gz;
@@ -899,6 +900,15 @@ __global__ void __launch_bounds__(kBcThreads, 1)
       fence_async_smem();
       mbar_arrive(&bar_ops);  // this thread's staged operands are visible to the MMAs
       epi_sync();             // sa2 / sx complete
+      // Column factors for column groups strictly inside the causal triangle:
+      // e^{a_l - a_s} delta_s = R_row * cf_col with the group's edge column m
+      // between the rows and the columns (dC: m = last column, cf_s =
+      // 2^{a_m - a_s} delta_s, R_l = 2^{a_l - a_m}; dB: m = first column, cf_l =
+      // 2^{a_l - a_m}, R_s = 2^{a_m - a_s} delta_s).  a is monotone, so every
+      // factor is <= 1 (or <= delta) and neither can overflow.
+      for (int i = tid; i < L; i += kBcEpi)
+        scf[i] = REV ? ex2_approx(sa2[i] - sa2[i & ~15]) : ex2_approx(sa2[i | 15] - sx[i]);
+      epi_sync();
       // the previous head's end, before this head's first P2 reaches a buffer
       // its state term reads and before this head's first accumulate restarts HD
       if (h > h_begin) finish_head(n_head - 1, h - 1 == h_begin);
@@ -909,14 +919,6 @@ __global__ void __launch_bounds__(kBcThreads, 1)
         mbar_wait(&bar_sfull[bs], (ph_sf >> bs) & 1u, status, &abort_flag);
         ph_sf ^= 1u << bs;
         fence_after_sync();
-        float s1[PC];
-#pragma unroll
-        for (int k = 0; k < PC / 16; ++k)
-          tmem_ld16(tlane + 64 * bs + PC * cq + 16 * k, *reinterpret_cast<float(*)[16]>(s1 + 16 * k));
-        tmem_wait_ld();
-        fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_sempty[bs]);
         if (j == npan - 1 && h + 1 < h_end) {
           stage_hc(h + 1);  // the head's last S1 product is done with the column operand
           cp_async_commit();
@@ -933,34 +935,61 @@ __global__ void __launch_bounds__(kBcThreads, 1)
           const int cg = col0 + 64 * j + PC * cq + 16 * qg, rw = r0 + 32 * q;
           const bool outside = REV ? cg + 15 < rw : cg > rw + 31;
           const bool inside = REV ? cg > rw + 31 : cg + 15 < rw;
+          // this group's 16 columns of S1 (the buffer is released after the last)
+          float s1[16];
+          tmem_ld16(tlane + 64 * bs + PC * cq + 16 * qg, s1);
+          tmem_wait_ld();
+          if (qg == PC / 16 - 1) {
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_sempty[bs]);
+          }
+          if (outside) {
 #pragma unroll
-          for (int k8 = 0; k8 < 2; ++k8) {
-            const int cb = PC * cq + 16 * qg + 8 * k8;  // column within the panel
-            const uint32_t off = sw128(rr, cb / 8);
-            if (outside) {
+            for (int k8 = 0; k8 < 2; ++k8) {
+              const uint32_t off = sw128(rr, (PC * cq + 16 * qg + 8 * k8) / 8);
               *reinterpret_cast<uint4*>(pb + off) = make_uint4(0, 0, 0, 0);
               *reinterpret_cast<uint4*>(pb + LT * 128 + off) = make_uint4(0, 0, 0, 0);
-              continue;
             }
-            const float* colv = (REV ? sa2 : sx) + col0 + 64 * j + cb;
-            const float4 w0 = *reinterpret_cast<const float4*>(colv);
-            const float4 w1 = *reinterpret_cast<const float4*>(colv + 4);
-            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            float v[8];
+          } else if (inside) {
+            // factorized decay: one ex2 per thread and group
+            const int m = REV ? cg : cg + 15;
+            const float R = REV ? ex2_approx(sa2[m] - arow) : ex2_approx(arow - sa2[m]);
+            const float2 R2 = make_float2(R, R);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float f = REV ? ex2_approx(wv[e] - arow) : ex2_approx(arow - wv[e]);
-              v[e] = f * s1[16 * qg + 8 * k8 + e];
+            for (int k8 = 0; k8 < 2; ++k8) {
+              const int cb = PC * cq + 16 * qg + 8 * k8;  // column within the panel
+              const float4 c0 = *reinterpret_cast<const float4*>(scf + cg + 8 * k8);
+              const float4 c1 = *reinterpret_cast<const float4*>(scf + cg + 8 * k8 + 4);
+              const float* sv = s1 + 8 * k8;
+              const float2 p0 = __fmul2_rn(__fmul2_rn(R2, make_float2(c0.x, c0.y)), make_float2(sv[0], sv[1]));
+              const float2 p1 = __fmul2_rn(__fmul2_rn(R2, make_float2(c0.z, c0.w)), make_float2(sv[2], sv[3]));
+              const float2 p2 = __fmul2_rn(__fmul2_rn(R2, make_float2(c1.x, c1.y)), make_float2(sv[4], sv[5]));
+              const float2 p3 = __fmul2_rn(__fmul2_rn(R2, make_float2(c1.z, c1.w)), make_float2(sv[6], sv[7]));
+              const float v[8] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y, p3.x, p3.y};
+              const uint32_t off = sw128(rr, cb / 8);
+              store_split8(pb + off, pb + LT * 128 + off, v);
             }
-            if (!inside) {
+          } else {
+#pragma unroll
+            for (int k8 = 0; k8 < 2; ++k8) {
+              const int cb = PC * cq + 16 * qg + 8 * k8;  // column within the panel
+              const uint32_t off = sw128(rr, cb / 8);
+              const float* colv = (REV ? sa2 : sx) + col0 + 64 * j + cb;
+              const float4 w0 = *reinterpret_cast<const float4*>(colv);
+              const float4 w1 = *reinterpret_cast<const float4*>(colv + 4);
+              const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+              float v[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
+                const float f = REV ? ex2_approx(wv[e] - arow) : ex2_approx(arow - wv[e]);
                 const int cl = col0 + 64 * j + cb + e;  // chunk-local column
+                v[e] = f * s1[8 * k8 + e];
                 if (cl == r) pdiag = v[e];
                 if (REV ? cl < r : cl > r) v[e] = 0.f;
               }
+              store_split8(pb + off, pb + LT * 128 + off, v);
             }
-            store_split8(pb + off, pb + LT * 128 + off, v);
           }
         }
         fence_async_smem();

@@ -250,10 +250,13 @@ __device__ __forceinline__ float lg2_approx(float x) {
 }
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Two fp32 values -> packed bf16 pairs hi = rn(v), lo = rn(v - hi).
+// Two fp32 values -> packed bf16 pairs hi = rn(v), lo = rn(v - hi).  The
+// residual v - hi is exact in fp32; one packed fma (-hi * 1 + v) forms both.
 __device__ __forceinline__ void split2_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
   hi = pack_bf16(a, b);
-  lo = pack_bf16(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xFFFF0000u));
+  const float2 hf = make_float2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xFFFF0000u));
+  const float2 res = __ffma2_rn(hf, make_float2(-1.f, -1.f), make_float2(a, b));
+  lo = pack_bf16(res.x, res.y);
 }
 
 // Split v into two bf16 whose sum carries ~16 significant bits: hi = rn(v),
