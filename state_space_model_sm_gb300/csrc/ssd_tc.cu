@@ -290,7 +290,7 @@ struct ScanSmem {
   static constexpr int kX = L * 128;                        // per group: x or dy rows
   static constexpr int kHlo = (N / 64) * 64 * 128;          // offset of the state's lo part
   static constexpr int kImg = 2 * kHlo;                     // bytes of one state image
-  static constexpr int kBytes = kC + kBP + 2 * kX + (8 * L + 6 * 128) * 4 + 1024;
+  static constexpr int kBytes = kC + kBP + 2 * kX + (10 * L + 6 * 128) * 4 + 1024;
 };
 
 __device__ __forceinline__ void group_sync(int id) {
@@ -351,6 +351,7 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t colY = 256 + 128 * wg, colST = colY + 64;
   const int gbar = 1 + wg;
   float* sred = sAall + 8 * L + wg * 3 * 128;  // [3][128] per pipeline: half-row partial sums
+  float* scf = sAall + 8 * L + 6 * 128 + wg * L;  // per pipeline: column factors (forward)
   uint32_t n_p = 0, n_st = 0, n_done = 0, n_units = 0;
 
   for (int64_t item = it_begin; item < it_end;) {
@@ -453,6 +454,15 @@ __global__ void __launch_bounds__(512, 1)
       }
       mma_commit(&bar_st[wg]);
     }
+    // Forward: column factors for column groups strictly inside the causal
+    // triangle, e^{a_l - a_s} delta_s = R_l * cf_s with the group's last column
+    // m as reference: cf_s = 2^{a_m - a_s} delta_s, R_l = 2^{a_l - a_m}; a is
+    // monotone, so both are <= 1.  (The dx direction keeps the per-element
+    // exponential: measured faster there.)
+    if constexpr (!REV) {
+      for (int i = wtid; i < L; i += 256) scf[i] = ex2_approx(sa2[i | 15] - sx[i]);
+      group_sync(gbar);
+    }
     ++n_st;
     mbar_wait(&bar_st[wg], (n_st - 1) & 1, status, &abort_flag);  // P buffer free again
     fence_after_sync();
@@ -469,21 +479,53 @@ __global__ void __launch_bounds__(512, 1)
       for (int qg = 0; qg < 2; ++qg) {
         float(&cur)[16] = qg ? cbB : cbA;
         if (qg == 0) tmem_ld16(tlane + 64 * j + 32 * half + 16, cbB);
+        // the warp's 32 rows [rw, rw + 32) against 16 columns [cg, cg + 16):
+        // outside the causal triangle, strictly inside it, or across the diagonal
+        const int cg = col0 + 64 * j + 32 * half + 16 * qg, rw = r0 + 32 * q;
+        const bool outside = !REV && cg > rw + 31;
+        const bool inside = !REV && cg + 15 < rw;
+        if (outside) {
 #pragma unroll
-        for (int k8 = 0; k8 < 2; ++k8) {
-          const int c8 = 32 * half + 16 * qg + 8 * k8;  // panel-local column of the chunk
-          const float4 w0 = *reinterpret_cast<const float4*>(colv + c8);
-          const float4 w1 = *reinterpret_cast<const float4*>(colv + c8 + 4);
-          const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-          float v[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int cl = col0 + 64 * j + c8 + e;  // chunk-local column
-            const float f = REV ? ex2_approx(wv[e] - ar2) : ex2_approx(ar2 - wv[e]);
-            v[e] = (REV ? cl >= r : cl <= r) ? cur[8 * k8 + e] * f : 0.f;
+          for (int k8 = 0; k8 < 2; ++k8) {
+            const uint32_t off = sw128(rr, (32 * half + 16 * qg + 8 * k8) / 8);
+            *reinterpret_cast<uint4*>(Pw + off) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(Pw + LT * 128 + off) = make_uint4(0, 0, 0, 0);
           }
-          const uint32_t off = sw128(rr, c8 / 8);
-          store_split8(Pw + off, Pw + LT * 128 + off, v);
+        } else if (inside) {
+          const int m = cg + 15;
+          const float R = ex2_approx(ar2 - sa2[m]);
+          const float2 R2 = make_float2(R, R);
+#pragma unroll
+          for (int k8 = 0; k8 < 2; ++k8) {
+            const int c8 = 32 * half + 16 * qg + 8 * k8;  // panel-local column of the chunk
+            const float4 c0 = *reinterpret_cast<const float4*>(scf + cg + 8 * k8);
+            const float4 c1 = *reinterpret_cast<const float4*>(scf + cg + 8 * k8 + 4);
+            const float* sv = cur + 8 * k8;
+            const float2 p0 = __fmul2_rn(__fmul2_rn(R2, make_float2(c0.x, c0.y)), make_float2(sv[0], sv[1]));
+            const float2 p1 = __fmul2_rn(__fmul2_rn(R2, make_float2(c0.z, c0.w)), make_float2(sv[2], sv[3]));
+            const float2 p2 = __fmul2_rn(__fmul2_rn(R2, make_float2(c1.x, c1.y)), make_float2(sv[4], sv[5]));
+            const float2 p3 = __fmul2_rn(__fmul2_rn(R2, make_float2(c1.z, c1.w)), make_float2(sv[6], sv[7]));
+            const float v[8] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y, p3.x, p3.y};
+            const uint32_t off = sw128(rr, c8 / 8);
+            store_split8(Pw + off, Pw + LT * 128 + off, v);
+          }
+        } else {
+#pragma unroll
+          for (int k8 = 0; k8 < 2; ++k8) {
+            const int c8 = 32 * half + 16 * qg + 8 * k8;  // panel-local column of the chunk
+            const float4 w0 = *reinterpret_cast<const float4*>(colv + c8);
+            const float4 w1 = *reinterpret_cast<const float4*>(colv + c8 + 4);
+            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int cl = col0 + 64 * j + c8 + e;  // chunk-local column
+              const float f = REV ? ex2_approx(wv[e] - ar2) : ex2_approx(ar2 - wv[e]);
+              v[e] = (REV ? cl >= r : cl <= r) ? cur[8 * k8 + e] * f : 0.f;
+            }
+            const uint32_t off = sw128(rr, c8 / 8);
+            store_split8(Pw + off, Pw + LT * 128 + off, v);
+          }
         }
         if (qg == 0) tmem_wait_ld();
       }
