@@ -1181,11 +1181,14 @@ __global__ void __launch_bounds__(256)
 }
 
 // out[i, :] = sum_k in[i, k, :] over the nblk head-block partials, in order
-// (float4 per thread; N % 4 == 0).
-__global__ void k_block_reduce(const float4* __restrict__ in, float4* __restrict__ out,
+// (float4 per thread; N % 4 == 0); blockIdx.y picks the tensor (dC, dB).
+__global__ void k_block_reduce(const float4* __restrict__ in0, float4* __restrict__ out0,
+                               const float4* __restrict__ in1, float4* __restrict__ out1,
                                int64_t rows, int nblk, int N4) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= rows * N4) return;
+  const float4* in = blockIdx.y ? in1 : in0;
+  float4* out = blockIdx.y ? out1 : out0;
   const int64_t row = i / N4;
   const int n = (int)(i % N4);
   float4 s = in[(row * nblk) * N4 + n];
@@ -1329,9 +1332,8 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     const int64_t rows = (int64_t)d.B * d.T * d.G;
     const int N4 = d.N / 4;
     const int blocks = (int)((rows * N4 + 255) / 256);
-    SSD_LAUNCH("k_block_reduce", s, k_block_reduce<<<blocks, 256, 0, s>>>(
-        reinterpret_cast<const float4*>(w.dCp), reinterpret_cast<float4*>(a.dC), rows, nblk, N4));
-    SSD_LAUNCH("k_block_reduce", s, k_block_reduce<<<blocks, 256, 0, s>>>(
+    SSD_LAUNCH("k_block_reduce", s, k_block_reduce<<<dim3(blocks, 2), 256, 0, s>>>(
+        reinterpret_cast<const float4*>(w.dCp), reinterpret_cast<float4*>(a.dC),
         reinterpret_cast<const float4*>(w.dBp), reinterpret_cast<float4*>(a.dB), rows, nblk, N4));
   }
   simt_param_grads(d, w.part, a.dA, a.ddt_bias, a.dD, s);

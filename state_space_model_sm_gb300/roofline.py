@@ -74,7 +74,8 @@ def kernel_bytes(name: str, d: Dims) -> int:
         "k_bwd_dc_tc": 2 * t["x"] + 2 * t["bc"] + 4 * t["vec"] + t["st"] + t["bcf"] * nb,
         "k_bwd_db_tc": 2 * t["x"] + 2 * t["bc"] + 3 * t["vec"] + t["st"] + t["bcf"] * nb,
         "k_bwd_finalize_tc": t["dtb"] + 7 * t["vec"] + d.B * d.T * d.H * 4,
-        "k_block_reduce": t["bcf"] * nb + t["bcf"],
+        # dC and dB in one launch
+        "k_block_reduce": 2 * (t["bcf"] * nb + t["bcf"]),
         # forward
         "k_chunk_cumsum": t["dtb"] + 2 * t["vec"],
         "k_bmm_cb": 2 * t["bc"] + t["cb"],
