@@ -914,25 +914,28 @@ __global__ void __launch_bounds__(kBcThreads, 1)
       }
       epi_sync();  // sred reused
     };
+    {
+      // R_r . G_r once per CTA (the tile rows and column rows are staged first)
+      cp_async_wait<0>();
+      epi_sync();
+      const int rc = r - col0;  // the row of the column operand at the diagonal
+      float sdot = 0.f;
+#pragma unroll 2
+      for (int cc = 0; cc < N; cc += 8) {
+        float u[8], w[8];
+        unpack8(*reinterpret_cast<const uint4*>(sGR + (cc / 64) * (LT * 128) +
+                                                sw128(rr, (cc % 64) / 8)), u);
+        unpack8(*reinterpret_cast<const uint4*>(sGC + (cc / 64) * (L * 128) +
+                                                sw128(rc, (cc % 64) / 8)), w);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sdot = fmaf(u[e], w[e], sdot);
+      }
+      cbdot = sdot;
+    }
     for (int h = h_begin; h < h_end; ++h, ++n_head) {
       const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
-      cp_async_wait<0>();  // HR, HC and a / delta of this head (and GR, GC the first time)
+      cp_async_wait<0>();  // HR, HC and a / delta of this head
       epi_sync();
-      if (h == h_begin) {
-        const int rc = r - col0;  // the row of the column operand at the diagonal
-        float s = 0.f;
-#pragma unroll
-        for (int cc = 0; cc < N; cc += 8) {
-          float u[8], w[8];
-          unpack8(*reinterpret_cast<const uint4*>(sGR + (cc / 64) * (LT * 128) +
-                                                  sw128(rr, (cc % 64) / 8)), u);
-          unpack8(*reinterpret_cast<const uint4*>(sGC + (cc / 64) * (L * 128) +
-                                                  sw128(rc, (cc % 64) / 8)), w);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) s = fmaf(u[e], w[e], s);
-        }
-        cbdot = s;
-      }
       for (int i = tid; i < L; i += kBcEpi) {
         const float a2 = sraw[i] * kLog2e, dl = sraw[L + i];
         const float l2 = dl > 0.f ? lg2_approx(dl) : -__int_as_float(0x7f800000);
