@@ -185,11 +185,15 @@ def run_ours(args, world, rank, local):
         raise RuntimeError("device status word set during warm-up")
 
     stream = torch.cuda.current_stream(dev)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    launches0 = ssd.launch_count()
-    ssd.profile_enable(True)
-    with ClockSampler(local) as clk:
+
+    def timed_steps(profiled):
+        """K steps, each after an L2 flush and bracketed by CUDA events on the
+        launch stream; with profiled, the library also records an event pair
+        around every kernel launch (per-kernel durations for the roofline)."""
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        launches0 = ssd.launch_count()
+        ssd.profile_enable(profiled)
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
@@ -201,13 +205,20 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-    launches = ssd.launch_count() - launches0
-    prof = ssd.profile_read()
-    ssd.profile_enable(False)
-    if ssd.device_status() != 0:
-        raise RuntimeError("device status word set during the timed region")
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms, value = aggregate_over_ranks(float(sum(step_ms)), Bt * T * args.steps, world, dev)
+        prof_ = ssd.profile_read() if profiled else None
+        ssd.profile_enable(False)
+        if ssd.device_status() != 0:
+            raise RuntimeError("device status word set during the timed region")
+        return (float(sum(s.elapsed_time(e) for s, e in zip(starts, ends))),
+                ssd.launch_count() - launches0, prof_)
+
+    with ClockSampler(local) as clk:
+        # the throughput: no per-kernel instrumentation inside the timed region
+        plain_ms, launches, _ = timed_steps(False)
+        # the same K steps again with per-kernel CUDA events (roofline inputs)
+        prof_ms, _, prof = timed_steps(True)
+    total_ms, value = aggregate_over_ranks(plain_ms, Bt * T * args.steps, world, dev)
+    prof_ms, _ = aggregate_over_ranks(prof_ms, Bt * T * args.steps, world, dev)
 
     # dominant kernel and its roofline
     rd = roofline.Dims(Bt, T, H, P, N, G, L, ib=2 if dtype == "bf16" else 4, ob=4)
@@ -253,6 +264,9 @@ def run_ours(args, world, rank, local):
             "config": workload_config(args.workload, "flushed (512 MB write) before every step"),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clk.summary(), "kernels": kernels_out, "path": ssd.last_path(),
+            "profiled_ms_per_step": round(prof_ms / args.steps, 4),
+            "timing": "value: K steps without per-kernel events; kernels / roofline: the same "
+                      "K steps again with an event pair around every launch",
             "gpu": torch.cuda.get_device_name(dev),
             "step_flops_algorithmic": roofline.step_flops(rd),
         }
