@@ -1128,16 +1128,32 @@ __device__ __forceinline__ float block_exclusive_scan256(float v, float* warp_to
   return before + incl - v;
 }
 
-__global__ void __launch_bounds__(256)
-    k_bwd_finalize_tc(const bf16* __restrict__ dt, const float* __restrict__ dt_bias,
-                      const float* __restrict__ A, const float* __restrict__ delta,
-                      const float* __restrict__ rowsum, const float* __restrict__ colsum,
-                      const float* __restrict__ ycs, const float* __restrict__ qrow,
-                      const float* __restrict__ ddir, const float* __restrict__ ddiag,
-                      const float* __restrict__ dlast, int nsplit, float* __restrict__ ddt,
-                      float* __restrict__ part, int T, int H, int L, int nc) {
+struct FinalizeArgs {
+  const bf16* dt;
+  const float *dt_bias, *A, *delta, *rowsum, *colsum, *ycs, *qrow, *ddir, *ddiag, *dlast;
+  int nsplit;
+  float *ddt, *part;
+  int T, H, L, nc;
+};
+
+// One (chunk c, head h, batch b) of the finalize step; 256 threads (= L rows).
+__device__ __forceinline__ void finalize_block(const FinalizeArgs& f, int c, int h, int b) {
+  const bf16* __restrict__ dt = f.dt;
+  const float* __restrict__ dt_bias = f.dt_bias;
+  const float* __restrict__ A = f.A;
+  const float* __restrict__ delta = f.delta;
+  const float* __restrict__ rowsum = f.rowsum;
+  const float* __restrict__ colsum = f.colsum;
+  const float* __restrict__ ycs = f.ycs;
+  const float* __restrict__ qrow = f.qrow;
+  const float* __restrict__ ddir = f.ddir;
+  const float* __restrict__ ddiag = f.ddiag;
+  const float* __restrict__ dlast = f.dlast;
+  float* __restrict__ ddt = f.ddt;
+  float* __restrict__ part = f.part;
+  const int nsplit = f.nsplit, T = f.T, H = f.H, L = f.L, nc = f.nc;
   __shared__ float wt[8], red[8];
-  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, r = threadIdx.x;
+  const int r = threadIdx.x;
   const int Lv = min(L, T - c * L);
   const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
   const bool live = r < Lv;
@@ -1184,14 +1200,9 @@ __global__ void __launch_bounds__(256)
 }
 
 // out[i, :] = sum_k in[i, k, :] over the nblk head-block partials, in order
-// (float4 per thread; N % 4 == 0); blockIdx.y picks the tensor (dC, dB).
-__global__ void k_block_reduce(const float4* __restrict__ in0, float4* __restrict__ out0,
-                               const float4* __restrict__ in1, float4* __restrict__ out1,
-                               int64_t rows, int nblk, int N4) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= rows * N4) return;
-  const float4* in = blockIdx.y ? in1 : in0;
-  float4* out = blockIdx.y ? out1 : out0;
+// (float4 per element i; N % 4 == 0).
+__device__ __forceinline__ void reduce_elem(const float4* __restrict__ in, float4* __restrict__ out,
+                                            int64_t i, int nblk, int N4) {
   const int64_t row = i / N4;
   const int n = (int)(i % N4);
   float4 s = in[(row * nblk) * N4 + n];
@@ -1203,6 +1214,25 @@ __global__ void k_block_reduce(const float4* __restrict__ in0, float4* __restric
     s.w += v.w;
   }
   out[i] = s;
+}
+
+// The backward's tail in one launch of 256-thread blocks: blocks [0, nfin)
+// run the finalize step for (c, h, b) = (i % nc, (i / nc) % H, i / (nc H));
+// the rest sum the dC, then the dB head-block partials (nred blocks each).
+// The two parts are independent, so the latency-bound finalize blocks and the
+// bandwidth-bound sums share the SMs.
+__global__ void __launch_bounds__(256)
+    k_bwd_tail_tc(FinalizeArgs f, int nfin, const float4* __restrict__ dCp,
+                  float4* __restrict__ dC, const float4* __restrict__ dBp, float4* __restrict__ dB,
+                  int nred, int64_t rows, int nblk, int N4) {
+  const int blk = blockIdx.x;
+  if (blk < nfin) {
+    finalize_block(f, blk % f.nc, (blk / f.nc) % f.H, blk / (f.nc * f.H));
+    return;
+  }
+  const int rb = blk - nfin, which = rb / nred;
+  const int64_t i = (int64_t)(rb % nred) * 256 + threadIdx.x;
+  if (i < rows * N4) reduce_elem(which ? dBp : dCp, which ? dB : dC, i, nblk, N4);
 }
 
 // ------------------------------------------------------------------ launch
@@ -1328,16 +1358,18 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
         w.colsum, nullptr, d.T, d.H, d.G, d.nc, hb,
         status));
   }
-  SSD_LAUNCH("k_bwd_finalize_tc", s, k_bwd_finalize_tc<<<dim3(d.nc, d.H, d.B), 256, 0, s>>>(
-      static_cast<const bf16*>(a.f.dt), a.f.dt_bias, a.f.A, w.delta, w.rowsum, w.colsum, w.ycs,
-      w.qrow, w.ddir, w.ddiag, w.dlast, nsplit, a.ddt, w.part, d.T, d.H, d.L, d.nc));
-  if (nblk > 1) {
+  {
+    const FinalizeArgs fa{static_cast<const bf16*>(a.f.dt), a.f.dt_bias, a.f.A, w.delta,
+                          w.rowsum, w.colsum, w.ycs, w.qrow, w.ddir, w.ddiag, w.dlast, nsplit,
+                          a.ddt, w.part, d.T, d.H, d.L, d.nc};
+    const int nfin = d.nc * d.H * d.B;
     const int64_t rows = (int64_t)d.B * d.T * d.G;
     const int N4 = d.N / 4;
-    const int blocks = (int)((rows * N4 + 255) / 256);
-    SSD_LAUNCH("k_block_reduce", s, k_block_reduce<<<dim3(blocks, 2), 256, 0, s>>>(
-        reinterpret_cast<const float4*>(w.dCp), reinterpret_cast<float4*>(a.dC),
-        reinterpret_cast<const float4*>(w.dBp), reinterpret_cast<float4*>(a.dB), rows, nblk, N4));
+    const int nred = nblk > 1 ? (int)((rows * N4 + 255) / 256) : 0;
+    SSD_LAUNCH("k_bwd_tail_tc", s, k_bwd_tail_tc<<<nfin + 2 * nred, 256, 0, s>>>(
+        fa, nfin, reinterpret_cast<const float4*>(w.dCp), reinterpret_cast<float4*>(a.dC),
+        reinterpret_cast<const float4*>(w.dBp), reinterpret_cast<float4*>(a.dB),
+        nred > 0 ? nred : 1, rows, nblk, N4));
   }
   simt_param_grads(d, w.part, a.dA, a.ddt_bias, a.dD, s);
   return cudaGetLastError();
