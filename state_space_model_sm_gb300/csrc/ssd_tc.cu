@@ -78,69 +78,108 @@ struct StateSmem {
   static constexpr int kBytes = 2 * kStage + 2 * L * 4 + 1024;
 };
 
-// grid (nc, B, ceil(H / (2 * pairs))), 256 threads, two CTAs per SM.  The
-// chunk's rows stream through a two-stage ring of 64-row blocks: the
-// threads stage block k+1 (Y rows by cp.async, w X split hi / lo) while the
-// tensor core accumulates block k.
+// Persistent: about two CTAs per SM, each taking the (batch, chunk, head
+// pair) items k = blockIdx.x, blockIdx.x + gridDim.x, ... (head pair fastest,
+// so CTAs running side by side share a chunk's Y rows in L2), 256 threads.
+// The chunk's rows stream through a two-stage ring of 64-row blocks: the x
+// rows of block k+1 are loaded into registers while block k is scaled,
+// split and multiplied.  The accumulator is double-buffered in TMEM and an
+// item's result is written out after the next item's MMAs are issued, so the
+// stores of one item overlap the loads and products of the next.
 template <int N, int L, int MODE>
 __global__ void __launch_bounds__(256, 2)
     k_state_tc(const bf16* __restrict__ x, const bf16* __restrict__ Bm,
                const bf16* __restrict__ dt, const float* __restrict__ dt_bias,
                const float* __restrict__ A, float* __restrict__ delta, float* __restrict__ acs,
-               float* __restrict__ S, int T, int H, int G, int nc, int pairs_per_cta,
-               int* status) {
+               float* __restrict__ S, int T, int H, int G, int nc, int n_items, int* status) {
   using SM = StateSmem<N, L>;
   constexpr int KB = SM::kKB, NKB = L / KB;
+  static_assert(NKB % 2 == 0, "ring stages alternate across items");
+  constexpr uint32_t kTmemCols = 2 * N;  // two accumulators (128 or 256 columns)
   extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t bar_stage[2], bar_done;
+  __shared__ uint64_t bar_stage[2], bar_done[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ float s_scan[8 + 2];  // per-warp totals, then a[L-1] of each head
   unsigned char* base = align1024(smem_raw);
   float* sw = reinterpret_cast<float*>(base + 2 * SM::kStage);  // [2][L]
 
-  const int c = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int hpg = H / G;
-  const int pair0 = blockIdx.z * pairs_per_cta;
-  const int npairs = min(pairs_per_cta, H / 2 - pair0);
-  const int g = (2 * pair0) / hpg;
-  const int64_t t0 = (int64_t)c * L;
-  const int Lv = min(L, T - (int)t0);
+  const int hpg = H / G, npairs = H / 2;
+  // item -> (b, c, first head of the pair)
+  auto decode = [&](int item, int& b, int& c, int& h) {
+    const int pp = item % npairs, bc = item / npairs;
+    c = bc % nc;
+    b = bc / nc;
+    h = 2 * pp;
+  };
 
   if (tid == 0) {
     abort_flag = 0;
     mbar_init(&bar_stage[0], 1);
     mbar_init(&bar_stage[1], 1);
-    mbar_init(&bar_done, 1);
+    mbar_init(&bar_done[0], 1);
+    mbar_init(&bar_done[1], 1);
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(&tmem_base, 128);
+  if (warp == 0) tmem_alloc(&tmem_base, kTmemCols);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tm = tmem_base;
   constexpr uint32_t idesc = idesc_bf16(128, N, 1, 1);
-  uint32_t n_stage0 = 0, n_stage1 = 0, n_done = 0;
+  uint32_t n_stage0 = 0, n_stage1 = 0;
 
-  // X rows (both heads of a pair, 256 contiguous bytes per row) of a 64-row
-  // block go through registers; the next block's rows are loaded while the
-  // current block is scaled, split and multiplied.
+  // a block's X rows (both heads of a pair, 256 contiguous bytes per row) go
+  // through registers one block ahead
   constexpr int kPer = KB * 16 / 256;
-  auto load_block = [&](uint4 (&u)[kPer], int hp, int l0) {
+  auto load_block = [&](uint4 (&u)[kPer], int bb, int cc, int hp, int l0) {
+    const int64_t t0 = (int64_t)cc * L;
+    const int Lv = min(L, T - (int)t0);
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       const int i = tid + k * 256, l = l0 + (i >> 4), j = i & 15;
-      u[k] = l < Lv ? *reinterpret_cast<const uint4*>(x + (((int64_t)b * T + t0 + l) * H + hp) *
+      u[k] = l < Lv ? *reinterpret_cast<const uint4*>(x + (((int64_t)bb * T + t0 + l) * H + hp) *
                                                               kP + j * 8)
                     : make_uint4(0, 0, 0, 0);
     }
   };
-  uint4 u[kPer], un[kPer];
-  if (npairs > 0) load_block(u, 2 * pair0, 0);
+  // the result of an item from TMEM buffer buf: rows m = 64 hh + p of the pair
+  auto epilogue = [&](int bb, int cc, int hp, uint32_t buf, uint32_t parity) {
+    const bool ok =
+        __all_sync(0xffffffffu, mbar_wait(&bar_done[buf], parity, status, &abort_flag));
+    fence_after_sync();
+    if (ok) {
+      const int q = warp & 3, half = warp >> 2;
+      const int m = 32 * q + lane, hh = m >> 6, p = m & 63;
+      float* out = S + ((((int64_t)bb * nc + cc) * H + hp + hh) * kP + p) * N;
+      const uint32_t ta = tm + buf * N + ((uint32_t)(32 * q) << 16);
+#pragma unroll
+      for (int c0 = half * (N / 2); c0 < (half + 1) * (N / 2); c0 += 16) {
+        float v[16];
+        tmem_ld16(ta + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 16; k += 4)
+          *reinterpret_cast<float4*>(out + c0 + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+      }
+    }
+    fence_before_sync();  // the buffer's next accumulate comes after the next __syncthreads
+  };
 
-  for (int ip = 0; ip < npairs; ++ip) {
-    const int h = 2 * (pair0 + ip);
+  uint4 u[kPer], un[kPer];
+  int b = 0, c = 0, h = 0;
+  if ((int)blockIdx.x < n_items) {
+    decode(blockIdx.x, b, c, h);
+    load_block(u, b, c, h, 0);
+  }
+  int pb = 0, pc = 0, ph = 0;  // the previous item, written out one item late
+  int k = 0;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++k) {
+    const int g = h / hpg;
+    const int64_t t0 = (int64_t)c * L;
+    const int Lv = min(L, T - (int)t0);
+    const uint32_t buf = k & 1;
     if constexpr (MODE == 0) {
       // chunk_cumsum of the pair's two heads, 128 threads per head, L/128
       // consecutive positions per thread: delta = softplus(dt + dt_bias) (0
@@ -164,10 +203,11 @@ __global__ void __launch_bounds__(256, 2)
         const float o = __shfl_up_sync(0xffffffffu, incl, off);
         if (lane >= off) incl += o;
       }
+      __syncthreads();  // s_scan and sw of the previous item are no longer read
       if (lane == 31) s_scan[warp] = incl;
       __syncthreads();
       float pre = incl - run;  // exclusive prefix within the warp
-      for (int k = 0; k < (warp & 3); ++k) pre += s_scan[4 * hh + k];
+      for (int kk = 0; kk < (warp & 3); ++kk) pre += s_scan[4 * hh + kk];
       const int64_t cv = (((int64_t)b * H + hd) * nc + c) * L;
 #pragma unroll
       for (int e = 0; e < E2; ++e) {
@@ -182,21 +222,25 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
       for (int e = 0; e < E2; ++e) sw[hh * L + tl * E2 + e] = __expf(alast - al[e]) * dl[e];
     } else {
+      __syncthreads();  // sw of the previous item is no longer read
       for (int i = tid; i < 2 * L; i += 256) {
         const int hh = i / L, l = i % L;
         const int64_t cv = (((int64_t)b * H + h + hh) * nc + c) * L;
         sw[i] = __expf(acs[cv + l]);
       }
     }
+    // the next item (its first block's X rows are loaded during the last block)
+    int nb = b, ncn = c, nh = h;
+    const bool has_next = item + (int)gridDim.x < n_items;
+    if (has_next) decode(item + gridDim.x, nb, ncn, nh);
     for (int kb = 0; kb < NKB; ++kb) {
       const int st = kb & 1;
       unsigned char* sB = base + st * SM::kStage;
       unsigned char* sXh = sB + SM::kB;
       unsigned char* sXl = sXh + SM::kX;
       const int l0 = kb * KB;
-      // next block's X rows (or the next pair's first block) start loading now
-      if (kb + 1 < NKB) load_block(un, h, l0 + KB);
-      else if (ip + 1 < npairs) load_block(un, h + 2, 0);
+      if (kb + 1 < NKB) load_block(un, b, c, h, l0 + KB);
+      else if (has_next) load_block(un, nb, ncn, nh, 0);
       // the stage is free once the MMAs that read it (two blocks ago) are done
       const uint32_t ns = st ? n_stage1 : n_stage0;
       if (ns > 0) mbar_wait(&bar_stage[st], (ns - 1) & 1, status, &abort_flag);
@@ -206,10 +250,10 @@ __global__ void __launch_bounds__(256, 2)
       cp_async_commit();
       if (kb == 0) __syncthreads();  // sw ready
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int i = tid + k * 256, lr = i >> 4, j = i & 15, hh = j >> 3;
+      for (int kk = 0; kk < kPer; ++kk) {
+        const int i = tid + kk * 256, lr = i >> 4, j = i & 15, hh = j >> 3;
         float v[8];
-        unpack8(u[k], v);
+        unpack8(u[kk], v);
         const float wl = sw[hh * L + l0 + lr];
 #pragma unroll
         for (int q = 0; q < 8; ++q) v[q] *= wl;
@@ -217,7 +261,7 @@ __global__ void __launch_bounds__(256, 2)
         store_split8(sXh + off, sXl + off, v);
       }
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) u[k] = un[k];
+      for (int kk = 0; kk < kPer; ++kk) u[kk] = un[kk];
       cp_async_wait<0>();
       fence_async_smem();
       fence_before_sync();
@@ -227,38 +271,29 @@ __global__ void __launch_bounds__(256, 2)
         for (int ks = 0; ks < KB / 16; ++ks) {
           const uint64_t bd = sdesc(smem_u32(sB) + ks * 2048, SM::kPanel, 1024);
           const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
-          mma_bf16(tm, sdesc(smem_u32(sXh) + ks * 2048, SM::kPanel, 1024), bd, idesc, acc);
-          mma_bf16(tm, sdesc(smem_u32(sXl) + ks * 2048, SM::kPanel, 1024), bd, idesc, 1u);
+          mma_bf16(tm + buf * N, sdesc(smem_u32(sXh) + ks * 2048, SM::kPanel, 1024), bd, idesc,
+                   acc);
+          mma_bf16(tm + buf * N, sdesc(smem_u32(sXl) + ks * 2048, SM::kPanel, 1024), bd, idesc,
+                   1u);
         }
         mma_commit(&bar_stage[st]);
-        if (kb == NKB - 1) mma_commit(&bar_done);
+        if (kb == NKB - 1) mma_commit(&bar_done[buf]);
       }
       if (st) ++n_stage1;
       else ++n_stage0;
     }
-    ++n_done;
-    const bool ok = mbar_wait(&bar_done, (n_done - 1) & 1, status, &abort_flag);
-    fence_after_sync();
-    if (ok) {
-      // lanes 32 q .. 32 q + 31 = rows m; warps q and q + 4 split the N columns
-      const int q = warp & 3, half = warp >> 2;
-      const int m = 32 * q + lane, hh = m >> 6, p = m & 63;
-      float* out = S + ((((int64_t)b * nc + c) * H + h + hh) * kP + p) * N;
-      const uint32_t ta = tm + ((uint32_t)(32 * q) << 16);
-#pragma unroll
-      for (int c0 = half * (N / 2); c0 < (half + 1) * (N / 2); c0 += 16) {
-        float v[16];
-        tmem_ld16(ta + c0, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 16; k += 4)
-          *reinterpret_cast<float4*>(out + c0 + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
-      }
-    }
-    fence_before_sync();
-    __syncthreads();  // accumulator and sw are reused by the next pair
+    // the previous item's result, while this item's products run
+    if (k > 0) epilogue(pb, pc, ph, buf ^ 1u, ((k - 1) >> 1) & 1u);
+    pb = b;
+    pc = c;
+    ph = h;
+    b = nb;
+    c = ncn;
+    h = nh;
   }
-  if (warp == 0) tmem_dealloc(tm, 128);
+  if (k > 0) epilogue(pb, pc, ph, (k - 1) & 1u, ((k - 1) >> 1) & 1u);
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tm, kTmemCols);
 }
 
 // ================================================================ chunk_scan
@@ -1246,14 +1281,6 @@ void scan_partition(const Dims& d, int sms, int* grid, int* per) {
   *grid = (int)((items + *per - 1) / *per);
 }
 
-int pick_heads_per_cta(int hpg, int units, int sms, int target_waves) {
-  // largest divisor of hpg that still gives >= target_waves * sms CTAs
-  int best = 1;
-  for (int d = 1; d <= hpg; ++d)
-    if (hpg % d == 0 && (int64_t)units * (hpg / d) * 1 >= (int64_t)target_waves * sms) best = d;
-  return best;
-}
-
 template <int N, int L, typename Tout>
 cudaError_t launch_tc_forward_t(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s,
                                 int* status, int sms) {
@@ -1262,14 +1289,13 @@ cudaError_t launch_tc_forward_t(const Dims& d, const FwdArgs& a, const FwdWs& w,
     using SM = StateSmem<N, L>;
     auto kern = k_state_tc<N, L, 0>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
-    const int pairs_total = d.H / 2;
-    const int ppc = pick_heads_per_cta((d.H / d.G) / 2, d.B * d.nc * d.G, sms, 4);
-    const dim3 grid(d.nc, d.B, (pairs_total + ppc - 1) / ppc);
+    const int n_items = d.B * d.nc * (d.H / 2);
+    const dim3 grid(std::min(n_items, 2 * sms));
     SSD_LAUNCH("k_state_tc", s,
                kern<<<grid, 256, SM::kBytes, s>>>(
                    static_cast<const bf16*>(a.x), static_cast<const bf16*>(a.B),
                    static_cast<const bf16*>(a.dt), a.dt_bias, a.A, w.delta, w.acs, w.S, d.T, d.H,
-                   d.G, d.nc, ppc, status));
+                   d.G, d.nc, n_items, status));
   }
   simt_state_passing(d, a, w, s);
   {
@@ -1307,21 +1333,21 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
   f.final_state = nullptr;
   FwdWs fw{w.delta, w.acs, w.S, nullptr, nullptr, w.Himg};
   using SS = StateSmem<N, L>;
-  const int ppc = pick_heads_per_cta((d.H / d.G) / 2, d.B * d.nc * d.G, sms, 4);
-  const dim3 sgrid(d.nc, d.B, (d.H / 2 + ppc - 1) / ppc);
+  const int n_items = d.B * d.nc * (d.H / 2);
+  const dim3 sgrid(std::min(n_items, 2 * sms));
   {
     auto kern = k_state_tc<N, L, 0>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::kBytes);
     SSD_LAUNCH("k_state_tc", s, kern<<<sgrid, 256, SS::kBytes, s>>>(
         x, Bm, static_cast<const bf16*>(f.dt), f.dt_bias, f.A, w.delta, w.acs, w.S, d.T, d.H,
-        d.G, d.nc, ppc, status));  // with chunk_cumsum
+        d.G, d.nc, n_items, status));  // with chunk_cumsum
   }
   simt_state_passing(d, f, fw, s);
   {
     auto kern = k_state_tc<N, L, 1>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::kBytes);
     SSD_LAUNCH("k_dstates_tc", s, kern<<<sgrid, 256, SS::kBytes, s>>>(
-        dy, Cm, nullptr, nullptr, nullptr, w.delta, w.acs, w.dHs, d.T, d.H, d.G, d.nc, ppc,
+        dy, Cm, nullptr, nullptr, nullptr, w.delta, w.acs, w.dHs, d.T, d.H, d.G, d.nc, n_items,
         status));
   }
   const int nsplit = simt_state_passing_bwd(d, w.dHs, w.acs, nullptr, a.dfinal, nullptr, w.dlast,
