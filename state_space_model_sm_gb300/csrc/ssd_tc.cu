@@ -167,11 +167,24 @@ __global__ void __launch_bounds__(256, 2)
     fence_before_sync();  // the buffer's next accumulate comes after the next __syncthreads
   };
 
+  // a block's Y rows by cp.async into ring stage st (one commit group)
+  auto stage_y = [&](int st, int bb, int cc, int gg, int l0) {
+    const int64_t t0 = (int64_t)cc * L;
+    const int Lv = min(L, T - (int)t0);
+    stage_rows_async(base + st * SM::kStage, KB, N / 8, SM::kPanel, Lv - l0, Bm, [&](int l) {
+      return Bm + (((int64_t)bb * T + t0 + l0 + l) * G + gg) * N;
+    });
+    cp_async_commit();
+  };
+
   uint4 u[kPer], un[kPer];
   int b = 0, c = 0, h = 0;
   if ((int)blockIdx.x < n_items) {
     decode(blockIdx.x, b, c, h);
     load_block(u, b, c, h, 0);
+    stage_y(0, b, c, h / hpg, 0);  // the first block's Y rows, one block ahead
+  } else {
+    cp_async_commit();
   }
   int pb = 0, pc = 0, ph = 0;  // the previous item, written out one item late
   int k = 0;
@@ -241,13 +254,10 @@ __global__ void __launch_bounds__(256, 2)
       const int l0 = kb * KB;
       if (kb + 1 < NKB) load_block(un, b, c, h, l0 + KB);
       else if (has_next) load_block(un, nb, ncn, nh, 0);
-      // the stage is free once the MMAs that read it (two blocks ago) are done
+      // the stage's X part is free once the MMAs that read it (two blocks ago)
+      // are done; its Y rows were staged during the previous block
       const uint32_t ns = st ? n_stage1 : n_stage0;
       if (ns > 0) mbar_wait(&bar_stage[st], (ns - 1) & 1, status, &abort_flag);
-      stage_rows_async(sB, KB, N / 8, SM::kPanel, Lv - l0, Bm, [&](int l) {
-        return Bm + (((int64_t)b * T + t0 + l0 + l) * G + g) * N;
-      });
-      cp_async_commit();
       if (kb == 0) __syncthreads();  // sw ready
 #pragma unroll
       for (int kk = 0; kk < kPer; ++kk) {
@@ -262,7 +272,16 @@ __global__ void __launch_bounds__(256, 2)
       }
 #pragma unroll
       for (int kk = 0; kk < kPer; ++kk) u[kk] = un[kk];
-      cp_async_wait<0>();
+      // the next block's Y rows (or the next item's first) into the other
+      // stage, once the MMAs of the previous block have read it
+      {
+        const uint32_t no = st ? n_stage0 : n_stage1;
+        if (no > 0) mbar_wait(&bar_stage[st ^ 1], (no - 1) & 1, status, &abort_flag);
+        if (kb + 1 < NKB) stage_y(st ^ 1, b, c, g, l0 + KB);
+        else if (has_next) stage_y(st ^ 1, nb, ncn, nh / hpg, 0);
+        else cp_async_commit();
+      }
+      cp_async_wait<1>();  // this block's Y rows (the next block's may still fly)
       fence_async_smem();
       fence_before_sync();
       __syncthreads();
