@@ -1,5 +1,6 @@
-// tcgen05 tensor-core kernels of the SSD forward (bf16 inputs, headdim 64,
-// d_state 64 or 128, chunk 128 or 256): chunk_state and chunk_scan.
+// tcgen05 tensor-core kernels of the SSD forward and backward (bf16 inputs,
+// headdim 64, d_state 64 or 128, chunk 128 or 256): chunk_state (with
+// chunk_cumsum) / dstates, chunk_scan / dx, dB / dC and the backward's tail.
 //
 // Precision: operands that the method forms in fp32 before a contraction
 // (the decay-weighted x of chunk_state, the masked decay-weighted C.B^T of
@@ -61,8 +62,7 @@ __device__ __forceinline__ void stage_rows_async(unsigned char* dst, int rows, i
 }
 
 // =============================================================== chunk_state
-// grid (nc, B, ceil(H / (2 * pairs))), 256 threads.  For a head pair (h, h+1)
-// of one group and chunk c:
+// For a head pair (h, h+1) of one group and chunk c:
 //   D[m = 64 hh + p, n] = sum_l w_hh[l] X[l, h+hh, p] Y[l, n]  ->  out[b, c, h+hh, p, n]
 //   MODE 0 (chunk_state): X = x,  Y = B, w = exp(a_last - a_l) delta_l  (S_c)
 //   MODE 1 (dstates):     X = dy, Y = C, w = exp(a_l)                   (dHs_c)
@@ -329,11 +329,11 @@ __global__ void __launch_bounds__(256, 2)
 //               u_s = Y + e^{a_last - a_s} ST;  dx_s = delta_s u_s + D dy_s
 //               ddir_s = <x_s, u_s>,  qrow_s = delta_s <x_s, e^{a_last - a_s} ST>,
 //               ddiag_s = <x_s, dy_s>
-// grid (nc * L/128, B, ceil(H / heads_per_cta)), 256 threads; the heads of a
-// CTA belong to one group.  After the shared score tile, the two warpgroups
-// run independent pipelines on alternate heads (own TMEM accumulators, P
-// buffer, operand rows and mbarriers), so one group's loads and waits overlap
-// the other's work.
+// Persistent, one CTA (512 threads) per SM over a balanced range of (batch,
+// chunk, 128-row tile, group) x head items.  Per unit the score tile is
+// formed once; then the two 8-warp pipelines run independent chains on
+// alternate heads (own TMEM accumulators, P buffer, operand rows and
+// mbarriers), so one pipeline's loads and waits overlap the other's work.
 template <int N, int L>
 struct ScanSmem {
   static constexpr int kLT = 128;

@@ -73,12 +73,9 @@ def kernel_bytes(name: str, d: Dims) -> int:
         "k_scan_tc_dx": 2 * t["x"] + 2 * t["bc"] + 5 * t["vec"] + t["st"] + t["xf"],
         "k_bwd_dc_tc": 2 * t["x"] + 2 * t["bc"] + 4 * t["vec"] + t["st"] + t["bcf"] * nb,
         "k_bwd_db_tc": 2 * t["x"] + 2 * t["bc"] + 3 * t["vec"] + t["st"] + t["bcf"] * nb,
-        "k_bwd_finalize_tc": t["dtb"] + 7 * t["vec"] + d.B * d.T * d.H * 4,
-        # finalize + the dC / dB head-block sums in one launch
+        # ddA / ddt finalize + the dC / dB head-block sums in one launch
         "k_bwd_tail_tc": (t["dtb"] + 7 * t["vec"] + d.B * d.T * d.H * 4
                           + (2 * (t["bcf"] * nb + t["bcf"]) if nb > 1 else 0)),
-        # dC and dB in one launch
-        "k_block_reduce": 2 * (t["bcf"] * nb + t["bcf"]),
         # forward
         "k_chunk_cumsum": t["dtb"] + 2 * t["vec"],
         "k_bmm_cb": 2 * t["bc"] + t["cb"],

@@ -10,7 +10,7 @@ import pytest
 import oracle
 from oracle import chunked
 from parity_util import assert_close, stats, to_np
-from state_space_model_sm_gb300.inputs import SSDShape, make_inputs, make_workload, to_torch
+from state_space_model_sm_gb300.inputs import WORKLOADS, SSDShape, make_inputs, make_workload, to_torch
 
 pytestmark = pytest.mark.gpu
 
@@ -170,6 +170,20 @@ def test_forward_backward_workload(cuda_lib):
     ref = oracle_bwd(inp)
     for k in ["dx", "ddt", "dA", "dB", "dC", "dD", "ddt_bias"]:
         s = assert_close(k, g[k], ref[k], "bf16")
+        print(k, s)
+
+
+def test_forward_backward_hybrid_shape(cuda_lib):
+    """The backward at the hybrid-model shape (batch 2, seqlen 8192, 64 heads in
+    8 groups, chunk 128) with nonzero initial states and a final-state
+    gradient: the group sums of dB / dC over 8 heads each and dinit."""
+    shape, dtype, init_std, seed, _ = WORKLOADS["hybrid_bf16"]
+    inp = make_inputs(shape, seed=seed + 100, dtype=dtype, init_std=init_std, with_dy=True,
+                      dfinal_std=0.5)
+    g = run_bwd(cuda_lib, inp)
+    ref = oracle_bwd(inp)
+    for k in ["dx", "ddt", "dA", "dB", "dC", "dD", "ddt_bias", "dinit"]:
+        s = assert_close(k, g["dinit_states"] if k == "dinit" else g[k], ref[k], "bf16")
         print(k, s)
 
 
