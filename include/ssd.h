@@ -151,6 +151,37 @@ int ssd_fwd_noalloc(const ssd_shape* shape, const void* x, const void* dt, const
                     const float* init_states, void* y, float* final_states, void* stream);
 size_t ssd_noalloc_scratch_bytes(void);
 
+/* Context (sequence) parallelism.  With the sequence split into contiguous
+ * segments r = 0 .. R-1, one per rank, the recurrence maps a segment's
+ * incoming state affinely, H_out(r) = D_r * H_in(r) + F_r, where F_r is the
+ * segment's final state from a zero initial state and D_r its total decay
+ * (the recurrence of "Mamba-2 offers a different scaling path", taken over
+ * the whole segment; the pages name sequence sharding as future work in
+ * "Closing thoughts").  Rank r's incoming state is an exclusive scan of these
+ * maps over the ranks before it; the gradient of its outgoing state is the
+ * same scan over the ranks after it, applied to the initial-state gradients.
+ *
+ * ssd_segment_decay: decay[b, h] = exp(A[h] * sum_t softplus(dt[b,t,h] +
+ * dt_bias[h])) over the shape's seqlen (the sum in fp64).  Uses shape->batch,
+ * seqlen, nheads and in_dtype (dt's dtype); dt (B, T, H), dt_bias (H) or
+ * NULL, A (H), decay (B, H) f32, device memory.  Asynchronous on `stream`.
+ * Returns SSD_ERR_INVALID_ARG for a NULL required pointer or a bad shape. */
+int ssd_segment_decay(const ssd_shape* shape, const void* dt, const float* dt_bias,
+                      const float* A, float* decay, void* stream);
+
+/* ssd_state_scan: out = the exclusive scan of the maps S -> D_k * S + S_k
+ * for rank `rank` of `nranks`: direction 0 runs over k = 0 .. rank-1
+ * (incoming state; S_0 is rank 0's final state with its own initial state),
+ * direction 1 over k = nranks-1 .. rank+1 (gradient of the outgoing state;
+ * S_{R-1} is the last rank's initial-state gradient with the caller's
+ * final-state gradient).  decays (nranks, bh) f32, states (nranks, bh, pn)
+ * f32, out (bh, pn) f32, device memory; bh = batch * nheads, pn = headdim *
+ * dstate.  Asynchronous on `stream`.  Returns SSD_ERR_INVALID_ARG for a rank
+ * outside [0, nranks), a direction other than 0 / 1, empty sizes or a NULL
+ * pointer. */
+int ssd_state_scan(int nranks, int rank, int direction, int64_t bh, int64_t pn,
+                   const float* decays, const float* states, float* out, void* stream);
+
 /* Diagnostic: one tcgen05 tile product on the current device,
  * D[128][nn] = A[128][k] * B[nn][k]^T (A, B bf16 row-major, D f32 row-major,
  * all device memory), with A and B staged in shared memory K-major (0) or

@@ -185,6 +185,52 @@ def ssd_bwd(x, dt, dt_bias, A, B, C, D, chunk_size: int, init_states, dy, dfinal
     return out
 
 
+def segment_decay(dt, dt_bias, A):
+    """decay (b, h) = exp(A[h] * sum_t softplus(dt[b, t, h] + dt_bias[h])) over
+    the whole of dt's sequence: the factor by which a state entering this
+    segment is carried to its end (context parallelism, ``ssd_segment_decay``)."""
+    torch = _torch()
+    lib = _native.load()
+    if dt.dim() != 3:
+        raise ValueError("dt: expected (batch, seqlen, nheads)")
+    Bt, T, H = dt.shape
+    _check(A, "A", (H,), torch.float32, dt.device)
+    _check(dt_bias, "dt_bias", (H,), torch.float32, dt.device)
+    dt = dt.contiguous()
+    out = torch.empty((Bt, H), dtype=torch.float32, device=dt.device)
+    shape = make_shape(Bt, T, H, 1, 1, 1, 1, _dtype_code(dt.dtype), SSD_F32)
+    stream = torch.cuda.current_stream(dt.device).cuda_stream
+    st = lib.ssd_segment_decay(ctypes.byref(shape), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(out),
+                               ctypes.c_void_p(stream))
+    if st != 0:
+        raise SSDError("ssd_segment_decay", st)
+    return out
+
+
+def state_scan(decays, states, rank: int, direction: int):
+    """Exclusive scan over ranks of S -> D_k * S + S_k (``ssd_state_scan``):
+    decays (R, b, h), states (R, b, h, p, n) float32 -> (b, h, p, n) for
+    ``rank``; direction 0 over the ranks before it (incoming state),
+    1 over the ranks after it (gradient of the outgoing state)."""
+    torch = _torch()
+    lib = _native.load()
+    R = decays.shape[0]
+    if states.dim() != 5 or states.shape[0] != R or tuple(decays.shape) != tuple(states.shape[:3]):
+        raise ValueError("state_scan: expected decays (R, b, h) and states (R, b, h, p, n)")
+    if decays.dtype != torch.float32 or states.dtype != torch.float32:
+        raise TypeError("state_scan: float32 tensors expected")
+    decays, states = decays.contiguous(), states.contiguous()
+    bh = states.shape[1] * states.shape[2]
+    pn = states.shape[3] * states.shape[4]
+    out = torch.empty(states.shape[1:], dtype=torch.float32, device=states.device)
+    stream = torch.cuda.current_stream(states.device).cuda_stream
+    st = lib.ssd_state_scan(int(R), int(rank), int(direction), int(bh), int(pn), _ptr(decays),
+                            _ptr(states), _ptr(out), ctypes.c_void_p(stream))
+    if st != 0:
+        raise SSDError("ssd_state_scan", st)
+    return out
+
+
 def device_status(stream=None) -> int:
     """Synchronise and read/clear the library's device status word."""
     torch = _torch()

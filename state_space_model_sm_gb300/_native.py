@@ -111,6 +111,9 @@ SIGNATURES = {
     "ssd_selftest_timeout": ([_VP], ctypes.c_int),
     "ssd_fwd_noalloc": ([_SP] + [_VP] * 10 + [_VP], ctypes.c_int),
     "ssd_noalloc_scratch_bytes": ([], ctypes.c_size_t),
+    "ssd_segment_decay": ([_SP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "ssd_state_scan": ([ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                        _VP, _VP, _VP, _VP], ctypes.c_int),
 }
 
 _lock = threading.Lock()
