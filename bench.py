@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--context-parallel", type=int, default=0, metavar="R",
+                    help="time each rank's share of an R-way sequence split (one GPU)")
     return ap.parse_args()
 
 
@@ -474,11 +476,107 @@ def run_reference(args, world, rank):
                 "d2h_bytes_per_step": 0}}))
 
 
+class _StandInComm:
+    """The exchange of one rank of an R-way split, stood in for on one GPU:
+    the all-gather stacks R copies of the rank's own tensor and the
+    all-reduce scales by R (same shapes and device copies, no transfer)."""
+
+    def __init__(self, rank, world):
+        self.rank, self.world = rank, world
+
+    def allgather(self, t):
+        import torch
+        return torch.stack([t] * self.world)
+
+    def allreduce_sum(self, t):
+        return t.mul_(self.world)
+
+
+def run_context_parallel(args):
+    """Per-rank step time of the context-parallel path (forward + backward
+    over one segment of an R-way split of the workload's sequence), each rank
+    role timed in turn on this GPU; the job's step time is the slowest
+    rank's.  The exchange (two all-gathers of b*h*p*n floats and one of b*h,
+    plus three (h,) all-reduces per step) is stood in for by local copies."""
+    import torch
+
+    import state_space_model_sm_gb300 as ssd
+    from state_space_model_sm_gb300 import context
+    from state_space_model_sm_gb300.inputs import WORKLOADS, make_inputs, to_torch
+
+    R = args.context_parallel
+    dev = torch.device("cuda", 0)
+    ssd.build()
+    ssd.load_library()
+    shape, dtype, init_std, seed, _ = WORKLOADS[args.workload]
+    inp = make_inputs(shape, seed=seed, dtype=dtype, init_std=init_std, with_dy=True)
+    t = to_torch(inp, dev)
+    Bt, T, L = shape.batch, shape.seqlen, shape.chunk_size
+    sizes = context.split_sizes(T, R, L)
+    bounds = [0]
+    for n in sizes:
+        bounds.append(bounds[-1] + n)
+    eng = context.LibraryEngine(L)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    per_rank = []
+    launches0 = ssd.launch_count()
+    with ClockSampler(0) as clk:
+        for r in range(R):
+            lo, hi = bounds[r], bounds[r + 1]
+            seg = {k: (t[k][:, lo:hi].contiguous() if k in ("x", "dt", "B", "C") else t[k])
+                   for k in ("x", "dt", "dt_bias", "A", "B", "C", "D")}
+            dy = t["dy"][:, lo:hi].contiguous()
+            comm = _StandInComm(r, R)
+
+            def step():
+                _, _, h_in = context.cp_forward(eng, comm, seg, t["init"] if r == 0 else None)
+                context.cp_backward(eng, comm, seg, h_in, dy, None)
+
+            for _ in range(args.warmup):
+                step()
+            torch.cuda.synchronize()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            for s0, s1 in ev:
+                flush.fill_(1.0)
+                s0.record(stream)
+                step()
+                s1.record(stream)
+            torch.cuda.synchronize()
+            per_rank.append(sum(a.elapsed_time(b) for a, b in ev) / args.steps)
+    if ssd.device_status() != 0:
+        raise RuntimeError("device status word set during the timed region")
+    launches = ssd.launch_count() - launches0
+    ms = max(per_rank)
+    out = {
+        "metric": METRIC, "impl": "ours", "context_parallel": R,
+        "value": round(Bt * T / (ms / 1e3), 1), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None, "dtype": "bf16 in / f32 accum+grads",
+        "data": "synthetic (seeded PCG64, workload distributions)",
+        "config": dict(workload_config(args.workload, "flushed (512 MB write) before every step"),
+                       segments=sizes),
+        "per_rank_ms": [round(v, 4) for v in per_rank],
+        "projection": f"value = tokens of the whole sequence over the slowest of the {R} rank "
+                      "roles, each timed alone on this GPU; the exchange is stood in for by "
+                      "local stacks of the same size (no inter-GPU transfer timed)",
+        "gpu_launches": launches, "clocks": clk.summary(),
+        "gpu": torch.cuda.get_device_name(dev),
+    }
+    print(json.dumps(out))
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if args.context_parallel:
+        if world > 1:
+            raise SystemExit("--context-parallel times rank roles on one GPU; run it without torchrun")
+        run_context_parallel(args)
         return
     if world > 1:
         import torch

@@ -182,6 +182,30 @@ int ssd_segment_decay(const ssd_shape* shape, const void* dt, const float* dt_bi
 int ssd_state_scan(int nranks, int rank, int direction, int64_t bh, int64_t pn,
                    const float* decays, const float* states, float* out, void* stream);
 
+/* ssd_fwd_final_state: the final state only, H_out = the state after the
+ * shape's seqlen from init_states (NULL: zero): chunk_cumsum, chunk_state
+ * and state_passing of ssd_fwd without chunk_scan (C and D are not read).
+ * Arguments as for ssd_fwd; final_states (B, H, P, N) f32.  Workspace: at
+ * least ssd_fwd_workspace_size(shape) bytes, 256-byte aligned, caller-owned.
+ * Asynchronous on `stream`.  Errors as ssd_fwd. */
+int ssd_fwd_final_state(const ssd_shape* shape, const void* x, const void* dt,
+                        const float* dt_bias, const float* A, const void* B,
+                        const float* init_states, float* final_states, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/* ssd_bwd_dinit: the gradient of <dy, y> + <dfinal, final> with respect to
+ * the initial state only: dinit = G_0 of the reverse chunk recurrence
+ * G_c = dH^scan_c + exp(a_c[L-1]) G_{c+1}, G_nc = dfinal_states (NULL:
+ * zero), with dH^scan_c = sum_l exp(a_l) dy_l (x) C_l.  It depends on dt,
+ * dt_bias, A, C and dy only (x and B are not read).  dt (B, T, H), C
+ * (B, T, G, N), dy (B, T, H, P) in shape->in_dtype; dt_bias (H) or NULL, A
+ * (H), dfinal_states and dinit_states (B, H, P, N) f32.  Workspace: at least
+ * ssd_fwd_workspace_size(shape) bytes, 256-byte aligned, caller-owned.
+ * Asynchronous on `stream`.  Errors as ssd_bwd. */
+int ssd_bwd_dinit(const ssd_shape* shape, const void* dt, const float* dt_bias, const float* A,
+                  const void* C, const void* dy, const float* dfinal_states,
+                  float* dinit_states, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Diagnostic: one tcgen05 tile product on the current device,
  * D[128][nn] = A[128][k] * B[nn][k]^T (A, B bf16 row-major, D f32 row-major,
  * all device memory), with A and B staged in shared memory K-major (0) or

@@ -185,6 +185,51 @@ def ssd_bwd(x, dt, dt_bias, A, B, C, D, chunk_size: int, init_states, dy, dfinal
     return out
 
 
+def ssd_final_state(x, dt, dt_bias, A, B, chunk_size: int = 256, init_states=None,
+                    workspace=None, final_states=None):
+    """The state after the whole sequence from ``init_states`` (None: zero),
+    without the outputs: chunk_cumsum, chunk_state, state_passing
+    (``ssd_fwd_final_state``)."""
+    torch = _torch()
+    lib = _native.load()
+    Bt, T, H, P, N, G = _validate(x, dt, dt_bias, A, B, B, None, init_states)
+    shape = _shape_from(x, B, chunk_size, torch.float32)
+    if final_states is None:
+        final_states = torch.empty((Bt, H, P, N), dtype=torch.float32, device=x.device)
+    _check(final_states, "final_states", (Bt, H, P, N), torch.float32, x.device)
+    ws = _workspace(lib.ssd_fwd_workspace_size(ctypes.byref(shape)), x.device, workspace)
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    st = lib.ssd_fwd_final_state(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A),
+                                 _ptr(B), _ptr(init_states), _ptr(final_states), _ptr(ws),
+                                 ctypes.c_size_t(ws.numel()), ctypes.c_void_p(stream))
+    if st != 0:
+        raise SSDError("ssd_fwd_final_state", st)
+    return final_states
+
+
+def ssd_dinit(x, dt, dt_bias, A, C, dy, chunk_size: int = 256, dfinal_states=None,
+              workspace=None, dinit_states=None):
+    """Gradient of <dy, y> + <dfinal, final> w.r.t. the initial state alone
+    (``ssd_bwd_dinit``); x is read for its shape only."""
+    torch = _torch()
+    lib = _native.load()
+    Bt, T, H, P, N, G = _validate(x, dt, dt_bias, A, C, C, None, None)
+    _check(dy, "dy", (Bt, T, H, P), x.dtype, x.device)
+    _check(dfinal_states, "dfinal_states", (Bt, H, P, N), torch.float32, x.device)
+    shape = _shape_from(x, C, chunk_size, torch.float32)
+    if dinit_states is None:
+        dinit_states = torch.empty((Bt, H, P, N), dtype=torch.float32, device=x.device)
+    _check(dinit_states, "dinit_states", (Bt, H, P, N), torch.float32, x.device)
+    ws = _workspace(lib.ssd_fwd_workspace_size(ctypes.byref(shape)), x.device, workspace)
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    st = lib.ssd_bwd_dinit(ctypes.byref(shape), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(C),
+                           _ptr(dy), _ptr(dfinal_states), _ptr(dinit_states), _ptr(ws),
+                           ctypes.c_size_t(ws.numel()), ctypes.c_void_p(stream))
+    if st != 0:
+        raise SSDError("ssd_bwd_dinit", st)
+    return dinit_states
+
+
 def segment_decay(dt, dt_bias, A):
     """decay (b, h) = exp(A[h] * sum_t softplus(dt[b, t, h] + dt_bias[h])) over
     the whole of dt's sequence: the factor by which a state entering this

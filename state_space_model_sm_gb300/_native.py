@@ -112,6 +112,8 @@ SIGNATURES = {
     "ssd_fwd_noalloc": ([_SP] + [_VP] * 10 + [_VP], ctypes.c_int),
     "ssd_noalloc_scratch_bytes": ([], ctypes.c_size_t),
     "ssd_segment_decay": ([_SP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "ssd_fwd_final_state": ([_SP] + [_VP] * 7 + [_VP, ctypes.c_size_t, _VP], ctypes.c_int),
+    "ssd_bwd_dinit": ([_SP] + [_VP] * 7 + [_VP, ctypes.c_size_t, _VP], ctypes.c_int),
     "ssd_state_scan": ([ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                         _VP, _VP, _VP, _VP], ctypes.c_int),
 }

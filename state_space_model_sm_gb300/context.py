@@ -10,28 +10,33 @@ that enters it affinely to the state that leaves it:
 with F_r the segment's final state from a zero start.  So:
 
 forward
-  1. every rank runs the forward from a zero initial state (rank 0 from the
-     caller's) and keeps its final state F_r; it also computes D_r;
-  2. one all-gather of (D_r, F_r);
+  1. rank 0 runs the whole forward from the caller's initial state (its
+     final state is F_0); ranks 0 < r < R-1 compute only F_r, the final
+     state from a zero start (chunk_cumsum, chunk_state, state_passing: no
+     chunk_scan); every rank computes D_r;
+  2. one all-gather of (D_r, F_r) (the last rank's map is applied by no
+     one: it sends zeros);
   3. rank r > 0 scans ranks 0 .. r-1 to its incoming state H_in(r) and runs
-     the forward again from it.
+     the whole forward from it.
 
 backward (loss <dy, y> + <dfinal, H_out(R-1)>)
-  1. every rank runs the backward with dfinal = 0 (the last rank with the
-     caller's) from its true incoming state; the gradient of its incoming
-     state G_r = dL_r/dH_in(r) comes out of it;
-  2. one all-gather of G_r;
-  3. rank r < R-1 scans ranks R-1 .. r+1 backwards to dL/dH_out(r) and runs
-     the backward again with it as dfinal;
+  1. ranks r > 0 compute only G_r, the gradient of their incoming state
+     with dfinal = 0 (the last rank: the caller's dfinal), from dy, C and the
+     decays (chunk_cumsum, dstates, the reverse chunk recurrence); it does
+     not depend on the incoming state;
+  2. one all-gather of G_r (rank 0's is read by no one: it sends zeros);
+  3. rank r < R-1 scans ranks R-1 .. r+1 backwards to dL/dH_out(r), and
+     every rank runs the whole backward once with it as dfinal;
   4. dA, dD and ddt_bias (shared over the sequence) are summed over ranks.
+
+So each rank runs one forward and one backward over its segment, plus the
+two cheap first passes and the exchange.
 
 The step on the device is the engine's (``LibraryEngine``: the CUDA library);
 the exchange is the communicator's (``DistComm``: ``torch.distributed``).
 Both are duck-typed, so another engine or communicator can stand in.
 """
 from __future__ import annotations
-
-from typing import Optional
 
 __all__ = ["LibraryEngine", "DistComm", "cp_forward", "cp_backward", "split_sizes"]
 
@@ -53,13 +58,15 @@ def split_sizes(seqlen: int, nranks: int, multiple: int = 1):
 
 
 class LibraryEngine:
-    """Per-segment steps on the CUDA library (``ssd_fwd``, ``ssd_bwd``,
-    ``ssd_segment_decay``, ``ssd_state_scan``)."""
+    """Per-segment steps on the CUDA library: ``ssd_fwd``, ``ssd_bwd``, the
+    first passes ``ssd_fwd_final_state`` / ``ssd_bwd_dinit``, and the
+    exchange's arithmetic ``ssd_segment_decay`` / ``ssd_state_scan``."""
 
     def __init__(self, chunk_size: int = 256):
-        from . import ssd_fwd, ssd_bwd, segment_decay, state_scan
+        from . import segment_decay, ssd_bwd, ssd_dinit, ssd_final_state, ssd_fwd, state_scan
         self.chunk_size = chunk_size
         self._fwd, self._bwd = ssd_fwd, ssd_bwd
+        self._final, self._dinit = ssd_final_state, ssd_dinit
         self._decay, self._scan = segment_decay, state_scan
 
     def fwd(self, seg, init):
@@ -67,16 +74,27 @@ class LibraryEngine:
                          seg.get("D"), chunk_size=self.chunk_size, init_states=init)
 
     def bwd(self, seg, init, dy, dfinal):
-        import torch
         x = seg["x"]
-        if init is None:  # the gradient of the incoming state is always needed
-            Bt, _, H, P = x.shape
-            init = torch.zeros((Bt, H, P, seg["B"].shape[-1]), dtype=torch.float32,
-                               device=x.device)
+        if init is None:  # the gradient of the incoming state is always returned
+            init = self.zeros_state(seg)
         g = self._bwd(x, seg["dt"], seg["dt_bias"], seg["A"], seg["B"], seg["C"], seg.get("D"),
                       self.chunk_size, init, dy, dfinal)
         g["dinit"] = g.pop("dinit_states")
         return g
+
+    def final_state(self, seg):
+        return self._final(seg["x"], seg["dt"], seg["dt_bias"], seg["A"], seg["B"],
+                           chunk_size=self.chunk_size)
+
+    def dinit(self, seg, dy, dfinal):
+        return self._dinit(seg["x"], seg["dt"], seg["dt_bias"], seg["A"], seg["C"], dy,
+                           chunk_size=self.chunk_size, dfinal_states=dfinal)
+
+    def zeros_state(self, seg):
+        import torch
+        x = seg["x"]
+        Bt, _, H, P = x.shape
+        return torch.zeros((Bt, H, P, seg["B"].shape[-1]), dtype=torch.float32, device=x.device)
 
     def decay(self, seg):
         return self._decay(seg["dt"], seg["dt_bias"], seg["A"])
@@ -114,14 +132,21 @@ def cp_forward(engine, comm, seg, init=None):
     Returns (y, H_out, H_in): this segment's output, the state leaving it
     (the sequence's final state on the last rank) and the state entering it
     (None on rank 0 without ``init``), which ``cp_backward`` takes back."""
-    y, final = engine.fwd(seg, init if comm.rank == 0 else None)
-    if comm.world == 1:
-        return y, final, init
+    R, r = comm.world, comm.rank
+    if r == 0:
+        y, final = engine.fwd(seg, init)
+        if R == 1:
+            return y, final, init
+        send = final
+    elif r < R - 1:
+        send = engine.final_state(seg)
+    else:
+        send = engine.zeros_state(seg)
     decays = comm.allgather(engine.decay(seg))
-    finals = comm.allgather(final)
-    if comm.rank == 0:
+    finals = comm.allgather(send)
+    if r == 0:
         return y, final, init
-    h_in = engine.scan(decays, finals, comm.rank, 0)
+    h_in = engine.scan(decays, finals, r, 0)
     y, final = engine.fwd(seg, h_in)
     return y, final, h_in
 
@@ -132,16 +157,17 @@ def cp_backward(engine, comm, seg, h_in, dy, dfinal=None):
     last rank only.  dx, ddt, dB, dC are this segment's; dA, dD, ddt_bias
     are summed over ranks; "dinit" (the gradient of the sequence's initial
     state) is returned on rank 0 only."""
-    last = comm.rank == comm.world - 1
-    g = engine.bwd(seg, h_in, dy, dfinal if last else None)
-    if comm.world > 1:
-        decays = comm.allgather(engine.decay(seg))
-        gin = comm.allgather(g["dinit"])
-        if not last:
-            g = engine.bwd(seg, h_in, dy, engine.scan(decays, gin, comm.rank, 1))
-        for k in _SHARED:
-            if g.get(k) is not None:
-                g[k] = comm.allreduce_sum(g[k])
-    if comm.rank != 0:
+    R, r = comm.world, comm.rank
+    last = r == R - 1
+    if R == 1:
+        return engine.bwd(seg, h_in, dy, dfinal)
+    send = engine.dinit(seg, dy, dfinal if last else None) if r > 0 else engine.zeros_state(seg)
+    decays = comm.allgather(engine.decay(seg))
+    gin = comm.allgather(send)
+    g = engine.bwd(seg, h_in, dy, dfinal if last else engine.scan(decays, gin, r, 1))
+    for k in _SHARED:
+        if g.get(k) is not None:
+            g[k] = comm.allreduce_sum(g[k])
+    if r != 0:
         g.pop("dinit", None)
     return g

@@ -312,6 +312,68 @@ int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
   return simt_backward(d, a, w, s) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
+int ssd_fwd_final_state(const ssd_shape* shape, const void* x, const void* dt,
+                        const float* dt_bias, const float* A, const void* B,
+                        const float* init_states, float* final_states, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  Dims d;
+  int st = make_dims(shape, &d);
+  if (st != SSD_OK) return st;
+  if (!x || !dt || !A || !B || !final_states) return SSD_ERR_INVALID_ARG;
+  const size_t in = d.in_bf16 ? 2 : 4;
+  if (!aligned(x, in) || !aligned(dt, in) || !aligned(B, in)) return SSD_ERR_INVALID_ARG;
+  const float* fp[] = {dt_bias, A, init_states, final_states};
+  for (const float* p : fp)
+    if (p && !aligned(p, 4)) return SSD_ERR_INVALID_ARG;
+  const FwdOffsets o = fwd_offsets(d);
+  if (!workspace || workspace_bytes < o.total || !aligned(workspace, kAlign))
+    return SSD_ERR_WORKSPACE;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const FwdArgs a{x, dt, dt_bias, A, B, nullptr, nullptr, init_states, nullptr, final_states};
+  FwdWs w = carve_fwd(static_cast<char*>(workspace), o);
+  const bool tc = !force_simt() && tc_forward_supported(d) && aligned(x, 16) && aligned(B, 16) &&
+                  aligned(init_states, 16) && aligned(final_states, 16);
+  t_last_path = tc ? 1 : 0;
+  if (tc) {
+    w.Himg = w.Hprev;  // the state images take the fp32 states' place, as in ssd_fwd
+    w.Hprev = nullptr;
+    return tc_front_final(d, a, w, s) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+  }
+  simt_front(d, a, w, s);
+  return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+int ssd_bwd_dinit(const ssd_shape* shape, const void* dt, const float* dt_bias, const float* A,
+                  const void* C, const void* dy, const float* dfinal_states,
+                  float* dinit_states, void* workspace, size_t workspace_bytes, void* stream) {
+  Dims d;
+  int st = make_dims(shape, &d);
+  if (st != SSD_OK) return st;
+  if (!dt || !A || !C || !dy || !dinit_states) return SSD_ERR_INVALID_ARG;
+  const size_t in = d.in_bf16 ? 2 : 4;
+  if (!aligned(dt, in) || !aligned(C, in) || !aligned(dy, in)) return SSD_ERR_INVALID_ARG;
+  const float* fp[] = {dt_bias, A, dfinal_states, dinit_states};
+  for (const float* p : fp)
+    if (p && !aligned(p, 4)) return SSD_ERR_INVALID_ARG;
+  const FwdOffsets o = fwd_offsets(d);
+  if (!workspace || workspace_bytes < o.total || !aligned(workspace, kAlign))
+    return SSD_ERR_WORKSPACE;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const FwdArgs a{nullptr, dt, dt_bias, A, nullptr, C, nullptr, nullptr, nullptr, nullptr};
+  const FwdWs w = carve_fwd(static_cast<char*>(workspace), o);
+  float* dHs = w.S;  // the chunk-state slot holds dH^scan here
+  const bool tc = !force_simt() && tc_forward_supported(d) && aligned(C, 16) && aligned(dy, 16);
+  t_last_path = tc ? 1 : 0;
+  simt_cumsum(d, a, w, s);
+  if (tc) {
+    if (tc_dstates(d, dy, C, w.delta, w.acs, dHs, s) != cudaSuccess) return SSD_ERR_CUDA;
+  } else {
+    simt_dstates(d, dy, C, w.delta, w.acs, dHs, s);
+  }
+  cp_dinit_chain(d, dHs, w.acs, dfinal_states, dinit_states, s);
+  return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
 int ssd_get_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SSD_ERR_CUDA;
   int v = 0;

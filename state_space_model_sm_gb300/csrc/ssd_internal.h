@@ -107,6 +107,19 @@ cudaError_t simt_backward(const Dims& d, const BwdArgs& a, const BwdWs& w, cudaS
 void simt_cumsum(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s);
 void simt_state_passing(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s);
 
+// The first passes of context parallelism: the front of the forward (cumsum,
+// chunk states, state passing: final state and Hprev) and the per-chunk
+// dstates of the backward (dH^scan_c from dy, C, delta, a).
+void simt_front(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s);
+void simt_dstates(const Dims& d, const void* dy, const void* C, const float* delta,
+                  const float* acs, float* dHs, cudaStream_t s);
+cudaError_t tc_front_final(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s);
+cudaError_t tc_dstates(const Dims& d, const void* dy, const void* C, const float* delta,
+                       const float* acs, float* dHs, cudaStream_t s);
+// dinit = G_0 of G_c = dH^scan_c + exp(a_c[L-1]) G_{c+1}, G_nc = dfinal (or 0).
+void cp_dinit_chain(const Dims& d, const float* dHs, const float* acs, const float* dfinal,
+                    float* dinit, cudaStream_t s);
+
 int simt_state_passing_bwd(const Dims& d, const float* dHs, const float* acs, const float* Hprev,
                            const float* dfinal, float* dS, float* dlast, float* dinit,
                            void* dSimg, const void* Himg,

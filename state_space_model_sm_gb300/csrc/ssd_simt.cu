@@ -1073,6 +1073,39 @@ void simt_state_passing(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStr
   launch_state_passing(d, a, w, s);
 }
 
+void simt_front(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
+  // chunk_cumsum, chunk_state, state_passing (no C B^T: the states do not need C)
+  const dim3 grid(d.nc, d.H, d.B);
+  if (d.in_bf16) {
+    using T = __nv_bfloat16;
+    launch_cumsum<T>(d, a, w, s);
+    SSD_LAUNCH("k_chunk_state", s, k_chunk_state<T, 0><<<grid, kThreads, 0, s>>>(
+        static_cast<const T*>(a.x), static_cast<const T*>(a.B), w.delta, w.acs, w.S, d.T, d.H,
+        d.G, d.P, d.N, d.L, d.nc));
+  } else {
+    launch_cumsum<float>(d, a, w, s);
+    SSD_LAUNCH("k_chunk_state", s, k_chunk_state<float, 0><<<grid, kThreads, 0, s>>>(
+        static_cast<const float*>(a.x), static_cast<const float*>(a.B), w.delta, w.acs, w.S, d.T,
+        d.H, d.G, d.P, d.N, d.L, d.nc));
+  }
+  launch_state_passing(d, a, w, s);
+}
+
+void simt_dstates(const Dims& d, const void* dy, const void* C, const float* delta,
+                  const float* acs, float* dHs, cudaStream_t s) {
+  const dim3 grid(d.nc, d.H, d.B);
+  if (d.in_bf16) {
+    using T = __nv_bfloat16;
+    SSD_LAUNCH("k_chunk_state", s, k_chunk_state<T, 1><<<grid, kThreads, 0, s>>>(
+        static_cast<const T*>(dy), static_cast<const T*>(C), delta, acs, dHs, d.T, d.H, d.G, d.P,
+        d.N, d.L, d.nc));
+  } else {
+    SSD_LAUNCH("k_chunk_state", s, k_chunk_state<float, 1><<<grid, kThreads, 0, s>>>(
+        static_cast<const float*>(dy), static_cast<const float*>(C), delta, acs, dHs, d.T, d.H,
+        d.G, d.P, d.N, d.L, d.nc));
+  }
+}
+
 int simt_state_passing_bwd(const Dims& d, const float* dHs, const float* acs, const float* Hprev,
                            const float* dfinal, float* dS, float* dlast, float* dinit,
                            void* dSimg, const void* Himg, cudaStream_t s) {

@@ -1300,22 +1300,41 @@ void scan_partition(const Dims& d, int sms, int* grid, int* per) {
   *grid = (int)((items + *per - 1) / *per);
 }
 
+// chunk_cumsum (delta, a) and chunk_state (S) in one persistent launch.
+template <int N, int L>
+void launch_state_front(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s,
+                        int* status, int sms) {
+  using SM = StateSmem<N, L>;
+  auto kern = k_state_tc<N, L, 0>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
+  const int n_items = d.B * d.nc * (d.H / 2);
+  const dim3 grid(std::min(n_items, 2 * sms));
+  SSD_LAUNCH("k_state_tc", s,
+             kern<<<grid, 256, SM::kBytes, s>>>(
+                 static_cast<const bf16*>(a.x), static_cast<const bf16*>(a.B),
+                 static_cast<const bf16*>(a.dt), a.dt_bias, a.A, w.delta, w.acs, w.S, d.T, d.H,
+                 d.G, d.nc, n_items, status));
+}
+
+// dH^scan_c = sum_l exp(a_l) dy_l (x) C_l per chunk, from delta / a already
+// in the workspace.
+template <int N, int L>
+void launch_dstates(const Dims& d, const bf16* dy, const bf16* Cm, const float* delta,
+                    const float* acs, float* dHs, cudaStream_t s, int* status, int sms) {
+  using SS = StateSmem<N, L>;
+  auto kern = k_state_tc<N, L, 1>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::kBytes);
+  const int n_items = d.B * d.nc * (d.H / 2);
+  const dim3 grid(std::min(n_items, 2 * sms));
+  SSD_LAUNCH("k_dstates_tc", s, kern<<<grid, 256, SS::kBytes, s>>>(
+      dy, Cm, nullptr, nullptr, nullptr, const_cast<float*>(delta), const_cast<float*>(acs), dHs,
+      d.T, d.H, d.G, d.nc, n_items, status));
+}
+
 template <int N, int L, typename Tout>
 cudaError_t launch_tc_forward_t(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s,
                                 int* status, int sms) {
-  {
-    // chunk_cumsum runs inside the chunk_state kernel
-    using SM = StateSmem<N, L>;
-    auto kern = k_state_tc<N, L, 0>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
-    const int n_items = d.B * d.nc * (d.H / 2);
-    const dim3 grid(std::min(n_items, 2 * sms));
-    SSD_LAUNCH("k_state_tc", s,
-               kern<<<grid, 256, SM::kBytes, s>>>(
-                   static_cast<const bf16*>(a.x), static_cast<const bf16*>(a.B),
-                   static_cast<const bf16*>(a.dt), a.dt_bias, a.A, w.delta, w.acs, w.S, d.T, d.H,
-                   d.G, d.nc, n_items, status));
-  }
+  launch_state_front<N, L>(d, a, w, s, status, sms);  // chunk_cumsum runs inside chunk_state
   simt_state_passing(d, a, w, s);
   {
     using SM = ScanSmem<N, L>;
@@ -1351,24 +1370,9 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
   FwdArgs f = a.f;
   f.final_state = nullptr;
   FwdWs fw{w.delta, w.acs, w.S, nullptr, nullptr, w.Himg};
-  using SS = StateSmem<N, L>;
-  const int n_items = d.B * d.nc * (d.H / 2);
-  const dim3 sgrid(std::min(n_items, 2 * sms));
-  {
-    auto kern = k_state_tc<N, L, 0>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::kBytes);
-    SSD_LAUNCH("k_state_tc", s, kern<<<sgrid, 256, SS::kBytes, s>>>(
-        x, Bm, static_cast<const bf16*>(f.dt), f.dt_bias, f.A, w.delta, w.acs, w.S, d.T, d.H,
-        d.G, d.nc, n_items, status));  // with chunk_cumsum
-  }
+  launch_state_front<N, L>(d, f, fw, s, status, sms);  // with chunk_cumsum
   simt_state_passing(d, f, fw, s);
-  {
-    auto kern = k_state_tc<N, L, 1>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::kBytes);
-    SSD_LAUNCH("k_dstates_tc", s, kern<<<sgrid, 256, SS::kBytes, s>>>(
-        dy, Cm, nullptr, nullptr, nullptr, w.delta, w.acs, w.dHs, d.T, d.H, d.G, d.nc, n_items,
-        status));
-  }
+  launch_dstates<N, L>(d, dy, Cm, w.delta, w.acs, w.dHs, s, status, sms);
   const int nsplit = simt_state_passing_bwd(d, w.dHs, w.acs, nullptr, a.dfinal, nullptr, w.dlast,
                                             a.dinit, w.dSimg, w.Himg, s);
   {
@@ -1446,6 +1450,36 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStre
   if (d.N == 128 && d.L == 128) return launch_tc_forward_nl<128, 128>(d, a, w, s, status, sms);
   if (d.N == 64 && d.L == 256) return launch_tc_forward_nl<64, 256>(d, a, w, s, status, sms);
   return launch_tc_forward_nl<64, 128>(d, a, w, s, status, sms);
+}
+
+cudaError_t tc_front_final(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
+  int* status = device_status_ptr();
+  if (!status) return cudaErrorUnknown;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (d.N == 128 && d.L == 256) launch_state_front<128, 256>(d, a, w, s, status, sms);
+  else if (d.N == 128 && d.L == 128) launch_state_front<128, 128>(d, a, w, s, status, sms);
+  else if (d.N == 64 && d.L == 256) launch_state_front<64, 256>(d, a, w, s, status, sms);
+  else launch_state_front<64, 128>(d, a, w, s, status, sms);
+  simt_state_passing(d, a, w, s);
+  return cudaGetLastError();
+}
+
+cudaError_t tc_dstates(const Dims& d, const void* dy, const void* C, const float* delta,
+                       const float* acs, float* dHs, cudaStream_t s) {
+  int* status = device_status_ptr();
+  if (!status) return cudaErrorUnknown;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const bf16* y = static_cast<const bf16*>(dy);
+  const bf16* c = static_cast<const bf16*>(C);
+  if (d.N == 128 && d.L == 256) launch_dstates<128, 256>(d, y, c, delta, acs, dHs, s, status, sms);
+  else if (d.N == 128 && d.L == 128) launch_dstates<128, 128>(d, y, c, delta, acs, dHs, s, status, sms);
+  else if (d.N == 64 && d.L == 256) launch_dstates<64, 256>(d, y, c, delta, acs, dHs, s, status, sms);
+  else launch_dstates<64, 128>(d, y, c, delta, acs, dHs, s, status, sms);
+  return cudaGetLastError();
 }
 
 cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w, cudaStream_t s) {

@@ -68,6 +68,17 @@ class OracleEngine:
                            None if dfinal is None else dfinal.numpy())
         return {k: torch.from_numpy(v) for k, v in g.items()}
 
+    def final_state(self, seg):
+        return self.fwd(seg, None)[1]
+
+    def dinit(self, seg, dy, dfinal):
+        return self.bwd(seg, None, dy, dfinal)["dinit"]
+
+    def zeros_state(self, seg):
+        import torch
+        Bt, _, H, P = seg["x"].shape
+        return torch.zeros((Bt, H, P, seg["B"].shape[-1]), dtype=torch.float64)
+
     def decay(self, seg):
         import torch
         dt, bias, A = (seg[k].numpy() for k in ("dt", "dt_bias", "A"))
@@ -273,6 +284,40 @@ def test_segment_decay_matches_definition(cuda_lib, dtype):
     s = np.logaddexp(0.0, inp.dt.astype(np.float64) + inp.dt_bias[None, None, :]).sum(1)
     ref = np.exp(inp.A[None, :].astype(np.float64) * s)
     np.testing.assert_allclose(got, ref, rtol=2e-5, atol=1e-30)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dtype,shape_args", [
+    ("f32", (2, 300, 4, 16, 32, 2, 64)),          # generic kernels, ragged last chunk
+    ("bf16", (2, 1000, 8, 64, 128, 2, 256)),      # tensor-core kernels, ragged last chunk
+    ("bf16", (1, 640, 4, 64, 64, 1, 128)),
+])
+def test_first_passes_match_oracle(cuda_lib, dtype, shape_args):
+    """ssd_final_state = the oracle forward's final state; ssd_dinit = the
+    oracle backward's initial-state gradient (with and without dfinal)."""
+    import torch
+
+    import oracle
+    from parity_util import assert_close, to_np
+    inp = _inputs(shape_args, seed=41, dtype=dtype)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+
+    def cv(a, dt=tdt):
+        return torch.from_numpy(np.ascontiguousarray(a)).to("cuda", dt)
+    f32 = torch.float32
+    x, dt, B, C, dy = (cv(a) for a in (inp.x, inp.dt, inp.B, inp.C, inp.dy))
+    dtb, A, init, dfin = (cv(a, f32) for a in (inp.dt_bias, inp.A, inp.init, inp.dfinal))
+    L = shape_args[-1]
+    _, f_ref = oracle.ssd_fwd(inp.x, inp.dt, inp.dt_bias, inp.A, inp.B, inp.C, inp.D, inp.init)
+    f = cuda_lib.ssd_final_state(x, dt, dtb, A, B, chunk_size=L, init_states=init)
+    assert_close("final", to_np(f), f_ref, dtype)
+    for with_dfinal in (False, True):
+        g_ref = oracle.ssd_bwd(inp.x, inp.dt, inp.dt_bias, inp.A, inp.B, inp.C, inp.D, None,
+                               inp.dy, inp.dfinal if with_dfinal else None)["dinit"]
+        g = cuda_lib.ssd_dinit(x, dt, dtb, A, C, dy, chunk_size=L,
+                               dfinal_states=dfin if with_dfinal else None)
+        assert_close(f"dinit(dfinal={with_dfinal})", to_np(g), g_ref, dtype)
+    assert cuda_lib.device_status() == 0
 
 
 @pytest.mark.gpu
