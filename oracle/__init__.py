@@ -10,6 +10,8 @@ Contents
   * ``chunked``: the chunked algorithm (chunk_cumsum, chunk_state,
     state_passing, chunk_scan) written step by step in fp64 numpy; it exposes
     the intermediate tensors the GPU kernels also produce.
+  * ``gated_norm``: the gated RMSNorm that follows the SSD output in the
+    layer (forward and backward), fp64 numpy.
 
 Parity pins for every function here live in ``tests/test_oracle.py``.
 """

@@ -137,3 +137,52 @@ def to_torch(inp: SSDInputs, device="cuda") -> dict:
     return dict(x=cv(inp.x), dt=cv(inp.dt), dt_bias=cv(inp.dt_bias, f32), A=cv(inp.A, f32),
                 B=cv(inp.B), C=cv(inp.C), D=cv(inp.D, f32), init=cv(inp.init, f32),
                 dy=cv(inp.dy), dfinal=cv(inp.dfinal, f32))
+
+
+# ------------------------------------------------------------ gated norm
+@dataclasses.dataclass
+class NormShape:
+    rows: int          # batch * seqlen
+    features: int      # nheads * headdim (d_inner)
+    group_size: int    # d_inner / ngroups
+    eps: float = 1e-5
+
+
+@dataclasses.dataclass
+class NormInputs:
+    shape: NormShape
+    dtype: str         # "bf16" or "f32": storage type of y, z, dout
+    y: np.ndarray      # (rows, features): the SSD output
+    z: np.ndarray      # (rows, features): the gate
+    w: np.ndarray      # (features,) fp32 weight
+    dout: np.ndarray   # (rows, features): upstream gradient
+
+
+def make_norm_inputs(shape: NormShape, *, seed: int, dtype: str = "bf16") -> NormInputs:
+    """Draw order y, z, w, dout (PCG64): y, z, dout ~ N(0, 1); w = 1 + 0.1 N(0, 1)
+    (the weight starts at one in the layer; the spread exercises it).  y, z
+    and dout are rounded to bf16 for dtype "bf16"."""
+    if dtype not in ("bf16", "f32"):
+        raise ValueError(f"dtype must be 'bf16' or 'f32', got {dtype!r}")
+    M, D = shape.rows, shape.features
+    rng = np.random.Generator(np.random.PCG64(seed))
+    y = rng.standard_normal((M, D), dtype=np.float32)
+    z = rng.standard_normal((M, D), dtype=np.float32)
+    w = (1.0 + 0.1 * rng.standard_normal(D, dtype=np.float32)).astype(np.float32)
+    dout = rng.standard_normal((M, D), dtype=np.float32)
+    if dtype == "bf16":
+        y, z, dout = (round_to_bf16(a) for a in (y, z, dout))
+    return NormInputs(shape, dtype, y, z, w, dout)
+
+
+# rows = batch * seqlen, features = nheads * headdim, group = features / ngroups
+NORM_WORKLOADS = {
+    "norm_tiny_f32": (NormShape(37, 64, 16), "f32", 0),
+    "norm_layer_bf16": (NormShape(4 * 4096, 24 * 64, 24 * 64), "bf16", 1),
+    "norm_hybrid_bf16": (NormShape(2 * 8192, 64 * 64, 64 * 64 // 8), "bf16", 2),
+}
+
+
+def make_norm_workload(name: str) -> NormInputs:
+    shape, dtype, seed = NORM_WORKLOADS[name]
+    return make_norm_inputs(shape, seed=seed, dtype=dtype)
