@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--context-parallel", type=int, default=0, metavar="R",
                     help="time each rank's share of an R-way sequence split (one GPU)")
+    ap.add_argument("--gated-norm", action="store_true",
+                    help="time the gated RMSNorm forward + backward instead of the SSD")
+    ap.add_argument("--norm-workload", default="norm_hybrid_bf16")
     return ap.parse_args()
 
 
@@ -567,11 +570,123 @@ def run_context_parallel(args):
     print(json.dumps(out))
 
 
+def run_gated_norm(args):
+    """Gated RMSNorm forward + backward (the step after the SSD output; its
+    backward is the pages' _layer_norm_bwd) on one GPU: tokens (rows) per
+    second, per-kernel times and the HBM roofline of the backward."""
+    import numpy as np
+    import torch
+
+    import state_space_model_sm_gb300 as ssd
+    from state_space_model_sm_gb300 import roofline
+    from state_space_model_sm_gb300.inputs import NORM_WORKLOADS, make_norm_workload
+
+    dev = torch.device("cuda", 0)
+    ssd.build()
+    ssd.load_library()
+    shape, dtype, seed = NORM_WORKLOADS[args.norm_workload]
+    inp = make_norm_workload(args.norm_workload)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+
+    def cv(a, dt=tdt):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+    y, z, dout, w = cv(inp.y), cv(inp.z), cv(inp.dout), cv(inp.w, torch.float32)
+    gs, eps = shape.group_size, shape.eps
+    out, rstd = ssd.gated_norm_fwd(y, z, w, gs, eps=eps)
+    ws = torch.empty(ssd.gated_norm_workspace_bytes(y, gs, eps), dtype=torch.uint8, device=dev)
+    grads = ssd.gated_norm_bwd(y, z, w, dout, gs, eps=eps, rstd=rstd, workspace=ws)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ssd.gated_norm_fwd(y, z, w, gs, eps=eps, out=out, rstd=rstd)
+        ssd.gated_norm_bwd(y, z, w, dout, gs, eps=eps, rstd=rstd, workspace=ws, out=grads)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    def timed(profiled):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        l0 = ssd.launch_count()
+        ssd.profile_enable(profiled)
+        torch.cuda.synchronize()
+        for a, b in ev:
+            flush.fill_(1.0)
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        prof = ssd.profile_read() if profiled else None
+        ssd.profile_enable(False)
+        return sum(a.elapsed_time(b) for a, b in ev), ssd.launch_count() - l0, prof
+
+    with ClockSampler(0) as clk:
+        ms, launches, _ = timed(False)
+        _, _, prof = timed(True)
+    if ssd.device_status() != 0:
+        raise RuntimeError("device status word set during the timed region")
+    rd = roofline.NormDims(shape.rows, shape.features, gs, 2 if dtype == "bf16" else 4,
+                           2 if dtype == "bf16" else 4)
+    peaks = load_peaks()
+    kernels = {}
+    for k, (tot, n) in prof.items():
+        if n == 0:
+            continue
+        us = 1e3 * tot / n
+        nb = roofline.norm_kernel_bytes(k, rd)
+        gbs = nb / (us / 1e6) / 1e9
+        kernels[k] = {"us": round(us, 2), "launches_per_step": n / args.steps,
+                      "algorithmic_bytes": nb, "hbm_GBps": round(gbs, 1),
+                      "frac": round(gbs / peaks["hbm"], 4)}
+    dom = "k_gated_norm_bwd"
+    roof = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["hbm_GBps"],
+            "peak": peaks["hbm"], "unit": "GB/s", "frac": kernels[dom]["frac"],
+            "traffic": measured_traffic(dom, args.norm_workload),
+            "algorithmic_bytes": kernels[dom]["algorithmic_bytes"],
+            "peak_source": peaks["source"]}
+    cpu = None
+    if not args.no_cpu_baseline:
+        from oracle import gated_norm as gn
+        n = 256
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 10.0:
+            gn.gated_rmsnorm_fwd(inp.y[:n], inp.z[:n], inp.w, gs, eps=eps)
+            gn.gated_rmsnorm_bwd(inp.y[:n], inp.z[:n], inp.w, inp.dout[:n], gs, eps=eps)
+            reps += 1
+        sec = time.perf_counter() - t0
+        cpu = {"value": round(n * reps / sec, 1), "unit": "tokens/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"rows 0..{n - 1} of {args.norm_workload}, forward + backward, "
+                         f"{reps} repetitions in {sec:.1f} s (numpy fp64, one thread)"}
+    rows = shape.rows
+    out_line = {
+        "metric": "gated RMSNorm fwd+bwd tokens/sec on 1 GB300 (the step after the SSD output)",
+        "impl": "ours", "value": round(rows * args.steps / (ms / 1e3), 1), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": f"{dtype} in/out, f32 statistics and dw",
+        "data": "synthetic (seeded PCG64: y, z, dout ~ N(0,1), w = 1 + 0.1 N(0,1))",
+        "config": {"workload": args.norm_workload, "rows": rows, "features": shape.features,
+                   "group_size": gs, "eps": eps, "l2": "flushed (512 MB write) before every step"},
+        "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "gpu_launches": launches,
+        "clocks": clk.summary(), "gpu": torch.cuda.get_device_name(dev),
+    }
+    print(json.dumps(out_line))
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if args.gated_norm:
+        if world > 1:
+            raise SystemExit("--gated-norm runs on one GPU; run it without torchrun")
+        run_gated_norm(args)
         return
     if args.context_parallel:
         if world > 1:

@@ -206,6 +206,53 @@ int ssd_bwd_dinit(const ssd_shape* shape, const void* dt, const float* dt_bias, 
                   const void* C, const void* dy, const float* dfinal_states,
                   float* dinit_states, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Gated RMSNorm: the normalisation that follows the SSD output in a Mamba-2
+ * layer; its backward is the pages' _layer_norm_bwd (step bwd_2 of the
+ * per-kernel table in "Latency and speedup by kernel").  The pages name the
+ * kernel but not its arithmetic; the reading implemented is the layer's
+ * output norm with the gate before the norm: with u = y * silu(z), per row
+ * and group g of group_size consecutive features,
+ *     rstd_g = 1 / sqrt(mean_g(u^2) + eps),   out = u * rstd_g * w,
+ * and the backward of <dout, out> with respect to y, z and w.  Rows are the
+ * (batch * seqlen) positions, features the (nheads * headdim) channels.
+ * Requirements: rows < 2^30, features and group_size multiples of 8,
+ * group_size dividing features (else SSD_ERR_INVALID_ARG); features <= 4096,
+ * features / 8 a multiple of 32 or a power of two below 32, group_size / 8 a
+ * multiple of 32 or a power of two below 32 (else SSD_ERR_UNSUPPORTED).
+ * Kernels: rows stream through shared memory by bulk asynchronous copies;
+ * waits are bounded (1 s) and an expired wait records SSD_ERR_TIMEOUT in
+ * the device status word (ssd_get_device_status). */
+typedef struct {
+  int64_t rows, features, group_size;
+  float eps;
+  int32_t in_dtype;  /* ssd_dtype of y, z and dout  */
+  int32_t out_dtype; /* ssd_dtype of out, dy and dz */
+} ssd_norm_shape;
+
+/* Bytes of workspace ssd_gated_norm_bwd needs (per-CTA partial sums of dw);
+ * 0 for an invalid or unsupported shape.  Depends on the current device's SM
+ * count. */
+size_t ssd_gated_norm_workspace_size(const ssd_norm_shape* shape);
+
+/* ssd_gated_norm_fwd: y, z (rows, features) in_dtype, w (features) f32,
+ * out (rows, features) out_dtype; rstd (rows, features / group_size) f32 or
+ * NULL (saved for the backward).  y, z, out 16-byte aligned; device memory;
+ * asynchronous on `stream`.  rows == 0 launches nothing.  Errors:
+ * SSD_ERR_INVALID_ARG (shape, NULL or misaligned pointer),
+ * SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA. */
+int ssd_gated_norm_fwd(const ssd_norm_shape* shape, const void* y, const void* z,
+                       const float* w, void* out, float* rstd, void* stream);
+
+/* ssd_gated_norm_bwd: gradients of <dout, out>: dy, dz (rows, features)
+ * out_dtype, dw (features) f32 (the sum over rows, taken in a fixed order).
+ * rstd as ssd_gated_norm_fwd wrote it, or NULL to recompute it.  y, z, dout,
+ * dy, dz 16-byte aligned; workspace of ssd_gated_norm_workspace_size bytes,
+ * 16-byte aligned, caller-owned.  rows == 0 sets dw to 0.  Errors as
+ * ssd_gated_norm_fwd, plus SSD_ERR_WORKSPACE. */
+int ssd_gated_norm_bwd(const ssd_norm_shape* shape, const void* y, const void* z,
+                       const float* w, const float* rstd, const void* dout, void* dy, void* dz,
+                       float* dw, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Diagnostic: one tcgen05 tile product on the current device,
  * D[128][nn] = A[128][k] * B[nn][k]^T (A, B bf16 row-major, D f32 row-major,
  * all device memory), with A and B staged in shared memory K-major (0) or

@@ -230,6 +230,82 @@ def ssd_dinit(x, dt, dt_bias, A, C, dy, chunk_size: int = 256, dfinal_states=Non
     return dinit_states
 
 
+def _norm_shape(y, group_size, eps, out_dtype):
+    D = y.shape[-1]
+    rows = y.numel() // D if D else 0
+    return _native.NormShape(rows, D, group_size, float(eps), _dtype_code(y.dtype),
+                             _dtype_code(out_dtype))
+
+
+def _norm_check(name, t, like, dtype=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    _check(t, name, tuple(like.shape), like.dtype if dtype is None else dtype, like.device)
+
+
+def gated_norm_fwd(y, z, w, group_size: int, eps: float = 1e-5, out_dtype=None,
+                   return_rstd: bool = True, out=None, rstd=None):
+    """out = rmsnorm over groups of ``group_size`` of (y * silu(z)), times w
+    (``ssd_gated_norm_fwd``).  y, z (..., features) float32 or bfloat16 (one
+    dtype), w (features,) float32.  Returns (out, rstd (rows, groups) or None)."""
+    torch = _torch()
+    lib = _native.load()
+    if y.dim() < 1 or y.device.type != "cuda":
+        raise ValueError("y must be a CUDA tensor (..., features)")
+    _norm_check("z", z, y)
+    D = y.shape[-1]
+    _check(w, "w", (D,), torch.float32, y.device)
+    out_dtype = y.dtype if out_dtype is None else out_dtype
+    shape = _norm_shape(y, group_size, eps, out_dtype)
+    if out is None:
+        out = torch.empty(y.shape, dtype=out_dtype, device=y.device)
+    _check(out, "out", tuple(y.shape), out_dtype, y.device)
+    if return_rstd and rstd is None:
+        rstd = torch.empty((shape.rows, max(D // max(group_size, 1), 1)), dtype=torch.float32,
+                           device=y.device)
+    stream = torch.cuda.current_stream(y.device).cuda_stream
+    st = lib.ssd_gated_norm_fwd(ctypes.byref(shape), _ptr(y), _ptr(z), _ptr(w), _ptr(out),
+                                _ptr(rstd) if return_rstd else None, ctypes.c_void_p(stream))
+    if st != 0:
+        raise SSDError("ssd_gated_norm_fwd", st)
+    return out, (rstd if return_rstd else None)
+
+
+def gated_norm_workspace_bytes(y, group_size: int, eps: float = 1e-5, out_dtype=None) -> int:
+    shape = _norm_shape(y, group_size, eps, y.dtype if out_dtype is None else out_dtype)
+    return int(_native.load().ssd_gated_norm_workspace_size(ctypes.byref(shape)))
+
+
+def gated_norm_bwd(y, z, w, dout, group_size: int, eps: float = 1e-5, rstd=None,
+                   out_dtype=None, workspace=None, out=None):
+    """Gradients of <dout, out> (``ssd_gated_norm_bwd``): dict dy, dz (shape of
+    y, ``out_dtype``: y's dtype by default) and dw (features,) float32.  rstd
+    as ``gated_norm_fwd`` returned it, or None to recompute it."""
+    torch = _torch()
+    lib = _native.load()
+    _norm_check("z", z, y)
+    _norm_check("dout", dout, y)
+    D = y.shape[-1]
+    _check(w, "w", (D,), torch.float32, y.device)
+    out_dtype = y.dtype if out_dtype is None else out_dtype
+    shape = _norm_shape(y, group_size, eps, out_dtype)
+    if out is None:
+        out = dict(dy=torch.empty(y.shape, dtype=out_dtype, device=y.device),
+                   dz=torch.empty(y.shape, dtype=out_dtype, device=y.device),
+                   dw=torch.empty((D,), dtype=torch.float32, device=y.device))
+    nbytes = lib.ssd_gated_norm_workspace_size(ctypes.byref(shape))
+    if nbytes == 0:
+        raise SSDError("ssd_gated_norm_workspace_size", 2)
+    ws = _workspace(nbytes, y.device, workspace)
+    stream = torch.cuda.current_stream(y.device).cuda_stream
+    st = lib.ssd_gated_norm_bwd(ctypes.byref(shape), _ptr(y), _ptr(z), _ptr(w), _ptr(rstd),
+                                _ptr(dout), _ptr(out["dy"]), _ptr(out["dz"]), _ptr(out["dw"]),
+                                _ptr(ws), ctypes.c_size_t(ws.numel()), ctypes.c_void_p(stream))
+    if st != 0:
+        raise SSDError("ssd_gated_norm_bwd", st)
+    return out
+
+
 def segment_decay(dt, dt_bias, A):
     """decay (b, h) = exp(A[h] * sum_t softplus(dt[b, t, h] + dt_bias[h])) over
     the whole of dt's sequence: the factor by which a state entering this

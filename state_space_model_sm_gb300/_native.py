@@ -92,8 +92,15 @@ class FwdLayout(ctypes.Structure):
 
 
 # Every symbol include/ssd.h declares, with its ctypes signature.
+class NormShape(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int64), ("features", ctypes.c_int64),
+                ("group_size", ctypes.c_int64), ("eps", ctypes.c_float),
+                ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32)]
+
+
 _VP = ctypes.c_void_p
 _SP = ctypes.POINTER(Shape)
+_NP = ctypes.POINTER(NormShape)
 SIGNATURES = {
     "ssd_fwd_workspace_size": ([_SP], ctypes.c_size_t),
     "ssd_bwd_workspace_size": ([_SP], ctypes.c_size_t),
@@ -112,6 +119,9 @@ SIGNATURES = {
     "ssd_fwd_noalloc": ([_SP] + [_VP] * 10 + [_VP], ctypes.c_int),
     "ssd_noalloc_scratch_bytes": ([], ctypes.c_size_t),
     "ssd_segment_decay": ([_SP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "ssd_gated_norm_workspace_size": ([_NP], ctypes.c_size_t),
+    "ssd_gated_norm_fwd": ([_NP] + [_VP] * 5 + [_VP], ctypes.c_int),
+    "ssd_gated_norm_bwd": ([_NP] + [_VP] * 9 + [ctypes.c_size_t, _VP], ctypes.c_int),
     "ssd_fwd_final_state": ([_SP] + [_VP] * 7 + [_VP, ctypes.c_size_t, _VP], ctypes.c_int),
     "ssd_bwd_dinit": ([_SP] + [_VP] * 7 + [_VP, ctypes.c_size_t, _VP], ctypes.c_int),
     "ssd_state_scan": ([ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,

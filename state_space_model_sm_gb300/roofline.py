@@ -132,3 +132,30 @@ def step_flops(d: Dims) -> int:
     bwd += bch * (tri * d.P + 2 * d.L * d.N * d.P)            # dx
     bwd += 2 * bch * (tri * d.N + 2 * d.L * d.P * d.N)        # dC, dB
     return int(fwd + bwd)
+
+
+# ------------------------------------------------------------ gated norm
+@dataclasses.dataclass
+class NormDims:
+    """rows = batch * seqlen, features = nheads * headdim; ib / ob bytes of an
+    element of y, z, dout / of out, dy, dz."""
+    rows: int
+    features: int
+    group_size: int
+    ib: int = 2
+    ob: int = 2
+
+
+def norm_kernel_bytes(name: str, d: NormDims) -> int:
+    """Algorithmic bytes of one launch: the forward reads y, z and writes out
+    and rstd; the backward reads y, z, dout and the saved rstd and writes dy,
+    dz (dw, one row of fp32, is counted where it is written)."""
+    md = d.rows * d.features
+    rs = d.rows * (d.features // d.group_size) * 4
+    if name == "k_gated_norm_fwd":
+        return md * (2 * d.ib + d.ob) + rs
+    if name == "k_gated_norm_bwd":
+        return md * (3 * d.ib + 2 * d.ob) + rs
+    if name == "k_norm_dw_reduce":
+        return d.features * 4
+    raise KeyError(name)
