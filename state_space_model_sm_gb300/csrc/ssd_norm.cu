@@ -122,7 +122,12 @@ __device__ __forceinline__ ThreadMap thread_map(const NormDims& d) {
 // barrier of the call in between.
 template <bool kBig>
 __device__ __forceinline__ float group_sum(float v, const ThreadMap& m, float (*red)[32], int ph) {
-  for (int o = m.wl >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if constexpr (kBig) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  } else {
+    for (int o = m.wl >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  }
   if constexpr (kBig) {
     if ((threadIdx.x & 31) == 0) red[ph][threadIdx.x >> 5] = v;
     __syncthreads();
@@ -192,8 +197,9 @@ __device__ __forceinline__ int ring_start(const NormDims& d, const RowRing<NTENS
   return mine;
 }
 
-// Item k's stage (s, phase) is full: warp 0 waits on its barrier (bounded)
-// while the other warps wait at the CTA barrier, which costs no issue slots;
+// Item k's stage (s, phase) is full: warp 0 waits on its barrier (bounded,
+// suspending between tries) while the other warps wait at the CTA barrier,
+// neither of which costs issue slots;
 // the barrier also tells thread 0 that every thread is past item k - 1, so it
 // refills item k - 1's stage (sprev).  False (for every thread) after a
 // timeout.
@@ -202,7 +208,7 @@ __device__ __forceinline__ bool ring_acquire(const NormDims& d, const RowRing<NT
                                              int k, int s, uint32_t phase, int sprev, int mine,
                                              int& issued, int* status, int* abort_flag) {
   bool got = true;
-  if (threadIdx.x < 32) got = mbar_wait(&ring.full[s], phase, status, abort_flag);
+  if (threadIdx.x < 32) got = mbar_wait_suspend(&ring.full[s], phase, status, abort_flag);
   if (!__syncthreads_and(got)) return false;
   if (threadIdx.x == 0 && k > 0 && issued < mine) {
     ring.issue(d, blockIdx.x + issued * gridDim.x, sprev);
@@ -290,12 +296,16 @@ __global__ void __launch_bounds__(kMaxNT, 2)
   for (int i = 0; i < 4; ++i) dw2[i] = f2(0.f);
   int row = blockIdx.x * d.RPC + m.slot;
   const int row_step = gridDim.x * d.RPC;
+  // the saved rstd of this thread's next row, loaded one item ahead
+  float r_next = (rstd && row < d.M) ? rstd[(int64_t)row * ngr + m.grp] : 0.f;
   int s = 0, sprev = 0;
   uint32_t phase = 0;
   int k = 0;
   for (; k < mine; ++k) {
     if (!ring_acquire(d, ring, k, s, phase, sprev, mine, issued, status, &abort_flag)) break;
     const bool live = row < d.M;
+    float r = r_next;
+    if (rstd && row + row_step < d.M) r_next = rstd[(int64_t)(row + row_step) * ngr + m.grp];
     const Tin* st = sy + s * 3 * tile_e;
     // live across the group sums: silu(z), y silu'(z), xhat, dout w, dw
     float2 sl[4], yd[4], xh[4], gv[4];
@@ -314,7 +324,6 @@ __global__ void __launch_bounds__(kMaxNT, 2)
       }
     }
     lds8(st + 2 * tile_e, gv);
-    float r = (rstd && live) ? rstd[(int64_t)row * ngr + m.grp] : 0.f;
     int ph = 0;
     if (!rstd) {
       float2 ss2 = f2(0.f);
@@ -370,22 +379,32 @@ __global__ void __launch_bounds__(kMaxNT, 2)
   }
 }
 
-// dw[f] = sum over parts p (in order) of part[p][f]; grid ceil(D / 32),
-// 256 threads: warp k sums parts k, k + 8, ..., then the 8 warp sums in order.
-__global__ void __launch_bounds__(256)
+// dw[f] = the sum over parts p of part[p][f] in a fixed order.  Grid
+// ceil(D / 32) blocks of 512 threads: thread (slice, c) sums parts slice,
+// slice + 16, ... of column c into four interleaved accumulators (loads in
+// flight), then the 16 slice sums are added in slice order.
+__global__ void __launch_bounds__(512)
     k_norm_dw_reduce(const float* __restrict__ part, float* __restrict__ dw, int nparts, int D) {
-  __shared__ float s8[8][32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int f = blockIdx.x * 32 + lane;
-  float s = 0.f;
-  if (f < D)
-    for (int p = warp; p < nparts; p += 8) s += part[(int64_t)p * D + f];
-  s8[warp][lane] = s;
+  __shared__ float ssum[16][32];
+  const int c = threadIdx.x & 31, sl = threadIdx.x >> 5;
+  const int f = blockIdx.x * 32 + c;
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  if (f < D) {
+    int p = sl;
+    for (; p + 48 < nparts; p += 64) {
+      a0 += part[(int64_t)p * D + f];
+      a1 += part[(int64_t)(p + 16) * D + f];
+      a2 += part[(int64_t)(p + 32) * D + f];
+      a3 += part[(int64_t)(p + 48) * D + f];
+    }
+    for (; p < nparts; p += 16) a0 += part[(int64_t)p * D + f];
+  }
+  ssum[sl][c] = (a0 + a1) + (a2 + a3);
   __syncthreads();
-  if (warp == 0 && f < D) {
+  if (sl == 0 && f < D) {
     float t = 0.f;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) t += s8[q][lane];
+    for (int q = 0; q < 16; ++q) t += ssum[q][c];
     dw[f] = t;
   }
 }
@@ -421,11 +440,23 @@ int norm_supported(const NormDims& d) {
   return tpr_ok && tpg_ok ? SSD_OK : SSD_ERR_UNSUPPORTED;
 }
 
-// ring depth for ntens tensors of elt bytes: about kRingBytes, 2 .. kMaxStages
-int ring_stages(const NormDims& d, int ntens, int elt) {
+// ring depth for ntens tensors of elt bytes: as many stages as fit in the
+// shared memory left to each CTA when registers allow `ctas` CTAs per SM
+// (at most kRingBytes), between 2 and kMaxStages
+int ring_stages(const NormDims& d, int ntens, int elt, int ctas, size_t other) {
   const size_t stage = (size_t)ntens * d.RPC * d.D * elt;
-  const size_t ns = kRingBytes / stage;
+  const size_t per_cta = (size_t)(220 * 1024) / (size_t)(ctas < 2 ? 2 : ctas);
+  size_t budget = per_cta > other ? per_cta - other : 0;
+  if (budget > (size_t)kRingBytes) budget = kRingBytes;
+  const size_t ns = budget / stage;
   return ns < 2 ? 2 : (ns > (size_t)kMaxStages ? kMaxStages : (int)ns);
+}
+
+// CTAs per SM that the kernel's registers and threads allow (at most 4)
+int reg_ctas(const void* kern, int nt) {
+  int per = 1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, nt, 0);
+  return per < 1 ? 1 : (per > 4 ? 4 : per);
 }
 
 int norm_grid(const NormDims& d, const void* kern, int nt, size_t smem) {
@@ -445,12 +476,13 @@ int launch_norm_fwd(NormDims d, const void* y, const void* z, const float* w, vo
   int* status = device_status_ptr();
   if (!status) return SSD_ERR_CUDA;
   const int nt = d.RPC * d.TPR;
-  d.NS = ring_stages(d, 2, sizeof(Tin));
-  const size_t smem = (size_t)d.NS * 2 * d.RPC * d.D * sizeof(Tin) + (size_t)d.D * sizeof(float);
   const bool big = d.TPG > 32;
   auto kb = k_gated_norm_fwd<Tin, Tout, true>;
   auto ks = k_gated_norm_fwd<Tin, Tout, false>;
-  const int grid = norm_grid(d, big ? (const void*)kb : (const void*)ks, nt, smem);
+  const void* kern = big ? (const void*)kb : (const void*)ks;
+  d.NS = ring_stages(d, 2, sizeof(Tin), reg_ctas(kern, nt), (size_t)d.D * sizeof(float));
+  const size_t smem = (size_t)d.NS * 2 * d.RPC * d.D * sizeof(Tin) + (size_t)d.D * sizeof(float);
+  const int grid = norm_grid(d, kern, nt, smem);
   const Tin* yy = static_cast<const Tin*>(y);
   const Tin* zz = static_cast<const Tin*>(z);
   Tout* oo = static_cast<Tout*>(out);
@@ -470,14 +502,15 @@ int launch_norm_bwd(NormDims d, const void* y, const void* z, const float* w,
   int* status = device_status_ptr();
   if (!status) return SSD_ERR_CUDA;
   const int nt = d.RPC * d.TPR;
-  d.NS = ring_stages(d, 3, sizeof(Tin));
-  const size_t ring_b = (size_t)d.NS * 3 * d.RPC * d.D * sizeof(Tin);
-  const size_t part_b = (size_t)nt * kV * sizeof(float);  // dw partials alias the ring
-  const size_t smem = (ring_b > part_b ? ring_b : part_b) + (size_t)d.D * sizeof(float);
   const bool big = d.TPG > 32;
   auto kb = k_gated_norm_bwd<Tin, Tout, true>;
   auto ks = k_gated_norm_bwd<Tin, Tout, false>;
-  const int grid = norm_grid(d, big ? (const void*)kb : (const void*)ks, nt, smem);
+  const void* kern = big ? (const void*)kb : (const void*)ks;
+  d.NS = ring_stages(d, 3, sizeof(Tin), reg_ctas(kern, nt), (size_t)d.D * sizeof(float));
+  const size_t ring_b = (size_t)d.NS * 3 * d.RPC * d.D * sizeof(Tin);
+  const size_t part_b = (size_t)nt * kV * sizeof(float);  // dw partials alias the ring
+  const size_t smem = (ring_b > part_b ? ring_b : part_b) + (size_t)d.D * sizeof(float);
+  const int grid = norm_grid(d, kern, nt, smem);
   const Tin* yy = static_cast<const Tin*>(y);
   const Tin* zz = static_cast<const Tin*>(z);
   const Tin* gg = static_cast<const Tin*>(dout);
@@ -490,7 +523,7 @@ int launch_norm_bwd(NormDims d, const void* y, const void* z, const float* w,
     SSD_LAUNCH("k_gated_norm_bwd", s,
                ks<<<grid, nt, smem, s>>>(yy, zz, w, rstd, gg, a, b, part, d, status));
   SSD_LAUNCH("k_norm_dw_reduce", s,
-             k_norm_dw_reduce<<<(d.D + 31) / 32, 256, 0, s>>>(part, dw, grid, d.D));
+             k_norm_dw_reduce<<<(d.D + 31) / 32, 512, 0, s>>>(part, dw, grid, d.D));
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

@@ -109,6 +109,37 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   }
 }
 
+// As mbar_wait, but each try suspends the thread until the phase completes
+// or about kSuspendHintNs pass (the hint of mbarrier.try_wait), so a thread
+// that waits long issues a few instructions instead of spinning.
+constexpr uint32_t kSuspendHintNs = 20000;
+__device__ __forceinline__ uint32_t mbar_try_wait_suspend(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok;
+}
+__device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity, int* status,
+                                                  volatile int* abort_flag) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_suspend(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (*abort_flag) return false;
+    if (mbar_try_wait_suspend(a, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (status) atomicExch(status, kStatusTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 // Arrive (release, CTA scope) on the mbarrier: one of its expected arrivals.
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
