@@ -661,6 +661,8 @@ def run_gated_norm(args):
                "kind": "oracle",
                "sample": f"rows 0..{n - 1} of {args.norm_workload}, forward + backward, "
                          f"{reps} repetitions in {sec:.1f} s (numpy fp64, one thread)"}
+    from state_space_model_sm_gb300 import tuning
+    launch_cfg, from_table = tuning.get_norm_config(shape.features, gs, dtype)
     rows = shape.rows
     out_line = {
         "metric": "gated RMSNorm fwd+bwd tokens/sec on 1 GB300 (the step after the SSD output)",
@@ -673,6 +675,9 @@ def run_gated_norm(args):
                    "group_size": gs, "eps": eps, "l2": "flushed (512 MB write) before every step"},
         "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "gpu_launches": launches,
         "clocks": clk.summary(), "gpu": torch.cuda.get_device_name(dev),
+        "launch_config": dict(launch_cfg, source="table" if from_table else "built-in",
+                              table=os.environ.get("SSD_TUNING_TABLE", tuning.DEFAULT_TABLE)
+                              if from_table else None),
     }
     print(json.dumps(out_line))
 

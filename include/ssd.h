@@ -253,6 +253,30 @@ int ssd_gated_norm_bwd(const ssd_norm_shape* shape, const void* y, const void* z
                        const float* w, const float* rstd, const void* dout, void* dy, void* dz,
                        float* dw, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Launch configuration of the gated-norm kernels for one shape, as an
+ * offline sweep chooses it (the pages' ahead-of-time config generator,
+ * "Cutting autotuning overhead with an automated config generator", Fig. 4:
+ * search per environment ahead of time, store the result, load it at start):
+ * rows_per_item = rows per CTA work
+ * item (the CTA has rows_per_item * features / 8 threads, at most 512 and a
+ * multiple of 32); ring_kb = shared-memory ring size aimed at per CTA
+ * (8 .. 200); ctas_per_sm = persistent CTAs per SM at most (1 .. 8).  A zero
+ * field keeps the built-in choice. */
+typedef struct {
+  int32_t rows_per_item, ring_kb, ctas_per_sm;
+} ssd_norm_config;
+
+/* Sets (config != NULL) or removes (NULL) the table entry for shape's
+ * (features, group_size, in_dtype, out_dtype); rows and eps are ignored.
+ * Thread-safe; at most 64 entries (else SSD_ERR_UNSUPPORTED).  Returns
+ * SSD_ERR_INVALID_ARG for an invalid shape or field. */
+int ssd_gated_norm_set_config(const ssd_norm_shape* shape, const ssd_norm_config* config);
+
+/* The configuration the next call with this shape will use (the table's
+ * fields where set, the built-in choice elsewhere) in *out.  Returns 1 if a
+ * table entry exists, 0 if not, -SSD_ERR_INVALID_ARG for a bad shape. */
+int ssd_gated_norm_get_config(const ssd_norm_shape* shape, ssd_norm_config* out);
+
 /* Diagnostic: one tcgen05 tile product on the current device,
  * D[128][nn] = A[128][k] * B[nn][k]^T (A, B bf16 row-major, D f32 row-major,
  * all device memory), with A and B staged in shared memory K-major (0) or

@@ -98,6 +98,11 @@ class NormShape(ctypes.Structure):
                 ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32)]
 
 
+class NormConfig(ctypes.Structure):
+    _fields_ = [("rows_per_item", ctypes.c_int32), ("ring_kb", ctypes.c_int32),
+                ("ctas_per_sm", ctypes.c_int32)]
+
+
 _VP = ctypes.c_void_p
 _SP = ctypes.POINTER(Shape)
 _NP = ctypes.POINTER(NormShape)
@@ -120,6 +125,8 @@ SIGNATURES = {
     "ssd_noalloc_scratch_bytes": ([], ctypes.c_size_t),
     "ssd_segment_decay": ([_SP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
     "ssd_gated_norm_workspace_size": ([_NP], ctypes.c_size_t),
+    "ssd_gated_norm_set_config": ([_NP, ctypes.POINTER(NormConfig)], ctypes.c_int),
+    "ssd_gated_norm_get_config": ([_NP, ctypes.POINTER(NormConfig)], ctypes.c_int),
     "ssd_gated_norm_fwd": ([_NP] + [_VP] * 5 + [_VP], ctypes.c_int),
     "ssd_gated_norm_bwd": ([_NP] + [_VP] * 9 + [ctypes.c_size_t, _VP], ctypes.c_int),
     "ssd_fwd_final_state": ([_SP] + [_VP] * 7 + [_VP, ctypes.c_size_t, _VP], ctypes.c_int),
@@ -146,5 +153,7 @@ def load(path: str = LIB):
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = res
+            from . import tuning  # the offline launch table, applied once at load
+            tuning.apply_default(lib)
             _lib = lib
     return _lib

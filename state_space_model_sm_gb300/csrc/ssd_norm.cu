@@ -24,6 +24,8 @@
 // (again bounded) and returns.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "ssd_internal.h"
 #include "tc_ptx.cuh"
 
@@ -83,6 +85,8 @@ struct NormDims {
   int n_iter;  // items: ceil(M / RPC)
   int NS;      // ring stages
   float eps;
+  int ring_cap;  // ring bytes aimed at
+  int cta_cap;   // CTAs per SM at most
 };
 
 // This thread's place: its row slot and 8 features within an item, its
@@ -409,6 +413,43 @@ __global__ void __launch_bounds__(512)
   }
 }
 
+// ------------------------------------------------------ launch-config table
+// Per-shape launch parameters set through ssd_gated_norm_set_config (an
+// offline sweep's table, loaded at start-up); a zero field keeps the
+// built-in choice.  Keyed by (features, group_size, in_dtype, out_dtype):
+// the row count does not change the best launch once there are many rows.
+struct NormEntry {
+  int64_t features, group_size;
+  int32_t in_dtype, out_dtype;
+  ssd_norm_config cfg;
+};
+constexpr int kMaxNormEntries = 64;
+NormEntry g_norm_table[kMaxNormEntries];
+int g_norm_entries = 0;
+std::mutex g_norm_mu;
+
+bool same_key(const NormEntry& e, const ssd_norm_shape* s) {
+  return e.features == s->features && e.group_size == s->group_size &&
+         e.in_dtype == s->in_dtype && e.out_dtype == s->out_dtype;
+}
+
+bool table_lookup(const ssd_norm_shape* s, ssd_norm_config* out) {
+  std::lock_guard<std::mutex> lk(g_norm_mu);
+  for (int i = 0; i < g_norm_entries; ++i)
+    if (same_key(g_norm_table[i], s)) {
+      *out = g_norm_table[i].cfg;
+      return true;
+    }
+  return false;
+}
+
+// rows per item valid for a row of TPR threads: the CTA (RPC * TPR threads)
+// stays within kMaxNT and tiles whole warps
+bool rpc_ok(int rpc, int TPR) {
+  const int nt = rpc * TPR;
+  return rpc >= 1 && nt <= kMaxNT && nt % 32 == 0;
+}
+
 bool norm_dims(const ssd_norm_shape* s, NormDims* d) {
   if (!s || s->rows < 0 || s->features < 8 || s->group_size < 8) return false;
   if (s->features % 8 || s->group_size % 8 || s->features % s->group_size) return false;
@@ -425,6 +466,14 @@ bool norm_dims(const ssd_norm_shape* s, NormDims* d) {
   d->TPG = d->gs / kV;
   d->eps = s->eps;
   d->RPC = d->TPR < kMaxNT ? kMaxNT / d->TPR : 1;
+  d->ring_cap = kRingBytes;
+  d->cta_cap = kNormMaxCtasPerSm;
+  ssd_norm_config cfg;
+  if (table_lookup(s, &cfg)) {
+    if (cfg.rows_per_item > 0 && rpc_ok(cfg.rows_per_item, d->TPR)) d->RPC = cfg.rows_per_item;
+    if (cfg.ring_kb > 0) d->ring_cap = cfg.ring_kb * 1024;
+    if (cfg.ctas_per_sm > 0) d->cta_cap = cfg.ctas_per_sm;
+  }
   d->n_iter = (int)((s->rows + d->RPC - 1) / d->RPC);
   d->NS = 0;
   return true;
@@ -447,7 +496,7 @@ int ring_stages(const NormDims& d, int ntens, int elt, int ctas, size_t other) {
   const size_t stage = (size_t)ntens * d.RPC * d.D * elt;
   const size_t per_cta = (size_t)(220 * 1024) / (size_t)(ctas < 2 ? 2 : ctas);
   size_t budget = per_cta > other ? per_cta - other : 0;
-  if (budget > (size_t)kRingBytes) budget = kRingBytes;
+  if (budget > (size_t)d.ring_cap) budget = d.ring_cap;
   const size_t ns = budget / stage;
   return ns < 2 ? 2 : (ns > (size_t)kMaxStages ? kMaxStages : (int)ns);
 }
@@ -465,7 +514,7 @@ int norm_grid(const NormDims& d, const void* kern, int nt, size_t smem) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, nt, smem);
-  per = per < 1 ? 1 : (per > kNormMaxCtasPerSm ? kNormMaxCtasPerSm : per);
+  per = per < 1 ? 1 : (per > d.cta_cap ? d.cta_cap : per);
   const int64_t g = (int64_t)per * sms;
   return (int)(d.n_iter < g ? d.n_iter : g);
 }
@@ -543,6 +592,45 @@ size_t ssd_gated_norm_workspace_size(const ssd_norm_shape* shape) {
   cudaGetDevice(&dev);
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 256;
   return (size_t)kNormMaxCtasPerSm * sms * d.D * sizeof(float);
+}
+
+int ssd_gated_norm_set_config(const ssd_norm_shape* shape, const ssd_norm_config* config) {
+  NormDims d;
+  if (!norm_dims(shape, &d) || norm_supported(d) != SSD_OK) return SSD_ERR_INVALID_ARG;
+  if (config) {
+    if (config->rows_per_item < 0 || config->ring_kb < 0 || config->ctas_per_sm < 0)
+      return SSD_ERR_INVALID_ARG;
+    if (config->rows_per_item > 0 && !rpc_ok(config->rows_per_item, d.TPR))
+      return SSD_ERR_INVALID_ARG;
+    if (config->ring_kb > 0 && (config->ring_kb < 8 || config->ring_kb > 200))
+      return SSD_ERR_INVALID_ARG;
+    if (config->ctas_per_sm > kNormMaxCtasPerSm) return SSD_ERR_INVALID_ARG;
+  }
+  std::lock_guard<std::mutex> lk(g_norm_mu);
+  int i = 0;
+  while (i < g_norm_entries && !same_key(g_norm_table[i], shape)) ++i;
+  if (!config) {  // remove
+    if (i < g_norm_entries) g_norm_table[i] = g_norm_table[--g_norm_entries];
+    return SSD_OK;
+  }
+  if (i == g_norm_entries) {
+    if (g_norm_entries == kMaxNormEntries) return SSD_ERR_UNSUPPORTED;
+    ++g_norm_entries;
+  }
+  g_norm_table[i] = NormEntry{shape->features, shape->group_size, shape->in_dtype,
+                              shape->out_dtype, *config};
+  return SSD_OK;
+}
+
+int ssd_gated_norm_get_config(const ssd_norm_shape* shape, ssd_norm_config* out) {
+  NormDims d;
+  if (!out || !norm_dims(shape, &d) || norm_supported(d) != SSD_OK) return -SSD_ERR_INVALID_ARG;
+  ssd_norm_config cfg;
+  const bool set = table_lookup(shape, &cfg);
+  out->rows_per_item = d.RPC;
+  out->ring_kb = d.ring_cap / 1024;
+  out->ctas_per_sm = d.cta_cap;
+  return set ? 1 : 0;
 }
 
 int ssd_gated_norm_fwd(const ssd_norm_shape* shape, const void* y, const void* z,

@@ -1,0 +1,145 @@
+"""The gated-norm launch table: validation, the per-shape table inside the
+library (set / get / remove through the C ABI, host-only calls that need no
+GPU), the packaged table, and on the GPU that a tuned launch computes the
+same result as the built-in one."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from state_space_model_sm_gb300 import tuning
+
+
+def _entry(**kw):
+    e = dict(features=4096, group_size=512, in_dtype="bf16", out_dtype="bf16", rows_per_item=1,
+             ring_kb=64, ctas_per_sm=2)
+    e.update(kw)
+    return e
+
+
+def _table(*entries):
+    return {"kind": tuning.TABLE_KIND, "entries": list(entries)}
+
+
+def test_validate_accepts_a_good_table():
+    tuning.validate_table(_table(_entry(), _entry(features=1536, group_size=1536,
+                                                  rows_per_item=2)))
+
+
+@pytest.mark.parametrize("bad", [
+    dict(rows_per_item=2),                  # 2 x 512 threads: more than a CTA
+    dict(features=1536, group_size=1536, rows_per_item=3),  # 576 threads
+    dict(features=64, group_size=16, rows_per_item=3),      # 24 threads: not whole warps
+    dict(ring_kb=4), dict(ring_kb=300), dict(ctas_per_sm=9), dict(ctas_per_sm=-1),
+    dict(group_size=500), dict(in_dtype="fp16"),
+])
+def test_validate_rejects(bad):
+    with pytest.raises(ValueError):
+        tuning.validate_table(_table(_entry(**bad)))
+
+
+def test_validate_rejects_duplicates_and_wrong_kind():
+    with pytest.raises(ValueError):
+        tuning.validate_table(_table(_entry(), _entry()))
+    with pytest.raises(ValueError):
+        tuning.validate_table({"kind": "other", "entries": []})
+
+
+def test_library_table_set_get_remove():
+    F, G = 2048, 256
+    tuning.clear_norm_config(F, G)
+    cfg, from_table = tuning.get_norm_config(F, G)
+    assert not from_table and cfg["rows_per_item"] == 512 // (F // 8)
+    tuning.set_norm_config(F, G, rows_per_item=1, ring_kb=48, ctas_per_sm=3)
+    cfg, from_table = tuning.get_norm_config(F, G)
+    assert from_table and cfg == dict(rows_per_item=1, ring_kb=48, ctas_per_sm=3)
+    # a zero field keeps the built-in choice
+    tuning.set_norm_config(F, G, ring_kb=40)
+    cfg, _ = tuning.get_norm_config(F, G)
+    assert cfg["rows_per_item"] == 2 and cfg["ring_kb"] == 40
+    # other dtypes are other entries
+    assert not tuning.get_norm_config(F, G, "f32")[1]
+    tuning.clear_norm_config(F, G)
+    assert not tuning.get_norm_config(F, G)[1]
+
+
+@pytest.mark.parametrize("kw", [dict(rows_per_item=3), dict(ring_kb=201), dict(ctas_per_sm=9)])
+def test_library_rejects_invalid_fields(kw):
+    with pytest.raises(ValueError):
+        tuning.set_norm_config(2048, 256, **kw)
+
+
+def test_table_file_roundtrip_and_apply(tmp_path):
+    t = _table(_entry(features=1024, group_size=128, rows_per_item=4, ring_kb=32, ctas_per_sm=1))
+    p = tmp_path / "t.json"
+    p.write_text(json.dumps(t))
+    assert tuning.apply_table(json.loads(p.read_text())) == 1
+    cfg, from_table = tuning.get_norm_config(1024, 128)
+    assert from_table and cfg == dict(rows_per_item=4, ring_kb=32, ctas_per_sm=1)
+    tuning.clear_norm_config(1024, 128)
+
+
+def test_default_table_env_control(tmp_path, monkeypatch):
+    monkeypatch.setenv("SSD_TUNING_TABLE", "none")
+    assert tuning.apply_default(None) is None
+    p = tmp_path / "t.json"
+    p.write_text(json.dumps(_table(_entry(features=512, group_size=64, rows_per_item=2))))
+    monkeypatch.setenv("SSD_TUNING_TABLE", str(p))
+    assert tuning.apply_default(tuning._native.load()) == str(p)
+    assert tuning.get_norm_config(512, 64)[1]
+    tuning.clear_norm_config(512, 64)
+
+
+def test_packaged_table_is_valid_and_loaded():
+    if not os.path.exists(tuning.DEFAULT_TABLE):
+        pytest.skip("no packaged table")
+    with open(tuning.DEFAULT_TABLE) as f:
+        t = json.load(f)
+    tuning.validate_table(t)
+    assert t.get("generated_by", "").startswith("python -m state_space_model_sm_gb300.tuning")
+    if os.environ.get("SSD_TUNING_TABLE", tuning.DEFAULT_TABLE) == tuning.DEFAULT_TABLE:
+        for e in t["entries"]:
+            cfg, from_table = tuning.get_norm_config(e["features"], e["group_size"],
+                                                     e["in_dtype"], e["out_dtype"])
+            assert from_table
+            assert cfg["ring_kb"] == e["ring_kb"] and cfg["ctas_per_sm"] == e["ctas_per_sm"]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("F,G,cfg", [
+    (4096, 512, dict(rows_per_item=1, ring_kb=32, ctas_per_sm=1)),
+    (1536, 1536, dict(rows_per_item=1, ring_kb=48, ctas_per_sm=3)),
+    (256, 64, dict(rows_per_item=4, ring_kb=16, ctas_per_sm=4)),
+])
+def test_tuned_launch_computes_the_same(cuda_lib, F, G, cfg):
+    """Every row is computed by the same per-thread arithmetic whatever the
+    launch, so out, rstd, dy and dz are bit-identical; dw is summed over a
+    different CTA partition, equal to rounding."""
+    import torch
+    rows = 777
+    g = torch.Generator().manual_seed(F + G)
+    y, z, dout = (torch.randn(rows, F, generator=g).to("cuda", torch.bfloat16) for _ in range(3))
+    w = (1.0 + 0.1 * torch.randn(F, generator=g)).cuda()
+    saved, had = tuning.get_norm_config(F, G)
+
+    def run():
+        out, rstd = cuda_lib.gated_norm_fwd(y, z, w, G)
+        gr = cuda_lib.gated_norm_bwd(y, z, w, dout, G, rstd=rstd)
+        torch.cuda.synchronize()
+        return out, rstd, gr
+    try:
+        tuning.clear_norm_config(F, G)
+        a = run()
+        tuning.set_norm_config(F, G, **cfg)
+        b = run()
+    finally:
+        if had:
+            tuning.set_norm_config(F, G, **saved)
+        else:
+            tuning.clear_norm_config(F, G)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    assert torch.equal(a[2]["dy"], b[2]["dy"]) and torch.equal(a[2]["dz"], b[2]["dz"])
+    np.testing.assert_allclose(b[2]["dw"].cpu().numpy(), a[2]["dw"].cpu().numpy(), rtol=1e-5,
+                               atol=1e-5)
+    assert cuda_lib.device_status() == 0
