@@ -294,6 +294,11 @@ int ssd_selftest_mma(int a_mn, int b_mn, int swap_mn_offsets, int nn, int k, con
  * of ssd_get_device_status() without any GPU fault.  Asynchronous. */
 int ssd_selftest_timeout(void* stream);
 
+/* Diagnostic: as ssd_selftest_timeout, with the suspending bounded wait
+ * (mbarrier try_wait with a suspend-time hint) that the gated-norm kernels'
+ * row ring uses; it too records SSD_ERR_TIMEOUT after about 1 s and returns. */
+int ssd_selftest_timeout_suspend(void* stream);
+
 /* Static description of a status code. */
 const char* ssd_strerror(int status);
 

@@ -121,6 +121,7 @@ SIGNATURES = {
     "ssd_launch_count": ([], ctypes.c_int64),
     "ssd_selftest_mma": ([ctypes.c_int] * 5 + [_VP] * 4, ctypes.c_int),
     "ssd_selftest_timeout": ([_VP], ctypes.c_int),
+    "ssd_selftest_timeout_suspend": ([_VP], ctypes.c_int),
     "ssd_fwd_noalloc": ([_SP] + [_VP] * 10 + [_VP], ctypes.c_int),
     "ssd_noalloc_scratch_bytes": ([], ctypes.c_size_t),
     "ssd_segment_decay": ([_SP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),

@@ -148,6 +148,19 @@ __global__ void k_selftest_timeout(int* status) {
   mbar_wait(&bar, 0, status, &abort_flag);
 }
 
+// The same with the suspending wait of the row-streaming kernels.
+__global__ void k_selftest_timeout_suspend(int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait_suspend(&bar, 0, status, &abort_flag);
+}
+
 }  // namespace
 }  // namespace ssd
 
@@ -156,5 +169,14 @@ extern "C" int ssd_selftest_timeout(void* stream) {
   if (!status) return SSD_ERR_CUDA;
   SSD_LAUNCH("k_selftest_timeout", static_cast<cudaStream_t>(stream),
              ssd::k_selftest_timeout<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status));
+  return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+extern "C" int ssd_selftest_timeout_suspend(void* stream) {
+  int* status = ssd::device_status_ptr();
+  if (!status) return SSD_ERR_CUDA;
+  SSD_LAUNCH("k_selftest_timeout_suspend", static_cast<cudaStream_t>(stream),
+             ssd::k_selftest_timeout_suspend<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+                 status));
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }

@@ -22,6 +22,10 @@ def test_bounded_wait_reports_timeout_and_context_survives(cuda_lib):
     assert lib.ssd_selftest_timeout(ctypes.c_void_p(stream)) == 0
     assert cuda_lib.device_status() == 5           # SSD_ERR_TIMEOUT, read and cleared
     assert cuda_lib.device_status() == 0
+    # the suspending wait of the gated-norm row ring ends the same way
+    assert lib.ssd_selftest_timeout_suspend(ctypes.c_void_p(stream)) == 0
+    assert cuda_lib.device_status() == 5
+    assert cuda_lib.device_status() == 0
     # the context still runs kernels correctly
     inp = make_inputs(SSDShape(1, 300, 4, 64, 128, 1, 256), seed=8, dtype="bf16")
     t = to_torch(inp)
