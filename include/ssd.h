@@ -162,12 +162,19 @@ size_t ssd_noalloc_scratch_bytes(void);
  * same scan over the ranks after it, applied to the initial-state gradients.
  *
  * ssd_segment_decay: decay[b, h] = exp(A[h] * sum_t softplus(dt[b,t,h] +
- * dt_bias[h])) over the shape's seqlen (the sum in fp64).  Uses shape->batch,
- * seqlen, nheads and in_dtype (dt's dtype); dt (B, T, H), dt_bias (H) or
- * NULL, A (H), decay (B, H) f32, device memory.  Asynchronous on `stream`.
- * Returns SSD_ERR_INVALID_ARG for a NULL required pointer or a bad shape. */
+ * dt_bias[h])) over the shape's seqlen (the sum in fp64, split over the
+ * sequence and added back in a fixed order).  Uses shape->batch, seqlen,
+ * nheads and in_dtype (dt's dtype); dt (B, T, H), dt_bias (H) or NULL, A
+ * (H), decay (B, H) f32, device memory; workspace of
+ * ssd_segment_decay_workspace_size(shape) bytes (8-byte aligned,
+ * caller-owned; the size depends on the current device's SM count).
+ * Asynchronous on `stream`.  Returns SSD_ERR_INVALID_ARG for a NULL
+ * required pointer or a bad shape, SSD_ERR_WORKSPACE for a missing or small
+ * workspace. */
+size_t ssd_segment_decay_workspace_size(const ssd_shape* shape);
 int ssd_segment_decay(const ssd_shape* shape, const void* dt, const float* dt_bias,
-                      const float* A, float* decay, void* stream);
+                      const float* A, float* decay, void* workspace, size_t workspace_bytes,
+                      void* stream);
 
 /* ssd_state_scan: out = the exclusive scan of the maps S -> D_k * S + S_k
  * for rank `rank` of `nranks`: direction 0 runs over k = 0 .. rank-1

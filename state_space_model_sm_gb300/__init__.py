@@ -320,9 +320,10 @@ def segment_decay(dt, dt_bias, A):
     dt = dt.contiguous()
     out = torch.empty((Bt, H), dtype=torch.float32, device=dt.device)
     shape = make_shape(Bt, T, H, 1, 1, 1, 1, _dtype_code(dt.dtype), SSD_F32)
+    ws = _workspace(lib.ssd_segment_decay_workspace_size(ctypes.byref(shape)), dt.device, None)
     stream = torch.cuda.current_stream(dt.device).cuda_stream
     st = lib.ssd_segment_decay(ctypes.byref(shape), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(out),
-                               ctypes.c_void_p(stream))
+                               _ptr(ws), ctypes.c_size_t(ws.numel()), ctypes.c_void_p(stream))
     if st != 0:
         raise SSDError("ssd_segment_decay", st)
     return out

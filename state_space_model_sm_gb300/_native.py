@@ -124,7 +124,8 @@ SIGNATURES = {
     "ssd_selftest_timeout_suspend": ([_VP], ctypes.c_int),
     "ssd_fwd_noalloc": ([_SP] + [_VP] * 10 + [_VP], ctypes.c_int),
     "ssd_noalloc_scratch_bytes": ([], ctypes.c_size_t),
-    "ssd_segment_decay": ([_SP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "ssd_segment_decay_workspace_size": ([_SP], ctypes.c_size_t),
+    "ssd_segment_decay": ([_SP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP], ctypes.c_int),
     "ssd_gated_norm_workspace_size": ([_NP], ctypes.c_size_t),
     "ssd_gated_norm_set_config": ([_NP, ctypes.POINTER(NormConfig)], ctypes.c_int),
     "ssd_gated_norm_get_config": ([_NP, ctypes.POINTER(NormConfig)], ctypes.c_int),

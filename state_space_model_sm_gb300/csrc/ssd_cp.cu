@@ -23,22 +23,66 @@ __device__ __forceinline__ float load_dt<__nv_bfloat16>(const __nv_bfloat16* p) 
   return __bfloat162float(*p);
 }
 
-// One warp per (b, h): decay[b, h] = exp(A[h] * sum_t softplus(dt[b,t,h] +
-// dt_bias[h])), the sum in fp64.
+// decay[b, h] = exp(A[h] * sum_t softplus(dt[b,t,h] + dt_bias[h])), the sum
+// in fp64, in two deterministic stages.  Stage 1: grid (ceil(H / 32), B, KT),
+// 256 threads; lane = head (a warp's loads at one position are 32
+// consecutive heads), warp w sums positions w, w + 8, ... of the block's
+// range [kt * span, (kt + 1) * span); the 8 warp sums are added in warp
+// order into part[(b * H + h) * KT + kt].
 template <typename Tin>
-__global__ void k_segment_decay(const Tin* __restrict__ dt, const float* __restrict__ dt_bias,
-                                const float* __restrict__ A, float* __restrict__ decay, int B,
-                                int T, int H) {
-  const int wid = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (wid >= B * H) return;
-  const int b = wid / H, h = wid % H;
-  const float bias = dt_bias ? dt_bias[h] : 0.f;
+__global__ void __launch_bounds__(256)
+    k_segment_decay_part(const Tin* __restrict__ dt, const float* __restrict__ dt_bias,
+                         double* __restrict__ part, int T, int H, int KT, int span) {
+  __shared__ double red[8][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int h = blockIdx.x * 32 + lane, b = blockIdx.y, kt = blockIdx.z;
+  const int t0 = kt * span, t1 = min(T, t0 + span);
   double s = 0.0;
-  for (int t = lane; t < T; t += 32)
-    s += (double)dt_softplus(load_dt(dt + ((int64_t)b * T + t) * H + h) + bias);
+  if (h < H) {
+    const float bias = dt_bias ? dt_bias[h] : 0.f;
+    const Tin* p = dt + (int64_t)b * T * H + h;
+    int t = t0 + warp;
+    for (; t + 24 < t1; t += 32) {  // four positions in flight per lane
+      const float v0 = load_dt(p + (int64_t)t * H), v1 = load_dt(p + (int64_t)(t + 8) * H);
+      const float v2 = load_dt(p + (int64_t)(t + 16) * H), v3 = load_dt(p + (int64_t)(t + 24) * H);
+      s += (double)dt_softplus(v0 + bias);
+      s += (double)dt_softplus(v1 + bias);
+      s += (double)dt_softplus(v2 + bias);
+      s += (double)dt_softplus(v3 + bias);
+    }
+    for (; t < t1; t += 8) s += (double)dt_softplus(load_dt(p + (int64_t)t * H) + bias);
+  }
+  red[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && h < H) {
+    double tot = 0.0;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (lane == 0) decay[wid] = (float)exp((double)A[h] * s);
+    for (int w = 0; w < 8; ++w) tot += red[w][lane];
+    part[((int64_t)b * H + h) * KT + kt] = tot;
+  }
+}
+
+// Stage 2: one thread per (b, h): the KT partials in order, then the decay.
+__global__ void __launch_bounds__(256)
+    k_segment_decay_finish(const double* __restrict__ part, const float* __restrict__ A,
+                           float* __restrict__ decay, int BH, int H, int KT) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= BH) return;
+  double s = 0.0;
+  for (int k = 0; k < KT; ++k) s += part[(int64_t)i * KT + k];
+  decay[i] = (float)exp((double)A[i % H] * s);
+}
+
+// positions per stage-1 block: about 4 blocks per SM over the whole grid,
+// at least 256 positions a block
+int decay_span(const ssd_shape* s, int sms) {
+  const int64_t hb = (s->nheads + 31) / 32;
+  const int64_t want = 4 * (int64_t)sms;
+  int64_t kt = (want + s->batch * hb - 1) / (s->batch * hb);
+  const int64_t kt_max = (s->seqlen + 255) / 256;
+  if (kt > kt_max) kt = kt_max;
+  if (kt < 1) kt = 1;
+  return (int)((s->seqlen + kt - 1) / kt);
 }
 
 // One thread per element of the (BH, PN) state: acc <- D_k * acc + S_k over
@@ -104,22 +148,50 @@ void cp_dinit_chain(const Dims& d, const float* dHs, const float* acs, const flo
 
 }  // namespace ssd
 
+namespace {
+bool decay_shape_ok(const ssd_shape* shape) {
+  if (!shape || shape->batch < 1 || shape->seqlen < 1 || shape->nheads < 1) return false;
+  if (shape->in_dtype != SSD_F32 && shape->in_dtype != SSD_BF16) return false;
+  return shape->batch < 65536 && shape->nheads < ((int64_t)1 << 20) &&
+         shape->seqlen < ((int64_t)1 << 31);
+}
+int current_sms() {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 148;
+  return sms;
+}
+}  // namespace
+
+extern "C" size_t ssd_segment_decay_workspace_size(const ssd_shape* shape) {
+  if (!decay_shape_ok(shape)) return 0;
+  const int span = ssd::decay_span(shape, current_sms());
+  const int64_t kt = (shape->seqlen + span - 1) / span;
+  return (size_t)(shape->batch * shape->nheads * kt) * sizeof(double);
+}
+
 extern "C" int ssd_segment_decay(const ssd_shape* shape, const void* dt, const float* dt_bias,
-                                 const float* A, float* decay, void* stream) {
-  if (!shape || !dt || !A || !decay) return SSD_ERR_INVALID_ARG;
-  if (shape->batch < 1 || shape->seqlen < 1 || shape->nheads < 1) return SSD_ERR_INVALID_ARG;
-  if (shape->in_dtype != SSD_F32 && shape->in_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
-  const int64_t warps = shape->batch * shape->nheads;
-  if (warps > (int64_t)1 << 30 || shape->seqlen > ((int64_t)1 << 31) - 1) return SSD_ERR_INVALID_ARG;
-  const int blocks = (int)((warps + 7) / 8);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+                                 const float* A, float* decay, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (!decay_shape_ok(shape) || !dt || !A || !decay) return SSD_ERR_INVALID_ARG;
+  const int span = ssd::decay_span(shape, current_sms());
+  const int KT = (int)((shape->seqlen + span - 1) / span);
   const int B = (int)shape->batch, T = (int)shape->seqlen, H = (int)shape->nheads;
+  if (!workspace || workspace_bytes < (size_t)B * H * KT * sizeof(double) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 7))
+    return SSD_ERR_WORKSPACE;
+  double* part = static_cast<double*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const dim3 grid((H + 31) / 32, B, KT);
   if (shape->in_dtype == SSD_BF16)
-    SSD_LAUNCH("k_segment_decay", s, ssd::k_segment_decay<__nv_bfloat16><<<blocks, 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(dt), dt_bias, A, decay, B, T, H));
+    SSD_LAUNCH("k_segment_decay", s, ssd::k_segment_decay_part<__nv_bfloat16><<<grid, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(dt), dt_bias, part, T, H, KT, span));
   else
-    SSD_LAUNCH("k_segment_decay", s, ssd::k_segment_decay<float><<<blocks, 256, 0, s>>>(
-        static_cast<const float*>(dt), dt_bias, A, decay, B, T, H));
+    SSD_LAUNCH("k_segment_decay", s, ssd::k_segment_decay_part<float><<<grid, 256, 0, s>>>(
+        static_cast<const float*>(dt), dt_bias, part, T, H, KT, span));
+  const int BH = B * H;
+  SSD_LAUNCH("k_segment_decay_finish", s, ssd::k_segment_decay_finish<<<(BH + 255) / 256, 256, 0, s>>>(
+      part, A, decay, BH, H, KT));
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
