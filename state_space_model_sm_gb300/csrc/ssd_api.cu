@@ -62,8 +62,13 @@ struct Carver {
 };
 
 struct FwdOffsets {
-  size_t delta, acs, S, Hprev, CB, total;
+  size_t delta, acs, S, Hprev, CB, seg, total;
 };
+
+// two-level state passing scratch: E and In, (B, K, H, P, N) floats each
+size_t seg_bytes(const Dims& d) {
+  return 2 * (size_t)d.B * seg_max_segments(d) * d.H * d.P * d.N * sizeof(float);
+}
 
 FwdOffsets fwd_offsets(const Dims& d) {
   Carver c;
@@ -75,6 +80,7 @@ FwdOffsets fwd_offsets(const Dims& d) {
   o.S = c.take(st);
   o.Hprev = c.take(st);
   o.CB = c.take((size_t)d.B * d.nc * d.G * d.L * d.L * sizeof(float));
+  o.seg = c.take(seg_bytes(d));
   o.total = c.off;
   return o;
 }
@@ -108,7 +114,7 @@ BwdOffsets bwd_offsets(const Dims& d) {
 
 struct TcBwdOffsets {
   size_t delta, acs, S, Himg, dHs, dSimg, dlast, rowsum, colsum, ycs, qrow, ddir, ddiag, dBp,
-      dCp, part, total;
+      dCp, part, seg, total;
 };
 
 TcBwdOffsets tc_bwd_offsets(const Dims& d) {
@@ -133,6 +139,7 @@ TcBwdOffsets tc_bwd_offsets(const Dims& d) {
   o.dBp = c.take(bp);
   o.dCp = c.take(bp);
   o.part = c.take((size_t)d.B * d.H * d.nc * 3 * sizeof(float));
+  o.seg = c.take(seg_bytes(d));
   o.total = c.off;
   return o;
 }
@@ -156,6 +163,8 @@ int check_fwd_ptrs(const Dims& d, const FwdArgs& a) {
   return SSD_OK;
 }
 
+size_t seg_bytes_of(const FwdOffsets& o) { return o.total - o.seg; }
+
 FwdWs carve_fwd(char* base, const FwdOffsets& o) {
   FwdWs w;
   w.delta = reinterpret_cast<float*>(base + o.delta);
@@ -164,6 +173,7 @@ FwdWs carve_fwd(char* base, const FwdOffsets& o) {
   w.Hprev = reinterpret_cast<float*>(base + o.Hprev);
   w.CB = reinterpret_cast<float*>(base + o.CB);
   w.Himg = nullptr;
+  w.seg = seg_bytes_of(o) ? reinterpret_cast<float*>(base + o.seg) : nullptr;
   return w;
 }
 
@@ -289,6 +299,7 @@ int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
     w.dBp = reinterpret_cast<float*>(base + o.dBp);
     w.dCp = reinterpret_cast<float*>(base + o.dCp);
     w.part = reinterpret_cast<float*>(base + o.part);
+    w.seg = o.total > o.seg ? reinterpret_cast<float*>(base + o.seg) : nullptr;
     t_last_path = 1;
     return tc_backward(d, a, w, s) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
   }

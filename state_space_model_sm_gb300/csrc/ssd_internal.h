@@ -80,7 +80,14 @@ struct FwdWs {
   float* Hprev;  // (B, nc, H, P, N)
   float* CB;     // (B, nc, G, L, L)
   void* Himg = nullptr;  // optional (B, nc, H) bf16 hi/lo images of Hprev (tensor-core path)
+  float* seg = nullptr;  // optional two-level state passing scratch (see seg_max_segments)
 };
+
+// Two-level state passing (image path) for shapes with few (batch, head)
+// pairs: the chunks are cut into K segments processed in parallel.  The
+// workspace holds 2 * B * seg_max_segments(d) * H * P * N floats for it;
+// 0 segments means the single-level walk only.
+int seg_max_segments(const Dims& d);
 
 struct BwdWs {
   FwdWs f;
@@ -122,7 +129,7 @@ void cp_dinit_chain(const Dims& d, const float* dHs, const float* acs, const flo
 
 int simt_state_passing_bwd(const Dims& d, const float* dHs, const float* acs, const float* Hprev,
                            const float* dfinal, float* dS, float* dlast, float* dinit,
-                           void* dSimg, const void* Himg,
+                           void* dSimg, const void* Himg, float* seg,
                            cudaStream_t s);  // returns the dlast partials per chunk
 void simt_param_grads(const Dims& d, const float* part, float* dA, float* ddt_bias, float* dD,
                       cudaStream_t s);
@@ -145,6 +152,7 @@ struct TcBwdWs {
   float* dBp;     // (B, T, G, nblk, N) head-block partials of dB
   float* dCp;     // (B, T, G, nblk, N)
   float* part;    // (B, H, nc, 3)
+  float* seg;     // two-level state passing scratch, or nullptr
 };
 
 // tcgen05 path (ssd_tc.cu): bf16 inputs, headdim 64, d_state 64 / 128,

@@ -341,54 +341,138 @@ __device__ __forceinline__ float4 fma4(float d, const float4& c, const float4& s
 
 // Three blocks per SM (registers capped) put the whole grid of the
 // workloads here in one wave; four chunks in flight per thread.
+// grid (P*N/2048, H, B*K): segment k = z % K of batch b = z / K walks chunks
+// [k*lseg, min(nc, (k+1)*lseg)) from its entering state (init for K == 1,
+// else seg_in (B, K, H, P, N)); only the last segment writes final_state.
+// kSeg = false is the single-level walk (K = 1), compiled on its own.
 constexpr int kPrefetchImg = 4;
+template <bool kSeg>
 __global__ void __launch_bounds__(kThreads, 3)
     k_state_passing_img(const float4* __restrict__ S, const float* __restrict__ acs,
                         const float4* __restrict__ init, unsigned char* __restrict__ img,
-                        float4* __restrict__ final_state, int N, int H, int PN8, int L, int nc) {
-  const int e = blockIdx.x * kThreads + threadIdx.x, h = blockIdx.y, b = blockIdx.z;
+                        float4* __restrict__ final_state, int N, int H, int PN8, int L, int nc,
+                        int K, int lseg, const float4* __restrict__ seg_in) {
+  const int e = blockIdx.x * kThreads + threadIdx.x, h = blockIdx.y;
+  const int b = kSeg ? blockIdx.z / K : blockIdx.z, sk = kSeg ? blockIdx.z % K : 0;
   if (e >= PN8) return;
+  const int cb = kSeg ? sk * lseg : 0, ce = kSeg ? min(nc, cb + lseg) : nc;
   const int64_t step = (int64_t)H * PN8 * 2;             // float4 units between chunks
   const int64_t base = ((int64_t)b * nc * H + h) * PN8 * 2;  // (b, c=0, h) state, float4 units
   const uint32_t off = image_chunk_off(e, N), lo_off = (N / 64) * 8192u;
   const float* ab = acs + ((int64_t)b * H + h) * (int64_t)nc * L + (L - 1);
   const int64_t sb = ((int64_t)b * H + h) * PN8 * 2 + 2 * e;
-  float4 c0 = init ? init[sb] : make_float4(0.f, 0.f, 0.f, 0.f);
-  float4 c1 = init ? init[sb + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k0 = 0; k0 < nc; k0 += kPrefetchImg) {
+  const float4* in = nullptr;  // the state entering the segment (null: zero)
+  if constexpr (!kSeg) {
+    if (init) in = init + sb;
+  } else {
+    in = seg_in + (((int64_t)b * K + sk) * H + h) * PN8 * 2 + 2 * e;
+  }
+  float4 c0 = in ? in[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 c1 = in ? in[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = cb; k0 < ce; k0 += kPrefetchImg) {
     float4 s0[kPrefetchImg], s1[kPrefetchImg];
     float dec[kPrefetchImg];
 #pragma unroll
     for (int k = 0; k < kPrefetchImg; ++k)
-      if (k0 + k < nc) {
+      if (k0 + k < ce) {
         s0[k] = S[base + (k0 + k) * step + 2 * e];
         s1[k] = S[base + (k0 + k) * step + 2 * e + 1];
         dec[k] = __expf(ab[(int64_t)(k0 + k) * L]);
       }
 #pragma unroll
     for (int k = 0; k < kPrefetchImg; ++k)
-      if (k0 + k < nc) {
+      if (k0 + k < ce) {
         unsigned char* dst = img + (base + (k0 + k) * step) * 16;
         split8_store(dst + off, dst + off + lo_off, c0, c1);
         c0 = fma4(dec[k], c0, s0[k]);
         c1 = fma4(dec[k], c1, s1[k]);
       }
   }
-  if (final_state) {
+  if (final_state && (!kSeg || sk == K - 1)) {
     final_state[sb] = c0;
     final_state[sb + 1] = c1;
   }
 }
 
+// Two-level pass 1: grid (P*N/2048, H, B*K); segment k's end state from a
+// zero start, E[b, k] = sum over its chunks c of (product of the later
+// chunks' decays in the segment) S_c.  The last segment's is not needed.
+__global__ void __launch_bounds__(kThreads, 3)
+    k_state_passing_seg_end(const float4* __restrict__ S, const float* __restrict__ acs,
+                            float4* __restrict__ E, int H, int PN8, int L, int nc, int K,
+                            int lseg) {
+  const int e = blockIdx.x * kThreads + threadIdx.x, h = blockIdx.y;
+  const int b = blockIdx.z / K, sk = blockIdx.z % K;
+  if (e >= PN8 || sk == K - 1) return;
+  const int cb = sk * lseg, ce = min(nc, cb + lseg);
+  const int64_t step = (int64_t)H * PN8 * 2;
+  const int64_t base = ((int64_t)b * nc * H + h) * PN8 * 2;
+  const float* ab = acs + ((int64_t)b * H + h) * (int64_t)nc * L + (L - 1);
+  float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f), c1 = c0;
+  for (int k0 = cb; k0 < ce; k0 += kPrefetchImg) {
+    float4 s0[kPrefetchImg], s1[kPrefetchImg];
+    float dec[kPrefetchImg];
+#pragma unroll
+    for (int k = 0; k < kPrefetchImg; ++k)
+      if (k0 + k < ce) {
+        s0[k] = S[base + (k0 + k) * step + 2 * e];
+        s1[k] = S[base + (k0 + k) * step + 2 * e + 1];
+        dec[k] = __expf(ab[(int64_t)(k0 + k) * L]);
+      }
+#pragma unroll
+    for (int k = 0; k < kPrefetchImg; ++k)
+      if (k0 + k < ce) {
+        c0 = fma4(dec[k], c0, s0[k]);
+        c1 = fma4(dec[k], c1, s1[k]);
+      }
+  }
+  const int64_t eo = (((int64_t)b * K + sk) * H + h) * PN8 * 2 + 2 * e;
+  E[eo] = c0;
+  E[eo + 1] = c1;
+}
+
+// Two-level pass 2: grid (P*N/2048, H, B); the state entering each segment,
+// In[b, 0] = init (or 0), In[b, k+1] = D_k In[b, k] + E[b, k] with D_k the
+// product of segment k's chunk decays.
+__global__ void __launch_bounds__(kThreads)
+    k_state_passing_seg_in(const float4* __restrict__ E, const float* __restrict__ acs,
+                           const float4* __restrict__ init, float4* __restrict__ In, int H,
+                           int PN8, int L, int nc, int K, int lseg) {
+  const int e = blockIdx.x * kThreads + threadIdx.x, h = blockIdx.y, b = blockIdx.z;
+  if (e >= PN8) return;
+  const float* ab = acs + ((int64_t)b * H + h) * (int64_t)nc * L + (L - 1);
+  const int64_t sb = ((int64_t)b * H + h) * PN8 * 2 + 2 * e;
+  float4 c0 = init ? init[sb] : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 c1 = init ? init[sb + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int sk = 0; sk < K; ++sk) {
+    const int64_t o = (((int64_t)b * K + sk) * H + h) * PN8 * 2 + 2 * e;
+    In[o] = c0;
+    In[o + 1] = c1;
+    if (sk == K - 1) break;
+    float D = 1.f;
+    const int cb = sk * lseg, ce = min(nc, cb + lseg);
+    for (int c = cb; c < ce; ++c) D *= __expf(ab[(int64_t)c * L]);
+    c0 = fma4(D, c0, E[o]);
+    c1 = fma4(D, c1, E[o + 1]);
+  }
+}
+
 // Image-mode state passing backward: grid (nsplit = P*N/2048, H, B); reads the
 // H_c images, writes the dS_c images; dlast partials as in the float4 kernel.
+template <bool kSeg>
 __global__ void __launch_bounds__(kThreads, 3)
     k_state_passing_bwd_img(const float4* __restrict__ dHs, const float* __restrict__ acs,
                             const unsigned char* __restrict__ himg,
                             const float4* __restrict__ dfinal, unsigned char* __restrict__ dsimg,
                             float* __restrict__ dlast_part, float4* __restrict__ dinit, int N,
-                            int H, int PN8, int L, int nc) {
-  const int split = blockIdx.x, nsplit = gridDim.x, h = blockIdx.y, b = blockIdx.z;
+                            int H, int PN8, int L, int nc, int K, int lseg,
+                            const float4* __restrict__ seg_out) {
+  // grid (nsplit, H, B*K): segment sk = z % K walks chunks [sk*lseg, min(nc,
+  // (sk+1)*lseg)) backwards from the gradient leaving it (dfinal for K == 1,
+  // else seg_out (B, K, H, P, N)); only segment 0 writes dinit
+  const int split = blockIdx.x, nsplit = gridDim.x, h = blockIdx.y;
+  const int b = kSeg ? blockIdx.z / K : blockIdx.z, sk = kSeg ? blockIdx.z % K : 0;
+  const int cb = kSeg ? sk * lseg : 0, ce = kSeg ? min(nc, cb + lseg) : nc;
   const int e = split * kThreads + threadIdx.x;
   const bool live = e < PN8;
   const int64_t step = (int64_t)H * PN8 * 2;
@@ -396,16 +480,22 @@ __global__ void __launch_bounds__(kThreads, 3)
   const uint32_t off = live ? image_chunk_off(e, N) : 0u, lo_off = (N / 64) * 8192u;
   const float* ab = acs + ((int64_t)b * H + h) * (int64_t)nc * L + (L - 1);
   const int64_t sb = ((int64_t)b * H + h) * PN8 * 2 + 2 * e;
-  float4 g0 = (live && dfinal) ? dfinal[sb] : make_float4(0.f, 0.f, 0.f, 0.f);
-  float4 g1 = (live && dfinal) ? dfinal[sb + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4* gin = nullptr;  // the gradient leaving the segment (null: zero)
+  if constexpr (!kSeg) {
+    if (dfinal) gin = dfinal + sb;
+  } else {
+    gin = seg_out + (((int64_t)b * K + sk) * H + h) * PN8 * 2 + 2 * e;
+  }
+  float4 g0 = (live && gin) ? gin[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 g1 = (live && gin) ? gin[1] : make_float4(0.f, 0.f, 0.f, 0.f);
   constexpr int kPf = 3;
-  for (int c1 = nc - 1; c1 >= 0; c1 -= kPf) {
+  for (int c1 = ce - 1; c1 >= cb; c1 -= kPf) {
     float4 h0[kPf], h1[kPf], d0[kPf], d1[kPf];
     float dec[kPf];
 #pragma unroll
     for (int k = 0; k < kPf; ++k) {
       const int c = c1 - k;
-      if (c >= 0) {
+      if (c >= cb) {
         dec[k] = __expf(ab[(int64_t)c * L]);
         if (live) {
           const unsigned char* src = himg + (base + c * step) * 16;
@@ -418,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
     for (int k = 0; k < kPf; ++k) {
       const int c = c1 - k;
-      if (c < 0) break;
+      if (c < cb) break;
       float part = 0.f;
       if (live) {
         unsigned char* dst = dsimg + (base + c * step) * 16;
@@ -436,9 +526,73 @@ __global__ void __launch_bounds__(kThreads, 3)
                    (threadIdx.x >> 5)] = dec[k] * part;
     }
   }
-  if (live && dinit) {
+  if (live && dinit && (!kSeg || sk == 0)) {
     dinit[sb] = g0;
     dinit[sb + 1] = g1;
+  }
+}
+
+// Two-level backward pass 1: grid (P*N/2048, H, B*K); segment k's own part of
+// the gradient entering its first chunk, from a zero gradient leaving it:
+// G <- dHs_c + dec_c G for c = last .. first chunk of the segment.  Segment
+// 0's is not needed.
+__global__ void __launch_bounds__(kThreads, 3)
+    k_state_passing_bwd_seg_end(const float4* __restrict__ dHs, const float* __restrict__ acs,
+                                float4* __restrict__ E, int H, int PN8, int L, int nc, int K,
+                                int lseg) {
+  const int e = blockIdx.x * kThreads + threadIdx.x, h = blockIdx.y;
+  const int b = blockIdx.z / K, sk = blockIdx.z % K;
+  if (e >= PN8 || sk == 0) return;
+  const int cb = sk * lseg, ce = min(nc, cb + lseg);
+  const int64_t step = (int64_t)H * PN8 * 2;
+  const int64_t base = ((int64_t)b * nc * H + h) * PN8 * 2;
+  const float* ab = acs + ((int64_t)b * H + h) * (int64_t)nc * L + (L - 1);
+  float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0;
+  for (int c1 = ce - 1; c1 >= cb; c1 -= kPrefetchImg) {
+    float4 d0[kPrefetchImg], d1[kPrefetchImg];
+    float dec[kPrefetchImg];
+#pragma unroll
+    for (int k = 0; k < kPrefetchImg; ++k)
+      if (c1 - k >= cb) {
+        d0[k] = dHs[base + (c1 - k) * step + 2 * e];
+        d1[k] = dHs[base + (c1 - k) * step + 2 * e + 1];
+        dec[k] = __expf(ab[(int64_t)(c1 - k) * L]);
+      }
+#pragma unroll
+    for (int k = 0; k < kPrefetchImg; ++k)
+      if (c1 - k >= cb) {
+        g0 = fma4(dec[k], g0, d0[k]);
+        g1 = fma4(dec[k], g1, d1[k]);
+      }
+  }
+  const int64_t eo = (((int64_t)b * K + sk) * H + h) * PN8 * 2 + 2 * e;
+  E[eo] = g0;
+  E[eo + 1] = g1;
+}
+
+// Two-level backward pass 2: grid (P*N/2048, H, B); the gradient leaving
+// each segment, Out[b, K-1] = dfinal (or 0), Out[b, k-1] = D_k Out[b, k] +
+// E[b, k] with D_k the product of segment k's chunk decays.
+__global__ void __launch_bounds__(kThreads)
+    k_state_passing_bwd_seg_in(const float4* __restrict__ E, const float* __restrict__ acs,
+                               const float4* __restrict__ dfinal, float4* __restrict__ Out,
+                               int H, int PN8, int L, int nc, int K, int lseg) {
+  const int e = blockIdx.x * kThreads + threadIdx.x, h = blockIdx.y, b = blockIdx.z;
+  if (e >= PN8) return;
+  const float* ab = acs + ((int64_t)b * H + h) * (int64_t)nc * L + (L - 1);
+  const int64_t sb = ((int64_t)b * H + h) * PN8 * 2 + 2 * e;
+  float4 g0 = dfinal ? dfinal[sb] : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 g1 = dfinal ? dfinal[sb + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int sk = K - 1; sk >= 0; --sk) {
+    const int64_t o = (((int64_t)b * K + sk) * H + h) * PN8 * 2 + 2 * e;
+    Out[o] = g0;
+    Out[o + 1] = g1;
+    if (sk == 0) break;
+    float D = 1.f;
+    const int cb = sk * lseg, ce = min(nc, cb + lseg);
+    for (int c = cb; c < ce; ++c) D *= __expf(ab[(int64_t)c * L]);
+    g0 = fma4(D, g0, E[o]);
+    g1 = fma4(D, g1, E[o + 1]);
   }
 }
 
@@ -951,14 +1105,45 @@ void launch_cumsum(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t
 
 bool vec4_ok(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// Segments of the two-level state passing: two levels only when the
+// (batch, head) grid alone (gx blocks per pair) would leave at least half the
+// SMs idle; then K segments of lseg chunks, about three blocks per SM in all.
+void seg_plan(const Dims& d, int gx, bool have_scratch, int* K, int* lseg) {
+  *K = 1;
+  *lseg = d.nc;
+  const int kmax = have_scratch ? seg_max_segments(d) : 0;
+  if (kmax < 2) return;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t base = (int64_t)gx * d.H * d.B;
+  if (2 * base > sms) return;
+  int k = (int)std::min<int64_t>(kmax, (3 * sms + base - 1) / base);
+  *lseg = (d.nc + k - 1) / k;
+  *K = (d.nc + *lseg - 1) / *lseg;
+}
+
 void launch_state_passing(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
   const int PN = d.P * d.N;
   if (w.Himg) {  // tensor-core path: states as split-bf16 images only
-    const int PN8 = PN / 8;
-    SSD_LAUNCH("k_state_passing", s, k_state_passing_img<<<dim3((PN8 + kThreads - 1) / kThreads, d.H, d.B), kThreads, 0, s>>>(
+    const int PN8 = PN / 8, gx = (PN8 + kThreads - 1) / kThreads;
+    int K, lseg;
+    seg_plan(d, gx, w.seg != nullptr, &K, &lseg);
+    const float4* in = nullptr;
+    if (K > 1) {
+      float4* E = reinterpret_cast<float4*>(w.seg);
+      float4* In = E + (size_t)d.B * K * d.H * PN8 * 2;
+      SSD_LAUNCH("k_state_passing_seg", s, k_state_passing_seg_end<<<dim3(gx, d.H, d.B * K), kThreads, 0, s>>>(
+          reinterpret_cast<const float4*>(w.S), w.acs, E, d.H, PN8, d.L, d.nc, K, lseg));
+      SSD_LAUNCH("k_state_passing_seg", s, k_state_passing_seg_in<<<dim3(gx, d.H, d.B), kThreads, 0, s>>>(
+          E, w.acs, reinterpret_cast<const float4*>(a.init), In, d.H, PN8, d.L, d.nc, K, lseg));
+      in = In;
+    }
+    auto kern = K > 1 ? k_state_passing_img<true> : k_state_passing_img<false>;
+    SSD_LAUNCH("k_state_passing", s, kern<<<dim3(gx, d.H, d.B * K), kThreads, 0, s>>>(
         reinterpret_cast<const float4*>(w.S), w.acs, reinterpret_cast<const float4*>(a.init),
         static_cast<unsigned char*>(w.Himg), reinterpret_cast<float4*>(a.final_state), d.N, d.H,
-        PN8, d.L, d.nc));
+        PN8, d.L, d.nc, K, lseg, in));
     return;
   }
   if (PN % 4 == 0 && vec4_ok(a.init) && vec4_ok(a.final_state)) {
@@ -997,11 +1182,25 @@ int launch_state_passing_bwd(const Dims& d, const BwdArgs& a, const BwdWs& w, cu
   const int PN = d.P * d.N;
   if (w.f.Himg && w.dSimg) {  // tensor-core path
     const int PN8 = PN / 8, nsplit = (PN8 + kThreads - 1) / kThreads;
-    SSD_LAUNCH("k_state_passing_bwd", s, k_state_passing_bwd_img<<<dim3(nsplit, d.H, d.B), kThreads, 0, s>>>(
+    int K, lseg;
+    seg_plan(d, nsplit, w.f.seg != nullptr, &K, &lseg);
+    const float4* out = nullptr;
+    if (K > 1) {
+      float4* E = reinterpret_cast<float4*>(w.f.seg);
+      float4* Out = E + (size_t)d.B * K * d.H * PN8 * 2;
+      SSD_LAUNCH("k_state_passing_bwd_seg", s, k_state_passing_bwd_seg_end<<<dim3(nsplit, d.H, d.B * K), kThreads, 0, s>>>(
+          reinterpret_cast<const float4*>(w.dHs), w.f.acs, E, d.H, PN8, d.L, d.nc, K, lseg));
+      SSD_LAUNCH("k_state_passing_bwd_seg", s, k_state_passing_bwd_seg_in<<<dim3(nsplit, d.H, d.B), kThreads, 0, s>>>(
+          E, w.f.acs, reinterpret_cast<const float4*>(a.dfinal), Out, d.H, PN8, d.L, d.nc, K,
+          lseg));
+      out = Out;
+    }
+    auto kern = K > 1 ? k_state_passing_bwd_img<true> : k_state_passing_bwd_img<false>;
+    SSD_LAUNCH("k_state_passing_bwd", s, kern<<<dim3(nsplit, d.H, d.B * K), kThreads, 0, s>>>(
         reinterpret_cast<const float4*>(w.dHs), w.f.acs,
         static_cast<const unsigned char*>(w.f.Himg), reinterpret_cast<const float4*>(a.dfinal),
         static_cast<unsigned char*>(w.dSimg), w.dlast, reinterpret_cast<float4*>(a.dinit), d.N,
-        d.H, PN8, d.L, d.nc));
+        d.H, PN8, d.L, d.nc, K, lseg, out));
     return nsplit * (kThreads / 32);  // one partial per warp
   }
   if (PN % 4 == 0 && vec4_ok(a.dfinal) && vec4_ok(a.dinit)) {
@@ -1064,6 +1263,15 @@ cudaError_t simt_forward(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaSt
   return cudaGetLastError();
 }
 
+int seg_max_segments(const Dims& d) {
+  // a property of the shape, so workspace sizes do not depend on the device:
+  // scratch only where the (batch, head) grid is small and there are chunks
+  // to split (at most 16 segments of at least 4 chunks)
+  const int64_t ctas = (int64_t)((d.P * d.N / 8 + kThreads - 1) / kThreads) * d.H * d.B;
+  if (d.nc < 8 || ctas >= 256) return 0;
+  return std::min(16, d.nc / 4);
+}
+
 void simt_cumsum(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
   if (d.in_bf16) launch_cumsum<__nv_bfloat16>(d, a, w, s);
   else launch_cumsum<float>(d, a, w, s);
@@ -1108,7 +1316,7 @@ void simt_dstates(const Dims& d, const void* dy, const void* C, const float* del
 
 int simt_state_passing_bwd(const Dims& d, const float* dHs, const float* acs, const float* Hprev,
                            const float* dfinal, float* dS, float* dlast, float* dinit,
-                           void* dSimg, const void* Himg, cudaStream_t s) {
+                           void* dSimg, const void* Himg, float* seg, cudaStream_t s) {
   BwdArgs a{};
   a.dfinal = dfinal;
   a.dinit = dinit;
@@ -1120,6 +1328,7 @@ int simt_state_passing_bwd(const Dims& d, const float* dHs, const float* acs, co
   w.f.Hprev = const_cast<float*>(Hprev);
   w.dS = dS;
   w.dlast = dlast;
+  w.f.seg = seg;
   return launch_state_passing_bwd(d, a, w, s);
 }
 

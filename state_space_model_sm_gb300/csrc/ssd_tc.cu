@@ -1369,12 +1369,12 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
   const bf16* dy = static_cast<const bf16*>(a.dy);
   FwdArgs f = a.f;
   f.final_state = nullptr;
-  FwdWs fw{w.delta, w.acs, w.S, nullptr, nullptr, w.Himg};
+  FwdWs fw{w.delta, w.acs, w.S, nullptr, nullptr, w.Himg, w.seg};
   launch_state_front<N, L>(d, f, fw, s, status, sms);  // with chunk_cumsum
   simt_state_passing(d, f, fw, s);
   launch_dstates<N, L>(d, dy, Cm, w.delta, w.acs, w.dHs, s, status, sms);
   const int nsplit = simt_state_passing_bwd(d, w.dHs, w.acs, nullptr, a.dfinal, nullptr, w.dlast,
-                                            a.dinit, w.dSimg, w.Himg, s);
+                                            a.dinit, w.dSimg, w.Himg, w.seg, s);
   {
     using SM = ScanSmem<N, L>;
     auto kern = k_scan_tc<N, L, float, true>;

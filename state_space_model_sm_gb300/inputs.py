@@ -117,6 +117,9 @@ WORKLOADS = {
     "hybrid_bf16": (SSDShape(2, 8192, 64, 64, 128, 8, 128), "bf16", 0.1, 2, False),
     "long_bf16": (SSDShape(1, 131072, 32, 64, 128, 1, 256), "bf16", 0.0, 3, False),
     "layer_fwdbwd_bf16": (SSDShape(4, 4096, 24, 64, 128, 1, 256), "bf16", 0.0, 4, True),
+    # long context with few heads (8 heads of 64: the chunk loop of state
+    # passing has few (batch, head) pairs to run in parallel)
+    "long_h8_bf16": (SSDShape(1, 131072, 8, 64, 128, 1, 256), "bf16", 0.0, 5, True),
 }
 
 

@@ -257,3 +257,37 @@ def test_tensor_core_backward_against_oracle_and_generic(cuda_lib, monkeypatch, 
     for k in keys:
         s = stats(g[k], g2[k])
         assert s["rel_l2"] < 1e-4, (k, s)
+
+
+# ------------------------------------- two-level state passing (few heads)
+
+SEG_CASES = [
+    # (batch x heads) small and enough chunks: the chunks are split into
+    # segments (8 of 4, 6 of 5 with a ragged last one, 2 with N = 64)
+    ("seg_8x4", SSDShape(1, 4000, 2, 64, 128, 1, 128), 0.3),
+    ("seg_ragged", SSDShape(1, 3800, 2, 64, 128, 1, 128), 0.3),
+    ("seg_n64", SSDShape(1, 1100, 2, 64, 64, 1, 128), 0.3),
+]
+
+
+@pytest.mark.parametrize("name,shape,init_std", SEG_CASES, ids=[c[0] for c in SEG_CASES])
+def test_two_level_state_passing(cuda_lib, name, shape, init_std):
+    """Forward (y, final) and backward (whose recompute runs the same state
+    passing) at shapes whose (batch, head) grid is small, with an initial
+    state and a final-state gradient; the segment kernels must have run."""
+    inp = make_inputs(shape, seed=41, dtype="bf16", init_std=init_std, with_dy=True,
+                      dfinal_std=0.5)
+    cuda_lib.profile_enable(True)
+    y, final = run_fwd(cuda_lib, inp)
+    g = run_bwd(cuda_lib, inp)
+    prof = cuda_lib.profile_read()
+    cuda_lib.profile_enable(False)
+    assert prof.get("k_state_passing_seg", (0, 0))[1] == 4, prof  # 2 kernels, fwd + recompute
+    assert prof.get("k_state_passing_bwd_seg", (0, 0))[1] == 2, prof
+    y_ref, f_ref = oracle_fwd(inp)
+    assert_close("y", to_np(y), y_ref, "bf16")
+    assert_close("final", to_np(final), f_ref, "bf16")
+    ref = oracle_bwd(inp)
+    for k in ["dx", "ddt", "dA", "dB", "dC", "dD", "ddt_bias", "dinit"]:
+        assert_close(k, g["dinit_states"] if k == "dinit" else g[k], ref[k], "bf16")
+    assert cuda_lib.device_status() == 0
