@@ -1118,7 +1118,8 @@ void seg_plan(const Dims& d, int gx, bool have_scratch, int* K, int* lseg) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t base = (int64_t)gx * d.H * d.B;
   if (2 * base > sms) return;
-  int k = (int)std::min<int64_t>(kmax, (3 * sms + base - 1) / base);
+  // at most three blocks per SM in all, so the segments run in one wave
+  int k = (int)std::min<int64_t>(kmax, std::max<int64_t>(2, (3 * sms) / base));
   *lseg = (d.nc + k - 1) / k;
   *K = (d.nc + *lseg - 1) / *lseg;
 }
