@@ -169,8 +169,8 @@ size_t ssd_noalloc_scratch_bytes(void);
  * ssd_segment_decay_workspace_size(shape) bytes (8-byte aligned,
  * caller-owned; the size depends on the current device's SM count).
  * Asynchronous on `stream`.  Returns SSD_ERR_INVALID_ARG for a NULL
- * required pointer or a bad shape, SSD_ERR_WORKSPACE for a missing or small
- * workspace. */
+ * required pointer or a bad shape (seqlen must be below 2^30),
+ * SSD_ERR_WORKSPACE for a missing or small workspace. */
 size_t ssd_segment_decay_workspace_size(const ssd_shape* shape);
 int ssd_segment_decay(const ssd_shape* shape, const void* dt, const float* dt_bias,
                       const float* A, float* decay, void* workspace, size_t workspace_bytes,

@@ -152,8 +152,9 @@ namespace {
 bool decay_shape_ok(const ssd_shape* shape) {
   if (!shape || shape->batch < 1 || shape->seqlen < 1 || shape->nheads < 1) return false;
   if (shape->in_dtype != SSD_F32 && shape->in_dtype != SSD_BF16) return false;
+  // positions are int in the kernels, with t + span computed: keep seqlen < 2^30
   return shape->batch < 65536 && shape->nheads < ((int64_t)1 << 20) &&
-         shape->seqlen < ((int64_t)1 << 31);
+         shape->seqlen < ((int64_t)1 << 30);
 }
 int current_sms() {
   int dev = 0, sms = 148;

@@ -145,6 +145,9 @@ def sweep_gated_norm(features: int, group_size: int, dtype: str = "bf16", rows: 
 
     from . import gated_norm_bwd, gated_norm_fwd, gated_norm_workspace_bytes
     lib = _native.load()
+    configs = list(configs if configs is not None else candidates(features))
+    if not configs:
+        raise ValueError(f"no launch configuration for {features} features (at most 4096)")
     dev = torch.device("cuda", torch.cuda.current_device())
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     g = torch.Generator(device="cpu").manual_seed(seed)
@@ -177,7 +180,7 @@ def sweep_gated_norm(features: int, group_size: int, dtype: str = "bf16", rows: 
     default_cfg, _ = get_norm_config(features, group_size, dtype, lib=lib)
     timings = []
     try:
-        for cfg in (configs if configs is not None else candidates(features)):
+        for cfg in configs:
             set_norm_config(features, group_size, dtype, dtype, lib=lib, **cfg)
             timings.append((time_us(), cfg))
     finally:
