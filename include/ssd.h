@@ -266,7 +266,9 @@ int ssd_gated_norm_bwd(const ssd_norm_shape* shape, const void* y, const void* z
  * search per environment ahead of time, store the result, load it at start):
  * rows_per_item = rows per CTA work
  * item (the CTA has rows_per_item * features / 8 threads, at most 512 and a
- * multiple of 32); ring_kb = shared-memory ring size aimed at per CTA
+ * multiple of 32; it applies to the backward, and to the forward where that
+ * keeps one 8-feature vector per thread: a forward with two vectors per
+ * thread takes as many rows as fill 512 threads); ring_kb = shared-memory ring size aimed at per CTA
  * (8 .. 200); ctas_per_sm = persistent CTAs per SM at most (1 .. 8).  A zero
  * field keeps the built-in choice. */
 typedef struct {

@@ -79,8 +79,9 @@ __device__ __forceinline__ float2 sigmoid2(float2 z) {
 
 struct NormDims {
   int M, D, gs;
-  int TPR;     // threads per row = D / 8
-  int TPG;     // threads per group = gs / 8
+  int VPT;     // 8-feature vectors per thread (1, or 2 in the forward where it fits)
+  int TPR;     // threads per row = D / (8 VPT)
+  int TPG;     // threads per group = gs / (8 VPT)
   int RPC;     // rows per item (one ring stage); NT = RPC * TPR threads
   int n_iter;  // items: ceil(M / RPC)
   int NS;      // ring stages
@@ -107,7 +108,7 @@ __device__ __forceinline__ ThreadMap thread_map(const NormDims& d) {
   const int tid = threadIdx.x;
   m.slot = tid / d.TPR;
   const int v = tid - m.slot * d.TPR;
-  m.f0 = v * kV;
+  m.f0 = v * kV * d.VPT;
   m.off = m.slot * d.D + m.f0;
   m.grp = v / d.TPG;
   m.lead = v == m.grp * d.TPG;
@@ -221,7 +222,7 @@ __device__ __forceinline__ bool ring_acquire(const NormDims& d, const RowRing<NT
   return true;
 }
 
-template <typename Tin, typename Tout, bool kBig>
+template <typename Tin, typename Tout, bool kBig, int VPT>
 __global__ void __launch_bounds__(kMaxNT, 2)
     k_gated_norm_fwd(const Tin* __restrict__ y, const Tin* __restrict__ z,
                      const float* __restrict__ w, Tout* __restrict__ out,
@@ -239,8 +240,9 @@ __global__ void __launch_bounds__(kMaxNT, 2)
   const int ngr = d.D / d.gs;
   const int tile_e = d.RPC * d.D;  // elements of one tensor's block
   const Tin* sy = reinterpret_cast<const Tin*>(smem) + m.off;
-  float2 wv[4];
-  lds8(sw + m.f0, wv);
+  float2 wv[4 * VPT];
+#pragma unroll
+  for (int q = 0; q < VPT; ++q) lds8(sw + m.f0 + 8 * q, *reinterpret_cast<float2(*)[4]>(wv + 4 * q));
   int row = blockIdx.x * d.RPC + m.slot;
   const int row_step = gridDim.x * d.RPC;
   int s = 0, sprev = 0;
@@ -249,23 +251,30 @@ __global__ void __launch_bounds__(kMaxNT, 2)
   for (; k < mine; ++k) {
     if (!ring_acquire(d, ring, k, s, phase, sprev, mine, issued, status, &abort_flag)) break;
     const bool live = row < d.M;
-    float2 yv[4], zv[4], u[4];
-    const Tin* st = sy + s * 2 * tile_e;
-    lds8(st, yv);
-    lds8(st + tile_e, zv);
+    float2 u[4 * VPT];
     float2 ss2 = f2(0.f);
+    const Tin* st = sy + s * 2 * tile_e;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      u[i] = __fmul2_rn(yv[i], __fmul2_rn(zv[i], sigmoid2(zv[i])));
-      ss2 = __ffma2_rn(u[i], u[i], ss2);
+    for (int q = 0; q < VPT; ++q) {
+      float2 yv[4], zv[4];
+      lds8(st + 8 * q, yv);
+      lds8(st + tile_e + 8 * q, zv);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        u[4 * q + i] = __fmul2_rn(yv[i], __fmul2_rn(zv[i], sigmoid2(zv[i])));
+        ss2 = __ffma2_rn(u[4 * q + i], u[4 * q + i], ss2);
+      }
     }
     const float ss = group_sum<kBig>(live ? ss2.x + ss2.y : 0.f, m, red, 0);
     const float r = rsqrtf(ss / (float)d.gs + d.eps);
     if (live) {
-      float2 o[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) o[i] = __fmul2_rn(__fmul2_rn(u[i], f2(r)), wv[i]);
-      store8(out + (int64_t)row * d.D + m.f0, o);
+      for (int q = 0; q < VPT; ++q) {
+        float2 o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = __fmul2_rn(__fmul2_rn(u[4 * q + i], f2(r)), wv[4 * q + i]);
+        store8(out + (int64_t)row * d.D + m.f0 + 8 * q, o);
+      }
       if (rstd && m.lead) rstd[(int64_t)row * ngr + m.grp] = r;
     }
     row += row_step;
@@ -462,6 +471,7 @@ bool norm_dims(const ssd_norm_shape* s, NormDims* d) {
   d->M = (int)s->rows;
   d->D = (int)s->features;
   d->gs = (int)s->group_size;
+  d->VPT = 1;
   d->TPR = d->D / kV;
   d->TPG = d->gs / kV;
   d->eps = s->eps;
@@ -519,15 +529,29 @@ int norm_grid(const NormDims& d, const void* kern, int nt, size_t smem) {
   return (int)(d.n_iter < g ? d.n_iter : g);
 }
 
-template <typename Tin, typename Tout>
-int launch_norm_fwd(NormDims d, const void* y, const void* z, const float* w, void* out,
-                    float* rstd, cudaStream_t s) {
-  int* status = device_status_ptr();
-  if (!status) return SSD_ERR_CUDA;
+// The forward's thread map with two vectors per thread, when the row and
+// group widths allow it (the same rules as for one vector); false if not.
+bool fwd_two_vectors(NormDims* d) {
+  if (d->D % 16 || d->gs % 16) return false;
+  NormDims e = *d;
+  e.VPT = 2;
+  e.TPR = d->D / 16;
+  e.TPG = d->gs / 16;
+  if (norm_supported(e) != SSD_OK) return false;
+  e.RPC = e.TPR < kMaxNT ? kMaxNT / e.TPR : 1;
+  if ((e.RPC * e.TPR) % 32) return false;
+  e.n_iter = (e.M + e.RPC - 1) / e.RPC;
+  *d = e;
+  return true;
+}
+
+template <typename Tin, typename Tout, int VPT>
+int launch_norm_fwd_v(NormDims d, const void* y, const void* z, const float* w, void* out,
+                      float* rstd, cudaStream_t s, int* status) {
   const int nt = d.RPC * d.TPR;
   const bool big = d.TPG > 32;
-  auto kb = k_gated_norm_fwd<Tin, Tout, true>;
-  auto ks = k_gated_norm_fwd<Tin, Tout, false>;
+  auto kb = k_gated_norm_fwd<Tin, Tout, true, VPT>;
+  auto ks = k_gated_norm_fwd<Tin, Tout, false, VPT>;
   const void* kern = big ? (const void*)kb : (const void*)ks;
   d.NS = ring_stages(d, 2, sizeof(Tin), reg_ctas(kern, nt), (size_t)d.D * sizeof(float));
   const size_t smem = (size_t)d.NS * 2 * d.RPC * d.D * sizeof(Tin) + (size_t)d.D * sizeof(float);
@@ -542,6 +566,17 @@ int launch_norm_fwd(NormDims d, const void* y, const void* z, const float* w, vo
     SSD_LAUNCH("k_gated_norm_fwd", s,
                ks<<<grid, nt, smem, s>>>(yy, zz, w, oo, rstd, d, status));
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+template <typename Tin, typename Tout>
+int launch_norm_fwd(NormDims d, const void* y, const void* z, const float* w, void* out,
+                    float* rstd, cudaStream_t s) {
+  int* status = device_status_ptr();
+  if (!status) return SSD_ERR_CUDA;
+  // two 8-feature vectors per thread halve the per-row fixed work (the
+  // backward keeps one: its live set would not fit the register budget)
+  if (fwd_two_vectors(&d)) return launch_norm_fwd_v<Tin, Tout, 2>(d, y, z, w, out, rstd, s, status);
+  return launch_norm_fwd_v<Tin, Tout, 1>(d, y, z, w, out, rstd, s, status);
 }
 
 template <typename Tin, typename Tout>
