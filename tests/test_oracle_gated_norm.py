@@ -115,3 +115,37 @@ def test_group_size_must_divide():
     y, z, w, _, _ = _data(D=24)
     with pytest.raises(ValueError):
         gn.gated_rmsnorm_fwd(y, z, w, 5)
+
+
+def test_random_shapes_match_torch_autograd():
+    """Property check over random shapes, group sizes, eps and gate scales:
+    forward and backward equal torch's rms_norm / silu with autograd."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+    import torch
+
+    @hyp.settings(max_examples=40, deadline=None, derandomize=True)
+    @hyp.given(rows=st.integers(1, 9), groups=st.integers(1, 4), gs=st.integers(1, 12),
+               eps=st.sampled_from([0.0, 1e-5, 0.3]), zscale=st.floats(0.1, 8.0),
+               seed=st.integers(0, 2 ** 16))
+    def check(rows, groups, gs, eps, zscale, seed):
+        D = groups * gs
+        rng = np.random.default_rng(seed)
+        y = rng.standard_normal((rows, D))
+        z = rng.standard_normal((rows, D)) * zscale
+        w = 1.0 + 0.3 * rng.standard_normal(D)
+        dout = rng.standard_normal((rows, D))
+        out, rstd = gn.gated_rmsnorm_fwd(y, z, w, gs, eps=eps)
+        g = gn.gated_rmsnorm_bwd(y, z, w, dout, gs, eps=eps)
+        ref, (yt, zt, wt) = _torch_ref(y, z, w, gs, eps)
+        ref.backward(torch.tensor(dout))
+        np.testing.assert_allclose(out, ref.detach().numpy(), rtol=1e-10, atol=1e-12)
+        # the backward subtracts terms of size rstd |dout w| (times |y| or |z|
+        # factors) that cancel exactly in degenerate groups (one element: xhat
+        # = +-1, du = 0); rounding there is relative to that size
+        scale = (float(rstd.max()) * float(np.abs(dout * w).max()) *
+                 max(1.0, float(np.abs(y).max())) * max(1.0, float(np.abs(z).max())))
+        for name, t in (("dy", yt), ("dz", zt), ("dw", wt)):
+            np.testing.assert_allclose(g[name], t.grad.numpy(), rtol=1e-8,
+                                       atol=1e-12 * scale + 1e-12, err_msg=name)
+    check()
