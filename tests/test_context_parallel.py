@@ -378,3 +378,20 @@ def test_library_context_parallel_matches_unsplit_oracle(cuda_lib, dtype, shape_
     ref = dict(y=y, final=final, **{k: g[k] for k in GRADS + SHARED + ("dinit",)})
     for k, r in ref.items():
         assert_close(k, got[k], r, dtype)
+
+
+def test_random_splits_match_unsplit_oracle():
+    """Property check of the orchestration: any split of the sequence into 1..5
+    contiguous non-empty segments gives the unsplit outputs and gradients."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+    inp = _inputs((1, 60, 2, 4, 3, 1, 16), seed=5)
+
+    @hyp.settings(max_examples=15, deadline=None, derandomize=True)
+    @hyp.given(cuts=st.lists(st.integers(1, 59), min_size=0, max_size=4, unique=True))
+    def check(cuts):
+        bounds = [0] + sorted(cuts) + [60]
+        sizes = [b - a for a, b in zip(bounds, bounds[1:])]
+        res = _run_threads(lambda r: OracleEngine(), inp, sizes, F64)
+        _check_fp64(_assemble(res), inp)
+    check()
