@@ -1165,8 +1165,8 @@ __global__ void __launch_bounds__(kBcThreads, 1)
 // (dC kernel) and column sums (dB kernel) of M:
 //   ddA_r = sum_{j<r} (colsum_j - rowsum_j) + sum_{l>=r} ycs_l + sum_{s<r} qrow_s + dlast_c
 //   ddt_r = (ddir_r + A ddA_r) softplus'(dt_r + dt_bias);  partials of dA, ddt_bias, dD.
-__device__ __forceinline__ float block_exclusive_scan256(float v, float* warp_tot) {
-  // exclusive prefix of v over the 256 threads of the block, in thread order
+__device__ __forceinline__ float block_exclusive_scan(float v, float* warp_tot) {
+  // exclusive prefix of v over the threads of the block (whole warps), in thread order
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float incl = v;
 #pragma unroll
@@ -1190,8 +1190,10 @@ struct FinalizeArgs {
   int T, H, L, nc;
 };
 
-// One (chunk c, head h, batch b) of the finalize step; 256 threads (= L rows).
+// One (chunk c, head h, batch b) of the finalize step; NT threads = L rows.
+template <int NT>
 __device__ __forceinline__ void finalize_block(const FinalizeArgs& f, int c, int h, int b) {
+  constexpr int NW = NT / 32;
   const bf16* __restrict__ dt = f.dt;
   const float* __restrict__ dt_bias = f.dt_bias;
   const float* __restrict__ A = f.A;
@@ -1206,7 +1208,7 @@ __device__ __forceinline__ void finalize_block(const FinalizeArgs& f, int c, int
   float* __restrict__ ddt = f.ddt;
   float* __restrict__ part = f.part;
   const int nsplit = f.nsplit, T = f.T, H = f.H, L = f.L, nc = f.nc;
-  __shared__ float wt[8], red[8];
+  __shared__ float wt[NW], red[NW];
   const int r = threadIdx.x;
   const int Lv = min(L, T - c * L);
   const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
@@ -1220,12 +1222,12 @@ __device__ __forceinline__ void finalize_block(const FinalizeArgs& f, int c, int
   float dl = 0.f;
   for (int k = 0; k < nsplit; ++k) dl += dlast[(((int64_t)b * H + h) * nc + c) * nsplit + k];
   // ddA_r = prefix_{j<r}(jump_j) + dlast + suffix_{l>=r}(ycs_l)
-  const float pre = block_exclusive_scan256(jump, wt);
-  const float ypre = block_exclusive_scan256(y, wt);   // sum_{l<r} ycs
+  const float pre = block_exclusive_scan(jump, wt);
+  const float ypre = block_exclusive_scan(y, wt);   // sum_{l<r} ycs
   __syncthreads();
   if ((r & 31) == 31) red[r >> 5] = ypre + y;
   __syncthreads();
-  const float ytot = red[7];
+  const float ytot = red[NW - 1];
   const float dd = pre + dl + (ytot - ypre);
   float pA = 0.f, pB = 0.f, pD = 0.f;
   if (live) {
@@ -1247,7 +1249,7 @@ __device__ __forceinline__ void finalize_block(const FinalizeArgs& f, int c, int
     __syncthreads();
     if (r == 0) {
       float t = 0.f;
-      for (int i = 0; i < 8; ++i) t += red[i];
+      for (int i = 0; i < NW; ++i) t += red[i];
       part[(((int64_t)b * H + h) * nc + c) * 3 + k] = t;
     }
   }
@@ -1270,22 +1272,23 @@ __device__ __forceinline__ void reduce_elem(const float4* __restrict__ in, float
   out[i] = s;
 }
 
-// The backward's tail in one launch of 256-thread blocks: blocks [0, nfin)
-// run the finalize step for (c, h, b) = (i % nc, (i / nc) % H, i / (nc H));
-// the rest sum the dC, then the dB head-block partials (nred blocks each).
-// The two parts are independent, so the latency-bound finalize blocks and the
-// bandwidth-bound sums share the SMs.
-__global__ void __launch_bounds__(256)
+// The backward's tail in one launch of NT-thread blocks (NT = L, one thread
+// per row of a chunk): blocks [0, nfin) run the finalize step for (c, h, b) =
+// (i % nc, (i / nc) % H, i / (nc H)); the rest sum the dC, then the dB
+// head-block partials (nred blocks each).  The two parts are independent, so
+// the latency-bound finalize blocks and the bandwidth-bound sums share the SMs.
+template <int NT>
+__global__ void __launch_bounds__(NT)
     k_bwd_tail_tc(FinalizeArgs f, int nfin, const float4* __restrict__ dCp,
                   float4* __restrict__ dC, const float4* __restrict__ dBp, float4* __restrict__ dB,
                   int nred, int64_t rows, int nblk, int N4) {
   const int blk = blockIdx.x;
   if (blk < nfin) {
-    finalize_block(f, blk % f.nc, (blk / f.nc) % f.H, blk / (f.nc * f.H));
+    finalize_block<NT>(f, blk % f.nc, (blk / f.nc) % f.H, blk / (f.nc * f.H));
     return;
   }
   const int rb = blk - nfin, which = rb / nred;
-  const int64_t i = (int64_t)(rb % nred) * 256 + threadIdx.x;
+  const int64_t i = (int64_t)(rb % nred) * NT + threadIdx.x;
   if (i < rows * N4) reduce_elem(which ? dBp : dCp, which ? dB : dC, i, nblk, N4);
 }
 
@@ -1414,8 +1417,8 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     const int nfin = d.nc * d.H * d.B;
     const int64_t rows = (int64_t)d.B * d.T * d.G;
     const int N4 = d.N / 4;
-    const int nred = nblk > 1 ? (int)((rows * N4 + 255) / 256) : 0;
-    SSD_LAUNCH("k_bwd_tail_tc", s, k_bwd_tail_tc<<<nfin + 2 * nred, 256, 0, s>>>(
+    const int nred = nblk > 1 ? (int)((rows * N4 + L - 1) / L) : 0;
+    SSD_LAUNCH("k_bwd_tail_tc", s, k_bwd_tail_tc<L><<<nfin + 2 * nred, L, 0, s>>>(
         fa, nfin, reinterpret_cast<const float4*>(w.dCp), reinterpret_cast<float4*>(a.dC),
         reinterpret_cast<const float4*>(w.dBp), reinterpret_cast<float4*>(a.dB),
         nred > 0 ? nred : 1, rows, nblk, N4));
