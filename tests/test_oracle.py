@@ -288,3 +288,35 @@ def test_golden_tiny_workload():
         assert abs(y[0, t, h, p] - v) <= 1e-12 * max(1.0, abs(v))
     assert abs(float(np.sum(y)) - gold["y_sum"]) <= 1e-9 * max(1.0, abs(gold["y_sum"]))
     assert abs(float(np.sum(final ** 2)) - gold["final_sq"]) <= 1e-9 * gold["final_sq"]
+
+
+def test_random_shapes_recurrence_dual_and_chunked_agree():
+    """Property check over random small shapes, group counts, chunk sizes,
+    with and without init / D: the recurrence oracle equals the quadratic
+    dual form (forward) and the chunked algorithm (forward and backward)."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+
+    @hyp.settings(max_examples=25, deadline=None, derandomize=True)
+    @hyp.given(Bt=st.integers(1, 2), T=st.integers(1, 40), hg=st.sampled_from([(1, 1), (2, 1),
+                                                                              (4, 2), (4, 4)]),
+               P=st.integers(1, 4), N=st.integers(1, 5), L=st.integers(1, 48),
+               init=st.booleans(), D=st.booleans(), seed=st.integers(0, 2 ** 16))
+    def check(Bt, T, hg, P, N, L, init, D, seed):
+        H, G = hg
+        args = rand_problem(Bt=Bt, T=T, H=H, P=P, N=N, G=G, seed=seed, init=init, D=D)
+        y, final = oracle.ssd_fwd(*args)
+        yq, fq = quadratic_form(*args)
+        assert close(y, yq) and close(final, fq)
+        out = chunked.ssd_chunked_fwd(*args, L)
+        assert close(out["y"], y) and close(out["final"], final)
+        rng = np.random.default_rng(seed + 1)
+        dy = rng.standard_normal(args[0].shape)
+        dfinal = rng.standard_normal((Bt, H, P, N))
+        ref = oracle.ssd_bwd(*args, dy, dfinal)
+        got = chunked.ssd_chunked_bwd(*args, dy, dfinal, L)
+        keys = ["dx", "ddt", "dA", "dB", "dC", "ddt_bias"] + (["dD"] if D else []) + \
+            (["dinit"] if init else [])
+        for k in keys:
+            assert close(got[k], ref[k], 1e-9), k
+    check()
