@@ -149,3 +149,25 @@ def test_random_shapes_match_torch_autograd():
             np.testing.assert_allclose(g[name], t.grad.numpy(), rtol=1e-8,
                                        atol=1e-12 * scale + 1e-12, err_msg=name)
     check()
+
+
+def test_norm_inputs_recipe():
+    """The norm workloads' seeded inputs: shapes, exact bf16 values, the
+    weight's spread around one, and determinism across calls."""
+    from state_space_model_sm_gb300.inputs import (NORM_WORKLOADS, NormShape,
+                                                   make_norm_inputs)
+    a = make_norm_inputs(NormShape(33, 64, 16), seed=3, dtype="bf16")
+    b = make_norm_inputs(NormShape(33, 64, 16), seed=3, dtype="bf16")
+    for x in (a.y, a.z, a.dout):
+        assert x.shape == (33, 64) and x.dtype == np.float32
+        assert (x.view(np.uint32) & 0xFFFF == 0).all()      # exactly representable in bf16
+    assert a.w.shape == (64,) and abs(float(a.w.mean()) - 1.0) < 0.1
+    for k in ("y", "z", "w", "dout"):
+        np.testing.assert_array_equal(getattr(a, k), getattr(b, k))
+    f = make_norm_inputs(NormShape(5, 16, 8), seed=3, dtype="f32")
+    assert (f.y.view(np.uint32) & 0xFFFF != 0).any()       # fp32 keeps its low bits
+    with pytest.raises(ValueError):
+        make_norm_inputs(NormShape(5, 16, 8), seed=0, dtype="fp16")
+    for name, (shape, dtype, _) in NORM_WORKLOADS.items():
+        assert shape.features % shape.group_size == 0, name
+        assert dtype in ("bf16", "f32"), name
