@@ -1,0 +1,938 @@
+// tcgen05 chunk kernels of the SSD, fed by TMA (sm_103a).  One template, four
+// roles, each over a 128-row tile of one chunk and a block of heads of one
+// group ("Optimizing Mamba-2 kernels for the B200", Stage 1 kernel table:
+// _chunk_scan_fwd fwd_5, _chunk_scan_chunk_state_bwd_dx bwd_8,
+// _chunk_scan_bwd_dC bwd_11, _chunk_state_bwd_db bwd_12):
+//
+//   FWD  rows l, columns s <= l:  P  = CB[l,s] e^{a_l-a_s} delta_s
+//        y_l  = sum_s P[l,s] x_s + e^{a_l} C_l.H_c^T + D x_l
+//   DX   rows s, columns l >= s:  P  = CB[l,s] e^{a_l-a_s}
+//        u_s  = sum_l P[s,l] dy_l + e^{a_last-a_s} B_s.dS_c^T
+//        dx_s = delta_s u_s + D dy_s;  <x_s,u_s>, delta_s <x_s, state part>, <x_s,dy_s>
+//   DC   rows l, columns s <= l:  P2 = e^{a_l-a_s} delta_s <dy_l, x_s>
+//        dC_l += sum_s P2[l,s] B_s + e^{a_l} dy_l.H_c   (summed over the block's heads)
+//        rowsum_l = sum_{s<l} CB[l,s] P2[l,s];  ycs_l = e^{a_l} <dy_l, C_l.H_c^T>
+//   DB   rows s, columns l >= s:  P2 = e^{a_l-a_s} delta_s <x_s, dy_l>
+//        dB_s += sum_l P2[s,l] C_l + delta_s e^{a_last-a_s} x_s.dS_c
+//        colsum_s = sum_{l>s} CB[l,s] P2[s,l]
+// with CB = C.B^T of the chunk (the column-row orientation in DX / DB).
+//
+// CB of the tile is formed once per CTA into TMEM and read by every head: it is
+// P's base in FWD / DX and gives the ddA sums of DC / DB directly, element by
+// element, so no per-head accumulator is needed for them.
+//
+// Warp roles (320 threads): warps 0-7 convert (TMEM -> decay, mask, hi/lo
+// bf16 split -> shared memory, and the epilogues), warp 8 issues every
+// tcgen05.mma, warp 9 issues every copy (TMA tiles of x, dy, B, C through
+// tensor maps; bulk copies of the state images and the per-head a / delta
+// vectors).  Full / empty mbarriers hand each buffer over; every wait is
+// bounded and records SSD_ERR_TIMEOUT on expiry.
+//
+// Precision: P and P2 are formed in fp32 and split into bf16 hi + lo; both
+// parts are multiplied (a single bf16 rounding of either exceeds the 2e-2
+// max-abs bar at the layer and hybrid workloads, measured on the CPU); state
+// images are split likewise; raw bf16 inputs enter unchanged; every product
+// accumulates in fp32 in TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "ssd_internal.h"
+#include "tc_ptx.cuh"
+
+namespace ssd {
+namespace {
+
+using namespace tc;
+using bf16 = __nv_bfloat16;
+
+enum : int { kFwd = 0, kDx = 1, kDc = 2, kDb = 3 };
+
+constexpr int kConvWarps = 8;  // 4 TMEM lane quarters x 2 column halves
+constexpr int kConv = 32 * kConvWarps;
+constexpr int kMmaWarp = kConvWarps;
+constexpr int kProdWarp = kConvWarps + 1;
+constexpr int kChunkThreads = 32 * (kConvWarps + 2);
+
+// Shared memory carving (byte offsets from a 1024-aligned base).
+template <int N, int L, int MODE>
+struct ChunkLayout {
+  static constexpr bool kRev = MODE == kDx || MODE == kDb;
+  static constexpr bool kS1 = MODE == kDc || MODE == kDb;
+  static constexpr int kLT = 128;                 // rows of a tile
+  static constexpr int kNP = N / 64;              // 64-wide panels of a B / C row
+  static constexpr int kRow = kNP * kLT * 128;    // the tile's row operand (C or B rows)
+  static constexpr int kCol = kNP * L * 128;      // column operand rows (B or C), up to L
+  static constexpr int kPB = 2 * kLT * 128;       // one P buffer: a 64-column panel, hi + lo
+  static constexpr int kHlo = kNP * 64 * 128;     // offset of a state image's lo panels
+  static constexpr int kImg = 2 * kHlo;           // one state image
+  static constexpr int kOps = L * 128;            // one head's x or dy rows (64 wide)
+  static constexpr int kHR = kLT * 128;           // DC / DB: the tile's dy (x) rows
+  // FWD / DX: the P buffers take the column operand's place once C.B^T is formed
+  static constexpr int kColP = kS1 ? kCol : (kCol > 2 * kPB ? kCol : 2 * kPB);
+  static constexpr int oRow = 0;
+  static constexpr int oCol = oRow + kRow;
+  static constexpr int oP = kS1 ? oCol + kCol : oCol;
+  static constexpr int oOps = kS1 ? oP + 2 * kPB : oCol + kColP;  // FWD / DX: two stages
+  static constexpr int oHR = oOps + (kS1 ? kOps : 2 * kOps);
+  static constexpr int oImg = oHR + (kS1 ? kHR : 0);               // FWD / DX only
+  static constexpr int oVec = oImg + (kS1 ? 0 : kImg);             // raw [2 stages][a, delta][L]
+  static constexpr int oDer = oVec + 4 * L * 4;                    // [3][a2, sx, cf][L]
+  static constexpr int oRed = oDer + 9 * L * 4;                    // [2][3][128] half-row sums
+  static constexpr int kBytes = oRed + 6 * 128 * 4 + 1024;
+  static_assert(kImg <= kPB, "a state image fits one P buffer");
+  static_assert(kBytes <= 227 * 1024, "shared memory budget");
+};
+
+struct ChunkArgs {
+  const float* delta;        // (B, H, nc, L)
+  const float* acs;          // (B, H, nc, L)
+  const unsigned char* img;  // state images (B, nc, H): H_c (FWD, DC) or dS_c (DX, DB)
+  const float* D;            // (H) or null
+  const bf16* xg;            // DX: x, for the epilogue's inner products
+  void* out;                 // FWD y, DX dx, DC / DB partials (B, T, G, nblk, N)
+  float* msum;               // DC rowsum, DB colsum  (B, H, nc, L)
+  float* ycs;                // DC
+  float* ddir;               // DX
+  float* qrow;               // DX
+  float* ddiag;              // DX
+  int T, H, G, nc, hb, nblk;
+  int* status;
+};
+
+__device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
+  return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 1023) &
+                                          ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void conv_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConv) : "memory");
+}
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&v)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// 8 fp32 values -> one 16-byte chunk of bf16 hi parts and one of lo parts.
+__device__ __forceinline__ void store_split8(unsigned char* hi, unsigned char* lo,
+                                             const float* v) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) split2_bf16(v[2 * i], v[2 * i + 1], h[i], l[i]);
+  *reinterpret_cast<uint4*>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Arrive once per warp (lane 0) after the warp's own work.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
+template <int N, int L, int MODE, typename Tout>
+__global__ void __launch_bounds__(kChunkThreads, 1)
+    k_chunk_tc(const __grid_constant__ CUtensorMap mRow, const __grid_constant__ CUtensorMap mCol,
+               const __grid_constant__ CUtensorMap mOps, const __grid_constant__ CUtensorMap mHR,
+               const ChunkArgs a) {
+  using LY = ChunkLayout<N, L, MODE>;
+  constexpr bool REV = LY::kRev, S1M = LY::kS1;
+  constexpr int LT = LY::kLT, NLT = L / LT, NP = LY::kNP;
+  constexpr uint32_t kColAcc = 256;  // FWD / DX: Y|ST pairs; DC / DB: S1 ring
+  constexpr uint32_t kColTot = 384;  // DC / DB: the block's dC / dB rows
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t bar_unit, bar_cb, bar_ops_full[2], bar_ops_empty[2], bar_vec_full[2],
+      bar_vec_empty[2], bar_img_full, bar_img_empty, bar_p_full[2], bar_p_empty[2],
+      bar_acc_full[2], bar_acc_empty[2], bar_tot, bar_final;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  unsigned char* base = align1024(smem_raw);
+  unsigned char* sRow = base + LY::oRow;
+  unsigned char* sCol = base + LY::oCol;
+  unsigned char* sP = base + LY::oP;
+  unsigned char* sOps = base + LY::oOps;
+  unsigned char* sHR = base + LY::oHR;
+  unsigned char* sImg = base + LY::oImg;
+  float* sVec = reinterpret_cast<float*>(base + LY::oVec);
+  float* sDer = reinterpret_cast<float*>(base + LY::oDer);
+  float* sRed = reinterpret_cast<float*>(base + LY::oRed);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // heavier row tiles (more columns) first: FWD / DC the last tile, DX / DB the first
+  const int gz = gridDim.z / NLT, zt = blockIdx.z / gz, zr = blockIdx.z % gz;
+  const int c = blockIdx.x, b = blockIdx.y, tile = REV ? zt : NLT - 1 - zt;
+  const int g = zr / a.nblk, kb = zr % a.nblk;
+  const int H = a.H, T = a.T, nc = a.nc, hb = a.hb;
+  const int h_begin = g * (H / a.G) + kb * hb;
+  const int r0 = tile * LT, col0 = REV ? r0 : 0, ncol = REV ? L - r0 : r0 + LT;
+  const int npan = ncol / 64;
+  const int t0 = c * L;
+  const int Lv = min(L, T - t0);
+  int* status = a.status;
+
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_unit, 1);
+    mbar_init(&bar_cb, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_ops_full[i], 1);
+      mbar_init(&bar_ops_empty[i], 1 + kConvWarps);
+      mbar_init(&bar_vec_full[i], 1);
+      mbar_init(&bar_vec_empty[i], kConvWarps);
+      mbar_init(&bar_p_full[i], kConvWarps);
+      mbar_init(&bar_p_empty[i], 1);
+      mbar_init(&bar_acc_full[i], 1);
+      mbar_init(&bar_acc_empty[i], kConvWarps);
+    }
+    mbar_init(&bar_img_full, 1);
+    mbar_init(&bar_img_empty, 1);
+    mbar_init(&bar_tot, 1);
+    mbar_init(&bar_final, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(&tmem_base, 512);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tm = tmem_base;
+  // uses of the two P buffers per head: the panels, then (DC / DB) the state
+  // image and the state term's A operand
+  const int upH = S1M ? npan + 2 : npan;
+
+  if (warp == kProdWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&mRow);
+      tma_prefetch_map(&mCol);
+      tma_prefetch_map(&mOps);
+      if constexpr (S1M) tma_prefetch_map(&mHR);
+      mbar_arrive_expect_tx(&bar_unit, (uint32_t)(NP * LT * 128 + NP * ncol * 128));
+      for (int kp = 0; kp < NP; ++kp) {
+        tma_load_4d(sRow + kp * LT * 128, &mRow, 64 * kp, g, t0 + r0, b, &bar_unit);
+        for (int k2 = 0; k2 < ncol / 128; ++k2)
+          tma_load_4d(sCol + kp * L * 128 + k2 * 128 * 128, &mCol, 64 * kp, g,
+                      t0 + col0 + 128 * k2, b, &bar_unit);
+      }
+      uint32_t n_vec[2] = {0, 0}, n_ops[2] = {0, 0}, n_img = 0;  // phases armed
+      auto load_vec = [&](int i) -> bool {
+        const int v = i & 1;
+        if (i >= 2 && !mbar_wait(&bar_vec_empty[v], ((i >> 1) - 1) & 1, status, &abort_flag))
+          return false;
+        const int64_t cv = (((int64_t)b * H + h_begin + i) * nc + c) * L;
+        mbar_arrive_expect_tx(&bar_vec_full[v], 2 * L * 4);
+        ++n_vec[v];
+        bulk_g2s(sVec + v * 2 * L, a.acs + cv, L * 4, &bar_vec_full[v]);
+        bulk_g2s(sVec + v * 2 * L + L, a.delta + cv, L * 4, &bar_vec_full[v]);
+        return true;
+      };
+      auto load_ops = [&](int i) -> bool {
+        const int h = h_begin + i;
+        if constexpr (!S1M) {
+          const int st = i & 1;
+          if (i >= 2 && !mbar_wait(&bar_ops_empty[st], ((i >> 1) - 1) & 1, status, &abort_flag))
+            return false;
+          mbar_arrive_expect_tx(&bar_ops_full[st], (uint32_t)(ncol * 128));
+          ++n_ops[st];
+          for (int k2 = 0; k2 < ncol / 128; ++k2)
+            tma_load_4d(sOps + st * LY::kOps + k2 * 128 * 128, &mOps, 0, h, t0 + col0 + 128 * k2,
+                        b, &bar_ops_full[st]);
+        } else {
+          if (i >= 1 && !mbar_wait(&bar_ops_empty[0], (i - 1) & 1, status, &abort_flag))
+            return false;
+          mbar_arrive_expect_tx(&bar_ops_full[0], (uint32_t)(LT * 128 + ncol * 128));
+          ++n_ops[0];
+          tma_load_4d(sHR, &mHR, 0, h, t0 + r0, b, &bar_ops_full[0]);
+          for (int k2 = 0; k2 < ncol / 128; ++k2)
+            tma_load_4d(sOps + k2 * 128 * 128, &mOps, 0, h, t0 + col0 + 128 * k2, b,
+                        &bar_ops_full[0]);
+        }
+        return true;
+      };
+      auto load_img = [&](int i) -> bool {
+        const unsigned char* src = a.img + (((int64_t)b * nc + c) * H + h_begin + i) * LY::kImg;
+        if constexpr (!S1M) {
+          if (i >= 1 && !mbar_wait(&bar_img_empty, (i - 1) & 1, status, &abort_flag)) return false;
+          mbar_arrive_expect_tx(&bar_img_full, LY::kImg);
+          ++n_img;
+          bulk_g2s(sImg, src, LY::kImg, &bar_img_full);
+        } else {
+          // the buffer of panel npan - 2, free once its product is done: the MMA
+          // warp signals that on bar_img_empty, one phase per head (a parity wait
+          // on the buffer's own barrier could alias across the phases skipped here)
+          const int bi = (i * upH + npan) & 1;
+          if (!mbar_wait(&bar_img_empty, i & 1, status, &abort_flag)) return false;
+          mbar_arrive_expect_tx(&bar_img_full, LY::kImg);
+          ++n_img;
+          bulk_g2s(sP + bi * LY::kPB, src, LY::kImg, &bar_img_full);
+        }
+        return true;
+      };
+      bool ok = hb > 0 && load_vec(0) && load_ops(0);
+      if constexpr (!S1M) ok = ok && load_img(0);
+      for (int i = 0; ok && i < hb; ++i) {
+        if (i + 1 < hb) {
+          ok = load_vec(i + 1) && load_ops(i + 1);
+          if constexpr (!S1M) ok = ok && load_img(i + 1);
+        }
+        if constexpr (S1M) ok = ok && load_img(i);
+      }
+      // copies still in flight (after an expired wait) land before the CTA exits
+      mbar_drain(&bar_unit, 0);
+      for (int v = 0; v < 2; ++v)
+        if (n_vec[v] > 0) mbar_drain(&bar_vec_full[v], (n_vec[v] - 1) & 1);
+      for (int v = 0; v < 2; ++v)
+        if (n_ops[v] > 0) mbar_drain(&bar_ops_full[v], (n_ops[v] - 1) & 1);
+      if (n_img > 0) mbar_drain(&bar_img_full, (n_img - 1) & 1);
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      bool ok = mbar_wait(&bar_unit, 0, status, &abort_flag);
+      fence_after_sync();
+      if (ok) {
+        const uint32_t id_cb = idesc_bf16(128, ncol, 0, 0);
+        for (int ks = 0; ks < N / 16; ++ks) {
+          const uint32_t kp = ks / 4, ko = (ks % 4) * 32;
+          mma_bf16(tm, sdesc(smem_u32(sRow) + kp * (LT * 128) + ko, 16, 1024),
+                   sdesc(smem_u32(sCol) + kp * (L * 128) + ko, 16, 1024), id_cb, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar_cb);
+      }
+      uint32_t nfull[2] = {0, 0};  // conversion uses of each P buffer seen so far
+      auto wait_pfull = [&](int bb) -> bool {
+        const bool r = mbar_wait(&bar_p_full[bb], nfull[bb] & 1, status, &abort_flag);
+        ++nfull[bb];
+        fence_after_sync();
+        return r;
+      };
+      // the state product X . img^T into TMEM column col (K = d_state), hi and lo
+      // parts of the image: C.H_c^T (FWD, DC) or B.dS_c^T (DX)
+      auto state_dot = [&](uint32_t col, const unsigned char* img) {
+        constexpr uint32_t id_st = idesc_bf16(128, 64, 0, 0);
+        for (int ks = 0; ks < N / 16; ++ks) {
+          const uint32_t kp = ks / 4, ko = (ks % 4) * 32;
+          const uint64_t ad = sdesc(smem_u32(sRow) + kp * (LT * 128) + ko, 16, 1024);
+          mma_bf16(tm + col, ad, sdesc(smem_u32(img) + kp * (64 * 128) + ko, 16, 1024), id_st,
+                   ks > 0 ? 1u : 0u);
+          mma_bf16(tm + col, ad, sdesc(smem_u32(img) + LY::kHlo + kp * (64 * 128) + ko, 16, 1024),
+                   id_st, 1u);
+        }
+      };
+      if constexpr (!S1M) {
+        constexpr uint32_t id_py = idesc_bf16(128, 64, 0, 1);
+        for (int i = 0; ok && i < hb; ++i) {
+          const int st = i & 1, ac = i & 1;
+          const uint32_t colY = kColAcc + 128 * ac;
+          ok = mbar_wait(&bar_ops_full[st], (i >> 1) & 1, status, &abort_flag);
+          if (ok && i >= 2)
+            ok = mbar_wait(&bar_acc_empty[ac], ((i >> 1) - 1) & 1, status, &abort_flag);
+          if (ok) ok = mbar_wait(&bar_img_full, i & 1, status, &abort_flag);
+          if (!ok) break;
+          fence_after_sync();
+          state_dot(colY + 64, sImg);
+          mma_commit(&bar_img_empty);
+          for (int j = 0; j < npan; ++j) {
+            const int bb = (i * upH + j) & 1;
+            if (!wait_pfull(bb)) {
+              ok = false;
+              break;
+            }
+            const unsigned char* pb = sP + bb * LY::kPB;
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t bd =
+                  sdesc(smem_u32(sOps) + st * LY::kOps + (64 * j + 16 * ks) * 128, L * 128, 1024);
+              mma_bf16(tm + colY, sdesc(smem_u32(pb) + ks * 32, 16, 1024), bd, id_py,
+                       (j > 0 || ks > 0) ? 1u : 0u);
+              mma_bf16(tm + colY, sdesc(smem_u32(pb) + LT * 128 + ks * 32, 16, 1024), bd, id_py, 1u);
+            }
+            mma_commit(&bar_p_empty[bb]);
+          }
+          if (!ok) break;
+          mma_commit(&bar_ops_empty[st]);
+          mma_commit(&bar_acc_full[ac]);
+        }
+      } else {
+        constexpr uint32_t id_s1 = idesc_bf16(128, 64, 0, 0);
+        constexpr uint32_t id_acc = idesc_bf16(128, N, 0, 1);
+        uint32_t ru = 0;  // ring uses: S1 panels and (DC) the state dot
+        auto ring_take = [&]() -> int {
+          const int slot = ru & 1;
+          if (ru >= 2 && !mbar_wait(&bar_acc_empty[slot], ((ru >> 1) - 1) & 1, status, &abort_flag))
+            return -1;
+          ++ru;
+          fence_after_sync();
+          return slot;
+        };
+        auto issue_s1 = [&](int j) -> bool {
+          const int slot = ring_take();
+          if (slot < 0) return false;
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tm + kColAcc + 64 * slot, sdesc(smem_u32(sHR) + ks * 32, 16, 1024),
+                     sdesc(smem_u32(sOps) + j * 64 * 128 + ks * 32, 16, 1024), id_s1,
+                     ks > 0 ? 1u : 0u);
+          mma_commit(&bar_acc_full[slot]);
+          return true;
+        };
+        bool first = true;
+        auto accumulate = [&](int u, int j) -> bool {
+          const int bb = u & 1;
+          if (!wait_pfull(bb)) return false;
+          const unsigned char* pb = sP + bb * LY::kPB;
+          const uint64_t dcol = sdesc(smem_u32(sCol), L * 128, 1024);
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t bd = desc_add(dcol, (j * 64 + ks * 16) * 128);
+            mma_bf16(tm + kColTot, sdesc(smem_u32(pb) + ks * 32, 16, 1024), bd, id_acc,
+                     first ? 0u : 1u);
+            first = false;
+            mma_bf16(tm + kColTot, sdesc(smem_u32(pb) + LT * 128 + ks * 32, 16, 1024), bd, id_acc,
+                     1u);
+          }
+          mma_commit(&bar_p_empty[bb]);
+          return true;
+        };
+        for (int i = 0; ok && i < hb; ++i) {
+          ok = mbar_wait(&bar_ops_full[0], i & 1, status, &abort_flag);
+          if (!ok) break;
+          fence_after_sync();
+          ok = issue_s1(0);
+          if (ok && npan == 1) mma_commit(&bar_ops_empty[0]);
+          for (int j = 0; ok && j < npan; ++j) {
+            if (j + 1 < npan) {
+              ok = issue_s1(j + 1);
+              // x / dy rows free once the head's S1 products are done
+              if (ok && j + 2 == npan) mma_commit(&bar_ops_empty[0]);
+            }
+            if (ok) ok = accumulate(i * upH + j, j);
+            if (ok && j + 2 == npan) mma_commit(&bar_img_empty);  // the image's buffer
+          }
+          if (!ok) break;
+          const int ui = i * upH + npan, bi = ui & 1, ba = (ui + 1) & 1;
+          ok = mbar_wait(&bar_img_full, i & 1, status, &abort_flag);
+          if (!ok) break;
+          fence_after_sync();
+          const unsigned char* img = sP + bi * LY::kPB;
+          if constexpr (MODE == kDc) {
+            const int slot = ring_take();
+            if (slot < 0) {
+              ok = false;
+              break;
+            }
+            state_dot(kColAcc + 64 * slot, img);
+            mma_commit(&bar_acc_full[slot]);
+          }
+          if (!wait_pfull(ba)) {
+            ok = false;
+            break;
+          }
+          // TOT += A_st . img with A_st = e^{a_l} dy_l (DC) or delta_s e^{a_last-a_s} x_s
+          // (DB) in hi / lo, the image MN-major (K = p rows, N = d_state)
+          const unsigned char* pa = sP + ba * LY::kPB;
+          const uint64_t dim = sdesc(smem_u32(img), 64 * 128, 1024);
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t ah = sdesc(smem_u32(pa) + ks * 32, 16, 1024);
+            const uint64_t al = sdesc(smem_u32(pa) + LT * 128 + ks * 32, 16, 1024);
+            const uint64_t bh = desc_add(dim, ks * 2048), bl = desc_add(dim, LY::kHlo + ks * 2048);
+            mma_bf16(tm + kColTot, ah, bh, id_acc, 1u);
+            mma_bf16(tm + kColTot, ah, bl, id_acc, 1u);
+            mma_bf16(tm + kColTot, al, bh, id_acc, 1u);
+          }
+          mma_commit(&bar_p_empty[bi]);
+          mma_commit(&bar_p_empty[ba]);
+        }
+        if (ok) mma_commit(&bar_tot);
+      }
+      // every product issued has completed before TMEM is released
+      mma_commit(&bar_final);
+      mbar_drain(&bar_final, 0);
+    }
+  } else {
+    // --------------------------------------------------- conversion warps
+    const int q = warp & 3, ch = warp >> 2;
+    const int rr = 32 * q + lane, r = r0 + rr;  // this thread's row (TMEM lane), chunk-local
+    const int rw = r0 + 32 * q;                 // the warp's first row
+    const uint32_t tl = tm + ((uint32_t)(32 * q) << 16);
+    const bool live = r < Lv;
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_cb, 0, status, &abort_flag));
+    fence_after_sync();
+
+    // per-head vectors -> derived arrays of stage v: a2 = a log2 e; sx: FWD / DC / DB
+    // a2 - log2 delta (+inf where delta = 0), DX delta; cf: column factors of the
+    // factorized decay inside the causal triangle
+    // (three buffers: a head's epilogue may still read its arrays while the
+    // next-but-one head derives, and the conversion warps stay within one head
+    // of each other through the barriers here)
+    auto derive = [&](int i) {
+      const int v = i & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_vec_full[v], (i >> 1) & 1, status, &abort_flag)) &&
+           ok;
+      const float* ra = sVec + v * 2 * L;
+      float* da2 = sDer + (i % 3) * 3 * L;
+      float* dsx = da2 + L;
+      float* dcf = dsx + L;
+      for (int t = tid; t < L; t += kConv) {
+        const float a2 = ra[t] * kLog2e, dl = ra[L + t];
+        da2[t] = a2;
+        if constexpr (MODE == kDx) dsx[t] = dl;
+        else dsx[t] = dl > 0.f ? a2 - lg2_approx(dl) : __int_as_float(0x7f800000);
+      }
+      warp_arrive(&bar_vec_empty[v], lane);
+      conv_sync();
+      for (int t = tid; t < L; t += kConv) {
+        if constexpr (REV) dcf[t] = ex2_approx(da2[t] - da2[t & ~15]);
+        else dcf[t] = ex2_approx(da2[t | 15] - dsx[t]);
+      }
+      conv_sync();
+    };
+
+    // one 64-column panel j of head i (P-buffer use u): form P / P2 in fp32
+    // from TMEM, split it into hi / lo bf16 and store it for the MMA warp
+    uint32_t ru = 0;  // DC / DB ring uses consumed
+    float msum = 0.f;
+    auto panel = [&](int i, int j, int u) {
+      const float* da2 = sDer + (i % 3) * 3 * L;
+      const float* dsx = da2 + L;
+      const float* dcf = dsx + L;
+      const float a2r = da2[r], sxr = dsx[r];
+      const int cbase = col0 + 64 * j + 32 * ch;  // chunk-local first column of this thread
+      float base[2][16], cbv[2][16];
+      bool outside[2], inside[2];
+#pragma unroll
+      for (int qg = 0; qg < 2; ++qg) {
+        const int cg = cbase + 16 * qg;
+        outside[qg] = REV ? cg + 15 < rw : cg > rw + 31;
+        inside[qg] = REV ? cg > rw + 31 : cg + 15 < rw;
+      }
+      int slot = 0;
+      if constexpr (S1M) {
+        slot = ru & 1;
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&bar_acc_full[slot], (ru >> 1) & 1, status, &abort_flag)) && ok;
+        ++ru;
+        fence_after_sync();
+      }
+      if (ok) {
+#pragma unroll
+        for (int qg = 0; qg < 2; ++qg) {
+          if (outside[qg]) continue;
+          const uint32_t cb_col = 64 * j + 32 * ch + 16 * qg;  // CB's column (from col0)
+          if constexpr (S1M) {
+            tmem_ld16(tl + kColAcc + 64 * slot + 32 * ch + 16 * qg, base[qg]);
+            tmem_ld16(tl + cb_col, cbv[qg]);
+          } else {
+            tmem_ld16(tl + cb_col, base[qg]);
+          }
+        }
+        tmem_wait_ld();
+      }
+      if constexpr (S1M) {
+        fence_before_sync();
+        warp_arrive(&bar_acc_empty[slot], lane);
+      }
+      const int bb = u & 1;
+      if (u >= 2)
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_p_empty[bb], ((u >> 1) - 1) & 1, status,
+                                               &abort_flag)) && ok;
+      unsigned char* pb = sP + bb * LY::kPB;
+#pragma unroll
+      for (int qg = 0; qg < 2; ++qg) {
+        const int cg = cbase + 16 * qg;
+        float vv[16];
+        if (outside[qg] || !ok) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) vv[e] = 0.f;
+        } else if (inside[qg]) {
+          // e^{a_l - a_s} (times delta) = R_row * cf_col, with the group's edge column m
+          float R;
+          if constexpr (MODE == kFwd || MODE == kDc) R = ex2_approx(a2r - da2[cg + 15]);
+          else if constexpr (MODE == kDx) R = ex2_approx(da2[cg] - a2r);
+          else R = ex2_approx(da2[cg] - sxr);
+          const float2 R2 = make_float2(R, R);
+#pragma unroll
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 cf = *reinterpret_cast<const float4*>(dcf + cg + 4 * e4);
+            const float2 f0 = __fmul2_rn(R2, make_float2(cf.x, cf.y));
+            const float2 f1 = __fmul2_rn(R2, make_float2(cf.z, cf.w));
+            const float2 p0 = __fmul2_rn(f0, make_float2(base[qg][4 * e4], base[qg][4 * e4 + 1]));
+            const float2 p1 =
+                __fmul2_rn(f1, make_float2(base[qg][4 * e4 + 2], base[qg][4 * e4 + 3]));
+            vv[4 * e4] = p0.x;
+            vv[4 * e4 + 1] = p0.y;
+            vv[4 * e4 + 2] = p1.x;
+            vv[4 * e4 + 3] = p1.y;
+          }
+          if constexpr (S1M) {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < 16; e += 2)
+              acc = __ffma2_rn(make_float2(vv[e], vv[e + 1]),
+                               make_float2(cbv[qg][e], cbv[qg][e + 1]), acc);
+            msum += acc.x + acc.y;
+          }
+        } else {
+          // across the diagonal: per-element exponent and mask
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int cl = cg + e;
+            float f;
+            if constexpr (MODE == kFwd || MODE == kDc) f = ex2_approx(a2r - dsx[cl]);
+            else if constexpr (MODE == kDx) f = ex2_approx(da2[cl] - a2r);
+            else f = ex2_approx(da2[cl] - sxr);
+            const bool valid = REV ? cl >= r : cl <= r;
+            vv[e] = valid ? f * base[qg][e] : 0.f;
+            if constexpr (S1M)
+              if (cl != r) msum = fmaf(vv[e], cbv[qg][e], msum);
+          }
+        }
+#pragma unroll
+        for (int k8 = 0; k8 < 2; ++k8) {
+          const uint32_t off = sw128(rr, 4 * ch + 2 * qg + k8);
+          store_split8(pb + off, pb + LT * 128 + off, vv + 8 * k8);
+        }
+      }
+      fence_async_smem();
+      warp_arrive(&bar_p_full[bb], lane);
+    };
+
+    if constexpr (!S1M) {
+      // FWD / DX: a head's epilogue runs after the next head's first panel, so
+      // its last products finish while that panel is converted
+      // DX: this thread's 32 x values of its row, loaded from global memory
+      // when its head starts (xa); head i's epilogue runs during head i + 1 (xb)
+      uint4 xa[4] = {}, xb[4] = {};
+      auto prefetch_x = [&](int i, uint4 (&xr)[4]) {
+        if constexpr (MODE == kDx) {
+          const int64_t off = (((int64_t)b * T + t0 + r) * H + h_begin + i) * 64 + 32 * ch;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            xr[k] = live ? *reinterpret_cast<const uint4*>(a.xg + off + 8 * k)
+                         : make_uint4(0, 0, 0, 0);
+        }
+      };
+      auto epilogue = [&](int i, const uint4 (&xr)[4]) {
+        const int st = i & 1, ac = i & 1, h = h_begin + i;
+        const float* da2 = sDer + (i % 3) * 3 * L;
+        const float* dsx = da2 + L;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full[ac], (i >> 1) & 1, status,
+                                               &abort_flag)) && ok;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_ops_full[st], (i >> 1) & 1, status,
+                                               &abort_flag)) && ok;
+        fence_after_sync();
+        float yv[2][16], sv[2][16];
+        const uint32_t colY = kColAcc + 128 * ac;
+        if (ok) {
+          tmem_ld16(tl + colY + 32 * ch, yv[0]);
+          tmem_ld16(tl + colY + 32 * ch + 16, yv[1]);
+          tmem_ld16(tl + colY + 64 + 32 * ch, sv[0]);
+          tmem_ld16(tl + colY + 64 + 32 * ch + 16, sv[1]);
+          tmem_wait_ld();
+        }
+        fence_before_sync();
+        warp_arrive(&bar_acc_empty[ac], lane);
+        // this thread's row of the stage's x (FWD) or dy (DX) rows
+        const unsigned char* orow = sOps + st * LY::kOps;
+        const int orr = r - col0;
+        const float Dh = a.D ? a.D[h] : 0.f;
+        const float a2r = da2[r];
+        float pd = 0.f, pq = 0.f, pdd = 0.f;
+        if (ok && live) {
+          const float ea = MODE == kFwd ? ex2_approx(a2r) : ex2_approx(da2[L - 1] - a2r);
+          const float dr = MODE == kDx ? dsx[r] : 0.f;
+          const int64_t ooff = (((int64_t)b * T + t0 + r) * H + h) * 64 + 32 * ch;
+#pragma unroll
+          for (int k8 = 0; k8 < 4; ++k8) {
+            float ov[8], o[8];
+            unpack8(*reinterpret_cast<const uint4*>(orow + sw128(orr, 4 * ch + k8)), ov);
+            const float* yk = yv[k8 >> 1] + 8 * (k8 & 1);
+            const float* sk = sv[k8 >> 1] + 8 * (k8 & 1);
+            if constexpr (MODE == kFwd) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o[e] = yk[e] + ea * sk[e] + Dh * ov[e];
+            } else {
+              float xv[8];
+              unpack8(xr[k8], xv);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float us = ea * sk[e];
+                const float uu = yk[e] + us;
+                o[e] = fmaf(dr, uu, Dh * ov[e]);
+                pd = fmaf(xv[e], uu, pd);
+                pq = fmaf(xv[e], us, pq);
+                pdd = fmaf(xv[e], ov[e], pdd);
+              }
+            }
+            Tout* op = static_cast<Tout*>(a.out) + ooff + 8 * k8;
+            if constexpr (sizeof(Tout) == 4) {
+              float* of = reinterpret_cast<float*>(op);
+              *reinterpret_cast<float4*>(of) = make_float4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<float4*>(of + 4) = make_float4(o[4], o[5], o[6], o[7]);
+            } else {
+              *reinterpret_cast<uint4*>(op) =
+                  make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]),
+                             pack_bf16(o[6], o[7]));
+            }
+          }
+        }
+        warp_arrive(&bar_ops_empty[st], lane);
+        if constexpr (MODE == kDx) {
+          float* red = sRed + (i & 1) * 3 * 128;
+          if (ch == 1) {
+            red[rr] = pd;
+            red[128 + rr] = pq;
+            red[256 + rr] = pdd;
+          }
+          conv_sync();
+          if (ch == 0 && live && ok) {
+            const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
+            a.ddir[cv + r] = pd + red[rr];
+            a.qrow[cv + r] = dsx[r] * (pq + red[128 + rr]);
+            a.ddiag[cv + r] = pdd + red[256 + rr];
+          }
+        }
+      };
+      for (int i = 0; i < hb; ++i) {
+        derive(i);
+        if constexpr (MODE == kDx) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) xb[k] = xa[k];  // the previous head's
+        }
+        prefetch_x(i, xa);
+        for (int j = 0; j < npan; ++j) {
+          panel(i, j, i * upH + j);
+          if (j == 0 && i > 0) epilogue(i - 1, xb);
+        }
+      }
+      if (hb > 0) epilogue(hb - 1, xa);
+    } else {
+      uint4 hrow[4];  // this thread's 32 values of its row of dy (DC) or x (DB)
+      for (int i = 0; i < hb; ++i) {
+        const int h = h_begin + i;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_ops_full[0], i & 1, status, &abort_flag)) &&
+             ok;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          hrow[k] = *reinterpret_cast<const uint4*>(sHR + sw128(rr, 4 * ch + k));
+        warp_arrive(&bar_ops_empty[0], lane);
+        derive(i);
+        msum = 0.f;
+        for (int j = 0; j < npan; ++j) panel(i, j, i * upH + j);
+        const float* da2 = sDer + (i % 3) * 3 * L;
+        const float* dsx = da2 + L;
+        // the state term's A operand into the buffer after the image's
+        const int ua = i * upH + npan + 1, ba = ua & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_p_empty[ba], ((ua >> 1) - 1) & 1, status,
+                                               &abort_flag)) && ok;
+        {
+          const float sc = MODE == kDc ? ex2_approx(da2[r]) : ex2_approx(da2[L - 1] - dsx[r]);
+          unsigned char* pa = sP + ba * LY::kPB;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float v[8];
+            unpack8(hrow[k], v);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] *= sc;
+            const uint32_t off = sw128(rr, 4 * ch + k);
+            store_split8(pa + off, pa + LT * 128 + off, v);
+          }
+        }
+        fence_async_smem();
+        warp_arrive(&bar_p_full[ba], lane);
+        float ypart = 0.f;
+        if constexpr (MODE == kDc) {
+          // ycs_l = e^{a_l} <dy_l, C_l . H_c^T> from the state dot in the ring
+          const int slot = ru & 1;
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(&bar_acc_full[slot], (ru >> 1) & 1, status, &abort_flag)) && ok;
+          ++ru;
+          fence_after_sync();
+          float sv[2][16];
+          if (ok) {
+            tmem_ld16(tl + kColAcc + 64 * slot + 32 * ch, sv[0]);
+            tmem_ld16(tl + kColAcc + 64 * slot + 32 * ch + 16, sv[1]);
+            tmem_wait_ld();
+          }
+          fence_before_sync();
+          warp_arrive(&bar_acc_empty[slot], lane);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float v[8];
+            unpack8(hrow[k], v);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ypart = fmaf(v[e], sv[k >> 1][8 * (k & 1) + e], ypart);
+          }
+          ypart *= ex2_approx(da2[r]);
+        }
+        float* red = sRed + (i & 1) * 3 * 128;
+        if (ch == 1) {
+          red[rr] = msum;
+          red[128 + rr] = ypart;
+        }
+        conv_sync();
+        if (ch == 0 && live && ok) {
+          const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
+          a.msum[cv + r] = msum + red[rr];
+          if constexpr (MODE == kDc) a.ycs[cv + r] = ypart + red[128 + rr];
+        }
+      }
+      // the block's accumulated dC / dB rows
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_tot, 0, status, &abort_flag)) && ok;
+      fence_after_sync();
+      if (ok && hb > 0) {
+        float* o = static_cast<float*>(a.out) +
+                   ((((int64_t)b * T + t0 + r) * a.G + g) * a.nblk + kb) * N + ch * (N / 2);
+#pragma unroll
+        for (int c0 = 0; c0 < N / 2; c0 += 16) {
+          float v[16];
+          tmem_ld16(tl + kColTot + ch * (N / 2) + c0, v);
+          tmem_wait_ld();
+          if (live) {
+#pragma unroll
+            for (int k4 = 0; k4 < 16; k4 += 4)
+              *reinterpret_cast<float4*>(o + c0 + k4) =
+                  make_float4(v[k4], v[k4 + 1], v[k4 + 2], v[k4 + 3]);
+          }
+        }
+      }
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tm, 512);
+}
+
+// ------------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tensor map of a (B, T, X, inner) bf16 tensor read in boxes of 64 inner
+// elements (128 bytes, the 128-byte swizzle span) x 128 rows of T, one X and
+// one batch index; rows past T read as zeros.
+bool make_map(CUtensorMap* m, const void* ptr, int inner, int X, int T, int B) {
+  const auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)X, (cuuint64_t)T, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)inner * 2, (cuuint64_t)X * inner * 2,
+                                 (cuuint64_t)T * X * inner * 2};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int N, int L, int MODE, typename Tout>
+cudaError_t launch_chunk(const Dims& d, const CUtensorMap& mRow, const CUtensorMap& mCol,
+                         const CUtensorMap& mOps, const CUtensorMap& mHR, const ChunkArgs& a,
+                         const char* name, cudaStream_t s) {
+  using LY = ChunkLayout<N, L, MODE>;
+  auto kern = k_chunk_tc<N, L, MODE, Tout>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes);
+  const dim3 grid(d.nc, d.B, (L / 128) * d.G * a.nblk);
+  SSD_LAUNCH(name, s, kern<<<grid, kChunkThreads, LY::kBytes, s>>>(mRow, mCol, mOps, mHR, a));
+  return cudaGetLastError();
+}
+
+template <int N, int L>
+cudaError_t chunk_fwd_nl(const Dims& d, const FwdArgs& f, const FwdWs& w, int nblk,
+                         cudaStream_t s) {
+  CUtensorMap mB, mC, mX;
+  if (!make_map(&mB, f.B, d.N, d.G, d.T, d.B) || !make_map(&mC, f.C, d.N, d.G, d.T, d.B) ||
+      !make_map(&mX, f.x, 64, d.H, d.T, d.B))
+    return cudaErrorInvalidValue;
+  ChunkArgs a{};
+  a.delta = w.delta;
+  a.acs = w.acs;
+  a.img = static_cast<const unsigned char*>(w.Himg);
+  a.D = f.D;
+  a.out = f.y;
+  a.T = d.T;
+  a.H = d.H;
+  a.G = d.G;
+  a.nc = d.nc;
+  a.nblk = nblk;
+  a.hb = d.H / d.G / nblk;
+  a.status = device_status_ptr();
+  if (!a.status) return cudaErrorUnknown;
+  return d.out_bf16 ? launch_chunk<N, L, kFwd, bf16>(d, mC, mB, mX, mX, a, "k_scan_tc", s)
+                    : launch_chunk<N, L, kFwd, float>(d, mC, mB, mX, mX, a, "k_scan_tc", s);
+}
+
+template <int N, int L>
+cudaError_t chunk_bwd_nl(const Dims& d, const BwdArgs& ba, const TcBwdWs& w, int nblk,
+                         float* dCout, float* dBout, cudaStream_t s) {
+  CUtensorMap mB, mC, mX, mDY;
+  if (!make_map(&mB, ba.f.B, d.N, d.G, d.T, d.B) || !make_map(&mC, ba.f.C, d.N, d.G, d.T, d.B) ||
+      !make_map(&mX, ba.f.x, 64, d.H, d.T, d.B) || !make_map(&mDY, ba.dy, 64, d.H, d.T, d.B))
+    return cudaErrorInvalidValue;
+  ChunkArgs a{};
+  a.delta = w.delta;
+  a.acs = w.acs;
+  a.D = ba.f.D;
+  a.xg = static_cast<const bf16*>(ba.f.x);
+  a.T = d.T;
+  a.H = d.H;
+  a.G = d.G;
+  a.nc = d.nc;
+  a.nblk = nblk;
+  a.hb = d.H / d.G / nblk;
+  a.status = device_status_ptr();
+  if (!a.status) return cudaErrorUnknown;
+  // dx (with the ddt / ddA inner products)
+  ChunkArgs ax = a;
+  ax.img = static_cast<const unsigned char*>(w.dSimg);
+  ax.out = ba.dx;
+  ax.ddir = w.ddir;
+  ax.qrow = w.qrow;
+  ax.ddiag = w.ddiag;
+  cudaError_t e = launch_chunk<N, L, kDx, float>(d, mB, mC, mDY, mDY, ax, "k_scan_tc_dx", s);
+  if (e != cudaSuccess) return e;
+  // dC: rows l, S1 = dy.x^T, H_c images
+  ChunkArgs ac = a;
+  ac.img = static_cast<const unsigned char*>(w.Himg);
+  ac.out = dCout;
+  ac.msum = w.rowsum;
+  ac.ycs = w.ycs;
+  e = launch_chunk<N, L, kDc, float>(d, mC, mB, mX, mDY, ac, "k_bwd_dc_tc", s);
+  if (e != cudaSuccess) return e;
+  // dB: rows s, S1 = x.dy^T, dS images
+  ChunkArgs ab = a;
+  ab.img = static_cast<const unsigned char*>(w.dSimg);
+  ab.out = dBout;
+  ab.msum = w.colsum;
+  return launch_chunk<N, L, kDb, float>(d, mB, mC, mDY, mX, ab, "k_bwd_db_tc", s);
+}
+
+}  // namespace
+
+cudaError_t tc_chunk_forward(const Dims& d, const FwdArgs& f, const FwdWs& w, int nblk,
+                             cudaStream_t s) {
+  if (d.N == 128 && d.L == 256) return chunk_fwd_nl<128, 256>(d, f, w, nblk, s);
+  if (d.N == 128 && d.L == 128) return chunk_fwd_nl<128, 128>(d, f, w, nblk, s);
+  if (d.N == 64 && d.L == 256) return chunk_fwd_nl<64, 256>(d, f, w, nblk, s);
+  return chunk_fwd_nl<64, 128>(d, f, w, nblk, s);
+}
+
+cudaError_t tc_chunk_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w, int nblk,
+                              float* dCout, float* dBout, cudaStream_t s) {
+  if (d.N == 128 && d.L == 256) return chunk_bwd_nl<128, 256>(d, a, w, nblk, dCout, dBout, s);
+  if (d.N == 128 && d.L == 128) return chunk_bwd_nl<128, 128>(d, a, w, nblk, dCout, dBout, s);
+  if (d.N == 64 && d.L == 256) return chunk_bwd_nl<64, 256>(d, a, w, nblk, dCout, dBout, s);
+  return chunk_bwd_nl<64, 128>(d, a, w, nblk, dCout, dBout, s);
+}
+
+}  // namespace ssd

@@ -164,4 +164,13 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStre
 int tc_bwd_nblk(const Dims& d);
 cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w, cudaStream_t s);
 
+// The TMA-fed chunk kernels (ssd_chunk_tc.cu), over (batch, chunk, row tile,
+// group, block of nblk heads): chunk_scan (y from the state images in w.Himg),
+// and the backward's dx, dC and dB (with the ddA row / column sums, ycs, qrow,
+// ddir and ddiag).  dCout / dBout receive (B, T, G, nblk, N) partials.
+cudaError_t tc_chunk_forward(const Dims& d, const FwdArgs& f, const FwdWs& w, int nblk,
+                             cudaStream_t s);
+cudaError_t tc_chunk_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w, int nblk,
+                              float* dCout, float* dBout, cudaStream_t s);
+
 }  // namespace ssd

@@ -315,852 +315,6 @@ __global__ void __launch_bounds__(256, 2)
   if (warp == 0) tmem_dealloc(tm, kTmemCols);
 }
 
-// ================================================================ chunk_scan
-// One kernel, two directions.
-//   forward (REV = false), rows r = l of chunk c, columns s in [0, l0 + 128):
-//     CB[l, s] = C_l . B_s                       (TMEM cols 0.., once per CTA)
-//     per head: Y  = sum_s P[l, s] x_s,  P = CB e^{a_l - a_s} delta_s [s <= l]
-//               ST = C_l . H_c[p, :]
-//               y_l = Y + e^{a_l} ST + D x_l
-//   backward dx (REV = true), rows r = s, columns l in [s0, L):
-//     CBT[s, l] = B_s . C_l
-//     per head: Y  = sum_l P[s, l] dy_l,  P = CBT e^{a_l - a_s} [l >= s]
-//               ST = B_s . dS_c[p, :]
-//               u_s = Y + e^{a_last - a_s} ST;  dx_s = delta_s u_s + D dy_s
-//               ddir_s = <x_s, u_s>,  qrow_s = delta_s <x_s, e^{a_last - a_s} ST>,
-//               ddiag_s = <x_s, dy_s>
-// Persistent, one CTA (512 threads) per SM over a balanced range of (batch,
-// chunk, 128-row tile, group) x head items.  Per unit the score tile is
-// formed once; then the two 8-warp pipelines run independent chains on
-// alternate heads (own TMEM accumulators, P buffer, operand rows and
-// mbarriers), so one pipeline's loads and waits overlap the other's work.
-template <int N, int L>
-struct ScanSmem {
-  static constexpr int kLT = 128;
-  static constexpr int kC = (N / 64) * kLT * 128;           // row-operand rows of the tile
-  static constexpr int kBrows = (N / 64) * L * 128;         // column-operand rows
-  static constexpr int kPw = 2 * kLT * 128;                 // per group: P panel hi + lo
-  static constexpr int kBP = kBrows > 2 * kPw ? kBrows : 2 * kPw;
-  static constexpr int kX = L * 128;                        // per group: x or dy rows
-  static constexpr int kHlo = (N / 64) * 64 * 128;          // offset of the state's lo part
-  static constexpr int kImg = 2 * kHlo;                     // bytes of one state image
-  static constexpr int kBytes = kC + kBP + 2 * kX + (10 * L + 6 * 128) * 4 + 1024;
-};
-
-__device__ __forceinline__ void group_sync(int id) {
-  asm volatile("bar.sync %0, 256;" ::"r"(id) : "memory");
-}
-
-template <int N, int L, typename Tout, bool REV>
-__global__ void __launch_bounds__(512, 1)
-    k_scan_tc(const bf16* __restrict__ x, const bf16* __restrict__ Bm,
-              const bf16* __restrict__ Cm, const bf16* __restrict__ dy,
-              const float* __restrict__ delta, const float* __restrict__ acs,
-              const unsigned char* __restrict__ simg, const float* __restrict__ D,
-              Tout* __restrict__ out, float* __restrict__ ddir, float* __restrict__ qrow,
-              float* __restrict__ ddiag, int B_, int T, int H, int G, int nc, int items_per_cta,
-              int* status) {
-  using SM = ScanSmem<N, L>;
-  constexpr int LT = SM::kLT, NLT = L / LT;
-  extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t bar_cb, bar_p[2], bar_st[2], bar_done[2];
-  __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag;
-  unsigned char* base = align1024(smem_raw);
-  unsigned char* sR = base;               // row operand: C (fwd) or B (rev) rows of the tile
-  unsigned char* sBP = sR + SM::kC;       // column operand rows, later the groups' P buffers
-  unsigned char* sXall = sBP + SM::kBP;   // per group: x (fwd) or dy (rev) rows
-  float* sAall = reinterpret_cast<float*>(sXall + 2 * SM::kX);  // per group: a [L], delta [L]
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int hpg = H / G;
-  const int64_t n_items = (int64_t)B_ * nc * NLT * H;  // (batch, chunk, tile, group) x head
-  const int64_t it_begin = (int64_t)blockIdx.x * items_per_cta;
-  const int64_t it_end = min(n_items, it_begin + items_per_cta);
-  const bf16* rowsrc = REV ? Bm : Cm;
-  const bf16* colsrc = REV ? Cm : Bm;
-  const bf16* opsrc = REV ? dy : x;
-
-  if (tid == 0) {
-    abort_flag = 0;
-    mbar_init(&bar_cb, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_p[i], 1);
-      mbar_init(&bar_st[i], 1);
-      mbar_init(&bar_done[i], 1);
-    }
-    fence_mbar_init();
-  }
-  if (warp == 0) tmem_alloc(&tmem_base, 512);
-  // TMEM and the per-group state live across the CTA's whole item range
-  fence_before_sync();
-  __syncthreads();
-  fence_after_sync();
-  const uint32_t tm = tmem_base;
-  // two pipelines of 8 warps; a TMEM row is shared by the warps q and q + 4
-  // of a pipeline, each taking 32 of a panel's 64 columns
-  const int wg = tid >> 8, wtid = tid & 255, wq = wtid >> 5, q = wq & 3, half = wq >> 2;
-  const int rr = 32 * q + lane;
-  const uint32_t tlane = tm + ((uint32_t)(32 * q) << 16);
-  const uint32_t colY = 256 + 128 * wg, colST = colY + 64;
-  const int gbar = 1 + wg;
-  float* sred = sAall + 8 * L + wg * 3 * 128;  // [3][128] per pipeline: half-row partial sums
-  float* scf = sAall + 8 * L + 6 * 128 + wg * L;  // per pipeline: column factors (forward)
-  uint32_t n_p = 0, n_st = 0, n_done = 0, n_units = 0;
-
-  for (int64_t item = it_begin; item < it_end;) {
-    // one unit = (batch, chunk, row tile, group); this CTA's heads of it
-    const int64_t unit = item / hpg;
-    const int j0 = (int)(item % hpg);
-    const int j1 = (int)min((int64_t)hpg, j0 + (it_end - item));
-    item += j1 - j0;
-    const int g = (int)(unit % G);
-    const int64_t bct = unit / G;
-    const int tile = (int)(bct % NLT);
-    const int64_t bc = bct / NLT;
-    const int c = (int)(bc % nc), b = (int)(bc / nc);
-    const int h_begin = g * hpg + j0, h_end = g * hpg + j1;
-    const int r0 = tile * LT;                       // first row (chunk-local)
-    const int col0 = REV ? r0 : 0;                  // first column
-    const int ncol = REV ? L - r0 : r0 + LT;        // number of columns
-    const int nsp = ncol / 64;
-    const int64_t t0 = (int64_t)c * L;
-    const int Lv = min(L, T - (int)t0);
-    const int r = r0 + rr;                          // this thread's row (TMEM lane)
-
-  stage_rows_async(sR, LT, N / 8, LT * 128, Lv - r0, rowsrc, [&](int rr2) {
-      return rowsrc + (((int64_t)b * T + t0 + r0 + rr2) * G + g) * N;
-    });
-    stage_rows_async(sBP, ncol, N / 8, L * 128, Lv - col0, colsrc, [&](int cc) {
-      return colsrc + (((int64_t)b * T + t0 + col0 + cc) * G + g) * N;
-    });
-    cp_async_commit();
-    cp_async_wait<0>();
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    if (tid == 0) {
-      const uint32_t id = idesc_bf16(128, ncol, 0, 0);
-      for (int ks = 0; ks < N / 16; ++ks) {
-        const uint32_t kp = ks / 4, ko = (ks % 4) * 32;
-        mma_bf16(tm, sdesc(smem_u32(sR) + kp * (LT * 128) + ko, 16, 1024),
-                 sdesc(smem_u32(sBP) + kp * (L * 128) + ko, 16, 1024), id, ks > 0 ? 1u : 0u);
-      }
-      mma_commit(&bar_cb);
-    }
-    mbar_wait(&bar_cb, n_units & 1, status, &abort_flag);
-    ++n_units;
-    fence_after_sync();
-    // sBP (the column operand) is free from here on: it becomes the P buffers.
-    __syncthreads();
-
-  unsigned char* Pw = sBP + wg * SM::kPw;
-  unsigned char* sX = sXall + wg * SM::kX;
-  float* sa2 = sAall + wg * 4 * L;  // a * log2(e)
-  float* sx = sa2 + L;              // fwd: a*log2e - log2(delta)  (+inf where delta = 0); rev: delta
-  float* sraw = sx + L;             // prefetched a [L], delta [L] of the next head
-  constexpr uint32_t id_py = idesc_bf16(128, kP, 0, 1);
-  constexpr uint32_t id_st = idesc_bf16(128, kP, 0, 0);
-
-  // cp.async of everything a head needs: its second-operand rows (sX), its
-  // inter-chunk state image (into the P buffer) and its raw a / delta.
-  auto prefetch = [&](int hh) {
-    for (int i = wtid; i < ncol * 8; i += 256) {
-      const int cc = i >> 3, j = i & 7, col = col0 + cc;
-      const bool v = col < Lv;
-      cp_async16(sX + sw128(cc, j),
-                 v ? opsrc + (((int64_t)b * T + t0 + col) * H + hh) * kP + j * 8 : opsrc, v);
-    }
-    const unsigned char* img = simg + ((((int64_t)b * nc + c) * H + hh) * (int64_t)SM::kImg);
-    for (int i = wtid; i < SM::kImg / 16; i += 256) cp_async16(Pw + 16 * i, img + 16 * i, true);
-    const int64_t cvh = (((int64_t)b * H + hh) * nc + c) * L;
-    for (int i = wtid; i < L / 4; i += 256) {
-      cp_async16(sraw + 4 * i, acs + cvh + 4 * i, true);
-      cp_async16(sraw + L + 4 * i, delta + cvh + 4 * i, true);
-    }
-  };
-  if (h_begin + wg < h_end) prefetch(h_begin + wg);
-  cp_async_commit();
-
-  for (int h = h_begin + wg; h < h_end; h += 2) {
-    const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
-    const float Dh = D ? D[h] : 0.f;
-    cp_async_wait<0>();
-    group_sync(gbar);  // the raw vectors were copied by other threads of the group
-    for (int i = wtid; i < L; i += 256) {
-      const float a2 = sraw[i] * kLog2e, dl = sraw[L + i];
-      sa2[i] = a2;
-      sx[i] = REV ? dl : (dl > 0.f ? a2 - lg2_approx(dl) : __int_as_float(0x7f800000));
-    }
-    fence_async_smem();
-    fence_before_sync();
-    group_sync(gbar);
-    if (wtid == 0) {
-      fence_after_sync();
-      for (int ks = 0; ks < N / 16; ++ks) {
-        const uint32_t kp = ks / 4, ko = (ks % 4) * 32;
-        const uint64_t ad = sdesc(smem_u32(sR) + kp * (LT * 128) + ko, 16, 1024);
-        mma_bf16(tm + colST, ad, sdesc(smem_u32(Pw) + kp * (64 * 128) + ko, 16, 1024), id_st,
-                 ks > 0 ? 1u : 0u);
-        mma_bf16(tm + colST, ad, sdesc(smem_u32(Pw) + SM::kHlo + kp * (64 * 128) + ko, 16, 1024),
-                 id_st, 1u);
-      }
-      mma_commit(&bar_st[wg]);
-    }
-    // Forward: column factors for column groups strictly inside the causal
-    // triangle, e^{a_l - a_s} delta_s = R_l * cf_s with the group's last column
-    // m as reference: cf_s = 2^{a_m - a_s} delta_s, R_l = 2^{a_l - a_m}; a is
-    // monotone, so both are <= 1.  (The dx direction keeps the per-element
-    // exponential: measured faster there.)
-    if constexpr (!REV) {
-      for (int i = wtid; i < L; i += 256) scf[i] = ex2_approx(sa2[i | 15] - sx[i]);
-      group_sync(gbar);
-    }
-    ++n_st;
-    mbar_wait(&bar_st[wg], (n_st - 1) & 1, status, &abort_flag);  // P buffer free again
-    fence_after_sync();
-    const float ar2 = sa2[r];
-    for (int j = 0; j < nsp; ++j) {
-      if (j > 0) mbar_wait(&bar_p[wg], (n_p - 1) & 1, status, &abort_flag);
-      const float* colv = (REV ? sa2 : sx) + col0 + 64 * j;  // per-column log2 terms
-      // the thread's 32 columns as two 16-column groups; the second group's
-      // TMEM load is in flight while the first is formed
-      float cbA[16], cbB[16];
-      tmem_ld16(tlane + 64 * j + 32 * half, cbA);
-      tmem_wait_ld();
-#pragma unroll
-      for (int qg = 0; qg < 2; ++qg) {
-        float(&cur)[16] = qg ? cbB : cbA;
-        if (qg == 0) tmem_ld16(tlane + 64 * j + 32 * half + 16, cbB);
-        // the warp's 32 rows [rw, rw + 32) against 16 columns [cg, cg + 16):
-        // outside the causal triangle, strictly inside it, or across the diagonal
-        const int cg = col0 + 64 * j + 32 * half + 16 * qg, rw = r0 + 32 * q;
-        const bool outside = !REV && cg > rw + 31;
-        const bool inside = !REV && cg + 15 < rw;
-        if (outside) {
-#pragma unroll
-          for (int k8 = 0; k8 < 2; ++k8) {
-            const uint32_t off = sw128(rr, (32 * half + 16 * qg + 8 * k8) / 8);
-            *reinterpret_cast<uint4*>(Pw + off) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(Pw + LT * 128 + off) = make_uint4(0, 0, 0, 0);
-          }
-        } else if (inside) {
-          const int m = cg + 15;
-          const float R = ex2_approx(ar2 - sa2[m]);
-          const float2 R2 = make_float2(R, R);
-#pragma unroll
-          for (int k8 = 0; k8 < 2; ++k8) {
-            const int c8 = 32 * half + 16 * qg + 8 * k8;  // panel-local column of the chunk
-            const float4 c0 = *reinterpret_cast<const float4*>(scf + cg + 8 * k8);
-            const float4 c1 = *reinterpret_cast<const float4*>(scf + cg + 8 * k8 + 4);
-            const float* sv = cur + 8 * k8;
-            const float2 p0 = __fmul2_rn(__fmul2_rn(R2, make_float2(c0.x, c0.y)), make_float2(sv[0], sv[1]));
-            const float2 p1 = __fmul2_rn(__fmul2_rn(R2, make_float2(c0.z, c0.w)), make_float2(sv[2], sv[3]));
-            const float2 p2 = __fmul2_rn(__fmul2_rn(R2, make_float2(c1.x, c1.y)), make_float2(sv[4], sv[5]));
-            const float2 p3 = __fmul2_rn(__fmul2_rn(R2, make_float2(c1.z, c1.w)), make_float2(sv[6], sv[7]));
-            const float v[8] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y, p3.x, p3.y};
-            const uint32_t off = sw128(rr, c8 / 8);
-            store_split8(Pw + off, Pw + LT * 128 + off, v);
-          }
-        } else {
-#pragma unroll
-          for (int k8 = 0; k8 < 2; ++k8) {
-            const int c8 = 32 * half + 16 * qg + 8 * k8;  // panel-local column of the chunk
-            const float4 w0 = *reinterpret_cast<const float4*>(colv + c8);
-            const float4 w1 = *reinterpret_cast<const float4*>(colv + c8 + 4);
-            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            float v[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int cl = col0 + 64 * j + c8 + e;  // chunk-local column
-              const float f = REV ? ex2_approx(wv[e] - ar2) : ex2_approx(ar2 - wv[e]);
-              v[e] = (REV ? cl >= r : cl <= r) ? cur[8 * k8 + e] * f : 0.f;
-            }
-            const uint32_t off = sw128(rr, c8 / 8);
-            store_split8(Pw + off, Pw + LT * 128 + off, v);
-          }
-        }
-        if (qg == 0) tmem_wait_ld();
-      }
-      fence_async_smem();
-      fence_before_sync();
-      group_sync(gbar);
-      if (wtid == 0) {
-        fence_after_sync();
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bd = sdesc(smem_u32(sX) + (64 * j + 16 * ks) * 128, L * 128, 1024);
-          mma_bf16(tm + colY, sdesc(smem_u32(Pw) + ks * 32, 16, 1024), bd, id_py,
-                   (j > 0 || ks > 0) ? 1u : 0u);
-          mma_bf16(tm + colY, sdesc(smem_u32(Pw) + LT * 128 + ks * 32, 16, 1024), bd, id_py, 1u);
-        }
-        mma_commit(&bar_p[wg]);
-        if (j == nsp - 1) mma_commit(&bar_done[wg]);  // one phase per head
-      }
-      ++n_p;
-    }
-    // this thread's 32 columns of its row of the second operand (x or dy) and,
-    // rev, of x: loaded now, so the latency overlaps the last MMAs
-    const int64_t rowoff = (((int64_t)b * T + t0 + r) * H + h) * kP;
-    const bool live = r < Lv;
-    uint4 orow[4], xrow[4];
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      orow[kk] = live ? *reinterpret_cast<const uint4*>(opsrc + rowoff + 32 * half + 8 * kk)
-                      : make_uint4(0, 0, 0, 0);
-      if constexpr (REV)
-        xrow[kk] = live ? *reinterpret_cast<const uint4*>(x + rowoff + 32 * half + 8 * kk)
-                        : make_uint4(0, 0, 0, 0);
-    }
-    ++n_done;
-    const bool ok = mbar_wait(&bar_done[wg], (n_done - 1) & 1, status, &abort_flag);
-    fence_after_sync();
-    // this head's MMAs are done: sX and the P buffer take the next head's data
-    if (h + 2 < h_end) prefetch(h + 2);
-    cp_async_commit();
-    float pd = 0.f, pq = 0.f, pdd = 0.f;  // rev: partial <x, u>, <x, state part>, <x, dy>
-    if (ok) {
-      const float ea = ex2_approx(ar2), es = ex2_approx(sa2[L - 1] - ar2);
-      const float dr = REV ? sx[r] : 0.f;
-#pragma unroll
-      for (int c16 = 0; c16 < 2; ++c16) {
-        float yv[16], st[16];
-        tmem_ld16(tlane + colY + 32 * half + 16 * c16, yv);
-        tmem_ld16(tlane + colST + 32 * half + 16 * c16, st);
-        tmem_wait_ld();
-        if (live) {
-#pragma unroll
-          for (int k8 = 0; k8 < 2; ++k8) {
-            float ov[8], o[8];
-            unpack8(orow[2 * c16 + k8], ov);
-            if constexpr (!REV) {
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                o[e] = yv[8 * k8 + e] + ea * st[8 * k8 + e] + Dh * ov[e];
-            } else {
-              float xv[8];
-              unpack8(xrow[2 * c16 + k8], xv);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float us = es * st[8 * k8 + e];
-                const float u = yv[8 * k8 + e] + us;
-                o[e] = fmaf(dr, u, Dh * ov[e]);
-                pd = fmaf(xv[e], u, pd);
-                pq = fmaf(xv[e], us, pq);
-                pdd = fmaf(xv[e], ov[e], pdd);
-              }
-            }
-            Tout* op = out + rowoff + 32 * half + 16 * c16 + 8 * k8;
-            if constexpr (sizeof(Tout) == 4) {
-              float* of = reinterpret_cast<float*>(op);
-              *reinterpret_cast<float4*>(of) = make_float4(o[0], o[1], o[2], o[3]);
-              *reinterpret_cast<float4*>(of + 4) = make_float4(o[4], o[5], o[6], o[7]);
-            } else {
-              *reinterpret_cast<uint4*>(op) =
-                  make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
-                             pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
-            }
-          }
-        }
-      }
-    }
-    if constexpr (REV) {
-      // combine the two half-rows (pipeline-local barrier)
-      if (half == 1) {
-        sred[rr] = pd;
-        sred[128 + rr] = pq;
-        sred[256 + rr] = pdd;
-      }
-      group_sync(gbar);
-      if (half == 0 && r < Lv) {
-        ddir[cv + r] = pd + sred[rr];
-        qrow[cv + r] = sx[r] * (pq + sred[128 + rr]);
-        ddiag[cv + r] = pdd + sred[256 + rr];
-      }
-    }
-    fence_before_sync();
-    group_sync(gbar);  // sX, sa, sd and the accumulators are reused by the next head
-  }
-    // both groups are done with this unit's C.B^T tile and buffers
-    fence_before_sync();
-    __syncthreads();
-  }
-  fence_before_sync();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tm, 512);
-}
-
-// ================================================================ dB and dC
-// grid (nc, B, L/128 * G * nblk), 288 threads.  CTA = a 128-row tile of chunk
-// c and one block of hb consecutive heads of group g (blockIdx.z = (tile order)
-// * G * nblk + g * nblk + k);
-// its accumulator sums the block's heads, so out holds one partial per block.
-// REV = false -> dC (rows l, columns s in [0, l0 + 128)):
-//   per head and 64-column panel: S1 = dy_l . x_s (K = P),
-//     P2[l,s] = e^{a_l - a_s} delta_s S1 [s <= l];  ACC += P2 . B  (K = s)
-//   then ACC += (e^{a_l} dy_l) . H_c (K = p)
-// REV = true -> dB (rows s, columns l in [s0, L)):
-//   S1 = x_s . dy_l,  P2[s,l] = e^{a_l - a_s} delta_s S1 [l >= s];  ACC += P2 . C
-//   then ACC += (delta_s e^{a_last - a_s} x_s) . dS_c (K = p)
-// The ddA terms come from the accumulator itself.  Each head accumulates
-// into its own TMEM region HD (started from zero), folded into the block's
-// total TOT by the conversion threads.  With R the tile's row operand of the
-// contraction HD feeds (C_l for dC, B_s for dB), x1 = R_r . HD_r after the
-// head's panels and x2 = R_r . HD_r after its state term:
-//   msum_r = x1 - P2[r,r] (R_r . G_r)   (strict row / column sum of
-//            M[l,s] = C_l.B_s e^{a_l - a_s} delta_s <dy_l, x_s>; G = the other operand)
-//   ycs_l  = x2 - x1 = e^{a_l} <dy_l, C_l . H_c^T>                  (dC only)
-// so no C.B^T or C.H^T product is formed.
-//
-// Warps 0-7 form P2 (rows split over the four TMEM lane quarters, columns
-// over two groups); warp 8 issues every MMA.  S1 panels alternate between two
-// TMEM buffers and P2 panels between two shared-memory buffers, handed over
-// with full / empty mbarriers, so the tensor core forms panel k+1 and
-// accumulates panel k-1 while panel k is converted.
-template <int N, int L>
-struct BcSmem {
-  static constexpr int kLT = 128;
-  static constexpr int kGR = (N / 64) * kLT * 128;
-  static constexpr int kGC = (N / 64) * L * 128;
-  static constexpr int kHR = kLT * 128;
-  static constexpr int kHC = L * 128;
-  static constexpr int kPB = 2 * kLT * 128;  // one P buffer: 64-column panel, hi + lo
-  static constexpr int kBytes = kGR + kGC + kHR + kHC + 2 * kPB + (5 * L + 8 * 128) * 4 + 1024;
-  static_assert(2 * (N / 64) * 8192 <= kPB, "state image fits one P buffer");
-};
-
-constexpr int kBcEpiWarps = 8;                 // conversion warps: 4 lane quarters x 2 column groups
-constexpr int kBcGroups = kBcEpiWarps / 4;      // column groups (1, 2 or 4)
-constexpr int kBcEpi = 32 * kBcEpiWarps;        // conversion threads
-constexpr int kBcThreads = kBcEpi + 32;         // + the MMA warp
-
-// rows [0, rows) of 8*nchunk bf16 into 128-byte-swizzle panels by the
-// conversion threads (t in [0, kBcEpi)); rows >= valid are zero-filled.
-template <class RowPtr>
-__device__ __forceinline__ void stage_rows_epi(unsigned char* dst, int rows, int nchunk,
-                                               uint32_t panel, int valid, const bf16* safe,
-                                               RowPtr rowptr, int t) {
-  for (int i = t; i < rows * nchunk; i += kBcEpi) {
-    const int r = i / nchunk, j = i % nchunk;
-    const bool v = r < valid;
-    cp_async16(dst + (j / 8) * panel + sw128(r, j % 8), v ? rowptr(r) + j * 8 : safe, v);
-  }
-}
-
-__device__ __forceinline__ void epi_sync() {  // the conversion threads
-  asm volatile("bar.sync 1, %0;" ::"n"(kBcEpi) : "memory");
-}
-
-template <int N, int L, bool REV>
-__global__ void __launch_bounds__(kBcThreads, 1)
-    k_bwd_bc_tc(const bf16* __restrict__ x, const bf16* __restrict__ Bm,
-                const bf16* __restrict__ Cm, const bf16* __restrict__ dy,
-                const float* __restrict__ delta, const float* __restrict__ acs,
-                const unsigned char* __restrict__ simg, float* __restrict__ out,
-                float* __restrict__ msum, float* __restrict__ ycs, int T, int H, int G, int nc,
-                int hb, int* status) {
-  using SM = BcSmem<N, L>;
-  constexpr int LT = SM::kLT, NLT = L / LT, NKP = N / 64;
-  constexpr uint32_t kColAcc = 128, kColTot = 256;  // HD, TOT; S1 buffers at columns 0 and 64
-  extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t bar_sfull[2], bar_sempty[2], bar_pfull[2], bar_pempty[2];
-  __shared__ uint64_t bar_ops, bar_stready, bar_sdone;
-  __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag;
-  unsigned char* base = align1024(smem_raw);
-  unsigned char* sGR = base;
-  unsigned char* sGC = sGR + SM::kGR;
-  unsigned char* sHR = sGC + SM::kGC;
-  unsigned char* sHC = sHR + SM::kHR;
-  unsigned char* sP = sHC + SM::kHC;  // P buffers 0 and 1
-  float* sa2 = reinterpret_cast<float*>(sP + 2 * SM::kPB);  // a * log2(e)
-  float* sx = sa2 + L;   // dC: a*log2e - log2(delta) (+inf at delta = 0); dB: log2(delta) (-inf)
-  float* sred = sx + L;  // [2][4][128]: per column group (up to 4), msum and ycs partials
-  float* sraw = sred + 8 * 128;  // prefetched a [L], delta [L] of the next head
-  float* scf = sraw + 2 * L;     // column factors of the decay against 16-column group edges
-
-  // row tiles with the most columns (dC: the last, dB: the first) are launched first
-  const int gz = gridDim.z / NLT, zt = blockIdx.z / gz, zr = blockIdx.z % gz;
-  const int c = blockIdx.x, b = blockIdx.y, tile = REV ? zt : NLT - 1 - zt;
-  const int nblk = gz / G, g = zr / nblk, kb = zr % nblk;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h_begin = g * (H / G) + kb * hb, h_end = h_begin + hb;
-  const int r0 = tile * LT, col0 = REV ? r0 : 0, ncol = REV ? L - r0 : r0 + LT;
-  const int npan = ncol / 64;
-  const int64_t t0 = (int64_t)c * L;
-  const int Lv = min(L, T - (int)t0);
-  const bf16* grow = REV ? Bm : Cm;
-  const bf16* gcol = REV ? Cm : Bm;
-  const bf16* hrow = REV ? x : dy;
-  const bf16* hcol = REV ? dy : x;
-
-  if (tid == 0) {
-    abort_flag = 0;
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_sfull[i], 1);
-      mbar_init(&bar_sempty[i], kBcEpiWarps);
-      mbar_init(&bar_pfull[i], kBcEpiWarps);
-      mbar_init(&bar_pempty[i], 1);
-    }
-    mbar_init(&bar_ops, kBcEpi);
-    mbar_init(&bar_stready, kBcEpi);
-    mbar_init(&bar_sdone, 1);
-    fence_mbar_init();
-  }
-  if (warp == 0) tmem_alloc(&tmem_base, 512);
-  fence_before_sync();
-  __syncthreads();
-  fence_after_sync();
-  const uint32_t tm = tmem_base;
-  constexpr uint32_t id_s = idesc_bf16(128, 64, 0, 0);
-  constexpr uint32_t id_acc = idesc_bf16(128, N, 0, 1);
-
-  if (warp == kBcEpiWarps) {
-    // ------------------------------------------------------------ MMA warp
-    const uint32_t leader = elect_one();
-    const uint64_t dHR = sdesc(smem_u32(sHR), 16, 1024), dHC = sdesc(smem_u32(sHC), 16, 1024);
-    const uint64_t dGC = sdesc(smem_u32(sGC), L * 128, 1024), dP = sdesc(smem_u32(sP), 16, 1024);
-    const uint64_t dIm0 = sdesc(smem_u32(sP), 64 * 128, 1024);
-    constexpr uint32_t kLo = NKP * 64 * 128;  // lo panels of the state image
-    uint32_t ph_se = 0, ph_pf = 0;  // per-buffer parity bits of the next wait
-    uint32_t n_head = 0, gp = 0;
-    auto issue_s1 = [&](int j, uint32_t bs) {
-      mbar_wait(&bar_sempty[bs], ((ph_se >> bs) & 1u) ^ 1u, status, &abort_flag);
-      ph_se ^= 1u << bs;
-      fence_after_sync();
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16_if(tm + 64 * bs, desc_add(dHR, ks * 32), desc_add(dHC, j * 64 * 128 + ks * 32),
-                    id_s, ks > 0 ? 1u : 0u, leader);
-      mma_commit_if(&bar_sfull[bs], leader);
-    };
-    for (int h = h_begin; h < h_end; ++h, ++n_head) {
-      mbar_wait(&bar_ops, n_head & 1u, status, &abort_flag);  // HR, HC of this head staged
-      fence_after_sync();
-      issue_s1(0, gp & 1u);
-      for (int j = 0; j < npan; ++j) {
-        const uint32_t bs = (gp + j) & 1u;
-        if (j + 1 < npan) issue_s1(j + 1, bs ^ 1u);
-        mbar_wait(&bar_pfull[bs], (ph_pf >> bs) & 1u, status, &abort_flag);
-        ph_pf ^= 1u << bs;
-        fence_after_sync();
-        const uint64_t dp = desc_add(dP, bs * SM::kPB);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bd = desc_add(dGC, (j * 64 + ks * 16) * 128);
-          mma_bf16_if(tm + kColAcc, desc_add(dp, ks * 32), bd, id_acc, (j > 0 || ks > 0) ? 1u : 0u,
-                      leader);
-          mma_bf16_if(tm + kColAcc, desc_add(dp, LT * 128 + ks * 32), bd, id_acc, 1u, leader);
-        }
-        mma_commit_if(&bar_pempty[bs], leader);
-      }
-      gp += npan;
-      // state term: A operand (hi / lo) in the last panel's P buffer, the state
-      // image in the other one
-      mbar_wait(&bar_stready, n_head & 1u, status, &abort_flag);
-      fence_after_sync();
-      const uint32_t pl = (gp - 1) & 1u;
-      const uint64_t dA = desc_add(dP, pl * SM::kPB), dIm = desc_add(dIm0, (pl ^ 1u) * SM::kPB);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        const uint64_t ah = desc_add(dA, ks * 32), al = desc_add(dA, LT * 128 + ks * 32);
-        const uint64_t bh = desc_add(dIm, ks * 2048), bl = desc_add(dIm, kLo + ks * 2048);
-        mma_bf16_if(tm + kColAcc, ah, bh, id_acc, 1u, leader);
-        mma_bf16_if(tm + kColAcc, ah, bl, id_acc, 1u, leader);
-        mma_bf16_if(tm + kColAcc, al, bh, id_acc, 1u, leader);
-      }
-      mma_commit_if(&bar_sdone, leader);
-    }
-  } else {
-    // ----------------------------------------------------- conversion warps
-    constexpr int NC = N / kBcGroups;   // accumulator columns of one column group
-    constexpr int PC = 64 / kBcGroups;  // columns of a 64-column panel per thread
-    const int q = warp & 3, cq = warp >> 2;
-    const int rr = 32 * q + lane, r = r0 + rr;
-    const uint32_t tlane = tm + ((uint32_t)(32 * q) << 16);
-    auto stage_hr = [&](int hh) {
-      stage_rows_epi(sHR, LT, 8, 0, Lv - r0, hrow, [&](int r2) {
-        return hrow + (((int64_t)b * T + t0 + r0 + r2) * H + hh) * kP;
-      }, tid);
-    };
-    auto stage_hc = [&](int hh) {
-      stage_rows_epi(sHC, ncol, 8, 0, Lv - col0, hcol, [&](int cc) {
-        return hcol + (((int64_t)b * T + t0 + col0 + cc) * H + hh) * kP;
-      }, tid);
-      const int64_t cvh = (((int64_t)b * H + hh) * nc + c) * L;
-      for (int i = tid; i < L / 4; i += kBcEpi) {
-        cp_async16(sraw + 4 * i, acs + cvh + 4 * i, true);
-        cp_async16(sraw + L + 4 * i, delta + cvh + 4 * i, true);
-      }
-    };
-    stage_rows_epi(sGR, LT, N / 8, LT * 128, Lv - r0, grow, [&](int rr2) {
-      return grow + (((int64_t)b * T + t0 + r0 + rr2) * G + g) * N;
-    }, tid);
-    stage_rows_epi(sGC, ncol, N / 8, L * 128, Lv - col0, gcol, [&](int cc) {
-      return gcol + (((int64_t)b * T + t0 + col0 + cc) * G + g) * N;
-    }, tid);
-    stage_hc(h_begin);
-    stage_hr(h_begin);
-    cp_async_commit();
-
-    // R_r . HD_r over this thread's column group; fold != 0 also adds HD into
-    // TOT (first == true: TOT = HD)
-    auto acc_dot = [&](bool fold, bool first) {
-      float s = 0.f;
-#pragma unroll
-      for (int c0 = 0; c0 < NC; c0 += 16) {
-        float v[16];
-        const uint32_t col = cq * NC + c0;
-        tmem_ld16(tlane + kColAcc + col, v);
-        tmem_wait_ld();
-        if (fold) {
-          float t[16];
-          if (!first) {
-            tmem_ld16(tlane + kColTot + col, t);
-            tmem_wait_ld();
-          }
-#pragma unroll
-          for (int e = 0; e < 16; ++e) t[e] = first ? v[e] : t[e] + v[e];
-          tmem_st16(tlane + kColTot + col, t);
-        }
-#pragma unroll
-        for (int k8 = 0; k8 < 2; ++k8) {
-          const int cc = cq * NC + c0 + 8 * k8;  // first of 8 columns
-          float rv[8];
-          unpack8(*reinterpret_cast<const uint4*>(sGR + (cc / 64) * (LT * 128) +
-                                                  sw128(rr, (cc % 64) / 8)), rv);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) s = fmaf(rv[e], v[8 * k8 + e], s);
-        }
-      }
-      if (fold) tmem_wait_st();
-      return s;
-    };
-
-    // per-buffer parity bits: S1 full waits, and the number of panels written
-    // into each P buffer (mod 2); CTA-uniform
-    uint32_t ph_sf = 0, ph_pe = 0, n_head = 0, gp = 0;
-    float cbdot = 0.f;  // R_r . G_r (the diagonal's M factor)
-    // The end of a head (its state term's x2, the TOT fold, msum / ycs) runs
-    // once the next head's operands are staged, so the state-term MMAs overlap
-    // the next head's start.  The pending head's values:
-    int64_t pv_cv = 0;
-    float pv_x1 = 0.f, pv_pdiag = 0.f;
-    auto finish_head = [&](uint32_t nh, bool first) {
-      // warp-uniform: the TMEM accesses below are warp-collective
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_sdone, nh & 1u, status, &abort_flag));
-      fence_after_sync();
-      const float x2 = ok ? acc_dot(true, first) : pv_x1;
-      const float mpart = pv_x1 - pv_pdiag * cbdot;
-      const float ypart = x2 - pv_x1;
-      sred[cq * 128 + rr] = mpart;
-      sred[512 + cq * 128 + rr] = ypart;
-      epi_sync();
-      if (cq == 0 && r < Lv) {
-        float ms = 0.f, ys = 0.f;
-#pragma unroll
-        for (int k = 0; k < kBcGroups; ++k) {
-          ms += sred[k * 128 + rr];
-          ys += sred[512 + k * 128 + rr];
-        }
-        msum[pv_cv + r] = ms;
-        if constexpr (!REV) ycs[pv_cv + r] = ys;
-      }
-      epi_sync();  // sred reused
-    };
-    {
-      // R_r . G_r once per CTA (the tile rows and column rows are staged first)
-      cp_async_wait<0>();
-      epi_sync();
-      const int rc = r - col0;  // the row of the column operand at the diagonal
-      float sdot = 0.f;
-#pragma unroll 2
-      for (int cc = 0; cc < N; cc += 8) {
-        float u[8], w[8];
-        unpack8(*reinterpret_cast<const uint4*>(sGR + (cc / 64) * (LT * 128) +
-                                                sw128(rr, (cc % 64) / 8)), u);
-        unpack8(*reinterpret_cast<const uint4*>(sGC + (cc / 64) * (L * 128) +
-                                                sw128(rc, (cc % 64) / 8)), w);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sdot = fmaf(u[e], w[e], sdot);
-      }
-      cbdot = sdot;
-    }
-    for (int h = h_begin; h < h_end; ++h, ++n_head) {
-      const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
-      cp_async_wait<0>();  // HR, HC and a / delta of this head
-      epi_sync();
-      for (int i = tid; i < L; i += kBcEpi) {
-        const float a2 = sraw[i] * kLog2e, dl = sraw[L + i];
-        const float l2 = dl > 0.f ? lg2_approx(dl) : -__int_as_float(0x7f800000);
-        sa2[i] = a2;
-        sx[i] = REV ? l2 : a2 - l2;
-      }
-      fence_async_smem();
-      mbar_arrive(&bar_ops);  // this thread's staged operands are visible to the MMAs
-      epi_sync();             // sa2 / sx complete
-      // Column factors for column groups strictly inside the causal triangle:
-      // e^{a_l - a_s} delta_s = R_row * cf_col with the group's edge column m
-      // between the rows and the columns (dC: m = last column, cf_s =
-      // 2^{a_m - a_s} delta_s, R_l = 2^{a_l - a_m}; dB: m = first column, cf_l =
-      // 2^{a_l - a_m}, R_s = 2^{a_m - a_s} delta_s).  a is monotone, so every
-      // factor is <= 1 (or <= delta) and neither can overflow.
-      for (int i = tid; i < L; i += kBcEpi)
-        scf[i] = REV ? ex2_approx(sa2[i] - sa2[i & ~15]) : ex2_approx(sa2[i | 15] - sx[i]);
-      epi_sync();
-      // the previous head's end, before this head's first P2 reaches a buffer
-      // its state term reads and before this head's first accumulate restarts HD
-      if (h > h_begin) finish_head(n_head - 1, h - 1 == h_begin);
-      const float arow = REV ? sa2[r] - sx[r] : sa2[r];
-      float pdiag = 0.f;  // P2 at the diagonal (this thread's row), if its columns hold it
-      for (int j = 0; j < npan; ++j) {
-        const uint32_t bs = (gp + j) & 1u;
-        mbar_wait(&bar_sfull[bs], (ph_sf >> bs) & 1u, status, &abort_flag);
-        ph_sf ^= 1u << bs;
-        fence_after_sync();
-        if (j == npan - 1 && h + 1 < h_end) {
-          stage_hc(h + 1);  // the head's last S1 product is done with the column operand
-          cp_async_commit();
-        }
-
-        // P buffer bs: the accumulate of its previous panel must be done with it
-        mbar_wait(&bar_pempty[bs], ((ph_pe >> bs) & 1u) ^ 1u, status, &abort_flag);
-        ph_pe ^= 1u << bs;
-        unsigned char* pb = sP + bs * SM::kPB;
-#pragma unroll
-        for (int qg = 0; qg < PC / 16; ++qg) {
-          // the warp's 32 rows [rw, rw + 32) against 16 columns [cg, cg + 16):
-          // outside the causal triangle, strictly inside it, or across the diagonal
-          const int cg = col0 + 64 * j + PC * cq + 16 * qg, rw = r0 + 32 * q;
-          const bool outside = REV ? cg + 15 < rw : cg > rw + 31;
-          const bool inside = REV ? cg > rw + 31 : cg + 15 < rw;
-          // this group's 16 columns of S1 (the buffer is released after the last)
-          float s1[16];
-          tmem_ld16(tlane + 64 * bs + PC * cq + 16 * qg, s1);
-          tmem_wait_ld();
-          if (qg == PC / 16 - 1) {
-            fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_sempty[bs]);
-          }
-          if (outside) {
-#pragma unroll
-            for (int k8 = 0; k8 < 2; ++k8) {
-              const uint32_t off = sw128(rr, (PC * cq + 16 * qg + 8 * k8) / 8);
-              *reinterpret_cast<uint4*>(pb + off) = make_uint4(0, 0, 0, 0);
-              *reinterpret_cast<uint4*>(pb + LT * 128 + off) = make_uint4(0, 0, 0, 0);
-            }
-          } else if (inside) {
-            // factorized decay: one ex2 per thread and group
-            const int m = REV ? cg : cg + 15;
-            const float R = REV ? ex2_approx(sa2[m] - arow) : ex2_approx(arow - sa2[m]);
-            const float2 R2 = make_float2(R, R);
-#pragma unroll
-            for (int k8 = 0; k8 < 2; ++k8) {
-              const int cb = PC * cq + 16 * qg + 8 * k8;  // column within the panel
-              const float4 c0 = *reinterpret_cast<const float4*>(scf + cg + 8 * k8);
-              const float4 c1 = *reinterpret_cast<const float4*>(scf + cg + 8 * k8 + 4);
-              const float* sv = s1 + 8 * k8;
-              const float2 p0 = __fmul2_rn(__fmul2_rn(R2, make_float2(c0.x, c0.y)), make_float2(sv[0], sv[1]));
-              const float2 p1 = __fmul2_rn(__fmul2_rn(R2, make_float2(c0.z, c0.w)), make_float2(sv[2], sv[3]));
-              const float2 p2 = __fmul2_rn(__fmul2_rn(R2, make_float2(c1.x, c1.y)), make_float2(sv[4], sv[5]));
-              const float2 p3 = __fmul2_rn(__fmul2_rn(R2, make_float2(c1.z, c1.w)), make_float2(sv[6], sv[7]));
-              const float v[8] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y, p3.x, p3.y};
-              const uint32_t off = sw128(rr, cb / 8);
-              store_split8(pb + off, pb + LT * 128 + off, v);
-            }
-          } else {
-#pragma unroll
-            for (int k8 = 0; k8 < 2; ++k8) {
-              const int cb = PC * cq + 16 * qg + 8 * k8;  // column within the panel
-              const uint32_t off = sw128(rr, cb / 8);
-              const float* colv = (REV ? sa2 : sx) + col0 + 64 * j + cb;
-              const float4 w0 = *reinterpret_cast<const float4*>(colv);
-              const float4 w1 = *reinterpret_cast<const float4*>(colv + 4);
-              const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-              float v[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float f = REV ? ex2_approx(wv[e] - arow) : ex2_approx(arow - wv[e]);
-                const int cl = col0 + 64 * j + cb + e;  // chunk-local column
-                v[e] = f * s1[8 * k8 + e];
-                if (cl == r) pdiag = v[e];
-                if (REV ? cl < r : cl > r) v[e] = 0.f;
-              }
-              store_split8(pb + off, pb + LT * 128 + off, v);
-            }
-          }
-        }
-        fence_async_smem();
-        fence_before_sync();  // HD reads of the previous head precede its next accumulate
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_pfull[bs]);
-      }
-      gp += npan;
-      // state term operands: the head's state image (hi / lo panels) goes to the
-      // second-to-last panel's buffer as soon as its accumulate is done, the A
-      // operand to the last panel's buffer
-      const uint32_t pl = (gp - 1) & 1u, po = pl ^ 1u;
-      mbar_wait(&bar_pempty[po], ((ph_pe >> po) & 1u) ^ 1u, status, &abort_flag);
-      {
-        const unsigned char* img =
-            simg + ((((int64_t)b * nc + c) * H + h) * (int64_t)(2 * NKP * 8192));
-        unsigned char* dst = sP + po * SM::kPB;
-        for (int i = tid; i < 2 * NKP * 8192 / 16; i += kBcEpi)
-          cp_async16(dst + 16 * i, img + 16 * i, true);
-        cp_async_commit();
-      }
-      // every accumulate of the head done (a commit covers all earlier MMAs)
-      mbar_wait(&bar_pempty[pl], ((ph_pe >> pl) & 1u) ^ 1u, status, &abort_flag);
-      fence_after_sync();
-      const float x1 = acc_dot(false, false);
-      unsigned char* sAh = sP + pl * SM::kPB;  // state A operand hi / lo (128 x 64)
-      unsigned char* sAl = sAh + LT * 128;
-      for (int i = tid; i < LT * 8; i += kBcEpi) {
-        const int r2 = i >> 3, jj = i & 7, row = r0 + r2;
-        float v[8];
-        unpack8(*reinterpret_cast<const uint4*>(sHR + sw128(r2, jj)), v);
-        const float sc = REV ? ex2_approx(sa2[L - 1] - sa2[row] + sx[row]) : ex2_approx(sa2[row]);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] *= sc;
-        store_split8(sAh + sw128(r2, jj), sAl + sw128(r2, jj), v);
-      }
-      cp_async_wait<0>();  // the state image (and the next head's column operand)
-      fence_async_smem();
-      fence_before_sync();  // the HD reads above precede the state term's accumulate
-      mbar_arrive(&bar_stready);
-      epi_sync();  // every thread is done with the row operand
-      if (h + 1 < h_end) {
-        stage_hr(h + 1);
-        cp_async_commit();
-      }
-      pv_cv = cv;
-      pv_x1 = x1;
-      pv_pdiag = pdiag;
-    }
-    if (hb > 0) finish_head(n_head - 1, hb == 1);
-    // the block's accumulated dB / dC rows
-    if (!abort_flag) {  // CTA-uniform: the TMEM loads below are warp-collective
-      float* o = out + (((((int64_t)b * T + t0 + r) * G + g) * nblk + kb) * N) + cq * NC;
-#pragma unroll
-      for (int c0 = 0; c0 < NC; c0 += 16) {
-        float v[16];
-        tmem_ld16(tlane + kColTot + cq * NC + c0, v);
-        tmem_wait_ld();
-        if (r < Lv) {
-#pragma unroll
-          for (int k4 = 0; k4 < 16; k4 += 4)
-            *reinterpret_cast<float4*>(o + c0 + k4) =
-                make_float4(v[k4], v[k4 + 1], v[k4 + 2], v[k4 + 3]);
-        }
-      }
-    }
-  }
-  fence_before_sync();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tm, 512);
-}
-
 // grid (nc, H, B).  Gradient w.r.t. dA_r = delta_r A from the strict row sums
 // (dC kernel) and column sums (dB kernel) of M:
 //   ddA_r = sum_{j<r} (colsum_j - rowsum_j) + sum_{l>=r} ycs_l + sum_{s<r} qrow_s + dlast_c
@@ -1293,16 +447,6 @@ __global__ void __launch_bounds__(NT)
 }
 
 // ------------------------------------------------------------------ launch
-// Persistent scan kernels: one CTA per SM, each taking a contiguous range of
-// the (batch, chunk, row tile, group) x head items, so every SM gets the same
-// number of heads (+-1) whatever the shape.
-void scan_partition(const Dims& d, int sms, int* grid, int* per) {
-  const int64_t items = (int64_t)d.B * d.nc * (d.L / 128) * d.H;
-  const int64_t g = items < sms ? items : sms;
-  *per = (int)((items + g - 1) / g);
-  *grid = (int)((items + *per - 1) / *per);
-}
-
 // chunk_cumsum (delta, a) and chunk_state (S) in one persistent launch.
 template <int N, int L>
 void launch_state_front(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s,
@@ -1339,20 +483,8 @@ cudaError_t launch_tc_forward_t(const Dims& d, const FwdArgs& a, const FwdWs& w,
                                 int* status, int sms) {
   launch_state_front<N, L>(d, a, w, s, status, sms);  // chunk_cumsum runs inside chunk_state
   simt_state_passing(d, a, w, s);
-  {
-    using SM = ScanSmem<N, L>;
-    auto kern = k_scan_tc<N, L, Tout, false>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
-    int grid, per;
-    scan_partition(d, sms, &grid, &per);
-    SSD_LAUNCH("k_scan_tc", s,
-               kern<<<grid, 512, SM::kBytes, s>>>(
-                   static_cast<const bf16*>(a.x), static_cast<const bf16*>(a.B),
-                   static_cast<const bf16*>(a.C), nullptr, w.delta, w.acs,
-                   static_cast<const unsigned char*>(w.Himg), a.D,
-                   static_cast<Tout*>(a.y), nullptr, nullptr, nullptr, d.B, d.T, d.H, d.G, d.nc,
-                   per, status));
-  }
+  const cudaError_t e = tc_chunk_forward(d, a, w, tc_bwd_nblk(d), s);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -1366,8 +498,6 @@ cudaError_t launch_tc_forward_nl(const Dims& d, const FwdArgs& a, const FwdWs& w
 template <int N, int L>
 cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs& w,
                                   cudaStream_t s, int* status, int sms) {
-  const bf16* x = static_cast<const bf16*>(a.f.x);
-  const bf16* Bm = static_cast<const bf16*>(a.f.B);
   const bf16* Cm = static_cast<const bf16*>(a.f.C);
   const bf16* dy = static_cast<const bf16*>(a.dy);
   FwdArgs f = a.f;
@@ -1378,37 +508,12 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
   launch_dstates<N, L>(d, dy, Cm, w.delta, w.acs, w.dHs, s, status, sms);
   const int nsplit = simt_state_passing_bwd(d, w.dHs, w.acs, nullptr, a.dfinal, nullptr, w.dlast,
                                             a.dinit, w.dSimg, w.Himg, w.seg, s);
-  {
-    using SM = ScanSmem<N, L>;
-    auto kern = k_scan_tc<N, L, float, true>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
-    int grid, per;
-    scan_partition(d, sms, &grid, &per);
-    SSD_LAUNCH("k_scan_tc_dx", s, kern<<<grid, 512, SM::kBytes, s>>>(
-        x, Bm, Cm, dy, w.delta, w.acs, static_cast<const unsigned char*>(w.dSimg), a.f.D, a.dx,
-        w.ddir, w.qrow, w.ddiag, d.B, d.T, d.H, d.G, d.nc, per, status));
-  }
-  const int nblk = tc_bwd_nblk(d), hb = (d.H / d.G) / nblk;
-  const dim3 bgrid(d.nc, d.B, (L / 128) * d.G * nblk);
+  const int nblk = tc_bwd_nblk(d);
   float* dCout = nblk == 1 ? a.dC : w.dCp;
   float* dBout = nblk == 1 ? a.dB : w.dBp;
   {
-    using SM = BcSmem<N, L>;
-    auto kern = k_bwd_bc_tc<N, L, false>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
-    SSD_LAUNCH("k_bwd_dc_tc", s, kern<<<bgrid, kBcThreads, SM::kBytes, s>>>(
-        x, Bm, Cm, dy, w.delta, w.acs, static_cast<const unsigned char*>(w.Himg), dCout,
-        w.rowsum, w.ycs, d.T, d.H, d.G, d.nc, hb,
-        status));
-  }
-  {
-    using SM = BcSmem<N, L>;
-    auto kern = k_bwd_bc_tc<N, L, true>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
-    SSD_LAUNCH("k_bwd_db_tc", s, kern<<<bgrid, kBcThreads, SM::kBytes, s>>>(
-        x, Bm, Cm, dy, w.delta, w.acs, static_cast<const unsigned char*>(w.dSimg), dBout,
-        w.colsum, nullptr, d.T, d.H, d.G, d.nc, hb,
-        status));
+    const cudaError_t e = tc_chunk_backward(d, a, w, nblk, dCout, dBout, s);
+    if (e != cudaSuccess) return e;
   }
   {
     const FinalizeArgs fa{static_cast<const bf16*>(a.f.dt), a.f.dt_bias, a.f.A, w.delta,

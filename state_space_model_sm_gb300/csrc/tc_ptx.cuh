@@ -164,6 +164,33 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Tiled tensor copy (TMA) of one box from global memory, described by a
+// tensor map in kernel-parameter space, into this CTA's shared memory at dst,
+// completing the box's bytes on bar.  Coordinates are element indices from
+// the innermost dimension out; the innermost one times the element size must
+// be a multiple of 16 bytes.  Rows outside the tensor are filled with zeros.
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int c0, int c1, int c2,
+                                            int c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_map(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// Waits for a phase like mbar_wait but ignores the abort flag: used at the
+// end of a kernel to let copies or products already in flight land before
+// the CTA releases its shared memory and TMEM.  Bounded by kWaitLimitNs.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity))
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+}
+
 // One lane of a converged warp: 1 in the elected lane, 0 in the others.
 __device__ __forceinline__ uint32_t elect_one() {
   uint32_t pred;
