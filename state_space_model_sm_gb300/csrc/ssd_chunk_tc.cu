@@ -21,9 +21,9 @@
 // P's base in FWD / DX and gives the ddA sums of DC / DB directly, element by
 // element, so no per-head accumulator is needed for them.
 //
-// Warp roles (320 threads): warps 0-7 convert (TMEM -> decay, mask, hi/lo
-// bf16 split -> shared memory, and the epilogues), warp 8 issues every
-// tcgen05.mma, warp 9 issues every copy (TMA tiles of x, dy, B, C through
+// Warp roles (576 threads): warps 0-15 convert (TMEM -> decay, mask, hi/lo
+// bf16 split -> shared memory, and the epilogues), warp 16 issues every
+// tcgen05.mma, warp 17 issues every copy (TMA tiles of x, dy, B, C through
 // tensor maps; bulk copies of the state images and the per-head a / delta
 // vectors).  Full / empty mbarriers hand each buffer over; every wait is
 // bounded and records SSD_ERR_TIMEOUT on expiry.
@@ -49,13 +49,21 @@ using bf16 = __nv_bfloat16;
 
 enum : int { kFwd = 0, kDx = 1, kDc = 2, kDb = 3 };
 
-constexpr int kConvWarps = 8;  // 4 TMEM lane quarters x 2 column halves
+constexpr int kConvWarps = 16;  // 4 TMEM lane quarters x 4 column groups
 constexpr int kConv = 32 * kConvWarps;
+// A thread owns 64 / kCG of a row's columns in every panel and epilogue.
+constexpr int kCG = kConvWarps / 4;
+constexpr int kPC = 64 / kCG;
+constexpr int kNG = kPC / 16;        // 16-column groups per thread
+constexpr int kCPT = kPC / 8;        // 16-byte bf16 chunks per thread
 constexpr int kMmaWarp = kConvWarps;
 constexpr int kProdWarp = kConvWarps + 1;
 constexpr int kChunkThreads = 32 * (kConvWarps + 2);
 
-// Shared memory carving (byte offsets from a 1024-aligned base).
+// Shared memory carving (byte offsets from a 1024-aligned base).  Only B
+// operands and the row operand live here: every A operand of the big
+// products (P, P2, the state terms' scaled rows) is written by the
+// conversion warps into tensor memory.
 template <int N, int L, int MODE>
 struct ChunkLayout {
   static constexpr bool kRev = MODE == kDx || MODE == kDb;
@@ -64,24 +72,22 @@ struct ChunkLayout {
   static constexpr int kNP = N / 64;              // 64-wide panels of a B / C row
   static constexpr int kRow = kNP * kLT * 128;    // the tile's row operand (C or B rows)
   static constexpr int kCol = kNP * L * 128;      // column operand rows (B or C), up to L
-  static constexpr int kPB = 2 * kLT * 128;       // one P buffer: a 64-column panel, hi + lo
   static constexpr int kHlo = kNP * 64 * 128;     // offset of a state image's lo panels
   static constexpr int kImg = 2 * kHlo;           // one state image
   static constexpr int kOps = L * 128;            // one head's x or dy rows (64 wide)
   static constexpr int kHR = kLT * 128;           // DC / DB: the tile's dy (x) rows
-  // FWD / DX: the P buffers take the column operand's place once C.B^T is formed
-  static constexpr int kColP = kS1 ? kCol : (kCol > 2 * kPB ? kCol : 2 * kPB);
   static constexpr int oRow = 0;
   static constexpr int oCol = oRow + kRow;
-  static constexpr int oP = kS1 ? oCol + kCol : oCol;
-  static constexpr int oOps = kS1 ? oP + 2 * kPB : oCol + kColP;  // FWD / DX: two stages
+  static constexpr int oOps = oCol + kCol;                          // FWD / DX: two stages
   static constexpr int oHR = oOps + (kS1 ? kOps : 2 * kOps);
-  static constexpr int oImg = oHR + (kS1 ? kHR : 0);               // FWD / DX only
-  static constexpr int oVec = oImg + (kS1 ? 0 : kImg);             // raw [2 stages][a, delta][L]
-  static constexpr int oDer = oVec + 4 * L * 4;                    // [3][a2, sx, cf][L]
-  static constexpr int oRed = oDer + 9 * L * 4;                    // [2][3][128] half-row sums
-  static constexpr int kBytes = oRed + 6 * 128 * 4 + 1024;
-  static_assert(kImg <= kPB, "a state image fits one P buffer");
+  static constexpr int oImg = oHR + (kS1 ? kHR : 0);
+  static constexpr int oVec = oImg + kImg;                         // raw [2 stages][a, delta][L]
+  // derived per-head arrays: FWD / DX keep three heads (a head's epilogue runs
+  // during the next one), DC / DB two
+  static constexpr int kNDer = kS1 ? 2 : 3;
+  static constexpr int oDer = oVec + 4 * L * 4;                    // [kNDer][a2, sx, cf][L]
+  static constexpr int oRed = oDer + kNDer * 3 * L * 4;            // [3][kCG][128] row partials
+  static constexpr int kBytes = oRed + 3 * kCG * 128 * 4 + 1024;
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -119,14 +125,15 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&v)[8]) {
   }
 }
 
-// 8 fp32 values -> one 16-byte chunk of bf16 hi parts and one of lo parts.
-__device__ __forceinline__ void store_split8(unsigned char* hi, unsigned char* lo,
-                                             const float* v) {
-  uint32_t h[4], l[4];
+// 16 fp32 values of this thread's row -> a 16-wide K group of a TMEM A operand:
+// hi = rn_bf16(v) packed in columns [col, col + 8), lo = rn_bf16(v - hi) in
+// [col + 8, col + 16).  Warp-collective.
+__device__ __forceinline__ void tmem_store_split16(uint32_t col, const float (&v)[16]) {
+  uint32_t h[8], l[8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) split2_bf16(v[2 * i], v[2 * i + 1], h[i], l[i]);
-  *reinterpret_cast<uint4*>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
-  *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
+  for (int e = 0; e < 8; ++e) split2_bf16(v[2 * e], v[2 * e + 1], h[e], l[e]);
+  tmem_st8u(col, h);
+  tmem_st8u(col + 8, l);
 }
 
 // Arrive once per warp (lane 0) after the warp's own work.
@@ -143,18 +150,20 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   using LY = ChunkLayout<N, L, MODE>;
   constexpr bool REV = LY::kRev, S1M = LY::kS1;
   constexpr int LT = LY::kLT, NLT = L / LT, NP = LY::kNP;
-  constexpr uint32_t kColAcc = 256;  // FWD / DX: Y|ST pairs; DC / DB: S1 ring
-  constexpr uint32_t kColTot = 384;  // DC / DB: the block's dC / dB rows
+  // TMEM columns: C.B^T of the tile [0, 256); two 64-column operand slots
+  // (a 64-wide K panel as hi / lo bf16 per 16-wide group; in DC / DB first the
+  // fp32 S1 panel, converted in place); accumulators from 384: FWD Y per head
+  // parity, DX U and ST, DC / DB the block's dC / dB rows
+  constexpr uint32_t kColSlot = 256, kColAcc = 384;
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t bar_unit, bar_cb, bar_ops_full[2], bar_ops_empty[2], bar_vec_full[2],
-      bar_vec_empty[2], bar_img_full, bar_img_empty, bar_p_full[2], bar_p_empty[2],
-      bar_acc_full[2], bar_acc_empty[2], bar_tot, bar_final;
+      bar_vec_empty[2], bar_img_full, bar_img_empty, bar_slot_ready[2], bar_slot_full[2],
+      bar_slot_free[2], bar_acc_full[2], bar_acc_empty[2], bar_tot, bar_final;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   unsigned char* base = align1024(smem_raw);
   unsigned char* sRow = base + LY::oRow;
   unsigned char* sCol = base + LY::oCol;
-  unsigned char* sP = base + LY::oP;
   unsigned char* sOps = base + LY::oOps;
   unsigned char* sHR = base + LY::oHR;
   unsigned char* sImg = base + LY::oImg;
@@ -184,8 +193,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
       mbar_init(&bar_ops_empty[i], 1 + kConvWarps);
       mbar_init(&bar_vec_full[i], 1);
       mbar_init(&bar_vec_empty[i], kConvWarps);
-      mbar_init(&bar_p_full[i], kConvWarps);
-      mbar_init(&bar_p_empty[i], 1);
+      mbar_init(&bar_slot_ready[i], 1);
+      mbar_init(&bar_slot_full[i], kConvWarps);
+      mbar_init(&bar_slot_free[i], 1);
       mbar_init(&bar_acc_full[i], 1);
       mbar_init(&bar_acc_empty[i], kConvWarps);
     }
@@ -200,9 +210,10 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   __syncthreads();
   fence_after_sync();
   const uint32_t tm = tmem_base;
-  // uses of the two P buffers per head: the panels, then (DC / DB) the state
-  // image and the state term's A operand
-  const int upH = S1M ? npan + 2 : npan;
+  // slot uses per head: FWD / DX the P panels, then the state term's K panels;
+  // DC the S1 panels, the state term's A operand and the state dot C.H_c^T; DB
+  // the S1 panels and the state term's A operand
+  const int upH = S1M ? npan + (MODE == kDc ? 2 : 1) : npan + NP;
 
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer
@@ -254,33 +265,16 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         return true;
       };
       auto load_img = [&](int i) -> bool {
+        if (i >= 1 && !mbar_wait(&bar_img_empty, (i - 1) & 1, status, &abort_flag)) return false;
         const unsigned char* src = a.img + (((int64_t)b * nc + c) * H + h_begin + i) * LY::kImg;
-        if constexpr (!S1M) {
-          if (i >= 1 && !mbar_wait(&bar_img_empty, (i - 1) & 1, status, &abort_flag)) return false;
-          mbar_arrive_expect_tx(&bar_img_full, LY::kImg);
-          ++n_img;
-          bulk_g2s(sImg, src, LY::kImg, &bar_img_full);
-        } else {
-          // the buffer of panel npan - 2, free once its product is done: the MMA
-          // warp signals that on bar_img_empty, one phase per head (a parity wait
-          // on the buffer's own barrier could alias across the phases skipped here)
-          const int bi = (i * upH + npan) & 1;
-          if (!mbar_wait(&bar_img_empty, i & 1, status, &abort_flag)) return false;
-          mbar_arrive_expect_tx(&bar_img_full, LY::kImg);
-          ++n_img;
-          bulk_g2s(sP + bi * LY::kPB, src, LY::kImg, &bar_img_full);
-        }
+        mbar_arrive_expect_tx(&bar_img_full, LY::kImg);
+        ++n_img;
+        bulk_g2s(sImg, src, LY::kImg, &bar_img_full);
         return true;
       };
-      bool ok = hb > 0 && load_vec(0) && load_ops(0);
-      if constexpr (!S1M) ok = ok && load_img(0);
-      for (int i = 0; ok && i < hb; ++i) {
-        if (i + 1 < hb) {
-          ok = load_vec(i + 1) && load_ops(i + 1);
-          if constexpr (!S1M) ok = ok && load_img(i + 1);
-        }
-        if constexpr (S1M) ok = ok && load_img(i);
-      }
+      bool ok = hb > 0 && load_vec(0) && load_ops(0) && load_img(0);
+      for (int i = 0; ok && i + 1 < hb; ++i)
+        ok = load_vec(i + 1) && load_ops(i + 1) && load_img(i + 1);
       // copies still in flight (after an expired wait) land before the CTA exits
       mbar_drain(&bar_unit, 0);
       for (int v = 0; v < 2; ++v)
@@ -292,157 +286,194 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
+      // Shared-memory descriptors are formed once; each product adds a
+      // compile-time offset (the issuing thread would otherwise spend more
+      // cycles building descriptors than the tensor pipe spends per product).
+      const uint64_t dRowK = sdesc(smem_u32(sRow), 16, 1024);
+      const uint64_t dColK = sdesc(smem_u32(sCol), 16, 1024);
+      const uint64_t dColMN = sdesc(smem_u32(sCol), L * 128, 1024);
+      const uint64_t dOpsK = sdesc(smem_u32(sOps), 16, 1024);
+      const uint64_t dOpsMN = sdesc(smem_u32(sOps), L * 128, 1024);
+      const uint64_t dHRK = sdesc(smem_u32(sHR), 16, 1024);
+      const uint64_t dImgK = sdesc(smem_u32(sImg), 16, 1024);
+      const uint64_t dImgMN = sdesc(smem_u32(sImg), 64 * 128, 1024);
       bool ok = mbar_wait(&bar_unit, 0, status, &abort_flag);
       fence_after_sync();
       if (ok) {
         const uint32_t id_cb = idesc_bf16(128, ncol, 0, 0);
+#pragma unroll
         for (int ks = 0; ks < N / 16; ++ks) {
-          const uint32_t kp = ks / 4, ko = (ks % 4) * 32;
-          mma_bf16(tm, sdesc(smem_u32(sRow) + kp * (LT * 128) + ko, 16, 1024),
-                   sdesc(smem_u32(sCol) + kp * (L * 128) + ko, 16, 1024), id_cb, ks > 0 ? 1u : 0u);
+          constexpr int kR = LT * 128, kC = L * 128;
+          const uint32_t oa = (ks / 4) * kR + (ks % 4) * 32, ob = (ks / 4) * kC + (ks % 4) * 32;
+          mma_bf16(tm, desc_add(dRowK, oa), desc_add(dColK, ob), id_cb, ks > 0 ? 1u : 0u);
         }
         mma_commit(&bar_cb);
       }
-      uint32_t nfull[2] = {0, 0};  // conversion uses of each P buffer seen so far
-      auto wait_pfull = [&](int bb) -> bool {
-        const bool r = mbar_wait(&bar_p_full[bb], nfull[bb] & 1, status, &abort_flag);
-        ++nfull[bb];
-        fence_after_sync();
-        return r;
-      };
-      // the state product X . img^T into TMEM column col (K = d_state), hi and lo
-      // parts of the image: C.H_c^T (FWD, DC) or B.dS_c^T (DX)
-      auto state_dot = [&](uint32_t col, const unsigned char* img) {
-        constexpr uint32_t id_st = idesc_bf16(128, 64, 0, 0);
-        for (int ks = 0; ks < N / 16; ++ks) {
-          const uint32_t kp = ks / 4, ko = (ks % 4) * 32;
-          const uint64_t ad = sdesc(smem_u32(sRow) + kp * (LT * 128) + ko, 16, 1024);
-          mma_bf16(tm + col, ad, sdesc(smem_u32(img) + kp * (64 * 128) + ko, 16, 1024), id_st,
-                   ks > 0 ? 1u : 0u);
-          mma_bf16(tm + col, ad, sdesc(smem_u32(img) + LY::kHlo + kp * (64 * 128) + ko, 16, 1024),
-                   id_st, 1u);
+      constexpr uint32_t id_n64k = idesc_bf16(128, 64, 0, 0);   // B K-major, N = 64
+      constexpr uint32_t id_n64m = idesc_bf16(128, 64, 0, 1);   // B MN-major, N = 64
+      constexpr uint32_t id_nNm = idesc_bf16(128, N, 0, 1);     // B MN-major, N = d_state
+      // the state term's K panel kp with A in slot sc: B = image K-major (rows
+      // p), hi and lo parts, three products per K step (hi.hi, hi.lo, lo.hi)
+      auto state_panel = [&](uint32_t dcol, uint32_t sc, int kp, bool first) {
+        const uint64_t bk = desc_add(dImgK, kp * (64 * 128));
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t bh = desc_add(bk, ks * 32), bl = desc_add(bk, LY::kHlo + ks * 32);
+          mma_bf16_ta(tm + dcol, sc + 16 * ks, bh, id_n64k, (first && ks == 0) ? 0u : 1u);
+          mma_bf16_ta(tm + dcol, sc + 16 * ks, bl, id_n64k, 1u);
+          mma_bf16_ta(tm + dcol, sc + 16 * ks + 8, bh, id_n64k, 1u);
         }
       };
       if constexpr (!S1M) {
-        constexpr uint32_t id_py = idesc_bf16(128, 64, 0, 1);
+        uint32_t u = 0;  // slot uses
         for (int i = 0; ok && i < hb; ++i) {
-          const int st = i & 1, ac = i & 1;
-          const uint32_t colY = kColAcc + 128 * ac;
+          const int st = i & 1;
+          // FWD: Y per head parity; DX: U and ST, single
+          const uint32_t colY = MODE == kFwd ? kColAcc + 64 * st : kColAcc;
+          const uint32_t colS = MODE == kFwd ? colY : kColAcc + 64;
+          const int ab = MODE == kFwd ? st : 0;
+          const int na = MODE == kFwd ? (i >> 1) : i;  // earlier uses of this accumulator
           ok = mbar_wait(&bar_ops_full[st], (i >> 1) & 1, status, &abort_flag);
-          if (ok && i >= 2)
-            ok = mbar_wait(&bar_acc_empty[ac], ((i >> 1) - 1) & 1, status, &abort_flag);
-          if (ok) ok = mbar_wait(&bar_img_full, i & 1, status, &abort_flag);
+          if (ok && na >= 1)
+            ok = mbar_wait(&bar_acc_empty[ab], (na - 1) & 1, status, &abort_flag);
           if (!ok) break;
-          fence_after_sync();
-          state_dot(colY + 64, sImg);
-          mma_commit(&bar_img_empty);
-          for (int j = 0; j < npan; ++j) {
-            const int bb = (i * upH + j) & 1;
-            if (!wait_pfull(bb)) {
+          const uint64_t dops = desc_add(dOpsMN, st * LY::kOps);
+          for (int k = 0; k < upH; ++k, ++u) {
+            const int s = u & 1;
+            // the state image is needed from the first state panel on
+            if (k == npan && !mbar_wait(&bar_img_full, i & 1, status, &abort_flag)) {
               ok = false;
               break;
             }
-            const unsigned char* pb = sP + bb * LY::kPB;
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t bd =
-                  sdesc(smem_u32(sOps) + st * LY::kOps + (64 * j + 16 * ks) * 128, L * 128, 1024);
-              mma_bf16(tm + colY, sdesc(smem_u32(pb) + ks * 32, 16, 1024), bd, id_py,
-                       (j > 0 || ks > 0) ? 1u : 0u);
-              mma_bf16(tm + colY, sdesc(smem_u32(pb) + LT * 128 + ks * 32, 16, 1024), bd, id_py, 1u);
+            if (!mbar_wait(&bar_slot_full[s], (u >> 1) & 1, status, &abort_flag)) {
+              ok = false;
+              break;
             }
-            mma_commit(&bar_p_empty[bb]);
+            fence_after_sync();
+            const uint32_t sc = tm + kColSlot + 64 * s;
+            if (k < npan) {
+              const uint64_t bp = desc_add(dops, k * 64 * 128);
+              const uint32_t acc0 = k > 0 ? 1u : 0u;
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t bd = desc_add(bp, ks * 16 * 128);
+                mma_bf16_ta(tm + colY, sc + 16 * ks, bd, id_n64m, ks > 0 ? 1u : acc0);
+                mma_bf16_ta(tm + colY, sc + 16 * ks + 8, bd, id_n64m, 1u);
+              }
+              if (k == npan - 1) mma_commit(&bar_ops_empty[st]);  // x / dy rows read
+            } else {
+              state_panel(colS, sc, k - npan, MODE == kDx && k == npan);
+            }
+            mma_commit(&bar_slot_ready[s]);  // the slot may be written again
           }
           if (!ok) break;
-          mma_commit(&bar_ops_empty[st]);
-          mma_commit(&bar_acc_full[ac]);
+          mma_commit(&bar_img_empty);
+          mma_commit(&bar_acc_full[ab]);
         }
       } else {
-        constexpr uint32_t id_s1 = idesc_bf16(128, 64, 0, 0);
-        constexpr uint32_t id_acc = idesc_bf16(128, N, 0, 1);
-        uint32_t ru = 0;  // ring uses: S1 panels and (DC) the state dot
-        auto ring_take = [&]() -> int {
-          const int slot = ru & 1;
-          if (ru >= 2 && !mbar_wait(&bar_acc_empty[slot], ((ru >> 1) - 1) & 1, status, &abort_flag))
+        uint32_t pu = 0, cu = 0;  // slot uses produced (MMA side) and consumed
+        uint32_t acc_first = 0;   // 0 until TOT holds its first product
+        auto slot_take = [&]() -> int {  // the next slot, once its previous use is over
+          const int s = pu & 1;
+          if (pu >= 2 && !mbar_wait(&bar_slot_free[s], ((pu >> 1) - 1) & 1, status, &abort_flag))
             return -1;
-          ++ru;
+          ++pu;
           fence_after_sync();
-          return slot;
+          return s;
         };
-        auto issue_s1 = [&](int j) -> bool {
-          const int slot = ring_take();
-          if (slot < 0) return false;
+        auto slot_wait_full = [&]() -> int {
+          const int s = cu & 1;
+          if (!mbar_wait(&bar_slot_full[s], (cu >> 1) & 1, status, &abort_flag)) return -1;
+          ++cu;
+          fence_after_sync();
+          return s;
+        };
+        auto produce_s1 = [&](int j) -> bool {
+          const int s = slot_take();
+          if (s < 0) return false;
+          const uint64_t bp = desc_add(dOpsK, j * 64 * 128);
+#pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tm + kColAcc + 64 * slot, sdesc(smem_u32(sHR) + ks * 32, 16, 1024),
-                     sdesc(smem_u32(sOps) + j * 64 * 128 + ks * 32, 16, 1024), id_s1,
-                     ks > 0 ? 1u : 0u);
-          mma_commit(&bar_acc_full[slot]);
+            mma_bf16(tm + kColSlot + 64 * s, desc_add(dHRK, ks * 32), desc_add(bp, ks * 32),
+                     id_n64k, ks > 0 ? 1u : 0u);
+          mma_commit(&bar_slot_ready[s]);
           return true;
         };
-        bool first = true;
-        auto accumulate = [&](int u, int j) -> bool {
-          const int bb = u & 1;
-          if (!wait_pfull(bb)) return false;
-          const unsigned char* pb = sP + bb * LY::kPB;
-          const uint64_t dcol = sdesc(smem_u32(sCol), L * 128, 1024);
+        auto consume_p2 = [&](int j) -> bool {
+          const int s = slot_wait_full();
+          if (s < 0) return false;
+          const uint32_t sc = tm + kColSlot + 64 * s;
+          const uint64_t bp = desc_add(dColMN, j * 64 * 128);
+#pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = desc_add(dcol, (j * 64 + ks * 16) * 128);
-            mma_bf16(tm + kColTot, sdesc(smem_u32(pb) + ks * 32, 16, 1024), bd, id_acc,
-                     first ? 0u : 1u);
-            first = false;
-            mma_bf16(tm + kColTot, sdesc(smem_u32(pb) + LT * 128 + ks * 32, 16, 1024), bd, id_acc,
-                     1u);
+            const uint64_t bd = desc_add(bp, ks * 16 * 128);
+            mma_bf16_ta(tm + kColAcc, sc + 16 * ks, bd, id_nNm, ks > 0 ? 1u : acc_first);
+            mma_bf16_ta(tm + kColAcc, sc + 16 * ks + 8, bd, id_nNm, 1u);
           }
-          mma_commit(&bar_p_empty[bb]);
+          acc_first = 1u;
+          mma_commit(&bar_slot_free[s]);
           return true;
         };
         for (int i = 0; ok && i < hb; ++i) {
           ok = mbar_wait(&bar_ops_full[0], i & 1, status, &abort_flag);
           if (!ok) break;
           fence_after_sync();
-          ok = issue_s1(0);
-          if (ok && npan == 1) mma_commit(&bar_ops_empty[0]);
+          ok = produce_s1(0) && (npan < 2 || produce_s1(1));
+          if (ok && npan <= 2) mma_commit(&bar_ops_empty[0]);  // x / dy rows read
           for (int j = 0; ok && j < npan; ++j) {
-            if (j + 1 < npan) {
-              ok = issue_s1(j + 1);
-              // x / dy rows free once the head's S1 products are done
-              if (ok && j + 2 == npan) mma_commit(&bar_ops_empty[0]);
+            ok = consume_p2(j);
+            if (ok && j + 2 < npan) {
+              ok = produce_s1(j + 2);
+              if (ok && j + 3 == npan) mma_commit(&bar_ops_empty[0]);
             }
-            if (ok) ok = accumulate(i * upH + j, j);
-            if (ok && j + 2 == npan) mma_commit(&bar_img_empty);  // the image's buffer
           }
           if (!ok) break;
-          const int ui = i * upH + npan, bi = ui & 1, ba = (ui + 1) & 1;
-          ok = mbar_wait(&bar_img_full, i & 1, status, &abort_flag);
-          if (!ok) break;
+          // the state term's A operand: hand a free slot to the conversion warps
+          int sa = slot_take();
+          if (sa < 0) break;
+          mbar_arrive(&bar_slot_ready[sa]);
+          if (!mbar_wait(&bar_img_full, i & 1, status, &abort_flag)) break;
           fence_after_sync();
-          const unsigned char* img = sP + bi * LY::kPB;
+          int sst = -1;
           if constexpr (MODE == kDc) {
-            const int slot = ring_take();
-            if (slot < 0) {
-              ok = false;
-              break;
+            // the state dot C.H_c^T (for ycs) into the other slot
+            sst = slot_take();
+            if (sst < 0) break;
+#pragma unroll
+            for (int ks = 0; ks < N / 16; ++ks) {
+              constexpr int kR = LT * 128;
+              const uint32_t oa = (ks / 4) * kR + (ks % 4) * 32;
+              const uint32_t ob = (ks / 4) * (64 * 128) + (ks % 4) * 32;
+              const uint64_t ad = desc_add(dRowK, oa);
+              mma_bf16(tm + kColSlot + 64 * sst, ad, desc_add(dImgK, ob), id_n64k,
+                       ks > 0 ? 1u : 0u);
+              mma_bf16(tm + kColSlot + 64 * sst, ad, desc_add(dImgK, LY::kHlo + ob), id_n64k, 1u);
             }
-            state_dot(kColAcc + 64 * slot, img);
-            mma_commit(&bar_acc_full[slot]);
-          }
-          if (!wait_pfull(ba)) {
-            ok = false;
-            break;
+            mma_commit(&bar_slot_ready[sst]);
           }
           // TOT += A_st . img with A_st = e^{a_l} dy_l (DC) or delta_s e^{a_last-a_s} x_s
-          // (DB) in hi / lo, the image MN-major (K = p rows, N = d_state)
-          const unsigned char* pa = sP + ba * LY::kPB;
-          const uint64_t dim = sdesc(smem_u32(img), 64 * 128, 1024);
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t ah = sdesc(smem_u32(pa) + ks * 32, 16, 1024);
-            const uint64_t al = sdesc(smem_u32(pa) + LT * 128 + ks * 32, 16, 1024);
-            const uint64_t bh = desc_add(dim, ks * 2048), bl = desc_add(dim, LY::kHlo + ks * 2048);
-            mma_bf16(tm + kColTot, ah, bh, id_acc, 1u);
-            mma_bf16(tm + kColTot, ah, bl, id_acc, 1u);
-            mma_bf16(tm + kColTot, al, bh, id_acc, 1u);
+          // (DB), the image MN-major (K = p rows, N = d_state)
+          sa = slot_wait_full();
+          if (sa < 0) break;
+          {
+            const uint32_t sc = tm + kColSlot + 64 * sa;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t bh = desc_add(dImgMN, ks * 2048);
+              const uint64_t bl = desc_add(dImgMN, LY::kHlo + ks * 2048);
+              mma_bf16_ta(tm + kColAcc, sc + 16 * ks, bh, id_nNm, 1u);
+              mma_bf16_ta(tm + kColAcc, sc + 16 * ks, bl, id_nNm, 1u);
+              mma_bf16_ta(tm + kColAcc, sc + 16 * ks + 8, bh, id_nNm, 1u);
+            }
+            mma_commit(&bar_slot_free[sa]);
           }
-          mma_commit(&bar_p_empty[bi]);
-          mma_commit(&bar_p_empty[ba]);
+          mma_commit(&bar_img_empty);
+          if constexpr (MODE == kDc) {
+            // the conversion warps have read the state dot: its slot is free
+            sst = slot_wait_full();
+            if (sst < 0) break;
+            mbar_arrive(&bar_slot_free[sst]);
+          }
         }
         if (ok) mma_commit(&bar_tot);
       }
@@ -452,7 +483,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     }
   } else {
     // --------------------------------------------------- conversion warps
-    const int q = warp & 3, ch = warp >> 2;
+    const int q = warp & 3, cq = warp >> 2;     // lane quarter, column group
     const int rr = 32 * q + lane, r = r0 + rr;  // this thread's row (TMEM lane), chunk-local
     const int rw = r0 + 32 * q;                 // the warp's first row
     const uint32_t tl = tm + ((uint32_t)(32 * q) << 16);
@@ -460,18 +491,17 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_cb, 0, status, &abort_flag));
     fence_after_sync();
 
-    // per-head vectors -> derived arrays of stage v: a2 = a log2 e; sx: FWD / DC / DB
+    // per-head vectors -> derived arrays: a2 = a log2 e; sx: FWD / DC / DB
     // a2 - log2 delta (+inf where delta = 0), DX delta; cf: column factors of the
-    // factorized decay inside the causal triangle
-    // (three buffers: a head's epilogue may still read its arrays while the
-    // next-but-one head derives, and the conversion warps stay within one head
-    // of each other through the barriers here)
+    // factorized decay inside the causal triangle.  The barriers here keep the
+    // conversion warps within one head of each other.
+    auto der = [&](int i) { return sDer + (i % LY::kNDer) * 3 * L; };
     auto derive = [&](int i) {
       const int v = i & 1;
       ok = __all_sync(0xffffffffu, mbar_wait(&bar_vec_full[v], (i >> 1) & 1, status, &abort_flag)) &&
            ok;
       const float* ra = sVec + v * 2 * L;
-      float* da2 = sDer + (i % 3) * 3 * L;
+      float* da2 = der(i);
       float* dsx = da2 + L;
       float* dcf = dsx + L;
       for (int t = tid; t < L; t += kConv) {
@@ -489,39 +519,52 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
       conv_sync();
     };
 
-    // one 64-column panel j of head i (P-buffer use u): form P / P2 in fp32
-    // from TMEM, split it into hi / lo bf16 and store it for the MMA warp
-    uint32_t ru = 0;  // DC / DB ring uses consumed
+    // slot protocol (conversion side): wait until the MMA warp hands the slot
+    // over (FWD / DX: the products that read its previous contents are done;
+    // DC / DB: S1, the state dot or an empty slot is there), then work on it
+    uint32_t u = 0;  // slot uses
+    auto slot_acquire = [&]() -> uint32_t {
+      const int s = u & 1;
+      if (S1M || u >= 2) {
+        const uint32_t par = S1M ? (u >> 1) & 1 : ((u >> 1) - 1) & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_slot_ready[s], par, status, &abort_flag)) &&
+             ok;
+      }
+      fence_after_sync();
+      return tl + kColSlot + 64 * s;
+    };
+    auto slot_release = [&](bool wrote) {
+      if (wrote) tmem_wait_st();
+      fence_before_sync();
+      warp_arrive(&bar_slot_full[u & 1], lane);
+      ++u;
+    };
+
+    // one 64-column panel j of head i: P (FWD / DX) or P2 (DC / DB) in fp32,
+    // then hi / lo bf16 into the slot; DC / DB also add the row's M terms
     float msum = 0.f;
-    auto panel = [&](int i, int j, int u) {
-      const float* da2 = sDer + (i % 3) * 3 * L;
+    auto panel = [&](int i, int j) {
+      const float* da2 = der(i);
       const float* dsx = da2 + L;
       const float* dcf = dsx + L;
       const float a2r = da2[r], sxr = dsx[r];
-      const int cbase = col0 + 64 * j + 32 * ch;  // chunk-local first column of this thread
-      float base[2][16], cbv[2][16];
-      bool outside[2], inside[2];
+      const int cbase = col0 + 64 * j + kPC * cq;  // chunk-local first column of this thread
+      float base[kNG][16], cbv[kNG][16];
+      bool outside[kNG], inside[kNG];
 #pragma unroll
-      for (int qg = 0; qg < 2; ++qg) {
+      for (int qg = 0; qg < kNG; ++qg) {
         const int cg = cbase + 16 * qg;
         outside[qg] = REV ? cg + 15 < rw : cg > rw + 31;
         inside[qg] = REV ? cg > rw + 31 : cg + 15 < rw;
       }
-      int slot = 0;
-      if constexpr (S1M) {
-        slot = ru & 1;
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(&bar_acc_full[slot], (ru >> 1) & 1, status, &abort_flag)) && ok;
-        ++ru;
-        fence_after_sync();
-      }
+      const uint32_t sc = slot_acquire();
       if (ok) {
 #pragma unroll
-        for (int qg = 0; qg < 2; ++qg) {
+        for (int qg = 0; qg < kNG; ++qg) {
           if (outside[qg]) continue;
-          const uint32_t cb_col = 64 * j + 32 * ch + 16 * qg;  // CB's column (from col0)
+          const uint32_t cb_col = 64 * j + kPC * cq + 16 * qg;  // CB's column (from col0)
           if constexpr (S1M) {
-            tmem_ld16(tl + kColAcc + 64 * slot + 32 * ch + 16 * qg, base[qg]);
+            tmem_ld16(sc + kPC * cq + 16 * qg, base[qg]);
             tmem_ld16(tl + cb_col, cbv[qg]);
           } else {
             tmem_ld16(tl + cb_col, base[qg]);
@@ -529,19 +572,10 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         }
         tmem_wait_ld();
       }
-      if constexpr (S1M) {
-        fence_before_sync();
-        warp_arrive(&bar_acc_empty[slot], lane);
-      }
-      const int bb = u & 1;
-      if (u >= 2)
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_p_empty[bb], ((u >> 1) - 1) & 1, status,
-                                               &abort_flag)) && ok;
-      unsigned char* pb = sP + bb * LY::kPB;
 #pragma unroll
-      for (int qg = 0; qg < 2; ++qg) {
+      for (int qg = 0; qg < kNG; ++qg) {
         const int cg = cbase + 16 * qg;
-        float vv[16];
+        float* vv = base[qg];  // formed in place
         if (outside[qg] || !ok) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) vv[e] = 0.f;
@@ -557,9 +591,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             const float4 cf = *reinterpret_cast<const float4*>(dcf + cg + 4 * e4);
             const float2 f0 = __fmul2_rn(R2, make_float2(cf.x, cf.y));
             const float2 f1 = __fmul2_rn(R2, make_float2(cf.z, cf.w));
-            const float2 p0 = __fmul2_rn(f0, make_float2(base[qg][4 * e4], base[qg][4 * e4 + 1]));
-            const float2 p1 =
-                __fmul2_rn(f1, make_float2(base[qg][4 * e4 + 2], base[qg][4 * e4 + 3]));
+            const float2 p0 = __fmul2_rn(f0, make_float2(vv[4 * e4], vv[4 * e4 + 1]));
+            const float2 p1 = __fmul2_rn(f1, make_float2(vv[4 * e4 + 2], vv[4 * e4 + 3]));
             vv[4 * e4] = p0.x;
             vv[4 * e4 + 1] = p0.y;
             vv[4 * e4 + 2] = p1.x;
@@ -583,85 +616,104 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             else if constexpr (MODE == kDx) f = ex2_approx(da2[cl] - a2r);
             else f = ex2_approx(da2[cl] - sxr);
             const bool valid = REV ? cl >= r : cl <= r;
-            vv[e] = valid ? f * base[qg][e] : 0.f;
+            vv[e] = valid ? f * vv[e] : 0.f;
             if constexpr (S1M)
               if (cl != r) msum = fmaf(vv[e], cbv[qg][e], msum);
           }
         }
+        tmem_store_split16(sc + kPC * cq + 16 * qg, base[qg]);
+      }
+      slot_release(true);
+    };
+
+    // a state-term K panel (FWD / DX): the row operand (C_l or B_s, 64 of its
+    // d_state columns) scaled by e^{a_l} (FWD) or e^{a_last - a_s} (DX)
+    auto state_panel = [&](int i, int kp) {
+      const float* da2 = der(i);
+      const float a2r = da2[r];
+      const float sc_r = MODE == kFwd ? ex2_approx(a2r) : ex2_approx(da2[L - 1] - a2r);
+      const uint32_t sc = slot_acquire();
+#pragma unroll
+      for (int qg = 0; qg < kNG; ++qg) {
+        const int co = kPC * cq + 16 * qg;  // column within the panel
+        float vv[16];
 #pragma unroll
         for (int k8 = 0; k8 < 2; ++k8) {
-          const uint32_t off = sw128(rr, 4 * ch + 2 * qg + k8);
-          store_split8(pb + off, pb + LT * 128 + off, vv + 8 * k8);
+          float v8[8];
+          unpack8(*reinterpret_cast<const uint4*>(sRow + kp * (LT * 128) +
+                                                  sw128(rr, co / 8 + k8)), v8);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) vv[8 * k8 + e] = v8[e] * sc_r;
         }
+        tmem_store_split16(sc + co, vv);
       }
-      fence_async_smem();
-      warp_arrive(&bar_p_full[bb], lane);
+      slot_release(true);
     };
 
     if constexpr (!S1M) {
       // FWD / DX: a head's epilogue runs after the next head's first panel, so
-      // its last products finish while that panel is converted
-      // DX: this thread's 32 x values of its row, loaded from global memory
-      // when its head starts (xa); head i's epilogue runs during head i + 1 (xb)
-      uint4 xa[4] = {}, xb[4] = {};
-      auto prefetch_x = [&](int i, uint4 (&xr)[4]) {
+      // its last products finish while that panel is converted.
+      // DX: this thread's x values of its row, loaded from global memory when
+      // its head starts (xa); head i's epilogue runs during head i + 1 (xb)
+      uint4 xa[kCPT] = {}, xb[kCPT] = {};
+      auto prefetch_x = [&](int i, uint4 (&xr)[kCPT]) {
         if constexpr (MODE == kDx) {
-          const int64_t off = (((int64_t)b * T + t0 + r) * H + h_begin + i) * 64 + 32 * ch;
+          const int64_t off = (((int64_t)b * T + t0 + r) * H + h_begin + i) * 64 + kPC * cq;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
+          for (int k = 0; k < kCPT; ++k)
             xr[k] = live ? *reinterpret_cast<const uint4*>(a.xg + off + 8 * k)
                          : make_uint4(0, 0, 0, 0);
         }
       };
-      auto epilogue = [&](int i, const uint4 (&xr)[4]) {
-        const int st = i & 1, ac = i & 1, h = h_begin + i;
-        const float* da2 = sDer + (i % 3) * 3 * L;
+      auto epilogue = [&](int i, const uint4 (&xr)[kCPT]) {
+        const int st = i & 1, h = h_begin + i;
+        const int ab = MODE == kFwd ? st : 0;
+        const int na = MODE == kFwd ? (i >> 1) : i;
+        const float* da2 = der(i);
         const float* dsx = da2 + L;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full[ac], (i >> 1) & 1, status,
-                                               &abort_flag)) && ok;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full[ab], na & 1, status, &abort_flag)) &&
+             ok;
         ok = __all_sync(0xffffffffu, mbar_wait(&bar_ops_full[st], (i >> 1) & 1, status,
                                                &abort_flag)) && ok;
         fence_after_sync();
-        float yv[2][16], sv[2][16];
-        const uint32_t colY = kColAcc + 128 * ac;
+        float yv[kNG][16], sv[kNG][16];
+        const uint32_t colY = MODE == kFwd ? kColAcc + 64 * st : kColAcc;
         if (ok) {
-          tmem_ld16(tl + colY + 32 * ch, yv[0]);
-          tmem_ld16(tl + colY + 32 * ch + 16, yv[1]);
-          tmem_ld16(tl + colY + 64 + 32 * ch, sv[0]);
-          tmem_ld16(tl + colY + 64 + 32 * ch + 16, sv[1]);
+#pragma unroll
+          for (int g2 = 0; g2 < kNG; ++g2) {
+            tmem_ld16(tl + colY + kPC * cq + 16 * g2, yv[g2]);
+            if constexpr (MODE == kDx) tmem_ld16(tl + colY + 64 + kPC * cq + 16 * g2, sv[g2]);
+          }
           tmem_wait_ld();
         }
         fence_before_sync();
-        warp_arrive(&bar_acc_empty[ac], lane);
+        warp_arrive(&bar_acc_empty[ab], lane);
         // this thread's row of the stage's x (FWD) or dy (DX) rows
         const unsigned char* orow = sOps + st * LY::kOps;
         const int orr = r - col0;
         const float Dh = a.D ? a.D[h] : 0.f;
-        const float a2r = da2[r];
         float pd = 0.f, pq = 0.f, pdd = 0.f;
         if (ok && live) {
-          const float ea = MODE == kFwd ? ex2_approx(a2r) : ex2_approx(da2[L - 1] - a2r);
           const float dr = MODE == kDx ? dsx[r] : 0.f;
-          const int64_t ooff = (((int64_t)b * T + t0 + r) * H + h) * 64 + 32 * ch;
+          const int64_t ooff = (((int64_t)b * T + t0 + r) * H + h) * 64 + kPC * cq;
 #pragma unroll
-          for (int k8 = 0; k8 < 4; ++k8) {
+          for (int k8 = 0; k8 < kCPT; ++k8) {
             float ov[8], o[8];
-            unpack8(*reinterpret_cast<const uint4*>(orow + sw128(orr, 4 * ch + k8)), ov);
+            unpack8(*reinterpret_cast<const uint4*>(orow + sw128(orr, kCPT * cq + k8)), ov);
             const float* yk = yv[k8 >> 1] + 8 * (k8 & 1);
-            const float* sk = sv[k8 >> 1] + 8 * (k8 & 1);
             if constexpr (MODE == kFwd) {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) o[e] = yk[e] + ea * sk[e] + Dh * ov[e];
+              for (int e = 0; e < 8; ++e) o[e] = fmaf(Dh, ov[e], yk[e]);
             } else {
+              const float* sk = sv[k8 >> 1] + 8 * (k8 & 1);
               float xv[8];
               unpack8(xr[k8], xv);
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                const float us = ea * sk[e];
-                const float uu = yk[e] + us;
+                const float uu = yk[e] + sk[e];
                 o[e] = fmaf(dr, uu, Dh * ov[e]);
                 pd = fmaf(xv[e], uu, pd);
-                pq = fmaf(xv[e], us, pq);
+                pq = fmaf(xv[e], sk[e], pq);
                 pdd = fmaf(xv[e], ov[e], pdd);
               }
             }
@@ -679,18 +731,25 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         }
         warp_arrive(&bar_ops_empty[st], lane);
         if constexpr (MODE == kDx) {
-          float* red = sRed + (i & 1) * 3 * 128;
-          if (ch == 1) {
-            red[rr] = pd;
-            red[128 + rr] = pq;
-            red[256 + rr] = pdd;
+          // the row's column groups meet in shared memory (the next writes come
+          // after the next head's derive barriers)
+          if (cq > 0) {
+            sRed[(0 * kCG + cq) * 128 + rr] = pd;
+            sRed[(1 * kCG + cq) * 128 + rr] = pq;
+            sRed[(2 * kCG + cq) * 128 + rr] = pdd;
           }
           conv_sync();
-          if (ch == 0 && live && ok) {
+          if (cq == 0 && live && ok) {
+#pragma unroll
+            for (int k = 1; k < kCG; ++k) {
+              pd += sRed[(0 * kCG + k) * 128 + rr];
+              pq += sRed[(1 * kCG + k) * 128 + rr];
+              pdd += sRed[(2 * kCG + k) * 128 + rr];
+            }
             const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
-            a.ddir[cv + r] = pd + red[rr];
-            a.qrow[cv + r] = dsx[r] * (pq + red[128 + rr]);
-            a.ddiag[cv + r] = pdd + red[256 + rr];
+            a.ddir[cv + r] = pd;
+            a.qrow[cv + r] = dsx[r] * pq;
+            a.ddiag[cv + r] = pdd;
           }
         }
       };
@@ -698,67 +757,62 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         derive(i);
         if constexpr (MODE == kDx) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) xb[k] = xa[k];  // the previous head's
+          for (int k = 0; k < kCPT; ++k) xb[k] = xa[k];  // the previous head's
         }
         prefetch_x(i, xa);
         for (int j = 0; j < npan; ++j) {
-          panel(i, j, i * upH + j);
+          panel(i, j);
           if (j == 0 && i > 0) epilogue(i - 1, xb);
         }
+        for (int kp = 0; kp < NP; ++kp) state_panel(i, kp);
       }
       if (hb > 0) epilogue(hb - 1, xa);
     } else {
-      uint4 hrow[4];  // this thread's 32 values of its row of dy (DC) or x (DB)
+      uint4 hrow[kCPT];  // this thread's values of its row of dy (DC) or x (DB)
       for (int i = 0; i < hb; ++i) {
         const int h = h_begin + i;
         ok = __all_sync(0xffffffffu, mbar_wait(&bar_ops_full[0], i & 1, status, &abort_flag)) &&
              ok;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          hrow[k] = *reinterpret_cast<const uint4*>(sHR + sw128(rr, 4 * ch + k));
+        for (int k = 0; k < kCPT; ++k)
+          hrow[k] = *reinterpret_cast<const uint4*>(sHR + sw128(rr, kCPT * cq + k));
         warp_arrive(&bar_ops_empty[0], lane);
         derive(i);
         msum = 0.f;
-        for (int j = 0; j < npan; ++j) panel(i, j, i * upH + j);
-        const float* da2 = sDer + (i % 3) * 3 * L;
+        for (int j = 0; j < npan; ++j) panel(i, j);
+        const float* da2 = der(i);
         const float* dsx = da2 + L;
-        // the state term's A operand into the buffer after the image's
-        const int ua = i * upH + npan + 1, ba = ua & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_p_empty[ba], ((ua >> 1) - 1) & 1, status,
-                                               &abort_flag)) && ok;
         {
-          const float sc = MODE == kDc ? ex2_approx(da2[r]) : ex2_approx(da2[L - 1] - dsx[r]);
-          unsigned char* pa = sP + ba * LY::kPB;
+          // the state term's A operand: e^{a_l} dy_l (DC), delta_s e^{a_last-a_s} x_s (DB)
+          const float sc_r = MODE == kDc ? ex2_approx(da2[r]) : ex2_approx(da2[L - 1] - dsx[r]);
+          const uint32_t sc = slot_acquire();
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            float v[8];
-            unpack8(hrow[k], v);
+          for (int qg = 0; qg < kNG; ++qg) {
+            float vv[16];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] *= sc;
-            const uint32_t off = sw128(rr, 4 * ch + k);
-            store_split8(pa + off, pa + LT * 128 + off, v);
+            for (int k8 = 0; k8 < 2; ++k8) {
+              float v8[8];
+              unpack8(hrow[2 * qg + k8], v8);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) vv[8 * k8 + e] = v8[e] * sc_r;
+            }
+            tmem_store_split16(sc + kPC * cq + 16 * qg, vv);
           }
+          slot_release(true);
         }
-        fence_async_smem();
-        warp_arrive(&bar_p_full[ba], lane);
         float ypart = 0.f;
         if constexpr (MODE == kDc) {
-          // ycs_l = e^{a_l} <dy_l, C_l . H_c^T> from the state dot in the ring
-          const int slot = ru & 1;
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(&bar_acc_full[slot], (ru >> 1) & 1, status, &abort_flag)) && ok;
-          ++ru;
-          fence_after_sync();
-          float sv[2][16];
+          // ycs_l = e^{a_l} <dy_l, C_l . H_c^T> from the state dot in the other slot
+          const uint32_t sc = slot_acquire();
+          float sv[kNG][16];
           if (ok) {
-            tmem_ld16(tl + kColAcc + 64 * slot + 32 * ch, sv[0]);
-            tmem_ld16(tl + kColAcc + 64 * slot + 32 * ch + 16, sv[1]);
+#pragma unroll
+            for (int g2 = 0; g2 < kNG; ++g2) tmem_ld16(sc + kPC * cq + 16 * g2, sv[g2]);
             tmem_wait_ld();
           }
-          fence_before_sync();
-          warp_arrive(&bar_acc_empty[slot], lane);
+          slot_release(false);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
+          for (int k = 0; k < kCPT; ++k) {
             float v[8];
             unpack8(hrow[k], v);
 #pragma unroll
@@ -766,28 +820,35 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
           }
           ypart *= ex2_approx(da2[r]);
         }
-        float* red = sRed + (i & 1) * 3 * 128;
-        if (ch == 1) {
-          red[rr] = msum;
-          red[128 + rr] = ypart;
+        // the row's column groups meet in shared memory (the next writes come
+        // after the next head's derive barriers)
+        if (cq > 0) {
+          sRed[cq * 128 + rr] = msum;
+          if constexpr (MODE == kDc) sRed[(kCG + cq) * 128 + rr] = ypart;
         }
         conv_sync();
-        if (ch == 0 && live && ok) {
+        if (cq == 0 && live && ok) {
+#pragma unroll
+          for (int k = 1; k < kCG; ++k) {
+            msum += sRed[k * 128 + rr];
+            if constexpr (MODE == kDc) ypart += sRed[(kCG + k) * 128 + rr];
+          }
           const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
-          a.msum[cv + r] = msum + red[rr];
-          if constexpr (MODE == kDc) a.ycs[cv + r] = ypart + red[128 + rr];
+          a.msum[cv + r] = msum;
+          if constexpr (MODE == kDc) a.ycs[cv + r] = ypart;
         }
       }
       // the block's accumulated dC / dB rows
+      constexpr int NT = N / kCG;  // accumulator columns per thread
       ok = __all_sync(0xffffffffu, mbar_wait(&bar_tot, 0, status, &abort_flag)) && ok;
       fence_after_sync();
       if (ok && hb > 0) {
         float* o = static_cast<float*>(a.out) +
-                   ((((int64_t)b * T + t0 + r) * a.G + g) * a.nblk + kb) * N + ch * (N / 2);
+                   ((((int64_t)b * T + t0 + r) * a.G + g) * a.nblk + kb) * N + cq * NT;
 #pragma unroll
-        for (int c0 = 0; c0 < N / 2; c0 += 16) {
+        for (int c0 = 0; c0 < NT; c0 += 16) {
           float v[16];
-          tmem_ld16(tl + kColTot + ch * (N / 2) + c0, v);
+          tmem_ld16(tl + kColAcc + cq * NT + c0, v);
           tmem_wait_ld();
           if (live) {
 #pragma unroll
@@ -892,15 +953,7 @@ cudaError_t chunk_bwd_nl(const Dims& d, const BwdArgs& ba, const TcBwdWs& w, int
   a.hb = d.H / d.G / nblk;
   a.status = device_status_ptr();
   if (!a.status) return cudaErrorUnknown;
-  // dx (with the ddt / ddA inner products)
-  ChunkArgs ax = a;
-  ax.img = static_cast<const unsigned char*>(w.dSimg);
-  ax.out = ba.dx;
-  ax.ddir = w.ddir;
-  ax.qrow = w.qrow;
-  ax.ddiag = w.ddiag;
-  cudaError_t e = launch_chunk<N, L, kDx, float>(d, mB, mC, mDY, mDY, ax, "k_scan_tc_dx", s);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   // dC: rows l, S1 = dy.x^T, H_c images
   ChunkArgs ac = a;
   ac.img = static_cast<const unsigned char*>(w.Himg);

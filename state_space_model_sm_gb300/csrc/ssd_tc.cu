@@ -315,6 +315,382 @@ __global__ void __launch_bounds__(256, 2)
   if (warp == 0) tmem_dealloc(tm, kTmemCols);
 }
 
+// ================================================================ dx
+// The cp.async scan kernel, in the direction the backward's dx uses (the
+// forward direction runs in ssd_chunk_tc.cu).  One kernel, two directions.
+//   forward (REV = false), rows r = l of chunk c, columns s in [0, l0 + 128):
+//     CB[l, s] = C_l . B_s                       (TMEM cols 0.., once per CTA)
+//     per head: Y  = sum_s P[l, s] x_s,  P = CB e^{a_l - a_s} delta_s [s <= l]
+//               ST = C_l . H_c[p, :]
+//               y_l = Y + e^{a_l} ST + D x_l
+//   backward dx (REV = true), rows r = s, columns l in [s0, L):
+//     CBT[s, l] = B_s . C_l
+//     per head: Y  = sum_l P[s, l] dy_l,  P = CBT e^{a_l - a_s} [l >= s]
+//               ST = B_s . dS_c[p, :]
+//               u_s = Y + e^{a_last - a_s} ST;  dx_s = delta_s u_s + D dy_s
+//               ddir_s = <x_s, u_s>,  qrow_s = delta_s <x_s, e^{a_last - a_s} ST>,
+//               ddiag_s = <x_s, dy_s>
+// Persistent, one CTA (512 threads) per SM over a balanced range of (batch,
+// chunk, 128-row tile, group) x head items.  Per unit the score tile is
+// formed once; then the two 8-warp pipelines run independent chains on
+// alternate heads (own TMEM accumulators, P buffer, operand rows and
+// mbarriers), so one pipeline's loads and waits overlap the other's work.
+template <int N, int L>
+struct ScanSmem {
+  static constexpr int kLT = 128;
+  static constexpr int kC = (N / 64) * kLT * 128;           // row-operand rows of the tile
+  static constexpr int kBrows = (N / 64) * L * 128;         // column-operand rows
+  static constexpr int kPw = 2 * kLT * 128;                 // per group: P panel hi + lo
+  static constexpr int kBP = kBrows > 2 * kPw ? kBrows : 2 * kPw;
+  static constexpr int kX = L * 128;                        // per group: x or dy rows
+  static constexpr int kHlo = (N / 64) * 64 * 128;          // offset of the state's lo part
+  static constexpr int kImg = 2 * kHlo;                     // bytes of one state image
+  static constexpr int kBytes = kC + kBP + 2 * kX + (10 * L + 6 * 128) * 4 + 1024;
+};
+
+__device__ __forceinline__ void group_sync(int id) {
+  asm volatile("bar.sync %0, 256;" ::"r"(id) : "memory");
+}
+
+template <int N, int L, typename Tout, bool REV>
+__global__ void __launch_bounds__(512, 1)
+    k_scan_tc(const bf16* __restrict__ x, const bf16* __restrict__ Bm,
+              const bf16* __restrict__ Cm, const bf16* __restrict__ dy,
+              const float* __restrict__ delta, const float* __restrict__ acs,
+              const unsigned char* __restrict__ simg, const float* __restrict__ D,
+              Tout* __restrict__ out, float* __restrict__ ddir, float* __restrict__ qrow,
+              float* __restrict__ ddiag, int B_, int T, int H, int G, int nc, int items_per_cta,
+              int* status) {
+  using SM = ScanSmem<N, L>;
+  constexpr int LT = SM::kLT, NLT = L / LT;
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t bar_cb, bar_p[2], bar_st[2], bar_done[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  unsigned char* base = align1024(smem_raw);
+  unsigned char* sR = base;               // row operand: C (fwd) or B (rev) rows of the tile
+  unsigned char* sBP = sR + SM::kC;       // column operand rows, later the groups' P buffers
+  unsigned char* sXall = sBP + SM::kBP;   // per group: x (fwd) or dy (rev) rows
+  float* sAall = reinterpret_cast<float*>(sXall + 2 * SM::kX);  // per group: a [L], delta [L]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hpg = H / G;
+  const int64_t n_items = (int64_t)B_ * nc * NLT * H;  // (batch, chunk, tile, group) x head
+  const int64_t it_begin = (int64_t)blockIdx.x * items_per_cta;
+  const int64_t it_end = min(n_items, it_begin + items_per_cta);
+  const bf16* rowsrc = REV ? Bm : Cm;
+  const bf16* colsrc = REV ? Cm : Bm;
+  const bf16* opsrc = REV ? dy : x;
+
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_cb, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_p[i], 1);
+      mbar_init(&bar_st[i], 1);
+      mbar_init(&bar_done[i], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(&tmem_base, 512);
+  // TMEM and the per-group state live across the CTA's whole item range
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tm = tmem_base;
+  // two pipelines of 8 warps; a TMEM row is shared by the warps q and q + 4
+  // of a pipeline, each taking 32 of a panel's 64 columns
+  const int wg = tid >> 8, wtid = tid & 255, wq = wtid >> 5, q = wq & 3, half = wq >> 2;
+  const int rr = 32 * q + lane;
+  const uint32_t tlane = tm + ((uint32_t)(32 * q) << 16);
+  const uint32_t colY = 256 + 128 * wg, colST = colY + 64;
+  const int gbar = 1 + wg;
+  float* sred = sAall + 8 * L + wg * 3 * 128;  // [3][128] per pipeline: half-row partial sums
+  float* scf = sAall + 8 * L + 6 * 128 + wg * L;  // per pipeline: column factors (forward)
+  uint32_t n_p = 0, n_st = 0, n_done = 0, n_units = 0;
+
+  for (int64_t item = it_begin; item < it_end;) {
+    // one unit = (batch, chunk, row tile, group); this CTA's heads of it
+    const int64_t unit = item / hpg;
+    const int j0 = (int)(item % hpg);
+    const int j1 = (int)min((int64_t)hpg, j0 + (it_end - item));
+    item += j1 - j0;
+    const int g = (int)(unit % G);
+    const int64_t bct = unit / G;
+    const int tile = (int)(bct % NLT);
+    const int64_t bc = bct / NLT;
+    const int c = (int)(bc % nc), b = (int)(bc / nc);
+    const int h_begin = g * hpg + j0, h_end = g * hpg + j1;
+    const int r0 = tile * LT;                       // first row (chunk-local)
+    const int col0 = REV ? r0 : 0;                  // first column
+    const int ncol = REV ? L - r0 : r0 + LT;        // number of columns
+    const int nsp = ncol / 64;
+    const int64_t t0 = (int64_t)c * L;
+    const int Lv = min(L, T - (int)t0);
+    const int r = r0 + rr;                          // this thread's row (TMEM lane)
+
+  stage_rows_async(sR, LT, N / 8, LT * 128, Lv - r0, rowsrc, [&](int rr2) {
+      return rowsrc + (((int64_t)b * T + t0 + r0 + rr2) * G + g) * N;
+    });
+    stage_rows_async(sBP, ncol, N / 8, L * 128, Lv - col0, colsrc, [&](int cc) {
+      return colsrc + (((int64_t)b * T + t0 + col0 + cc) * G + g) * N;
+    });
+    cp_async_commit();
+    cp_async_wait<0>();
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      const uint32_t id = idesc_bf16(128, ncol, 0, 0);
+      for (int ks = 0; ks < N / 16; ++ks) {
+        const uint32_t kp = ks / 4, ko = (ks % 4) * 32;
+        mma_bf16(tm, sdesc(smem_u32(sR) + kp * (LT * 128) + ko, 16, 1024),
+                 sdesc(smem_u32(sBP) + kp * (L * 128) + ko, 16, 1024), id, ks > 0 ? 1u : 0u);
+      }
+      mma_commit(&bar_cb);
+    }
+    mbar_wait(&bar_cb, n_units & 1, status, &abort_flag);
+    ++n_units;
+    fence_after_sync();
+    // sBP (the column operand) is free from here on: it becomes the P buffers.
+    __syncthreads();
+
+  unsigned char* Pw = sBP + wg * SM::kPw;
+  unsigned char* sX = sXall + wg * SM::kX;
+  float* sa2 = sAall + wg * 4 * L;  // a * log2(e)
+  float* sx = sa2 + L;              // fwd: a*log2e - log2(delta)  (+inf where delta = 0); rev: delta
+  float* sraw = sx + L;             // prefetched a [L], delta [L] of the next head
+  constexpr uint32_t id_py = idesc_bf16(128, kP, 0, 1);
+  constexpr uint32_t id_st = idesc_bf16(128, kP, 0, 0);
+
+  // cp.async of everything a head needs: its second-operand rows (sX), its
+  // inter-chunk state image (into the P buffer) and its raw a / delta.
+  auto prefetch = [&](int hh) {
+    for (int i = wtid; i < ncol * 8; i += 256) {
+      const int cc = i >> 3, j = i & 7, col = col0 + cc;
+      const bool v = col < Lv;
+      cp_async16(sX + sw128(cc, j),
+                 v ? opsrc + (((int64_t)b * T + t0 + col) * H + hh) * kP + j * 8 : opsrc, v);
+    }
+    const unsigned char* img = simg + ((((int64_t)b * nc + c) * H + hh) * (int64_t)SM::kImg);
+    for (int i = wtid; i < SM::kImg / 16; i += 256) cp_async16(Pw + 16 * i, img + 16 * i, true);
+    const int64_t cvh = (((int64_t)b * H + hh) * nc + c) * L;
+    for (int i = wtid; i < L / 4; i += 256) {
+      cp_async16(sraw + 4 * i, acs + cvh + 4 * i, true);
+      cp_async16(sraw + L + 4 * i, delta + cvh + 4 * i, true);
+    }
+  };
+  if (h_begin + wg < h_end) prefetch(h_begin + wg);
+  cp_async_commit();
+
+  for (int h = h_begin + wg; h < h_end; h += 2) {
+    const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
+    const float Dh = D ? D[h] : 0.f;
+    cp_async_wait<0>();
+    group_sync(gbar);  // the raw vectors were copied by other threads of the group
+    for (int i = wtid; i < L; i += 256) {
+      const float a2 = sraw[i] * kLog2e, dl = sraw[L + i];
+      sa2[i] = a2;
+      sx[i] = REV ? dl : (dl > 0.f ? a2 - lg2_approx(dl) : __int_as_float(0x7f800000));
+    }
+    fence_async_smem();
+    fence_before_sync();
+    group_sync(gbar);
+    if (wtid == 0) {
+      fence_after_sync();
+      for (int ks = 0; ks < N / 16; ++ks) {
+        const uint32_t kp = ks / 4, ko = (ks % 4) * 32;
+        const uint64_t ad = sdesc(smem_u32(sR) + kp * (LT * 128) + ko, 16, 1024);
+        mma_bf16(tm + colST, ad, sdesc(smem_u32(Pw) + kp * (64 * 128) + ko, 16, 1024), id_st,
+                 ks > 0 ? 1u : 0u);
+        mma_bf16(tm + colST, ad, sdesc(smem_u32(Pw) + SM::kHlo + kp * (64 * 128) + ko, 16, 1024),
+                 id_st, 1u);
+      }
+      mma_commit(&bar_st[wg]);
+    }
+    // Forward: column factors for column groups strictly inside the causal
+    // triangle, e^{a_l - a_s} delta_s = R_l * cf_s with the group's last column
+    // m as reference: cf_s = 2^{a_m - a_s} delta_s, R_l = 2^{a_l - a_m}; a is
+    // monotone, so both are <= 1.  (The dx direction keeps the per-element
+    // exponential: measured faster there.)
+    if constexpr (!REV) {
+      for (int i = wtid; i < L; i += 256) scf[i] = ex2_approx(sa2[i | 15] - sx[i]);
+      group_sync(gbar);
+    }
+    ++n_st;
+    mbar_wait(&bar_st[wg], (n_st - 1) & 1, status, &abort_flag);  // P buffer free again
+    fence_after_sync();
+    const float ar2 = sa2[r];
+    for (int j = 0; j < nsp; ++j) {
+      if (j > 0) mbar_wait(&bar_p[wg], (n_p - 1) & 1, status, &abort_flag);
+      const float* colv = (REV ? sa2 : sx) + col0 + 64 * j;  // per-column log2 terms
+      // the thread's 32 columns as two 16-column groups; the second group's
+      // TMEM load is in flight while the first is formed
+      float cbA[16], cbB[16];
+      tmem_ld16(tlane + 64 * j + 32 * half, cbA);
+      tmem_wait_ld();
+#pragma unroll
+      for (int qg = 0; qg < 2; ++qg) {
+        float(&cur)[16] = qg ? cbB : cbA;
+        if (qg == 0) tmem_ld16(tlane + 64 * j + 32 * half + 16, cbB);
+        // the warp's 32 rows [rw, rw + 32) against 16 columns [cg, cg + 16):
+        // outside the causal triangle, strictly inside it, or across the diagonal
+        const int cg = col0 + 64 * j + 32 * half + 16 * qg, rw = r0 + 32 * q;
+        const bool outside = !REV && cg > rw + 31;
+        const bool inside = !REV && cg + 15 < rw;
+        if (outside) {
+#pragma unroll
+          for (int k8 = 0; k8 < 2; ++k8) {
+            const uint32_t off = sw128(rr, (32 * half + 16 * qg + 8 * k8) / 8);
+            *reinterpret_cast<uint4*>(Pw + off) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(Pw + LT * 128 + off) = make_uint4(0, 0, 0, 0);
+          }
+        } else if (inside) {
+          const int m = cg + 15;
+          const float R = ex2_approx(ar2 - sa2[m]);
+          const float2 R2 = make_float2(R, R);
+#pragma unroll
+          for (int k8 = 0; k8 < 2; ++k8) {
+            const int c8 = 32 * half + 16 * qg + 8 * k8;  // panel-local column of the chunk
+            const float4 c0 = *reinterpret_cast<const float4*>(scf + cg + 8 * k8);
+            const float4 c1 = *reinterpret_cast<const float4*>(scf + cg + 8 * k8 + 4);
+            const float* sv = cur + 8 * k8;
+            const float2 p0 = __fmul2_rn(__fmul2_rn(R2, make_float2(c0.x, c0.y)), make_float2(sv[0], sv[1]));
+            const float2 p1 = __fmul2_rn(__fmul2_rn(R2, make_float2(c0.z, c0.w)), make_float2(sv[2], sv[3]));
+            const float2 p2 = __fmul2_rn(__fmul2_rn(R2, make_float2(c1.x, c1.y)), make_float2(sv[4], sv[5]));
+            const float2 p3 = __fmul2_rn(__fmul2_rn(R2, make_float2(c1.z, c1.w)), make_float2(sv[6], sv[7]));
+            const float v[8] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y, p3.x, p3.y};
+            const uint32_t off = sw128(rr, c8 / 8);
+            store_split8(Pw + off, Pw + LT * 128 + off, v);
+          }
+        } else {
+#pragma unroll
+          for (int k8 = 0; k8 < 2; ++k8) {
+            const int c8 = 32 * half + 16 * qg + 8 * k8;  // panel-local column of the chunk
+            const float4 w0 = *reinterpret_cast<const float4*>(colv + c8);
+            const float4 w1 = *reinterpret_cast<const float4*>(colv + c8 + 4);
+            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int cl = col0 + 64 * j + c8 + e;  // chunk-local column
+              const float f = REV ? ex2_approx(wv[e] - ar2) : ex2_approx(ar2 - wv[e]);
+              v[e] = (REV ? cl >= r : cl <= r) ? cur[8 * k8 + e] * f : 0.f;
+            }
+            const uint32_t off = sw128(rr, c8 / 8);
+            store_split8(Pw + off, Pw + LT * 128 + off, v);
+          }
+        }
+        if (qg == 0) tmem_wait_ld();
+      }
+      fence_async_smem();
+      fence_before_sync();
+      group_sync(gbar);
+      if (wtid == 0) {
+        fence_after_sync();
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t bd = sdesc(smem_u32(sX) + (64 * j + 16 * ks) * 128, L * 128, 1024);
+          mma_bf16(tm + colY, sdesc(smem_u32(Pw) + ks * 32, 16, 1024), bd, id_py,
+                   (j > 0 || ks > 0) ? 1u : 0u);
+          mma_bf16(tm + colY, sdesc(smem_u32(Pw) + LT * 128 + ks * 32, 16, 1024), bd, id_py, 1u);
+        }
+        mma_commit(&bar_p[wg]);
+        if (j == nsp - 1) mma_commit(&bar_done[wg]);  // one phase per head
+      }
+      ++n_p;
+    }
+    // this thread's 32 columns of its row of the second operand (x or dy) and,
+    // rev, of x: loaded now, so the latency overlaps the last MMAs
+    const int64_t rowoff = (((int64_t)b * T + t0 + r) * H + h) * kP;
+    const bool live = r < Lv;
+    uint4 orow[4], xrow[4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      orow[kk] = live ? *reinterpret_cast<const uint4*>(opsrc + rowoff + 32 * half + 8 * kk)
+                      : make_uint4(0, 0, 0, 0);
+      if constexpr (REV)
+        xrow[kk] = live ? *reinterpret_cast<const uint4*>(x + rowoff + 32 * half + 8 * kk)
+                        : make_uint4(0, 0, 0, 0);
+    }
+    ++n_done;
+    const bool ok = mbar_wait(&bar_done[wg], (n_done - 1) & 1, status, &abort_flag);
+    fence_after_sync();
+    // this head's MMAs are done: sX and the P buffer take the next head's data
+    if (h + 2 < h_end) prefetch(h + 2);
+    cp_async_commit();
+    float pd = 0.f, pq = 0.f, pdd = 0.f;  // rev: partial <x, u>, <x, state part>, <x, dy>
+    if (ok) {
+      const float ea = ex2_approx(ar2), es = ex2_approx(sa2[L - 1] - ar2);
+      const float dr = REV ? sx[r] : 0.f;
+#pragma unroll
+      for (int c16 = 0; c16 < 2; ++c16) {
+        float yv[16], st[16];
+        tmem_ld16(tlane + colY + 32 * half + 16 * c16, yv);
+        tmem_ld16(tlane + colST + 32 * half + 16 * c16, st);
+        tmem_wait_ld();
+        if (live) {
+#pragma unroll
+          for (int k8 = 0; k8 < 2; ++k8) {
+            float ov[8], o[8];
+            unpack8(orow[2 * c16 + k8], ov);
+            if constexpr (!REV) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                o[e] = yv[8 * k8 + e] + ea * st[8 * k8 + e] + Dh * ov[e];
+            } else {
+              float xv[8];
+              unpack8(xrow[2 * c16 + k8], xv);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float us = es * st[8 * k8 + e];
+                const float u = yv[8 * k8 + e] + us;
+                o[e] = fmaf(dr, u, Dh * ov[e]);
+                pd = fmaf(xv[e], u, pd);
+                pq = fmaf(xv[e], us, pq);
+                pdd = fmaf(xv[e], ov[e], pdd);
+              }
+            }
+            Tout* op = out + rowoff + 32 * half + 16 * c16 + 8 * k8;
+            if constexpr (sizeof(Tout) == 4) {
+              float* of = reinterpret_cast<float*>(op);
+              *reinterpret_cast<float4*>(of) = make_float4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<float4*>(of + 4) = make_float4(o[4], o[5], o[6], o[7]);
+            } else {
+              *reinterpret_cast<uint4*>(op) =
+                  make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
+                             pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
+            }
+          }
+        }
+      }
+    }
+    if constexpr (REV) {
+      // combine the two half-rows (pipeline-local barrier)
+      if (half == 1) {
+        sred[rr] = pd;
+        sred[128 + rr] = pq;
+        sred[256 + rr] = pdd;
+      }
+      group_sync(gbar);
+      if (half == 0 && r < Lv) {
+        ddir[cv + r] = pd + sred[rr];
+        qrow[cv + r] = sx[r] * (pq + sred[128 + rr]);
+        ddiag[cv + r] = pdd + sred[256 + rr];
+      }
+    }
+    fence_before_sync();
+    group_sync(gbar);  // sX, sa, sd and the accumulators are reused by the next head
+  }
+    // both groups are done with this unit's C.B^T tile and buffers
+    fence_before_sync();
+    __syncthreads();
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tm, 512);
+}
+
 // grid (nc, H, B).  Gradient w.r.t. dA_r = delta_r A from the strict row sums
 // (dC kernel) and column sums (dB kernel) of M:
 //   ddA_r = sum_{j<r} (colsum_j - rowsum_j) + sum_{l>=r} ycs_l + sum_{s<r} qrow_s + dlast_c
@@ -447,6 +823,16 @@ __global__ void __launch_bounds__(NT)
 }
 
 // ------------------------------------------------------------------ launch
+// Persistent scan kernels: one CTA per SM, each taking a contiguous range of
+// the (batch, chunk, row tile, group) x head items, so every SM gets the same
+// number of heads (+-1) whatever the shape.
+void scan_partition(const Dims& d, int sms, int* grid, int* per) {
+  const int64_t items = (int64_t)d.B * d.nc * (d.L / 128) * d.H;
+  const int64_t g = items < sms ? items : sms;
+  *per = (int)((items + g - 1) / g);
+  *grid = (int)((items + *per - 1) / *per);
+}
+
 // chunk_cumsum (delta, a) and chunk_state (S) in one persistent launch.
 template <int N, int L>
 void launch_state_front(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s,
@@ -508,6 +894,17 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
   launch_dstates<N, L>(d, dy, Cm, w.delta, w.acs, w.dHs, s, status, sms);
   const int nsplit = simt_state_passing_bwd(d, w.dHs, w.acs, nullptr, a.dfinal, nullptr, w.dlast,
                                             a.dinit, w.dSimg, w.Himg, w.seg, s);
+  {
+    using SM = ScanSmem<N, L>;
+    auto kern = k_scan_tc<N, L, float, true>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
+    int grid, per;
+    scan_partition(d, sms, &grid, &per);
+    SSD_LAUNCH("k_scan_tc_dx", s, kern<<<grid, 512, SM::kBytes, s>>>(
+        static_cast<const bf16*>(a.f.x), static_cast<const bf16*>(a.f.B), Cm, dy, w.delta, w.acs,
+        static_cast<const unsigned char*>(w.dSimg), a.f.D, a.dx, w.ddir, w.qrow, w.ddiag, d.B, d.T,
+        d.H, d.G, d.nc, per, status));
+  }
   const int nblk = tc_bwd_nblk(d);
   float* dCout = nblk == 1 ? a.dC : w.dCp;
   float* dBout = nblk == 1 ? a.dB : w.dBp;

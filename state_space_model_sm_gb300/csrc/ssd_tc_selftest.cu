@@ -1,7 +1,8 @@
 // ssd_selftest_mma: one tcgen05 tile product, D[128][nn] = A[128][k] * B[nn][k]^T,
 // with each operand staged K-major or MN-major in the 128-byte-swizzle
-// layout the SSD kernels use.  A diagnostic entry point: it checks the
-// descriptor conventions of tc_ptx.cuh on the device it runs on.
+// layout the SSD kernels use, or (a_mn == 2) A held in tensor memory as
+// packed bf16 pairs.  A diagnostic entry point: it checks the descriptor and
+// tensor-memory conventions of tc_ptx.cuh on the device it runs on.
 #include "ssd_internal.h"
 #include "tc_ptx.cuh"
 
@@ -26,7 +27,10 @@ __global__ void __launch_bounds__(128)
   unsigned char* sB = base + 32768;  // <= 256 x 128 bf16
   const int tid = threadIdx.x, warp = tid >> 5;
   const int kc = K / 8;  // 16-byte chunks per K row
-  if (!a_mn) {
+  const bool a_tm = a_mn == 2;
+  if (a_tm) {
+    // staged below, in tensor memory
+  } else if (!a_mn) {
     for (int i = tid; i < 128 * kc; i += 128) {
       const int m = i / kc, c = i % kc;
       const uint4 v = *reinterpret_cast<const uint4*>(A + (size_t)m * K + c * 8);
@@ -60,7 +64,7 @@ __global__ void __launch_bounds__(128)
     }
   }
   uint32_t ncols = 32;
-  while ((int)ncols < nn) ncols <<= 1;
+  while ((int)ncols < nn + (a_tm ? K / 2 : 0)) ncols <<= 1;
   if (tid == 0) {
     abort_flag = 0;
     mbar_init(&bar, 1);
@@ -72,11 +76,31 @@ __global__ void __launch_bounds__(128)
   __syncthreads();
   fence_after_sync();
   const uint32_t tm = tmem_base;
+  const uint32_t acol = (uint32_t)nn;  // A's columns follow D's
+  if (a_tm) {
+    // row tid of A: column c holds elements 2c (low half) and 2c + 1 (high half)
+    const uint32_t lane_addr = tm + ((uint32_t)(warp * 32) << 16) + acol;
+    for (int c0 = 0; c0 < K / 2; c0 += 8) {
+      uint32_t w[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const __nv_bfloat16 lo = A[(size_t)tid * K + 2 * (c0 + q)];
+        const __nv_bfloat16 hi = A[(size_t)tid * K + 2 * (c0 + q) + 1];
+        w[q] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+      }
+      tmem_st8u(lane_addr + c0, w);
+    }
+    tmem_wait_st();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+  }
   if (tid == 0) {
-    const uint32_t idesc = idesc_bf16(128, nn, a_mn, b_mn);
+    const uint32_t idesc = idesc_bf16(128, nn, a_tm ? 0 : a_mn, b_mn);
     for (int ks = 0; ks < K / 16; ++ks) {
-      uint64_t ad, bd;
-      if (!a_mn) {
+      uint64_t ad = 0, bd;
+      if (a_tm) {
+      } else if (!a_mn) {
         ad = sdesc(smem_u32(sA) + (ks / 4) * (128 * 128) + (ks % 4) * 32, 16, 1024);
       } else {
         const uint32_t panel = K * 128;
@@ -88,7 +112,8 @@ __global__ void __launch_bounds__(128)
         const uint32_t panel = K * 128;
         bd = sdesc(smem_u32(sB) + ks * 2048, swap_mn ? 1024 : panel, swap_mn ? panel : 1024);
       }
-      mma_bf16(tm, ad, bd, idesc, ks > 0 ? 1u : 0u);
+      if (a_tm) mma_bf16_ta(tm, tm + acol + ks * 8, bd, idesc, ks > 0 ? 1u : 0u);
+      else mma_bf16(tm, ad, bd, idesc, ks > 0 ? 1u : 0u);
     }
     mma_commit(&bar);
   }
@@ -118,6 +143,7 @@ extern "C" int ssd_selftest_mma(int a_mn, int b_mn, int swap_mn_offsets, int nn,
   if (!A || !B || !D) return SSD_ERR_INVALID_ARG;
   if (((uintptr_t)A | (uintptr_t)B) % 16) return SSD_ERR_INVALID_ARG;
   if (b_mn && nn % 64) return SSD_ERR_INVALID_ARG;
+  if (a_mn < 0 || a_mn > 2 || (a_mn == 2 && nn + k / 2 > 512)) return SSD_ERR_INVALID_ARG;
   int* status = ssd::device_status_ptr();
   if (!status) return SSD_ERR_CUDA;
   if (cudaFuncSetAttribute(ssd::k_selftest_mma, cudaFuncAttributeMaxDynamicSharedMemorySize,

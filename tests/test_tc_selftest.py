@@ -1,6 +1,7 @@
 """tcgen05 tile product against a CPU product (GPU): checks the shared-memory
 descriptor, instruction descriptor and TMEM conventions the tensor-core
-kernels rely on, for K-major and MN-major operands."""
+kernels rely on, for K-major and MN-major operands and for an A operand held
+in tensor memory (a_mn = 2)."""
 import ctypes
 
 import numpy as np
@@ -12,7 +13,8 @@ from state_space_model_sm_gb300.inputs import round_to_bf16
 pytestmark = pytest.mark.gpu
 
 CASES = [(0, 0, 64, 64), (0, 0, 256, 128), (0, 0, 128, 16), (1, 0, 64, 64), (0, 1, 128, 64),
-         (1, 1, 128, 128), (1, 1, 64, 32)]
+         (1, 1, 128, 128), (1, 1, 64, 32), (2, 0, 64, 64), (2, 0, 128, 128), (2, 1, 64, 64),
+         (2, 1, 128, 32)]
 
 
 @pytest.mark.parametrize("a_mn,b_mn,nn,k", CASES)
@@ -25,7 +27,7 @@ def test_tile_mma(cuda_lib, a_mn, b_mn, nn, k):
     tA = torch.from_numpy(A).to("cuda", torch.bfloat16)
     tB = torch.from_numpy(B).to("cuda", torch.bfloat16)
     results = {}
-    for swap in (0, 1) if (a_mn or b_mn) else (0,):
+    for swap in (0, 1) if (a_mn == 1 or b_mn) else (0,):
         D = torch.full((128, nn), float("nan"), device="cuda")
         st = _native.load().ssd_selftest_mma(a_mn, b_mn, swap, nn, k,
                                             ctypes.c_void_p(tA.data_ptr()),
