@@ -433,9 +433,18 @@ def cpu_baseline_sample(workload, min_seconds=10.0):
         if el >= min_seconds or reps >= 50:
             break
     tokens = reps * one.seqlen
+    # the same oracle on one host thread, one repetition
+    t1 = time.perf_counter()
+    oracle.ssd_fwd(*args, nthreads=1)
+    oracle.ssd_bwd(*args, dy, None, nthreads=1)
+    el1 = time.perf_counter() - t1
     return {"value": round(tokens / el, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{reps} x (batch row 0 of {workload}: seqlen {one.seqlen}, "
-                      f"{one.nheads} heads), fp64 forward + backward, {el:.1f} s"}
+                      f"{one.nheads} heads), fp64 forward + backward, {el:.1f} s; tokens/s "
+                      f"of the whole {shape.batch}-row workload extrapolated from these rows "
+                      f"(rows are independent and cost the same)",
+            "value_1core": round(one.seqlen / el1, 1),
+            "sample_1core": f"1 x the same batch row on 1 thread, {el1:.1f} s"}
 
 
 def run_reference(args, world, rank):
@@ -466,7 +475,8 @@ def run_reference(args, world, rank):
     el = time.perf_counter() - t0
     value = args.steps * one.seqlen / el
     sample = (f"per step: batch row 0 of {args.workload} (seqlen {one.seqlen}, "
-              f"{one.nheads} heads), fp64 forward + backward")
+              f"{one.nheads} heads), fp64 forward + backward; tokens/s extrapolated from "
+              f"1 of {shape.batch} batch rows (rows are independent and cost the same)")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

@@ -52,8 +52,12 @@ typedef enum {
   SSD_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement   */
   SSD_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than the size query   */
   SSD_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed            */
-  SSD_ERR_TIMEOUT = 5      /* a device-side bounded wait expired              */
+  SSD_ERR_TIMEOUT = 5,     /* a device-side bounded wait expired              */
+  SSD_ERR_NONFINITE = 6    /* an output holds NaN or Inf (opt-in check)       */
 } ssd_status;
+
+/* Bytes of the fixed scratch array behind ssd_fwd_noalloc (64 MiB). */
+#define SSD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 
@@ -107,8 +111,21 @@ int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
             float* dinit_states, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Synchronises `stream`, returns the device status word of the current
- * device (SSD_OK or SSD_ERR_TIMEOUT) and clears it. */
+ * device (SSD_OK, SSD_ERR_TIMEOUT or SSD_ERR_NONFINITE) and clears it.  The
+ * outputs of a call are only meaningful once this word reads SSD_OK: a
+ * kernel whose bounded wait expired skips the rest of its work. */
 int ssd_get_device_status(void* stream);
+
+/* Opt-in scan of every output for NaN / Inf ("End-to-end validation": no NaNs
+ * and no loss spikes).  With enable != 0, each later ssd_fwd, ssd_fwd_noalloc
+ * and ssd_bwd launches, after its kernels and on the same stream, one more
+ * kernel that reads every output it wrote (y, final_states; dx, ddt, dA, dB,
+ * dC and, when requested, dD, ddt_bias, dinit_states) and records
+ * SSD_ERR_NONFINITE in the device status word if any element is NaN or Inf
+ * (an earlier SSD_ERR_TIMEOUT is kept).  Read it with ssd_get_device_status.
+ * The scan reads the outputs once more (bandwidth-bound).  Process-wide;
+ * returns the previous setting.  Default: off. */
+int ssd_set_check_finite(int enable);
 
 /* Which kernel family the last ssd_fwd / ssd_bwd on this host thread used:
  * 0 = generic SIMT path, 1 = tcgen05 tensor-core path. */
@@ -133,14 +150,19 @@ int64_t ssd_launch_count(void);
  * device, a plugin that is handed only its tensors, or a latency-critical loop
  * that cannot afford cudaMalloc (which may synchronise the device) use it
  * instead of ssd_fwd.
- *   - Scratch: a fixed array of ssd_noalloc_scratch_bytes() bytes (64 MiB) of
- *     device memory inside the library, held on every GPU that loads the
- *     library until the process exits.  Shapes whose ssd_fwd_workspace_size()
- *     exceeds it return SSD_ERR_WORKSPACE; nothing is launched.
+ *   - Scratch: a fixed array of SSD_NOALLOC_SCRATCH_BYTES (64 MiB; also
+ *     ssd_noalloc_scratch_bytes()) of device memory inside the library, held
+ *     on every GPU that loads the library until the process exits.  Shapes
+ *     whose ssd_fwd_workspace_size() exceeds it return SSD_ERR_WORKSPACE;
+ *     nothing is launched.
+ *   - The scratch used is the one of the CURRENT device (cudaGetDevice), like
+ *     every other pointer argument: `stream` must belong to that device.
  *   - Inputs, outputs, results and errors are those of ssd_fwd.  It calls no
  *     cudaMalloc, cudaFree or other allocating routine.
- *   - The first call on each device looks up the scratch's device address
- *     (with that device current) and caches it; make that first call before
+ *   - The first call on each device (and the first after the device's
+ *     context changed, e.g. after cudaDeviceReset or under another driver
+ *     context) looks up the scratch's device address with that device
+ *     current and caches it with the context; make that first call before
  *     any stream capture.
  *   - Every call on a device shares the one scratch array and leaves the last
  *     call's intermediates in it: calls that overlap on the GPU (different

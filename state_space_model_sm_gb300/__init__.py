@@ -116,14 +116,29 @@ def _workspace(nbytes, device, workspace):
     return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
 
 
+def _raise_on_device_status(fn, device):
+    """Synchronise and raise SSDError if the device status word is set."""
+    torch = _torch()
+    st = int(_native.load().ssd_get_device_status(
+        ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)))
+    if st != 0:
+        raise SSDError(fn, st)
+
+
 def ssd_fwd(x, dt, dt_bias, A, B, C, D=None, chunk_size: int = 256, init_states=None,
             out_dtype=None, return_final_states: bool = True, workspace=None, y=None,
-            final_states=None):
+            final_states=None, check: bool = False):
     """y, final_states = SSD(x, dt, A, B, C, D, init_states) by the chunked scan.
 
     x (b, t, h, p), dt (b, t, h), B/C (b, t, g, n) in float32 or bfloat16 (one
     dtype for all four); dt_bias, A, D (h,) and init_states (b, h, p, n) float32.
-    y is float32 by default (``out_dtype=torch.bfloat16`` for bf16)."""
+    y is float32 by default (``out_dtype=torch.bfloat16`` for bf16).
+
+    The call is asynchronous: y and final_states are only meaningful once the
+    library's device status word reads 0 (``device_status()``), since a
+    kernel whose bounded wait expired skips its remaining work.  With
+    ``check=True`` the call synchronises and raises SSDError when the word is
+    set (a timeout, or NaN / Inf in an output when ``set_check_finite(True)``)."""
     torch = _torch()
     lib = _native.load()
     Bt, T, H, P, N, G = _validate(x, dt, dt_bias, A, B, C, D, init_states)
@@ -145,16 +160,20 @@ def ssd_fwd(x, dt, dt_bias, A, B, C, D=None, chunk_size: int = 256, init_states=
                      ctypes.c_size_t(ws.numel()), ctypes.c_void_p(stream))
     if st != 0:
         raise SSDError("ssd_fwd", st)
+    if check:
+        _raise_on_device_status("ssd_fwd", x.device)
     return y, (final_states if return_final_states else None)
 
 
 def ssd_bwd(x, dt, dt_bias, A, B, C, D, chunk_size: int, init_states, dy, dfinal_states=None,
-            workspace=None, out=None):
+            workspace=None, out=None, check: bool = False):
     """Gradients of <dy, y> + <dfinal, final> w.r.t. every input of ssd_fwd.
 
     Returns a dict with dx, ddt, dA, dB, dC (float32, shapes of the inputs)
     and dD, ddt_bias, dinit_states (when D / init_states are given; dD and
-    ddt_bias are always returned)."""
+    ddt_bias are always returned).  As for ssd_fwd, the gradients are only
+    meaningful once the device status word reads 0; ``check=True``
+    synchronises and raises SSDError otherwise."""
     torch = _torch()
     lib = _native.load()
     Bt, T, H, P, N, G = _validate(x, dt, dt_bias, A, B, C, D, init_states)
@@ -182,6 +201,8 @@ def ssd_bwd(x, dt, dt_bias, A, B, C, D, chunk_size: int, init_states, dy, dfinal
                      ctypes.c_void_p(stream))
     if st != 0:
         raise SSDError("ssd_bwd", st)
+    if check:
+        _raise_on_device_status("ssd_bwd", x.device)
     return out
 
 
@@ -358,6 +379,13 @@ def device_status(stream=None) -> int:
     torch = _torch()
     s = torch.cuda.current_stream().cuda_stream if stream is None else stream
     return int(_native.load().ssd_get_device_status(ctypes.c_void_p(s)))
+
+
+def set_check_finite(on: bool = True) -> bool:
+    """Turn the library's opt-in NaN / Inf scan of every output on or off
+    (process-wide); returns the previous setting.  A non-finite output shows
+    as status 6 (SSD_ERR_NONFINITE) in ``device_status()``."""
+    return bool(_native.load().ssd_set_check_finite(1 if on else 0))
 
 
 def last_path() -> int:

@@ -114,6 +114,7 @@ SIGNATURES = {
     "ssd_bwd": ([_SP] + [_VP] * 18 + [_VP, ctypes.c_size_t, _VP], ctypes.c_int),
     "ssd_get_device_status": ([_VP], ctypes.c_int),
     "ssd_last_path": ([], ctypes.c_int),
+    "ssd_set_check_finite": ([ctypes.c_int], ctypes.c_int),
     "ssd_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "ssd_profile_enable": ([ctypes.c_int], ctypes.c_int),
     "ssd_profile_read": ([ctypes.c_int, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),

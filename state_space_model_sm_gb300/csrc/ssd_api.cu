@@ -1,5 +1,6 @@
 // C ABI of libssd (declared in include/ssd.h): argument checks, workspace
 // carving and dispatch to the kernel families.
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 
@@ -8,6 +9,46 @@
 namespace ssd {
 
 __device__ int g_device_status = 0;
+
+namespace {
+
+std::atomic<int> g_check_finite{0};
+
+// Records SSD_ERR_NONFINITE in the status word when any of n values is NaN or
+// Inf (an earlier status is kept).  bf16 values are checked on their exponent
+// field directly.
+__global__ void k_check_finite(const void* p, int64_t n, int is_bf16, int* status) {
+  bool bad = false;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  if (is_bf16) {
+    const uint16_t* v = static_cast<const uint16_t*>(p);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+      bad |= (v[i] & 0x7F80u) == 0x7F80u;
+  } else {
+    const float* v = static_cast<const float*>(p);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+      bad |= !isfinite(v[i]);
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0)
+    atomicCAS(status, 0, (int)SSD_ERR_NONFINITE);
+}
+
+}  // namespace
+
+bool check_finite_enabled() { return g_check_finite.load(std::memory_order_relaxed) != 0; }
+
+cudaError_t launch_check_finite(const void* p, int64_t n, bool is_bf16, cudaStream_t s) {
+  if (!p || n <= 0) return cudaSuccess;
+  int* status = device_status_ptr();
+  if (!status) return cudaErrorUnknown;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (n + 255) / 256;
+  const int grid = (int)(want < 4LL * sms ? want : 4LL * sms);
+  SSD_LAUNCH("k_check_finite", s, k_check_finite<<<grid, 256, 0, s>>>(p, n, is_bf16, status));
+  return cudaGetLastError();
+}
 
 int* device_status_ptr() {
   void* p = nullptr;
@@ -177,6 +218,21 @@ FwdWs carve_fwd(char* base, const FwdOffsets& o) {
   return w;
 }
 
+// The opt-in scan of every gradient ssd_bwd wrote.
+cudaError_t check_bwd_outputs(const Dims& d, const BwdArgs& a, cudaStream_t s) {
+  if (!check_finite_enabled()) return cudaSuccess;
+  const int64_t tok = (int64_t)d.B * d.T;
+  const struct { const float* p; int64_t n; } outs[] = {
+      {a.dx, tok * d.H * d.P}, {a.ddt, tok * d.H},       {a.dA, d.H},
+      {a.dB, tok * d.G * d.N}, {a.dC, tok * d.G * d.N},   {a.dD, d.H},
+      {a.ddt_bias, d.H},       {a.dinit, (int64_t)d.B * d.H * d.P * d.N}};
+  for (const auto& o : outs) {
+    const cudaError_t e = launch_check_finite(o.p, o.n, false, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace
 }  // namespace ssd
 
@@ -241,7 +297,13 @@ int ssd_fwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
     w.Hprev = nullptr;
   }
   t_last_path = tc ? 1 : 0;
-  const cudaError_t e = tc ? tc_forward(d, a, w, s) : simt_forward(d, a, w, s);
+  cudaError_t e = tc ? tc_forward(d, a, w, s) : simt_forward(d, a, w, s);
+  if (e == cudaSuccess && check_finite_enabled()) {
+    const int64_t ny = (int64_t)d.B * d.T * d.H * d.P;
+    e = launch_check_finite(y, ny, d.out_bf16, s);
+    if (e == cudaSuccess)
+      e = launch_check_finite(final_states, (int64_t)d.B * d.H * d.P * d.N, false, s);
+  }
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
@@ -301,7 +363,8 @@ int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
     w.part = reinterpret_cast<float*>(base + o.part);
     w.seg = o.total > o.seg ? reinterpret_cast<float*>(base + o.seg) : nullptr;
     t_last_path = 1;
-    return tc_backward(d, a, w, s) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    if (tc_backward(d, a, w, s) != cudaSuccess) return SSD_ERR_CUDA;
+    return check_bwd_outputs(d, a, s) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
   }
   const BwdOffsets o = bwd_offsets(d);
   if (!workspace || workspace_bytes < o.total || !aligned(workspace, kAlign))
@@ -320,7 +383,8 @@ int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
   w.dCh = reinterpret_cast<float*>(base + o.dCh);
   w.part = reinterpret_cast<float*>(base + o.part);
   t_last_path = 0;
-  return simt_backward(d, a, w, s) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+  if (simt_backward(d, a, w, s) != cudaSuccess) return SSD_ERR_CUDA;
+  return check_bwd_outputs(d, a, s) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
 int ssd_fwd_final_state(const ssd_shape* shape, const void* x, const void* dt,
@@ -397,6 +461,8 @@ int ssd_get_device_status(void* stream) {
 
 int ssd_last_path(void) { return t_last_path; }
 
+int ssd_set_check_finite(int enable) { return g_check_finite.exchange(enable ? 1 : 0); }
+
 const char* ssd_strerror(int status) {
   switch (status) {
     case SSD_OK: return "ok";
@@ -405,6 +471,7 @@ const char* ssd_strerror(int status) {
     case SSD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case SSD_ERR_CUDA: return "CUDA runtime or launch error";
     case SSD_ERR_TIMEOUT: return "device-side bounded wait timed out";
+    case SSD_ERR_NONFINITE: return "an output holds NaN or Inf";
     default: return "unknown status";
   }
 }

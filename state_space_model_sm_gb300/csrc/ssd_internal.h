@@ -19,6 +19,11 @@ struct Dims {
 // ssd_api.cu).  Kernels whose bounded waits expire store SSD_ERR_TIMEOUT there.
 int* device_status_ptr();
 
+// The opt-in NaN / Inf scan of outputs (ssd_set_check_finite): whether it is
+// on, and one scan launch over n values (f32, or bf16 when is_bf16).
+bool check_finite_enabled();
+cudaError_t launch_check_finite(const void* p, int64_t n, bool is_bf16, cudaStream_t s);
+
 // Brackets one kernel launch: counts it and, when profiling is enabled,
 // records CUDA events around it on the launch stream (ssd_profile.cu).
 class LaunchScope {

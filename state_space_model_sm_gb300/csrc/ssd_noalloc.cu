@@ -6,6 +6,9 @@
 // the device and take milliseconds.  This entry point needs no workspace from
 // them: its scratch lives in one file-scope device array of fixed size that
 // the library holds on every GPU that loads it, until the process exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "ssd_internal.h"
@@ -13,27 +16,54 @@
 namespace {
 
 // The fixed scratch: large enough for the forward workspace of small and
-// medium problems (see SSD_NOALLOC_SCRATCH_BYTES in ssd.h).
-constexpr size_t kScratchBytes = (size_t)64 << 20;
+// medium problems (SSD_NOALLOC_SCRATCH_BYTES in ssd.h).
+constexpr size_t kScratchBytes = SSD_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct Cached {
+  CUcontext ctx;
+  void* addr;
+};
+Cached g_cache[kMaxDevices] = {};
+
+// The driver context current on this thread (null if the query is unavailable).
+CUcontext current_context() {
+  static PFN_cuCtxGetCurrent_v4000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuCtxGetCurrent_v4000>(nullptr);
+    return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+  }();
+  CUcontext c = nullptr;
+  if (fn) fn(&c);
+  return c;
+}
 
 // Device address of the scratch on the current device.  In host code the
-// array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+// array's name is only a host-side stand-in, so the address is looked up with
+// the device current, once per device and driver context, and cached with
+// the context: after cudaDeviceReset, or under another context, it is looked
+// up again instead of reusing an address of a context that is gone.
 int scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSD_ERR_CUDA;
+  const CUcontext ctx = current_context();
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_addr[dev]) {
+  Cached& c = g_cache[dev];
+  if (!c.addr || !ctx || c.ctx != ctx) {
+    // (the lookup also makes the device's primary context current if this
+    // thread had none, so the context is read again after it)
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SSD_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    c.addr = p;
+    c.ctx = current_context();
   }
-  *out = g_scratch_addr[dev];
+  *out = c.addr;
   return SSD_OK;
 }
 

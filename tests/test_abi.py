@@ -39,9 +39,24 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(6):
-        assert lib.ssd_strerror(code)
+    for code in range(7):
+        assert lib.ssd_strerror(code) and lib.ssd_strerror(code) != b"unknown status"
+    assert b"NaN" in lib.ssd_strerror(6)   # SSD_ERR_NONFINITE
     assert lib.ssd_strerror(99) == b"unknown status"
+
+
+def test_check_finite_setting_round_trips(lib):
+    # host-only: the process-wide switch of the opt-in NaN / Inf output scan
+    assert lib.ssd_set_check_finite(1) == 0
+    assert lib.ssd_set_check_finite(0) == 1
+    assert ssd.set_check_finite(False) is False
+
+
+def test_noalloc_scratch_size_matches_header_macro(lib):
+    text = open(os.path.join(ROOT, "include", "ssd.h")).read()
+    m = re.search(r"#define SSD_NOALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", text)
+    assert m, "SSD_NOALLOC_SCRATCH_BYTES missing from ssd.h"
+    assert lib.ssd_noalloc_scratch_bytes() == int(m.group(1)) << int(m.group(2))
 
 
 def shape(**kw):

@@ -113,6 +113,37 @@ def test_forward_single_token_by_hand():
         assert close(y[0, 0, h], yh)
 
 
+def test_softplus_linear_branch_above_20():
+    """softplus(v) = v exactly for v > 20, log1p(exp(v)) at and below (the
+    convention both sides share).  One token with N = P = 1, x = B = C = 1,
+    D = 0 and no initial state gives y = final = delta, and with dy = 1 the
+    gradient ddt = softplus'(v): exactly 1 above 20, sigmoid(v) below.  At
+    v = 25 the two branches differ by 1.4e-11 (delta) and 1.4e-11 (slope), at
+    v = 19 by 5.6e-9, so a threshold on the wrong side of either value fails."""
+    v = np.array([25.0, 19.0, 20.0])
+    x = np.ones((1, 1, 3, 1))
+    dt = v.reshape(1, 1, 3)
+    dt_bias = np.zeros(3)
+    A = -np.ones(3)
+    Bm = np.ones((1, 1, 1, 1))
+    Cm = np.ones((1, 1, 1, 1))
+    y, final = oracle.ssd_fwd(x, dt, dt_bias, A, Bm, Cm, np.zeros(3), None)
+    expect = np.array([25.0, np.log1p(np.exp(19.0)), np.log1p(np.exp(20.0))])
+    assert y[0, 0, 0, 0] == 25.0                       # linear branch, exactly
+    assert abs(y[0, 0, 1, 0] - expect[1]) < 1e-15 * expect[1] and y[0, 0, 1, 0] != 19.0
+    assert abs(y[0, 0, 2, 0] - expect[2]) < 1e-15 * expect[2]
+    assert np.array_equal(final.reshape(3), y.reshape(3))
+    g = oracle.ssd_bwd(x, dt, dt_bias, A, Bm, Cm, np.zeros(3), None, np.ones((1, 1, 3, 1)))
+    assert g["ddt"][0, 0, 0] == 1.0                    # slope of the linear branch
+    sig = 1.0 / (1.0 + np.exp(-np.array([19.0, 20.0])))
+    assert np.allclose(g["ddt"][0, 0, 1:], sig, rtol=1e-15, atol=0)
+    assert g["ddt"][0, 0, 1] != 1.0
+    # the chunked numpy oracle uses the same convention
+    assert chunked.softplus(25.0) == 25.0 and chunked.softplus_grad(25.0) == 1.0
+    assert chunked.softplus(19.0) == np.log1p(np.exp(19.0))
+    assert chunked.softplus_grad(19.0) == sig[0]
+
+
 def test_forward_initial_state_only():
     x, dt, dt_bias, A, Bm, Cm, D, init = rand_problem(G=2)
     x = np.zeros_like(x)

@@ -10,7 +10,8 @@ import ctypes
 import numpy as np
 import pytest
 
-from parity_util import stats, to_np
+import oracle
+from parity_util import assert_close, stats, to_np
 from state_space_model_sm_gb300 import _native
 from state_space_model_sm_gb300.inputs import SSDShape, make_inputs, to_torch
 
@@ -61,6 +62,10 @@ def test_noalloc_matches_workspace_forward_on_consecutive_calls(cuda_lib):
             s = stats(to_np(got), to_np(ref))
             assert np.isfinite(to_np(got)).all()
             assert s["rel_l2"] <= tol and (inp.dtype == "f32" or s["max_abs"] <= 2e-2), s
+        # and against the CPU oracle itself, at the library's parity bars
+        y_or, f_or = oracle.ssd_fwd(*oracle.from_inputs(inp))
+        assert_close("y", to_np(y), y_or, inp.dtype)
+        assert_close("final", to_np(final), f_or, inp.dtype)
     assert cuda_lib.device_status() == 0
 
 
