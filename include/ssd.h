@@ -308,6 +308,32 @@ int ssd_gated_norm_set_config(const ssd_norm_shape* shape, const ssd_norm_config
  * table entry exists, 0 if not, -SSD_ERR_INVALID_ARG for a bad shape. */
 int ssd_gated_norm_get_config(const ssd_norm_shape* shape, ssd_norm_config* out);
 
+/* Launch table of the SSD chunk kernels (the tensor-core path), the SSD side
+ * of the offline config generator of "Cutting autotuning overhead with an
+ * automated config generator" (Fig. 4): a sweep finds the best launch per
+ * shape ahead of time, and the table is applied when the library loads.
+ *   scan_head_blocks: chunk_scan CTAs per (batch, chunk, row tile, group)
+ *     split the group's heads into this many blocks;
+ *   bc_head_blocks: the same for the dC and dB kernels, whose per-block
+ *     partial sums live in the ssd_bwd workspace (so this field changes
+ *     ssd_bwd_workspace_size: query the size after setting the table).
+ * 0 keeps the built-in rule (the fewest blocks giving two CTAs per SM); a
+ * nonzero value must divide nheads / ngroups and be at most 32. */
+typedef struct {
+  int32_t scan_head_blocks, bc_head_blocks;
+} ssd_scan_config;
+
+/* Sets (config != NULL) or removes (NULL) the entry of shape's (batch,
+ * seqlen, nheads, headdim, dstate, ngroups, chunk_size).  Thread-safe; at
+ * most 64 entries (else SSD_ERR_UNSUPPORTED); SSD_ERR_INVALID_ARG for an
+ * invalid shape or field. */
+int ssd_scan_set_config(const ssd_shape* shape, const ssd_scan_config* config);
+
+/* The head blocks the next ssd_fwd / ssd_bwd with this shape will use (the
+ * table's where set, the built-in rule's elsewhere) in *out.  Returns 1 if a
+ * table entry exists, 0 if not, -SSD_ERR_INVALID_ARG for a bad shape. */
+int ssd_scan_get_config(const ssd_shape* shape, ssd_scan_config* out);
+
 /* Diagnostic: one tcgen05 tile product on the current device,
  * D[128][nn] = A[128][k] * B[nn][k]^T (A, B bf16 row-major, D f32 row-major,
  * all device memory), with A and B staged in shared memory K-major (0) or

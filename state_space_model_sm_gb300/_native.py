@@ -98,6 +98,10 @@ class NormShape(ctypes.Structure):
                 ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32)]
 
 
+class ScanConfig(ctypes.Structure):
+    _fields_ = [("scan_head_blocks", ctypes.c_int32), ("bc_head_blocks", ctypes.c_int32)]
+
+
 class NormConfig(ctypes.Structure):
     _fields_ = [("rows_per_item", ctypes.c_int32), ("ring_kb", ctypes.c_int32),
                 ("ctas_per_sm", ctypes.c_int32)]
@@ -115,6 +119,8 @@ SIGNATURES = {
     "ssd_get_device_status": ([_VP], ctypes.c_int),
     "ssd_last_path": ([], ctypes.c_int),
     "ssd_set_check_finite": ([ctypes.c_int], ctypes.c_int),
+    "ssd_scan_set_config": ([_SP, ctypes.POINTER(ScanConfig)], ctypes.c_int),
+    "ssd_scan_get_config": ([_SP, ctypes.POINTER(ScanConfig)], ctypes.c_int),
     "ssd_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "ssd_profile_enable": ([ctypes.c_int], ctypes.c_int),
     "ssd_profile_read": ([ctypes.c_int, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),

@@ -3,6 +3,7 @@
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "ssd_internal.h"
 
@@ -36,6 +37,55 @@ __global__ void k_check_finite(const void* p, int64_t n, int is_bf16, int* statu
 }  // namespace
 
 bool check_finite_enabled() { return g_check_finite.load(std::memory_order_relaxed) != 0; }
+
+// ------------------------------------------------------ launch-config table
+namespace {
+struct ScanEntry {
+  int B, T, H, P, N, G, L;
+  ssd_scan_config cfg;
+};
+constexpr int kMaxScanEntries = 64;
+ScanEntry g_scan_table[kMaxScanEntries];
+int g_scan_entries = 0;
+std::mutex g_scan_mu;
+
+bool same_shape(const ScanEntry& e, const Dims& d) {
+  return e.B == d.B && e.T == d.T && e.H == d.H && e.P == d.P && e.N == d.N && e.G == d.G &&
+         e.L == d.L;
+}
+
+// the built-in rule: the fewest head blocks per group that still give >= 2
+// CTAs per SM (the count of the GPU the tables were made on)
+int rule_nblk(const Dims& d) {
+  const int hpg = d.H / d.G;
+  const int64_t units = (int64_t)d.B * d.nc * (d.L / 128) * d.G;
+  for (int nb = 1; nb <= hpg; ++nb)
+    if (hpg % nb == 0 && units * nb >= 2 * 152) return nb;
+  return hpg;
+}
+
+bool scan_lookup(const Dims& d, ssd_scan_config* out) {
+  std::lock_guard<std::mutex> lk(g_scan_mu);
+  for (int i = 0; i < g_scan_entries; ++i)
+    if (same_shape(g_scan_table[i], d)) {
+      *out = g_scan_table[i].cfg;
+      return true;
+    }
+  return false;
+}
+}  // namespace
+
+int tc_scan_nblk(const Dims& d) {
+  ssd_scan_config c;
+  if (scan_lookup(d, &c) && c.scan_head_blocks > 0) return c.scan_head_blocks;
+  return rule_nblk(d);
+}
+
+int tc_bwd_nblk(const Dims& d) {
+  ssd_scan_config c;
+  if (scan_lookup(d, &c) && c.bc_head_blocks > 0) return c.bc_head_blocks;
+  return rule_nblk(d);
+}
 
 cudaError_t launch_check_finite(const void* p, int64_t n, bool is_bf16, cudaStream_t s) {
   if (!p || n <= 0) return cudaSuccess;
@@ -158,11 +208,11 @@ struct TcBwdOffsets {
       dCp, part, seg, total;
 };
 
-TcBwdOffsets tc_bwd_offsets(const Dims& d) {
+TcBwdOffsets tc_bwd_offsets(const Dims& d, int nblk) {
   Carver c;
   const size_t vec = (size_t)d.B * d.H * d.nc * d.L * sizeof(float);
   const size_t st = (size_t)d.B * d.nc * d.H * d.P * d.N * sizeof(float);
-  const size_t bp = (size_t)d.B * d.T * d.G * tc_bwd_nblk(d) * d.N * sizeof(float);
+  const size_t bp = (size_t)d.B * d.T * d.G * nblk * d.N * sizeof(float);
   TcBwdOffsets o;
   o.delta = c.take(vec);
   o.acs = c.take(vec);
@@ -251,7 +301,7 @@ size_t ssd_bwd_workspace_size(const ssd_shape* shape) {
   if (make_dims(shape, &d) != SSD_OK) return 0;
   size_t total = bwd_offsets(d).total;
   if (tc_forward_supported(d)) {
-    const size_t t = tc_bwd_offsets(d).total;
+    const size_t t = tc_bwd_offsets(d, tc_bwd_nblk(d)).total;
     if (t > total) total = t;
   }
   return total;
@@ -341,7 +391,8 @@ int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
                   aligned(dC, 16) && aligned(init_states, 16) && aligned(dfinal_states, 16) &&
                   aligned(dinit_states, 16);
   if (tc) {
-    const TcBwdOffsets o = tc_bwd_offsets(d);
+    const int nblk = tc_bwd_nblk(d);  // once: the layout and the launch must agree
+    const TcBwdOffsets o = tc_bwd_offsets(d, nblk);
     if (!workspace || workspace_bytes < o.total || !aligned(workspace, kAlign))
       return SSD_ERR_WORKSPACE;
     TcBwdWs w;
@@ -362,6 +413,7 @@ int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
     w.dCp = reinterpret_cast<float*>(base + o.dCp);
     w.part = reinterpret_cast<float*>(base + o.part);
     w.seg = o.total > o.seg ? reinterpret_cast<float*>(base + o.seg) : nullptr;
+    w.nblk = nblk;
     t_last_path = 1;
     if (tc_backward(d, a, w, s) != cudaSuccess) return SSD_ERR_CUDA;
     return check_bwd_outputs(d, a, s) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
@@ -462,6 +514,39 @@ int ssd_get_device_status(void* stream) {
 int ssd_last_path(void) { return t_last_path; }
 
 int ssd_set_check_finite(int enable) { return g_check_finite.exchange(enable ? 1 : 0); }
+
+int ssd_scan_set_config(const ssd_shape* shape, const ssd_scan_config* config) {
+  Dims d;
+  if (make_dims(shape, &d) != SSD_OK) return SSD_ERR_INVALID_ARG;
+  if (config) {
+    const int hpg = d.H / d.G;
+    for (const int v : {config->scan_head_blocks, config->bc_head_blocks})
+      if (v < 0 || v > 32 || (v > 0 && hpg % v != 0)) return SSD_ERR_INVALID_ARG;
+  }
+  std::lock_guard<std::mutex> lk(g_scan_mu);
+  int i = 0;
+  while (i < g_scan_entries && !same_shape(g_scan_table[i], d)) ++i;
+  if (!config) {  // remove
+    if (i < g_scan_entries) g_scan_table[i] = g_scan_table[--g_scan_entries];
+    return SSD_OK;
+  }
+  if (i == g_scan_entries) {
+    if (g_scan_entries == kMaxScanEntries) return SSD_ERR_UNSUPPORTED;
+    ++g_scan_entries;
+  }
+  g_scan_table[i] = ScanEntry{d.B, d.T, d.H, d.P, d.N, d.G, d.L, *config};
+  return SSD_OK;
+}
+
+int ssd_scan_get_config(const ssd_shape* shape, ssd_scan_config* out) {
+  Dims d;
+  if (!out || make_dims(shape, &d) != SSD_OK) return -SSD_ERR_INVALID_ARG;
+  ssd_scan_config c{0, 0};
+  const bool set = scan_lookup(d, &c);
+  out->scan_head_blocks = tc_scan_nblk(d);
+  out->bc_head_blocks = tc_bwd_nblk(d);
+  return set ? 1 : 0;
+}
 
 const char* ssd_strerror(int status) {
   switch (status) {

@@ -158,15 +158,19 @@ struct TcBwdWs {
   float* dCp;     // (B, T, G, nblk, N)
   float* part;    // (B, H, nc, 3)
   float* seg;     // two-level state passing scratch, or nullptr
+  int nblk;       // head blocks of dB / dC (read from the launch table once per call)
 };
 
 // tcgen05 path (ssd_tc.cu): bf16 inputs, headdim 64, d_state 64 / 128,
 // chunk 128 / 256, an even number of heads per group.
 bool tc_forward_supported(const Dims& d);
 cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s);
-// Head blocks per group of the dB / dC kernels (a function of the shape only,
-// so the workspace size and the launch always agree).
+// Head blocks per group of the dB / dC kernels and of chunk_scan: the launch
+// table's entry for the shape (ssd_scan_set_config), else the built-in rule.
+// The workspace size and the launch read the same table, so they agree as
+// long as the entry does not change between the size query and the call.
 int tc_bwd_nblk(const Dims& d);
+int tc_scan_nblk(const Dims& d);
 cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w, cudaStream_t s);
 
 // The TMA-fed chunk kernels (ssd_chunk_tc.cu), over (batch, chunk, row tile,

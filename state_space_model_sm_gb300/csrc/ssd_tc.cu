@@ -869,7 +869,7 @@ cudaError_t launch_tc_forward_t(const Dims& d, const FwdArgs& a, const FwdWs& w,
                                 int* status, int sms) {
   launch_state_front<N, L>(d, a, w, s, status, sms);  // chunk_cumsum runs inside chunk_state
   simt_state_passing(d, a, w, s);
-  const cudaError_t e = tc_chunk_forward(d, a, w, tc_bwd_nblk(d), s);
+  const cudaError_t e = tc_chunk_forward(d, a, w, tc_scan_nblk(d), s);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -905,7 +905,7 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
         static_cast<const unsigned char*>(w.dSimg), a.f.D, a.dx, w.ddir, w.qrow, w.ddiag, d.B, d.T,
         d.H, d.G, d.nc, per, status));
   }
-  const int nblk = tc_bwd_nblk(d);
+  const int nblk = w.nblk;
   float* dCout = nblk == 1 ? a.dC : w.dCp;
   float* dBout = nblk == 1 ? a.dB : w.dBp;
   {
@@ -936,14 +936,6 @@ bool tc_forward_supported(const Dims& d) {
          (d.H / d.G) % 2 == 0;
 }
 
-int tc_bwd_nblk(const Dims& d) {
-  // fewest head blocks per group that still give >= 2 x 152 CTAs
-  const int hpg = d.H / d.G;
-  const int64_t units = (int64_t)d.B * d.nc * (d.L / 128) * d.G;
-  for (int nb = 1; nb <= hpg; ++nb)
-    if (hpg % nb == 0 && units * nb >= 2 * 152) return nb;
-  return hpg;
-}
 
 cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
   int* status = device_status_ptr();

@@ -1,4 +1,4 @@
-"""Offline launch-configuration table for the gated-norm kernels.
+"""Offline launch-configuration tables for the gated-norm and SSD chunk kernels.
 
 The pages' config generator ("Cutting autotuning overhead with an automated
 config generator", Fig. 4) separates the search from the run: the best
@@ -17,6 +17,13 @@ file, and loaded when training starts.  The same split here:
 
 The parameters (``ssd_norm_config`` in ``include/ssd.h``): rows per CTA work
 item, the shared-memory ring size aimed at, and the persistent CTAs per SM.
+
+The SSD chunk kernels have a table of their own (``ssd_scan_config``): how
+many blocks of heads the chunk_scan and the dC / dB CTAs split each group
+into.  ``sweep_scan`` times the forward + backward step of a workload for each
+candidate, ``--sweep-scan W[,W...] --out`` writes the table, and the packaged
+``tuning_tables/ssd_scan_gb300.json`` is applied at load like the norm's
+(``SSD_SCAN_TABLE`` names another table or ``none``).
 """
 from __future__ import annotations
 
@@ -31,6 +38,11 @@ from . import _native
 TABLE_KIND = "gated_norm_launch_table"
 DEFAULT_TABLE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "tuning_tables",
                              "gated_norm_gb300.json")
+SCAN_TABLE_KIND = "ssd_scan_launch_table"
+DEFAULT_SCAN_TABLE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "tuning_tables",
+                                  "ssd_scan_gb300.json")
+_SCAN_KEYS = ("batch", "seqlen", "nheads", "headdim", "dstate", "ngroups", "chunk_size")
+_SCAN_FIELDS = ("scan_head_blocks", "bc_head_blocks")
 _DTYPES = {"f32": 0, "bf16": 1}
 _FIELDS = ("rows_per_item", "ring_kb", "ctas_per_sm")
 
@@ -114,15 +126,153 @@ def apply_table(table: dict, lib=None) -> int:
 
 
 def apply_default(lib) -> Optional[str]:
-    """Called once when the library is loaded: applies the table named by
-    SSD_TUNING_TABLE (``none``: no table), else the packaged one if present.
-    Returns the path applied, or None."""
+    """Called once when the library is loaded: applies the norm table named by
+    SSD_TUNING_TABLE (``none``: no table), else the packaged one if present,
+    and likewise the SSD chunk-kernel table (SSD_SCAN_TABLE).  Returns the
+    norm table's path, or None."""
+    scan_path = os.environ.get("SSD_SCAN_TABLE", DEFAULT_SCAN_TABLE)
+    if scan_path.lower() != "none" and os.path.exists(scan_path):
+        with open(scan_path) as f:
+            apply_scan_table(json.load(f), lib=lib)
     path = os.environ.get("SSD_TUNING_TABLE", DEFAULT_TABLE)
     if path.lower() == "none" or not os.path.exists(path):
         return None
     with open(path) as f:
         apply_table(json.load(f), lib=lib)
     return path
+
+
+# ------------------------------------------------------ SSD chunk kernels
+def _scan_shape(e: dict):
+    return _native.Shape(*(int(e[k]) for k in _SCAN_KEYS), 1, 0)
+
+
+def validate_scan_table(table: dict) -> None:
+    """Raises ValueError unless ``table`` is a well-formed SSD launch table
+    (field ranges as ``ssd_scan_set_config`` accepts them)."""
+    if table.get("kind") != SCAN_TABLE_KIND:
+        raise ValueError(f"not a {SCAN_TABLE_KIND}")
+    entries = table.get("entries")
+    if not isinstance(entries, list) or len(entries) > 64:
+        raise ValueError("entries must be a list of at most 64")
+    seen = set()
+    for e in entries:
+        for k in _SCAN_KEYS + _SCAN_FIELDS:
+            if k not in e:
+                raise ValueError(f"entry misses {k!r}: {e}")
+        H, G = int(e["nheads"]), int(e["ngroups"])
+        if min(int(e[k]) for k in _SCAN_KEYS) < 1 or H % G:
+            raise ValueError(f"bad shape in {e}")
+        for k in _SCAN_FIELDS:
+            v = int(e[k])
+            if v < 0 or v > 32 or (v > 0 and (H // G) % v):
+                raise ValueError(f"bad {k} in {e}")
+        key = tuple(int(e[k]) for k in _SCAN_KEYS)
+        if key in seen:
+            raise ValueError(f"duplicate entry {key}")
+        seen.add(key)
+
+
+def set_scan_config(shape: dict, scan_head_blocks=0, bc_head_blocks=0, lib=None) -> None:
+    """Sets the table entry of one SSD shape (``shape``: the _SCAN_KEYS);
+    zero fields keep the built-in rule."""
+    lib = lib or _native.load()
+    cfg = _native.ScanConfig(int(scan_head_blocks), int(bc_head_blocks))
+    st = lib.ssd_scan_set_config(ctypes.byref(_scan_shape(shape)), ctypes.byref(cfg))
+    if st != 0:
+        raise ValueError(f"ssd_scan_set_config: status {st}")
+
+
+def clear_scan_config(shape: dict, lib=None) -> None:
+    lib = lib or _native.load()
+    st = lib.ssd_scan_set_config(ctypes.byref(_scan_shape(shape)), None)
+    if st != 0:
+        raise ValueError(f"ssd_scan_set_config: status {st}")
+
+
+def get_scan_config(shape: dict, lib=None):
+    """(head blocks the next call will use, True if they come from the table)."""
+    lib = lib or _native.load()
+    cfg = _native.ScanConfig()
+    st = lib.ssd_scan_get_config(ctypes.byref(_scan_shape(shape)), ctypes.byref(cfg))
+    if st < 0:
+        raise ValueError(f"ssd_scan_get_config: status {-st}")
+    return {k: int(getattr(cfg, k)) for k in _SCAN_FIELDS}, st == 1
+
+
+def apply_scan_table(table: dict, lib=None) -> int:
+    validate_scan_table(table)
+    for e in table["entries"]:
+        set_scan_config({k: e[k] for k in _SCAN_KEYS}, e["scan_head_blocks"],
+                        e["bc_head_blocks"], lib=lib)
+    return len(table["entries"])
+
+
+def sweep_scan(workload: str, steps: int = 10, warmup: int = 3, max_blocks: int = 12) -> dict:
+    """Times the forward + backward step of a workload (CUDA events, a 512 MB
+    L2 flush before each step) for every head-block count of chunk_scan, then
+    of dC / dB with chunk_scan's best, on the current GPU; returns the best
+    entry with the built-in rule's time."""
+    import torch
+
+    from . import ssd_bwd, ssd_fwd
+    from .inputs import WORKLOADS, make_inputs, to_torch
+    lib = _native.load()
+    shape, dtype, init_std, seed, _ = WORKLOADS[workload]
+    inp = make_inputs(shape, seed=seed, dtype=dtype, init_std=init_std, with_dy=True)
+    s = inp.shape
+    key = dict(batch=s.batch, seqlen=s.seqlen, nheads=s.nheads, headdim=s.headdim,
+               dstate=s.dstate, ngroups=s.ngroups, chunk_size=s.chunk_size)
+    t = to_torch(inp)
+    dev = t["x"].device
+    flush = torch.empty(512 * 1024 * 1024 // 4, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ssd_fwd(t["x"], t["dt"], t["dt_bias"], t["A"], t["B"], t["C"], t["D"],
+                chunk_size=s.chunk_size, init_states=t["init"])
+        ssd_bwd(t["x"], t["dt"], t["dt_bias"], t["A"], t["B"], t["C"], t["D"], s.chunk_size,
+                t["init"], t["dy"], t["dfinal"])
+
+    def time_us():
+        for _ in range(warmup):
+            step()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for a, b in ev:
+            flush.fill_(1.0)
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return 1e3 * sum(a.elapsed_time(b) for a, b in ev) / steps
+
+    hpg = s.nheads // s.ngroups
+    blocks = [nb for nb in range(1, min(hpg, max_blocks) + 1) if hpg % nb == 0]
+    saved, had = get_scan_config(key, lib=lib)
+    clear_scan_config(key, lib=lib)
+    default_cfg, _ = get_scan_config(key, lib=lib)
+    default_us = time_us()
+    timings = []
+    try:
+        scan_t = []
+        for nb in blocks:
+            set_scan_config(key, nb, default_cfg["bc_head_blocks"], lib=lib)
+            scan_t.append((time_us(), nb))
+        best_scan = min(scan_t)[1]
+        for nb in blocks:
+            set_scan_config(key, best_scan, nb, lib=lib)
+            timings.append((time_us(), dict(scan_head_blocks=best_scan, bc_head_blocks=nb)))
+    finally:
+        if had:
+            set_scan_config(key, saved["scan_head_blocks"], saved["bc_head_blocks"], lib=lib)
+        else:
+            clear_scan_config(key, lib=lib)
+    best_us, best = min(timings, key=lambda x: x[0])
+    return dict(**key, **best, workload=workload, tuned_us=round(best_us, 2),
+                default_us=round(default_us, 2), default=default_cfg,
+                scan_sweep={str(nb): round(us, 2) for us, nb in scan_t},
+                bc_sweep={str(c["bc_head_blocks"]): round(us, 2) for us, c in timings})
 
 
 def candidates(features: int) -> Iterable[dict]:
@@ -196,13 +346,33 @@ def sweep_gated_norm(features: int, group_size: int, dtype: str = "bf16", rows: 
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("--sweep", required=True,
+    ap.add_argument("--sweep", default=None,
                     help="comma-separated features:group_size shapes, e.g. 4096:512,1536:1536")
+    ap.add_argument("--sweep-scan", default=None,
+                    help="comma-separated SSD workloads, e.g. layer_fwdbwd_bf16,hybrid_bf16")
     ap.add_argument("--dtype", default="bf16", choices=sorted(_DTYPES))
     ap.add_argument("--rows", type=int, default=16384)
     ap.add_argument("--out", required=True)
     args = ap.parse_args(argv)
     import torch
+    if args.sweep_scan:
+        os.environ.setdefault("SSD_SCAN_TABLE", "none")
+        entries = []
+        for w in args.sweep_scan.split(","):
+            e = sweep_scan(w)
+            print(json.dumps(e))
+            entries.append(e)
+        table = {"kind": SCAN_TABLE_KIND, "gpu": torch.cuda.get_device_name(),
+                 "sms": torch.cuda.get_device_properties(0).multi_processor_count,
+                 "generated_by": "SSD_SCAN_TABLE=none python -m state_space_model_sm_gb300.tuning "
+                                 "--sweep-scan " + args.sweep_scan + " --out <table>",
+                 "entries": entries}
+        validate_scan_table(table)
+        with open(args.out, "w") as f:
+            json.dump(table, f, indent=1)
+        return
+    if not args.sweep:
+        ap.error("--sweep or --sweep-scan is required")
     entries = []
     for item in args.sweep.split(","):
         F, G = (int(v) for v in item.split(":"))

@@ -1,7 +1,7 @@
-"""The gated-norm launch table: validation, the per-shape table inside the
-library (set / get / remove through the C ABI, host-only calls that need no
-GPU), the packaged table, and on the GPU that a tuned launch computes the
-same result as the built-in one."""
+"""The launch tables of the gated-norm and the SSD chunk kernels: validation,
+the per-shape tables inside the library (set / get / remove through the C
+ABI, host-only calls that need no GPU), the packaged tables, and on the GPU
+that a tuned launch computes the same result as the built-in one."""
 import json
 import os
 
@@ -143,3 +143,119 @@ def test_tuned_launch_computes_the_same(cuda_lib, F, G, cfg):
     np.testing.assert_allclose(b[2]["dw"].cpu().numpy(), a[2]["dw"].cpu().numpy(), rtol=1e-5,
                                atol=1e-5)
     assert cuda_lib.device_status() == 0
+
+
+# ------------------------------------------------------ SSD chunk kernels
+_SSD_KEY = dict(batch=2, seqlen=1000, nheads=12, headdim=64, dstate=128, ngroups=2,
+                chunk_size=128)
+
+
+def _scan_table(*entries):
+    return {"kind": tuning.SCAN_TABLE_KIND, "entries": list(entries)}
+
+
+def _scan_entry(**kw):
+    e = dict(_SSD_KEY, scan_head_blocks=3, bc_head_blocks=2)
+    e.update(kw)
+    return e
+
+
+def test_scan_validate():
+    tuning.validate_scan_table(_scan_table(_scan_entry(), _scan_entry(seqlen=2000)))
+    for bad in (dict(scan_head_blocks=4), dict(bc_head_blocks=-1), dict(bc_head_blocks=33),
+                dict(ngroups=5), dict(headdim=0)):
+        with pytest.raises(ValueError):
+            tuning.validate_scan_table(_scan_table(_scan_entry(**bad)))
+    with pytest.raises(ValueError):
+        tuning.validate_scan_table(_scan_table(_scan_entry(), _scan_entry()))
+    with pytest.raises(ValueError):
+        tuning.validate_scan_table(_table())
+
+
+def test_scan_table_set_get_remove():
+    """Host-only calls: the entry overrides the built-in head-block rule, a
+    zero field keeps the rule's choice, and removing the entry restores it."""
+    tuning.clear_scan_config(_SSD_KEY)
+    rule, from_table = tuning.get_scan_config(_SSD_KEY)
+    assert not from_table
+    # 2 x 8 x 2 chunk tiles per head block: the rule takes the fewest blocks
+    # (a divisor of the 6 heads per group) giving at least 2 x 152 units
+    assert rule == dict(scan_head_blocks=6, bc_head_blocks=6)
+    tuning.set_scan_config(_SSD_KEY, 2, 3)
+    assert tuning.get_scan_config(_SSD_KEY) == (dict(scan_head_blocks=2, bc_head_blocks=3), True)
+    tuning.set_scan_config(_SSD_KEY, 0, 1)
+    assert tuning.get_scan_config(_SSD_KEY)[0] == dict(scan_head_blocks=6, bc_head_blocks=1)
+    for bad in ((4, 0), (0, 5), (-1, 0), (33, 0)):
+        with pytest.raises(ValueError):
+            tuning.set_scan_config(_SSD_KEY, *bad)
+    tuning.clear_scan_config(_SSD_KEY)
+    assert tuning.get_scan_config(_SSD_KEY) == (rule, False)
+
+
+def test_scan_table_apply_and_env(tmp_path, monkeypatch):
+    p = tmp_path / "s.json"
+    p.write_text(json.dumps(_scan_table(_scan_entry(seqlen=777))))
+    monkeypatch.setenv("SSD_TUNING_TABLE", "none")
+    monkeypatch.setenv("SSD_SCAN_TABLE", str(p))
+    tuning.apply_default(tuning._native.load())
+    key = dict(_SSD_KEY, seqlen=777)
+    assert tuning.get_scan_config(key) == (dict(scan_head_blocks=3, bc_head_blocks=2), True)
+    tuning.clear_scan_config(key)
+
+
+def test_packaged_scan_table_is_valid_and_loaded():
+    if not os.path.exists(tuning.DEFAULT_SCAN_TABLE):
+        pytest.skip("no packaged table")
+    with open(tuning.DEFAULT_SCAN_TABLE) as f:
+        t = json.load(f)
+    tuning.validate_scan_table(t)
+    assert t.get("generated_by", "").startswith("SSD_SCAN_TABLE=none python -m")
+    if os.environ.get("SSD_SCAN_TABLE", tuning.DEFAULT_SCAN_TABLE) == tuning.DEFAULT_SCAN_TABLE:
+        for e in t["entries"]:
+            cfg, from_table = tuning.get_scan_config({k: e[k] for k in tuning._SCAN_KEYS})
+            assert from_table
+            assert cfg == {k: e[k] for k in tuning._SCAN_FIELDS}
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("scan_nb,bc_nb", [(1, 1), (2, 3), (6, 2)])
+def test_tuned_ssd_launch_computes_the_same(cuda_lib, scan_nb, bc_nb):
+    """Each head of a chunk tile is computed by the same arithmetic whichever
+    head block holds it, so y, final_states, dx and ddt are bit-identical under
+    any table entry; dB and dC sum the heads of a group over a different
+    partition (per block, then over blocks), equal to rounding."""
+    import torch
+
+    from state_space_model_sm_gb300.inputs import SSDShape, make_inputs, to_torch
+    k = _SSD_KEY
+    inp = make_inputs(SSDShape(k["batch"], k["seqlen"], k["nheads"], k["headdim"], k["dstate"],
+                               k["ngroups"], k["chunk_size"]), seed=31, dtype="bf16",
+                      init_std=0.1, with_dy=True, dfinal_std=0.1)
+    t = to_torch(inp)
+    saved, had = tuning.get_scan_config(k)
+
+    def run():
+        y, fin = cuda_lib.ssd_fwd(t["x"], t["dt"], t["dt_bias"], t["A"], t["B"], t["C"], t["D"],
+                                  chunk_size=k["chunk_size"], init_states=t["init"])
+        g = cuda_lib.ssd_bwd(t["x"], t["dt"], t["dt_bias"], t["A"], t["B"], t["C"], t["D"],
+                             k["chunk_size"], t["init"], t["dy"], t["dfinal"])
+        torch.cuda.synchronize()
+        return y, fin, g
+    try:
+        tuning.clear_scan_config(k)
+        a = run()
+        tuning.set_scan_config(k, scan_nb, bc_nb)
+        b = run()
+    finally:
+        if had:
+            tuning.set_scan_config(k, saved["scan_head_blocks"], saved["bc_head_blocks"])
+        else:
+            tuning.clear_scan_config(k)
+    assert cuda_lib.device_status() == 0
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    for name in ("dx", "ddt"):
+        assert torch.equal(a[2][name], b[2][name]), name
+    for name in ("dB", "dC", "dA", "ddt_bias", "dD", "dinit_states"):
+        np.testing.assert_allclose(b[2][name].cpu().numpy(), a[2][name].cpu().numpy(),
+                                   rtol=1e-5, atol=1e-5 * float(a[2][name].abs().max()),
+                                   err_msg=name)
