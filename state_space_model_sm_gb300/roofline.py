@@ -50,8 +50,19 @@ def _terms(d: Dims):
 
 
 def tc_bwd_nblk(d: Dims) -> int:
-    """Head blocks per group of the tensor-core dB / dC kernels (same rule as
-    the library: fewest blocks giving >= 2 x 152 CTAs)."""
+    """Head blocks per group of the tensor-core dB / dC kernels: the library's
+    launch-table entry for this shape when one is set, else its built-in rule
+    (fewest blocks giving >= 2 x 152 CTAs).  The dB / dC partials written and
+    summed scale with it."""
+    from . import _native, tuning
+    try:
+        lib = _native.load()
+    except (OSError, RuntimeError):   # library not built: the rule alone
+        lib = None
+    if lib is not None:
+        key = dict(batch=d.B, seqlen=d.T, nheads=d.H, headdim=d.P, dstate=d.N, ngroups=d.G,
+                   chunk_size=d.L)
+        return tuning.get_scan_config(key, lib=lib)[0]["bc_head_blocks"]
     hpg = d.H // d.G
     units = d.B * d.nc * (d.L // 128) * d.G
     for nb in range(1, hpg + 1):
