@@ -1,8 +1,8 @@
 // tcgen05 chunk kernels of the SSD, fed by TMA (sm_103a).  One template, four
 // roles, each over a 128-row tile of one chunk and a block of heads of one
 // group ("Optimizing Mamba-2 kernels for the B200", Stage 1 kernel table:
-// _chunk_scan_fwd fwd_5, _chunk_scan_chunk_state_bwd_dx bwd_8,
-// _chunk_scan_bwd_dC bwd_11, _chunk_state_bwd_db bwd_12):
+// _chunk_scan_fwd fwd_5, _chunk_scan_chunk_state_bwd_dx bwd_10,
+// _chunk_scan_bwd_dC bwd_12, _chunk_state_bwd_db bwd_11):
 //
 //   FWD  rows l, columns s <= l:  P  = CB[l,s] e^{a_l-a_s} delta_s
 //        y_l  = sum_s P[l,s] x_s + e^{a_l} C_l.H_c^T + D x_l
@@ -880,20 +880,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Tensor map of a (B, T, X, inner) bf16 tensor read in boxes of 64 inner
-// elements (128 bytes, the 128-byte swizzle span) x 128 rows of T, one X and
-// one batch index; rows past T read as zeros.
 bool make_map(CUtensorMap* m, const void* ptr, int inner, int X, int T, int B) {
-  const auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)X, (cuuint64_t)T, (cuuint64_t)B};
-  const cuuint64_t strides[3] = {(cuuint64_t)inner * 2, (cuuint64_t)X * inner * 2,
-                                 (cuuint64_t)T * X * inner * 2};
-  const cuuint32_t box[4] = {64, 1, 128, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_tma_map(m, ptr, inner, X, T, B, 1, 128);
 }
 
 template <int N, int L, int MODE, typename Tout>
@@ -971,6 +959,36 @@ cudaError_t chunk_bwd_nl(const Dims& d, const BwdArgs& ba, const TcBwdWs& w, int
 }
 
 }  // namespace
+
+// Tensor map of a (B, T, X, inner) bf16 tensor read in boxes of 64 inner
+// elements (128 bytes, the 128-byte swizzle span) x box_x of X x box_t rows
+// of T x one batch index; rows past T read as zeros.
+bool make_tma_map(CUtensorMap* m, const void* ptr, int inner, int X, int T, int B, int box_x,
+                  int box_t) {
+  const auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)X, (cuuint64_t)T, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)inner * 2, (cuuint64_t)X * inner * 2,
+                                 (cuuint64_t)T * X * inner * 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)box_x, (cuuint32_t)box_t, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tma_map_f32(CUtensorMap* m, void* ptr, int inner, int64_t rows, int box_inner,
+                      int box_rows) {
+  const auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)inner * 4};
+  const cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 cudaError_t tc_chunk_forward(const Dims& d, const FwdArgs& f, const FwdWs& w, int nblk,
                              cudaStream_t s) {

@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libssd.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -173,13 +174,30 @@ int tc_bwd_nblk(const Dims& d);
 int tc_scan_nblk(const Dims& d);
 cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w, cudaStream_t s);
 
+// Tensor map (for TMA) of a (B, T, X, inner) bf16 tensor, 128-byte swizzle,
+// boxes of 64 inner elements x box_x x box_t rows x 1; false if the driver
+// entry point is missing or rejects the layout (ssd_chunk_tc.cu).
+bool make_tma_map(CUtensorMap* m, const void* ptr, int inner, int X, int T, int B, int box_x,
+                  int box_t);
+// Tensor map of a (rows, inner) fp32 matrix, 128-byte swizzle, boxes of
+// box_inner (32: 128 bytes) x box_rows, for TMA stores.
+bool make_tma_map_f32(CUtensorMap* m, void* ptr, int inner, int64_t rows, int box_inner,
+                      int box_rows);
+
 // The TMA-fed chunk kernels (ssd_chunk_tc.cu), over (batch, chunk, row tile,
 // group, block of nblk heads): chunk_scan (y from the state images in w.Himg),
-// and the backward's dx, dC and dB (with the ddA row / column sums, ycs, qrow,
-// ddir and ddiag).  dCout / dBout receive (B, T, G, nblk, N) partials.
+// and the backward's dC and dB (with the ddA row / column sums and ycs).
+// dCout / dBout receive (B, T, G, nblk, N) partials.
 cudaError_t tc_chunk_forward(const Dims& d, const FwdArgs& f, const FwdWs& w, int nblk,
                              cudaStream_t s);
 cudaError_t tc_chunk_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w, int nblk,
                               float* dCout, float* dBout, cudaStream_t s);
+
+// The TMA-fed chunk_state kernels (ssd_state_tc.cu): chunk_cumsum + chunk
+// state (writes delta, acs and S), and dstates (dHs from dy, C and acs).
+cudaError_t tc_chunk_state(const Dims& d, const FwdArgs& f, float* delta, float* acs, float* S,
+                           cudaStream_t s);
+cudaError_t tc_chunk_dstates(const Dims& d, const void* dy, const void* C, const float* acs,
+                             float* dHs, cudaStream_t s);
 
 }  // namespace ssd

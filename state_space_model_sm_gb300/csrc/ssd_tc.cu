@@ -1,10 +1,11 @@
-// tcgen05 tensor-core kernels of the SSD forward and backward (bf16 inputs,
-// headdim 64, d_state 64 or 128, chunk 128 or 256): chunk_state (with
-// chunk_cumsum) / dstates, chunk_scan / dx, dB / dC and the backward's tail.
+// tcgen05 tensor-core path of the SSD forward and backward (bf16 inputs,
+// headdim 64, d_state 64 or 128, chunk 128 or 256): the launch sequences of
+// both directions, the backward's dx kernel and its tail.  chunk_state /
+// dstates run in ssd_state_tc.cu, chunk_scan, dC and dB in ssd_chunk_tc.cu.
 //
 // Precision: operands that the method forms in fp32 before a contraction
-// (the decay-weighted x of chunk_state, the masked decay-weighted C.B^T of
-// chunk_scan, the fp32 inter-chunk state) are split into two bf16 terms,
+// (the masked decay-weighted C.B^T of dx, the fp32 inter-chunk state) are
+// split into two bf16 terms,
 // v = hi + lo with hi = rn_bf16(v), and both terms are multiplied; raw bf16
 // inputs enter as they are.  Every product is accumulated in fp32 in TMEM,
 // so the results carry ~16 significant bits per operand instead of bf16's 8.
@@ -59,260 +60,6 @@ __device__ __forceinline__ void stage_rows_async(unsigned char* dst, int rows, i
     const bool v = r < valid;
     cp_async16(dst + (j / 8) * panel + sw128(r, j % 8), v ? rowptr(r) + j * 8 : safe, v);
   }
-}
-
-// =============================================================== chunk_state
-// For a head pair (h, h+1) of one group and chunk c:
-//   D[m = 64 hh + p, n] = sum_l w_hh[l] X[l, h+hh, p] Y[l, n]  ->  out[b, c, h+hh, p, n]
-//   MODE 0 (chunk_state): X = x,  Y = B, w = exp(a_last - a_l) delta_l  (S_c)
-//   MODE 1 (dstates):     X = dy, Y = C, w = exp(a_l)                   (dHs_c)
-// A = (w X)^T as an MN-major operand (rows l, 128 columns = two heads x 64),
-// B = the chunk's Y rows as an MN-major operand (rows l, N columns).
-template <int N, int L>
-struct StateSmem {
-  static constexpr int kKB = 64;                    // rows of l per pipeline stage
-  static constexpr int kPanel = kKB * 128;          // one 64-column panel of a stage
-  static constexpr int kB = (N / 64) * kPanel;      // Y rows of the stage
-  static constexpr int kX = 2 * kPanel;             // w X of the head pair (hi or lo)
-  static constexpr int kStage = kB + 2 * kX;
-  static constexpr int kBytes = 2 * kStage + 2 * L * 4 + 1024;
-};
-
-// Persistent: about two CTAs per SM, each taking the (batch, chunk, head
-// pair) items k = blockIdx.x, blockIdx.x + gridDim.x, ... (head pair fastest,
-// so CTAs running side by side share a chunk's Y rows in L2), 256 threads.
-// The chunk's rows stream through a two-stage ring of 64-row blocks: the x
-// rows of block k+1 are loaded into registers while block k is scaled,
-// split and multiplied.  The accumulator is double-buffered in TMEM and an
-// item's result is written out after the next item's MMAs are issued, so the
-// stores of one item overlap the loads and products of the next.
-template <int N, int L, int MODE>
-__global__ void __launch_bounds__(256, 2)
-    k_state_tc(const bf16* __restrict__ x, const bf16* __restrict__ Bm,
-               const bf16* __restrict__ dt, const float* __restrict__ dt_bias,
-               const float* __restrict__ A, float* __restrict__ delta, float* __restrict__ acs,
-               float* __restrict__ S, int T, int H, int G, int nc, int n_items, int* status) {
-  using SM = StateSmem<N, L>;
-  constexpr int KB = SM::kKB, NKB = L / KB;
-  static_assert(NKB % 2 == 0, "ring stages alternate across items");
-  constexpr uint32_t kTmemCols = 2 * N;  // two accumulators (128 or 256 columns)
-  extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t bar_stage[2], bar_done[2];
-  __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag;
-  __shared__ float s_scan[8 + 2];  // per-warp totals, then a[L-1] of each head
-  unsigned char* base = align1024(smem_raw);
-  float* sw = reinterpret_cast<float*>(base + 2 * SM::kStage);  // [2][L]
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int hpg = H / G, npairs = H / 2;
-  // item -> (b, c, first head of the pair)
-  auto decode = [&](int item, int& b, int& c, int& h) {
-    const int pp = item % npairs, bc = item / npairs;
-    c = bc % nc;
-    b = bc / nc;
-    h = 2 * pp;
-  };
-
-  if (tid == 0) {
-    abort_flag = 0;
-    mbar_init(&bar_stage[0], 1);
-    mbar_init(&bar_stage[1], 1);
-    mbar_init(&bar_done[0], 1);
-    mbar_init(&bar_done[1], 1);
-    fence_mbar_init();
-  }
-  if (warp == 0) tmem_alloc(&tmem_base, kTmemCols);
-  fence_before_sync();
-  __syncthreads();
-  fence_after_sync();
-  const uint32_t tm = tmem_base;
-  constexpr uint32_t idesc = idesc_bf16(128, N, 1, 1);
-  uint32_t n_stage0 = 0, n_stage1 = 0;
-
-  // a block's X rows (both heads of a pair, 256 contiguous bytes per row) go
-  // through registers one block ahead
-  constexpr int kPer = KB * 16 / 256;
-  auto load_block = [&](uint4 (&u)[kPer], int bb, int cc, int hp, int l0) {
-    const int64_t t0 = (int64_t)cc * L;
-    const int Lv = min(L, T - (int)t0);
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int i = tid + k * 256, l = l0 + (i >> 4), j = i & 15;
-      u[k] = l < Lv ? *reinterpret_cast<const uint4*>(x + (((int64_t)bb * T + t0 + l) * H + hp) *
-                                                              kP + j * 8)
-                    : make_uint4(0, 0, 0, 0);
-    }
-  };
-  // the result of an item from TMEM buffer buf: rows m = 64 hh + p of the pair
-  auto epilogue = [&](int bb, int cc, int hp, uint32_t buf, uint32_t parity) {
-    const bool ok =
-        __all_sync(0xffffffffu, mbar_wait(&bar_done[buf], parity, status, &abort_flag));
-    fence_after_sync();
-    if (ok) {
-      const int q = warp & 3, half = warp >> 2;
-      const int m = 32 * q + lane, hh = m >> 6, p = m & 63;
-      float* out = S + ((((int64_t)bb * nc + cc) * H + hp + hh) * kP + p) * N;
-      const uint32_t ta = tm + buf * N + ((uint32_t)(32 * q) << 16);
-#pragma unroll
-      for (int c0 = half * (N / 2); c0 < (half + 1) * (N / 2); c0 += 16) {
-        float v[16];
-        tmem_ld16(ta + c0, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 16; k += 4)
-          *reinterpret_cast<float4*>(out + c0 + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
-      }
-    }
-    fence_before_sync();  // the buffer's next accumulate comes after the next __syncthreads
-  };
-
-  // a block's Y rows by cp.async into ring stage st (one commit group)
-  auto stage_y = [&](int st, int bb, int cc, int gg, int l0) {
-    const int64_t t0 = (int64_t)cc * L;
-    const int Lv = min(L, T - (int)t0);
-    stage_rows_async(base + st * SM::kStage, KB, N / 8, SM::kPanel, Lv - l0, Bm, [&](int l) {
-      return Bm + (((int64_t)bb * T + t0 + l0 + l) * G + gg) * N;
-    });
-    cp_async_commit();
-  };
-
-  uint4 u[kPer], un[kPer];
-  int b = 0, c = 0, h = 0;
-  if ((int)blockIdx.x < n_items) {
-    decode(blockIdx.x, b, c, h);
-    load_block(u, b, c, h, 0);
-    stage_y(0, b, c, h / hpg, 0);  // the first block's Y rows, one block ahead
-  } else {
-    cp_async_commit();
-  }
-  int pb = 0, pc = 0, ph = 0;  // the previous item, written out one item late
-  int k = 0;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++k) {
-    const int g = h / hpg;
-    const int64_t t0 = (int64_t)c * L;
-    const int Lv = min(L, T - (int)t0);
-    const uint32_t buf = k & 1;
-    if constexpr (MODE == 0) {
-      // chunk_cumsum of the pair's two heads, 128 threads per head, L/128
-      // consecutive positions per thread: delta = softplus(dt + dt_bias) (0
-      // past seqlen), a = in-chunk inclusive cumsum of delta * A; both are
-      // written for the later kernels
-      constexpr int E2 = L / 128;
-      const int hh = tid >> 7, tl = tid & 127, hd = h + hh;
-      const float bias = dt_bias ? dt_bias[hd] : 0.f, Ah = A[hd];
-      float dl[E2], al[E2], run = 0.f;
-#pragma unroll
-      for (int e = 0; e < E2; ++e) {
-        const int l = tl * E2 + e;
-        dl[e] = l < Lv ? dt_softplus(__bfloat162float(dt[((int64_t)b * T + t0 + l) * H + hd]) + bias)
-                       : 0.f;
-        run += dl[e] * Ah;
-        al[e] = run;
-      }
-      float incl = run;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-      }
-      __syncthreads();  // s_scan and sw of the previous item are no longer read
-      if (lane == 31) s_scan[warp] = incl;
-      __syncthreads();
-      float pre = incl - run;  // exclusive prefix within the warp
-      for (int kk = 0; kk < (warp & 3); ++kk) pre += s_scan[4 * hh + kk];
-      const int64_t cv = (((int64_t)b * H + hd) * nc + c) * L;
-#pragma unroll
-      for (int e = 0; e < E2; ++e) {
-        const int l = tl * E2 + e;
-        al[e] += pre;
-        delta[cv + l] = dl[e];
-        acs[cv + l] = al[e];
-      }
-      if (tl == 127) s_scan[8 + hh] = al[E2 - 1];  // a[L-1] as written
-      __syncthreads();
-      const float alast = s_scan[8 + hh];
-#pragma unroll
-      for (int e = 0; e < E2; ++e) sw[hh * L + tl * E2 + e] = __expf(alast - al[e]) * dl[e];
-    } else {
-      __syncthreads();  // sw of the previous item is no longer read
-      for (int i = tid; i < 2 * L; i += 256) {
-        const int hh = i / L, l = i % L;
-        const int64_t cv = (((int64_t)b * H + h + hh) * nc + c) * L;
-        sw[i] = __expf(acs[cv + l]);
-      }
-    }
-    // the next item (its first block's X rows are loaded during the last block)
-    int nb = b, ncn = c, nh = h;
-    const bool has_next = item + (int)gridDim.x < n_items;
-    if (has_next) decode(item + gridDim.x, nb, ncn, nh);
-    for (int kb = 0; kb < NKB; ++kb) {
-      const int st = kb & 1;
-      unsigned char* sB = base + st * SM::kStage;
-      unsigned char* sXh = sB + SM::kB;
-      unsigned char* sXl = sXh + SM::kX;
-      const int l0 = kb * KB;
-      if (kb + 1 < NKB) load_block(un, b, c, h, l0 + KB);
-      else if (has_next) load_block(un, nb, ncn, nh, 0);
-      // the stage's X part is free once the MMAs that read it (two blocks ago)
-      // are done; its Y rows were staged during the previous block
-      const uint32_t ns = st ? n_stage1 : n_stage0;
-      if (ns > 0) mbar_wait(&bar_stage[st], (ns - 1) & 1, status, &abort_flag);
-      if (kb == 0) __syncthreads();  // sw ready
-#pragma unroll
-      for (int kk = 0; kk < kPer; ++kk) {
-        const int i = tid + kk * 256, lr = i >> 4, j = i & 15, hh = j >> 3;
-        float v[8];
-        unpack8(u[kk], v);
-        const float wl = sw[hh * L + l0 + lr];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] *= wl;
-        const uint32_t off = hh * SM::kPanel + sw128(lr, j & 7);
-        store_split8(sXh + off, sXl + off, v);
-      }
-#pragma unroll
-      for (int kk = 0; kk < kPer; ++kk) u[kk] = un[kk];
-      // the next block's Y rows (or the next item's first) into the other
-      // stage, once the MMAs of the previous block have read it
-      {
-        const uint32_t no = st ? n_stage0 : n_stage1;
-        if (no > 0) mbar_wait(&bar_stage[st ^ 1], (no - 1) & 1, status, &abort_flag);
-        if (kb + 1 < NKB) stage_y(st ^ 1, b, c, g, l0 + KB);
-        else if (has_next) stage_y(st ^ 1, nb, ncn, nh / hpg, 0);
-        else cp_async_commit();
-      }
-      cp_async_wait<1>();  // this block's Y rows (the next block's may still fly)
-      fence_async_smem();
-      fence_before_sync();
-      __syncthreads();
-      if (tid == 0) {
-        fence_after_sync();
-        for (int ks = 0; ks < KB / 16; ++ks) {
-          const uint64_t bd = sdesc(smem_u32(sB) + ks * 2048, SM::kPanel, 1024);
-          const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
-          mma_bf16(tm + buf * N, sdesc(smem_u32(sXh) + ks * 2048, SM::kPanel, 1024), bd, idesc,
-                   acc);
-          mma_bf16(tm + buf * N, sdesc(smem_u32(sXl) + ks * 2048, SM::kPanel, 1024), bd, idesc,
-                   1u);
-        }
-        mma_commit(&bar_stage[st]);
-        if (kb == NKB - 1) mma_commit(&bar_done[buf]);
-      }
-      if (st) ++n_stage1;
-      else ++n_stage0;
-    }
-    // the previous item's result, while this item's products run
-    if (k > 0) epilogue(pb, pc, ph, buf ^ 1u, ((k - 1) >> 1) & 1u);
-    pb = b;
-    pc = c;
-    ph = h;
-    b = nb;
-    c = ncn;
-    h = nh;
-  }
-  if (k > 0) epilogue(pb, pc, ph, (k - 1) & 1u, ((k - 1) >> 1) & 1u);
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tm, kTmemCols);
 }
 
 // ================================================================ dx
@@ -833,41 +580,13 @@ void scan_partition(const Dims& d, int sms, int* grid, int* per) {
   *grid = (int)((items + *per - 1) / *per);
 }
 
-// chunk_cumsum (delta, a) and chunk_state (S) in one persistent launch.
-template <int N, int L>
-void launch_state_front(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s,
-                        int* status, int sms) {
-  using SM = StateSmem<N, L>;
-  auto kern = k_state_tc<N, L, 0>;
-  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
-  const int n_items = d.B * d.nc * (d.H / 2);
-  const dim3 grid(std::min(n_items, 2 * sms));
-  SSD_LAUNCH("k_state_tc", s,
-             kern<<<grid, 256, SM::kBytes, s>>>(
-                 static_cast<const bf16*>(a.x), static_cast<const bf16*>(a.B),
-                 static_cast<const bf16*>(a.dt), a.dt_bias, a.A, w.delta, w.acs, w.S, d.T, d.H,
-                 d.G, d.nc, n_items, status));
-}
-
-// dH^scan_c = sum_l exp(a_l) dy_l (x) C_l per chunk, from delta / a already
-// in the workspace.
-template <int N, int L>
-void launch_dstates(const Dims& d, const bf16* dy, const bf16* Cm, const float* delta,
-                    const float* acs, float* dHs, cudaStream_t s, int* status, int sms) {
-  using SS = StateSmem<N, L>;
-  auto kern = k_state_tc<N, L, 1>;
-  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::kBytes);
-  const int n_items = d.B * d.nc * (d.H / 2);
-  const dim3 grid(std::min(n_items, 2 * sms));
-  SSD_LAUNCH("k_dstates_tc", s, kern<<<grid, 256, SS::kBytes, s>>>(
-      dy, Cm, nullptr, nullptr, nullptr, const_cast<float*>(delta), const_cast<float*>(acs), dHs,
-      d.T, d.H, d.G, d.nc, n_items, status));
-}
-
 template <int N, int L, typename Tout>
 cudaError_t launch_tc_forward_t(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s,
                                 int* status, int sms) {
-  launch_state_front<N, L>(d, a, w, s, status, sms);  // chunk_cumsum runs inside chunk_state
+  {
+    const cudaError_t e = tc_chunk_state(d, a, w.delta, w.acs, w.S, s);  // with chunk_cumsum
+    if (e != cudaSuccess) return e;
+  }
   simt_state_passing(d, a, w, s);
   const cudaError_t e = tc_chunk_forward(d, a, w, tc_scan_nblk(d), s);
   if (e != cudaSuccess) return e;
@@ -889,9 +608,13 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
   FwdArgs f = a.f;
   f.final_state = nullptr;
   FwdWs fw{w.delta, w.acs, w.S, nullptr, nullptr, w.Himg, w.seg};
-  launch_state_front<N, L>(d, f, fw, s, status, sms);  // with chunk_cumsum
-  simt_state_passing(d, f, fw, s);
-  launch_dstates<N, L>(d, dy, Cm, w.delta, w.acs, w.dHs, s, status, sms);
+  {
+    cudaError_t e = tc_chunk_state(d, f, w.delta, w.acs, w.S, s);  // with chunk_cumsum
+    if (e != cudaSuccess) return e;
+    simt_state_passing(d, f, fw, s);
+    e = tc_chunk_dstates(d, dy, Cm, w.acs, w.dHs, s);
+    if (e != cudaSuccess) return e;
+  }
   const int nsplit = simt_state_passing_bwd(d, w.dHs, w.acs, nullptr, a.dfinal, nullptr, w.dlast,
                                             a.dinit, w.dSimg, w.Himg, w.seg, s);
   {
@@ -950,33 +673,16 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStre
 }
 
 cudaError_t tc_front_final(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
-  int* status = device_status_ptr();
-  if (!status) return cudaErrorUnknown;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (d.N == 128 && d.L == 256) launch_state_front<128, 256>(d, a, w, s, status, sms);
-  else if (d.N == 128 && d.L == 128) launch_state_front<128, 128>(d, a, w, s, status, sms);
-  else if (d.N == 64 && d.L == 256) launch_state_front<64, 256>(d, a, w, s, status, sms);
-  else launch_state_front<64, 128>(d, a, w, s, status, sms);
+  const cudaError_t e = tc_chunk_state(d, a, w.delta, w.acs, w.S, s);
+  if (e != cudaSuccess) return e;
   simt_state_passing(d, a, w, s);
   return cudaGetLastError();
 }
 
 cudaError_t tc_dstates(const Dims& d, const void* dy, const void* C, const float* delta,
                        const float* acs, float* dHs, cudaStream_t s) {
-  int* status = device_status_ptr();
-  if (!status) return cudaErrorUnknown;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const bf16* y = static_cast<const bf16*>(dy);
-  const bf16* c = static_cast<const bf16*>(C);
-  if (d.N == 128 && d.L == 256) launch_dstates<128, 256>(d, y, c, delta, acs, dHs, s, status, sms);
-  else if (d.N == 128 && d.L == 128) launch_dstates<128, 128>(d, y, c, delta, acs, dHs, s, status, sms);
-  else if (d.N == 64 && d.L == 256) launch_dstates<64, 256>(d, y, c, delta, acs, dHs, s, status, sms);
-  else launch_dstates<64, 128>(d, y, c, delta, acs, dHs, s, status, sms);
-  return cudaGetLastError();
+  (void)delta;
+  return tc_chunk_dstates(d, dy, C, acs, dHs, s);
 }
 
 cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w, cudaStream_t s) {

@@ -181,6 +181,29 @@ __device__ __forceinline__ void tma_prefetch_map(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// Tiled tensor store (TMA) of one box from this CTA's shared memory at src to
+// global memory, in the issuing thread's current bulk group.  The writes to
+// src must be made visible to the async proxy first (fence_async_smem).
+// Coordinates: innermost first; the innermost one times the element size is a
+// multiple of 16 bytes, and neither is negative.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int c0, int c1, const void* src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::
+                   "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Waits until every bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Waits for a phase like mbar_wait but ignores the abort flag: used at the
 // end of a kernel to let copies or products already in flight land before
 // the CTA releases its shared memory and TMEM.  Bounded by kWaitLimitNs.
