@@ -13,17 +13,18 @@
 // one M = 128 accumulator per item (the pair's two heads), N = d_state, K =
 // the chunk's rows in blocks of 64.
 //
-// Warp roles (448 threads, one persistent CTA per SM over items k =
+// Warp roles (704 threads, one persistent CTA per SM over items k =
 // blockIdx.x, blockIdx.x + gridDim.x, ...; head pair fastest, so the CTAs
 // running side by side share a chunk's Y rows in L2):
-//   warps 0-7   convert: the item's weights w (chunk_cumsum in MODE 0), then
-//               per block the TMA-landed x (dy) rows times w, split into bf16
-//               hi + lo, into the MN-major A operand;
-//   warps 8-11  epilogue: TMEM accumulator -> shared-memory slabs -> TMA
-//               stores of the item's two 64 x N states (the load/store unit
-//               stays free for the converters);
-//   warp 12     issues every tcgen05.mma (hi and lo A against the same Y);
-//   warp 13     issues every TMA copy (x / dy pair boxes, Y panels).
+//   warps 0-15  convert: per block the TMA-landed x (dy) rows times the
+//               item's weights w, split into bf16 hi + lo, into the MN-major
+//               A operand;
+//   warps 16-19 epilogue: TMEM accumulator -> shared-memory slabs -> TMA
+//               stores of the item's two 64 x N states; between items they
+//               also form the weights two items ahead (chunk_cumsum in MODE
+//               0), off the converters' path;
+//   warp 20     issues every tcgen05.mma (hi and lo A against the same Y);
+//   warp 21     issues every TMA copy (x / dy pair boxes, Y panels).
 // Rings: four raw-x stages, three Y stages, two A stages and two TMEM
 // accumulators, each handed over by full / empty mbarriers; every wait is
 // bounded and records SSD_ERR_TIMEOUT on expiry.
@@ -47,13 +48,14 @@ constexpr int kKB = 64;         // rows of l per block
 constexpr int kNX = 4;          // raw x stages
 constexpr int kNY = 3;          // Y stages
 constexpr int kNA = 2;          // A operand stages
-constexpr int kConvW = 8;       // converter warps
+constexpr int kConvW = 16;      // converter warps
 constexpr int kEpiW = 4;        // epilogue warps (one per TMEM lane quarter)
 constexpr int kEpi0 = kConvW;   // first epilogue warp
 constexpr int kMmaW = kConvW + kEpiW;
 constexpr int kProdW = kMmaW + 1;
 constexpr int kStateThreads = 32 * (kProdW + 1);
 constexpr int kConvT = 32 * kConvW;
+constexpr int kEpiT = 32 * kEpiW;
 
 template <int N, int L>
 struct StateLayout {
@@ -79,8 +81,8 @@ __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
                                           ~uintptr_t(1023));
 }
 
-__device__ __forceinline__ void conv_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConvT) : "memory");
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiT) : "memory");
 }
 
 __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
@@ -107,10 +109,10 @@ __global__ void __launch_bounds__(kStateThreads, 1)
   constexpr int NKB = L / kKB, NP = N / 64;
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t bar_xf[kNX], bar_xe[kNX], bar_yf[kNY], bar_ye[kNY], bar_af[kNA],
-      bar_ae[kNA], bar_accf[2], bar_acce[2], bar_final;
+      bar_ae[kNA], bar_accf[2], bar_acce[2], bar_wf[2], bar_final;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
-  __shared__ float s_scan[kConvW], s_alast[2];
+  __shared__ float s_scan[kEpiW], s_alast[2];
   unsigned char* base = align1024(smem_raw);
   float* sw = reinterpret_cast<float*>(base + LY::oW);
 
@@ -146,6 +148,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_accf[i], 1);
       mbar_init(&bar_acce[i], kEpiW);
+      mbar_init(&bar_wf[i], kEpiW);
     }
     mbar_init(&bar_final, 1);
     fence_mbar_init();
@@ -238,86 +241,32 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     // them 32 columns at a time: registers -> a 128-byte-swizzled slab in
     // shared memory -> one TMA store, double-buffered per warp.
     const int q = warp & 3;               // TMEM lane quarter of this warp
+    const int et = tid - 32 * kEpi0;      // 0 .. 127
     unsigned char* stg = base + LY::oStg + q * LY::kStg;
     if (lane == 0) tma_prefetch_map(&mOut);
-    int js = 0;                           // slabs this warp has stored
-    bool ok = true;
-    for (int k = 0; ok && k < nk; ++k) {
-      const int buf = k & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_accf[buf], (k >> 1) & 1, status, &abort_flag));
-      fence_after_sync();
-      if (!ok) break;
+
+    // The weights of item k into sw[k & 1]: 64 threads per head, EV
+    // consecutive positions each.  MODE 0 also runs chunk_cumsum for the
+    // pair (delta = softplus(dt + dt_bias), a = in-chunk inclusive cumsum of
+    // delta A, both written out) and w = e^{a_last - a} delta; MODE 1 w = e^a.
+    // Every epilogue thread calls it for every item (it holds named barriers).
+    constexpr int EV = L / 64;
+    const int eh = et >> 6, ev = et & 63;
+    auto compute_w = [&](int k) {
       int b, c, h;
       decode(k, b, c, h);
-      const int row0 = (((b * nc + c) * H + h) * kSP) + 32 * q;  // rows (b, c, h, p) of out
-      const uint32_t ta = tm + buf * N + ((uint32_t)(32 * q) << 16);
-#pragma unroll
-      for (int s = 0; s < N / 32; ++s, ++js) {
-        float v[32];
-        tmem_ld16(ta + 32 * s, *reinterpret_cast<float(*)[16]>(v));
-        tmem_ld16(ta + 32 * s + 16, *reinterpret_cast<float(*)[16]>(v + 16));
-        tmem_wait_ld();
-        unsigned char* slab = stg + (js & 1) * (32 * 128);
-        if (js >= 2) {  // the store issued from this slab two slabs ago has read it
-          if (lane == 0) bulk_wait_read<1>();
-          __syncwarp();
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<float4*>(slab + sw128(lane, j)) =
-              make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&mOut, 32 * s, row0, slab);
-          bulk_commit_group();
-        }
-      }
-      fence_before_sync();
-      warp_arrive(&bar_acce[buf], lane);
-    }
-    if (lane == 0) bulk_wait_all();  // the stores have read shared memory and landed
-  } else {
-    // ------------------------------------------------------------ converters
-    // per-item vectors, loaded one item ahead: MODE 0 the pair's dt (thread
-    // tid: head tid / 128, positions E2 (tid % 128) .. + E2 - 1), MODE 1 a
-    constexpr int E2 = L / 128;
-    const int vh = tid >> 7, vt = tid & 127;
-    float vin[E2], vbias = 0.f, vA = 0.f;
-    auto load_vec = [&](int k) {
-      int b, c, h;
-      decode(k, b, c, h);
-      const int t0 = c * L, Lv = min(L, T - t0);
+      const int hd = h + eh, t0 = c * L, Lv = min(L, T - t0);
+      float* w = sw + (k & 1) * 2 * L + eh * L;
+      const int64_t cv = (((int64_t)b * H + hd) * nc + c) * L;
       if constexpr (MODE == 0) {
-        vbias = a.dt_bias ? a.dt_bias[h + vh] : 0.f;
-        vA = a.A[h + vh];
-      }
+        const float bias = a.dt_bias ? a.dt_bias[hd] : 0.f, Ah = a.A[hd];
+        float dl[EV], al[EV], run = 0.f;
 #pragma unroll
-      for (int e = 0; e < E2; ++e) {
-        const int l = vt * E2 + e;
-        if constexpr (MODE == 0)
-          vin[e] = l < Lv ? __bfloat162float(a.dt[((int64_t)b * T + t0 + l) * H + h + vh]) : 0.f;
-        else
-          vin[e] = a.acs[(((int64_t)b * H + h + vh) * nc + c) * L + l];
-      }
-    };
-    if (nk > 0) load_vec(0);
-    bool ok = true;
-    for (int k = 0; k < nk; ++k) {
-      int b, c, h;
-      decode(k, b, c, h);
-      float* w = sw + (k & 1) * 2 * L;
-      if constexpr (MODE == 0) {
-        // chunk_cumsum of the pair: delta, then the inclusive scan of delta A
-        // over the chunk (128 threads per head, warp scans joined in smem)
-        const int hd = h + vh;
-        const float bias = vbias, Ah = vA;
-        const int t0 = c * L, Lv = min(L, T - t0);
-        float dl[E2], al[E2], run = 0.f;
-#pragma unroll
-        for (int e = 0; e < E2; ++e) {
-          const int l = vt * E2 + e;
-          dl[e] = l < Lv ? dt_softplus(vin[e] + bias) : 0.f;
+        for (int e = 0; e < EV; ++e) {
+          const int l = ev * EV + e;
+          dl[e] = l < Lv ? dt_softplus(__bfloat162float(a.dt[((int64_t)b * T + t0 + l) * H + hd]) +
+                                       bias)
+                         : 0.f;
           run += dl[e] * Ah;
           al[e] = run;
         }
@@ -327,32 +276,84 @@ __global__ void __launch_bounds__(kStateThreads, 1)
           const float o = __shfl_up_sync(0xffffffffu, incl, off);
           if (lane >= off) incl += o;
         }
-        if (lane == 31) s_scan[warp] = incl;
-        conv_sync();
-        float pre = incl - run;  // exclusive prefix within the warp
-        for (int kk = 0; kk < (warp & 3); ++kk) pre += s_scan[4 * vh + kk];
-        const int64_t cv = (((int64_t)b * a.H + hd) * nc + c) * L;
+        if (lane == 31) s_scan[q] = incl;
+        epi_sync();
+        const float pre = incl - run + ((q & 1) ? s_scan[q - 1] : 0.f);  // exclusive prefix
 #pragma unroll
-        for (int e = 0; e < E2; ++e) {
-          const int l = vt * E2 + e;
+        for (int e = 0; e < EV; ++e) {
+          const int l = ev * EV + e;
           al[e] += pre;
           a.delta[cv + l] = dl[e];
           a.acs[cv + l] = al[e];
         }
-        if (vt == 127) s_alast[vh] = al[E2 - 1];  // a[L-1] as written
-        conv_sync();
-        const float alast = s_alast[vh];
+        if (ev == 63) s_alast[eh] = al[EV - 1];  // a[L-1] as written
+        epi_sync();
+        const float alast = s_alast[eh];
 #pragma unroll
-        for (int e = 0; e < E2; ++e) w[vh * L + vt * E2 + e] = __expf(alast - al[e]) * dl[e];
+        for (int e = 0; e < EV; ++e) w[ev * EV + e] = __expf(alast - al[e]) * dl[e];
       } else {
 #pragma unroll
-        for (int e = 0; e < E2; ++e) w[vh * L + vt * E2 + e] = __expf(vin[e]);
+        for (int e = 0; e < EV; ++e) w[ev * EV + e] = __expf(a.acs[cv + ev * EV + e]);
       }
-      conv_sync();  // w complete; s_scan / s_alast free again
-      if (k + 1 < nk) load_vec(k + 1);
-      // after an expired wait the loop still runs to the end (its waits
-      // return at once), so every converter thread meets the same named
-      // barriers
+    };
+
+    bool ok = true;
+    for (int k = 0; k < 2 && k < nk; ++k) {
+      compute_w(k);
+      warp_arrive(&bar_wf[k], lane);
+    }
+    int js = 0;                           // slabs this warp has stored
+    // after an expired wait the loop still runs to the end (its waits return
+    // at once), so all four warps meet the same named barriers
+    for (int k = 0; k < nk; ++k) {
+      const int buf = k & 1;
+      ok = ok && __all_sync(0xffffffffu,
+                            mbar_wait(&bar_accf[buf], (k >> 1) & 1, status, &abort_flag));
+      fence_after_sync();
+      if (ok) {
+        int b, c, h;
+        decode(k, b, c, h);
+        const int row0 = (((b * nc + c) * H + h) * kSP) + 32 * q;  // rows (b, c, h, p) of out
+        const uint32_t ta = tm + buf * N + ((uint32_t)(32 * q) << 16);
+#pragma unroll
+        for (int s = 0; s < N / 32; ++s, ++js) {
+          float v[32];
+          tmem_ld16(ta + 32 * s, *reinterpret_cast<float(*)[16]>(v));
+          tmem_ld16(ta + 32 * s + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+          tmem_wait_ld();
+          unsigned char* slab = stg + (js & 1) * (32 * 128);
+          if (js >= 2) {  // the store issued from this slab two slabs ago has read it
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(slab + sw128(lane, j)) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&mOut, 32 * s, row0, slab);
+            bulk_commit_group();
+          }
+        }
+        fence_before_sync();
+        warp_arrive(&bar_acce[buf], lane);
+      }
+      // item k's products are complete, so the converters no longer read
+      // sw[k & 1]: the weights of item k + 2 go there
+      if (k + 2 < nk) {
+        compute_w(k + 2);
+        if (ok) warp_arrive(&bar_wf[buf], lane);
+      }
+    }
+    if (lane == 0) bulk_wait_all();  // the stores have read shared memory and landed
+  } else {
+    // ------------------------------------------------------------ converters
+    bool ok = true;
+    for (int k = 0; ok && k < nk; ++k) {
+      const float* w = sw + (k & 1) * 2 * L;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_wf[k & 1], (k >> 1) & 1, status, &abort_flag));
       for (int kb = 0; kb < NKB; ++kb) {
         const int u = k * NKB + kb;
         const int sx = u % kNX, sa = u % kNA;
