@@ -191,6 +191,14 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, int c0, int c1, c
                    "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(src))
                : "memory");
 }
+__device__ __forceinline__ void tma_store_4d(const void* tmap, int c0, int c1, int c2, int c3,
+                                             const void* src) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+          tmap),
+      "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(src))
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
