@@ -88,10 +88,10 @@ struct ChunkLayout {
   static constexpr int oDer = oVec + 4 * L * 4;                    // [kNDer][a2, sx, cf][L]
   static constexpr int oRed = oDer + kNDer * 3 * L * 4;            // [3][kCG][128] row partials
   static constexpr int kEnd = (oRed + 3 * kCG * 128 * 4 + 1023) / 1024 * 1024;
-  // FWD with fp32 y: each conversion warp stages its 32 x 16 block of a head's
-  // y (2 KB) for one TMA store; the column operand's rows are dead once C.B^T
+  // FWD / DX: each conversion warp stages its 32 x 16 block of a head's y or
+  // dx (2 KB) for one TMA store; the column operand's rows are dead once C.B^T
   // is formed, so the staging reuses them when they are large enough
-  static constexpr int kStg = MODE == kFwd ? kConvWarps * 2048 : 0;
+  static constexpr int kStg = MODE == kFwd || MODE == kDx ? kConvWarps * 2048 : 0;
   static constexpr bool kStgInCol = kCol >= kStg;
   static constexpr int oStg = kStgInCol ? oCol : kEnd;
   static constexpr int kBytes = kEnd + (kStgInCol ? 0 : kStg) + 1024;
@@ -154,8 +154,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     k_chunk_tc(const __grid_constant__ CUtensorMap mRow, const __grid_constant__ CUtensorMap mCol,
                const __grid_constant__ CUtensorMap mOps, const __grid_constant__ CUtensorMap mHR,
                const ChunkArgs a) {
-  // mHR: DC / DB the tile's dy (x) rows; FWD with fp32 y the map y is stored
-  // through (fp32 (B, T, H, 64), boxes of 16 x 1 x 32 rows, 64-byte swizzle)
+  // mHR: DC / DB the tile's dy (x) rows; FWD (fp32 y) and DX the map y or dx
+  // is stored through (fp32 (B, T, H, 64), boxes of 16 x 1 x 32, 64-byte swizzle)
   using LY = ChunkLayout<N, L, MODE>;
   constexpr bool REV = LY::kRev, S1M = LY::kS1;
   constexpr int LT = LY::kLT, NLT = L / LT, NP = LY::kNP;
@@ -665,7 +665,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
       // DX: this thread's x values of its row, loaded from global memory when
       // its head starts (xa); head i's epilogue runs during head i + 1 (xb)
       uint4 xa[kCPT] = {}, xb[kCPT] = {};
-      int n_ystores = 0;  // FWD: TMA stores this warp has issued
+      int n_ostores = 0;  // FWD / DX: TMA stores this warp has issued
       auto prefetch_x = [&](int i, uint4 (&xr)[kCPT]) {
         if constexpr (MODE == kDx) {
           const int64_t off = (((int64_t)b * T + t0 + r) * H + h_begin + i) * 64 + kPC * cq;
@@ -703,40 +703,16 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         const int orr = r - col0;
         const float Dh = a.D ? a.D[h] : 0.f;
         float pd = 0.f, pq = 0.f, pdd = 0.f;
-        constexpr bool kTmaY = MODE == kFwd && sizeof(Tout) == 4;
-        if constexpr (kTmaY) {
-          // y rows of this warp's 32 x 16 block -> staging -> one TMA store
-          // (rows past seqlen are clipped by the store)
-          unsigned char* stg = base + LY::oStg + warp * 2048;
-          if (ok) {
-            if (n_ystores > 0) {  // the previous head's store has read the staging
-              if (lane == 0) bulk_wait_read<0>();
-              __syncwarp();
-            }
-#pragma unroll
-            for (int k8 = 0; k8 < kCPT; ++k8) {
-              float ov[8], o[8];
-              unpack8(*reinterpret_cast<const uint4*>(orow + sw128(orr, kCPT * cq + k8)), ov);
-              const float* yk = yv[k8 >> 1] + 8 * (k8 & 1);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) o[e] = fmaf(Dh, ov[e], yk[e]);
-#pragma unroll
-              for (int j2 = 0; j2 < 2; ++j2) {
-                const int j = 2 * k8 + j2;  // 16-byte chunk of the 64-byte row
-                *reinterpret_cast<float4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
-                    make_float4(o[4 * j2], o[4 * j2 + 1], o[4 * j2 + 2], o[4 * j2 + 3]);
-              }
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0 && rw + t0 < T) {
-              tma_store_4d(&mHR, kPC * cq, h, t0 + rw, b, stg);
-              bulk_commit_group();
-            }
-            ++n_ystores;
-          }
+        // y (FWD, fp32) and dx (DX) leave through TMA: this warp's 32 x 16
+        // block goes to its staging slot, then one store (rows past seqlen
+        // are clipped by it); bf16 y is written directly
+        constexpr bool kTmaO = (MODE == kFwd && sizeof(Tout) == 4) || MODE == kDx;
+        unsigned char* stg = base + LY::oStg + warp * 2048;
+        if (kTmaO && ok && n_ostores > 0) {  // the previous head's store has read the slot
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
         }
-        if (!kTmaY && ok && live) {
+        if (ok && (kTmaO || live)) {
           const float dr = MODE == kDx ? dsx[r] : 0.f;
           const int64_t ooff = (((int64_t)b * T + t0 + r) * H + h) * 64 + kPC * cq;
 #pragma unroll
@@ -760,17 +736,29 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 pdd = fmaf(xv[e], ov[e], pdd);
               }
             }
-            Tout* op = static_cast<Tout*>(a.out) + ooff + 8 * k8;
-            if constexpr (sizeof(Tout) == 4) {
-              float* of = reinterpret_cast<float*>(op);
-              *reinterpret_cast<float4*>(of) = make_float4(o[0], o[1], o[2], o[3]);
-              *reinterpret_cast<float4*>(of + 4) = make_float4(o[4], o[5], o[6], o[7]);
+            if constexpr (kTmaO) {
+#pragma unroll
+              for (int j2 = 0; j2 < 2; ++j2) {
+                const int j = 2 * k8 + j2;  // 16-byte chunk of the 64-byte row (64-byte swizzle)
+                *reinterpret_cast<float4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                    make_float4(o[4 * j2], o[4 * j2 + 1], o[4 * j2 + 2], o[4 * j2 + 3]);
+              }
             } else {
+              Tout* op = static_cast<Tout*>(a.out) + ooff + 8 * k8;
               *reinterpret_cast<uint4*>(op) =
                   make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]),
                              pack_bf16(o[6], o[7]));
             }
           }
+        }
+        if (kTmaO && ok) {
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0 && rw + t0 < T) {
+            tma_store_4d(&mHR, kPC * cq, h, t0 + rw, b, stg);
+            bulk_commit_group();
+          }
+          ++n_ostores;
         }
         warp_arrive(&bar_ops_empty[st], lane);
         if constexpr (MODE == kDx) {
@@ -810,8 +798,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         for (int kp = 0; kp < NP; ++kp) state_panel(i, kp);
       }
       if (hb > 0) epilogue(hb - 1, xa);
-      if constexpr (MODE == kFwd)
-        if (lane == 0) bulk_wait_all();  // y stores have read the staging and landed
+      if (lane == 0) bulk_wait_all();  // y / dx stores have read the staging and landed
     } else {
       uint4 hrow[kCPT];  // this thread's values of its row of dy (DC) or x (DB)
       for (int i = 0; i < hb; ++i) {
@@ -929,20 +916,6 @@ bool make_map(CUtensorMap* m, const void* ptr, int inner, int X, int T, int B) {
   return make_tma_map(m, ptr, inner, X, T, B, 1, 128);
 }
 
-// Map of the fp32 y (B, T, H, 64) for the forward's TMA stores: boxes of 16
-// columns x one head x 32 rows, 64-byte swizzle (each conversion warp's block).
-bool make_y_map(CUtensorMap* m, void* y, int H, int T, int B) {
-  const auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[4] = {64, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
-  const cuuint64_t strides[3] = {64 * 4, (cuuint64_t)H * 64 * 4, (cuuint64_t)T * H * 64 * 4};
-  const cuuint32_t box[4] = {16, 1, 32, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int N, int L, int MODE, typename Tout>
 cudaError_t launch_chunk(const Dims& d, const CUtensorMap& mRow, const CUtensorMap& mCol,
                          const CUtensorMap& mOps, const CUtensorMap& mHR, const ChunkArgs& a,
@@ -1036,6 +1009,20 @@ bool make_tma_map(CUtensorMap* m, const void* ptr, int inner, int X, int T, int 
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Map of an fp32 (B, T, H, 64) tensor (y, dx) for TMA stores: boxes of 16
+// columns x one head x 32 rows, 64-byte swizzle (one warp's block).
+bool make_y_map(CUtensorMap* m, void* y, int H, int T, int B) {
+  const auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {64, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {64 * 4, (cuuint64_t)H * 64 * 4, (cuuint64_t)T * H * 64 * 4};
+  const cuuint32_t box[4] = {16, 1, 32, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool make_tma_map_f32(CUtensorMap* m, void* ptr, int inner, int64_t rows, int box_inner,
