@@ -49,32 +49,9 @@ def _terms(d: Dims):
     return dict(x=x, xf=xf, bc=bc, bcf=bcf, dtb=dtb, vec=vec, st=st, fin=fin, cb=cb, y=y)
 
 
-def tc_bwd_nblk(d: Dims) -> int:
-    """Head blocks per group of the tensor-core dB / dC kernels: the library's
-    launch-table entry for this shape when one is set, else its built-in rule
-    (fewest blocks giving >= 2 x 152 CTAs).  The dB / dC partials written and
-    summed scale with it."""
-    from . import _native, tuning
-    try:
-        lib = _native.load()
-    except (OSError, RuntimeError):   # library not built: the rule alone
-        lib = None
-    if lib is not None:
-        key = dict(batch=d.B, seqlen=d.T, nheads=d.H, headdim=d.P, dstate=d.N, ngroups=d.G,
-                   chunk_size=d.L)
-        return tuning.get_scan_config(key, lib=lib)[0]["bc_head_blocks"]
-    hpg = d.H // d.G
-    units = d.B * d.nc * (d.L // 128) * d.G
-    for nb in range(1, hpg + 1):
-        if hpg % nb == 0 and units * nb >= 2 * 152:
-            return nb
-    return hpg
-
-
 def kernel_bytes(name: str, d: Dims) -> int:
     """Algorithmic DRAM bytes of one launch of the kernel `name`."""
     t = _terms(d)
-    nb = tc_bwd_nblk(d)
     table = {
         # tensor-core path
         # chunk_state with chunk_cumsum inside: reads dt, writes delta and dA_cumsum
@@ -82,11 +59,13 @@ def kernel_bytes(name: str, d: Dims) -> int:
         "k_dstates_tc": t["x"] + t["bc"] + t["vec"] + t["st"],
         "k_scan_tc": t["x"] + 2 * t["bc"] + 2 * t["vec"] + t["st"] + t["y"],
         "k_scan_tc_dx": 2 * t["x"] + 2 * t["bc"] + 5 * t["vec"] + t["st"] + t["xf"],
-        "k_bwd_dc_tc": 2 * t["x"] + 2 * t["bc"] + 4 * t["vec"] + t["st"] + t["bcf"] * nb,
-        "k_bwd_db_tc": 2 * t["x"] + 2 * t["bc"] + 3 * t["vec"] + t["st"] + t["bcf"] * nb,
-        # ddA / ddt finalize + the dC / dB head-block sums in one launch
-        "k_bwd_tail_tc": (t["dtb"] + 7 * t["vec"] + d.B * d.T * d.H * 4
-                          + (2 * (t["bcf"] * nb + t["bcf"]) if nb > 1 else 0)),
+        # dC / dB: the method writes each gradient once; the head-block
+        # partials the kernels write instead when nb > 1 (and the tail sums)
+        # are the implementation's choice, not counted
+        "k_bwd_dc_tc": 2 * t["x"] + 2 * t["bc"] + 4 * t["vec"] + t["st"] + t["bcf"],
+        "k_bwd_db_tc": 2 * t["x"] + 2 * t["bc"] + 3 * t["vec"] + t["st"] + t["bcf"],
+        # ddA / ddt finalize (with the dC / dB head-block sums in the same launch)
+        "k_bwd_tail_tc": t["dtb"] + 7 * t["vec"] + d.B * d.T * d.H * 4,
         # forward
         "k_chunk_cumsum": t["dtb"] + 2 * t["vec"],
         "k_bmm_cb": 2 * t["bc"] + t["cb"],

@@ -224,6 +224,94 @@ def test_chunked_backward_matches_oracle(L):
         assert close(got[k], ref[k], 1e-10), k
 
 
+# ------------------------------------ the chunked oracle's own intermediates
+# Each intermediate of the chunked algorithm is the answer to a smaller
+# question the sequential recurrence (the C++ oracle) answers on its own:
+# the states on a prefix or on one chunk, gradients of a suffix.
+
+def _slice(args, t0, t1, init):
+    x, dt, dt_bias, A, Bm, Cm, D, _ = args
+    return (x[:, t0:t1], dt[:, t0:t1], dt_bias, A, Bm[:, t0:t1], Cm[:, t0:t1], D, init)
+
+
+@pytest.mark.parametrize("L", [16, 32])
+def test_chunked_states_are_recurrence_states(L):
+    """Hprev[c] is the recurrence's state after the prefix [0, cL); S_c its
+    state after chunk c alone from a zero start; e^{a_c[L-1]} the decay a
+    chunk applies to the state entering it (a run with x = 0 from init = 1);
+    delta is softplus(dt + dt_bias) with zeros past seqlen."""
+    args = rand_problem(T=100, P=5, N=7)
+    x, dt, dt_bias, A, Bm, Cm, D, init = args
+    T, H = x.shape[1], x.shape[2]
+    f = chunked.ssd_chunked_fwd(*args, L)
+    nc = f["S"].shape[1]
+    for c in range(nc):
+        t0, t1 = c * L, min(T, (c + 1) * L)
+        want = init if c == 0 else oracle.ssd_fwd(*_slice(args, 0, t0, init))[1]
+        assert close(f["Hprev"][:, c], want, 1e-10), c
+        zero = np.zeros_like(init)
+        assert close(f["S"][:, c], oracle.ssd_fwd(*_slice(args, t0, t1, zero))[1], 1e-10), c
+        ones = np.ones_like(init)
+        sl = list(_slice(args, t0, t1, ones))
+        sl[0] = np.zeros_like(sl[0])
+        decay = oracle.ssd_fwd(*sl)[1][:, :, 0, 0]               # (B, H)
+        assert close(np.exp(f["a"][:, :, c, -1]), decay, 1e-12), c
+    v = dt + dt_bias[None, None, :]
+    want_delta = np.log1p(np.exp(v)).transpose(0, 2, 1)          # (B, H, T)
+    got = f["delta"].reshape(x.shape[0], H, -1)
+    assert close(got[:, :, :T], want_delta, 1e-14)
+    assert np.all(got[:, :, T:] == 0.0)
+
+
+@pytest.mark.parametrize("L", [16, 32])
+def test_chunked_backward_intermediates_are_recurrence_gradients(L):
+    """dS_c (the gradient entering chunk c from later chunks) is the
+    recurrence's dinit of the suffix from chunk c + 1 on (dfinal at the last
+    chunk); dHs_c is the dinit of chunk c alone with no dfinal."""
+    args = rand_problem(T=100, P=5, N=7, seed=3)
+    x, dt, dt_bias, A, Bm, Cm, D, init = args
+    T = x.shape[1]
+    rng = np.random.default_rng(11)
+    dy = rng.standard_normal(x.shape)
+    dfinal = rng.standard_normal(init.shape)
+    g = chunked.ssd_chunked_bwd(*args, dy, dfinal, L)
+    Hprev = g["fwd"]["Hprev"]
+    nc = Hprev.shape[1]
+    for c in range(nc):
+        t0, t1 = c * L, min(T, (c + 1) * L)
+        if c == nc - 1:
+            want = dfinal
+        else:
+            want = oracle.ssd_bwd(*_slice(args, t1, T, Hprev[:, c + 1]), dy[:, t1:], dfinal)["dinit"]
+        assert close(g["dS"][:, c], want, 1e-10), c
+        own = oracle.ssd_bwd(*_slice(args, t0, t1, Hprev[:, c]), dy[:, t0:t1], None)["dinit"]
+        assert close(g["dHs"][:, c], own, 1e-10), c
+
+
+def test_chunked_ddA_from_the_recurrence_gradients():
+    """The per-position gradient w.r.t. delta_r A that the chunked backward
+    forms through its "stable" sums follows from the recurrence's own
+    gradients by the chain rule of delta_r = softplus(dt_r + dt_bias):
+    ddt_r = (<x_r, u_r> + A ddA_r) softplus'(v_r), with u_r = (dx_r - D dy_r) /
+    delta_r (dx_r = delta_r u_r + D dy_r)."""
+    args = rand_problem(T=70, P=5, N=7, seed=5)
+    x, dt, dt_bias, A, Bm, Cm, D, init = args
+    Bt, T, H, _ = x.shape
+    rng = np.random.default_rng(12)
+    dy = rng.standard_normal(x.shape)
+    dfinal = rng.standard_normal(init.shape)
+    L = 16
+    g = chunked.ssd_chunked_bwd(*args, dy, dfinal, L)
+    ref = oracle.ssd_bwd(*args, dy, dfinal)
+    v = dt + dt_bias[None, None, :]
+    delta = np.log1p(np.exp(v))
+    sig = 1.0 / (1.0 + np.exp(-v))
+    u = (ref["dx"] - D[None, None, :, None] * dy) / delta[..., None]
+    want = (ref["ddt"] / sig - np.einsum("bthp,bthp->bth", x, u)) / A[None, None, :]
+    got = g["ddA"].reshape(Bt, H, -1)[:, :, :T].transpose(0, 2, 1)
+    assert close(got, want, 1e-8)
+
+
 # ------------------------------------------------------------- backward pins
 
 def _loss(args, dy, dfinal):
