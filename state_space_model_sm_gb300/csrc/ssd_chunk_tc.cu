@@ -660,8 +660,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     };
 
     if constexpr (!S1M) {
-      // FWD / DX: a head's epilogue runs after the next head's first panel, so
-      // its last products finish while that panel is converted.
+      // FWD / DX: a head's epilogue runs after the next head's second panel,
+      // so its last products finish while those panels are converted.
       // DX: this thread's x values of its row, loaded from global memory when
       // its head starts (xa); head i's epilogue runs during head i + 1 (xb)
       uint4 xa[kCPT] = {}, xb[kCPT] = {};
@@ -791,9 +791,12 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
           for (int k = 0; k < kCPT; ++k) xb[k] = xa[k];  // the previous head's
         }
         prefetch_x(i, xa);
+        // the previous head's epilogue runs once two of this head's panels are
+        // handed over, so the MMA warp has both to work on meanwhile
+        const int jepi = npan > 1 ? 1 : 0;
         for (int j = 0; j < npan; ++j) {
           panel(i, j);
-          if (j == 0 && i > 0) epilogue(i - 1, xb);
+          if (j == jepi && i > 0) epilogue(i - 1, xb);
         }
         for (int kp = 0; kp < NP; ++kp) state_panel(i, kp);
       }
