@@ -954,7 +954,7 @@ cudaError_t chunk_fwd_nl(const Dims& d, const FwdArgs& f, const FwdWs& w, int nb
   if (!a.status) return cudaErrorUnknown;
   if (d.out_bf16) return launch_chunk<N, L, kFwd, bf16>(d, mC, mB, mX, mX, a, "k_scan_tc", s);
   CUtensorMap mY;
-  if (!make_y_map(&mY, f.y, d.H, d.T, d.B)) return cudaErrorInvalidValue;
+  if (!make_y_map(&mY, f.y, d.H, d.T, d.B, 16)) return cudaErrorInvalidValue;
   return launch_chunk<N, L, kFwd, float>(d, mC, mB, mX, mY, a, "k_scan_tc", s);
 }
 
@@ -1014,17 +1014,19 @@ bool make_tma_map(CUtensorMap* m, const void* ptr, int inner, int X, int T, int 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Map of an fp32 (B, T, H, 64) tensor (y, dx) for TMA stores: boxes of 16
-// columns x one head x 32 rows, 64-byte swizzle (one warp's block).
-bool make_y_map(CUtensorMap* m, void* y, int H, int T, int B) {
+// Map of an fp32 (B, T, H, 64) tensor (y, dx) for TMA stores: boxes of cols
+// (16 or 32) columns x one head x 32 rows (one warp's block), 64- or 128-byte
+// swizzle to match.
+bool make_y_map(CUtensorMap* m, void* y, int H, int T, int B, int cols) {
   const auto fn = encode_fn();
-  if (!fn) return false;
+  if (!fn || (cols != 16 && cols != 32)) return false;
   const cuuint64_t dims[4] = {64, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
   const cuuint64_t strides[3] = {64 * 4, (cuuint64_t)H * 64 * 4, (cuuint64_t)T * H * 64 * 4};
-  const cuuint32_t box[4] = {16, 1, 32, 1};
+  const cuuint32_t box[4] = {(cuuint32_t)cols, 1, 32, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            cols == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -183,9 +183,9 @@ bool make_tma_map(CUtensorMap* m, const void* ptr, int inner, int X, int T, int 
 // box_inner (32: 128 bytes) x box_rows, for TMA stores.
 bool make_tma_map_f32(CUtensorMap* m, void* ptr, int inner, int64_t rows, int box_inner,
                       int box_rows);
-// Map of an fp32 (B, T, H, 64) tensor (y, dx) for TMA stores: boxes of 16
-// columns x one head x 32 rows, 64-byte swizzle.
-bool make_y_map(CUtensorMap* m, void* y, int H, int T, int B);
+// Map of an fp32 (B, T, H, 64) tensor (y, dx) for TMA stores: boxes of cols
+// (16 or 32) columns x one head x 32 rows, 64- or 128-byte swizzle to match.
+bool make_y_map(CUtensorMap* m, void* y, int H, int T, int B, int cols);
 
 // The TMA-fed chunk kernels (ssd_chunk_tc.cu), over (batch, chunk, row tile,
 // group, block of nblk heads): chunk_scan (y from the state images in w.Himg),

@@ -101,7 +101,8 @@ __device__ __forceinline__ void group_sync(int id) {
 
 template <int N, int L, typename Tout, bool REV>
 __global__ void __launch_bounds__(512, 1)
-    k_scan_tc(const bf16* __restrict__ x, const bf16* __restrict__ Bm,
+    k_scan_tc(const __grid_constant__ CUtensorMap mOut, const bf16* __restrict__ x,
+              const bf16* __restrict__ Bm,
               const bf16* __restrict__ Cm, const bf16* __restrict__ dy,
               const float* __restrict__ delta, const float* __restrict__ acs,
               const unsigned char* __restrict__ simg, const float* __restrict__ D,
@@ -211,15 +212,24 @@ __global__ void __launch_bounds__(512, 1)
   constexpr uint32_t id_py = idesc_bf16(128, kP, 0, 1);
   constexpr uint32_t id_st = idesc_bf16(128, kP, 0, 0);
 
-  // cp.async of everything a head needs: its second-operand rows (sX), its
-  // inter-chunk state image (into the P buffer) and its raw a / delta.
-  auto prefetch = [&](int hh) {
+  // fp32 out leaves through TMA stores when the operand-row buffer can stage
+  // every warp's 32 x 32 block (4 KB each, 128-byte swizzle): each head's
+  // epilogue reads its own x / dy row from sX first, then the block is staged
+  // there and stored, and only then do the next head's rows come in
+  constexpr bool kTmaO = sizeof(Tout) == 4 && SM::kX >= 8 * 4096;
+  // cp.async of what a head needs, in two commit groups: its inter-chunk
+  // state image (into the P buffer) and raw a / delta, then its
+  // second-operand rows (sX), which the first P product waits for.
+  auto prefetch_x = [&](int hh) {
     for (int i = wtid; i < ncol * 8; i += 256) {
       const int cc = i >> 3, j = i & 7, col = col0 + cc;
       const bool v = col < Lv;
       cp_async16(sX + sw128(cc, j),
                  v ? opsrc + (((int64_t)b * T + t0 + col) * H + hh) * kP + j * 8 : opsrc, v);
     }
+  };
+  auto prefetch = [&](int hh) {
+    if constexpr (!kTmaO) prefetch_x(hh);
     const unsigned char* img = simg + ((((int64_t)b * nc + c) * H + hh) * (int64_t)SM::kImg);
     for (int i = wtid; i < SM::kImg / 16; i += 256) cp_async16(Pw + 16 * i, img + 16 * i, true);
     const int64_t cvh = (((int64_t)b * H + hh) * nc + c) * L;
@@ -230,11 +240,17 @@ __global__ void __launch_bounds__(512, 1)
   };
   if (h_begin + wg < h_end) prefetch(h_begin + wg);
   cp_async_commit();
+  if constexpr (kTmaO) {
+    if (h_begin + wg < h_end) prefetch_x(h_begin + wg);
+    cp_async_commit();
+  }
 
   for (int h = h_begin + wg; h < h_end; h += 2) {
     const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
     const float Dh = D ? D[h] : 0.f;
-    cp_async_wait<0>();
+    // the image and vectors (the operand rows may still be in flight)
+    if constexpr (kTmaO) cp_async_wait<1>();
+    else cp_async_wait<0>();
     group_sync(gbar);  // the raw vectors were copied by other threads of the group
     for (int i = wtid; i < L; i += 256) {
       const float a2 = sraw[i] * kLog2e, dl = sraw[L + i];
@@ -331,6 +347,7 @@ __global__ void __launch_bounds__(512, 1)
         }
         if (qg == 0) tmem_wait_ld();
       }
+      if (kTmaO && j == 0) cp_async_wait<0>();  // the operand rows
       fence_async_smem();
       fence_before_sync();
       group_sync(gbar);
@@ -354,18 +371,30 @@ __global__ void __launch_bounds__(512, 1)
     uint4 orow[4], xrow[4];
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-      orow[kk] = live ? *reinterpret_cast<const uint4*>(opsrc + rowoff + 32 * half + 8 * kk)
-                      : make_uint4(0, 0, 0, 0);
+      if constexpr (!kTmaO)
+        orow[kk] = live ? *reinterpret_cast<const uint4*>(opsrc + rowoff + 32 * half + 8 * kk)
+                        : make_uint4(0, 0, 0, 0);
       if constexpr (REV)
         xrow[kk] = live ? *reinterpret_cast<const uint4*>(x + rowoff + 32 * half + 8 * kk)
                         : make_uint4(0, 0, 0, 0);
     }
     ++n_done;
-    const bool ok = mbar_wait(&bar_done[wg], (n_done - 1) & 1, status, &abort_flag);
+    const bool ok =
+        __all_sync(0xffffffffu, mbar_wait(&bar_done[wg], (n_done - 1) & 1, status, &abort_flag));
     fence_after_sync();
-    // this head's MMAs are done: sX and the P buffer take the next head's data
+    // this head's MMAs are done: the P buffer (and, without the TMA epilogue,
+    // sX) take the next head's data
     if (h + 2 < h_end) prefetch(h + 2);
     cp_async_commit();
+    unsigned char* stg = sX + wq * 4096;  // this warp's staging (TMA epilogue)
+    if constexpr (kTmaO) {
+      // the row of the operand this thread's outputs need, from sX (rows
+      // past seqlen were zero-filled), before any warp stages over it
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        orow[kk] = *reinterpret_cast<const uint4*>(sX + sw128(r - col0, 4 * half + kk));
+      group_sync(gbar);
+    }
     float pd = 0.f, pq = 0.f, pdd = 0.f;  // rev: partial <x, u>, <x, state part>, <x, dy>
     if (ok) {
       const float ea = ex2_approx(ar2), es = ex2_approx(sa2[L - 1] - ar2);
@@ -376,7 +405,7 @@ __global__ void __launch_bounds__(512, 1)
         tmem_ld16(tlane + colY + 32 * half + 16 * c16, yv);
         tmem_ld16(tlane + colST + 32 * half + 16 * c16, st);
         tmem_wait_ld();
-        if (live) {
+        if (kTmaO || live) {
 #pragma unroll
           for (int k8 = 0; k8 < 2; ++k8) {
             float ov[8], o[8];
@@ -398,18 +427,39 @@ __global__ void __launch_bounds__(512, 1)
                 pdd = fmaf(xv[e], ov[e], pdd);
               }
             }
-            Tout* op = out + rowoff + 32 * half + 16 * c16 + 8 * k8;
-            if constexpr (sizeof(Tout) == 4) {
-              float* of = reinterpret_cast<float*>(op);
-              *reinterpret_cast<float4*>(of) = make_float4(o[0], o[1], o[2], o[3]);
-              *reinterpret_cast<float4*>(of + 4) = make_float4(o[4], o[5], o[6], o[7]);
+            if constexpr (kTmaO) {
+              const int j = 4 * c16 + 2 * k8;  // 16-byte chunks j, j + 1 of the 128-byte row
+              *reinterpret_cast<float4*>(stg + sw128(lane, j)) = make_float4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<float4*>(stg + sw128(lane, j + 1)) =
+                  make_float4(o[4], o[5], o[6], o[7]);
             } else {
-              *reinterpret_cast<uint4*>(op) =
-                  make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
-                             pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
+              Tout* op = out + rowoff + 32 * half + 16 * c16 + 8 * k8;
+              if constexpr (sizeof(Tout) == 4) {
+                float* of = reinterpret_cast<float*>(op);
+                *reinterpret_cast<float4*>(of) = make_float4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<float4*>(of + 4) = make_float4(o[4], o[5], o[6], o[7]);
+              } else {
+                *reinterpret_cast<uint4*>(op) =
+                    make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
+                               pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
+              }
             }
           }
         }
+      }
+      if constexpr (kTmaO) {
+        // one store of the warp's 32 rows x 32 columns (rows past seqlen are
+        // clipped by it); its reads of the staging end before sX is refilled
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (t0 + r0 + 32 * q < T) {
+            tma_store_4d(&mOut, 32 * half, h, (int)t0 + r0 + 32 * q, b, stg);
+            bulk_commit_group();
+          }
+          bulk_wait_read<0>();
+        }
+        __syncwarp();
       }
     }
     if constexpr (REV) {
@@ -428,11 +478,16 @@ __global__ void __launch_bounds__(512, 1)
     }
     fence_before_sync();
     group_sync(gbar);  // sX, sa, sd and the accumulators are reused by the next head
+    if constexpr (kTmaO) {
+      if (h + 2 < h_end) prefetch_x(h + 2);
+      cp_async_commit();
+    }
   }
     // both groups are done with this unit's C.B^T tile and buffers
     fence_before_sync();
     __syncthreads();
   }
+  if (lane == 0) bulk_wait_all();  // the dx stores have landed
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tm, 512);
@@ -623,8 +678,10 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
     int grid, per;
     scan_partition(d, sms, &grid, &per);
+    CUtensorMap mDX;
+    if (!make_y_map(&mDX, a.dx, d.H, d.T, d.B, 32)) return cudaErrorInvalidValue;
     SSD_LAUNCH("k_scan_tc_dx", s, kern<<<grid, 512, SM::kBytes, s>>>(
-        static_cast<const bf16*>(a.f.x), static_cast<const bf16*>(a.f.B), Cm, dy, w.delta, w.acs,
+        mDX, static_cast<const bf16*>(a.f.x), static_cast<const bf16*>(a.f.B), Cm, dy, w.delta, w.acs,
         static_cast<const unsigned char*>(w.dSimg), a.f.D, a.dx, w.ddir, w.qrow, w.ddiag, d.B, d.T,
         d.H, d.G, d.nc, per, status));
   }
