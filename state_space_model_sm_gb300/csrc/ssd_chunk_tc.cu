@@ -429,18 +429,23 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
           fence_after_sync();
           ok = produce_s1(0) && (npan < 2 || produce_s1(1));
           if (ok && npan <= 2) mma_commit(&bar_ops_empty[0]);  // x / dy rows read
+          int sa = -1;
           for (int j = 0; ok && j < npan; ++j) {
             ok = consume_p2(j);
             if (ok && j + 2 < npan) {
               ok = produce_s1(j + 2);
               if (ok && j + 3 == npan) mma_commit(&bar_ops_empty[0]);
             }
+            if (ok && j == npan - 2) {
+              // the state term's A operand: the slot the next-to-last P2 frees
+              // goes to the conversion warps now, so they form it right after
+              // the last P2 panel instead of after its products
+              sa = slot_take();
+              if (sa < 0) ok = false;
+              else mbar_arrive(&bar_slot_ready[sa]);
+            }
           }
           if (!ok) break;
-          // the state term's A operand: hand a free slot to the conversion warps
-          int sa = slot_take();
-          if (sa < 0) break;
-          mbar_arrive(&bar_slot_ready[sa]);
           if (!mbar_wait(&bar_img_full, i & 1, status, &abort_flag)) break;
           fence_after_sync();
           int sst = -1;
