@@ -312,15 +312,21 @@ int ssd_gated_norm_get_config(const ssd_norm_shape* shape, ssd_norm_config* out)
  * of the offline config generator of "Cutting autotuning overhead with an
  * automated config generator" (Fig. 4): a sweep finds the best launch per
  * shape ahead of time, and the table is applied when the library loads.
- *   scan_head_blocks: chunk_scan CTAs per (batch, chunk, row tile, group)
- *     split the group's heads into this many blocks;
- *   bc_head_blocks: the same for the dC and dB kernels, whose per-block
- *     partial sums live in the ssd_bwd workspace (so this field changes
- *     ssd_bwd_workspace_size: query the size after setting the table).
- * 0 keeps the built-in rule (the fewest blocks giving two CTAs per SM); a
- * nonzero value must divide nheads / ngroups and be at most 32. */
+ * Each kernel's CTAs cover (batch, chunk, 128-row tile, group, block of
+ * heads); with chunk 256 a chunk has two row tiles, one with twice the
+ * column panels of the other (the heavy tile, launched first).
+ *   scan_head_blocks: the blocks chunk_scan splits a group's heads into for
+ *     the heavy tile, scan_head_blocks_light for the other;
+ *   bc_head_blocks, bc_head_blocks_light: the same for the dC and dB
+ *     kernels, whose per-block partial sums live in the ssd_bwd workspace
+ *     (so they change ssd_bwd_workspace_size: query the size after setting
+ *     the table).
+ * With chunk 128 (one row tile) the light fields are ignored.  0 keeps the
+ * built-in rule's count (a list-scheduling model of the launch); a nonzero
+ * value must divide nheads / ngroups and be at most 32. */
 typedef struct {
   int32_t scan_head_blocks, bc_head_blocks;
+  int32_t scan_head_blocks_light, bc_head_blocks_light;
 } ssd_scan_config;
 
 /* Sets (config != NULL) or removes (NULL) the entry of shape's (batch,

@@ -99,7 +99,9 @@ class NormShape(ctypes.Structure):
 
 
 class ScanConfig(ctypes.Structure):
-    _fields_ = [("scan_head_blocks", ctypes.c_int32), ("bc_head_blocks", ctypes.c_int32)]
+    _fields_ = [("scan_head_blocks", ctypes.c_int32), ("bc_head_blocks", ctypes.c_int32),
+                ("scan_head_blocks_light", ctypes.c_int32),
+                ("bc_head_blocks_light", ctypes.c_int32)]
 
 
 class NormConfig(ctypes.Structure):

@@ -4,6 +4,8 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <queue>
+#include <vector>
 
 #include "ssd_internal.h"
 
@@ -54,14 +56,94 @@ bool same_shape(const ScanEntry& e, const Dims& d) {
          e.L == d.L;
 }
 
-// the built-in rule: the fewest head blocks per group that still give >= 2
-// CTAs per SM (the count of the GPU the tables were made on)
-int rule_nblk(const Dims& d) {
+// The built-in rule, a list-scheduling model of the launch: CTAs in grid
+// order (every CTA of the heavier row tile first) each go to the SM that
+// frees first, one at a time; a CTA costs its heads' 64-column operand
+// uses (column panels + 4 per head) plus 6 for its prologue (the tile's rows
+// and C.B^T).  The pair of head-block counts (divisors of the heads per
+// group, at most 32) with the shortest modelled launch wins, fewer CTAs on a
+// tie.  152 SMs: the GPU the tables were made on.  The model ranked the
+// measured layer-shape pairs in their measured order.
+constexpr int kRuleSms = 152;
+
+double model_makespan(int64_t n_heavy, double c_heavy, int64_t n_light, double c_light) {
+  std::priority_queue<double, std::vector<double>, std::greater<double>> sm;
+  for (int i = 0; i < kRuleSms; ++i) sm.push(0.0);
+  double end = 0.0;
+  auto place = [&](int64_t n, double cost) {
+    for (int64_t k = 0; k < n; ++k) {
+      const double t = sm.top() + cost;
+      sm.pop();
+      sm.push(t);
+      if (t > end) end = t;
+    }
+  };
+  place(n_heavy, c_heavy);
+  place(n_light, c_light);
+  return end;
+}
+
+HeadBlocks rule_blocks_uncached(const Dims& d) {
   const int hpg = d.H / d.G;
-  const int64_t units = (int64_t)d.B * d.nc * (d.L / 128) * d.G;
-  for (int nb = 1; nb <= hpg; ++nb)
-    if (hpg % nb == 0 && units * nb >= 2 * 152) return nb;
-  return hpg;
+  const int64_t units = (int64_t)d.B * d.nc * d.G;  // per row tile
+  std::vector<int> div;
+  for (int nb = 1; nb <= hpg && nb <= 32; ++nb)
+    if (hpg % nb == 0) div.push_back(nb);
+  const double o = 6.0, heavy_uses = d.L / 64 + 4, light_uses = 2 + 4;
+  HeadBlocks best{div[0], div[0]};
+  double best_t = 1e300;
+  int64_t best_n = 0;
+  if (d.L <= 128) {  // one row tile
+    for (const int nb : div) {
+      const double t = model_makespan(units * nb, (hpg / nb) * light_uses + o, 0, 0.0);
+      if (t < best_t - 1e-9 || (t < best_t + 1e-9 && units * nb < best_n)) {
+        best_t = t;
+        best_n = units * nb;
+        best = HeadBlocks{nb, nb};
+      }
+    }
+    return best;
+  }
+  for (const int nh : div)
+    for (const int nl : div) {
+      const double t = model_makespan(units * nh, (hpg / nh) * heavy_uses + o, units * nl,
+                                      (hpg / nl) * light_uses + o);
+      const int64_t n = units * (nh + nl);
+      if (t < best_t - 1e-9 || (t < best_t + 1e-9 && n < best_n)) {
+        best_t = t;
+        best_n = n;
+        best = HeadBlocks{nh, nl};
+      }
+    }
+  return best;
+}
+
+// the rule's choice per shape, computed once (the model takes milliseconds
+// at long-context shapes)
+struct RuleEntry {
+  int B, T, H, P, N, G, L;
+  HeadBlocks hb;
+};
+constexpr int kMaxRuleEntries = 64;
+RuleEntry g_rule_cache[kMaxRuleEntries];
+int g_rule_entries = 0, g_rule_next = 0;
+std::mutex g_rule_mu;
+
+HeadBlocks rule_blocks(const Dims& d) {
+  {
+    std::lock_guard<std::mutex> lk(g_rule_mu);
+    for (int i = 0; i < g_rule_entries; ++i) {
+      const RuleEntry& e = g_rule_cache[i];
+      if (e.B == d.B && e.T == d.T && e.H == d.H && e.P == d.P && e.N == d.N && e.G == d.G &&
+          e.L == d.L)
+        return e.hb;
+    }
+  }
+  const HeadBlocks hb = rule_blocks_uncached(d);
+  std::lock_guard<std::mutex> lk(g_rule_mu);
+  const int i = g_rule_entries < kMaxRuleEntries ? g_rule_entries++ : (g_rule_next++ % kMaxRuleEntries);
+  g_rule_cache[i] = RuleEntry{d.B, d.T, d.H, d.P, d.N, d.G, d.L, hb};
+  return hb;
 }
 
 bool scan_lookup(const Dims& d, ssd_scan_config* out) {
@@ -75,16 +157,25 @@ bool scan_lookup(const Dims& d, ssd_scan_config* out) {
 }
 }  // namespace
 
-int tc_scan_nblk(const Dims& d) {
-  ssd_scan_config c;
-  if (scan_lookup(d, &c) && c.scan_head_blocks > 0) return c.scan_head_blocks;
-  return rule_nblk(d);
+// a table field > 0 overrides the rule's count for that tile
+HeadBlocks pick_blocks(const Dims& d, int heavy, int light) {
+  HeadBlocks hb = rule_blocks(d);
+  if (heavy > 0) hb.heavy = heavy;
+  if (light > 0) hb.light = light;
+  if (d.L <= 128) hb.light = hb.heavy;  // one row tile
+  return hb;
 }
 
-int tc_bwd_nblk(const Dims& d) {
-  ssd_scan_config c;
-  if (scan_lookup(d, &c) && c.bc_head_blocks > 0) return c.bc_head_blocks;
-  return rule_nblk(d);
+HeadBlocks tc_scan_blocks(const Dims& d) {
+  ssd_scan_config c{};
+  if (!scan_lookup(d, &c)) return pick_blocks(d, 0, 0);
+  return pick_blocks(d, c.scan_head_blocks, c.scan_head_blocks_light);
+}
+
+HeadBlocks tc_bwd_blocks(const Dims& d) {
+  ssd_scan_config c{};
+  if (!scan_lookup(d, &c)) return pick_blocks(d, 0, 0);
+  return pick_blocks(d, c.bc_head_blocks, c.bc_head_blocks_light);
 }
 
 cudaError_t launch_check_finite(const void* p, int64_t n, bool is_bf16, cudaStream_t s) {
@@ -301,7 +392,7 @@ size_t ssd_bwd_workspace_size(const ssd_shape* shape) {
   if (make_dims(shape, &d) != SSD_OK) return 0;
   size_t total = bwd_offsets(d).total;
   if (tc_forward_supported(d)) {
-    const size_t t = tc_bwd_offsets(d, tc_bwd_nblk(d)).total;
+    const size_t t = tc_bwd_offsets(d, tc_bwd_blocks(d).max()).total;
     if (t > total) total = t;
   }
   return total;
@@ -391,8 +482,8 @@ int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
                   aligned(dC, 16) && aligned(init_states, 16) && aligned(dfinal_states, 16) &&
                   aligned(dinit_states, 16);
   if (tc) {
-    const int nblk = tc_bwd_nblk(d);  // once: the layout and the launch must agree
-    const TcBwdOffsets o = tc_bwd_offsets(d, nblk);
+    const HeadBlocks nb = tc_bwd_blocks(d);  // once: the layout and the launch must agree
+    const TcBwdOffsets o = tc_bwd_offsets(d, nb.max());
     if (!workspace || workspace_bytes < o.total || !aligned(workspace, kAlign))
       return SSD_ERR_WORKSPACE;
     TcBwdWs w;
@@ -413,7 +504,7 @@ int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
     w.dCp = reinterpret_cast<float*>(base + o.dCp);
     w.part = reinterpret_cast<float*>(base + o.part);
     w.seg = o.total > o.seg ? reinterpret_cast<float*>(base + o.seg) : nullptr;
-    w.nblk = nblk;
+    w.nb = nb;
     t_last_path = 1;
     if (tc_backward(d, a, w, s) != cudaSuccess) return SSD_ERR_CUDA;
     return check_bwd_outputs(d, a, s) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
@@ -520,7 +611,8 @@ int ssd_scan_set_config(const ssd_shape* shape, const ssd_scan_config* config) {
   if (make_dims(shape, &d) != SSD_OK) return SSD_ERR_INVALID_ARG;
   if (config) {
     const int hpg = d.H / d.G;
-    for (const int v : {config->scan_head_blocks, config->bc_head_blocks})
+    for (const int v : {config->scan_head_blocks, config->bc_head_blocks,
+                         config->scan_head_blocks_light, config->bc_head_blocks_light})
       if (v < 0 || v > 32 || (v > 0 && hpg % v != 0)) return SSD_ERR_INVALID_ARG;
   }
   std::lock_guard<std::mutex> lk(g_scan_mu);
@@ -541,10 +633,13 @@ int ssd_scan_set_config(const ssd_shape* shape, const ssd_scan_config* config) {
 int ssd_scan_get_config(const ssd_shape* shape, ssd_scan_config* out) {
   Dims d;
   if (!out || make_dims(shape, &d) != SSD_OK) return -SSD_ERR_INVALID_ARG;
-  ssd_scan_config c{0, 0};
+  ssd_scan_config c{};
   const bool set = scan_lookup(d, &c);
-  out->scan_head_blocks = tc_scan_nblk(d);
-  out->bc_head_blocks = tc_bwd_nblk(d);
+  const HeadBlocks sc = tc_scan_blocks(d), bc = tc_bwd_blocks(d);
+  out->scan_head_blocks = sc.heavy;
+  out->scan_head_blocks_light = sc.light;
+  out->bc_head_blocks = bc.heavy;
+  out->bc_head_blocks_light = bc.light;
   return set ? 1 : 0;
 }
 

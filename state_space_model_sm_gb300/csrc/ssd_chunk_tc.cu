@@ -110,7 +110,9 @@ struct ChunkArgs {
   float* ddir;               // DX
   float* qrow;               // DX
   float* ddiag;              // DX
-  int T, H, G, nc, hb, nblk;
+  int T, H, G, nc;
+  int nbt[2];  // head blocks per group of row tile 0 / 1 (the grid holds the heavier first)
+  int nblk;    // DC / DB: head-block slots per row of the partials (the larger of nbt)
   int* status;
 };
 
@@ -181,11 +183,18 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   float* sRed = reinterpret_cast<float*>(base + LY::oRed);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // heavier row tiles (more columns) first: FWD / DC the last tile, DX / DB the first
-  const int gz = gridDim.z / NLT, zt = blockIdx.z / gz, zr = blockIdx.z % gz;
-  const int c = blockIdx.x, b = blockIdx.y, tile = REV ? zt : NLT - 1 - zt;
-  const int g = zr / a.nblk, kb = zr % a.nblk;
-  const int H = a.H, T = a.T, nc = a.nc, hb = a.hb;
+  // heavier row tiles (more columns) first: FWD / DC the last tile, DX / DB the
+  // first; each tile cuts a group's heads into its own number of blocks
+  const int th = REV ? 0 : NLT - 1;  // the heavier tile
+  const int zh = NLT > 1 ? a.G * a.nbt[th] : 0;
+  const int tile = (int)blockIdx.z < zh || NLT == 1 ? th : NLT - 1 - th;
+  // (a select, not an index: a runtime index into the parameter struct would
+  // copy it to local memory)
+  const int nbk = tile == 0 ? a.nbt[0] : a.nbt[1];
+  const int zr = (int)blockIdx.z - (tile == th ? 0 : zh);
+  const int c = blockIdx.x, b = blockIdx.y;
+  const int g = zr / nbk, kb = zr % nbk;
+  const int H = a.H, T = a.T, nc = a.nc, hb = H / a.G / nbk;
   const int h_begin = g * (H / a.G) + kb * hb;
   const int r0 = tile * LT, col0 = REV ? r0 : 0, ncol = REV ? L - r0 : r0 + LT;
   const int npan = ncol / 64;
@@ -931,13 +940,13 @@ cudaError_t launch_chunk(const Dims& d, const CUtensorMap& mRow, const CUtensorM
   using LY = ChunkLayout<N, L, MODE>;
   auto kern = k_chunk_tc<N, L, MODE, Tout>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes);
-  const dim3 grid(d.nc, d.B, (L / 128) * d.G * a.nblk);
+  const dim3 grid(d.nc, d.B, d.G * (L > 128 ? a.nbt[0] + a.nbt[1] : a.nbt[0]));
   SSD_LAUNCH(name, s, kern<<<grid, kChunkThreads, LY::kBytes, s>>>(mRow, mCol, mOps, mHR, a));
   return cudaGetLastError();
 }
 
 template <int N, int L>
-cudaError_t chunk_fwd_nl(const Dims& d, const FwdArgs& f, const FwdWs& w, int nblk,
+cudaError_t chunk_fwd_nl(const Dims& d, const FwdArgs& f, const FwdWs& w, HeadBlocks nb,
                          cudaStream_t s) {
   CUtensorMap mB, mC, mX;
   if (!make_map(&mB, f.B, d.N, d.G, d.T, d.B) || !make_map(&mC, f.C, d.N, d.G, d.T, d.B) ||
@@ -953,8 +962,10 @@ cudaError_t chunk_fwd_nl(const Dims& d, const FwdArgs& f, const FwdWs& w, int nb
   a.H = d.H;
   a.G = d.G;
   a.nc = d.nc;
-  a.nblk = nblk;
-  a.hb = d.H / d.G / nblk;
+  // the heavy tile is the chunk's last (its rows see more columns)
+  a.nbt[0] = L > 128 ? nb.light : nb.heavy;
+  a.nbt[1] = nb.heavy;
+  a.nblk = nb.max();
   a.status = device_status_ptr();
   if (!a.status) return cudaErrorUnknown;
   if (d.out_bf16) return launch_chunk<N, L, kFwd, bf16>(d, mC, mB, mX, mX, a, "k_scan_tc", s);
@@ -964,7 +975,7 @@ cudaError_t chunk_fwd_nl(const Dims& d, const FwdArgs& f, const FwdWs& w, int nb
 }
 
 template <int N, int L>
-cudaError_t chunk_bwd_nl(const Dims& d, const BwdArgs& ba, const TcBwdWs& w, int nblk,
+cudaError_t chunk_bwd_nl(const Dims& d, const BwdArgs& ba, const TcBwdWs& w, HeadBlocks nb,
                          float* dCout, float* dBout, cudaStream_t s) {
   CUtensorMap mB, mC, mX, mDY;
   if (!make_map(&mB, ba.f.B, d.N, d.G, d.T, d.B) || !make_map(&mC, ba.f.C, d.N, d.G, d.T, d.B) ||
@@ -979,13 +990,14 @@ cudaError_t chunk_bwd_nl(const Dims& d, const BwdArgs& ba, const TcBwdWs& w, int
   a.H = d.H;
   a.G = d.G;
   a.nc = d.nc;
-  a.nblk = nblk;
-  a.hb = d.H / d.G / nblk;
+  a.nblk = nb.max();  // partial slots per row
   a.status = device_status_ptr();
   if (!a.status) return cudaErrorUnknown;
   cudaError_t e;
   // dC: rows l, S1 = dy.x^T, H_c images
-  ChunkArgs ac = a;
+  ChunkArgs ac = a;  // dC: the heavy tile is the chunk's last
+  ac.nbt[0] = L > 128 ? nb.light : nb.heavy;
+  ac.nbt[1] = nb.heavy;
   ac.img = static_cast<const unsigned char*>(w.Himg);
   ac.out = dCout;
   ac.msum = w.rowsum;
@@ -993,7 +1005,9 @@ cudaError_t chunk_bwd_nl(const Dims& d, const BwdArgs& ba, const TcBwdWs& w, int
   e = launch_chunk<N, L, kDc, float>(d, mC, mB, mX, mDY, ac, "k_bwd_dc_tc", s);
   if (e != cudaSuccess) return e;
   // dB: rows s, S1 = x.dy^T, dS images
-  ChunkArgs ab = a;
+  ChunkArgs ab = a;  // dB: the heavy tile is the chunk's first
+  ab.nbt[0] = nb.heavy;
+  ab.nbt[1] = nb.light;
   ab.img = static_cast<const unsigned char*>(w.dSimg);
   ab.out = dBout;
   ab.msum = w.colsum;
@@ -1048,20 +1062,20 @@ bool make_tma_map_f32(CUtensorMap* m, void* ptr, int inner, int64_t rows, int bo
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t tc_chunk_forward(const Dims& d, const FwdArgs& f, const FwdWs& w, int nblk,
+cudaError_t tc_chunk_forward(const Dims& d, const FwdArgs& f, const FwdWs& w, HeadBlocks nb,
                              cudaStream_t s) {
-  if (d.N == 128 && d.L == 256) return chunk_fwd_nl<128, 256>(d, f, w, nblk, s);
-  if (d.N == 128 && d.L == 128) return chunk_fwd_nl<128, 128>(d, f, w, nblk, s);
-  if (d.N == 64 && d.L == 256) return chunk_fwd_nl<64, 256>(d, f, w, nblk, s);
-  return chunk_fwd_nl<64, 128>(d, f, w, nblk, s);
+  if (d.N == 128 && d.L == 256) return chunk_fwd_nl<128, 256>(d, f, w, nb, s);
+  if (d.N == 128 && d.L == 128) return chunk_fwd_nl<128, 128>(d, f, w, nb, s);
+  if (d.N == 64 && d.L == 256) return chunk_fwd_nl<64, 256>(d, f, w, nb, s);
+  return chunk_fwd_nl<64, 128>(d, f, w, nb, s);
 }
 
-cudaError_t tc_chunk_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w, int nblk,
+cudaError_t tc_chunk_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w, HeadBlocks nb,
                               float* dCout, float* dBout, cudaStream_t s) {
-  if (d.N == 128 && d.L == 256) return chunk_bwd_nl<128, 256>(d, a, w, nblk, dCout, dBout, s);
-  if (d.N == 128 && d.L == 128) return chunk_bwd_nl<128, 128>(d, a, w, nblk, dCout, dBout, s);
-  if (d.N == 64 && d.L == 256) return chunk_bwd_nl<64, 256>(d, a, w, nblk, dCout, dBout, s);
-  return chunk_bwd_nl<64, 128>(d, a, w, nblk, dCout, dBout, s);
+  if (d.N == 128 && d.L == 256) return chunk_bwd_nl<128, 256>(d, a, w, nb, dCout, dBout, s);
+  if (d.N == 128 && d.L == 128) return chunk_bwd_nl<128, 128>(d, a, w, nb, dCout, dBout, s);
+  if (d.N == 64 && d.L == 256) return chunk_bwd_nl<64, 256>(d, a, w, nb, dCout, dBout, s);
+  return chunk_bwd_nl<64, 128>(d, a, w, nb, dCout, dBout, s);
 }
 
 }  // namespace ssd

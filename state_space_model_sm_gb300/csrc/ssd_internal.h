@@ -140,6 +140,13 @@ int simt_state_passing_bwd(const Dims& d, const float* dHs, const float* acs, co
 void simt_param_grads(const Dims& d, const float* part, float* dA, float* ddt_bias, float* dD,
                       cudaStream_t s);
 
+// Head blocks per group of the chunk kernels' two row tiles (see
+// tc_scan_blocks below).
+struct HeadBlocks {
+  int heavy, light;
+  int max() const { return heavy > light ? heavy : light; }
+};
+
 // Workspace of the tensor-core backward.
 struct TcBwdWs {
   float* delta;   // (B, H, nc, L)
@@ -159,19 +166,21 @@ struct TcBwdWs {
   float* dCp;     // (B, T, G, nblk, N)
   float* part;    // (B, H, nc, 3)
   float* seg;     // two-level state passing scratch, or nullptr
-  int nblk;       // head blocks of dB / dC (read from the launch table once per call)
+  HeadBlocks nb;  // head blocks of dB / dC (read from the launch table once per call)
 };
 
 // tcgen05 path (ssd_tc.cu): bf16 inputs, headdim 64, d_state 64 / 128,
 // chunk 128 / 256, an even number of heads per group.
 bool tc_forward_supported(const Dims& d);
 cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s);
-// Head blocks per group of the dB / dC kernels and of chunk_scan: the launch
-// table's entry for the shape (ssd_scan_set_config), else the built-in rule.
-// The workspace size and the launch read the same table, so they agree as
-// long as the entry does not change between the size query and the call.
-int tc_bwd_nblk(const Dims& d);
-int tc_scan_nblk(const Dims& d);
+// Head blocks per group of the chunk kernels' row tiles: `heavy` for the tile
+// with more column panels (first in the grid), `light` for the other (chunk
+// 256; equal to heavy at chunk 128, one tile).  From the launch table's entry
+// for the shape (ssd_scan_set_config), else the built-in rule.  The workspace
+// size and the launch read the same table, so they agree as long as the
+// entry does not change between the size query and the call.
+HeadBlocks tc_bwd_blocks(const Dims& d);
+HeadBlocks tc_scan_blocks(const Dims& d);
 cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w, cudaStream_t s);
 
 // Tensor map (for TMA) of a (B, T, X, inner) bf16 tensor, 128-byte swizzle,
@@ -191,9 +200,9 @@ bool make_y_map(CUtensorMap* m, void* y, int H, int T, int B, int cols);
 // group, block of nblk heads): chunk_scan (y from the state images in w.Himg),
 // and the backward's dC and dB (with the ddA row / column sums and ycs).
 // dCout / dBout receive (B, T, G, nblk, N) partials.
-cudaError_t tc_chunk_forward(const Dims& d, const FwdArgs& f, const FwdWs& w, int nblk,
+cudaError_t tc_chunk_forward(const Dims& d, const FwdArgs& f, const FwdWs& w, HeadBlocks nb,
                              cudaStream_t s);
-cudaError_t tc_chunk_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w, int nblk,
+cudaError_t tc_chunk_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w, HeadBlocks nb,
                               float* dCout, float* dBout, cudaStream_t s);
 
 // The TMA-fed chunk_state kernels (ssd_state_tc.cu): chunk_cumsum + chunk

@@ -587,15 +587,25 @@ __device__ __forceinline__ void finalize_block(const FinalizeArgs& f, int c, int
   }
 }
 
-// out[i, :] = sum_k in[i, k, :] over the nblk head-block partials, in order
+// Head-block partials of dC / dB: row (b, t, g) holds `stride` slots, of
+// which the first nb[tile of t] were written (the chunk's 128-row tile; each
+// tile has its own block count).
+struct PartialRows {
+  int stride, G, T, L;
+  int nb[2];
+};
+
+// out[i, :] = sum_k in[i, k, :] over the row's head-block partials, in order
 // (float4 per element i; N % 4 == 0).
 __device__ __forceinline__ void reduce_elem(const float4* __restrict__ in, float4* __restrict__ out,
-                                            int64_t i, int nblk, int N4) {
+                                            int64_t i, const PartialRows& pr, int N4) {
   const int64_t row = i / N4;
   const int n = (int)(i % N4);
-  float4 s = in[(row * nblk) * N4 + n];
-  for (int k = 1; k < nblk; ++k) {
-    const float4 v = in[(row * nblk + k) * N4 + n];
+  const int t = (int)((row / pr.G) % pr.T);
+  const int nb = (t % pr.L) < 128 ? pr.nb[0] : pr.nb[1];
+  float4 s = in[(row * pr.stride) * N4 + n];
+  for (int k = 1; k < nb; ++k) {
+    const float4 v = in[(row * pr.stride + k) * N4 + n];
     s.x += v.x;
     s.y += v.y;
     s.z += v.z;
@@ -613,7 +623,7 @@ template <int NT>
 __global__ void __launch_bounds__(NT)
     k_bwd_tail_tc(FinalizeArgs f, int nfin, const float4* __restrict__ dCp,
                   float4* __restrict__ dC, const float4* __restrict__ dBp, float4* __restrict__ dB,
-                  int nred, int64_t rows, int nblk, int N4) {
+                  int nred, int64_t rows, PartialRows prC, PartialRows prB, int N4) {
   const int blk = blockIdx.x;
   if (blk < nfin) {
     finalize_block<NT>(f, blk % f.nc, (blk / f.nc) % f.H, blk / (f.nc * f.H));
@@ -621,7 +631,7 @@ __global__ void __launch_bounds__(NT)
   }
   const int rb = blk - nfin, which = rb / nred;
   const int64_t i = (int64_t)(rb % nred) * NT + threadIdx.x;
-  if (i < rows * N4) reduce_elem(which ? dBp : dCp, which ? dB : dC, i, nblk, N4);
+  if (i < rows * N4) reduce_elem(which ? dBp : dCp, which ? dB : dC, i, which ? prB : prC, N4);
 }
 
 // ------------------------------------------------------------------ launch
@@ -643,7 +653,7 @@ cudaError_t launch_tc_forward_t(const Dims& d, const FwdArgs& a, const FwdWs& w,
     if (e != cudaSuccess) return e;
   }
   simt_state_passing(d, a, w, s);
-  const cudaError_t e = tc_chunk_forward(d, a, w, tc_scan_nblk(d), s);
+  const cudaError_t e = tc_chunk_forward(d, a, w, tc_scan_blocks(d), s);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -685,11 +695,11 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
         static_cast<const unsigned char*>(w.dSimg), a.f.D, a.dx, w.ddir, w.qrow, w.ddiag, d.B, d.T,
         d.H, d.G, d.nc, per, status));
   }
-  const int nblk = w.nblk;
+  const int nblk = w.nb.max();  // partial slots per row
   float* dCout = nblk == 1 ? a.dC : w.dCp;
   float* dBout = nblk == 1 ? a.dB : w.dBp;
   {
-    const cudaError_t e = tc_chunk_backward(d, a, w, nblk, dCout, dBout, s);
+    const cudaError_t e = tc_chunk_backward(d, a, w, w.nb, dCout, dBout, s);
     if (e != cudaSuccess) return e;
   }
   {
@@ -700,10 +710,15 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     const int64_t rows = (int64_t)d.B * d.T * d.G;
     const int N4 = d.N / 4;
     const int nred = nblk > 1 ? (int)((rows * N4 + L - 1) / L) : 0;
+    // dC's heavy tile is the chunk's last (its rows see more columns), dB's
+    // the first; with one tile both counts are the heavy one
+    const int c0 = L > 128 ? w.nb.light : w.nb.heavy;
+    const PartialRows prC{nblk, d.G, d.T, d.L, {c0, w.nb.heavy}};
+    const PartialRows prB{nblk, d.G, d.T, d.L, {w.nb.heavy, w.nb.light}};
     SSD_LAUNCH("k_bwd_tail_tc", s, k_bwd_tail_tc<L><<<nfin + 2 * nred, L, 0, s>>>(
         fa, nfin, reinterpret_cast<const float4*>(w.dCp), reinterpret_cast<float4*>(a.dC),
         reinterpret_cast<const float4*>(w.dBp), reinterpret_cast<float4*>(a.dB),
-        nred > 0 ? nred : 1, rows, nblk, N4));
+        nred > 0 ? nred : 1, rows, prC, prB, N4));
   }
   simt_param_grads(d, w.part, a.dA, a.ddt_bias, a.dD, s);
   return cudaGetLastError();

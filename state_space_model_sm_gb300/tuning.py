@@ -20,10 +20,11 @@ item, the shared-memory ring size aimed at, and the persistent CTAs per SM.
 
 The SSD chunk kernels have a table of their own (``ssd_scan_config``): how
 many blocks of heads the chunk_scan and the dC / dB CTAs split each group
-into.  ``sweep_scan`` times the forward + backward step of a workload for each
-candidate, ``--sweep-scan W[,W...] --out`` writes the table, and the packaged
-``tuning_tables/ssd_scan_gb300.json`` is applied at load like the norm's
-(``SSD_SCAN_TABLE`` names another table or ``none``).
+into, for the chunk's heavy row tile (more column panels) and its light one.
+``sweep_scan`` times the forward + backward step of a workload for each
+candidate pair, ``--sweep-scan W[,W...] --out`` writes the table, and the
+packaged ``tuning_tables/ssd_scan_gb300.json`` is applied at load like the
+norm's (``SSD_SCAN_TABLE`` names another table or ``none``).
 """
 from __future__ import annotations
 
@@ -42,7 +43,8 @@ SCAN_TABLE_KIND = "ssd_scan_launch_table"
 DEFAULT_SCAN_TABLE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "tuning_tables",
                                   "ssd_scan_gb300.json")
 _SCAN_KEYS = ("batch", "seqlen", "nheads", "headdim", "dstate", "ngroups", "chunk_size")
-_SCAN_FIELDS = ("scan_head_blocks", "bc_head_blocks")
+_SCAN_FIELDS = ("scan_head_blocks", "bc_head_blocks", "scan_head_blocks_light",
+                "bc_head_blocks_light")
 _DTYPES = {"f32": 0, "bf16": 1}
 _FIELDS = ("rows_per_item", "ring_kb", "ctas_per_sm")
 
@@ -157,14 +159,14 @@ def validate_scan_table(table: dict) -> None:
         raise ValueError("entries must be a list of at most 64")
     seen = set()
     for e in entries:
-        for k in _SCAN_KEYS + _SCAN_FIELDS:
+        for k in _SCAN_KEYS + _SCAN_FIELDS[:2]:
             if k not in e:
                 raise ValueError(f"entry misses {k!r}: {e}")
         H, G = int(e["nheads"]), int(e["ngroups"])
         if min(int(e[k]) for k in _SCAN_KEYS) < 1 or H % G:
             raise ValueError(f"bad shape in {e}")
         for k in _SCAN_FIELDS:
-            v = int(e[k])
+            v = int(e.get(k, 0))
             if v < 0 or v > 32 or (v > 0 and (H // G) % v):
                 raise ValueError(f"bad {k} in {e}")
         key = tuple(int(e[k]) for k in _SCAN_KEYS)
@@ -173,11 +175,13 @@ def validate_scan_table(table: dict) -> None:
         seen.add(key)
 
 
-def set_scan_config(shape: dict, scan_head_blocks=0, bc_head_blocks=0, lib=None) -> None:
+def set_scan_config(shape: dict, scan_head_blocks=0, bc_head_blocks=0, scan_head_blocks_light=0,
+                    bc_head_blocks_light=0, lib=None) -> None:
     """Sets the table entry of one SSD shape (``shape``: the _SCAN_KEYS);
-    zero fields keep the built-in rule."""
+    zero fields keep the built-in rule's count."""
     lib = lib or _native.load()
-    cfg = _native.ScanConfig(int(scan_head_blocks), int(bc_head_blocks))
+    cfg = _native.ScanConfig(int(scan_head_blocks), int(bc_head_blocks),
+                             int(scan_head_blocks_light), int(bc_head_blocks_light))
     st = lib.ssd_scan_set_config(ctypes.byref(_scan_shape(shape)), ctypes.byref(cfg))
     if st != 0:
         raise ValueError(f"ssd_scan_set_config: status {st}")
@@ -203,8 +207,8 @@ def get_scan_config(shape: dict, lib=None):
 def apply_scan_table(table: dict, lib=None) -> int:
     validate_scan_table(table)
     for e in table["entries"]:
-        set_scan_config({k: e[k] for k in _SCAN_KEYS}, e["scan_head_blocks"],
-                        e["bc_head_blocks"], lib=lib)
+        set_scan_config({k: e[k] for k in _SCAN_KEYS}, lib=lib,
+                        **{k: int(e.get(k, 0)) for k in _SCAN_FIELDS})
     return len(table["entries"])
 
 
@@ -249,99 +253,36 @@ def sweep_scan(workload: str, steps: int = 10, warmup: int = 3, max_blocks: int 
 
     hpg = s.nheads // s.ngroups
     blocks = [nb for nb in range(1, min(hpg, max_blocks) + 1) if hpg % nb == 0]
+    # (heavy, light) pairs; with chunk 128 there is one row tile
+    pairs = [(h, l) for h in blocks for l in blocks] if s.chunk_size > 128 else \
+        [(h, h) for h in blocks]
     saved, had = get_scan_config(key, lib=lib)
     clear_scan_config(key, lib=lib)
     default_cfg, _ = get_scan_config(key, lib=lib)
     default_us = time_us()
-    timings = []
     try:
         scan_t = []
-        for nb in blocks:
-            set_scan_config(key, nb, default_cfg["bc_head_blocks"], lib=lib)
-            scan_t.append((time_us(), nb))
+        for h, l in pairs:
+            set_scan_config(key, h, default_cfg["bc_head_blocks"], l,
+                            default_cfg["bc_head_blocks_light"], lib=lib)
+            scan_t.append((time_us(), (h, l)))
         best_scan = min(scan_t)[1]
-        for nb in blocks:
-            set_scan_config(key, best_scan, nb, lib=lib)
-            timings.append((time_us(), dict(scan_head_blocks=best_scan, bc_head_blocks=nb)))
+        timings = []
+        for h, l in pairs:
+            set_scan_config(key, best_scan[0], h, best_scan[1], l, lib=lib)
+            timings.append((time_us(), (h, l)))
     finally:
         if had:
-            set_scan_config(key, saved["scan_head_blocks"], saved["bc_head_blocks"], lib=lib)
+            set_scan_config(key, lib=lib, **saved)
         else:
             clear_scan_config(key, lib=lib)
-    best_us, best = min(timings, key=lambda x: x[0])
+    best_us, best_bc = min(timings)
+    best = dict(scan_head_blocks=best_scan[0], bc_head_blocks=best_bc[0],
+                scan_head_blocks_light=best_scan[1], bc_head_blocks_light=best_bc[1])
     return dict(**key, **best, workload=workload, tuned_us=round(best_us, 2),
                 default_us=round(default_us, 2), default=default_cfg,
-                scan_sweep={str(nb): round(us, 2) for us, nb in scan_t},
-                bc_sweep={str(c["bc_head_blocks"]): round(us, 2) for us, c in timings})
-
-
-def candidates(features: int) -> Iterable[dict]:
-    """Launch configurations worth timing for a row of ``features``."""
-    tpr = features // 8
-    rpcs = sorted({r for r in (1, 2, 4, 8, 16, 32, 64, 512 // max(tpr, 1))
-                   if r >= 1 and r * tpr <= 512 and (r * tpr) % 32 == 0})
-    for rpc in rpcs:
-        for ring in (32, 64, 96, 128):
-            for ctas in (1, 2, 3, 4):
-                yield dict(rows_per_item=rpc, ring_kb=ring, ctas_per_sm=ctas)
-
-
-def sweep_gated_norm(features: int, group_size: int, dtype: str = "bf16", rows: int = 16384,
-                     steps: int = 10, warmup: int = 3, seed: int = 0, configs=None) -> dict:
-    """Times forward + backward for every candidate configuration of one
-    shape on the current GPU (CUDA events around each step, a 512 MB L2
-    flush before each) and returns the best entry with the default's time."""
-    import torch
-
-    from . import gated_norm_bwd, gated_norm_fwd, gated_norm_workspace_bytes
-    lib = _native.load()
-    configs = list(configs if configs is not None else candidates(features))
-    if not configs:
-        raise ValueError(f"no launch configuration for {features} features (at most 4096)")
-    dev = torch.device("cuda", torch.cuda.current_device())
-    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
-    g = torch.Generator(device="cpu").manual_seed(seed)
-    y, z, dout = (torch.randn(rows, features, generator=g).to(dev, tdt) for _ in range(3))
-    w = (1.0 + 0.1 * torch.randn(features, generator=g)).to(dev)
-    flush = torch.empty(512 * 1024 * 1024 // 4, device=dev)
-    ws = torch.empty(gated_norm_workspace_bytes(y, group_size), dtype=torch.uint8, device=dev)
-    out, rstd = gated_norm_fwd(y, z, w, group_size)
-    grads = gated_norm_bwd(y, z, w, dout, group_size, rstd=rstd, workspace=ws)
-    stream = torch.cuda.current_stream(dev)
-
-    def time_us():
-        for _ in range(warmup):
-            gated_norm_fwd(y, z, w, group_size, out=out, rstd=rstd)
-            gated_norm_bwd(y, z, w, dout, group_size, rstd=rstd, workspace=ws, out=grads)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(steps)]
-        for a, b in ev:
-            flush.fill_(1.0)
-            a.record(stream)
-            gated_norm_fwd(y, z, w, group_size, out=out, rstd=rstd)
-            gated_norm_bwd(y, z, w, dout, group_size, rstd=rstd, workspace=ws, out=grads)
-            b.record(stream)
-        torch.cuda.synchronize()
-        return 1e3 * sum(a.elapsed_time(b) for a, b in ev) / steps
-
-    saved, had = get_norm_config(features, group_size, dtype, lib=lib)
-    clear_norm_config(features, group_size, dtype, lib=lib)
-    default_us = time_us()
-    default_cfg, _ = get_norm_config(features, group_size, dtype, lib=lib)
-    timings = []
-    try:
-        for cfg in configs:
-            set_norm_config(features, group_size, dtype, dtype, lib=lib, **cfg)
-            timings.append((time_us(), cfg))
-    finally:
-        if had:
-            set_norm_config(features, group_size, dtype, dtype, lib=lib, **saved)
-        else:
-            clear_norm_config(features, group_size, dtype, lib=lib)
-    best_us, best = min(timings, key=lambda t: t[0])
-    return dict(features=features, group_size=group_size, in_dtype=dtype, out_dtype=dtype,
-                **best, rows=rows, tuned_us=round(best_us, 2), default_us=round(default_us, 2),
-                default=default_cfg, candidates=len(timings))
+                scan_sweep={f"{h},{l}": round(us, 2) for us, (h, l) in scan_t},
+                bc_sweep={f"{h},{l}": round(us, 2) for us, (h, l) in timings})
 
 
 def main(argv=None):

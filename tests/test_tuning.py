@@ -160,6 +160,39 @@ def _scan_entry(**kw):
     return e
 
 
+def _model_rule(key, sms=152):
+    """The built-in rule re-derived here: list scheduling of the launch (the
+    heavy row tile's CTAs first, each to the SM that frees first), a CTA
+    costing (column panels + 4) per head plus 6; the best (heavy, light)
+    pair, fewer CTAs on a tie."""
+    import heapq
+    hpg = key["nheads"] // key["ngroups"]
+    nc = -(-key["seqlen"] // key["chunk_size"])
+    units = key["batch"] * nc * key["ngroups"]
+    divs = [d for d in range(1, min(hpg, 32) + 1) if hpg % d == 0]
+
+    def span(jobs):
+        heap = [0.0] * sms
+        end = 0.0
+        for n, c in jobs:
+            for _ in range(n):
+                t = heapq.heappop(heap) + c
+                heapq.heappush(heap, t)
+                end = max(end, t)
+        return end
+    best = None
+    if key["chunk_size"] <= 128:
+        cands = [((d, d), span([(units * d, hpg // d * 6 + 6)]), units * d) for d in divs]
+    else:
+        hu = key["chunk_size"] // 64 + 4
+        cands = [((h, l), span([(units * h, hpg // h * hu + 6), (units * l, hpg // l * 6 + 6)]),
+                  units * (h + l)) for h in divs for l in divs]
+    for pair, t, n in cands:
+        if best is None or t < best[1] - 1e-9 or (t < best[1] + 1e-9 and n < best[2]):
+            best = (pair, t, n)
+    return best[0]
+
+
 def test_scan_validate():
     tuning.validate_scan_table(_scan_table(_scan_entry(), _scan_entry(seqlen=2000)))
     for bad in (dict(scan_head_blocks=4), dict(bc_head_blocks=-1), dict(bc_head_blocks=33),
@@ -178,18 +211,59 @@ def test_scan_table_set_get_remove():
     tuning.clear_scan_config(_SSD_KEY)
     rule, from_table = tuning.get_scan_config(_SSD_KEY)
     assert not from_table
-    # 2 x 8 x 2 chunk tiles per head block: the rule takes the fewest blocks
-    # (a divisor of the 6 heads per group) giving at least 2 x 152 units
-    assert rule == dict(scan_head_blocks=6, bc_head_blocks=6)
+    h, l = _model_rule(_SSD_KEY)
+    # chunk 128: one row tile, so the light count equals the heavy one
+    assert rule == dict(scan_head_blocks=h, bc_head_blocks=h, scan_head_blocks_light=h,
+                        bc_head_blocks_light=h)
     tuning.set_scan_config(_SSD_KEY, 2, 3)
-    assert tuning.get_scan_config(_SSD_KEY) == (dict(scan_head_blocks=2, bc_head_blocks=3), True)
+    got, from_table = tuning.get_scan_config(_SSD_KEY)
+    assert from_table and got["scan_head_blocks"] == 2 and got["bc_head_blocks"] == 3
     tuning.set_scan_config(_SSD_KEY, 0, 1)
-    assert tuning.get_scan_config(_SSD_KEY)[0] == dict(scan_head_blocks=6, bc_head_blocks=1)
-    for bad in ((4, 0), (0, 5), (-1, 0), (33, 0)):
+    got = tuning.get_scan_config(_SSD_KEY)[0]
+    assert got["scan_head_blocks"] == h and got["bc_head_blocks"] == 1
+    for bad in ((4, 0), (0, 5), (-1, 0), (33, 0), (0, 0, 4, 0), (0, 0, 0, 5)):
         with pytest.raises(ValueError):
             tuning.set_scan_config(_SSD_KEY, *bad)
     tuning.clear_scan_config(_SSD_KEY)
     assert tuning.get_scan_config(_SSD_KEY) == (rule, False)
+
+
+@pytest.mark.parametrize("key", [
+    dict(batch=4, seqlen=4096, nheads=24, headdim=64, dstate=128, ngroups=1, chunk_size=256),
+    dict(batch=1, seqlen=700, nheads=12, headdim=64, dstate=64, ngroups=2, chunk_size=256),
+    dict(batch=2, seqlen=8192, nheads=64, headdim=64, dstate=128, ngroups=8, chunk_size=128),
+])
+def test_scan_rule_is_the_list_scheduling_model(key):
+    """The library's built-in (heavy, light) head blocks equal the model's,
+    re-derived in Python; table fields override one tile at a time."""
+    saved = _table_entry(key)
+    try:
+        tuning.clear_scan_config(key)
+        rule, from_table = tuning.get_scan_config(key)
+        h, l = _model_rule(key)
+        assert not from_table
+        assert (rule["scan_head_blocks"], rule["scan_head_blocks_light"]) == (h, l)
+        assert (rule["bc_head_blocks"], rule["bc_head_blocks_light"]) == (h, l)
+        if key["chunk_size"] > 128:
+            tuning.set_scan_config(key, 0, 0, 1, 0)
+            got = tuning.get_scan_config(key)[0]
+            assert got["scan_head_blocks"] == h and got["scan_head_blocks_light"] == 1
+            assert got["bc_head_blocks_light"] == l
+    finally:
+        tuning.clear_scan_config(key)
+        if saved is not None:
+            tuning.set_scan_config(key, **saved)
+
+
+def _table_entry(key):
+    """The packaged table's fields for key (as loaded), or None."""
+    if not os.path.exists(tuning.DEFAULT_SCAN_TABLE):
+        return None
+    with open(tuning.DEFAULT_SCAN_TABLE) as f:
+        for e in json.load(f)["entries"]:
+            if all(e[k] == key[k] for k in tuning._SCAN_KEYS):
+                return {k: int(e.get(k, 0)) for k in tuning._SCAN_FIELDS}
+    return None
 
 
 def test_scan_table_apply_and_env(tmp_path, monkeypatch):
@@ -199,7 +273,8 @@ def test_scan_table_apply_and_env(tmp_path, monkeypatch):
     monkeypatch.setenv("SSD_SCAN_TABLE", str(p))
     tuning.apply_default(tuning._native.load())
     key = dict(_SSD_KEY, seqlen=777)
-    assert tuning.get_scan_config(key) == (dict(scan_head_blocks=3, bc_head_blocks=2), True)
+    got, from_table = tuning.get_scan_config(key)
+    assert from_table and got["scan_head_blocks"] == 3 and got["bc_head_blocks"] == 2
     tuning.clear_scan_config(key)
 
 
@@ -214,20 +289,29 @@ def test_packaged_scan_table_is_valid_and_loaded():
         for e in t["entries"]:
             cfg, from_table = tuning.get_scan_config({k: e[k] for k in tuning._SCAN_KEYS})
             assert from_table
-            assert cfg == {k: e[k] for k in tuning._SCAN_FIELDS}
+            for k in tuning._SCAN_FIELDS:
+                if e.get(k, 0) > 0 and not (k.endswith("_light") and e["chunk_size"] <= 128):
+                    assert cfg[k] == e[k], k
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("scan_nb,bc_nb", [(1, 1), (2, 3), (6, 2)])
-def test_tuned_ssd_launch_computes_the_same(cuda_lib, scan_nb, bc_nb):
+@pytest.mark.parametrize("key,cfg", [
+    (_SSD_KEY, (1, 1, 0, 0)), (_SSD_KEY, (2, 3, 0, 0)), (_SSD_KEY, (6, 2, 0, 0)),
+    (dict(batch=1, seqlen=700, nheads=12, headdim=64, dstate=64, ngroups=2, chunk_size=256),
+     (2, 3, 3, 1)),
+    (dict(batch=1, seqlen=700, nheads=12, headdim=64, dstate=64, ngroups=2, chunk_size=256),
+     (6, 1, 1, 6)),
+])
+def test_tuned_ssd_launch_computes_the_same(cuda_lib, key, cfg):
     """Each head of a chunk tile is computed by the same arithmetic whichever
     head block holds it, so y, final_states, dx and ddt are bit-identical under
-    any table entry; dB and dC sum the heads of a group over a different
+    any table entry (including different counts for the two row tiles of a
+    256-row chunk); dB and dC sum the heads of a group over a different
     partition (per block, then over blocks), equal to rounding."""
     import torch
 
     from state_space_model_sm_gb300.inputs import SSDShape, make_inputs, to_torch
-    k = _SSD_KEY
+    k = key
     inp = make_inputs(SSDShape(k["batch"], k["seqlen"], k["nheads"], k["headdim"], k["dstate"],
                                k["ngroups"], k["chunk_size"]), seed=31, dtype="bf16",
                       init_std=0.1, with_dy=True, dfinal_std=0.1)
@@ -244,11 +328,11 @@ def test_tuned_ssd_launch_computes_the_same(cuda_lib, scan_nb, bc_nb):
     try:
         tuning.clear_scan_config(k)
         a = run()
-        tuning.set_scan_config(k, scan_nb, bc_nb)
+        tuning.set_scan_config(k, *cfg)
         b = run()
     finally:
         if had:
-            tuning.set_scan_config(k, saved["scan_head_blocks"], saved["bc_head_blocks"])
+            tuning.set_scan_config(k, **saved)
         else:
             tuning.clear_scan_config(k)
     assert cuda_lib.device_status() == 0
