@@ -17,15 +17,17 @@
 // blockIdx.x, blockIdx.x + gridDim.x, ...; head pair fastest, so the CTAs
 // running side by side share a chunk's Y rows in L2):
 //   warps 0-15  convert: per block the TMA-landed x (dy) rows times the
-//               item's weights w, split into bf16 hi + lo, into the MN-major
-//               A operand;
+//               item's weights w, split into bf16 hi + lo, stored as the A
+//               operand in tensor memory (lane m = 64 hh + p, two bf16 of
+//               consecutive l per column), so A costs shared memory neither
+//               a write nor the tensor core's read;
 //   warps 16-19 epilogue: TMEM accumulator -> shared-memory slabs -> TMA
 //               stores of the item's two 64 x N states; between items they
 //               also form the weights two items ahead (chunk_cumsum in MODE
 //               0), off the converters' path;
 //   warp 20     issues every tcgen05.mma (hi and lo A against the same Y);
 //   warp 21     issues every TMA copy (x / dy pair boxes, Y panels).
-// Rings: four raw-x stages, three Y stages, two A stages and two TMEM
+// Rings: four raw-x stages, three Y stages, two TMEM A stages and two TMEM
 // accumulators, each handed over by full / empty mbarriers; every wait is
 // bounded and records SSD_ERR_TIMEOUT on expiry.
 //
@@ -62,18 +64,18 @@ struct StateLayout {
   static constexpr int kX = kKB * 2 * 128;           // a block's x rows of the pair
   static constexpr int kYPanel = kKB * 128;          // 64 of Y's columns
   static constexpr int kY = (N / 64) * kYPanel;      // a block's Y rows
-  static constexpr int kAPanel = kKB * 128;          // one head of the A operand
-  static constexpr int kALo = 2 * kAPanel;           // offset of the lo part
-  static constexpr int kA = 2 * kALo;                // hi + lo, both heads
   static constexpr int oX = 0;
   static constexpr int oY = oX + kNX * kX;
-  static constexpr int oA = oY + kNY * kY;
-  static constexpr int oW = oA + kNA * kA;            // [2 items][2 heads][L] weights
+  static constexpr int oW = oY + kNY * kY;            // [2 items][2 heads][L] weights
   static constexpr int kStg = 2 * 32 * 128;            // per epilogue warp: two 32 x 32 fp32 slabs
   static constexpr int oStg = (oW + 2 * 2 * L * 4 + 1023) / 1024 * 1024;
   static constexpr int kBytes = oStg + kEpiW * kStg + 1024;
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
-  static_assert(kX % 1024 == 0 && kY % 1024 == 0 && kA % 1024 == 0, "1024-byte stages");
+  static_assert(kX % 1024 == 0 && kY % 1024 == 0, "1024-byte stages");
+  // TMEM: two N-column accumulators, then two 64-column A stages (a block's
+  // 64 values of l as hi / lo bf16 per 16-wide K group)
+  static constexpr uint32_t kColA = 2 * N;
+  static constexpr uint32_t kTmemCols = 2 * N + 2 * 64 > 256 ? 512 : 256;
 };
 
 __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
@@ -83,6 +85,18 @@ __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
 
 __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiT) : "memory");
+}
+
+// 16 fp32 values of this thread's TMEM lane -> one 16-wide K group of an A
+// operand in tensor memory: hi = rn_bf16(v) packed two per column in
+// [col, col + 8), lo = rn_bf16(v - hi) in [col + 8, col + 16).
+// Warp-collective.
+__device__ __forceinline__ void tmem_store_split16(uint32_t col, const float (&v)[16]) {
+  uint32_t h[8], l[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) split2_bf16(v[2 * e], v[2 * e + 1], h[e], l[e]);
+  tmem_st8u(col, h);
+  tmem_st8u(col + 8, l);
 }
 
 __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
@@ -153,7 +167,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     mbar_init(&bar_final, 1);
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(&tmem_base, 2 * N);
+  if (warp == 0) tmem_alloc(&tmem_base, LY::kTmemCols);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
@@ -201,8 +215,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
   } else if (warp == kMmaW) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(128, N, 1, 1);  // A and B MN-major
-      const uint64_t dA0 = sdesc(smem_u32(base + LY::oA), LY::kAPanel, 1024);
+      constexpr uint32_t idesc = idesc_bf16(128, N, 0, 1);  // A in TMEM, B MN-major
       const uint64_t dY0 = sdesc(smem_u32(base + LY::oY), LY::kYPanel, 1024);
       bool ok = true;
       for (int k = 0; ok && k < nk; ++k) {
@@ -218,13 +231,13 @@ __global__ void __launch_bounds__(kStateThreads, 1)
             break;
           }
           fence_after_sync();
-          const uint64_t ah = desc_add(dA0, sa * LY::kA), al = desc_add(ah, LY::kALo);
+          const uint32_t at = tm + LY::kColA + 64 * sa;
           const uint64_t yd = desc_add(dY0, sy * LY::kY);
 #pragma unroll
           for (int ks = 0; ks < kKB / 16; ++ks) {
-            mma_bf16(tm + buf * N, desc_add(ah, ks * 2048), desc_add(yd, ks * 2048), idesc,
-                     (kb > 0 || ks > 0) ? 1u : 0u);
-            mma_bf16(tm + buf * N, desc_add(al, ks * 2048), desc_add(yd, ks * 2048), idesc, 1u);
+            mma_bf16_ta(tm + buf * N, at + 16 * ks, desc_add(yd, ks * 2048), idesc,
+                        (kb > 0 || ks > 0) ? 1u : 0u);
+            mma_bf16_ta(tm + buf * N, at + 16 * ks + 8, desc_add(yd, ks * 2048), idesc, 1u);
           }
           mma_commit(&bar_ae[sa]);
           mma_commit(&bar_ye[sy]);
@@ -363,34 +376,35 @@ __global__ void __launch_bounds__(kStateThreads, 1)
           ok = __all_sync(0xffffffffu,
                           mbar_wait(&bar_ae[sa], ((u / kNA) - 1) & 1, status, &abort_flag));
         if (!ok) continue;
+        // this warp: TMEM lane quarter q (A rows m = 64 hh + p), K group lg
+        // (16 of the block's 64 values of l); a lane reads its (hh, p) column
+        // of 16 box rows R = 2 l + hh (2 bytes each; a warp's 32 lanes read
+        // 64 contiguous bytes of one row)
         const unsigned char* xs = base + LY::oX + sx * LY::kX;
-        unsigned char* ah = base + LY::oA + sa * LY::kA;
-        const float* wb = w + kb * kKB;
+        const int q = warp & 3, lg = warp >> 2;
+        const int m = 32 * q + lane, hx = m >> 6, p = m & 63;
+        const float* wb = w + hx * L + kb * kKB + 16 * lg;
+        const uint32_t pb = ((uint32_t)(p & 7)) * 2;
+        float v[16];
 #pragma unroll
-        for (int kk = 0; kk < kKB * 2 * 8 / kConvT; ++kk) {
-          // box row R = 2 l + hh of the x pair, 16-byte chunk j
-          const int i = tid + kk * kConvT, R = i >> 3, j = i & 7, l = R >> 1, hx = R & 1;
-          const uint4 raw = *reinterpret_cast<const uint4*>(xs + sw128(R, j));
-          const float wl = wb[hx * L + l];
-          const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            split2_bf16(__uint_as_float(wd[e] << 16) * wl,
-                        __uint_as_float(wd[e] & 0xFFFF0000u) * wl, hi[e], lo[e]);
-          const uint32_t off = hx * LY::kAPanel + sw128(l, j);
-          *reinterpret_cast<uint4*>(ah + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(ah + LY::kALo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        for (int e = 0; e < 16; ++e) {
+          const int R = 2 * (16 * lg + e) + hx;
+          const unsigned short raw = *reinterpret_cast<const unsigned short*>(
+              xs + sw128(R, (uint32_t)(p >> 3)) + pb);
+          v[e] = __uint_as_float((uint32_t)raw << 16) * wb[e];
         }
-        fence_async_smem();  // the A operand is read by the tensor core's proxy
-        warp_arrive(&bar_xe[sx], lane);
+        warp_arrive(&bar_xe[sx], lane);  // the x rows are read
+        const uint32_t at = tm + ((uint32_t)(32 * q) << 16) + LY::kColA + 64 * sa;
+        tmem_store_split16(at + 16 * lg, v);
+        tmem_wait_st();
+        fence_before_sync();  // the A operand is read by the tensor core
         warp_arrive(&bar_af[sa], lane);
       }
     }
   }
   fence_before_sync();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tm, 2 * N);
+  if (warp == 0) tmem_dealloc(tm, LY::kTmemCols);
 }
 
 template <int N, int L, int MODE>
