@@ -63,8 +63,13 @@ bool same_shape(const ScanEntry& e, const Dims& d) {
 // and C.B^T).  The pair of head-block counts (divisors of the heads per
 // group, at most 32) with the shortest modelled launch wins, fewer CTAs on a
 // tie.  152 SMs: the GPU the tables were made on.  The model ranked the
-// measured layer-shape pairs in their measured order.
+// measured layer-shape pairs in their measured order.  For dC / dB, more than
+// one block per tile also costs the tail's pass over the head-block partials
+// (each row's slots read, the sum written, for both gradients), converted at
+// the HBM copy rate into the same unit (one operand use ~ 1100 cycles at
+// 2.07 GHz).
 constexpr int kRuleSms = 152;
+constexpr double kUseSeconds = 1100.0 / 2.07e9, kHbmBytesPerSecond = 6.8e12;
 
 double model_makespan(int64_t n_heavy, double c_heavy, int64_t n_light, double c_light) {
   std::priority_queue<double, std::vector<double>, std::greater<double>> sm;
@@ -83,19 +88,24 @@ double model_makespan(int64_t n_heavy, double c_heavy, int64_t n_light, double c
   return end;
 }
 
-HeadBlocks rule_blocks_uncached(const Dims& d) {
+HeadBlocks rule_blocks_uncached(const Dims& d, bool partials) {
   const int hpg = d.H / d.G;
   const int64_t units = (int64_t)d.B * d.nc * d.G;  // per row tile
   std::vector<int> div;
   for (int nb = 1; nb <= hpg && nb <= 32; ++nb)
     if (hpg % nb == 0) div.push_back(nb);
   const double o = 6.0, heavy_uses = d.L / 64 + 4, light_uses = 2 + 4;
+  const double row_bytes = 2.0 * d.B * d.T * d.G * d.N * 4.0;  // dB and dC, one slot
+  auto tail = [&](int nmax) {
+    return partials && nmax > 1 ? row_bytes * (nmax + 1) / kHbmBytesPerSecond / kUseSeconds
+                                : 0.0;
+  };
   HeadBlocks best{div[0], div[0]};
   double best_t = 1e300;
   int64_t best_n = 0;
   if (d.L <= 128) {  // one row tile
     for (const int nb : div) {
-      const double t = model_makespan(units * nb, (hpg / nb) * light_uses + o, 0, 0.0);
+      const double t = model_makespan(units * nb, (hpg / nb) * light_uses + o, 0, 0.0) + tail(nb);
       if (t < best_t - 1e-9 || (t < best_t + 1e-9 && units * nb < best_n)) {
         best_t = t;
         best_n = units * nb;
@@ -107,7 +117,8 @@ HeadBlocks rule_blocks_uncached(const Dims& d) {
   for (const int nh : div)
     for (const int nl : div) {
       const double t = model_makespan(units * nh, (hpg / nh) * heavy_uses + o, units * nl,
-                                      (hpg / nl) * light_uses + o);
+                                      (hpg / nl) * light_uses + o) +
+                       tail(nh > nl ? nh : nl);
       const int64_t n = units * (nh + nl);
       if (t < best_t - 1e-9 || (t < best_t + 1e-9 && n < best_n)) {
         best_t = t;
@@ -122,28 +133,28 @@ HeadBlocks rule_blocks_uncached(const Dims& d) {
 // at long-context shapes)
 struct RuleEntry {
   int B, T, H, P, N, G, L;
-  HeadBlocks hb;
+  HeadBlocks scan, bc;  // chunk_scan; dC / dB (with the tail's partial sums)
 };
 constexpr int kMaxRuleEntries = 64;
 RuleEntry g_rule_cache[kMaxRuleEntries];
 int g_rule_entries = 0, g_rule_next = 0;
 std::mutex g_rule_mu;
 
-HeadBlocks rule_blocks(const Dims& d) {
+HeadBlocks rule_blocks(const Dims& d, bool bc) {
   {
     std::lock_guard<std::mutex> lk(g_rule_mu);
     for (int i = 0; i < g_rule_entries; ++i) {
       const RuleEntry& e = g_rule_cache[i];
       if (e.B == d.B && e.T == d.T && e.H == d.H && e.P == d.P && e.N == d.N && e.G == d.G &&
           e.L == d.L)
-        return e.hb;
+        return bc ? e.bc : e.scan;
     }
   }
-  const HeadBlocks hb = rule_blocks_uncached(d);
+  const HeadBlocks sc = rule_blocks_uncached(d, false), b = rule_blocks_uncached(d, true);
   std::lock_guard<std::mutex> lk(g_rule_mu);
   const int i = g_rule_entries < kMaxRuleEntries ? g_rule_entries++ : (g_rule_next++ % kMaxRuleEntries);
-  g_rule_cache[i] = RuleEntry{d.B, d.T, d.H, d.P, d.N, d.G, d.L, hb};
-  return hb;
+  g_rule_cache[i] = RuleEntry{d.B, d.T, d.H, d.P, d.N, d.G, d.L, sc, b};
+  return bc ? b : sc;
 }
 
 bool scan_lookup(const Dims& d, ssd_scan_config* out) {
@@ -158,8 +169,8 @@ bool scan_lookup(const Dims& d, ssd_scan_config* out) {
 }  // namespace
 
 // a table field > 0 overrides the rule's count for that tile
-HeadBlocks pick_blocks(const Dims& d, int heavy, int light) {
-  HeadBlocks hb = rule_blocks(d);
+HeadBlocks pick_blocks(const Dims& d, bool bc, int heavy, int light) {
+  HeadBlocks hb = rule_blocks(d, bc);
   if (heavy > 0) hb.heavy = heavy;
   if (light > 0) hb.light = light;
   if (d.L <= 128) hb.light = hb.heavy;  // one row tile
@@ -168,14 +179,14 @@ HeadBlocks pick_blocks(const Dims& d, int heavy, int light) {
 
 HeadBlocks tc_scan_blocks(const Dims& d) {
   ssd_scan_config c{};
-  if (!scan_lookup(d, &c)) return pick_blocks(d, 0, 0);
-  return pick_blocks(d, c.scan_head_blocks, c.scan_head_blocks_light);
+  if (!scan_lookup(d, &c)) return pick_blocks(d, false, 0, 0);
+  return pick_blocks(d, false, c.scan_head_blocks, c.scan_head_blocks_light);
 }
 
 HeadBlocks tc_bwd_blocks(const Dims& d) {
   ssd_scan_config c{};
-  if (!scan_lookup(d, &c)) return pick_blocks(d, 0, 0);
-  return pick_blocks(d, c.bc_head_blocks, c.bc_head_blocks_light);
+  if (!scan_lookup(d, &c)) return pick_blocks(d, true, 0, 0);
+  return pick_blocks(d, true, c.bc_head_blocks, c.bc_head_blocks_light);
 }
 
 cudaError_t launch_check_finite(const void* p, int64_t n, bool is_bf16, cudaStream_t s) {

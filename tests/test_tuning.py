@@ -160,11 +160,13 @@ def _scan_entry(**kw):
     return e
 
 
-def _model_rule(key, sms=152):
+def _model_rule(key, sms=152, partials=False):
     """The built-in rule re-derived here: list scheduling of the launch (the
     heavy row tile's CTAs first, each to the SM that frees first), a CTA
-    costing (column panels + 4) per head plus 6; the best (heavy, light)
-    pair, fewer CTAs on a tie."""
+    costing (column panels + 4) per head plus 6; for dC / dB (partials) more
+    than one block adds the tail's pass over the partials (2 B T G N 4 bytes
+    per slot read and per sum written, at 6.8e12 B/s, in units of 1100
+    cycles at 2.07 GHz); the best (heavy, light) pair, fewer CTAs on a tie."""
     import heapq
     hpg = key["nheads"] // key["ngroups"]
     nc = -(-key["seqlen"] // key["chunk_size"])
@@ -180,13 +182,20 @@ def _model_rule(key, sms=152):
                 heapq.heappush(heap, t)
                 end = max(end, t)
         return end
+    row_bytes = 2.0 * key["batch"] * key["seqlen"] * key["ngroups"] * key["dstate"] * 4.0
+
+    def tail(nmax):
+        if not partials or nmax <= 1:
+            return 0.0
+        return row_bytes * (nmax + 1) / 6.8e12 / (1100.0 / 2.07e9)
     best = None
     if key["chunk_size"] <= 128:
-        cands = [((d, d), span([(units * d, hpg // d * 6 + 6)]), units * d) for d in divs]
+        cands = [((d, d), span([(units * d, hpg // d * 6 + 6)]) + tail(d), units * d)
+                 for d in divs]
     else:
         hu = key["chunk_size"] // 64 + 4
-        cands = [((h, l), span([(units * h, hpg // h * hu + 6), (units * l, hpg // l * 6 + 6)]),
-                  units * (h + l)) for h in divs for l in divs]
+        cands = [((h, l), span([(units * h, hpg // h * hu + 6), (units * l, hpg // l * 6 + 6)])
+                  + tail(max(h, l)), units * (h + l)) for h in divs for l in divs]
     for pair, t, n in cands:
         if best is None or t < best[1] - 1e-9 or (t < best[1] + 1e-9 and n < best[2]):
             best = (pair, t, n)
@@ -211,10 +220,11 @@ def test_scan_table_set_get_remove():
     tuning.clear_scan_config(_SSD_KEY)
     rule, from_table = tuning.get_scan_config(_SSD_KEY)
     assert not from_table
-    h, l = _model_rule(_SSD_KEY)
+    h, _ = _model_rule(_SSD_KEY)
+    hb, _ = _model_rule(_SSD_KEY, partials=True)
     # chunk 128: one row tile, so the light count equals the heavy one
-    assert rule == dict(scan_head_blocks=h, bc_head_blocks=h, scan_head_blocks_light=h,
-                        bc_head_blocks_light=h)
+    assert rule == dict(scan_head_blocks=h, bc_head_blocks=hb, scan_head_blocks_light=h,
+                        bc_head_blocks_light=hb)
     tuning.set_scan_config(_SSD_KEY, 2, 3)
     got, from_table = tuning.get_scan_config(_SSD_KEY)
     assert from_table and got["scan_head_blocks"] == 2 and got["bc_head_blocks"] == 3
@@ -232,6 +242,7 @@ def test_scan_table_set_get_remove():
     dict(batch=4, seqlen=4096, nheads=24, headdim=64, dstate=128, ngroups=1, chunk_size=256),
     dict(batch=1, seqlen=700, nheads=12, headdim=64, dstate=64, ngroups=2, chunk_size=256),
     dict(batch=2, seqlen=8192, nheads=64, headdim=64, dstate=128, ngroups=8, chunk_size=128),
+    dict(batch=1, seqlen=131072, nheads=32, headdim=64, dstate=128, ngroups=1, chunk_size=256),
 ])
 def test_scan_rule_is_the_list_scheduling_model(key):
     """The library's built-in (heavy, light) head blocks equal the model's,
@@ -241,14 +252,15 @@ def test_scan_rule_is_the_list_scheduling_model(key):
         tuning.clear_scan_config(key)
         rule, from_table = tuning.get_scan_config(key)
         h, l = _model_rule(key)
+        bh, bl = _model_rule(key, partials=True)
         assert not from_table
         assert (rule["scan_head_blocks"], rule["scan_head_blocks_light"]) == (h, l)
-        assert (rule["bc_head_blocks"], rule["bc_head_blocks_light"]) == (h, l)
+        assert (rule["bc_head_blocks"], rule["bc_head_blocks_light"]) == (bh, bl)
         if key["chunk_size"] > 128:
             tuning.set_scan_config(key, 0, 0, 1, 0)
             got = tuning.get_scan_config(key)[0]
             assert got["scan_head_blocks"] == h and got["scan_head_blocks_light"] == 1
-            assert got["bc_head_blocks_light"] == l
+            assert got["bc_head_blocks_light"] == bl
     finally:
         tuning.clear_scan_config(key)
         if saved is not None:
