@@ -1107,8 +1107,9 @@ bool vec4_ok(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t
 
 // Segments of the two-level state passing: two levels only when the
 // (batch, head) grid alone (gx blocks per pair) would leave at least half the
-// SMs idle; then K segments of lseg chunks, about three blocks per SM in all.
-void seg_plan(const Dims& d, int gx, bool have_scratch, int* K, int* lseg) {
+// SMs idle (the backward: any SM idle, its per-chunk walk being longer); then
+// K segments of lseg chunks, about three blocks per SM in all.
+void seg_plan(const Dims& d, int gx, bool have_scratch, bool bwd, int* K, int* lseg) {
   *K = 1;
   *lseg = d.nc;
   const int kmax = have_scratch ? seg_max_segments(d) : 0;
@@ -1117,7 +1118,7 @@ void seg_plan(const Dims& d, int gx, bool have_scratch, int* K, int* lseg) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t base = (int64_t)gx * d.H * d.B;
-  if (2 * base > sms) return;
+  if (bwd ? base >= sms : 2 * base > sms) return;
   // at most three blocks per SM in all, so the segments run in one wave
   int k = (int)std::min<int64_t>(kmax, std::max<int64_t>(2, (3 * sms) / base));
   *lseg = (d.nc + k - 1) / k;
@@ -1129,7 +1130,7 @@ void launch_state_passing(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaS
   if (w.Himg) {  // tensor-core path: states as split-bf16 images only
     const int PN8 = PN / 8, gx = (PN8 + kThreads - 1) / kThreads;
     int K, lseg;
-    seg_plan(d, gx, w.seg != nullptr, &K, &lseg);
+    seg_plan(d, gx, w.seg != nullptr, false, &K, &lseg);
     const float4* in = nullptr;
     if (K > 1) {
       float4* E = reinterpret_cast<float4*>(w.seg);
@@ -1184,7 +1185,7 @@ int launch_state_passing_bwd(const Dims& d, const BwdArgs& a, const BwdWs& w, cu
   if (w.f.Himg && w.dSimg) {  // tensor-core path
     const int PN8 = PN / 8, nsplit = (PN8 + kThreads - 1) / kThreads;
     int K, lseg;
-    seg_plan(d, nsplit, w.f.seg != nullptr, &K, &lseg);
+    seg_plan(d, nsplit, w.f.seg != nullptr, true, &K, &lseg);
     const float4* out = nullptr;
     if (K > 1) {
       float4* E = reinterpret_cast<float4*>(w.f.seg);
