@@ -332,3 +332,25 @@ def test_two_level_state_passing(cuda_lib, name, shape, init_std):
     for k in ["dx", "ddt", "dA", "dB", "dC", "dD", "ddt_bias", "dinit"]:
         assert_close(k, g["dinit_states"] if k == "dinit" else g[k], ref[k], "bf16")
     assert cuda_lib.device_status() == 0
+
+
+def test_two_level_backward_only(cuda_lib):
+    """A (batch, head) grid of 128 blocks (32 heads): too many for a
+    two-level forward (more than half the SMs), too few for the backward's
+    longer walk, so only the backward's state passing is cut into segments."""
+    inp = make_inputs(SSDShape(1, 2000, 32, 64, 128, 1, 256), seed=43, dtype="bf16",
+                      init_std=0.3, with_dy=True, dfinal_std=0.5)
+    cuda_lib.profile_enable(True)
+    y, final = run_fwd(cuda_lib, inp)
+    g = run_bwd(cuda_lib, inp)
+    prof = cuda_lib.profile_read()
+    cuda_lib.profile_enable(False)
+    assert prof.get("k_state_passing_seg", (0, 0))[1] == 0, prof
+    assert prof.get("k_state_passing_bwd_seg", (0, 0))[1] == 2, prof
+    y_ref, f_ref = oracle_fwd(inp)
+    assert_close("y", to_np(y), y_ref, "bf16")
+    assert_close("final", to_np(final), f_ref, "bf16")
+    ref = oracle_bwd(inp)
+    for k in ["dx", "ddt", "dA", "dB", "dC", "dD", "ddt_bias", "dinit"]:
+        assert_close(k, g["dinit_states"] if k == "dinit" else g[k], ref[k], "bf16")
+    assert cuda_lib.device_status() == 0
