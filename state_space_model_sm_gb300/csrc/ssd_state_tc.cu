@@ -67,7 +67,7 @@ struct StateLayout {
   static constexpr int oX = 0;
   static constexpr int oY = oX + kNX * kX;
   static constexpr int oW = oY + kNY * kY;            // [2 items][2 heads][L] weights
-  static constexpr int kStg = 2 * 32 * 128;            // per epilogue warp: two 32 x 32 fp32 slabs
+  static constexpr int kStg = (N / 32) * 32 * 128;     // per epilogue warp: an item's 32 x N rows
   static constexpr int oStg = (oW + 2 * 2 * L * 4 + 1023) / 1024 * 1024;
   static constexpr int kBytes = oStg + kEpiW * kStg + 1024;
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
@@ -252,7 +252,8 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     // ------------------------------------------------------------ epilogue
     // Each warp owns 32 accumulator rows (its TMEM lane quarter) and writes
     // them 32 columns at a time: registers -> a 128-byte-swizzled slab in
-    // shared memory -> one TMA store, double-buffered per warp.
+    // shared memory -> one TMA store; a warp's slabs hold a whole item, so it
+    // waits for its stores to have read them only once per item.
     const int q = warp & 3;               // TMEM lane quarter of this warp
     const int et = tid - 32 * kEpi0;      // 0 .. 127
     unsigned char* stg = base + LY::oStg + q * LY::kStg;
@@ -265,6 +266,29 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     // Every epilogue thread calls it for every item (it holds named barriers).
     constexpr int EV = L / 64;
     const int eh = et >> 6, ev = et & 63;
+    // The inputs of item k's weights are loaded into registers before the
+    // epilogue of item k - 2 and used after it, so the epilogue hides their
+    // latency (every address is valid: positions past seqlen re-read the
+    // last one and are masked at use).
+    unsigned short vdt[EV];
+    float vin[EV], vbias = 0.f, vA = 0.f;
+    auto load_w = [&](int k) {
+      int b, c, h;
+      decode(k, b, c, h);
+      const int hd = h + eh, t0 = c * L, Lv = min(L, T - t0);
+      if constexpr (MODE == 0) {
+        vbias = (a.dt_bias ? a.dt_bias : a.A)[hd];
+        vA = a.A[hd];
+#pragma unroll
+        for (int e = 0; e < EV; ++e)
+          vdt[e] = reinterpret_cast<const unsigned short*>(
+              a.dt)[((int64_t)b * T + t0 + min(ev * EV + e, Lv - 1)) * H + hd];
+      } else {
+        const int64_t cv = (((int64_t)b * H + hd) * nc + c) * L;
+#pragma unroll
+        for (int e = 0; e < EV; ++e) vin[e] = a.acs[cv + ev * EV + e];
+      }
+    };
     auto compute_w = [&](int k) {
       int b, c, h;
       decode(k, b, c, h);
@@ -272,14 +296,12 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       float* w = sw + (k & 1) * 2 * L + eh * L;
       const int64_t cv = (((int64_t)b * H + hd) * nc + c) * L;
       if constexpr (MODE == 0) {
-        const float bias = a.dt_bias ? a.dt_bias[hd] : 0.f, Ah = a.A[hd];
+        const float bias = a.dt_bias ? vbias : 0.f, Ah = vA;
         float dl[EV], al[EV], run = 0.f;
 #pragma unroll
         for (int e = 0; e < EV; ++e) {
           const int l = ev * EV + e;
-          dl[e] = l < Lv ? dt_softplus(__bfloat162float(a.dt[((int64_t)b * T + t0 + l) * H + hd]) +
-                                       bias)
-                         : 0.f;
+          dl[e] = l < Lv ? dt_softplus(__uint_as_float((uint32_t)vdt[e] << 16) + bias) : 0.f;
           run += dl[e] * Ah;
           al[e] = run;
         }
@@ -306,12 +328,13 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         for (int e = 0; e < EV; ++e) w[ev * EV + e] = __expf(alast - al[e]) * dl[e];
       } else {
 #pragma unroll
-        for (int e = 0; e < EV; ++e) w[ev * EV + e] = __expf(a.acs[cv + ev * EV + e]);
+        for (int e = 0; e < EV; ++e) w[ev * EV + e] = __expf(vin[e]);
       }
     };
 
     bool ok = true;
     for (int k = 0; k < 2 && k < nk; ++k) {
+      load_w(k);
       compute_w(k);
       warp_arrive(&bar_wf[k], lane);
     }
@@ -320,6 +343,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     // at once), so all four warps meet the same named barriers
     for (int k = 0; k < nk; ++k) {
       const int buf = k & 1;
+      if (k + 2 < nk) load_w(k + 2);
       ok = ok && __all_sync(0xffffffffu,
                             mbar_wait(&bar_accf[buf], (k >> 1) & 1, status, &abort_flag));
       fence_after_sync();
@@ -328,17 +352,17 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         decode(k, b, c, h);
         const int row0 = (((b * nc + c) * H + h) * kSP) + 32 * q;  // rows (b, c, h, p) of out
         const uint32_t ta = tm + buf * N + ((uint32_t)(32 * q) << 16);
+        if (js > 0) {  // the previous item's stores have read the slabs
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+        }
 #pragma unroll
         for (int s = 0; s < N / 32; ++s, ++js) {
           float v[32];
           tmem_ld16(ta + 32 * s, *reinterpret_cast<float(*)[16]>(v));
           tmem_ld16(ta + 32 * s + 16, *reinterpret_cast<float(*)[16]>(v + 16));
           tmem_wait_ld();
-          unsigned char* slab = stg + (js & 1) * (32 * 128);
-          if (js >= 2) {  // the store issued from this slab two slabs ago has read it
-            if (lane == 0) bulk_wait_read<1>();
-            __syncwarp();
-          }
+          unsigned char* slab = stg + s * (32 * 128);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             *reinterpret_cast<float4*>(slab + sw128(lane, j)) =
