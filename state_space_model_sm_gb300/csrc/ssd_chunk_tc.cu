@@ -227,6 +227,10 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
+  // the next kernel may start once every CTA of this one holds its TMEM: a
+  // dependent CTA that allocates TMEM on the same SM then only waits for CTAs
+  // that need nothing from it
+  griddep_launch_dependents();
   const uint32_t tm = tmem_base;
   // slot uses per head: FWD / DX the P panels, then the state term's K panels;
   // DC the S1 panels, the state term's A operand and the state dot C.H_c^T; DB
@@ -247,6 +251,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
           tma_load_4d(sCol + kp * L * 128 + k2 * 128 * 128, &mCol, 64 * kp, g,
                       t0 + col0 + 128 * k2, b, &bar_unit);
       }
+      // the tile's rows above are inputs; a / delta and the state images
+      // come from the previous kernels (launched with launch_pdl)
+      griddep_wait();
       uint32_t n_vec[2] = {0, 0}, n_ops[2] = {0, 0}, n_img = 0;  // phases armed
       auto load_vec = [&](int i) -> bool {
         const int v = i & 1;
@@ -941,7 +948,8 @@ cudaError_t launch_chunk(const Dims& d, const CUtensorMap& mRow, const CUtensorM
   auto kern = k_chunk_tc<N, L, MODE, Tout>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes);
   const dim3 grid(d.nc, d.B, d.G * (L > 128 ? a.nbt[0] + a.nbt[1] : a.nbt[0]));
-  SSD_LAUNCH(name, s, kern<<<grid, kChunkThreads, LY::kBytes, s>>>(mRow, mCol, mOps, mHR, a));
+  SSD_LAUNCH(name, s, launch_pdl(kern, grid, dim3(kChunkThreads), LY::kBytes, s, mRow, mCol, mOps,
+                                 mHR, a));
   return cudaGetLastError();
 }
 

@@ -46,6 +46,39 @@ class LaunchScope {
     __VA_ARGS__;                                       \
   } while (0)
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may
+// start while the previous kernel on its stream is still running (once every
+// CTA of that one has called griddep_launch_dependents or exited), so its
+// prologue (TMEM, barriers, operand loads that depend on no earlier kernel)
+// overlaps that kernel's last wave.  Every such kernel calls griddep_wait
+// before it reads anything an earlier kernel of the call wrote, or writes
+// anything an earlier kernel may still read; griddep_wait returns once the
+// previous grid has completed and its writes are visible.  The first kernel
+// of an ssd_fwd / ssd_bwd call is launched normally: its inputs may come from
+// the caller's previous kernel.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------- pointers
 // delta = softplus(dt + dt_bias): the linear branch above 20, where
 // log(1 + e^v) equals v in fp32.
@@ -209,7 +242,8 @@ cudaError_t tc_chunk_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w,
 // state (writes delta, acs and S), and dstates (dHs from dy, C and acs).
 cudaError_t tc_chunk_state(const Dims& d, const FwdArgs& f, float* delta, float* acs, float* S,
                            cudaStream_t s);
+// pdl: launched with launch_pdl (inside a call, after its other kernels).
 cudaError_t tc_chunk_dstates(const Dims& d, const void* dy, const void* C, const float* acs,
-                             float* dHs, cudaStream_t s);
+                             float* dHs, bool pdl, cudaStream_t s);
 
 }  // namespace ssd

@@ -352,6 +352,8 @@ __global__ void __launch_bounds__(kThreads, 3)
                         const float4* __restrict__ init, unsigned char* __restrict__ img,
                         float4* __restrict__ final_state, int N, int H, int PN8, int L, int nc,
                         int K, int lseg, const float4* __restrict__ seg_in) {
+  griddep_launch_dependents();
+  griddep_wait();  // S and a come from the previous kernel (launched with launch_pdl)
   const int e = blockIdx.x * kThreads + threadIdx.x, h = blockIdx.y;
   const int b = kSeg ? blockIdx.z / K : blockIdx.z, sk = kSeg ? blockIdx.z % K : 0;
   if (e >= PN8) return;
@@ -467,6 +469,8 @@ __global__ void __launch_bounds__(kThreads, 3)
                             float* __restrict__ dlast_part, float4* __restrict__ dinit, int N,
                             int H, int PN8, int L, int nc, int K, int lseg,
                             const float4* __restrict__ seg_out) {
+  griddep_launch_dependents();
+  griddep_wait();  // dHs comes from the previous kernel (launched with launch_pdl)
   // grid (nsplit, H, B*K): segment sk = z % K walks chunks [sk*lseg, min(nc,
   // (sk+1)*lseg)) backwards from the gradient leaving it (dfinal for K == 1,
   // else seg_out (B, K, H, P, N)); only segment 0 writes dinit
@@ -1074,6 +1078,7 @@ __global__ void k_group_reduce(const float* __restrict__ perhead, float* __restr
 __global__ void k_param_grads(const float* __restrict__ part, float* __restrict__ dA,
                               float* __restrict__ ddt_bias, float* __restrict__ dD, int B, int H,
                               int nc) {
+  griddep_wait();  // the partials come from the previous kernel (launched with launch_pdl)
   const int h = blockIdx.x, lane = threadIdx.x;
   float a = 0.f, bb = 0.f, dd = 0.f;
   for (int i = lane; i < B * nc; i += 32) {
@@ -1142,7 +1147,7 @@ void launch_state_passing(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaS
       in = In;
     }
     auto kern = K > 1 ? k_state_passing_img<true> : k_state_passing_img<false>;
-    SSD_LAUNCH("k_state_passing", s, kern<<<dim3(gx, d.H, d.B * K), kThreads, 0, s>>>(
+    SSD_LAUNCH("k_state_passing", s, launch_pdl(kern, dim3(gx, d.H, d.B * K), dim3(kThreads), 0, s,
         reinterpret_cast<const float4*>(w.S), w.acs, reinterpret_cast<const float4*>(a.init),
         static_cast<unsigned char*>(w.Himg), reinterpret_cast<float4*>(a.final_state), d.N, d.H,
         PN8, d.L, d.nc, K, lseg, in));
@@ -1198,7 +1203,8 @@ int launch_state_passing_bwd(const Dims& d, const BwdArgs& a, const BwdWs& w, cu
       out = Out;
     }
     auto kern = K > 1 ? k_state_passing_bwd_img<true> : k_state_passing_bwd_img<false>;
-    SSD_LAUNCH("k_state_passing_bwd", s, kern<<<dim3(nsplit, d.H, d.B * K), kThreads, 0, s>>>(
+    SSD_LAUNCH("k_state_passing_bwd", s, launch_pdl(kern, dim3(nsplit, d.H, d.B * K),
+        dim3(kThreads), 0, s,
         reinterpret_cast<const float4*>(w.dHs), w.f.acs,
         static_cast<const unsigned char*>(w.f.Himg), reinterpret_cast<const float4*>(a.dfinal),
         static_cast<unsigned char*>(w.dSimg), w.dlast, reinterpret_cast<float4*>(a.dinit), d.N,
@@ -1336,7 +1342,8 @@ int simt_state_passing_bwd(const Dims& d, const float* dHs, const float* acs, co
 
 void simt_param_grads(const Dims& d, const float* part, float* dA, float* ddt_bias, float* dD,
                       cudaStream_t s) {
-  SSD_LAUNCH("k_param_grads", s, k_param_grads<<<d.H, 32, 0, s>>>(part, dA, ddt_bias, dD, d.B, d.H, d.nc));
+  SSD_LAUNCH("k_param_grads", s, launch_pdl(k_param_grads, dim3(d.H), dim3(32), 0, s, part, dA,
+                                            ddt_bias, dD, d.B, d.H, d.nc));
 }
 
 cudaError_t simt_backward(const Dims& d, const BwdArgs& a, const BwdWs& w, cudaStream_t s) {

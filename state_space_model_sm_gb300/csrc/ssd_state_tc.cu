@@ -171,6 +171,10 @@ __global__ void __launch_bounds__(kStateThreads, 1)
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
+  // the next kernel may start once every CTA of this one holds its TMEM: a
+  // dependent CTA that allocates TMEM on the same SM then only waits for CTAs
+  // that need nothing from it
+  griddep_launch_dependents();
   const uint32_t tm = tmem_base;
 
   if (warp == kProdW) {
@@ -254,6 +258,9 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     // them 32 columns at a time: registers -> a 128-byte-swizzled slab in
     // shared memory -> one TMA store; a warp's slabs hold a whole item, so it
     // waits for its stores to have read them only once per item.
+    // the epilogue warps read a (dstates) and write every global output, so
+    // they alone wait for the previous kernel (x / dy, B / C are inputs)
+    griddep_wait();
     const int q = warp & 3;               // TMEM lane quarter of this warp
     const int et = tid - 32 * kEpi0;      // 0 .. 127
     unsigned char* stg = base + LY::oStg + q * LY::kStg;
@@ -433,7 +440,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 
 template <int N, int L, int MODE>
 cudaError_t launch_state(const Dims& d, const void* X, const void* Y, const StateArgs& a0,
-                         const char* name, cudaStream_t s) {
+                         const char* name, bool pdl, cudaStream_t s) {
   using LY = StateLayout<N, L>;
   CUtensorMap mX, mY, mOut;
   if (!make_tma_map(&mX, X, kSP, d.H, d.T, d.B, 2, kKB) ||
@@ -455,17 +462,21 @@ cudaError_t launch_state(const Dims& d, const void* X, const void* Y, const Stat
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes);
   const int grid = a.n_items < sms ? a.n_items : sms;
   if (grid <= 0) return cudaSuccess;
-  SSD_LAUNCH(name, s, kern<<<grid, kStateThreads, LY::kBytes, s>>>(mX, mY, mOut, a));
+  if (pdl)
+    SSD_LAUNCH(name, s, launch_pdl(kern, dim3(grid), dim3(kStateThreads), LY::kBytes, s, mX, mY,
+                                   mOut, a));
+  else
+    SSD_LAUNCH(name, s, kern<<<grid, kStateThreads, LY::kBytes, s>>>(mX, mY, mOut, a));
   return cudaGetLastError();
 }
 
 template <int MODE>
 cudaError_t state_dispatch(const Dims& d, const void* X, const void* Y, const StateArgs& a,
-                           const char* name, cudaStream_t s) {
-  if (d.N == 128 && d.L == 256) return launch_state<128, 256, MODE>(d, X, Y, a, name, s);
-  if (d.N == 128 && d.L == 128) return launch_state<128, 128, MODE>(d, X, Y, a, name, s);
-  if (d.N == 64 && d.L == 256) return launch_state<64, 256, MODE>(d, X, Y, a, name, s);
-  return launch_state<64, 128, MODE>(d, X, Y, a, name, s);
+                           const char* name, bool pdl, cudaStream_t s) {
+  if (d.N == 128 && d.L == 256) return launch_state<128, 256, MODE>(d, X, Y, a, name, pdl, s);
+  if (d.N == 128 && d.L == 128) return launch_state<128, 128, MODE>(d, X, Y, a, name, pdl, s);
+  if (d.N == 64 && d.L == 256) return launch_state<64, 256, MODE>(d, X, Y, a, name, pdl, s);
+  return launch_state<64, 128, MODE>(d, X, Y, a, name, pdl, s);
 }
 
 }  // namespace
@@ -479,15 +490,15 @@ cudaError_t tc_chunk_state(const Dims& d, const FwdArgs& f, float* delta, float*
   a.delta = delta;
   a.acs = acs;
   a.out = S;
-  return state_dispatch<0>(d, f.x, f.B, a, "k_state_tc", s);
+  return state_dispatch<0>(d, f.x, f.B, a, "k_state_tc", false, s);  // a call's first kernel
 }
 
 cudaError_t tc_chunk_dstates(const Dims& d, const void* dy, const void* C, const float* acs,
-                             float* dHs, cudaStream_t s) {
+                             float* dHs, bool pdl, cudaStream_t s) {
   StateArgs a{};
   a.acs = const_cast<float*>(acs);
   a.out = dHs;
-  return state_dispatch<1>(d, dy, C, a, "k_dstates_tc", s);
+  return state_dispatch<1>(d, dy, C, a, "k_dstates_tc", pdl, s);
 }
 
 }  // namespace ssd

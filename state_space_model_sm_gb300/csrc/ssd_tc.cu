@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(512, 1)
               int* status) {
   using SM = ScanSmem<N, L>;
   constexpr int LT = SM::kLT, NLT = L / LT;
+  griddep_wait();  // the state images and vectors come from the previous kernels
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t bar_cb, bar_p[2], bar_st[2], bar_done[2];
   __shared__ uint32_t tmem_base;
@@ -145,6 +146,10 @@ __global__ void __launch_bounds__(512, 1)
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
+  // the next kernel may start once every CTA of this one holds its TMEM: a
+  // dependent CTA that allocates TMEM on the same SM then only waits for CTAs
+  // that need nothing from it
+  griddep_launch_dependents();
   const uint32_t tm = tmem_base;
   // two pipelines of 8 warps; a TMEM row is shared by the warps q and q + 4
   // of a pipeline, each taking 32 of a panel's 64 columns
@@ -624,6 +629,8 @@ __global__ void __launch_bounds__(NT)
     k_bwd_tail_tc(FinalizeArgs f, int nfin, const float4* __restrict__ dCp,
                   float4* __restrict__ dC, const float4* __restrict__ dBp, float4* __restrict__ dB,
                   int nred, int64_t rows, PartialRows prC, PartialRows prB, int N4) {
+  griddep_launch_dependents();
+  griddep_wait();  // every input comes from the previous kernels
   const int blk = blockIdx.x;
   if (blk < nfin) {
     finalize_block<NT>(f, blk % f.nc, (blk / f.nc) % f.H, blk / (f.nc * f.H));
@@ -677,7 +684,7 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     cudaError_t e = tc_chunk_state(d, f, w.delta, w.acs, w.S, s);  // with chunk_cumsum
     if (e != cudaSuccess) return e;
     simt_state_passing(d, f, fw, s);
-    e = tc_chunk_dstates(d, dy, Cm, w.acs, w.dHs, s);
+    e = tc_chunk_dstates(d, dy, Cm, w.acs, w.dHs, true, s);
     if (e != cudaSuccess) return e;
   }
   const int nsplit = simt_state_passing_bwd(d, w.dHs, w.acs, nullptr, a.dfinal, nullptr, w.dlast,
@@ -690,7 +697,7 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     scan_partition(d, sms, &grid, &per);
     CUtensorMap mDX;
     if (!make_y_map(&mDX, a.dx, d.H, d.T, d.B, 32)) return cudaErrorInvalidValue;
-    SSD_LAUNCH("k_scan_tc_dx", s, kern<<<grid, 512, SM::kBytes, s>>>(
+    SSD_LAUNCH("k_scan_tc_dx", s, launch_pdl(kern, dim3(grid), dim3(512), SM::kBytes, s,
         mDX, static_cast<const bf16*>(a.f.x), static_cast<const bf16*>(a.f.B), Cm, dy, w.delta, w.acs,
         static_cast<const unsigned char*>(w.dSimg), a.f.D, a.dx, w.ddir, w.qrow, w.ddiag, d.B, d.T,
         d.H, d.G, d.nc, per, status));
@@ -715,7 +722,7 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     const int c0 = L > 128 ? w.nb.light : w.nb.heavy;
     const PartialRows prC{nblk, d.G, d.T, d.L, {c0, w.nb.heavy}};
     const PartialRows prB{nblk, d.G, d.T, d.L, {w.nb.heavy, w.nb.light}};
-    SSD_LAUNCH("k_bwd_tail_tc", s, k_bwd_tail_tc<L><<<nfin + 2 * nred, L, 0, s>>>(
+    SSD_LAUNCH("k_bwd_tail_tc", s, launch_pdl(k_bwd_tail_tc<L>, dim3(nfin + 2 * nred), dim3(L), 0, s,
         fa, nfin, reinterpret_cast<const float4*>(w.dCp), reinterpret_cast<float4*>(a.dC),
         reinterpret_cast<const float4*>(w.dBp), reinterpret_cast<float4*>(a.dB),
         nred > 0 ? nred : 1, rows, prC, prB, N4));
@@ -754,7 +761,7 @@ cudaError_t tc_front_final(const Dims& d, const FwdArgs& a, const FwdWs& w, cuda
 cudaError_t tc_dstates(const Dims& d, const void* dy, const void* C, const float* delta,
                        const float* acs, float* dHs, cudaStream_t s) {
   (void)delta;
-  return tc_chunk_dstates(d, dy, C, acs, dHs, s);
+  return tc_chunk_dstates(d, dy, C, acs, dHs, false, s);  // the call's first kernel
 }
 
 cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w, cudaStream_t s) {
