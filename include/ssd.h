@@ -78,10 +78,11 @@ typedef struct {
  *   hprev     (B, nc, H, P, N)    state entering chunk c (state_passing output)
  * They stay valid until the workspace is reused.  When the call took the
  * tensor-core path (ssd_last_path() == 1), the hprev bytes hold each state
- * (P = 64 rows x N) split into bf16 hi = rn(v) and lo = rn(v - hi) in the
- * kernels' shared-memory layout instead of f32: per (b, c, h) N/64 "hi"
- * panels then N/64 "lo" panels, each 64 rows of 128 bytes (64 bf16 of one
- * row p); the 16-byte chunk j of row p is stored at chunk j ^ (p % 8). */
+ * split into bf16 hi = rn(v) and lo = rn(v - hi) in the kernels'
+ * shared-memory layout instead of f32: per (b, c, h) and 64-row half of the
+ * state (one half at headdim 64, rows 0-63 then 64-127 at headdim 128) N/64
+ * "hi" panels then N/64 "lo" panels, each 64 rows of 128 bytes (64 bf16 of
+ * one row p); the 16-byte chunk j of row p is stored at chunk j ^ (p % 8). */
 typedef struct {
   size_t delta, dA_cumsum, states, hprev, total;
 } ssd_fwd_layout;
@@ -128,7 +129,11 @@ int ssd_get_device_status(void* stream);
 int ssd_set_check_finite(int enable);
 
 /* Which kernel family the last ssd_fwd / ssd_bwd on this host thread used:
- * 0 = generic SIMT path, 1 = tcgen05 tensor-core path. */
+ * 0 = generic SIMT path, 1 = tcgen05 tensor-core path.  The tensor-core path
+ * takes bf16 inputs with headdim 64 or 128, dstate 64 or 128, chunk_size 128
+ * or 256, x / B / C / y / dy / dx / dB / dC / states 16-byte aligned, and an
+ * even nheads / ngroups at headdim 64; everything else runs on the generic
+ * kernels. */
 int ssd_last_path(void);
 
 /* Optional per-kernel timing.  ssd_profile_enable(1) clears the counters and
@@ -323,7 +328,9 @@ int ssd_gated_norm_get_config(const ssd_norm_shape* shape, ssd_norm_config* out)
  *     the table).
  * With chunk 128 (one row tile) the light fields are ignored.  0 keeps the
  * built-in rule's count (a list-scheduling model of the launch); a nonzero
- * value must divide nheads / ngroups and be at most 32. */
+ * value must divide the heads per group and be at most 32.  The kernels see
+ * a head of headdim 128 as two 64-wide heads, so there the blocks split
+ * 2 * nheads / ngroups heads. */
 typedef struct {
   int32_t scan_head_blocks, bc_head_blocks;
   int32_t scan_head_blocks_light, bc_head_blocks_light;

@@ -51,9 +51,10 @@ ScanEntry g_scan_table[kMaxScanEntries];
 int g_scan_entries = 0;
 std::mutex g_scan_mu;
 
+// (entries hold the caller's shape; d may be the tensor-core path's view)
 bool same_shape(const ScanEntry& e, const Dims& d) {
-  return e.B == d.B && e.T == d.T && e.H == d.H && e.P == d.P && e.N == d.N && e.G == d.G &&
-         e.L == d.L;
+  return e.B == d.B && e.T == d.T && e.H == (d.H >> d.hs) && e.P == (d.P << d.hs) &&
+         e.N == d.N && e.G == d.G && e.L == d.L;
 }
 
 // The built-in rule, a list-scheduling model of the launch: CTAs in grid
@@ -177,13 +178,15 @@ HeadBlocks pick_blocks(const Dims& d, bool bc, int heavy, int light) {
   return hb;
 }
 
-HeadBlocks tc_scan_blocks(const Dims& d) {
+HeadBlocks tc_scan_blocks(const Dims& d0) {
+  const Dims d = tc_dims(d0);  // blocks of 64-wide head parts
   ssd_scan_config c{};
   if (!scan_lookup(d, &c)) return pick_blocks(d, false, 0, 0);
   return pick_blocks(d, false, c.scan_head_blocks, c.scan_head_blocks_light);
 }
 
-HeadBlocks tc_bwd_blocks(const Dims& d) {
+HeadBlocks tc_bwd_blocks(const Dims& d0) {
+  const Dims d = tc_dims(d0);
   ssd_scan_config c{};
   if (!scan_lookup(d, &c)) return pick_blocks(d, true, 0, 0);
   return pick_blocks(d, true, c.bc_head_blocks, c.bc_head_blocks_light);
@@ -403,7 +406,7 @@ size_t ssd_bwd_workspace_size(const ssd_shape* shape) {
   if (make_dims(shape, &d) != SSD_OK) return 0;
   size_t total = bwd_offsets(d).total;
   if (tc_forward_supported(d)) {
-    const size_t t = tc_bwd_offsets(d, tc_bwd_blocks(d).max()).total;
+    const size_t t = tc_bwd_offsets(tc_dims(d), tc_bwd_blocks(d).max()).total;
     if (t > total) total = t;
   }
   return total;
@@ -494,7 +497,8 @@ int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
                   aligned(dinit_states, 16);
   if (tc) {
     const HeadBlocks nb = tc_bwd_blocks(d);  // once: the layout and the launch must agree
-    const TcBwdOffsets o = tc_bwd_offsets(d, nb.max());
+    // sized for the 64-wide head parts (the per-part row vectors of ddA)
+    const TcBwdOffsets o = tc_bwd_offsets(tc_dims(d), nb.max());
     if (!workspace || workspace_bytes < o.total || !aligned(workspace, kAlign))
       return SSD_ERR_WORKSPACE;
     TcBwdWs w;
@@ -621,7 +625,7 @@ int ssd_scan_set_config(const ssd_shape* shape, const ssd_scan_config* config) {
   Dims d;
   if (make_dims(shape, &d) != SSD_OK) return SSD_ERR_INVALID_ARG;
   if (config) {
-    const int hpg = d.H / d.G;
+    const int hpg = tc_dims(d).H / d.G;  // 64-wide head parts per group
     for (const int v : {config->scan_head_blocks, config->bc_head_blocks,
                          config->scan_head_blocks_light, config->bc_head_blocks_light})
       if (v < 0 || v > 32 || (v > 0 && hpg % v != 0)) return SSD_ERR_INVALID_ARG;

@@ -99,10 +99,10 @@ struct ChunkLayout {
 };
 
 struct ChunkArgs {
-  const float* delta;        // (B, H, nc, L)
-  const float* acs;          // (B, H, nc, L)
+  const float* delta;        // (B, H >> hs, nc, L)
+  const float* acs;          // (B, H >> hs, nc, L)
   const unsigned char* img;  // state images (B, nc, H): H_c (FWD, DC) or dS_c (DX, DB)
-  const float* D;            // (H) or null
+  const float* D;            // (H >> hs) or null
   const bf16* xg;            // DX: x, for the epilogue's inner products
   void* out;                 // FWD y, DX dx, DC / DB partials (B, T, G, nblk, N)
   float* msum;               // DC rowsum, DB colsum  (B, H, nc, L)
@@ -111,6 +111,7 @@ struct ChunkArgs {
   float* qrow;               // DX
   float* ddiag;              // DX
   int T, H, G, nc;
+  int hs;      // H counts 64-wide head parts, 1 << hs per head of delta / a / D
   int nbt[2];  // head blocks per group of row tile 0 / 1 (the grid holds the heavier first)
   int nblk;    // DC / DB: head-block slots per row of the partials (the larger of nbt)
   int* status;
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         const int v = i & 1;
         if (i >= 2 && !mbar_wait(&bar_vec_empty[v], ((i >> 1) - 1) & 1, status, &abort_flag))
           return false;
-        const int64_t cv = (((int64_t)b * H + h_begin + i) * nc + c) * L;
+        const int64_t cv = ((((int64_t)b * H + h_begin + i) >> a.hs) * nc + c) * L;
         mbar_arrive_expect_tx(&bar_vec_full[v], 2 * L * 4);
         ++n_vec[v];
         bulk_g2s(sVec + v * 2 * L, a.acs + cv, L * 4, &bar_vec_full[v]);
@@ -722,7 +723,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         // this thread's row of the stage's x (FWD) or dy (DX) rows
         const unsigned char* orow = sOps + st * LY::kOps;
         const int orr = r - col0;
-        const float Dh = a.D ? a.D[h] : 0.f;
+        const float Dh = a.D ? a.D[h >> a.hs] : 0.f;
         float pd = 0.f, pq = 0.f, pdd = 0.f;
         // y (FWD, fp32) and dx (DX) leave through TMA: this warp's 32 x 16
         // block goes to its staging slot, then one store (rows past seqlen
@@ -970,6 +971,7 @@ cudaError_t chunk_fwd_nl(const Dims& d, const FwdArgs& f, const FwdWs& w, HeadBl
   a.H = d.H;
   a.G = d.G;
   a.nc = d.nc;
+  a.hs = d.hs;
   // the heavy tile is the chunk's last (its rows see more columns)
   a.nbt[0] = L > 128 ? nb.light : nb.heavy;
   a.nbt[1] = nb.heavy;
@@ -998,6 +1000,7 @@ cudaError_t chunk_bwd_nl(const Dims& d, const BwdArgs& ba, const TcBwdWs& w, Hea
   a.H = d.H;
   a.G = d.G;
   a.nc = d.nc;
+  a.hs = d.hs;
   a.nblk = nb.max();  // partial slots per row
   a.status = device_status_ptr();
   if (!a.status) return cudaErrorUnknown;

@@ -14,6 +14,10 @@ namespace ssd {
 struct Dims {
   int B, T, H, P, N, G, L, nc;
   int in_bf16, out_bf16;
+  // log2 of the 64-wide parts a head is split into on the tensor-core path
+  // (tc_dims): H and P then count parts; dt, dt_bias, A, D and the per-head
+  // vectors delta / a are indexed by the head, (b * H + h) >> hs
+  int hs = 0;
 };
 
 // Device address of the status word of the current device (defined in
@@ -205,6 +209,9 @@ struct TcBwdWs {
 // tcgen05 path (ssd_tc.cu): bf16 inputs, headdim 64, d_state 64 / 128,
 // chunk 128 / 256, an even number of heads per group.
 bool tc_forward_supported(const Dims& d);
+// The tensor-core path's view of a shape: headdim 128 as two 64-wide parts
+// per head (hs = 1); other shapes unchanged.
+Dims tc_dims(const Dims& d);
 cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s);
 // Head blocks per group of the chunk kernels' row tiles: `heavy` for the tile
 // with more column panels (first in the grid), `light` for the other (chunk

@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     k_state_passing_img(const float4* __restrict__ S, const float* __restrict__ acs,
                         const float4* __restrict__ init, unsigned char* __restrict__ img,
                         float4* __restrict__ final_state, int N, int H, int PN8, int L, int nc,
-                        int K, int lseg, const float4* __restrict__ seg_in) {
+                        int K, int lseg, const float4* __restrict__ seg_in, int hs) {
   griddep_launch_dependents();
   griddep_wait();  // S and a come from the previous kernel (launched with launch_pdl)
   const int e = blockIdx.x * kThreads + threadIdx.x, h = blockIdx.y;
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int64_t step = (int64_t)H * PN8 * 2;             // float4 units between chunks
   const int64_t base = ((int64_t)b * nc * H + h) * PN8 * 2;  // (b, c=0, h) state, float4 units
   const uint32_t off = image_chunk_off(e, N), lo_off = (N / 64) * 8192u;
-  const float* ab = acs + ((int64_t)b * H + h) * (int64_t)nc * L + (L - 1);
+  const float* ab = acs + (((int64_t)b * H + h) >> hs) * (int64_t)nc * L + (L - 1);
   const int64_t sb = ((int64_t)b * H + h) * PN8 * 2 + 2 * e;
   const float4* in = nullptr;  // the state entering the segment (null: zero)
   if constexpr (!kSeg) {
@@ -402,14 +402,14 @@ __global__ void __launch_bounds__(kThreads, 3)
 __global__ void __launch_bounds__(kThreads, 3)
     k_state_passing_seg_end(const float4* __restrict__ S, const float* __restrict__ acs,
                             float4* __restrict__ E, int H, int PN8, int L, int nc, int K,
-                            int lseg) {
+                            int lseg, int hs) {
   const int e = blockIdx.x * kThreads + threadIdx.x, h = blockIdx.y;
   const int b = blockIdx.z / K, sk = blockIdx.z % K;
   if (e >= PN8 || sk == K - 1) return;
   const int cb = sk * lseg, ce = min(nc, cb + lseg);
   const int64_t step = (int64_t)H * PN8 * 2;
   const int64_t base = ((int64_t)b * nc * H + h) * PN8 * 2;
-  const float* ab = acs + ((int64_t)b * H + h) * (int64_t)nc * L + (L - 1);
+  const float* ab = acs + (((int64_t)b * H + h) >> hs) * (int64_t)nc * L + (L - 1);
   float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f), c1 = c0;
   for (int k0 = cb; k0 < ce; k0 += kPrefetchImg) {
     float4 s0[kPrefetchImg], s1[kPrefetchImg];
@@ -439,10 +439,10 @@ __global__ void __launch_bounds__(kThreads, 3)
 __global__ void __launch_bounds__(kThreads)
     k_state_passing_seg_in(const float4* __restrict__ E, const float* __restrict__ acs,
                            const float4* __restrict__ init, float4* __restrict__ In, int H,
-                           int PN8, int L, int nc, int K, int lseg) {
+                           int PN8, int L, int nc, int K, int lseg, int hs) {
   const int e = blockIdx.x * kThreads + threadIdx.x, h = blockIdx.y, b = blockIdx.z;
   if (e >= PN8) return;
-  const float* ab = acs + ((int64_t)b * H + h) * (int64_t)nc * L + (L - 1);
+  const float* ab = acs + (((int64_t)b * H + h) >> hs) * (int64_t)nc * L + (L - 1);
   const int64_t sb = ((int64_t)b * H + h) * PN8 * 2 + 2 * e;
   float4 c0 = init ? init[sb] : make_float4(0.f, 0.f, 0.f, 0.f);
   float4 c1 = init ? init[sb + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                             const float4* __restrict__ dfinal, unsigned char* __restrict__ dsimg,
                             float* __restrict__ dlast_part, float4* __restrict__ dinit, int N,
                             int H, int PN8, int L, int nc, int K, int lseg,
-                            const float4* __restrict__ seg_out) {
+                            const float4* __restrict__ seg_out, int hs) {
   griddep_launch_dependents();
   griddep_wait();  // dHs comes from the previous kernel (launched with launch_pdl)
   // grid (nsplit, H, B*K): segment sk = z % K walks chunks [sk*lseg, min(nc,
@@ -482,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int64_t step = (int64_t)H * PN8 * 2;
   const int64_t base = ((int64_t)b * nc * H + h) * PN8 * 2;
   const uint32_t off = live ? image_chunk_off(e, N) : 0u, lo_off = (N / 64) * 8192u;
-  const float* ab = acs + ((int64_t)b * H + h) * (int64_t)nc * L + (L - 1);
+  const float* ab = acs + (((int64_t)b * H + h) >> hs) * (int64_t)nc * L + (L - 1);
   const int64_t sb = ((int64_t)b * H + h) * PN8 * 2 + 2 * e;
   const float4* gin = nullptr;  // the gradient leaving the segment (null: zero)
   if constexpr (!kSeg) {
@@ -543,14 +543,14 @@ __global__ void __launch_bounds__(kThreads, 3)
 __global__ void __launch_bounds__(kThreads, 3)
     k_state_passing_bwd_seg_end(const float4* __restrict__ dHs, const float* __restrict__ acs,
                                 float4* __restrict__ E, int H, int PN8, int L, int nc, int K,
-                                int lseg) {
+                                int lseg, int hs) {
   const int e = blockIdx.x * kThreads + threadIdx.x, h = blockIdx.y;
   const int b = blockIdx.z / K, sk = blockIdx.z % K;
   if (e >= PN8 || sk == 0) return;
   const int cb = sk * lseg, ce = min(nc, cb + lseg);
   const int64_t step = (int64_t)H * PN8 * 2;
   const int64_t base = ((int64_t)b * nc * H + h) * PN8 * 2;
-  const float* ab = acs + ((int64_t)b * H + h) * (int64_t)nc * L + (L - 1);
+  const float* ab = acs + (((int64_t)b * H + h) >> hs) * (int64_t)nc * L + (L - 1);
   float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0;
   for (int c1 = ce - 1; c1 >= cb; c1 -= kPrefetchImg) {
     float4 d0[kPrefetchImg], d1[kPrefetchImg];
@@ -580,10 +580,10 @@ __global__ void __launch_bounds__(kThreads, 3)
 __global__ void __launch_bounds__(kThreads)
     k_state_passing_bwd_seg_in(const float4* __restrict__ E, const float* __restrict__ acs,
                                const float4* __restrict__ dfinal, float4* __restrict__ Out,
-                               int H, int PN8, int L, int nc, int K, int lseg) {
+                               int H, int PN8, int L, int nc, int K, int lseg, int hs) {
   const int e = blockIdx.x * kThreads + threadIdx.x, h = blockIdx.y, b = blockIdx.z;
   if (e >= PN8) return;
-  const float* ab = acs + ((int64_t)b * H + h) * (int64_t)nc * L + (L - 1);
+  const float* ab = acs + (((int64_t)b * H + h) >> hs) * (int64_t)nc * L + (L - 1);
   const int64_t sb = ((int64_t)b * H + h) * PN8 * 2 + 2 * e;
   float4 g0 = dfinal ? dfinal[sb] : make_float4(0.f, 0.f, 0.f, 0.f);
   float4 g1 = dfinal ? dfinal[sb + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1141,16 +1141,16 @@ void launch_state_passing(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaS
       float4* E = reinterpret_cast<float4*>(w.seg);
       float4* In = E + (size_t)d.B * K * d.H * PN8 * 2;
       SSD_LAUNCH("k_state_passing_seg", s, k_state_passing_seg_end<<<dim3(gx, d.H, d.B * K), kThreads, 0, s>>>(
-          reinterpret_cast<const float4*>(w.S), w.acs, E, d.H, PN8, d.L, d.nc, K, lseg));
+          reinterpret_cast<const float4*>(w.S), w.acs, E, d.H, PN8, d.L, d.nc, K, lseg, d.hs));
       SSD_LAUNCH("k_state_passing_seg", s, k_state_passing_seg_in<<<dim3(gx, d.H, d.B), kThreads, 0, s>>>(
-          E, w.acs, reinterpret_cast<const float4*>(a.init), In, d.H, PN8, d.L, d.nc, K, lseg));
+          E, w.acs, reinterpret_cast<const float4*>(a.init), In, d.H, PN8, d.L, d.nc, K, lseg, d.hs));
       in = In;
     }
     auto kern = K > 1 ? k_state_passing_img<true> : k_state_passing_img<false>;
     SSD_LAUNCH("k_state_passing", s, launch_pdl(kern, dim3(gx, d.H, d.B * K), dim3(kThreads), 0, s,
         reinterpret_cast<const float4*>(w.S), w.acs, reinterpret_cast<const float4*>(a.init),
         static_cast<unsigned char*>(w.Himg), reinterpret_cast<float4*>(a.final_state), d.N, d.H,
-        PN8, d.L, d.nc, K, lseg, in));
+        PN8, d.L, d.nc, K, lseg, in, d.hs));
     return;
   }
   if (PN % 4 == 0 && vec4_ok(a.init) && vec4_ok(a.final_state)) {
@@ -1196,10 +1196,10 @@ int launch_state_passing_bwd(const Dims& d, const BwdArgs& a, const BwdWs& w, cu
       float4* E = reinterpret_cast<float4*>(w.f.seg);
       float4* Out = E + (size_t)d.B * K * d.H * PN8 * 2;
       SSD_LAUNCH("k_state_passing_bwd_seg", s, k_state_passing_bwd_seg_end<<<dim3(nsplit, d.H, d.B * K), kThreads, 0, s>>>(
-          reinterpret_cast<const float4*>(w.dHs), w.f.acs, E, d.H, PN8, d.L, d.nc, K, lseg));
+          reinterpret_cast<const float4*>(w.dHs), w.f.acs, E, d.H, PN8, d.L, d.nc, K, lseg, d.hs));
       SSD_LAUNCH("k_state_passing_bwd_seg", s, k_state_passing_bwd_seg_in<<<dim3(nsplit, d.H, d.B), kThreads, 0, s>>>(
           E, w.f.acs, reinterpret_cast<const float4*>(a.dfinal), Out, d.H, PN8, d.L, d.nc, K,
-          lseg));
+          lseg, d.hs));
       out = Out;
     }
     auto kern = K > 1 ? k_state_passing_bwd_img<true> : k_state_passing_bwd_img<false>;
@@ -1208,7 +1208,7 @@ int launch_state_passing_bwd(const Dims& d, const BwdArgs& a, const BwdWs& w, cu
         reinterpret_cast<const float4*>(w.dHs), w.f.acs,
         static_cast<const unsigned char*>(w.f.Himg), reinterpret_cast<const float4*>(a.dfinal),
         static_cast<unsigned char*>(w.dSimg), w.dlast, reinterpret_cast<float4*>(a.dinit), d.N,
-        d.H, PN8, d.L, d.nc, K, lseg, out));
+        d.H, PN8, d.L, d.nc, K, lseg, out, d.hs));
     return nsplit * (kThreads / 32);  // one partial per warp
   }
   if (PN % 4 == 0 && vec4_ok(a.dfinal) && vec4_ok(a.dinit)) {
@@ -1275,7 +1275,8 @@ int seg_max_segments(const Dims& d) {
   // a property of the shape, so workspace sizes do not depend on the device:
   // scratch only where the (batch, head) grid is small and there are chunks
   // to split (at most 16 segments of at least 4 chunks)
-  const int64_t ctas = (int64_t)((d.P * d.N / 8 + kThreads - 1) / kThreads) * d.H * d.B;
+  const int64_t ctas =
+      (int64_t)(((d.P << d.hs) * d.N / 8 + kThreads - 1) / kThreads) * (d.H >> d.hs) * d.B;
   if (d.nc < 8 || ctas >= 256) return 0;
   return std::min(16, d.nc / 4);
 }

@@ -112,6 +112,7 @@ struct StateArgs {
   float* acs;            // MODE 0 writes, MODE 1 reads (B, H, nc, L)
   float* out;            // (B, nc, H, P, N)
   int T, H, G, nc, n_items;
+  int hs;  // log2 of the 64-wide parts per head: dt, dt_bias, A, delta, a index (b, h) >> hs
   int* status;
 };
 
@@ -284,14 +285,14 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       decode(k, b, c, h);
       const int hd = h + eh, t0 = c * L, Lv = min(L, T - t0);
       if constexpr (MODE == 0) {
-        vbias = (a.dt_bias ? a.dt_bias : a.A)[hd];
-        vA = a.A[hd];
+        vbias = (a.dt_bias ? a.dt_bias : a.A)[hd >> a.hs];
+        vA = a.A[hd >> a.hs];
 #pragma unroll
         for (int e = 0; e < EV; ++e)
           vdt[e] = reinterpret_cast<const unsigned short*>(
-              a.dt)[((int64_t)b * T + t0 + min(ev * EV + e, Lv - 1)) * H + hd];
+              a.dt)[(((int64_t)b * T + t0 + min(ev * EV + e, Lv - 1)) * H + hd) >> a.hs];
       } else {
-        const int64_t cv = (((int64_t)b * H + hd) * nc + c) * L;
+        const int64_t cv = ((((int64_t)b * H + hd) >> a.hs) * nc + c) * L;
 #pragma unroll
         for (int e = 0; e < EV; ++e) vin[e] = a.acs[cv + ev * EV + e];
       }
@@ -301,7 +302,9 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       decode(k, b, c, h);
       const int hd = h + eh, t0 = c * L, Lv = min(L, T - t0);
       float* w = sw + (k & 1) * 2 * L + eh * L;
-      const int64_t cv = (((int64_t)b * H + hd) * nc + c) * L;
+      const int64_t cv = ((((int64_t)b * H + hd) >> a.hs) * nc + c) * L;
+      // a head split in parts: its first part writes delta and a
+      const bool wr = (hd & ((1 << a.hs) - 1)) == 0;
       if constexpr (MODE == 0) {
         const float bias = a.dt_bias ? vbias : 0.f, Ah = vA;
         float dl[EV], al[EV], run = 0.f;
@@ -325,8 +328,10 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         for (int e = 0; e < EV; ++e) {
           const int l = ev * EV + e;
           al[e] += pre;
-          a.delta[cv + l] = dl[e];
-          a.acs[cv + l] = al[e];
+          if (wr) {
+            a.delta[cv + l] = dl[e];
+            a.acs[cv + l] = al[e];
+          }
         }
         if (ev == 63) s_alast[eh] = al[EV - 1];  // a[L-1] as written
         epi_sync();
@@ -452,6 +457,7 @@ cudaError_t launch_state(const Dims& d, const void* X, const void* Y, const Stat
   a.H = d.H;
   a.G = d.G;
   a.nc = d.nc;
+  a.hs = d.hs;
   a.n_items = d.B * d.nc * (d.H / 2);
   a.status = device_status_ptr();
   if (!a.status) return cudaErrorUnknown;

@@ -107,8 +107,8 @@ __global__ void __launch_bounds__(512, 1)
               const float* __restrict__ delta, const float* __restrict__ acs,
               const unsigned char* __restrict__ simg, const float* __restrict__ D,
               Tout* __restrict__ out, float* __restrict__ ddir, float* __restrict__ qrow,
-              float* __restrict__ ddiag, int B_, int T, int H, int G, int nc, int items_per_cta,
-              int* status) {
+              float* __restrict__ ddiag, int B_, int T, int H, int G, int nc, int hs,
+              int items_per_cta, int* status) {
   using SM = ScanSmem<N, L>;
   constexpr int LT = SM::kLT, NLT = L / LT;
   griddep_wait();  // the state images and vectors come from the previous kernels
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(512, 1)
     if constexpr (!kTmaO) prefetch_x(hh);
     const unsigned char* img = simg + ((((int64_t)b * nc + c) * H + hh) * (int64_t)SM::kImg);
     for (int i = wtid; i < SM::kImg / 16; i += 256) cp_async16(Pw + 16 * i, img + 16 * i, true);
-    const int64_t cvh = (((int64_t)b * H + hh) * nc + c) * L;
+    const int64_t cvh = ((((int64_t)b * H + hh) >> hs) * nc + c) * L;
     for (int i = wtid; i < L / 4; i += 256) {
       cp_async16(sraw + 4 * i, acs + cvh + 4 * i, true);
       cp_async16(sraw + L + 4 * i, delta + cvh + 4 * i, true);
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(512, 1)
 
   for (int h = h_begin + wg; h < h_end; h += 2) {
     const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
-    const float Dh = D ? D[h] : 0.f;
+    const float Dh = D ? D[h >> hs] : 0.f;
     // the image and vectors (the operand rows may still be in flight)
     if constexpr (kTmaO) cp_async_wait<1>();
     else cp_async_wait<0>();
@@ -525,9 +525,12 @@ struct FinalizeArgs {
   int nsplit;
   float *ddt, *part;
   int T, H, L, nc;
+  int hs;  // H counts 64-wide head parts, 1 << hs per head of dt / delta / ddt / part
 };
 
 // One (chunk c, head h, batch b) of the finalize step; NT threads = L rows.
+// A head of 1 << hs parts sums its parts' row vectors first: every term of
+// ddA and of the direct dt gradient is a sum over the head's channels.
 template <int NT>
 __device__ __forceinline__ void finalize_block(const FinalizeArgs& f, int c, int h, int b) {
   constexpr int NW = NT / 32;
@@ -544,7 +547,7 @@ __device__ __forceinline__ void finalize_block(const FinalizeArgs& f, int c, int
   const float* __restrict__ dlast = f.dlast;
   float* __restrict__ ddt = f.ddt;
   float* __restrict__ part = f.part;
-  const int nsplit = f.nsplit, T = f.T, H = f.H, L = f.L, nc = f.nc;
+  const int nsplit = f.nsplit, T = f.T, H = f.H >> f.hs, L = f.L, nc = f.nc, V = 1 << f.hs;
   __shared__ float wt[NW], red[NW];
   const int r = threadIdx.x;
   const int Lv = min(L, T - c * L);
@@ -552,12 +555,19 @@ __device__ __forceinline__ void finalize_block(const FinalizeArgs& f, int c, int
   const bool live = r < Lv;
   const int64_t ti = ((int64_t)b * T + (int64_t)c * L + r) * H + h;
   const float vdt = live ? __bfloat162float(dt[ti]) : 0.f;
-  const float jump = live ? colsum[cv + r] - rowsum[cv + r] + qrow[cv + r] : 0.f;
-  const float y = live ? ycs[cv + r] : 0.f;
-  const float dirr = live ? ddir[cv + r] : 0.f, dg = live ? ddiag[cv + r] : 0.f;
   const float dlt = live ? delta[cv + r] : 0.f;
-  float dl = 0.f;
-  for (int k = 0; k < nsplit; ++k) dl += dlast[(((int64_t)b * H + h) * nc + c) * nsplit + k];
+  float jump = 0.f, y = 0.f, dirr = 0.f, dg = 0.f, dl = 0.f;
+  for (int j = 0; j < V; ++j) {
+    const int64_t bhc = ((int64_t)b * H + h) * V + j;  // the part's (b, part) row
+    const int64_t cp = (bhc * nc + c) * L;
+    if (live) {
+      jump += colsum[cp + r] - rowsum[cp + r] + qrow[cp + r];
+      y += ycs[cp + r];
+      dirr += ddir[cp + r];
+      dg += ddiag[cp + r];
+    }
+    for (int k = 0; k < nsplit; ++k) dl += dlast[(bhc * nc + c) * nsplit + k];
+  }
   // ddA_r = prefix_{j<r}(jump_j) + dlast + suffix_{l>=r}(ycs_l)
   const float pre = block_exclusive_scan(jump, wt);
   const float ypre = block_exclusive_scan(y, wt);   // sum_{l<r} ycs
@@ -633,7 +643,8 @@ __global__ void __launch_bounds__(NT)
   griddep_wait();  // every input comes from the previous kernels
   const int blk = blockIdx.x;
   if (blk < nfin) {
-    finalize_block<NT>(f, blk % f.nc, (blk / f.nc) % f.H, blk / (f.nc * f.H));
+    const int H = f.H >> f.hs;
+    finalize_block<NT>(f, blk % f.nc, (blk / f.nc) % H, blk / (f.nc * H));
     return;
   }
   const int rb = blk - nfin, which = rb / nred;
@@ -700,7 +711,7 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     SSD_LAUNCH("k_scan_tc_dx", s, launch_pdl(kern, dim3(grid), dim3(512), SM::kBytes, s,
         mDX, static_cast<const bf16*>(a.f.x), static_cast<const bf16*>(a.f.B), Cm, dy, w.delta, w.acs,
         static_cast<const unsigned char*>(w.dSimg), a.f.D, a.dx, w.ddir, w.qrow, w.ddiag, d.B, d.T,
-        d.H, d.G, d.nc, per, status));
+        d.H, d.G, d.nc, d.hs, per, status));
   }
   const int nblk = w.nb.max();  // partial slots per row
   float* dCout = nblk == 1 ? a.dC : w.dCp;
@@ -712,8 +723,8 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
   {
     const FinalizeArgs fa{static_cast<const bf16*>(a.f.dt), a.f.dt_bias, a.f.A, w.delta,
                           w.rowsum, w.colsum, w.ycs, w.qrow, w.ddir, w.ddiag, w.dlast, nsplit,
-                          a.ddt, w.part, d.T, d.H, d.L, d.nc};
-    const int nfin = d.nc * d.H * d.B;
+                          a.ddt, w.part, d.T, d.H, d.L, d.nc, d.hs};
+    const int nfin = d.nc * (d.H >> d.hs) * d.B;
     const int64_t rows = (int64_t)d.B * d.T * d.G;
     const int N4 = d.N / 4;
     const int nred = nblk > 1 ? (int)((rows * N4 + L - 1) / L) : 0;
@@ -727,19 +738,39 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
         reinterpret_cast<const float4*>(w.dBp), reinterpret_cast<float4*>(a.dB),
         nred > 0 ? nred : 1, rows, prC, prB, N4));
   }
-  simt_param_grads(d, w.part, a.dA, a.ddt_bias, a.dD, s);
+  Dims dh = d;  // the partials are per head (of dt), not per 64-wide part
+  dh.H = d.H >> d.hs;
+  simt_param_grads(dh, w.part, a.dA, a.ddt_bias, a.dD, s);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool tc_forward_supported(const Dims& d) {
-  return d.in_bf16 && d.P == kP && (d.N == 64 || d.N == 128) && (d.L == 128 || d.L == 256) &&
-         (d.H / d.G) % 2 == 0;
+  const Dims v = tc_dims(d);
+  return d.in_bf16 && v.P == kP && (d.N == 64 || d.N == 128) && (d.L == 128 || d.L == 256) &&
+         (v.H / d.G) % 2 == 0;
+}
+
+// A head of 128 channels runs as two 64-wide parts (the kernels' M = 128
+// operand rows hold two parts, i.e. the whole head): the parts share the
+// head's dt, A, D and decay vectors, and their x, y, states and images are
+// the head's own bytes (channel p of head h is channel p % 64 of part
+// 2h + p / 64).  Each part writes its own row vectors of the backward, which
+// the finalize step sums per head.
+Dims tc_dims(const Dims& d) {
+  Dims v = d;
+  if (d.hs == 0 && d.P == 2 * kP) {
+    v.H = 2 * d.H;
+    v.P = kP;
+    v.hs = 1;
+  }
+  return v;
 }
 
 
-cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
+cudaError_t tc_forward(const Dims& d0, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
+  const Dims d = tc_dims(d0);
   int* status = device_status_ptr();
   if (!status) return cudaErrorUnknown;
   int dev = 0, sms = 148;
@@ -751,7 +782,8 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStre
   return launch_tc_forward_nl<64, 128>(d, a, w, s, status, sms);
 }
 
-cudaError_t tc_front_final(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
+cudaError_t tc_front_final(const Dims& d0, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
+  const Dims d = tc_dims(d0);
   const cudaError_t e = tc_chunk_state(d, a, w.delta, w.acs, w.S, s);
   if (e != cudaSuccess) return e;
   simt_state_passing(d, a, w, s);
@@ -761,10 +793,11 @@ cudaError_t tc_front_final(const Dims& d, const FwdArgs& a, const FwdWs& w, cuda
 cudaError_t tc_dstates(const Dims& d, const void* dy, const void* C, const float* delta,
                        const float* acs, float* dHs, cudaStream_t s) {
   (void)delta;
-  return tc_chunk_dstates(d, dy, C, acs, dHs, false, s);  // the call's first kernel
+  return tc_chunk_dstates(tc_dims(d), dy, C, acs, dHs, false, s);  // the call's first kernel
 }
 
-cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w, cudaStream_t s) {
+cudaError_t tc_backward(const Dims& d0, const BwdArgs& a, const TcBwdWs& w, cudaStream_t s) {
+  const Dims d = tc_dims(d0);
   int* status = device_status_ptr();
   if (!status) return cudaErrorUnknown;
   int dev = 0, sms = 148;

@@ -120,6 +120,8 @@ WORKLOADS = {
     # long context with few heads (8 heads of 64: the chunk loop of state
     # passing has few (batch, head) pairs to run in parallel)
     "long_h8_bf16": (SSDShape(1, 131072, 8, 64, 128, 1, 256), "bf16", 0.0, 5, True),
+    # the layer with headdim 128 (same d_inner 1536: 12 heads of 128)
+    "layer_p128_fwdbwd_bf16": (SSDShape(4, 4096, 12, 128, 128, 1, 256), "bf16", 0.0, 6, True),
 }
 
 

@@ -149,6 +149,13 @@ def _scan_shape(e: dict):
     return _native.Shape(*(int(e[k]) for k in _SCAN_KEYS), 1, 0)
 
 
+def _kernel_heads_per_group(shape: dict) -> int:
+    """Heads per group as the chunk kernels count them: a head of headdim 128
+    runs as two 64-wide heads."""
+    hpg = int(shape["nheads"]) // int(shape["ngroups"])
+    return 2 * hpg if int(shape["headdim"]) == 128 else hpg
+
+
 def validate_scan_table(table: dict) -> None:
     """Raises ValueError unless ``table`` is a well-formed SSD launch table
     (field ranges as ``ssd_scan_set_config`` accepts them)."""
@@ -165,9 +172,10 @@ def validate_scan_table(table: dict) -> None:
         H, G = int(e["nheads"]), int(e["ngroups"])
         if min(int(e[k]) for k in _SCAN_KEYS) < 1 or H % G:
             raise ValueError(f"bad shape in {e}")
+        hpg = _kernel_heads_per_group(e)
         for k in _SCAN_FIELDS:
             v = int(e.get(k, 0))
-            if v < 0 or v > 32 or (v > 0 and (H // G) % v):
+            if v < 0 or v > 32 or (v > 0 and hpg % v):
                 raise ValueError(f"bad {k} in {e}")
         key = tuple(int(e[k]) for k in _SCAN_KEYS)
         if key in seen:
@@ -251,7 +259,7 @@ def sweep_scan(workload: str, steps: int = 10, warmup: int = 3, max_blocks: int 
         torch.cuda.synchronize()
         return 1e3 * sum(a.elapsed_time(b) for a, b in ev) / steps
 
-    hpg = s.nheads // s.ngroups
+    hpg = _kernel_heads_per_group(key)
     blocks = [nb for nb in range(1, min(hpg, max_blocks) + 1) if hpg % nb == 0]
     # (heavy, light) pairs; with chunk 128 there is one row tile
     pairs = [(h, l) for h in blocks for l in blocks] if s.chunk_size > 128 else \

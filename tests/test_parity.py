@@ -82,13 +82,16 @@ def test_backward_small(cuda_lib, name, shape, dtype, init_std):
         assert_close(k, got, ref[k], dtype)
 
 
-def test_forward_intermediates_match_chunked_reference(cuda_lib):
+@pytest.mark.parametrize("P", [64, 128])
+def test_forward_intermediates_match_chunked_reference(cuda_lib, P):
     """Per-kernel parity: delta, dA_cumsum (chunk_cumsum), states (chunk_state)
-    and hprev (state_passing), read from the documented workspace layout."""
+    and hprev (state_passing), read from the documented workspace layout (at
+    headdim 128 the tensor-core path writes delta / dA_cumsum once per head
+    and a state image per 64-wide half of a head)."""
     import torch
-    inp = make_inputs(SSDShape(2, 300, 4, 64, 128, 2, 128), seed=5, dtype="bf16", init_std=0.1)
+    Bt, T, H, N, G, L = 2, 300, 4, 128, 2, 128
+    inp = make_inputs(SSDShape(Bt, T, H, P, N, G, L), seed=5, dtype="bf16", init_std=0.1)
     t = to_torch(inp)
-    Bt, T, H, P, N, G, L = 2, 300, 4, 64, 128, 2, 128
     nc = 3
     shape = cuda_lib.make_shape(Bt, T, H, P, N, G, L, cuda_lib.SSD_BF16, cuda_lib.SSD_F32)
     lay = cuda_lib.fwd_workspace_layout(shape)
@@ -109,7 +112,7 @@ def test_forward_intermediates_match_chunked_reference(cuda_lib):
     assert s["rel_l2"] < 1e-3, s
     if cuda_lib.last_path() == 1:
         raw = ws[lay["hprev"]:lay["hprev"] + 4 * Bt * nc * H * P * N].cpu().numpy()
-        hprev = decode_state_images(raw, Bt * nc * H, N).reshape(Bt, nc, H, P, N)
+        hprev = decode_state_images(raw, Bt * nc * H * (P // 64), N).reshape(Bt, nc, H, P, N)
     else:
         hprev = view(lay["hprev"], (Bt, nc, H, P, N))
     s = stats(hprev, ref["Hprev"])
@@ -161,8 +164,9 @@ def test_forward_workload(cuda_lib, name):
     print(name, s)
 
 
-def test_forward_backward_workload(cuda_lib):
-    inp = make_workload("layer_fwdbwd_bf16")
+@pytest.mark.parametrize("name", ["layer_fwdbwd_bf16", "layer_p128_fwdbwd_bf16"])
+def test_forward_backward_workload(cuda_lib, name):
+    inp = make_workload(name)
     y, final = run_fwd(cuda_lib, inp)
     y_ref, f_ref = oracle_fwd(inp)
     assert_close("y", to_np(y), y_ref, "bf16")
@@ -195,6 +199,9 @@ TC_CASES = [
     ("tc_n64_l128_tail", SSDShape(1, 333, 6, 64, 64, 3, 128), 0.1),
     ("tc_n64_l256", SSDShape(3, 512, 4, 64, 64, 1, 256), 0.0),
     ("tc_partial_second_tile", SSDShape(1, 300, 2, 64, 128, 1, 256), 0.0),
+    # headdim 128: a head runs as two 64-wide parts sharing its dt / A / D
+    ("tc_p128_n128_l256", SSDShape(2, 1024, 4, 128, 128, 1, 256), 0.2),
+    ("tc_p128_n64_l128_tail", SSDShape(1, 333, 3, 128, 64, 3, 128), 0.1),
 ]
 
 
@@ -203,7 +210,7 @@ def test_tensor_core_forward_against_oracle_and_generic(cuda_lib, monkeypatch, n
                                                        init_std):
     inp = make_inputs(shape, seed=31, dtype="bf16", init_std=init_std)
     y, final = run_fwd(cuda_lib, inp)
-    assert cuda_lib.last_path() == 1, "bf16 headdim-64 problem did not take the tcgen05 path"
+    assert cuda_lib.last_path() == 1, "bf16 problem did not take the tcgen05 path"
     y_ref, f_ref = oracle_fwd(inp)
     s = assert_close("y", to_np(y), y_ref, "bf16")
     assert s["rel_l2"] < 1e-4, s      # split-bf16 operands keep ~fp32 accuracy
@@ -232,6 +239,8 @@ TC_BWD_CASES = [
     ("tcb_n64_l128_tail", SSDShape(1, 333, 6, 64, 64, 3, 128), 0.1, 0.3),
     ("tcb_n64_l256_heads", SSDShape(2, 512, 12, 64, 64, 1, 256), 0.0, 0.0),
     ("tcb_partial_tile", SSDShape(1, 300, 2, 64, 128, 1, 256), 0.3, 0.2),
+    ("tcb_p128_n128_l256_init", SSDShape(2, 1024, 4, 128, 128, 1, 256), 0.2, 0.5),
+    ("tcb_p128_n64_l128_tail", SSDShape(1, 333, 3, 128, 64, 3, 128), 0.1, 0.3),
 ]
 
 

@@ -168,7 +168,7 @@ def _model_rule(key, sms=152, partials=False):
     per slot read and per sum written, at 6.8e12 B/s, in units of 1100
     cycles at 2.07 GHz); the best (heavy, light) pair, fewer CTAs on a tie."""
     import heapq
-    hpg = key["nheads"] // key["ngroups"]
+    hpg = key["nheads"] // key["ngroups"] * (2 if key["headdim"] == 128 else 1)
     nc = -(-key["seqlen"] // key["chunk_size"])
     units = key["batch"] * nc * key["ngroups"]
     divs = [d for d in range(1, min(hpg, 32) + 1) if hpg % d == 0]
@@ -214,6 +214,25 @@ def test_scan_validate():
         tuning.validate_scan_table(_table())
 
 
+def test_scan_table_counts_headdim_128_heads_twice():
+    """At headdim 128 the head blocks split two 64-wide heads per head: 3
+    heads in 3 groups give 2 kernel heads per group, so 2 blocks are valid
+    and 4 are not (library and Python validation agree)."""
+    key = dict(batch=1, seqlen=333, nheads=3, headdim=128, dstate=64, ngroups=3, chunk_size=128)
+    try:
+        tuning.set_scan_config(key, 2, 2)
+        got, from_table = tuning.get_scan_config(key)
+        assert from_table and got["scan_head_blocks"] == 2 and got["bc_head_blocks"] == 2
+        tuning.validate_scan_table(_scan_table(dict(key, scan_head_blocks=2, bc_head_blocks=2)))
+        with pytest.raises(ValueError):
+            tuning.set_scan_config(key, 4, 0)
+        with pytest.raises(ValueError):
+            tuning.validate_scan_table(_scan_table(dict(key, scan_head_blocks=4,
+                                                        bc_head_blocks=0)))
+    finally:
+        tuning.clear_scan_config(key)
+
+
 def test_scan_table_set_get_remove():
     """Host-only calls: the entry overrides the built-in head-block rule, a
     zero field keeps the rule's choice, and removing the entry restores it."""
@@ -243,6 +262,8 @@ def test_scan_table_set_get_remove():
     dict(batch=1, seqlen=700, nheads=12, headdim=64, dstate=64, ngroups=2, chunk_size=256),
     dict(batch=2, seqlen=8192, nheads=64, headdim=64, dstate=128, ngroups=8, chunk_size=128),
     dict(batch=1, seqlen=131072, nheads=32, headdim=64, dstate=128, ngroups=1, chunk_size=256),
+    # headdim 128: the kernels split a group's 2 x 6 64-wide heads
+    dict(batch=4, seqlen=4096, nheads=12, headdim=128, dstate=128, ngroups=1, chunk_size=256),
 ])
 def test_scan_rule_is_the_list_scheduling_model(key):
     """The library's built-in (heavy, light) head blocks equal the model's,
