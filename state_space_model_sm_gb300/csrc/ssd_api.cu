@@ -310,7 +310,7 @@ BwdOffsets bwd_offsets(const Dims& d) {
 
 struct TcBwdOffsets {
   size_t delta, acs, S, Himg, dHs, dSimg, dlast, rowsum, colsum, ycs, qrow, ddir, ddiag, dBp,
-      dCp, part, seg, total;
+      dCp, part, done, seg, total;
 };
 
 TcBwdOffsets tc_bwd_offsets(const Dims& d, int nblk) {
@@ -335,6 +335,7 @@ TcBwdOffsets tc_bwd_offsets(const Dims& d, int nblk) {
   o.dBp = c.take(bp);
   o.dCp = c.take(bp);
   o.part = c.take((size_t)d.B * d.H * d.nc * 3 * sizeof(float));
+  o.done = c.take(sizeof(int));
   o.seg = c.take(seg_bytes(d));
   o.total = c.off;
   return o;
@@ -518,6 +519,7 @@ int ssd_bwd(const ssd_shape* shape, const void* x, const void* dt, const float* 
     w.dBp = reinterpret_cast<float*>(base + o.dBp);
     w.dCp = reinterpret_cast<float*>(base + o.dCp);
     w.part = reinterpret_cast<float*>(base + o.part);
+    w.done = reinterpret_cast<int*>(base + o.done);
     w.seg = o.total > o.seg ? reinterpret_cast<float*>(base + o.seg) : nullptr;
     w.nb = nb;
     t_last_path = 1;

@@ -202,6 +202,7 @@ struct TcBwdWs {
   float* dBp;     // (B, T, G, nblk, N) head-block partials of dB
   float* dCp;     // (B, T, G, nblk, N)
   float* part;    // (B, H, nc, 3)
+  int* done;      // finalize blocks done (zeroed by the chunk_state recompute)
   float* seg;     // two-level state passing scratch, or nullptr
   HeadBlocks nb;  // head blocks of dB / dC (read from the launch table once per call)
 };
@@ -246,9 +247,10 @@ cudaError_t tc_chunk_backward(const Dims& d, const BwdArgs& a, const TcBwdWs& w,
                               float* dCout, float* dBout, cudaStream_t s);
 
 // The TMA-fed chunk_state kernels (ssd_state_tc.cu): chunk_cumsum + chunk
-// state (writes delta, acs and S), and dstates (dHs from dy, C and acs).
+// state (writes delta, acs and S; and 0 to *zero when zero is not null), and
+// dstates (dHs from dy, C and acs).
 cudaError_t tc_chunk_state(const Dims& d, const FwdArgs& f, float* delta, float* acs, float* S,
-                           cudaStream_t s);
+                           int* zero, cudaStream_t s);
 // pdl: launched with launch_pdl (inside a call, after its other kernels).
 cudaError_t tc_chunk_dstates(const Dims& d, const void* dy, const void* C, const float* acs,
                              float* dHs, bool pdl, cudaStream_t s);

@@ -526,6 +526,9 @@ struct FinalizeArgs {
   float *ddt, *part;
   int T, H, L, nc;
   int hs;  // H counts 64-wide head parts, 1 << hs per head of dt / delta / ddt / part
+  int B;
+  float *dA, *ddt_bias, *dD;  // per head (ddt_bias / dD may be null)
+  int* done;                  // finalize blocks finished, 0 at launch
 };
 
 // One (chunk c, head h, batch b) of the finalize step; NT threads = L rows.
@@ -634,6 +637,36 @@ __device__ __forceinline__ void reduce_elem(const float4* __restrict__ in, float
 // (i % nc, (i / nc) % H, i / (nc H)); the rest sum the dC, then the dB
 // head-block partials (nred blocks each).  The two parts are independent, so
 // the latency-bound finalize blocks and the bandwidth-bound sums share the SMs.
+// dA, ddt_bias, dD of every head from the per-chunk partials, by the block
+// that finishes the finalize step last: per head, lane k of a warp sums the
+// chunks k, k + 32, ... of every batch row in order, then a fixed xor tree
+// combines the lanes (bit-reproducible).  part was written by other blocks:
+// it is read around L1.
+template <int NT>
+__device__ __forceinline__ void param_grads_block(const FinalizeArgs& f) {
+  const int H = f.H >> f.hs, n = f.B * f.nc, lane = threadIdx.x & 31;
+  for (int h = threadIdx.x >> 5; h < H; h += NT / 32) {
+    float a = 0.f, bb = 0.f, dd = 0.f;
+    for (int i = lane; i < n; i += 32) {
+      const int b = i / f.nc, c = i % f.nc;
+      const float* o = f.part + (((int64_t)b * H + h) * f.nc + c) * 3;
+      a += __ldcg(o);
+      bb += __ldcg(o + 1);
+      dd += __ldcg(o + 2);
+    }
+    for (int off = 16; off > 0; off >>= 1) {
+      a += __shfl_xor_sync(0xffffffffu, a, off);
+      bb += __shfl_xor_sync(0xffffffffu, bb, off);
+      dd += __shfl_xor_sync(0xffffffffu, dd, off);
+    }
+    if (lane == 0) {
+      f.dA[h] = a;
+      if (f.ddt_bias) f.ddt_bias[h] = bb;
+      if (f.dD) f.dD[h] = dd;
+    }
+  }
+}
+
 template <int NT>
 __global__ void __launch_bounds__(NT)
     k_bwd_tail_tc(FinalizeArgs f, int nfin, const float4* __restrict__ dCp,
@@ -645,6 +678,18 @@ __global__ void __launch_bounds__(NT)
   if (blk < nfin) {
     const int H = f.H >> f.hs;
     finalize_block<NT>(f, blk % f.nc, (blk / f.nc) % H, blk / (f.nc * H));
+    // the last finalize block to finish also forms the parameter gradients
+    __shared__ int last;
+    __syncthreads();  // this block's partials are written
+    if (threadIdx.x == 0) {
+      __threadfence();
+      last = atomicAdd(f.done, 1) == nfin - 1;
+    }
+    __syncthreads();
+    if (last) {
+      __threadfence();
+      param_grads_block<NT>(f);
+    }
     return;
   }
   const int rb = blk - nfin, which = rb / nred;
@@ -667,7 +712,7 @@ template <int N, int L, typename Tout>
 cudaError_t launch_tc_forward_t(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t s,
                                 int* status, int sms) {
   {
-    const cudaError_t e = tc_chunk_state(d, a, w.delta, w.acs, w.S, s);  // with chunk_cumsum
+    const cudaError_t e = tc_chunk_state(d, a, w.delta, w.acs, w.S, nullptr, s);  // + cumsum
     if (e != cudaSuccess) return e;
   }
   simt_state_passing(d, a, w, s);
@@ -692,7 +737,8 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
   f.final_state = nullptr;
   FwdWs fw{w.delta, w.acs, w.S, nullptr, nullptr, w.Himg, w.seg};
   {
-    cudaError_t e = tc_chunk_state(d, f, w.delta, w.acs, w.S, s);  // with chunk_cumsum
+    // with chunk_cumsum; zeroes the tail's count of finished finalize blocks
+    cudaError_t e = tc_chunk_state(d, f, w.delta, w.acs, w.S, w.done, s);
     if (e != cudaSuccess) return e;
     simt_state_passing(d, f, fw, s);
     e = tc_chunk_dstates(d, dy, Cm, w.acs, w.dHs, true, s);
@@ -723,7 +769,8 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
   {
     const FinalizeArgs fa{static_cast<const bf16*>(a.f.dt), a.f.dt_bias, a.f.A, w.delta,
                           w.rowsum, w.colsum, w.ycs, w.qrow, w.ddir, w.ddiag, w.dlast, nsplit,
-                          a.ddt, w.part, d.T, d.H, d.L, d.nc, d.hs};
+                          a.ddt, w.part, d.T, d.H, d.L, d.nc, d.hs, d.B, a.dA, a.ddt_bias,
+                          a.dD, w.done};
     const int nfin = d.nc * (d.H >> d.hs) * d.B;
     const int64_t rows = (int64_t)d.B * d.T * d.G;
     const int N4 = d.N / 4;
@@ -738,9 +785,6 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
         reinterpret_cast<const float4*>(w.dBp), reinterpret_cast<float4*>(a.dB),
         nred > 0 ? nred : 1, rows, prC, prB, N4));
   }
-  Dims dh = d;  // the partials are per head (of dt), not per 64-wide part
-  dh.H = d.H >> d.hs;
-  simt_param_grads(dh, w.part, a.dA, a.ddt_bias, a.dD, s);
   return cudaGetLastError();
 }
 
@@ -784,7 +828,7 @@ cudaError_t tc_forward(const Dims& d0, const FwdArgs& a, const FwdWs& w, cudaStr
 
 cudaError_t tc_front_final(const Dims& d0, const FwdArgs& a, const FwdWs& w, cudaStream_t s) {
   const Dims d = tc_dims(d0);
-  const cudaError_t e = tc_chunk_state(d, a, w.delta, w.acs, w.S, s);
+  const cudaError_t e = tc_chunk_state(d, a, w.delta, w.acs, w.S, nullptr, s);
   if (e != cudaSuccess) return e;
   simt_state_passing(d, a, w, s);
   return cudaGetLastError();
