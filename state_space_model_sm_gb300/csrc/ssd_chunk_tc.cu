@@ -199,6 +199,12 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   const int h_begin = g * (H / a.G) + kb * hb;
   const int r0 = tile * LT, col0 = REV ? r0 : 0, ncol = REV ? L - r0 : r0 + LT;
   const int npan = ncol / 64;
+  // chunk_scan on a tile of 128 columns: TMEM has room beside its C.B^T for
+  // a separate state accumulator per head parity (columns 128 + 64 st), so
+  // the state term C.H_c^T is one product of the tile's C rows (shared
+  // memory) with the image, scaled by e^{a_l} in the epilogue, instead of
+  // converted, scaled C panels
+  const bool st_direct = MODE == kFwd && ncol <= 128;
   const int t0 = c * L;
   const int Lv = min(L, T - t0);
   int* status = a.status;
@@ -352,6 +358,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
       };
       if constexpr (!S1M) {
         uint32_t u = 0;  // slot uses
+        const int upHt = st_direct ? npan : upH;
         for (int i = 0; ok && i < hb; ++i) {
           const int st = i & 1;
           // FWD: Y per head parity; DX: U and ST, single
@@ -364,7 +371,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             ok = mbar_wait(&bar_acc_empty[ab], (na - 1) & 1, status, &abort_flag);
           if (!ok) break;
           const uint64_t dops = desc_add(dOpsMN, st * LY::kOps);
-          for (int k = 0; k < upH; ++k, ++u) {
+          for (int k = 0; k < upHt; ++k, ++u) {
             const int s = u & 1;
             // the state image is needed from the first state panel on
             if (k == npan && !mbar_wait(&bar_img_full, i & 1, status, &abort_flag)) {
@@ -391,6 +398,20 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
               state_panel(colS, sc, k - npan, MODE == kDx && k == npan);
             }
             mma_commit(&bar_slot_ready[s]);  // the slot may be written again
+          }
+          if (ok && st_direct) {
+            ok = mbar_wait(&bar_img_full, i & 1, status, &abort_flag);
+            fence_after_sync();
+            if (ok) {
+#pragma unroll
+              for (int ks = 0; ks < N / 16; ++ks) {
+                const uint32_t oa = (ks / 4) * (LT * 128) + (ks % 4) * 32;
+                const uint32_t ob = (ks / 4) * (64 * 128) + (ks % 4) * 32;
+                const uint64_t ad = desc_add(dRowK, oa);
+                mma_bf16(tm + 128 + 64 * st, ad, desc_add(dImgK, ob), id_n64k, ks > 0 ? 1u : 0u);
+                mma_bf16(tm + 128 + 64 * st, ad, desc_add(dImgK, LY::kHlo + ob), id_n64k, 1u);
+              }
+            }
           }
           if (!ok) break;
           mma_commit(&bar_img_empty);
@@ -715,6 +736,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
           for (int g2 = 0; g2 < kNG; ++g2) {
             tmem_ld16(tl + colY + kPC * cq + 16 * g2, yv[g2]);
             if constexpr (MODE == kDx) tmem_ld16(tl + colY + 64 + kPC * cq + 16 * g2, sv[g2]);
+            else if (st_direct) tmem_ld16(tl + 128 + 64 * st + kPC * cq + 16 * g2, sv[g2]);
           }
           tmem_wait_ld();
         }
@@ -724,6 +746,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         const unsigned char* orow = sOps + st * LY::kOps;
         const int orr = r - col0;
         const float Dh = a.D ? a.D[h >> a.hs] : 0.f;
+        const float ea = MODE == kFwd && st_direct ? ex2_approx(da2[r]) : 0.f;  // e^{a_l}
         float pd = 0.f, pq = 0.f, pdd = 0.f;
         // y (FWD, fp32) and dx (DX) leave through TMA: this warp's 32 x 16
         // block goes to its staging slot, then one store (rows past seqlen
@@ -743,8 +766,14 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             unpack8(*reinterpret_cast<const uint4*>(orow + sw128(orr, kCPT * cq + k8)), ov);
             const float* yk = yv[k8 >> 1] + 8 * (k8 & 1);
             if constexpr (MODE == kFwd) {
+              if (st_direct) {
+                const float* sk = sv[k8 >> 1] + 8 * (k8 & 1);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) o[e] = fmaf(Dh, ov[e], yk[e]);
+                for (int e = 0; e < 8; ++e) o[e] = fmaf(Dh, ov[e], fmaf(ea, sk[e], yk[e]));
+              } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = fmaf(Dh, ov[e], yk[e]);
+              }
             } else {
               const float* sk = sv[k8 >> 1] + 8 * (k8 & 1);
               float xv[8];
@@ -820,7 +849,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
           panel(i, j);
           if (j == jepi && i > 0) epilogue(i - 1, xb);
         }
-        for (int kp = 0; kp < NP; ++kp) state_panel(i, kp);
+        if (!st_direct)
+          for (int kp = 0; kp < NP; ++kp) state_panel(i, kp);
       }
       if (hb > 0) epilogue(hb - 1, xa);
       if (lane == 0) bulk_wait_all();  // y / dx stores have read the staging and landed
