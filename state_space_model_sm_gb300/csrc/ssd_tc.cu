@@ -502,21 +502,36 @@ __global__ void __launch_bounds__(512, 1)
 // (dC kernel) and column sums (dB kernel) of M:
 //   ddA_r = sum_{j<r} (colsum_j - rowsum_j) + sum_{l>=r} ycs_l + sum_{s<r} qrow_s + dlast_c
 //   ddt_r = (ddir_r + A ddA_r) softplus'(dt_r + dt_bias);  partials of dA, ddt_bias, dD.
-__device__ __forceinline__ float block_exclusive_scan(float v, float* warp_tot) {
-  // exclusive prefix of v over the threads of the block (whole warps), in thread order
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float incl = v;
+// Exclusive prefix sums of two values over the block's threads (whole
+// warps), in thread order, and the block totals: a warp scan, the warps'
+// totals through shared memory, one barrier.
+__device__ __forceinline__ void block_exclusive_scan2(float a, float b, float2* warp_tot,
+                                                      float2& pre, float2& tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  float ia = a, ib = b;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const float o = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += o;
+    const float oa = __shfl_up_sync(0xffffffffu, ia, off);
+    const float ob = __shfl_up_sync(0xffffffffu, ib, off);
+    if (lane >= off) {
+      ia += oa;
+      ib += ob;
+    }
   }
+  if (lane == 31) warp_tot[warp] = make_float2(ia, ib);
   __syncthreads();
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  float before = 0.f;
-  for (int w = 0; w < warp; ++w) before += warp_tot[w];
-  return before + incl - v;
+  float2 before = make_float2(0.f, 0.f), all = make_float2(0.f, 0.f);
+  for (int w = 0; w < nw; ++w) {
+    const float2 t = warp_tot[w];
+    if (w < warp) {
+      before.x += t.x;
+      before.y += t.y;
+    }
+    all.x += t.x;
+    all.y += t.y;
+  }
+  pre = make_float2(before.x + ia - a, before.y + ib - b);
+  tot = all;
 }
 
 struct FinalizeArgs {
@@ -551,7 +566,9 @@ __device__ __forceinline__ void finalize_block(const FinalizeArgs& f, int c, int
   float* __restrict__ ddt = f.ddt;
   float* __restrict__ part = f.part;
   const int nsplit = f.nsplit, T = f.T, H = f.H >> f.hs, L = f.L, nc = f.nc, V = 1 << f.hs;
-  __shared__ float wt[NW], red[NW];
+  __shared__ float2 wt[NW];
+  __shared__ float3 red[NW];
+  __shared__ float s_dl;
   const int r = threadIdx.x;
   const int Lv = min(L, T - c * L);
   const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
@@ -559,7 +576,7 @@ __device__ __forceinline__ void finalize_block(const FinalizeArgs& f, int c, int
   const int64_t ti = ((int64_t)b * T + (int64_t)c * L + r) * H + h;
   const float vdt = live ? __bfloat162float(dt[ti]) : 0.f;
   const float dlt = live ? delta[cv + r] : 0.f;
-  float jump = 0.f, y = 0.f, dirr = 0.f, dg = 0.f, dl = 0.f;
+  float jump = 0.f, y = 0.f, dirr = 0.f, dg = 0.f;
   for (int j = 0; j < V; ++j) {
     const int64_t bhc = ((int64_t)b * H + h) * V + j;  // the part's (b, part) row
     const int64_t cp = (bhc * nc + c) * L;
@@ -569,16 +586,23 @@ __device__ __forceinline__ void finalize_block(const FinalizeArgs& f, int c, int
       dirr += ddir[cp + r];
       dg += ddiag[cp + r];
     }
-    for (int k = 0; k < nsplit; ++k) dl += dlast[(bhc * nc + c) * nsplit + k];
+  }
+  // dlast: the state-passing partials of every part, summed by warp 0 (lane
+  // k takes the partials k, k + 32, ..., then a fixed xor tree), visible to
+  // the block after the scans' barriers
+  if (r < 32) {
+    float v = 0.f;
+    for (int j = 0; j < V; ++j) {
+      const int64_t bhc = ((int64_t)b * H + h) * V + j;
+      for (int k = r; k < nsplit; k += 32) v += dlast[(bhc * nc + c) * nsplit + k];
+    }
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (r == 0) s_dl = v;
   }
   // ddA_r = prefix_{j<r}(jump_j) + dlast + suffix_{l>=r}(ycs_l)
-  const float pre = block_exclusive_scan(jump, wt);
-  const float ypre = block_exclusive_scan(y, wt);   // sum_{l<r} ycs
-  __syncthreads();
-  if ((r & 31) == 31) red[r >> 5] = ypre + y;
-  __syncthreads();
-  const float ytot = red[NW - 1];
-  const float dd = pre + dl + (ytot - ypre);
+  float2 pre, tot;  // .x jump, .y ycs
+  block_exclusive_scan2(jump, y, wt, pre, tot);
+  const float dd = pre.x + s_dl + (tot.y - pre.y);
   float pA = 0.f, pB = 0.f, pD = 0.f;
   if (live) {
     const float v = vdt + (dt_bias ? dt_bias[h] : 0.f);
@@ -589,19 +613,26 @@ __device__ __forceinline__ void finalize_block(const FinalizeArgs& f, int c, int
     pB = gv;
     pD = dg;
   }
-  float vals[3] = {pA, pB, pD};
-#pragma unroll
-  for (int k = 0; k < 3; ++k) {
-    float v = vals[k];
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    __syncthreads();
-    if ((r & 31) == 0) red[r >> 5] = v;
-    __syncthreads();
-    if (r == 0) {
-      float t = 0.f;
-      for (int i = 0; i < NW; ++i) t += red[i];
-      part[(((int64_t)b * H + h) * nc + c) * 3 + k] = t;
+  // the block's partials of dA, ddt_bias and dD: warp trees, then the warps
+  // in order
+  for (int o = 16; o > 0; o >>= 1) {
+    pA += __shfl_xor_sync(0xffffffffu, pA, o);
+    pB += __shfl_xor_sync(0xffffffffu, pB, o);
+    pD += __shfl_xor_sync(0xffffffffu, pD, o);
+  }
+  if ((r & 31) == 0) red[r >> 5] = make_float3(pA, pB, pD);
+  __syncthreads();
+  if (r == 0) {
+    float3 t = make_float3(0.f, 0.f, 0.f);
+    for (int i = 0; i < NW; ++i) {
+      t.x += red[i].x;
+      t.y += red[i].y;
+      t.z += red[i].z;
     }
+    float* o = part + (((int64_t)b * H + h) * nc + c) * 3;
+    o[0] = t.x;
+    o[1] = t.y;
+    o[2] = t.z;
   }
 }
 
@@ -679,8 +710,8 @@ __global__ void __launch_bounds__(NT)
     const int H = f.H >> f.hs;
     finalize_block<NT>(f, blk % f.nc, (blk / f.nc) % H, blk / (f.nc * H));
     // the last finalize block to finish also forms the parameter gradients
+    // (thread 0 wrote this block's partials)
     __shared__ int last;
-    __syncthreads();  // this block's partials are written
     if (threadIdx.x == 0) {
       __threadfence();
       last = atomicAdd(f.done, 1) == nfin - 1;
