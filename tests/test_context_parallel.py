@@ -298,6 +298,7 @@ def test_segment_decay_matches_definition(cuda_lib, dtype, B, T, H):
     ("f32", (2, 300, 4, 16, 32, 2, 64)),          # generic kernels, ragged last chunk
     ("bf16", (2, 1000, 8, 64, 128, 2, 256)),      # tensor-core kernels, ragged last chunk
     ("bf16", (1, 640, 4, 64, 64, 1, 128)),
+    ("bf16", (1, 640, 3, 128, 64, 3, 128)),       # headdim 128 on the tensor cores
 ])
 def test_first_passes_match_oracle(cuda_lib, dtype, shape_args):
     """ssd_final_state = the oracle forward's final state; ssd_dinit = the
@@ -347,6 +348,7 @@ def test_state_scan_matches_definition(cuda_lib, R):
 @pytest.mark.parametrize("dtype,shape_args,sizes", [
     ("f32", (2, 700, 4, 16, 32, 2, 64), [256, 192, 252]),
     ("bf16", (2, 2048, 8, 64, 128, 2, 256), [1024, 512, 512]),
+    ("bf16", (1, 1024, 4, 128, 128, 1, 256), [512, 256, 256]),
 ])
 def test_library_context_parallel_matches_unsplit_oracle(cuda_lib, dtype, shape_args, sizes):
     import torch

@@ -317,6 +317,8 @@ SEG_CASES = [
     ("seg_8x4", SSDShape(1, 4000, 2, 64, 128, 1, 128), 0.3),
     ("seg_ragged", SSDShape(1, 3800, 2, 64, 128, 1, 128), 0.3),
     ("seg_n64", SSDShape(1, 1100, 2, 64, 64, 1, 128), 0.3),
+    # one head of headdim 128 (two 64-wide parts sharing its decay)
+    ("seg_p128", SSDShape(1, 4000, 1, 128, 128, 1, 128), 0.3),
 ]
 
 
