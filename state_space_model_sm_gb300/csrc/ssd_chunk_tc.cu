@@ -1,24 +1,21 @@
-// tcgen05 chunk kernels of the SSD, fed by TMA (sm_103a).  One template, four
-// roles, each over a 128-row tile of one chunk and a block of heads of one
-// group ("Optimizing Mamba-2 kernels for the B200", Stage 1 kernel table:
-// _chunk_scan_fwd fwd_5, _chunk_scan_chunk_state_bwd_dx bwd_10,
-// _chunk_scan_bwd_dC bwd_12, _chunk_state_bwd_db bwd_11):
+// tcgen05 chunk kernels of the SSD, fed by TMA (sm_103a).  One template,
+// three roles, each over a 128-row tile of one chunk and a block of heads of
+// one group ("Optimizing Mamba-2 kernels for the B200", Stage 1 kernel table:
+// _chunk_scan_fwd fwd_5, _chunk_scan_bwd_dC bwd_12, _chunk_state_bwd_db
+// bwd_11; the backward's dx, bwd_10, runs in ssd_tc.cu):
 //
 //   FWD  rows l, columns s <= l:  P  = CB[l,s] e^{a_l-a_s} delta_s
 //        y_l  = sum_s P[l,s] x_s + e^{a_l} C_l.H_c^T + D x_l
-//   DX   rows s, columns l >= s:  P  = CB[l,s] e^{a_l-a_s}
-//        u_s  = sum_l P[s,l] dy_l + e^{a_last-a_s} B_s.dS_c^T
-//        dx_s = delta_s u_s + D dy_s;  <x_s,u_s>, delta_s <x_s, state part>, <x_s,dy_s>
 //   DC   rows l, columns s <= l:  P2 = e^{a_l-a_s} delta_s <dy_l, x_s>
 //        dC_l += sum_s P2[l,s] B_s + e^{a_l} dy_l.H_c   (summed over the block's heads)
 //        rowsum_l = sum_{s<l} CB[l,s] P2[l,s];  ycs_l = e^{a_l} <dy_l, C_l.H_c^T>
 //   DB   rows s, columns l >= s:  P2 = e^{a_l-a_s} delta_s <x_s, dy_l>
 //        dB_s += sum_l P2[s,l] C_l + delta_s e^{a_last-a_s} x_s.dS_c
 //        colsum_s = sum_{l>s} CB[l,s] P2[s,l]
-// with CB = C.B^T of the chunk (the column-row orientation in DX / DB).
+// with CB = C.B^T of the chunk (the column-row orientation in DB).
 //
 // CB of the tile is formed once per CTA into TMEM and read by every head: it is
-// P's base in FWD / DX and gives the ddA sums of DC / DB directly, element by
+// P's base in FWD and gives the ddA sums of DC / DB directly, element by
 // element, so no per-head accumulator is needed for them.
 //
 // Warp roles (576 threads): warps 0-15 convert (TMEM -> decay, mask, hi/lo
@@ -47,7 +44,7 @@ namespace {
 using namespace tc;
 using bf16 = __nv_bfloat16;
 
-enum : int { kFwd = 0, kDx = 1, kDc = 2, kDb = 3 };
+enum : int { kFwd = 0, kDc = 2, kDb = 3 };
 
 constexpr int kConvWarps = 16;  // 4 TMEM lane quarters x 4 column groups
 constexpr int kConv = 32 * kConvWarps;
@@ -66,7 +63,7 @@ constexpr int kChunkThreads = 32 * (kConvWarps + 2);
 // conversion warps into tensor memory.
 template <int N, int L, int MODE>
 struct ChunkLayout {
-  static constexpr bool kRev = MODE == kDx || MODE == kDb;
+  static constexpr bool kRev = MODE == kDb;
   static constexpr bool kS1 = MODE == kDc || MODE == kDb;
   static constexpr int kLT = 128;                 // rows of a tile
   static constexpr int kNP = N / 64;              // 64-wide panels of a B / C row
@@ -78,20 +75,20 @@ struct ChunkLayout {
   static constexpr int kHR = kLT * 128;           // DC / DB: the tile's dy (x) rows
   static constexpr int oRow = 0;
   static constexpr int oCol = oRow + kRow;
-  static constexpr int oOps = oCol + kCol;                          // FWD / DX: two stages
+  static constexpr int oOps = oCol + kCol;                          // FWD: two stages
   static constexpr int oHR = oOps + (kS1 ? kOps : 2 * kOps);
   static constexpr int oImg = oHR + (kS1 ? kHR : 0);
   static constexpr int oVec = oImg + kImg;                         // raw [2 stages][a, delta][L]
-  // derived per-head arrays: FWD / DX keep three heads (a head's epilogue runs
+  // derived per-head arrays: FWD keeps three heads (a head's epilogue runs
   // during the next one), DC / DB two
   static constexpr int kNDer = kS1 ? 2 : 3;
   static constexpr int oDer = oVec + 4 * L * 4;                    // [kNDer][a2, sx, cf][L]
   static constexpr int oRed = oDer + kNDer * 3 * L * 4;            // [3][kCG][128] row partials
   static constexpr int kEnd = (oRed + 3 * kCG * 128 * 4 + 1023) / 1024 * 1024;
-  // FWD / DX: each conversion warp stages its 32 x 16 block of a head's y or
-  // dx (2 KB) for one TMA store; the column operand's rows are dead once C.B^T
+  // FWD: each conversion warp stages its 32 x 16 block of a head's y (2 KB)
+  // for one TMA store; the column operand's rows are dead once C.B^T
   // is formed, so the staging reuses them when they are large enough
-  static constexpr int kStg = MODE == kFwd || MODE == kDx ? kConvWarps * 2048 : 0;
+  static constexpr int kStg = MODE == kFwd ? kConvWarps * 2048 : 0;
   static constexpr bool kStgInCol = kCol >= kStg;
   static constexpr int oStg = kStgInCol ? oCol : kEnd;
   static constexpr int kBytes = kEnd + (kStgInCol ? 0 : kStg) + 1024;
@@ -101,15 +98,11 @@ struct ChunkLayout {
 struct ChunkArgs {
   const float* delta;        // (B, H >> hs, nc, L)
   const float* acs;          // (B, H >> hs, nc, L)
-  const unsigned char* img;  // state images (B, nc, H): H_c (FWD, DC) or dS_c (DX, DB)
+  const unsigned char* img;  // state images (B, nc, H): H_c (FWD, DC) or dS_c (DB)
   const float* D;            // (H >> hs) or null
-  const bf16* xg;            // DX: x, for the epilogue's inner products
-  void* out;                 // FWD y, DX dx, DC / DB partials (B, T, G, nblk, N)
+  void* out;                 // FWD y, DC / DB partials (B, T, G, nblk, N)
   float* msum;               // DC rowsum, DB colsum  (B, H, nc, L)
   float* ycs;                // DC
-  float* ddir;               // DX
-  float* qrow;               // DX
-  float* ddiag;              // DX
   int T, H, G, nc;
   int hs;      // H counts 64-wide head parts, 1 << hs per head of delta / a / D
   int nbt[2];  // head blocks per group of row tile 0 / 1 (the grid holds the heavier first)
@@ -157,15 +150,15 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     k_chunk_tc(const __grid_constant__ CUtensorMap mRow, const __grid_constant__ CUtensorMap mCol,
                const __grid_constant__ CUtensorMap mOps, const __grid_constant__ CUtensorMap mHR,
                const ChunkArgs a) {
-  // mHR: DC / DB the tile's dy (x) rows; FWD (fp32 y) and DX the map y or dx
-  // is stored through (fp32 (B, T, H, 64), boxes of 16 x 1 x 32, 64-byte swizzle)
+  // mHR: DC / DB the tile's dy (x) rows; FWD (fp32 y) the map y is stored
+  // through (fp32 (B, T, H, 64), boxes of 16 x 1 x 32, 64-byte swizzle)
   using LY = ChunkLayout<N, L, MODE>;
   constexpr bool REV = LY::kRev, S1M = LY::kS1;
   constexpr int LT = LY::kLT, NLT = L / LT, NP = LY::kNP;
   // TMEM columns: C.B^T of the tile [0, 256); two 64-column operand slots
   // (a 64-wide K panel as hi / lo bf16 per 16-wide group; in DC / DB first the
   // fp32 S1 panel, converted in place); accumulators from 384: FWD Y per head
-  // parity, DX U and ST, DC / DB the block's dC / dB rows
+  // parity, DC / DB the block's dC / dB rows
   constexpr uint32_t kColSlot = 256, kColAcc = 384;
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t bar_unit, bar_cb, bar_ops_full[2], bar_ops_empty[2], bar_vec_full[2],
@@ -184,7 +177,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   float* sRed = reinterpret_cast<float*>(base + LY::oRed);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // heavier row tiles (more columns) first: FWD / DC the last tile, DX / DB the
+  // heavier row tiles (more columns) first: FWD / DC the last tile, DB the
   // first; each tile cuts a group's heads into its own number of blocks
   const int th = REV ? 0 : NLT - 1;  // the heavier tile
   const int zh = NLT > 1 ? a.G * a.nbt[th] : 0;
@@ -239,7 +232,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   // that need nothing from it
   griddep_launch_dependents();
   const uint32_t tm = tmem_base;
-  // slot uses per head: FWD / DX the P panels, then the state term's K panels;
+  // slot uses per head: FWD the P panels, then the state term's K panels;
   // DC the S1 panels, the state term's A operand and the state dot C.H_c^T; DB
   // the S1 panels and the state term's A operand
   const int upH = S1M ? npan + (MODE == kDc ? 2 : 1) : npan + NP;
@@ -346,12 +339,12 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
       constexpr uint32_t id_nNm = idesc_bf16(128, N, 0, 1);     // B MN-major, N = d_state
       // the state term's K panel kp with A in slot sc: B = image K-major (rows
       // p), hi and lo parts, three products per K step (hi.hi, hi.lo, lo.hi)
-      auto state_panel = [&](uint32_t dcol, uint32_t sc, int kp, bool first) {
+      auto state_panel = [&](uint32_t dcol, uint32_t sc, int kp) {
         const uint64_t bk = desc_add(dImgK, kp * (64 * 128));
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           const uint64_t bh = desc_add(bk, ks * 32), bl = desc_add(bk, LY::kHlo + ks * 32);
-          mma_bf16_ta(tm + dcol, sc + 16 * ks, bh, id_n64k, (first && ks == 0) ? 0u : 1u);
+          mma_bf16_ta(tm + dcol, sc + 16 * ks, bh, id_n64k, 1u);
           mma_bf16_ta(tm + dcol, sc + 16 * ks, bl, id_n64k, 1u);
           mma_bf16_ta(tm + dcol, sc + 16 * ks + 8, bh, id_n64k, 1u);
         }
@@ -361,11 +354,10 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         const int upHt = st_direct ? npan : upH;
         for (int i = 0; ok && i < hb; ++i) {
           const int st = i & 1;
-          // FWD: Y per head parity; DX: U and ST, single
-          const uint32_t colY = MODE == kFwd ? kColAcc + 64 * st : kColAcc;
-          const uint32_t colS = MODE == kFwd ? colY : kColAcc + 64;
-          const int ab = MODE == kFwd ? st : 0;
-          const int na = MODE == kFwd ? (i >> 1) : i;  // earlier uses of this accumulator
+          // Y per head parity (the state panels add into it)
+          const uint32_t colY = kColAcc + 64 * st;
+          const int ab = st;
+          const int na = i >> 1;  // earlier uses of this accumulator
           ok = mbar_wait(&bar_ops_full[st], (i >> 1) & 1, status, &abort_flag);
           if (ok && na >= 1)
             ok = mbar_wait(&bar_acc_empty[ab], (na - 1) & 1, status, &abort_flag);
@@ -395,7 +387,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
               }
               if (k == npan - 1) mma_commit(&bar_ops_empty[st]);  // x / dy rows read
             } else {
-              state_panel(colS, sc, k - npan, MODE == kDx && k == npan);
+              state_panel(colY, sc, k - npan);
             }
             mma_commit(&bar_slot_ready[s]);  // the slot may be written again
           }
@@ -544,7 +536,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     fence_after_sync();
 
     // per-head vectors -> derived arrays: a2 = a log2 e; sx: FWD / DC / DB
-    // a2 - log2 delta (+inf where delta = 0), DX delta; cf: column factors of the
+    // a2 - log2 delta (+inf where delta = 0); cf: column factors of the
     // factorized decay inside the causal triangle.  The barriers here keep the
     // conversion warps within one head of each other.
     auto der = [&](int i) { return sDer + (i % LY::kNDer) * 3 * L; };
@@ -559,8 +551,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
       for (int t = tid; t < L; t += kConv) {
         const float a2 = ra[t] * kLog2e, dl = ra[L + t];
         da2[t] = a2;
-        if constexpr (MODE == kDx) dsx[t] = dl;
-        else dsx[t] = dl > 0.f ? a2 - lg2_approx(dl) : __int_as_float(0x7f800000);
+        dsx[t] = dl > 0.f ? a2 - lg2_approx(dl) : __int_as_float(0x7f800000);
       }
       warp_arrive(&bar_vec_empty[v], lane);
       conv_sync();
@@ -572,7 +563,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     };
 
     // slot protocol (conversion side): wait until the MMA warp hands the slot
-    // over (FWD / DX: the products that read its previous contents are done;
+    // over (FWD: the products that read its previous contents are done;
     // DC / DB: S1, the state dot or an empty slot is there), then work on it
     uint32_t u = 0;  // slot uses
     auto slot_acquire = [&]() -> uint32_t {
@@ -592,7 +583,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
       ++u;
     };
 
-    // one 64-column panel j of head i: P (FWD / DX) or P2 (DC / DB) in fp32,
+    // one 64-column panel j of head i: P (FWD) or P2 (DC / DB) in fp32,
     // then hi / lo bf16 into the slot; DC / DB also add the row's M terms
     float msum = 0.f;
     auto panel = [&](int i, int j) {
@@ -635,7 +626,6 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
           // e^{a_l - a_s} (times delta) = R_row * cf_col, with the group's edge column m
           float R;
           if constexpr (MODE == kFwd || MODE == kDc) R = ex2_approx(a2r - da2[cg + 15]);
-          else if constexpr (MODE == kDx) R = ex2_approx(da2[cg] - a2r);
           else R = ex2_approx(da2[cg] - sxr);
           const float2 R2 = make_float2(R, R);
 #pragma unroll
@@ -665,7 +655,6 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             const int cl = cg + e;
             float f;
             if constexpr (MODE == kFwd || MODE == kDc) f = ex2_approx(a2r - dsx[cl]);
-            else if constexpr (MODE == kDx) f = ex2_approx(da2[cl] - a2r);
             else f = ex2_approx(da2[cl] - sxr);
             const bool valid = REV ? cl >= r : cl <= r;
             vv[e] = valid ? f * vv[e] : 0.f;
@@ -678,12 +667,11 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
       slot_release(true);
     };
 
-    // a state-term K panel (FWD / DX): the row operand (C_l or B_s, 64 of its
-    // d_state columns) scaled by e^{a_l} (FWD) or e^{a_last - a_s} (DX)
+    // a state-term K panel (chunk_scan): 64 of the d_state columns of the
+    // row's C scaled by e^{a_l}
     auto state_panel = [&](int i, int kp) {
       const float* da2 = der(i);
-      const float a2r = da2[r];
-      const float sc_r = MODE == kFwd ? ex2_approx(a2r) : ex2_approx(da2[L - 1] - a2r);
+      const float sc_r = ex2_approx(da2[r]);
       const uint32_t sc = slot_acquire();
 #pragma unroll
       for (int qg = 0; qg < kNG; ++qg) {
@@ -703,89 +691,58 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     };
 
     if constexpr (!S1M) {
-      // FWD / DX: a head's epilogue runs after the next head's second panel,
-      // so its last products finish while those panels are converted.
-      // DX: this thread's x values of its row, loaded from global memory when
-      // its head starts (xa); head i's epilogue runs during head i + 1 (xb)
-      uint4 xa[kCPT] = {}, xb[kCPT] = {};
-      int n_ostores = 0;  // FWD / DX: TMA stores this warp has issued
-      auto prefetch_x = [&](int i, uint4 (&xr)[kCPT]) {
-        if constexpr (MODE == kDx) {
-          const int64_t off = (((int64_t)b * T + t0 + r) * H + h_begin + i) * 64 + kPC * cq;
-#pragma unroll
-          for (int k = 0; k < kCPT; ++k)
-            xr[k] = live ? *reinterpret_cast<const uint4*>(a.xg + off + 8 * k)
-                         : make_uint4(0, 0, 0, 0);
-        }
-      };
-      auto epilogue = [&](int i, const uint4 (&xr)[kCPT]) {
+      // chunk_scan: a head's epilogue runs after the next head's second panel,
+      // so its last products finish while those panels are converted
+      int n_ostores = 0;  // TMA stores this warp has issued
+      auto epilogue = [&](int i) {
         const int st = i & 1, h = h_begin + i;
-        const int ab = MODE == kFwd ? st : 0;
-        const int na = MODE == kFwd ? (i >> 1) : i;
+        const int na = i >> 1;
         const float* da2 = der(i);
-        const float* dsx = da2 + L;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full[ab], na & 1, status, &abort_flag)) &&
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full[st], na & 1, status, &abort_flag)) &&
              ok;
         ok = __all_sync(0xffffffffu, mbar_wait(&bar_ops_full[st], (i >> 1) & 1, status,
                                                &abort_flag)) && ok;
         fence_after_sync();
         float yv[kNG][16], sv[kNG][16];
-        const uint32_t colY = MODE == kFwd ? kColAcc + 64 * st : kColAcc;
+        const uint32_t colY = kColAcc + 64 * st;
         if (ok) {
 #pragma unroll
           for (int g2 = 0; g2 < kNG; ++g2) {
             tmem_ld16(tl + colY + kPC * cq + 16 * g2, yv[g2]);
-            if constexpr (MODE == kDx) tmem_ld16(tl + colY + 64 + kPC * cq + 16 * g2, sv[g2]);
-            else if (st_direct) tmem_ld16(tl + 128 + 64 * st + kPC * cq + 16 * g2, sv[g2]);
+            if (st_direct) tmem_ld16(tl + 128 + 64 * st + kPC * cq + 16 * g2, sv[g2]);
           }
           tmem_wait_ld();
         }
         fence_before_sync();
-        warp_arrive(&bar_acc_empty[ab], lane);
-        // this thread's row of the stage's x (FWD) or dy (DX) rows
+        warp_arrive(&bar_acc_empty[st], lane);
+        // this thread's row of the stage's x rows
         const unsigned char* orow = sOps + st * LY::kOps;
         const int orr = r - col0;
         const float Dh = a.D ? a.D[h >> a.hs] : 0.f;
-        const float ea = MODE == kFwd && st_direct ? ex2_approx(da2[r]) : 0.f;  // e^{a_l}
-        float pd = 0.f, pq = 0.f, pdd = 0.f;
-        // y (FWD, fp32) and dx (DX) leave through TMA: this warp's 32 x 16
-        // block goes to its staging slot, then one store (rows past seqlen
-        // are clipped by it); bf16 y is written directly
-        constexpr bool kTmaO = (MODE == kFwd && sizeof(Tout) == 4) || MODE == kDx;
+        const float ea = st_direct ? ex2_approx(da2[r]) : 0.f;  // e^{a_l}
+        // fp32 y leaves through TMA: this warp's 32 x 16 block goes to its
+        // staging slot, then one store (rows past seqlen are clipped by it);
+        // bf16 y is written directly
+        constexpr bool kTmaO = sizeof(Tout) == 4;
         unsigned char* stg = base + LY::oStg + warp * 2048;
         if (kTmaO && ok && n_ostores > 0) {  // the previous head's store has read the slot
           if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
         }
         if (ok && (kTmaO || live)) {
-          const float dr = MODE == kDx ? dsx[r] : 0.f;
           const int64_t ooff = (((int64_t)b * T + t0 + r) * H + h) * 64 + kPC * cq;
 #pragma unroll
           for (int k8 = 0; k8 < kCPT; ++k8) {
             float ov[8], o[8];
             unpack8(*reinterpret_cast<const uint4*>(orow + sw128(orr, kCPT * cq + k8)), ov);
             const float* yk = yv[k8 >> 1] + 8 * (k8 & 1);
-            if constexpr (MODE == kFwd) {
-              if (st_direct) {
-                const float* sk = sv[k8 >> 1] + 8 * (k8 & 1);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = fmaf(Dh, ov[e], fmaf(ea, sk[e], yk[e]));
-              } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = fmaf(Dh, ov[e], yk[e]);
-              }
-            } else {
+            if (st_direct) {
               const float* sk = sv[k8 >> 1] + 8 * (k8 & 1);
-              float xv[8];
-              unpack8(xr[k8], xv);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float uu = yk[e] + sk[e];
-                o[e] = fmaf(dr, uu, Dh * ov[e]);
-                pd = fmaf(xv[e], uu, pd);
-                pq = fmaf(xv[e], sk[e], pq);
-                pdd = fmaf(xv[e], ov[e], pdd);
-              }
+              for (int e = 0; e < 8; ++e) o[e] = fmaf(Dh, ov[e], fmaf(ea, sk[e], yk[e]));
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o[e] = fmaf(Dh, ov[e], yk[e]);
             }
             if constexpr (kTmaO) {
 #pragma unroll
@@ -812,48 +769,21 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
           ++n_ostores;
         }
         warp_arrive(&bar_ops_empty[st], lane);
-        if constexpr (MODE == kDx) {
-          // the row's column groups meet in shared memory (the next writes come
-          // after the next head's derive barriers)
-          if (cq > 0) {
-            sRed[(0 * kCG + cq) * 128 + rr] = pd;
-            sRed[(1 * kCG + cq) * 128 + rr] = pq;
-            sRed[(2 * kCG + cq) * 128 + rr] = pdd;
-          }
-          conv_sync();
-          if (cq == 0 && live && ok) {
-#pragma unroll
-            for (int k = 1; k < kCG; ++k) {
-              pd += sRed[(0 * kCG + k) * 128 + rr];
-              pq += sRed[(1 * kCG + k) * 128 + rr];
-              pdd += sRed[(2 * kCG + k) * 128 + rr];
-            }
-            const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
-            a.ddir[cv + r] = pd;
-            a.qrow[cv + r] = dsx[r] * pq;
-            a.ddiag[cv + r] = pdd;
-          }
-        }
       };
       for (int i = 0; i < hb; ++i) {
         derive(i);
-        if constexpr (MODE == kDx) {
-#pragma unroll
-          for (int k = 0; k < kCPT; ++k) xb[k] = xa[k];  // the previous head's
-        }
-        prefetch_x(i, xa);
         // the previous head's epilogue runs once two of this head's panels are
         // handed over, so the MMA warp has both to work on meanwhile
         const int jepi = npan > 1 ? 1 : 0;
         for (int j = 0; j < npan; ++j) {
           panel(i, j);
-          if (j == jepi && i > 0) epilogue(i - 1, xb);
+          if (j == jepi && i > 0) epilogue(i - 1);
         }
         if (!st_direct)
           for (int kp = 0; kp < NP; ++kp) state_panel(i, kp);
       }
-      if (hb > 0) epilogue(hb - 1, xa);
-      if (lane == 0) bulk_wait_all();  // y / dx stores have read the staging and landed
+      if (hb > 0) epilogue(hb - 1);
+      if (lane == 0) bulk_wait_all();  // the y stores have read the staging and landed
     } else {
       uint4 hrow[kCPT];  // this thread's values of its row of dy (DC) or x (DB)
       for (int i = 0; i < hb; ++i) {
@@ -1025,7 +955,6 @@ cudaError_t chunk_bwd_nl(const Dims& d, const BwdArgs& ba, const TcBwdWs& w, Hea
   a.delta = w.delta;
   a.acs = w.acs;
   a.D = ba.f.D;
-  a.xg = static_cast<const bf16*>(ba.f.x);
   a.T = d.T;
   a.H = d.H;
   a.G = d.G;
