@@ -216,6 +216,11 @@ __global__ void __launch_bounds__(512, 1)
   float* sraw = sx + L;             // prefetched a [L], delta [L] of the next head
   constexpr uint32_t id_py = idesc_bf16(128, kP, 0, 1);
   constexpr uint32_t id_st = idesc_bf16(128, kP, 0, 0);
+  // shared-memory descriptors formed once; each product adds its offset (the
+  // issuing thread shares its scheduler with the group's other warps)
+  const uint64_t dR = sdesc(smem_u32(sR), 16, 1024);        // row operand, K-major
+  const uint64_t dP = sdesc(smem_u32(Pw), 16, 1024);        // P panel / state image, K-major
+  const uint64_t dX = sdesc(smem_u32(sX), L * 128, 1024);   // x / dy rows, MN-major
 
   // fp32 out leaves through TMA stores when the operand-row buffer can stage
   // every warp's 32 x 32 block (4 KB each, 128-byte swizzle): each head's
@@ -267,13 +272,12 @@ __global__ void __launch_bounds__(512, 1)
     group_sync(gbar);
     if (wtid == 0) {
       fence_after_sync();
+#pragma unroll
       for (int ks = 0; ks < N / 16; ++ks) {
         const uint32_t kp = ks / 4, ko = (ks % 4) * 32;
-        const uint64_t ad = sdesc(smem_u32(sR) + kp * (LT * 128) + ko, 16, 1024);
-        mma_bf16(tm + colST, ad, sdesc(smem_u32(Pw) + kp * (64 * 128) + ko, 16, 1024), id_st,
-                 ks > 0 ? 1u : 0u);
-        mma_bf16(tm + colST, ad, sdesc(smem_u32(Pw) + SM::kHlo + kp * (64 * 128) + ko, 16, 1024),
-                 id_st, 1u);
+        const uint64_t ad = desc_add(dR, kp * (LT * 128) + ko);
+        mma_bf16(tm + colST, ad, desc_add(dP, kp * (64 * 128) + ko), id_st, ks > 0 ? 1u : 0u);
+        mma_bf16(tm + colST, ad, desc_add(dP, SM::kHlo + kp * (64 * 128) + ko), id_st, 1u);
       }
       mma_commit(&bar_st[wg]);
     }
@@ -358,11 +362,12 @@ __global__ void __launch_bounds__(512, 1)
       group_sync(gbar);
       if (wtid == 0) {
         fence_after_sync();
+        const uint64_t dXj = desc_add(dX, 64 * j * 128);
+#pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bd = sdesc(smem_u32(sX) + (64 * j + 16 * ks) * 128, L * 128, 1024);
-          mma_bf16(tm + colY, sdesc(smem_u32(Pw) + ks * 32, 16, 1024), bd, id_py,
-                   (j > 0 || ks > 0) ? 1u : 0u);
-          mma_bf16(tm + colY, sdesc(smem_u32(Pw) + LT * 128 + ks * 32, 16, 1024), bd, id_py, 1u);
+          const uint64_t bd = desc_add(dXj, 16 * ks * 128);
+          mma_bf16(tm + colY, desc_add(dP, ks * 32), bd, id_py, (j > 0 || ks > 0) ? 1u : 0u);
+          mma_bf16(tm + colY, desc_add(dP, LT * 128 + ks * 32), bd, id_py, 1u);
         }
         mma_commit(&bar_p[wg]);
         if (j == nsp - 1) mma_commit(&bar_done[wg]);  // one phase per head
