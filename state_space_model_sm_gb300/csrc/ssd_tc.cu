@@ -101,7 +101,8 @@ __device__ __forceinline__ void group_sync(int id) {
 
 template <int N, int L, typename Tout, bool REV>
 __global__ void __launch_bounds__(512, 1)
-    k_scan_tc(const __grid_constant__ CUtensorMap mOut, const bf16* __restrict__ x,
+    k_scan_tc(const __grid_constant__ CUtensorMap mOut, const __grid_constant__ CUtensorMap mOp,
+              const bf16* __restrict__ x,
               const bf16* __restrict__ Bm,
               const bf16* __restrict__ Cm, const bf16* __restrict__ dy,
               const float* __restrict__ delta, const float* __restrict__ acs,
@@ -113,7 +114,7 @@ __global__ void __launch_bounds__(512, 1)
   constexpr int LT = SM::kLT, NLT = L / LT;
   griddep_wait();  // the state images and vectors come from the previous kernels
   extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t bar_cb, bar_p[2], bar_st[2], bar_done[2];
+  __shared__ uint64_t bar_cb, bar_p[2], bar_st[2], bar_done[2], bar_ld[2], bar_xr[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   unsigned char* base = align1024(smem_raw);
@@ -138,6 +139,8 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&bar_p[i], 1);
       mbar_init(&bar_st[i], 1);
       mbar_init(&bar_done[i], 1);
+      mbar_init(&bar_ld[i], 1);
+      mbar_init(&bar_xr[i], 1);
     }
     fence_mbar_init();
   }
@@ -161,6 +164,9 @@ __global__ void __launch_bounds__(512, 1)
   float* sred = sAall + 8 * L + wg * 3 * 128;  // [3][128] per pipeline: half-row partial sums
   float* scf = sAall + 8 * L + 6 * 128 + wg * L;  // per pipeline: column factors (forward)
   uint32_t n_p = 0, n_st = 0, n_done = 0, n_units = 0;
+  // per pipeline: heads started (all threads), and (thread wtid 0) the copies
+  // issued of the image + vectors and of the operand rows
+  uint32_t n_heads = 0, n_ld = 0, n_xr = 0;
 
   for (int64_t item = it_begin; item < it_end;) {
     // one unit = (batch, chunk, row tile, group); this CTA's heads of it
@@ -227,41 +233,39 @@ __global__ void __launch_bounds__(512, 1)
   // epilogue reads its own x / dy row from sX first, then the block is staged
   // there and stored, and only then do the next head's rows come in
   constexpr bool kTmaO = sizeof(Tout) == 4 && SM::kX >= 8 * 4096;
-  // cp.async of what a head needs, in two commit groups: its inter-chunk
-  // state image (into the P buffer) and raw a / delta, then its
-  // second-operand rows (sX), which the first P product waits for.
+  // What a head needs, copied by thread wtid 0 of its pipeline: its
+  // inter-chunk state image (into the P buffer) and raw a / delta with bulk
+  // copies on bar_ld, and its second-operand rows (sX, 128-byte swizzle; rows
+  // past seqlen read as zeros) with TMA on bar_xr, which the first P product
+  // waits for.
   auto prefetch_x = [&](int hh) {
-    for (int i = wtid; i < ncol * 8; i += 256) {
-      const int cc = i >> 3, j = i & 7, col = col0 + cc;
-      const bool v = col < Lv;
-      cp_async16(sX + sw128(cc, j),
-                 v ? opsrc + (((int64_t)b * T + t0 + col) * H + hh) * kP + j * 8 : opsrc, v);
-    }
+    mbar_arrive_expect_tx(&bar_xr[wg], (uint32_t)(ncol * 128));
+    ++n_xr;
+    for (int k2 = 0; k2 < ncol / 128; ++k2)
+      tma_load_4d(sX + k2 * 128 * 128, &mOp, 0, hh, (int)t0 + col0 + 128 * k2, b, &bar_xr[wg]);
   };
   auto prefetch = [&](int hh) {
     if constexpr (!kTmaO) prefetch_x(hh);
     const unsigned char* img = simg + ((((int64_t)b * nc + c) * H + hh) * (int64_t)SM::kImg);
-    for (int i = wtid; i < SM::kImg / 16; i += 256) cp_async16(Pw + 16 * i, img + 16 * i, true);
     const int64_t cvh = ((((int64_t)b * H + hh) >> hs) * nc + c) * L;
-    for (int i = wtid; i < L / 4; i += 256) {
-      cp_async16(sraw + 4 * i, acs + cvh + 4 * i, true);
-      cp_async16(sraw + L + 4 * i, delta + cvh + 4 * i, true);
-    }
+    mbar_arrive_expect_tx(&bar_ld[wg], (uint32_t)(SM::kImg + 2 * L * 4));
+    ++n_ld;
+    bulk_g2s(Pw, img, SM::kImg, &bar_ld[wg]);
+    bulk_g2s(sraw, acs + cvh, L * 4, &bar_ld[wg]);
+    bulk_g2s(sraw + L, delta + cvh, L * 4, &bar_ld[wg]);
   };
-  if (h_begin + wg < h_end) prefetch(h_begin + wg);
-  cp_async_commit();
-  if constexpr (kTmaO) {
-    if (h_begin + wg < h_end) prefetch_x(h_begin + wg);
-    cp_async_commit();
+  if (wtid == 0 && h_begin + wg < h_end) {
+    prefetch(h_begin + wg);
+    if constexpr (kTmaO) prefetch_x(h_begin + wg);
   }
 
   for (int h = h_begin + wg; h < h_end; h += 2) {
     const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
     const float Dh = D ? D[h >> hs] : 0.f;
     // the image and vectors (the operand rows may still be in flight)
-    if constexpr (kTmaO) cp_async_wait<1>();
-    else cp_async_wait<0>();
-    group_sync(gbar);  // the raw vectors were copied by other threads of the group
+    const uint32_t hpar = n_heads & 1;
+    ++n_heads;
+    mbar_wait(&bar_ld[wg], hpar, status, &abort_flag);
     for (int i = wtid; i < L; i += 256) {
       const float a2 = sraw[i] * kLog2e, dl = sraw[L + i];
       sa2[i] = a2;
@@ -356,11 +360,11 @@ __global__ void __launch_bounds__(512, 1)
         }
         if (qg == 0) tmem_wait_ld();
       }
-      if (kTmaO && j == 0) cp_async_wait<0>();  // the operand rows
       fence_async_smem();
       fence_before_sync();
       group_sync(gbar);
       if (wtid == 0) {
+        if (j == 0) mbar_wait(&bar_xr[wg], hpar, status, &abort_flag);  // the operand rows
         fence_after_sync();
         const uint64_t dXj = desc_add(dX, 64 * j * 128);
 #pragma unroll
@@ -394,8 +398,7 @@ __global__ void __launch_bounds__(512, 1)
     fence_after_sync();
     // this head's MMAs are done: the P buffer (and, without the TMA epilogue,
     // sX) take the next head's data
-    if (h + 2 < h_end) prefetch(h + 2);
-    cp_async_commit();
+    if (wtid == 0 && h + 2 < h_end) prefetch(h + 2);
     unsigned char* stg = sX + wq * 4096;  // this warp's staging (TMA epilogue)
     if constexpr (kTmaO) {
       // the row of the operand this thread's outputs need, from sX (rows
@@ -489,8 +492,7 @@ __global__ void __launch_bounds__(512, 1)
     fence_before_sync();
     group_sync(gbar);  // sX, sa, sd and the accumulators are reused by the next head
     if constexpr (kTmaO) {
-      if (h + 2 < h_end) prefetch_x(h + 2);
-      cp_async_commit();
+      if (wtid == 0 && h + 2 < h_end) prefetch_x(h + 2);
     }
   }
     // both groups are done with this unit's C.B^T tile and buffers
@@ -498,6 +500,10 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
   }
   if (lane == 0) bulk_wait_all();  // the dx stores have landed
+  if (wtid == 0) {  // copies still in flight (after an expired wait) land before the CTA exits
+    if (n_ld > 0) mbar_drain(&bar_ld[wg], (n_ld - 1) & 1);
+    if (n_xr > 0) mbar_drain(&bar_xr[wg], (n_xr - 1) & 1);
+  }
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tm, 512);
@@ -788,10 +794,12 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
     int grid, per;
     scan_partition(d, sms, &grid, &per);
-    CUtensorMap mDX;
-    if (!make_y_map(&mDX, a.dx, d.H, d.T, d.B, 32)) return cudaErrorInvalidValue;
+    CUtensorMap mDX, mDY;
+    if (!make_y_map(&mDX, a.dx, d.H, d.T, d.B, 32) ||
+        !make_tma_map(&mDY, dy, 64, d.H, d.T, d.B, 1, 128))
+      return cudaErrorInvalidValue;
     SSD_LAUNCH("k_scan_tc_dx", s, launch_pdl(kern, dim3(grid), dim3(512), SM::kBytes, s,
-        mDX, static_cast<const bf16*>(a.f.x), static_cast<const bf16*>(a.f.B), Cm, dy, w.delta, w.acs,
+        mDX, mDY, static_cast<const bf16*>(a.f.x), static_cast<const bf16*>(a.f.B), Cm, dy, w.delta, w.acs,
         static_cast<const unsigned char*>(w.dSimg), a.f.D, a.dx, w.ddir, w.qrow, w.ddiag, d.B, d.T,
         d.H, d.G, d.nc, d.hs, per, status));
   }
