@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(512, 1)
   constexpr int LT = SM::kLT, NLT = L / LT;
   griddep_wait();  // the state images and vectors come from the previous kernels
   extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t bar_cb, bar_p[2], bar_st[2], bar_done[2], bar_ld[2], bar_xr[2];
+  __shared__ uint64_t bar_cb, bar_p[2], bar_st[2], bar_done[2], bar_ld[2], bar_xr[2], bar_stg;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   unsigned char* base = align1024(smem_raw);
@@ -135,6 +135,7 @@ __global__ void __launch_bounds__(512, 1)
   if (tid == 0) {
     abort_flag = 0;
     mbar_init(&bar_cb, 1);
+    mbar_init(&bar_stg, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_p[i], 1);
       mbar_init(&bar_st[i], 1);
@@ -167,6 +168,7 @@ __global__ void __launch_bounds__(512, 1)
   // per pipeline: heads started (all threads), and (thread wtid 0) the copies
   // issued of the image + vectors and of the operand rows
   uint32_t n_heads = 0, n_ld = 0, n_xr = 0;
+  uint32_t n_stg = 0;  // units in which pipeline 0 has released pipeline 1
 
   for (int64_t item = it_begin; item < it_end;) {
     // one unit = (batch, chunk, row tile, group); this CTA's heads of it
@@ -187,6 +189,11 @@ __global__ void __launch_bounds__(512, 1)
     const int64_t t0 = (int64_t)c * L;
     const int Lv = min(L, T - (int)t0);
     const int r = r0 + rr;                          // this thread's row (TMEM lane)
+    // pipeline 1 starts a unit once pipeline 0 has issued its first head's
+    // state products, so the two alternate between forming P and waiting
+    // for the tensor core instead of doing both at the same time
+    const uint32_t stg_par = n_stg & 1;
+    if (h_begin < h_end) ++n_stg;
 
   stage_rows_async(sR, LT, N / 8, LT * 128, Lv - r0, rowsrc, [&](int rr2) {
       return rowsrc + (((int64_t)b * T + t0 + r0 + rr2) * G + g) * N;
@@ -266,6 +273,7 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t hpar = n_heads & 1;
     ++n_heads;
     mbar_wait(&bar_ld[wg], hpar, status, &abort_flag);
+    if (wg == 1 && h == h_begin + 1) mbar_wait(&bar_stg, stg_par, status, &abort_flag);
     for (int i = wtid; i < L; i += 256) {
       const float a2 = sraw[i] * kLog2e, dl = sraw[L + i];
       sa2[i] = a2;
@@ -284,6 +292,7 @@ __global__ void __launch_bounds__(512, 1)
         mma_bf16(tm + colST, ad, desc_add(dP, SM::kHlo + kp * (64 * 128) + ko), id_st, 1u);
       }
       mma_commit(&bar_st[wg]);
+      if (wg == 0 && h == h_begin) mbar_arrive(&bar_stg);
     }
     // Forward: column factors for column groups strictly inside the causal
     // triangle, e^{a_l - a_s} delta_s = R_l * cf_s with the group's last column
