@@ -279,9 +279,14 @@ __global__ void __launch_bounds__(512, 1)
       sa2[i] = a2;
       sx[i] = REV ? dl : (dl > 0.f ? a2 - lg2_approx(dl) : __int_as_float(0x7f800000));
     }
+    // (TMA epilogue) the previous head's dx stores have read their staging
+    // in sX before this head's operand rows are copied over it
+    if (kTmaO && lane == 0) bulk_wait_read<0>();
     fence_async_smem();
     fence_before_sync();
     group_sync(gbar);
+    if constexpr (kTmaO)
+      if (wtid == 0 && h != h_begin + wg) prefetch_x(h);
     if (wtid == 0) {
       fence_after_sync();
 #pragma unroll
@@ -471,17 +476,14 @@ __global__ void __launch_bounds__(512, 1)
       }
       if constexpr (kTmaO) {
         // one store of the warp's 32 rows x 32 columns (rows past seqlen are
-        // clipped by it); its reads of the staging end before sX is refilled
+        // clipped by it); the next head (or unit) waits for its reads of the
+        // staging before sX is refilled
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          if (t0 + r0 + 32 * q < T) {
-            tma_store_4d(&mOut, 32 * half, h, (int)t0 + r0 + 32 * q, b, stg);
-            bulk_commit_group();
-          }
-          bulk_wait_read<0>();
+        if (lane == 0 && t0 + r0 + 32 * q < T) {
+          tma_store_4d(&mOut, 32 * half, h, (int)t0 + r0 + 32 * q, b, stg);
+          bulk_commit_group();
         }
-        __syncwarp();
       }
     }
     if constexpr (REV) {
@@ -500,11 +502,10 @@ __global__ void __launch_bounds__(512, 1)
     }
     fence_before_sync();
     group_sync(gbar);  // sX, sa, sd and the accumulators are reused by the next head
-    if constexpr (kTmaO) {
-      if (wtid == 0 && h + 2 < h_end) prefetch_x(h + 2);
-    }
   }
-    // both groups are done with this unit's C.B^T tile and buffers
+    // both groups are done with this unit's C.B^T tile and buffers (and the
+    // dx stores with their staging, before the next unit's rows come in)
+    if (kTmaO && lane == 0) bulk_wait_read<0>();
     fence_before_sync();
     __syncthreads();
   }
