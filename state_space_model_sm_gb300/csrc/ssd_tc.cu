@@ -719,8 +719,9 @@ __device__ __forceinline__ void param_grads_block(const FinalizeArgs& f) {
   }
 }
 
+// (1536 threads per SM: six 256-thread blocks resident, 40 registers each)
 template <int NT>
-__global__ void __launch_bounds__(NT)
+__global__ void __launch_bounds__(NT, 1536 / NT)
     k_bwd_tail_tc(FinalizeArgs f, int nfin, const float4* __restrict__ dCp,
                   float4* __restrict__ dC, const float4* __restrict__ dBp, float4* __restrict__ dB,
                   int nred, int64_t rows, PartialRows prC, PartialRows prB, int N4) {
