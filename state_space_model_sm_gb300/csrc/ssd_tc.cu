@@ -63,15 +63,10 @@ __device__ __forceinline__ void stage_rows_async(unsigned char* dst, int rows, i
 }
 
 // ================================================================ dx
-// The cp.async scan kernel, in the direction the backward's dx uses (the
-// forward direction runs in ssd_chunk_tc.cu).  One kernel, two directions.
-//   forward (REV = false), rows r = l of chunk c, columns s in [0, l0 + 128):
-//     CB[l, s] = C_l . B_s                       (TMEM cols 0.., once per CTA)
-//     per head: Y  = sum_s P[l, s] x_s,  P = CB e^{a_l - a_s} delta_s [s <= l]
-//               ST = C_l . H_c[p, :]
-//               y_l = Y + e^{a_l} ST + D x_l
-//   backward dx (REV = true), rows r = s, columns l in [s0, L):
-//     CBT[s, l] = B_s . C_l
+// The backward's dx ("Optimizing Mamba-2 kernels for the B200", Stage 1
+// kernel table: _chunk_scan_chunk_state_bwd_dx, bwd_10), rows r = s of chunk
+// c, columns l in [s0, L):
+//     CBT[s, l] = B_s . C_l                      (TMEM cols 0.., once per unit)
 //     per head: Y  = sum_l P[s, l] dy_l,  P = CBT e^{a_l - a_s} [l >= s]
 //               ST = B_s . dS_c[p, :]
 //               u_s = Y + e^{a_last - a_s} ST;  dx_s = delta_s u_s + D dy_s
@@ -79,9 +74,10 @@ __device__ __forceinline__ void stage_rows_async(unsigned char* dst, int rows, i
 //               ddiag_s = <x_s, dy_s>
 // Persistent, one CTA (512 threads) per SM over a balanced range of (batch,
 // chunk, 128-row tile, group) x head items.  Per unit the score tile is
-// formed once; then the two 8-warp pipelines run independent chains on
-// alternate heads (own TMEM accumulators, P buffer, operand rows and
-// mbarriers), so one pipeline's loads and waits overlap the other's work.
+// formed once; then the two 8-warp pipelines run chains on alternate heads
+// (own TMEM accumulators, P buffer, operand rows and mbarriers), the second
+// starting each unit once the first has issued its state products, so one
+// forms P while the other waits for the tensor core.
 template <int N, int L>
 struct ScanSmem {
   static constexpr int kLT = 128;
@@ -89,17 +85,17 @@ struct ScanSmem {
   static constexpr int kBrows = (N / 64) * L * 128;         // column-operand rows
   static constexpr int kPw = 2 * kLT * 128;                 // per group: P panel hi + lo
   static constexpr int kBP = kBrows > 2 * kPw ? kBrows : 2 * kPw;
-  static constexpr int kX = L * 128;                        // per group: x or dy rows
+  static constexpr int kX = L * 128;                        // per group: dy rows
   static constexpr int kHlo = (N / 64) * 64 * 128;          // offset of the state's lo part
   static constexpr int kImg = 2 * kHlo;                     // bytes of one state image
-  static constexpr int kBytes = kC + kBP + 2 * kX + (10 * L + 6 * 128) * 4 + 1024;
+  static constexpr int kBytes = kC + kBP + 2 * kX + (8 * L + 6 * 128) * 4 + 1024;
 };
 
 __device__ __forceinline__ void group_sync(int id) {
   asm volatile("bar.sync %0, 256;" ::"r"(id) : "memory");
 }
 
-template <int N, int L, typename Tout, bool REV>
+template <int N, int L>
 __global__ void __launch_bounds__(512, 1)
     k_scan_tc(const __grid_constant__ CUtensorMap mOut, const __grid_constant__ CUtensorMap mOp,
               const bf16* __restrict__ x,
@@ -107,7 +103,7 @@ __global__ void __launch_bounds__(512, 1)
               const bf16* __restrict__ Cm, const bf16* __restrict__ dy,
               const float* __restrict__ delta, const float* __restrict__ acs,
               const unsigned char* __restrict__ simg, const float* __restrict__ D,
-              Tout* __restrict__ out, float* __restrict__ ddir, float* __restrict__ qrow,
+              float* __restrict__ out, float* __restrict__ ddir, float* __restrict__ qrow,
               float* __restrict__ ddiag, int B_, int T, int H, int G, int nc, int hs,
               int items_per_cta, int* status) {
   using SM = ScanSmem<N, L>;
@@ -128,9 +124,8 @@ __global__ void __launch_bounds__(512, 1)
   const int64_t n_items = (int64_t)B_ * nc * NLT * H;  // (batch, chunk, tile, group) x head
   const int64_t it_begin = (int64_t)blockIdx.x * items_per_cta;
   const int64_t it_end = min(n_items, it_begin + items_per_cta);
-  const bf16* rowsrc = REV ? Bm : Cm;
-  const bf16* colsrc = REV ? Cm : Bm;
-  const bf16* opsrc = REV ? dy : x;
+  const bf16* rowsrc = Bm;
+  const bf16* colsrc = Cm;
 
   if (tid == 0) {
     abort_flag = 0;
@@ -163,7 +158,6 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t colY = 256 + 128 * wg, colST = colY + 64;
   const int gbar = 1 + wg;
   float* sred = sAall + 8 * L + wg * 3 * 128;  // [3][128] per pipeline: half-row partial sums
-  float* scf = sAall + 8 * L + 6 * 128 + wg * L;  // per pipeline: column factors (forward)
   uint32_t n_p = 0, n_st = 0, n_done = 0, n_units = 0;
   // per pipeline: heads started (all threads), and (thread wtid 0) the copies
   // issued of the image + vectors and of the operand rows
@@ -183,8 +177,8 @@ __global__ void __launch_bounds__(512, 1)
     const int c = (int)(bc % nc), b = (int)(bc / nc);
     const int h_begin = g * hpg + j0, h_end = g * hpg + j1;
     const int r0 = tile * LT;                       // first row (chunk-local)
-    const int col0 = REV ? r0 : 0;                  // first column
-    const int ncol = REV ? L - r0 : r0 + LT;        // number of columns
+    const int col0 = r0;                            // first column
+    const int ncol = L - r0;                        // number of columns
     const int nsp = ncol / 64;
     const int64_t t0 = (int64_t)c * L;
     const int Lv = min(L, T - (int)t0);
@@ -239,7 +233,7 @@ __global__ void __launch_bounds__(512, 1)
   // every warp's 32 x 32 block (4 KB each, 128-byte swizzle): each head's
   // epilogue reads its own x / dy row from sX first, then the block is staged
   // there and stored, and only then do the next head's rows come in
-  constexpr bool kTmaO = sizeof(Tout) == 4 && SM::kX >= 8 * 4096;
+  constexpr bool kTmaO = SM::kX >= 8 * 4096;
   // What a head needs, copied by thread wtid 0 of its pipeline: its
   // inter-chunk state image (into the P buffer) and raw a / delta with bulk
   // copies on bar_ld, and its second-operand rows (sX, 128-byte swizzle; rows
@@ -277,7 +271,7 @@ __global__ void __launch_bounds__(512, 1)
     for (int i = wtid; i < L; i += 256) {
       const float a2 = sraw[i] * kLog2e, dl = sraw[L + i];
       sa2[i] = a2;
-      sx[i] = REV ? dl : (dl > 0.f ? a2 - lg2_approx(dl) : __int_as_float(0x7f800000));
+      sx[i] = dl;
     }
     // (TMA epilogue) the previous head's dx stores have read their staging
     // in sX before this head's operand rows are copied over it
@@ -299,22 +293,13 @@ __global__ void __launch_bounds__(512, 1)
       mma_commit(&bar_st[wg]);
       if (wg == 0 && h == h_begin) mbar_arrive(&bar_stg);
     }
-    // Forward: column factors for column groups strictly inside the causal
-    // triangle, e^{a_l - a_s} delta_s = R_l * cf_s with the group's last column
-    // m as reference: cf_s = 2^{a_m - a_s} delta_s, R_l = 2^{a_l - a_m}; a is
-    // monotone, so both are <= 1.  (The dx direction keeps the per-element
-    // exponential: measured faster there.)
-    if constexpr (!REV) {
-      for (int i = wtid; i < L; i += 256) scf[i] = ex2_approx(sa2[i | 15] - sx[i]);
-      group_sync(gbar);
-    }
     ++n_st;
     mbar_wait(&bar_st[wg], (n_st - 1) & 1, status, &abort_flag);  // P buffer free again
     fence_after_sync();
     const float ar2 = sa2[r];
     for (int j = 0; j < nsp; ++j) {
       if (j > 0) mbar_wait(&bar_p[wg], (n_p - 1) & 1, status, &abort_flag);
-      const float* colv = (REV ? sa2 : sx) + col0 + 64 * j;  // per-column log2 terms
+      const float* colv = sa2 + col0 + 64 * j;  // per-column a log2(e)
       // the thread's 32 columns as two 16-column groups; the second group's
       // TMEM load is in flight while the first is formed
       float cbA[16], cbB[16];
@@ -324,53 +309,21 @@ __global__ void __launch_bounds__(512, 1)
       for (int qg = 0; qg < 2; ++qg) {
         float(&cur)[16] = qg ? cbB : cbA;
         if (qg == 0) tmem_ld16(tlane + 64 * j + 32 * half + 16, cbB);
-        // the warp's 32 rows [rw, rw + 32) against 16 columns [cg, cg + 16):
-        // outside the causal triangle, strictly inside it, or across the diagonal
-        const int cg = col0 + 64 * j + 32 * half + 16 * qg, rw = r0 + 32 * q;
-        const bool outside = !REV && cg > rw + 31;
-        const bool inside = !REV && cg + 15 < rw;
-        if (outside) {
+        // P[s, l] = CBT e^{a_l - a_s} for l >= s (one exponential per element)
 #pragma unroll
-          for (int k8 = 0; k8 < 2; ++k8) {
-            const uint32_t off = sw128(rr, (32 * half + 16 * qg + 8 * k8) / 8);
-            *reinterpret_cast<uint4*>(Pw + off) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(Pw + LT * 128 + off) = make_uint4(0, 0, 0, 0);
+        for (int k8 = 0; k8 < 2; ++k8) {
+          const int c8 = 32 * half + 16 * qg + 8 * k8;  // panel-local column of the chunk
+          const float4 w0 = *reinterpret_cast<const float4*>(colv + c8);
+          const float4 w1 = *reinterpret_cast<const float4*>(colv + c8 + 4);
+          const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int cl = col0 + 64 * j + c8 + e;  // chunk-local column
+            v[e] = cl >= r ? cur[8 * k8 + e] * ex2_approx(wv[e] - ar2) : 0.f;
           }
-        } else if (inside) {
-          const int m = cg + 15;
-          const float R = ex2_approx(ar2 - sa2[m]);
-          const float2 R2 = make_float2(R, R);
-#pragma unroll
-          for (int k8 = 0; k8 < 2; ++k8) {
-            const int c8 = 32 * half + 16 * qg + 8 * k8;  // panel-local column of the chunk
-            const float4 c0 = *reinterpret_cast<const float4*>(scf + cg + 8 * k8);
-            const float4 c1 = *reinterpret_cast<const float4*>(scf + cg + 8 * k8 + 4);
-            const float* sv = cur + 8 * k8;
-            const float2 p0 = __fmul2_rn(__fmul2_rn(R2, make_float2(c0.x, c0.y)), make_float2(sv[0], sv[1]));
-            const float2 p1 = __fmul2_rn(__fmul2_rn(R2, make_float2(c0.z, c0.w)), make_float2(sv[2], sv[3]));
-            const float2 p2 = __fmul2_rn(__fmul2_rn(R2, make_float2(c1.x, c1.y)), make_float2(sv[4], sv[5]));
-            const float2 p3 = __fmul2_rn(__fmul2_rn(R2, make_float2(c1.z, c1.w)), make_float2(sv[6], sv[7]));
-            const float v[8] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y, p3.x, p3.y};
-            const uint32_t off = sw128(rr, c8 / 8);
-            store_split8(Pw + off, Pw + LT * 128 + off, v);
-          }
-        } else {
-#pragma unroll
-          for (int k8 = 0; k8 < 2; ++k8) {
-            const int c8 = 32 * half + 16 * qg + 8 * k8;  // panel-local column of the chunk
-            const float4 w0 = *reinterpret_cast<const float4*>(colv + c8);
-            const float4 w1 = *reinterpret_cast<const float4*>(colv + c8 + 4);
-            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            float v[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int cl = col0 + 64 * j + c8 + e;  // chunk-local column
-              const float f = REV ? ex2_approx(wv[e] - ar2) : ex2_approx(ar2 - wv[e]);
-              v[e] = (REV ? cl >= r : cl <= r) ? cur[8 * k8 + e] * f : 0.f;
-            }
-            const uint32_t off = sw128(rr, c8 / 8);
-            store_split8(Pw + off, Pw + LT * 128 + off, v);
-          }
+          const uint32_t off = sw128(rr, c8 / 8);
+          store_split8(Pw + off, Pw + LT * 128 + off, v);
         }
         if (qg == 0) tmem_wait_ld();
       }
@@ -392,19 +345,18 @@ __global__ void __launch_bounds__(512, 1)
       }
       ++n_p;
     }
-    // this thread's 32 columns of its row of the second operand (x or dy) and,
-    // rev, of x: loaded now, so the latency overlaps the last MMAs
+    // this thread's 32 columns of its row of dy (without the TMA epilogue)
+    // and of x: loaded now, so the latency overlaps the last MMAs
     const int64_t rowoff = (((int64_t)b * T + t0 + r) * H + h) * kP;
     const bool live = r < Lv;
     uint4 orow[4], xrow[4];
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       if constexpr (!kTmaO)
-        orow[kk] = live ? *reinterpret_cast<const uint4*>(opsrc + rowoff + 32 * half + 8 * kk)
+        orow[kk] = live ? *reinterpret_cast<const uint4*>(dy + rowoff + 32 * half + 8 * kk)
                         : make_uint4(0, 0, 0, 0);
-      if constexpr (REV)
-        xrow[kk] = live ? *reinterpret_cast<const uint4*>(x + rowoff + 32 * half + 8 * kk)
-                        : make_uint4(0, 0, 0, 0);
+      xrow[kk] = live ? *reinterpret_cast<const uint4*>(x + rowoff + 32 * half + 8 * kk)
+                      : make_uint4(0, 0, 0, 0);
     }
     ++n_done;
     const bool ok =
@@ -422,10 +374,10 @@ __global__ void __launch_bounds__(512, 1)
         orow[kk] = *reinterpret_cast<const uint4*>(sX + sw128(r - col0, 4 * half + kk));
       group_sync(gbar);
     }
-    float pd = 0.f, pq = 0.f, pdd = 0.f;  // rev: partial <x, u>, <x, state part>, <x, dy>
+    float pd = 0.f, pq = 0.f, pdd = 0.f;  // partial <x, u>, <x, state part>, <x, dy>
     if (ok) {
-      const float ea = ex2_approx(ar2), es = ex2_approx(sa2[L - 1] - ar2);
-      const float dr = REV ? sx[r] : 0.f;
+      const float es = ex2_approx(sa2[L - 1] - ar2);
+      const float dr = sx[r];
 #pragma unroll
       for (int c16 = 0; c16 < 2; ++c16) {
         float yv[16], st[16];
@@ -437,22 +389,16 @@ __global__ void __launch_bounds__(512, 1)
           for (int k8 = 0; k8 < 2; ++k8) {
             float ov[8], o[8];
             unpack8(orow[2 * c16 + k8], ov);
-            if constexpr (!REV) {
+            float xv[8];
+            unpack8(xrow[2 * c16 + k8], xv);
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                o[e] = yv[8 * k8 + e] + ea * st[8 * k8 + e] + Dh * ov[e];
-            } else {
-              float xv[8];
-              unpack8(xrow[2 * c16 + k8], xv);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float us = es * st[8 * k8 + e];
-                const float u = yv[8 * k8 + e] + us;
-                o[e] = fmaf(dr, u, Dh * ov[e]);
-                pd = fmaf(xv[e], u, pd);
-                pq = fmaf(xv[e], us, pq);
-                pdd = fmaf(xv[e], ov[e], pdd);
-              }
+            for (int e = 0; e < 8; ++e) {
+              const float us = es * st[8 * k8 + e];
+              const float u = yv[8 * k8 + e] + us;
+              o[e] = fmaf(dr, u, Dh * ov[e]);
+              pd = fmaf(xv[e], u, pd);
+              pq = fmaf(xv[e], us, pq);
+              pdd = fmaf(xv[e], ov[e], pdd);
             }
             if constexpr (kTmaO) {
               const int j = 4 * c16 + 2 * k8;  // 16-byte chunks j, j + 1 of the 128-byte row
@@ -460,16 +406,9 @@ __global__ void __launch_bounds__(512, 1)
               *reinterpret_cast<float4*>(stg + sw128(lane, j + 1)) =
                   make_float4(o[4], o[5], o[6], o[7]);
             } else {
-              Tout* op = out + rowoff + 32 * half + 16 * c16 + 8 * k8;
-              if constexpr (sizeof(Tout) == 4) {
-                float* of = reinterpret_cast<float*>(op);
-                *reinterpret_cast<float4*>(of) = make_float4(o[0], o[1], o[2], o[3]);
-                *reinterpret_cast<float4*>(of + 4) = make_float4(o[4], o[5], o[6], o[7]);
-              } else {
-                *reinterpret_cast<uint4*>(op) =
-                    make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
-                               pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
-              }
+              float* of = out + rowoff + 32 * half + 16 * c16 + 8 * k8;
+              *reinterpret_cast<float4*>(of) = make_float4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<float4*>(of + 4) = make_float4(o[4], o[5], o[6], o[7]);
             }
           }
         }
@@ -486,19 +425,17 @@ __global__ void __launch_bounds__(512, 1)
         }
       }
     }
-    if constexpr (REV) {
-      // combine the two half-rows (pipeline-local barrier)
-      if (half == 1) {
-        sred[rr] = pd;
-        sred[128 + rr] = pq;
-        sred[256 + rr] = pdd;
-      }
-      group_sync(gbar);
-      if (half == 0 && r < Lv) {
-        ddir[cv + r] = pd + sred[rr];
-        qrow[cv + r] = sx[r] * (pq + sred[128 + rr]);
-        ddiag[cv + r] = pdd + sred[256 + rr];
-      }
+    // combine the two half-rows (pipeline-local barrier)
+    if (half == 1) {
+      sred[rr] = pd;
+      sred[128 + rr] = pq;
+      sred[256 + rr] = pdd;
+    }
+    group_sync(gbar);
+    if (half == 0 && r < Lv) {
+      ddir[cv + r] = pd + sred[rr];
+      qrow[cv + r] = sx[r] * (pq + sred[128 + rr]);
+      ddiag[cv + r] = pdd + sred[256 + rr];
     }
     fence_before_sync();
     group_sync(gbar);  // sX, sa, sd and the accumulators are reused by the next head
@@ -801,7 +738,7 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
                                             a.dinit, w.dSimg, w.Himg, w.seg, s);
   {
     using SM = ScanSmem<N, L>;
-    auto kern = k_scan_tc<N, L, float, true>;
+    auto kern = k_scan_tc<N, L>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
     int grid, per;
     scan_partition(d, sms, &grid, &per);
