@@ -192,12 +192,13 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   const int h_begin = g * (H / a.G) + kb * hb;
   const int r0 = tile * LT, col0 = REV ? r0 : 0, ncol = REV ? L - r0 : r0 + LT;
   const int npan = ncol / 64;
-  // chunk_scan on a tile of 128 columns: TMEM has room beside its C.B^T for
-  // a separate state accumulator per head parity (columns 128 + 64 st), so
-  // the state term C.H_c^T is one product of the tile's C rows (shared
-  // memory) with the image, scaled by e^{a_l} in the epilogue, instead of
-  // converted, scaled C panels
-  const bool st_direct = MODE == kFwd && ncol <= 128;
+  // chunk_scan: the state term C.H_c^T is one product of the tile's C rows
+  // (shared memory) with the state image into its own accumulator ST,
+  // scaled by e^{a_l} in the epilogue.  A tile of 128 columns leaves TMEM room
+  // for Y and ST per head parity (Y at 384 + 64 st, ST at 128 + 64 st); a
+  // tile of 256 holds one of each (Y at 384, ST at 448), so a head's first
+  // product waits for the previous head's epilogue.
+  const bool acc2 = ncol <= 128;
   const int t0 = c * L;
   const int Lv = min(L, T - t0);
   int* status = a.status;
@@ -232,10 +233,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   // that need nothing from it
   griddep_launch_dependents();
   const uint32_t tm = tmem_base;
-  // slot uses per head: FWD the P panels, then the state term's K panels;
-  // DC the S1 panels, the state term's A operand and the state dot C.H_c^T; DB
-  // the S1 panels and the state term's A operand
-  const int upH = S1M ? npan + (MODE == kDc ? 2 : 1) : npan + NP;
+  // slot uses per head: FWD the P panels; DC the S1 panels, the state term's
+  // A operand and the state dot C.H_c^T; DB the S1 panels and the state term's
+  // A operand
 
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer
@@ -337,61 +337,40 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
       constexpr uint32_t id_n64k = idesc_bf16(128, 64, 0, 0);   // B K-major, N = 64
       constexpr uint32_t id_n64m = idesc_bf16(128, 64, 0, 1);   // B MN-major, N = 64
       constexpr uint32_t id_nNm = idesc_bf16(128, N, 0, 1);     // B MN-major, N = d_state
-      // the state term's K panel kp with A in slot sc: B = image K-major (rows
-      // p), hi and lo parts, three products per K step (hi.hi, hi.lo, lo.hi)
-      auto state_panel = [&](uint32_t dcol, uint32_t sc, int kp) {
-        const uint64_t bk = desc_add(dImgK, kp * (64 * 128));
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bh = desc_add(bk, ks * 32), bl = desc_add(bk, LY::kHlo + ks * 32);
-          mma_bf16_ta(tm + dcol, sc + 16 * ks, bh, id_n64k, 1u);
-          mma_bf16_ta(tm + dcol, sc + 16 * ks, bl, id_n64k, 1u);
-          mma_bf16_ta(tm + dcol, sc + 16 * ks + 8, bh, id_n64k, 1u);
-        }
-      };
       if constexpr (!S1M) {
         uint32_t u = 0;  // slot uses
-        const int upHt = st_direct ? npan : upH;
         for (int i = 0; ok && i < hb; ++i) {
           const int st = i & 1;
-          // Y per head parity (the state panels add into it)
-          const uint32_t colY = kColAcc + 64 * st;
-          const int ab = st;
-          const int na = i >> 1;  // earlier uses of this accumulator
+          const int ab = acc2 ? st : 0;             // the accumulator pair of this head
+          const int na = acc2 ? (i >> 1) : i;       // earlier uses of that pair
+          const uint32_t colY = kColAcc + (acc2 ? 64 * st : 0);
+          const uint32_t colS = acc2 ? 128 + 64 * st : kColAcc + 64;
           ok = mbar_wait(&bar_ops_full[st], (i >> 1) & 1, status, &abort_flag);
           if (ok && na >= 1)
             ok = mbar_wait(&bar_acc_empty[ab], (na - 1) & 1, status, &abort_flag);
           if (!ok) break;
           const uint64_t dops = desc_add(dOpsMN, st * LY::kOps);
-          for (int k = 0; k < upHt; ++k, ++u) {
+          for (int k = 0; k < npan; ++k, ++u) {
             const int s = u & 1;
-            // the state image is needed from the first state panel on
-            if (k == npan && !mbar_wait(&bar_img_full, i & 1, status, &abort_flag)) {
-              ok = false;
-              break;
-            }
             if (!mbar_wait(&bar_slot_full[s], (u >> 1) & 1, status, &abort_flag)) {
               ok = false;
               break;
             }
             fence_after_sync();
             const uint32_t sc = tm + kColSlot + 64 * s;
-            if (k < npan) {
-              const uint64_t bp = desc_add(dops, k * 64 * 128);
-              const uint32_t acc0 = k > 0 ? 1u : 0u;
+            const uint64_t bp = desc_add(dops, k * 64 * 128);
+            const uint32_t acc0 = k > 0 ? 1u : 0u;
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t bd = desc_add(bp, ks * 16 * 128);
-                mma_bf16_ta(tm + colY, sc + 16 * ks, bd, id_n64m, ks > 0 ? 1u : acc0);
-                mma_bf16_ta(tm + colY, sc + 16 * ks + 8, bd, id_n64m, 1u);
-              }
-              if (k == npan - 1) mma_commit(&bar_ops_empty[st]);  // x / dy rows read
-            } else {
-              state_panel(colY, sc, k - npan);
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t bd = desc_add(bp, ks * 16 * 128);
+              mma_bf16_ta(tm + colY, sc + 16 * ks, bd, id_n64m, ks > 0 ? 1u : acc0);
+              mma_bf16_ta(tm + colY, sc + 16 * ks + 8, bd, id_n64m, 1u);
             }
+            if (k == npan - 1) mma_commit(&bar_ops_empty[st]);  // x rows read
             mma_commit(&bar_slot_ready[s]);  // the slot may be written again
           }
-          if (ok && st_direct) {
+          // the state term: ST = C . H_c^T (hi and lo parts of the image)
+          if (ok) {
             ok = mbar_wait(&bar_img_full, i & 1, status, &abort_flag);
             fence_after_sync();
             if (ok) {
@@ -400,8 +379,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 const uint32_t oa = (ks / 4) * (LT * 128) + (ks % 4) * 32;
                 const uint32_t ob = (ks / 4) * (64 * 128) + (ks % 4) * 32;
                 const uint64_t ad = desc_add(dRowK, oa);
-                mma_bf16(tm + 128 + 64 * st, ad, desc_add(dImgK, ob), id_n64k, ks > 0 ? 1u : 0u);
-                mma_bf16(tm + 128 + 64 * st, ad, desc_add(dImgK, LY::kHlo + ob), id_n64k, 1u);
+                mma_bf16(tm + colS, ad, desc_add(dImgK, ob), id_n64k, ks > 0 ? 1u : 0u);
+                mma_bf16(tm + colS, ad, desc_add(dImgK, LY::kHlo + ob), id_n64k, 1u);
               }
             }
           }
@@ -667,59 +646,38 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
       slot_release(true);
     };
 
-    // a state-term K panel (chunk_scan): 64 of the d_state columns of the
-    // row's C scaled by e^{a_l}
-    auto state_panel = [&](int i, int kp) {
-      const float* da2 = der(i);
-      const float sc_r = ex2_approx(da2[r]);
-      const uint32_t sc = slot_acquire();
-#pragma unroll
-      for (int qg = 0; qg < kNG; ++qg) {
-        const int co = kPC * cq + 16 * qg;  // column within the panel
-        float vv[16];
-#pragma unroll
-        for (int k8 = 0; k8 < 2; ++k8) {
-          float v8[8];
-          unpack8(*reinterpret_cast<const uint4*>(sRow + kp * (LT * 128) +
-                                                  sw128(rr, co / 8 + k8)), v8);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) vv[8 * k8 + e] = v8[e] * sc_r;
-        }
-        tmem_store_split16(sc + co, vv);
-      }
-      slot_release(true);
-    };
-
     if constexpr (!S1M) {
-      // chunk_scan: a head's epilogue runs after the next head's second panel,
-      // so its last products finish while those panels are converted
+      // chunk_scan: a head's epilogue runs once the next head's first panel
+      // (both of its first two, where Y and ST are double-buffered) is handed
+      // over, so the MMA warp has work meanwhile
       int n_ostores = 0;  // TMA stores this warp has issued
       auto epilogue = [&](int i) {
         const int st = i & 1, h = h_begin + i;
-        const int na = i >> 1;
+        const int ab = acc2 ? st : 0, na = acc2 ? (i >> 1) : i;
         const float* da2 = der(i);
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full[st], na & 1, status, &abort_flag)) &&
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full[ab], na & 1, status, &abort_flag)) &&
              ok;
         ok = __all_sync(0xffffffffu, mbar_wait(&bar_ops_full[st], (i >> 1) & 1, status,
                                                &abort_flag)) && ok;
         fence_after_sync();
         float yv[kNG][16], sv[kNG][16];
-        const uint32_t colY = kColAcc + 64 * st;
+        const uint32_t colY = kColAcc + (acc2 ? 64 * st : 0);
+        const uint32_t colS = acc2 ? 128 + 64 * st : kColAcc + 64;
         if (ok) {
 #pragma unroll
           for (int g2 = 0; g2 < kNG; ++g2) {
             tmem_ld16(tl + colY + kPC * cq + 16 * g2, yv[g2]);
-            if (st_direct) tmem_ld16(tl + 128 + 64 * st + kPC * cq + 16 * g2, sv[g2]);
+            tmem_ld16(tl + colS + kPC * cq + 16 * g2, sv[g2]);
           }
           tmem_wait_ld();
         }
         fence_before_sync();
-        warp_arrive(&bar_acc_empty[st], lane);
+        warp_arrive(&bar_acc_empty[ab], lane);
         // this thread's row of the stage's x rows
         const unsigned char* orow = sOps + st * LY::kOps;
         const int orr = r - col0;
         const float Dh = a.D ? a.D[h >> a.hs] : 0.f;
-        const float ea = st_direct ? ex2_approx(da2[r]) : 0.f;  // e^{a_l}
+        const float ea = ex2_approx(da2[r]);  // e^{a_l}
         // fp32 y leaves through TMA: this warp's 32 x 16 block goes to its
         // staging slot, then one store (rows past seqlen are clipped by it);
         // bf16 y is written directly
@@ -736,14 +694,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             float ov[8], o[8];
             unpack8(*reinterpret_cast<const uint4*>(orow + sw128(orr, kCPT * cq + k8)), ov);
             const float* yk = yv[k8 >> 1] + 8 * (k8 & 1);
-            if (st_direct) {
-              const float* sk = sv[k8 >> 1] + 8 * (k8 & 1);
+            const float* sk = sv[k8 >> 1] + 8 * (k8 & 1);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) o[e] = fmaf(Dh, ov[e], fmaf(ea, sk[e], yk[e]));
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) o[e] = fmaf(Dh, ov[e], yk[e]);
-            }
+            for (int e = 0; e < 8; ++e) o[e] = fmaf(Dh, ov[e], fmaf(ea, sk[e], yk[e]));
             if constexpr (kTmaO) {
 #pragma unroll
               for (int j2 = 0; j2 < 2; ++j2) {
@@ -774,13 +727,11 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         derive(i);
         // the previous head's epilogue runs once two of this head's panels are
         // handed over, so the MMA warp has both to work on meanwhile
-        const int jepi = npan > 1 ? 1 : 0;
+        const int jepi = acc2 && npan > 1 ? 1 : 0;
         for (int j = 0; j < npan; ++j) {
           panel(i, j);
           if (j == jepi && i > 0) epilogue(i - 1);
         }
-        if (!st_direct)
-          for (int kp = 0; kp < NP; ++kp) state_panel(i, kp);
       }
       if (hb > 0) epilogue(hb - 1);
       if (lane == 0) bulk_wait_all();  // the y stores have read the staging and landed
