@@ -19,7 +19,7 @@
 // element, so no per-head accumulator is needed for them.
 //
 // Warp roles (576 threads): warps 0-15 convert (TMEM -> decay, mask, hi/lo
-// bf16 split -> shared memory, and the epilogues), warp 16 issues every
+// bf16 split -> a TMEM operand slot, and the epilogues), warp 16 issues every
 // tcgen05.mma, warp 17 issues every copy (TMA tiles of x, dy, B, C through
 // tensor maps; bulk copies of the state images and the per-head a / delta
 // vectors).  Full / empty mbarriers hand each buffer over; every wait is
