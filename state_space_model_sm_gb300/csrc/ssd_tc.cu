@@ -86,9 +86,14 @@ struct ScanSmem {
   static constexpr int kPw = 2 * kLT * 128;                 // per group: P panel hi + lo
   static constexpr int kBP = kBrows > 2 * kPw ? kBrows : 2 * kPw;
   static constexpr int kX = L * 128;                        // per group: dy rows
+  // fp32 out leaves through TMA stores when the operand-row buffer can stage
+  // every warp's 32 x 32 block (4 KB each, 128-byte swizzle)
+  static constexpr bool kTmaO = kX >= 8 * 4096;
+  // without them the tile's x rows come by TMA too (per group)
+  static constexpr int kXr = kTmaO ? 0 : kLT * 128;
   static constexpr int kHlo = (N / 64) * 64 * 128;          // offset of the state's lo part
   static constexpr int kImg = 2 * kHlo;                     // bytes of one state image
-  static constexpr int kBytes = kC + kBP + 2 * kX + (8 * L + 6 * 128) * 4 + 1024;
+  static constexpr int kBytes = kC + kBP + 2 * kX + 2 * kXr + (8 * L + 6 * 128) * 4 + 1024;
 };
 
 __device__ __forceinline__ void group_sync(int id) {
@@ -98,9 +103,9 @@ __device__ __forceinline__ void group_sync(int id) {
 template <int N, int L>
 __global__ void __launch_bounds__(512, 1)
     k_scan_tc(const __grid_constant__ CUtensorMap mOut, const __grid_constant__ CUtensorMap mOp,
-              const bf16* __restrict__ x,
+              const __grid_constant__ CUtensorMap mX, const bf16* __restrict__ x,
               const bf16* __restrict__ Bm,
-              const bf16* __restrict__ Cm, const bf16* __restrict__ dy,
+              const bf16* __restrict__ Cm,
               const float* __restrict__ delta, const float* __restrict__ acs,
               const unsigned char* __restrict__ simg, const float* __restrict__ D,
               float* __restrict__ out, float* __restrict__ ddir, float* __restrict__ qrow,
@@ -110,14 +115,16 @@ __global__ void __launch_bounds__(512, 1)
   constexpr int LT = SM::kLT, NLT = L / LT;
   griddep_wait();  // the state images and vectors come from the previous kernels
   extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t bar_cb, bar_p[2], bar_st[2], bar_done[2], bar_ld[2], bar_xr[2], bar_stg;
+  __shared__ uint64_t bar_cb, bar_p[2], bar_st[2], bar_done[2], bar_ld[2], bar_xr[2], bar_xx[2],
+      bar_stg;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   unsigned char* base = align1024(smem_raw);
-  unsigned char* sR = base;               // row operand: C (fwd) or B (rev) rows of the tile
+  unsigned char* sR = base;               // row operand: B rows of the tile
   unsigned char* sBP = sR + SM::kC;       // column operand rows, later the groups' P buffers
-  unsigned char* sXall = sBP + SM::kBP;   // per group: x (fwd) or dy (rev) rows
-  float* sAall = reinterpret_cast<float*>(sXall + 2 * SM::kX);  // per group: a [L], delta [L]
+  unsigned char* sXall = sBP + SM::kBP;   // per group: dy rows
+  unsigned char* sXrall = sXall + 2 * SM::kX;  // per group: x rows of the tile
+  float* sAall = reinterpret_cast<float*>(sXrall + 2 * SM::kXr);  // per group: a [L], delta [L]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hpg = H / G;
@@ -137,6 +144,7 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&bar_done[i], 1);
       mbar_init(&bar_ld[i], 1);
       mbar_init(&bar_xr[i], 1);
+      mbar_init(&bar_xx[i], 1);
     }
     fence_mbar_init();
   }
@@ -161,7 +169,7 @@ __global__ void __launch_bounds__(512, 1)
   uint32_t n_p = 0, n_st = 0, n_done = 0, n_units = 0;
   // per pipeline: heads started (all threads), and (thread wtid 0) the copies
   // issued of the image + vectors and of the operand rows
-  uint32_t n_heads = 0, n_ld = 0, n_xr = 0;
+  uint32_t n_heads = 0, n_ld = 0, n_xr = 0, n_xx = 0;
   uint32_t n_stg = 0;  // units in which pipeline 0 has released pipeline 1
 
   for (int64_t item = it_begin; item < it_end;) {
@@ -218,8 +226,9 @@ __global__ void __launch_bounds__(512, 1)
 
   unsigned char* Pw = sBP + wg * SM::kPw;
   unsigned char* sX = sXall + wg * SM::kX;
+  unsigned char* sXr = sXrall + wg * SM::kXr;
   float* sa2 = sAall + wg * 4 * L;  // a * log2(e)
-  float* sx = sa2 + L;              // fwd: a*log2e - log2(delta)  (+inf where delta = 0); rev: delta
+  float* sx = sa2 + L;              // delta
   float* sraw = sx + L;             // prefetched a [L], delta [L] of the next head
   constexpr uint32_t id_py = idesc_bf16(128, kP, 0, 1);
   constexpr uint32_t id_st = idesc_bf16(128, kP, 0, 0);
@@ -227,26 +236,33 @@ __global__ void __launch_bounds__(512, 1)
   // issuing thread shares its scheduler with the group's other warps)
   const uint64_t dR = sdesc(smem_u32(sR), 16, 1024);        // row operand, K-major
   const uint64_t dP = sdesc(smem_u32(Pw), 16, 1024);        // P panel / state image, K-major
-  const uint64_t dX = sdesc(smem_u32(sX), L * 128, 1024);   // x / dy rows, MN-major
+  const uint64_t dX = sdesc(smem_u32(sX), L * 128, 1024);   // dy rows, MN-major
 
-  // fp32 out leaves through TMA stores when the operand-row buffer can stage
-  // every warp's 32 x 32 block (4 KB each, 128-byte swizzle): each head's
-  // epilogue reads its own x / dy row from sX first, then the block is staged
-  // there and stored, and only then do the next head's rows come in
-  constexpr bool kTmaO = SM::kX >= 8 * 4096;
+  // Each head's epilogue reads its own dy row from sX; with TMA stores of dx
+  // the block is then staged there and stored.  Only after that do the next
+  // head's rows come in.
+  constexpr bool kTmaO = SM::kTmaO;
   // What a head needs, copied by thread wtid 0 of its pipeline: its
   // inter-chunk state image (into the P buffer) and raw a / delta with bulk
-  // copies on bar_ld, and its second-operand rows (sX, 128-byte swizzle; rows
-  // past seqlen read as zeros) with TMA on bar_xr, which the first P product
-  // waits for.
+  // copies on bar_ld, issued once the previous head's products are done; its
+  // second-operand rows (sX, 128-byte swizzle; rows past seqlen read as
+  // zeros) with TMA on bar_xr, issued at the head's start, which the first P
+  // product waits for.
   auto prefetch_x = [&](int hh) {
     mbar_arrive_expect_tx(&bar_xr[wg], (uint32_t)(ncol * 128));
     ++n_xr;
     for (int k2 = 0; k2 < ncol / 128; ++k2)
       tma_load_4d(sX + k2 * 128 * 128, &mOp, 0, hh, (int)t0 + col0 + 128 * k2, b, &bar_xr[wg]);
   };
+  // (without the TMA epilogue) the tile's rows of x, which only the epilogue
+  // reads: on bar_xx, issued once the previous head's epilogue is over (rows
+  // past seqlen read as zeros)
+  auto prefetch_xr = [&](int hh) {
+    mbar_arrive_expect_tx(&bar_xx[wg], (uint32_t)(LT * 128));
+    ++n_xx;
+    tma_load_4d(sXr, &mX, 0, hh, (int)t0 + r0, b, &bar_xx[wg]);
+  };
   auto prefetch = [&](int hh) {
-    if constexpr (!kTmaO) prefetch_x(hh);
     const unsigned char* img = simg + ((((int64_t)b * nc + c) * H + hh) * (int64_t)SM::kImg);
     const int64_t cvh = ((((int64_t)b * H + hh) >> hs) * nc + c) * L;
     mbar_arrive_expect_tx(&bar_ld[wg], (uint32_t)(SM::kImg + 2 * L * 4));
@@ -257,7 +273,8 @@ __global__ void __launch_bounds__(512, 1)
   };
   if (wtid == 0 && h_begin + wg < h_end) {
     prefetch(h_begin + wg);
-    if constexpr (kTmaO) prefetch_x(h_begin + wg);
+    prefetch_x(h_begin + wg);
+    if constexpr (!kTmaO) prefetch_xr(h_begin + wg);
   }
 
   for (int h = h_begin + wg; h < h_end; h += 2) {
@@ -279,8 +296,10 @@ __global__ void __launch_bounds__(512, 1)
     fence_async_smem();
     fence_before_sync();
     group_sync(gbar);
-    if constexpr (kTmaO)
-      if (wtid == 0 && h != h_begin + wg) prefetch_x(h);
+    if (wtid == 0 && h != h_begin + wg) {
+      prefetch_x(h);
+      if constexpr (!kTmaO) prefetch_xr(h);
+    }
     if (wtid == 0) {
       fence_after_sync();
 #pragma unroll
@@ -345,34 +364,38 @@ __global__ void __launch_bounds__(512, 1)
       }
       ++n_p;
     }
-    // this thread's 32 columns of its row of dy (without the TMA epilogue)
-    // and of x: loaded now, so the latency overlaps the last MMAs
+    // (with the TMA epilogue) this thread's 32 columns of its row of x:
+    // loaded now, so the latency overlaps the last MMAs
     const int64_t rowoff = (((int64_t)b * T + t0 + r) * H + h) * kP;
     const bool live = r < Lv;
     uint4 orow[4], xrow[4];
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-      if constexpr (!kTmaO)
-        orow[kk] = live ? *reinterpret_cast<const uint4*>(dy + rowoff + 32 * half + 8 * kk)
+      if constexpr (kTmaO)
+        xrow[kk] = live ? *reinterpret_cast<const uint4*>(x + rowoff + 32 * half + 8 * kk)
                         : make_uint4(0, 0, 0, 0);
-      xrow[kk] = live ? *reinterpret_cast<const uint4*>(x + rowoff + 32 * half + 8 * kk)
-                      : make_uint4(0, 0, 0, 0);
     }
     ++n_done;
-    const bool ok =
-        __all_sync(0xffffffffu, mbar_wait(&bar_done[wg], (n_done - 1) & 1, status, &abort_flag));
+    const bool ok = __all_sync(
+        0xffffffffu, mbar_wait(&bar_done[wg], (n_done - 1) & 1, status, &abort_flag) &&
+                         (kTmaO || mbar_wait(&bar_xx[wg], hpar, status, &abort_flag)));
     fence_after_sync();
-    // this head's MMAs are done: the P buffer (and, without the TMA epilogue,
-    // sX) take the next head's data
+    if constexpr (!kTmaO) {
+      // the row of x, from the tile's x rows
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        xrow[kk] = *reinterpret_cast<const uint4*>(sXr + sw128(rr, 4 * half + kk));
+    }
+    // this head's MMAs are done: the P buffer takes the next head's image
     if (wtid == 0 && h + 2 < h_end) prefetch(h + 2);
     unsigned char* stg = sX + wq * 4096;  // this warp's staging (TMA epilogue)
-    if constexpr (kTmaO) {
+    {
       // the row of the operand this thread's outputs need, from sX (rows
       // past seqlen were zero-filled), before any warp stages over it
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
         orow[kk] = *reinterpret_cast<const uint4*>(sX + sw128(r - col0, 4 * half + kk));
-      group_sync(gbar);
+      if constexpr (kTmaO) group_sync(gbar);
     }
     float pd = 0.f, pq = 0.f, pdd = 0.f;  // partial <x, u>, <x, state part>, <x, dy>
     if (ok) {
@@ -450,6 +473,7 @@ __global__ void __launch_bounds__(512, 1)
   if (wtid == 0) {  // copies still in flight (after an expired wait) land before the CTA exits
     if (n_ld > 0) mbar_drain(&bar_ld[wg], (n_ld - 1) & 1);
     if (n_xr > 0) mbar_drain(&bar_xr[wg], (n_xr - 1) & 1);
+    if (n_xx > 0) mbar_drain(&bar_xx[wg], (n_xx - 1) & 1);
   }
   fence_before_sync();
   __syncthreads();
@@ -742,12 +766,13 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
     int grid, per;
     scan_partition(d, sms, &grid, &per);
-    CUtensorMap mDX, mDY;
+    CUtensorMap mDX, mDY, mXr;
     if (!make_y_map(&mDX, a.dx, d.H, d.T, d.B, 32) ||
-        !make_tma_map(&mDY, dy, 64, d.H, d.T, d.B, 1, 128))
+        !make_tma_map(&mDY, dy, 64, d.H, d.T, d.B, 1, 128) ||
+        !make_tma_map(&mXr, a.f.x, 64, d.H, d.T, d.B, 1, 128))
       return cudaErrorInvalidValue;
     SSD_LAUNCH("k_scan_tc_dx", s, launch_pdl(kern, dim3(grid), dim3(512), SM::kBytes, s,
-        mDX, mDY, static_cast<const bf16*>(a.f.x), static_cast<const bf16*>(a.f.B), Cm, dy, w.delta, w.acs,
+        mDX, mDY, mXr, static_cast<const bf16*>(a.f.x), static_cast<const bf16*>(a.f.B), Cm, w.delta, w.acs,
         static_cast<const unsigned char*>(w.dSimg), a.f.D, a.dx, w.ddir, w.qrow, w.ddiag, d.B, d.T,
         d.H, d.G, d.nc, d.hs, per, status));
   }
