@@ -339,22 +339,24 @@ __device__ __forceinline__ float4 fma4(float d, const float4& c, const float4& s
   return make_float4(fmaf(d, c.x, s.x), fmaf(d, c.y, s.y), fmaf(d, c.z, s.z), fmaf(d, c.w, s.w));
 }
 
-// Three blocks per SM (registers capped) put the whole grid of the
-// workloads here in one wave; four chunks in flight per thread.
-// grid (P*N/2048, H, B*K): segment k = z % K of batch b = z / K walks chunks
+// NT = 256: three blocks per SM (registers capped); NT = 128: seven, for
+// grids that three blocks of 256 per SM would hold in more than one wave (the
+// walk is as long for every block, so a second, partial wave costs a whole
+// walk); four chunks in flight per thread.
+// grid (P*N/(8 NT), H, B*K): segment k = z % K of batch b = z / K walks chunks
 // [k*lseg, min(nc, (k+1)*lseg)) from its entering state (init for K == 1,
 // else seg_in (B, K, H, P, N)); only the last segment writes final_state.
 // kSeg = false is the single-level walk (K = 1), compiled on its own.
 constexpr int kPrefetchImg = 4;
-template <bool kSeg>
-__global__ void __launch_bounds__(kThreads, 3)
+template <bool kSeg, int NT>
+__global__ void __launch_bounds__(NT, NT == 256 ? 3 : 7)
     k_state_passing_img(const float4* __restrict__ S, const float* __restrict__ acs,
                         const float4* __restrict__ init, unsigned char* __restrict__ img,
                         float4* __restrict__ final_state, int N, int H, int PN8, int L, int nc,
                         int K, int lseg, const float4* __restrict__ seg_in, int hs) {
   griddep_launch_dependents();
   griddep_wait();  // S and a come from the previous kernel (launched with launch_pdl)
-  const int e = blockIdx.x * kThreads + threadIdx.x, h = blockIdx.y;
+  const int e = blockIdx.x * NT + threadIdx.x, h = blockIdx.y;
   const int b = kSeg ? blockIdx.z / K : blockIdx.z, sk = kSeg ? blockIdx.z % K : 0;
   if (e >= PN8) return;
   const int cb = kSeg ? sk * lseg : 0, ce = kSeg ? min(nc, cb + lseg) : nc;
@@ -459,10 +461,12 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// Image-mode state passing backward: grid (nsplit = P*N/2048, H, B); reads the
-// H_c images, writes the dS_c images; dlast partials as in the float4 kernel.
-template <bool kSeg>
-__global__ void __launch_bounds__(kThreads, 3)
+// Image-mode state passing backward: grid (nsplit = P*N/(8 NT), H, B); reads
+// the H_c images, writes the dS_c images; dlast partials as in the float4
+// kernel (one per warp: P*N/256 per chunk for either NT).  NT as in the
+// forward.
+template <bool kSeg, int NT>
+__global__ void __launch_bounds__(NT, NT == 256 ? 3 : 7)
     k_state_passing_bwd_img(const float4* __restrict__ dHs, const float* __restrict__ acs,
                             const unsigned char* __restrict__ himg,
                             const float4* __restrict__ dfinal, unsigned char* __restrict__ dsimg,
@@ -477,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int split = blockIdx.x, nsplit = gridDim.x, h = blockIdx.y;
   const int b = kSeg ? blockIdx.z / K : blockIdx.z, sk = kSeg ? blockIdx.z % K : 0;
   const int cb = kSeg ? sk * lseg : 0, ce = kSeg ? min(nc, cb + lseg) : nc;
-  const int e = split * kThreads + threadIdx.x;
+  const int e = split * NT + threadIdx.x;
   const bool live = e < PN8;
   const int64_t step = (int64_t)H * PN8 * 2;
   const int64_t base = ((int64_t)b * nc * H + h) * PN8 * 2;
@@ -526,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
       if ((threadIdx.x & 31) == 0)
-        dlast_part[((((int64_t)b * H + h) * nc + c) * nsplit + split) * (kThreads / 32) +
+        dlast_part[((((int64_t)b * H + h) * nc + c) * nsplit + split) * (NT / 32) +
                    (threadIdx.x >> 5)] = dec[k] * part;
     }
   }
@@ -1110,6 +1114,20 @@ void launch_cumsum(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaStream_t
 
 bool vec4_ok(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+int sm_count() {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
+
+// Blocks of 128 threads (seven per SM) for the image-mode walks when a
+// single-level grid of 256-thread blocks (gx per (batch, head)) would not fit
+// in one wave at three per SM.
+bool narrow_walk(const Dims& d, int gx, int K) {
+  return K == 1 && (int64_t)gx * d.H * d.B > 3 * (int64_t)sm_count();
+}
+
 // Segments of the two-level state passing: two levels only when the
 // (batch, head) grid alone (gx blocks per pair) would leave at least half the
 // SMs idle (the backward: any SM idle, its per-chunk walk being longer); then
@@ -1119,9 +1137,7 @@ void seg_plan(const Dims& d, int gx, bool have_scratch, bool bwd, int* K, int* l
   *lseg = d.nc;
   const int kmax = have_scratch ? seg_max_segments(d) : 0;
   if (kmax < 2) return;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = sm_count();
   const int64_t base = (int64_t)gx * d.H * d.B;
   if (bwd ? base >= sms : 2 * base > sms) return;
   // at most three blocks per SM in all, so the segments run in one wave
@@ -1146,8 +1162,12 @@ void launch_state_passing(const Dims& d, const FwdArgs& a, const FwdWs& w, cudaS
           E, w.acs, reinterpret_cast<const float4*>(a.init), In, d.H, PN8, d.L, d.nc, K, lseg, d.hs));
       in = In;
     }
-    auto kern = K > 1 ? k_state_passing_img<true> : k_state_passing_img<false>;
-    SSD_LAUNCH("k_state_passing", s, launch_pdl(kern, dim3(gx, d.H, d.B * K), dim3(kThreads), 0, s,
+    const bool nw = narrow_walk(d, gx, K);
+    auto kern = K > 1 ? k_state_passing_img<true, 256>
+                      : (nw ? k_state_passing_img<false, 128> : k_state_passing_img<false, 256>);
+    const int nt = nw ? 128 : 256;
+    SSD_LAUNCH("k_state_passing", s, launch_pdl(kern, dim3((PN8 + nt - 1) / nt, d.H, d.B * K),
+        dim3(nt), 0, s,
         reinterpret_cast<const float4*>(w.S), w.acs, reinterpret_cast<const float4*>(a.init),
         static_cast<unsigned char*>(w.Himg), reinterpret_cast<float4*>(a.final_state), d.N, d.H,
         PN8, d.L, d.nc, K, lseg, in, d.hs));
@@ -1202,14 +1222,18 @@ int launch_state_passing_bwd(const Dims& d, const BwdArgs& a, const BwdWs& w, cu
           lseg, d.hs));
       out = Out;
     }
-    auto kern = K > 1 ? k_state_passing_bwd_img<true> : k_state_passing_bwd_img<false>;
-    SSD_LAUNCH("k_state_passing_bwd", s, launch_pdl(kern, dim3(nsplit, d.H, d.B * K),
-        dim3(kThreads), 0, s,
+    const bool nw = narrow_walk(d, nsplit, K);
+    auto kern = K > 1 ? k_state_passing_bwd_img<true, 256>
+                      : (nw ? k_state_passing_bwd_img<false, 128>
+                            : k_state_passing_bwd_img<false, 256>);
+    const int nt = nw ? 128 : 256;
+    SSD_LAUNCH("k_state_passing_bwd", s, launch_pdl(kern, dim3((PN8 + nt - 1) / nt, d.H, d.B * K),
+        dim3(nt), 0, s,
         reinterpret_cast<const float4*>(w.dHs), w.f.acs,
         static_cast<const unsigned char*>(w.f.Himg), reinterpret_cast<const float4*>(a.dfinal),
         static_cast<unsigned char*>(w.dSimg), w.dlast, reinterpret_cast<float4*>(a.dinit), d.N,
         d.H, PN8, d.L, d.nc, K, lseg, out, d.hs));
-    return nsplit * (kThreads / 32);  // one partial per warp
+    return (PN8 + nt - 1) / nt * (nt / 32);  // one partial per warp
   }
   if (PN % 4 == 0 && vec4_ok(a.dfinal) && vec4_ok(a.dinit)) {
     const int PN4 = PN / 4, nsplit = (PN4 + kThreads - 1) / kThreads;
