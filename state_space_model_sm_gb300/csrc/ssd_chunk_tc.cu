@@ -527,17 +527,19 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
       float* da2 = der(i);
       float* dsx = da2 + L;
       float* dcf = dsx + L;
+      // the column factor's edge value is recomputed from the raw vector, so
+      // one pass and one barrier suffice; it must equal the edge's own entry
+      // bit for bit (the group factor R uses that entry and the two cancel),
+      // hence rounded products that cannot fuse into the subtraction
       for (int t = tid; t < L; t += kConv) {
-        const float a2 = ra[t] * kLog2e, dl = ra[L + t];
+        const float a2 = __fmul_rn(ra[t], kLog2e), dl = ra[L + t];
+        const float sx = dl > 0.f ? a2 - lg2_approx(dl) : __int_as_float(0x7f800000);
         da2[t] = a2;
-        dsx[t] = dl > 0.f ? a2 - lg2_approx(dl) : __int_as_float(0x7f800000);
+        dsx[t] = sx;
+        if constexpr (REV) dcf[t] = ex2_approx(a2 - __fmul_rn(ra[t & ~15], kLog2e));
+        else dcf[t] = ex2_approx(__fmul_rn(ra[t | 15], kLog2e) - sx);
       }
       warp_arrive(&bar_vec_empty[v], lane);
-      conv_sync();
-      for (int t = tid; t < L; t += kConv) {
-        if constexpr (REV) dcf[t] = ex2_approx(da2[t] - da2[t & ~15]);
-        else dcf[t] = ex2_approx(da2[t | 15] - dsx[t]);
-      }
       conv_sync();
     };
 
