@@ -634,13 +634,28 @@ __device__ __forceinline__ void reduce_elem(const float4* __restrict__ in, float
   const int n = (int)(i % N4);
   const int t = (int)((row / pr.G) % pr.T);
   const int nb = (t % pr.L) < 128 ? pr.nb[0] : pr.nb[1];
-  float4 s = in[(row * pr.stride) * N4 + n];
-  for (int k = 1; k < nb; ++k) {
-    const float4 v = in[(row * pr.stride + k) * N4 + n];
-    s.x += v.x;
-    s.y += v.y;
-    s.z += v.z;
-    s.w += v.w;
+  // the first four partials are loaded before any is added (all in flight
+  // at once); the sum keeps the partials' order
+  const float4* p = in + (row * pr.stride) * N4 + n;
+  float4 v[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    if (k < nb) v[k] = p[(int64_t)k * N4];
+  float4 s = v[0];
+#pragma unroll
+  for (int k = 1; k < 4; ++k)
+    if (k < nb) {
+      s.x += v[k].x;
+      s.y += v[k].y;
+      s.z += v[k].z;
+      s.w += v[k].w;
+    }
+  for (int k = 4; k < nb; ++k) {
+    const float4 u = p[(int64_t)k * N4];
+    s.x += u.x;
+    s.y += u.y;
+    s.z += u.z;
+    s.w += u.w;
   }
   out[i] = s;
 }
