@@ -484,38 +484,6 @@ __global__ void __launch_bounds__(512, 1)
 // (dC kernel) and column sums (dB kernel) of M:
 //   ddA_r = sum_{j<r} (colsum_j - rowsum_j) + sum_{l>=r} ycs_l + sum_{s<r} qrow_s + dlast_c
 //   ddt_r = (ddir_r + A ddA_r) softplus'(dt_r + dt_bias);  partials of dA, ddt_bias, dD.
-// Exclusive prefix sums of two values over the block's threads (whole
-// warps), in thread order, and the block totals: a warp scan, the warps'
-// totals through shared memory, one barrier.
-__device__ __forceinline__ void block_exclusive_scan2(float a, float b, float2* warp_tot,
-                                                      float2& pre, float2& tot) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  float ia = a, ib = b;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const float oa = __shfl_up_sync(0xffffffffu, ia, off);
-    const float ob = __shfl_up_sync(0xffffffffu, ib, off);
-    if (lane >= off) {
-      ia += oa;
-      ib += ob;
-    }
-  }
-  if (lane == 31) warp_tot[warp] = make_float2(ia, ib);
-  __syncthreads();
-  float2 before = make_float2(0.f, 0.f), all = make_float2(0.f, 0.f);
-  for (int w = 0; w < nw; ++w) {
-    const float2 t = warp_tot[w];
-    if (w < warp) {
-      before.x += t.x;
-      before.y += t.y;
-    }
-    all.x += t.x;
-    all.y += t.y;
-  }
-  pre = make_float2(before.x + ia - a, before.y + ib - b);
-  tot = all;
-}
-
 struct FinalizeArgs {
   const bf16* dt;
   const float *dt_bias, *A, *delta, *rowsum, *colsum, *ycs, *qrow, *ddir, *ddiag, *dlast;
@@ -528,93 +496,142 @@ struct FinalizeArgs {
   int* done;                  // finalize blocks finished, 0 at launch
 };
 
-// One (chunk c, head h, batch b) of the finalize step; NT threads = L rows.
-// A head of 1 << hs parts sums its parts' row vectors first: every term of
-// ddA and of the direct dt gradient is a sum over the head's channels.
-template <int NT>
-__device__ __forceinline__ void finalize_block(const FinalizeArgs& f, int c, int h, int b) {
-  constexpr int NW = NT / 32;
-  const bf16* __restrict__ dt = f.dt;
-  const float* __restrict__ dt_bias = f.dt_bias;
-  const float* __restrict__ A = f.A;
-  const float* __restrict__ delta = f.delta;
-  const float* __restrict__ rowsum = f.rowsum;
-  const float* __restrict__ colsum = f.colsum;
-  const float* __restrict__ ycs = f.ycs;
-  const float* __restrict__ qrow = f.qrow;
-  const float* __restrict__ ddir = f.ddir;
-  const float* __restrict__ ddiag = f.ddiag;
-  const float* __restrict__ dlast = f.dlast;
-  float* __restrict__ ddt = f.ddt;
-  float* __restrict__ part = f.part;
-  const int nsplit = f.nsplit, T = f.T, H = f.H >> f.hs, L = f.L, nc = f.nc, V = 1 << f.hs;
-  __shared__ float2 wt[NW];
-  __shared__ float3 red[NW];
-  __shared__ float s_dl;
-  const int r = threadIdx.x;
+// One (chunk c, head h, batch b) of the finalize step, by W = L / 128 warps:
+// lane k of the item's warp w takes the four consecutive rows from
+// 128 w + 4 k, so its loads are float4 and the scans are a lane-local pass,
+// one warp scan and, for W > 1, the warps' totals through shared memory (a
+// barrier of the item's warps only).  A head of 1 << hs parts sums its
+// parts' row vectors first: every term of ddA and of the direct dt gradient
+// is a sum over the head's channels.
+template <int L>
+__device__ __forceinline__ void finalize_item(const FinalizeArgs& f, int c, int h, int b,
+                                              int w, int bar_id, float4* xch) {
+  constexpr int R = 4, W = L / 128;
+  const int lane = threadIdx.x & 31;
+  const int nsplit = f.nsplit, T = f.T, H = f.H >> f.hs, nc = f.nc, V = 1 << f.hs;
   const int Lv = min(L, T - c * L);
-  const int64_t cv = (((int64_t)b * H + h) * nc + c) * L;
-  const bool live = r < Lv;
-  const int64_t ti = ((int64_t)b * T + (int64_t)c * L + r) * H + h;
-  const float vdt = live ? __bfloat162float(dt[ti]) : 0.f;
-  const float dlt = live ? delta[cv + r] : 0.f;
-  float jump = 0.f, y = 0.f, dirr = 0.f, dg = 0.f;
+  const int r0 = 128 * w + lane * R;
+  const int64_t cv = (((int64_t)b * H + h) * nc + c) * L + r0;
+  const int64_t ti0 = ((int64_t)b * T + (int64_t)c * L + r0) * H + h;
+  float vdt[R], jump[R], y[R], dirr[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    vdt[i] = r0 + i < Lv ? __bfloat162float(f.dt[ti0 + (int64_t)i * H]) : 0.f;
+    jump[i] = y[i] = dirr[i] = 0.f;
+  }
+  const float4 d4 = *reinterpret_cast<const float4*>(f.delta + cv);
+  float dlt[R] = {d4.x, d4.y, d4.z, d4.w}, dg[R] = {0.f, 0.f, 0.f, 0.f};
   for (int j = 0; j < V; ++j) {
     const int64_t bhc = ((int64_t)b * H + h) * V + j;  // the part's (b, part) row
-    const int64_t cp = (bhc * nc + c) * L;
-    if (live) {
-      jump += colsum[cp + r] - rowsum[cp + r] + qrow[cp + r];
-      y += ycs[cp + r];
-      dirr += ddir[cp + r];
-      dg += ddiag[cp + r];
+    const int64_t cp = (bhc * nc + c) * L + r0;
+    const float4 cs = *reinterpret_cast<const float4*>(f.colsum + cp);
+    const float4 rs = *reinterpret_cast<const float4*>(f.rowsum + cp);
+    const float4 qr = *reinterpret_cast<const float4*>(f.qrow + cp);
+    const float4 yc = *reinterpret_cast<const float4*>(f.ycs + cp);
+    const float4 di = *reinterpret_cast<const float4*>(f.ddir + cp);
+    const float4 dd = *reinterpret_cast<const float4*>(f.ddiag + cp);
+    const float csv[R] = {cs.x, cs.y, cs.z, cs.w}, rsv[R] = {rs.x, rs.y, rs.z, rs.w};
+    const float qrv[R] = {qr.x, qr.y, qr.z, qr.w}, ycv[R] = {yc.x, yc.y, yc.z, yc.w};
+    const float div[R] = {di.x, di.y, di.z, di.w}, ddv[R] = {dd.x, dd.y, dd.z, dd.w};
+#pragma unroll
+    for (int e = 0; e < R; ++e) {
+      jump[e] += csv[e] - rsv[e] + qrv[e];
+      y[e] += ycv[e];
+      dirr[e] += div[e];
+      dg[e] += ddv[e];
     }
   }
-  // dlast: the state-passing partials of every part, summed by warp 0 (lane
-  // k takes the partials k, k + 32, ..., then a fixed xor tree), visible to
-  // the block after the scans' barriers
-  if (r < 32) {
-    float v = 0.f;
-    for (int j = 0; j < V; ++j) {
-      const int64_t bhc = ((int64_t)b * H + h) * V + j;
-      for (int k = r; k < nsplit; k += 32) v += dlast[(bhc * nc + c) * nsplit + k];
-    }
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (r == 0) s_dl = v;
+  // rows past seqlen take no part (their entries are not defined)
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+    if (r0 + i >= Lv) dlt[i] = jump[i] = y[i] = dirr[i] = dg[i] = 0.f;
+  // dlast: the state-passing partials of every part (lane k takes the
+  // partials k, k + 32, ..., then a fixed xor tree)
+  float dl = 0.f;
+  for (int j = 0; j < V; ++j) {
+    const int64_t bhc = ((int64_t)b * H + h) * V + j;
+    for (int k = lane; k < nsplit; k += 32) dl += f.dlast[(bhc * nc + c) * nsplit + k];
   }
-  // ddA_r = prefix_{j<r}(jump_j) + dlast + suffix_{l>=r}(ycs_l)
-  float2 pre, tot;  // .x jump, .y ycs
-  block_exclusive_scan2(jump, y, wt, pre, tot);
-  const float dd = pre.x + s_dl + (tot.y - pre.y);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
+  // ddA_r = prefix_{j<r}(jump_j) + dlast + suffix_{l>=r}(ycs_l): the lane's
+  // totals, their scan over the lanes, then over the item's warps
+  const float tj = (jump[0] + jump[1]) + (jump[2] + jump[3]);
+  const float ty = (y[0] + y[1]) + (y[2] + y[3]);
+  float ij = tj, iy = ty;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float oj = __shfl_up_sync(0xffffffffu, ij, off);
+    const float oy = __shfl_up_sync(0xffffffffu, iy, off);
+    if (lane >= off) {
+      ij += oj;
+      iy += oy;
+    }
+  }
+  float pj = ij - tj, py = iy - ty;  // before the lane's first row, within the warp
+  float toty = __shfl_sync(0xffffffffu, iy, 31);
+  if constexpr (W > 1) {
+    if (lane == 31) xch[w] = make_float4(ij, iy, 0.f, 0.f);
+    asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(32 * W) : "memory");
+    float bj = 0.f, by = 0.f, ay = 0.f;
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      const float4 t = xch[k];
+      if (k < w) {
+        bj += t.x;
+        by += t.y;
+      }
+      ay += t.y;
+    }
+    pj += bj;
+    py += by;
+    toty = ay;
+  }
+  const float Ah = f.A[h], bias = f.dt_bias ? f.dt_bias[h] : 0.f;
   float pA = 0.f, pB = 0.f, pD = 0.f;
-  if (live) {
-    const float v = vdt + (dt_bias ? dt_bias[h] : 0.f);
-    const float sg = v > 20.f ? 1.f : 1.f / (1.f + __expf(-v));
-    const float gv = fmaf(A[h], dd, dirr) * sg;
-    ddt[ti] = gv;
-    pA = dlt * dd;
-    pB = gv;
-    pD = dg;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const float dd = pj + dl + (toty - py);
+    pj += jump[i];
+    py += y[i];
+    if (r0 + i < Lv) {
+      const float v = vdt[i] + bias;
+      const float sg = v > 20.f ? 1.f : 1.f / (1.f + __expf(-v));
+      const float gv = fmaf(Ah, dd, dirr[i]) * sg;
+      f.ddt[ti0 + (int64_t)i * H] = gv;
+      pA += dlt[i] * dd;
+      pB += gv;
+      pD += dg[i];
+    }
   }
-  // the block's partials of dA, ddt_bias and dD: warp trees, then the warps
-  // in order
+  // the item's partials of dA, ddt_bias and dD: a fixed xor tree per warp,
+  // then the warps in order
+#pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     pA += __shfl_xor_sync(0xffffffffu, pA, o);
     pB += __shfl_xor_sync(0xffffffffu, pB, o);
     pD += __shfl_xor_sync(0xffffffffu, pD, o);
   }
-  if ((r & 31) == 0) red[r >> 5] = make_float3(pA, pB, pD);
-  __syncthreads();
-  if (r == 0) {
-    float3 t = make_float3(0.f, 0.f, 0.f);
-    for (int i = 0; i < NW; ++i) {
-      t.x += red[i].x;
-      t.y += red[i].y;
-      t.z += red[i].z;
+  if constexpr (W > 1) {
+    if (lane == 0) xch[W + w] = make_float4(pA, pB, pD, 0.f);
+    asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(32 * W) : "memory");
+    if (w == 0) {
+      pA = pB = pD = 0.f;
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        const float4 t = xch[W + k];
+        pA += t.x;
+        pB += t.y;
+        pD += t.z;
+      }
     }
-    float* o = part + (((int64_t)b * H + h) * nc + c) * 3;
-    o[0] = t.x;
-    o[1] = t.y;
-    o[2] = t.z;
+  }
+  if (w == 0 && lane == 0) {
+    float* o = f.part + (((int64_t)b * H + h) * nc + c) * 3;
+    o[0] = pA;
+    o[1] = pB;
+    o[2] = pD;
+    __threadfence();  // before the block counts itself finished
   }
 }
 
@@ -660,10 +677,10 @@ __device__ __forceinline__ void reduce_elem(const float4* __restrict__ in, float
   out[i] = s;
 }
 
-// The backward's tail in one launch of NT-thread blocks (NT = L, one thread
-// per row of a chunk): blocks [0, nfin) run the finalize step for (c, h, b) =
-// (i % nc, (i / nc) % H, i / (nc H)); the rest sum the dC, then the dB
-// head-block partials (nred blocks each).  The two parts are independent, so
+// The backward's tail in one launch of NT-thread blocks (NT = L): the first
+// ceil(nfin / 4) blocks run the finalize step, four items i = (c, h, b) =
+// (i % nc, (i / nc) % H, i / (nc H)) per block, 128 rows per warp; the rest
+// sum the dC, then the dB head-block partials (nred blocks each).  The two parts are independent, so
 // the latency-bound finalize blocks and the bandwidth-bound sums share the SMs.
 // dA, ddt_bias, dD of every head from the per-chunk partials, by the block
 // that finishes the finalize step last: per head, lane k of a warp sums the
@@ -695,24 +712,32 @@ __device__ __forceinline__ void param_grads_block(const FinalizeArgs& f) {
   }
 }
 
-// (1536 threads per SM: six 256-thread blocks resident, 40 registers each)
+// (1024 threads per SM: four 256-thread or eight 128-thread blocks, 64
+// registers each, for the four rows of six vectors a finalize lane holds)
 template <int NT>
-__global__ void __launch_bounds__(NT, 1536 / NT)
+__global__ void __launch_bounds__(NT, 1024 / NT)
     k_bwd_tail_tc(FinalizeArgs f, int nfin, const float4* __restrict__ dCp,
                   float4* __restrict__ dC, const float4* __restrict__ dBp, float4* __restrict__ dB,
                   int nred, int64_t rows, PartialRows prC, PartialRows prB, int N4) {
   griddep_launch_dependents();
   griddep_wait();  // every input comes from the previous kernels
   const int blk = blockIdx.x;
-  if (blk < nfin) {
-    const int H = f.H >> f.hs;
-    finalize_block<NT>(f, blk % f.nc, (blk / f.nc) % H, blk / (f.nc * H));
+  constexpr int W = NT / 128, IPB = NT / 32 / W;  // warps per item, items per block
+  const int nfb = (nfin + IPB - 1) / IPB;        // finalize blocks
+  if (blk < nfb) {
+    __shared__ float4 xch[NT / 32][2];  // per item: its warps' totals, then partials
+    const int H = f.H >> f.hs, warp = (int)(threadIdx.x >> 5), k = warp / W;
+    const int item = blk * IPB + k;
+    if (item < nfin)
+      finalize_item<NT>(f, item % f.nc, (item / f.nc) % H, item / (f.nc * H), warp % W, 1 + k,
+                        &xch[k * W][0]);
     // the last finalize block to finish also forms the parameter gradients
-    // (thread 0 wrote this block's partials)
+    // (each item's first lane wrote and fenced its partials)
     __shared__ int last;
+    __syncthreads();
     if (threadIdx.x == 0) {
       __threadfence();
-      last = atomicAdd(f.done, 1) == nfin - 1;
+      last = atomicAdd(f.done, 1) == nfb - 1;
     }
     __syncthreads();
     if (last) {
@@ -721,7 +746,7 @@ __global__ void __launch_bounds__(NT, 1536 / NT)
     }
     return;
   }
-  const int rb = blk - nfin, which = rb / nred;
+  const int rb = blk - nfb, which = rb / nred;
   const int64_t i = (int64_t)(rb % nred) * NT + threadIdx.x;
   if (i < rows * N4) reduce_elem(which ? dBp : dCp, which ? dB : dC, i, which ? prB : prC, N4);
 }
@@ -812,7 +837,8 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     const int c0 = L > 128 ? w.nb.light : w.nb.heavy;
     const PartialRows prC{nblk, d.G, d.T, d.L, {c0, w.nb.heavy}};
     const PartialRows prB{nblk, d.G, d.T, d.L, {w.nb.heavy, w.nb.light}};
-    SSD_LAUNCH("k_bwd_tail_tc", s, launch_pdl(k_bwd_tail_tc<L>, dim3(nfin + 2 * nred), dim3(L), 0, s,
+    const int nfb = (nfin + 3) / 4;  // finalize blocks: four items each (128 rows per warp)
+    SSD_LAUNCH("k_bwd_tail_tc", s, launch_pdl(k_bwd_tail_tc<L>, dim3(nfb + 2 * nred), dim3(L), 0, s,
         fa, nfin, reinterpret_cast<const float4*>(w.dCp), reinterpret_cast<float4*>(a.dC),
         reinterpret_cast<const float4*>(w.dBp), reinterpret_cast<float4*>(a.dB),
         nred > 0 ? nred : 1, rows, prC, prB, N4));
