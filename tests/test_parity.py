@@ -241,6 +241,9 @@ TC_BWD_CASES = [
     ("tcb_partial_tile", SSDShape(1, 300, 2, 64, 128, 1, 256), 0.3, 0.2),
     ("tcb_p128_n128_l256_init", SSDShape(2, 1024, 4, 128, 128, 1, 256), 0.2, 0.5),
     ("tcb_p128_n64_l128_tail", SSDShape(1, 333, 3, 128, 64, 3, 128), 0.1, 0.3),
+    # 2 x 64 heads x 4 blocks of 256 = 512 state-passing blocks, more than
+    # three per SM hold in one wave: the walks run as 128-thread blocks
+    ("tcb_wide_walk_tail_init", SSDShape(2, 333, 64, 64, 128, 8, 128), 0.2, 0.5),
 ]
 
 
