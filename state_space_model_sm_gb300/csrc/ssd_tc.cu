@@ -86,14 +86,17 @@ struct ScanSmem {
   static constexpr int kPw = 2 * kLT * 128;                 // per group: P panel hi + lo
   static constexpr int kBP = kBrows > 2 * kPw ? kBrows : 2 * kPw;
   static constexpr int kX = L * 128;                        // per group: dy rows
-  // fp32 out leaves through TMA stores when the operand-row buffer can stage
-  // every warp's 32 x 32 block (4 KB each, 128-byte swizzle)
-  static constexpr bool kTmaO = kX >= 8 * 4096;
-  // without them the tile's x rows come by TMA too (per group)
-  static constexpr int kXr = kTmaO ? 0 : kLT * 128;
+  // Where the dy rows alone cannot stage every warp's 32 x 32 fp32 block of
+  // dx (4 KB each, 128-byte swizzle) for its TMA store, the tile's x rows
+  // come by TMA into a buffer right after them, and the two together are
+  // the staging
+  static constexpr bool kXT = kX < 8 * 4096;
+  static constexpr int kXr = kXT ? kLT * 128 : 0;
+  static constexpr int kXg = kX + kXr;                      // per group: dy (+ x) rows
+  static_assert(kXg >= 8 * 4096, "dx staging: eight warps' 4 KB blocks");
   static constexpr int kHlo = (N / 64) * 64 * 128;          // offset of the state's lo part
   static constexpr int kImg = 2 * kHlo;                     // bytes of one state image
-  static constexpr int kBytes = kC + kBP + 2 * kX + 2 * kXr + (8 * L + 6 * 128) * 4 + 1024;
+  static constexpr int kBytes = kC + kBP + 2 * kXg + (8 * L + 6 * 128) * 4 + 1024;
 };
 
 __device__ __forceinline__ void group_sync(int id) {
@@ -108,7 +111,7 @@ __global__ void __launch_bounds__(512, 1)
               const bf16* __restrict__ Cm,
               const float* __restrict__ delta, const float* __restrict__ acs,
               const unsigned char* __restrict__ simg, const float* __restrict__ D,
-              float* __restrict__ out, float* __restrict__ ddir, float* __restrict__ qrow,
+              float* __restrict__ ddir, float* __restrict__ qrow,
               float* __restrict__ ddiag, int B_, int T, int H, int G, int nc, int hs,
               int items_per_cta, int* status) {
   using SM = ScanSmem<N, L>;
@@ -122,9 +125,8 @@ __global__ void __launch_bounds__(512, 1)
   unsigned char* base = align1024(smem_raw);
   unsigned char* sR = base;               // row operand: B rows of the tile
   unsigned char* sBP = sR + SM::kC;       // column operand rows, later the groups' P buffers
-  unsigned char* sXall = sBP + SM::kBP;   // per group: dy rows
-  unsigned char* sXrall = sXall + 2 * SM::kX;  // per group: x rows of the tile
-  float* sAall = reinterpret_cast<float*>(sXrall + 2 * SM::kXr);  // per group: a [L], delta [L]
+  unsigned char* sXall = sBP + SM::kBP;   // per group: dy rows (and the tile's x rows)
+  float* sAall = reinterpret_cast<float*>(sXall + 2 * SM::kXg);  // per group: a [L], delta [L]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hpg = H / G;
@@ -225,8 +227,8 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
 
   unsigned char* Pw = sBP + wg * SM::kPw;
-  unsigned char* sX = sXall + wg * SM::kX;
-  unsigned char* sXr = sXrall + wg * SM::kXr;
+  unsigned char* sX = sXall + wg * SM::kXg;
+  unsigned char* sXr = sX + SM::kX;
   float* sa2 = sAall + wg * 4 * L;  // a * log2(e)
   float* sx = sa2 + L;              // delta
   float* sraw = sx + L;             // prefetched a [L], delta [L] of the next head
@@ -238,10 +240,10 @@ __global__ void __launch_bounds__(512, 1)
   const uint64_t dP = sdesc(smem_u32(Pw), 16, 1024);        // P panel / state image, K-major
   const uint64_t dX = sdesc(smem_u32(sX), L * 128, 1024);   // dy rows, MN-major
 
-  // Each head's epilogue reads its own dy row from sX; with TMA stores of dx
-  // the block is then staged there and stored.  Only after that do the next
-  // head's rows come in.
-  constexpr bool kTmaO = SM::kTmaO;
+  // Each head's epilogue reads its own dy row from sX (and x row from sXr);
+  // its block of dx is then staged there for a TMA store.  Only after that do
+  // the next head's rows come in.
+  constexpr bool kXT = SM::kXT;
   // What a head needs, copied by thread wtid 0 of its pipeline: its
   // inter-chunk state image (into the P buffer) and raw a / delta with bulk
   // copies on bar_ld, issued once the previous head's products are done; its
@@ -254,9 +256,9 @@ __global__ void __launch_bounds__(512, 1)
     for (int k2 = 0; k2 < ncol / 128; ++k2)
       tma_load_4d(sX + k2 * 128 * 128, &mOp, 0, hh, (int)t0 + col0 + 128 * k2, b, &bar_xr[wg]);
   };
-  // (without the TMA epilogue) the tile's rows of x, which only the epilogue
-  // reads: on bar_xx, issued once the previous head's epilogue is over (rows
-  // past seqlen read as zeros)
+  // (kXT) the tile's rows of x, which only the epilogue reads: on bar_xx,
+  // issued once the previous head's epilogue is over (rows past seqlen read
+  // as zeros)
   auto prefetch_xr = [&](int hh) {
     mbar_arrive_expect_tx(&bar_xx[wg], (uint32_t)(LT * 128));
     ++n_xx;
@@ -274,7 +276,7 @@ __global__ void __launch_bounds__(512, 1)
   if (wtid == 0 && h_begin + wg < h_end) {
     prefetch(h_begin + wg);
     prefetch_x(h_begin + wg);
-    if constexpr (!kTmaO) prefetch_xr(h_begin + wg);
+    if constexpr (kXT) prefetch_xr(h_begin + wg);
   }
 
   for (int h = h_begin + wg; h < h_end; h += 2) {
@@ -292,13 +294,13 @@ __global__ void __launch_bounds__(512, 1)
     }
     // (TMA epilogue) the previous head's dx stores have read their staging
     // in sX before this head's operand rows are copied over it
-    if (kTmaO && lane == 0) bulk_wait_read<0>();
+    if (lane == 0) bulk_wait_read<0>();
     fence_async_smem();
     fence_before_sync();
     group_sync(gbar);
     if (wtid == 0 && h != h_begin + wg) {
       prefetch_x(h);
-      if constexpr (!kTmaO) prefetch_xr(h);
+      if constexpr (kXT) prefetch_xr(h);
     }
     if (wtid == 0) {
       fence_after_sync();
@@ -364,23 +366,23 @@ __global__ void __launch_bounds__(512, 1)
       }
       ++n_p;
     }
-    // (with the TMA epilogue) this thread's 32 columns of its row of x:
-    // loaded now, so the latency overlaps the last MMAs
+    // (without kXT) this thread's 32 columns of its row of x: loaded now, so
+    // the latency overlaps the last MMAs
     const int64_t rowoff = (((int64_t)b * T + t0 + r) * H + h) * kP;
     const bool live = r < Lv;
     uint4 orow[4], xrow[4];
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-      if constexpr (kTmaO)
+      if constexpr (!kXT)
         xrow[kk] = live ? *reinterpret_cast<const uint4*>(x + rowoff + 32 * half + 8 * kk)
                         : make_uint4(0, 0, 0, 0);
     }
     ++n_done;
     const bool ok = __all_sync(
         0xffffffffu, mbar_wait(&bar_done[wg], (n_done - 1) & 1, status, &abort_flag) &&
-                         (kTmaO || mbar_wait(&bar_xx[wg], hpar, status, &abort_flag)));
+                         (!kXT || mbar_wait(&bar_xx[wg], hpar, status, &abort_flag)));
     fence_after_sync();
-    if constexpr (!kTmaO) {
+    if constexpr (kXT) {
       // the row of x, from the tile's x rows
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
@@ -388,14 +390,15 @@ __global__ void __launch_bounds__(512, 1)
     }
     // this head's MMAs are done: the P buffer takes the next head's image
     if (wtid == 0 && h + 2 < h_end) prefetch(h + 2);
-    unsigned char* stg = sX + wq * 4096;  // this warp's staging (TMA epilogue)
+    unsigned char* stg = sX + wq * 4096;  // this warp's staging (TMA epilogue; spans sXr)
     {
       // the row of the operand this thread's outputs need, from sX (rows
-      // past seqlen were zero-filled), before any warp stages over it
+      // past seqlen were zero-filled), before any warp stages over it (and
+      // over the x rows, read above)
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
         orow[kk] = *reinterpret_cast<const uint4*>(sX + sw128(r - col0, 4 * half + kk));
-      if constexpr (kTmaO) group_sync(gbar);
+      group_sync(gbar);
     }
     float pd = 0.f, pq = 0.f, pdd = 0.f;  // partial <x, u>, <x, state part>, <x, dy>
     if (ok) {
@@ -407,45 +410,36 @@ __global__ void __launch_bounds__(512, 1)
         tmem_ld16(tlane + colY + 32 * half + 16 * c16, yv);
         tmem_ld16(tlane + colST + 32 * half + 16 * c16, st);
         tmem_wait_ld();
-        if (kTmaO || live) {
+        // (rows past seqlen: x reads as zeros, and the store clips them)
 #pragma unroll
-          for (int k8 = 0; k8 < 2; ++k8) {
-            float ov[8], o[8];
-            unpack8(orow[2 * c16 + k8], ov);
-            float xv[8];
-            unpack8(xrow[2 * c16 + k8], xv);
+        for (int k8 = 0; k8 < 2; ++k8) {
+          float ov[8], o[8];
+          unpack8(orow[2 * c16 + k8], ov);
+          float xv[8];
+          unpack8(xrow[2 * c16 + k8], xv);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float us = es * st[8 * k8 + e];
-              const float u = yv[8 * k8 + e] + us;
-              o[e] = fmaf(dr, u, Dh * ov[e]);
-              pd = fmaf(xv[e], u, pd);
-              pq = fmaf(xv[e], us, pq);
-              pdd = fmaf(xv[e], ov[e], pdd);
-            }
-            if constexpr (kTmaO) {
-              const int j = 4 * c16 + 2 * k8;  // 16-byte chunks j, j + 1 of the 128-byte row
-              *reinterpret_cast<float4*>(stg + sw128(lane, j)) = make_float4(o[0], o[1], o[2], o[3]);
-              *reinterpret_cast<float4*>(stg + sw128(lane, j + 1)) =
-                  make_float4(o[4], o[5], o[6], o[7]);
-            } else {
-              float* of = out + rowoff + 32 * half + 16 * c16 + 8 * k8;
-              *reinterpret_cast<float4*>(of) = make_float4(o[0], o[1], o[2], o[3]);
-              *reinterpret_cast<float4*>(of + 4) = make_float4(o[4], o[5], o[6], o[7]);
-            }
+          for (int e = 0; e < 8; ++e) {
+            const float us = es * st[8 * k8 + e];
+            const float u = yv[8 * k8 + e] + us;
+            o[e] = fmaf(dr, u, Dh * ov[e]);
+            pd = fmaf(xv[e], u, pd);
+            pq = fmaf(xv[e], us, pq);
+            pdd = fmaf(xv[e], ov[e], pdd);
           }
+          const int j = 4 * c16 + 2 * k8;  // 16-byte chunks j, j + 1 of the 128-byte row
+          *reinterpret_cast<float4*>(stg + sw128(lane, j)) = make_float4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<float4*>(stg + sw128(lane, j + 1)) =
+              make_float4(o[4], o[5], o[6], o[7]);
         }
       }
-      if constexpr (kTmaO) {
-        // one store of the warp's 32 rows x 32 columns (rows past seqlen are
-        // clipped by it); the next head (or unit) waits for its reads of the
-        // staging before sX is refilled
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0 && t0 + r0 + 32 * q < T) {
-          tma_store_4d(&mOut, 32 * half, h, (int)t0 + r0 + 32 * q, b, stg);
-          bulk_commit_group();
-        }
+      // one store of the warp's 32 rows x 32 columns (rows past seqlen are
+      // clipped by it); the next head (or unit) waits for its reads of the
+      // staging before sX is refilled
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0 && t0 + r0 + 32 * q < T) {
+        tma_store_4d(&mOut, 32 * half, h, (int)t0 + r0 + 32 * q, b, stg);
+        bulk_commit_group();
       }
     }
     // combine the two half-rows (pipeline-local barrier)
@@ -465,7 +459,7 @@ __global__ void __launch_bounds__(512, 1)
   }
     // both groups are done with this unit's C.B^T tile and buffers (and the
     // dx stores with their staging, before the next unit's rows come in)
-    if (kTmaO && lane == 0) bulk_wait_read<0>();
+    if (lane == 0) bulk_wait_read<0>();
     fence_before_sync();
     __syncthreads();
   }
@@ -813,7 +807,7 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
       return cudaErrorInvalidValue;
     SSD_LAUNCH("k_scan_tc_dx", s, launch_pdl(kern, dim3(grid), dim3(512), SM::kBytes, s,
         mDX, mDY, mXr, static_cast<const bf16*>(a.f.x), static_cast<const bf16*>(a.f.B), Cm, w.delta, w.acs,
-        static_cast<const unsigned char*>(w.dSimg), a.f.D, a.dx, w.ddir, w.qrow, w.ddiag, d.B, d.T,
+        static_cast<const unsigned char*>(w.dSimg), a.f.D, w.ddir, w.qrow, w.ddiag, d.B, d.T,
         d.H, d.G, d.nc, d.hs, per, status));
   }
   const int nblk = w.nb.max();  // partial slots per row
