@@ -638,37 +638,47 @@ struct PartialRows {
 };
 
 // out[i, :] = sum_k in[i, k, :] over the row's head-block partials, in order
-// (float4 per element i; N % 4 == 0).
-__device__ __forceinline__ void reduce_elem(const float4* __restrict__ in, float4* __restrict__ out,
-                                            int64_t i, const PartialRows& pr, int N4) {
-  const int64_t row = i / N4;
-  const int n = (int)(i % N4);
-  const int t = (int)((row / pr.G) % pr.T);
-  const int nb = (t % pr.L) < 128 ? pr.nb[0] : pr.nb[1];
-  // the first four partials are loaded before any is added (all in flight
-  // at once); the sum keeps the partials' order
-  const float4* p = in + (row * pr.stride) * N4 + n;
-  float4 v[4];
+// (float4 per element; N % 4 == 0), for the elements i0 and i0 + stride: the
+// first four partials of both are loaded before any is added, so eight
+// loads are in flight at once.
+__device__ __forceinline__ void reduce_elem2(const float4* __restrict__ in,
+                                             float4* __restrict__ out, int64_t i0, int stride,
+                                             int64_t n, const PartialRows& pr, int N4) {
+  const float4* p[2];
+  int nb[2];
+  float4 v[2][4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k)
-    if (k < nb) v[k] = p[(int64_t)k * N4];
-  float4 s = v[0];
+  for (int u = 0; u < 2; ++u) {
+    const int64_t i = i0 + (int64_t)u * stride;
+    const int64_t row = (i < n ? i : 0) / N4;
+    const int t = (int)((row / pr.G) % pr.T);
+    nb[u] = i < n ? ((t % pr.L) < 128 ? pr.nb[0] : pr.nb[1]) : 0;
+    p[u] = in + (row * pr.stride) * N4 + (i < n ? i : 0) % N4;
 #pragma unroll
-  for (int k = 1; k < 4; ++k)
-    if (k < nb) {
-      s.x += v[k].x;
-      s.y += v[k].y;
-      s.z += v[k].z;
-      s.w += v[k].w;
-    }
-  for (int k = 4; k < nb; ++k) {
-    const float4 u = p[(int64_t)k * N4];
-    s.x += u.x;
-    s.y += u.y;
-    s.z += u.z;
-    s.w += u.w;
+    for (int k = 0; k < 4; ++k)
+      if (k < nb[u]) v[u][k] = p[u][(int64_t)k * N4];
   }
-  out[i] = s;
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    if (nb[u] == 0) continue;
+    float4 s = v[u][0];
+#pragma unroll
+    for (int k = 1; k < 4; ++k)
+      if (k < nb[u]) {
+        s.x += v[u][k].x;
+        s.y += v[u][k].y;
+        s.z += v[u][k].z;
+        s.w += v[u][k].w;
+      }
+    for (int k = 4; k < nb[u]; ++k) {
+      const float4 w = p[u][(int64_t)k * N4];
+      s.x += w.x;
+      s.y += w.y;
+      s.z += w.z;
+      s.w += w.w;
+    }
+    out[i0 + (int64_t)u * stride] = s;
+  }
 }
 
 // The backward's tail in one launch of NT-thread blocks (NT = L): the first
@@ -741,8 +751,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
     return;
   }
   const int rb = blk - nfb, which = rb / nred;
-  const int64_t i = (int64_t)(rb % nred) * NT + threadIdx.x;
-  if (i < rows * N4) reduce_elem(which ? dBp : dCp, which ? dB : dC, i, which ? prB : prC, N4);
+  const int64_t i0 = (int64_t)(rb % nred) * (2 * NT) + threadIdx.x;  // two elements a thread
+  reduce_elem2(which ? dBp : dCp, which ? dB : dC, i0, NT, rows * N4, which ? prB : prC, N4);
 }
 
 // ------------------------------------------------------------------ launch
@@ -825,7 +835,7 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     const int nfin = d.nc * (d.H >> d.hs) * d.B;
     const int64_t rows = (int64_t)d.B * d.T * d.G;
     const int N4 = d.N / 4;
-    const int nred = nblk > 1 ? (int)((rows * N4 + L - 1) / L) : 0;
+    const int nred = nblk > 1 ? (int)((rows * N4 + 2 * L - 1) / (2 * L)) : 0;
     // dC's heavy tile is the chunk's last (its rows see more columns), dB's
     // the first; with one tile both counts are the heavy one
     const int c0 = L > 128 ? w.nb.light : w.nb.heavy;
