@@ -682,8 +682,8 @@ __device__ __forceinline__ void reduce_elem2(const float4* __restrict__ in,
 }
 
 // The backward's tail in one launch of NT-thread blocks (NT = L): the first
-// ceil(nfin / 4) blocks run the finalize step, four items i = (c, h, b) =
-// (i % nc, (i / nc) % H, i / (nc H)) per block, 128 rows per warp; the rest
+// ceil(nfin / 4) blocks run the finalize step, four items i = (h, c, b) =
+// (i % H, (i / H) % nc, i / (nc H)) per block, 128 rows per warp; the rest
 // sum the dC, then the dB head-block partials (nred blocks each).  The two parts are independent, so
 // the latency-bound finalize blocks and the bandwidth-bound sums share the SMs.
 // dA, ddt_bias, dD of every head from the per-chunk partials, by the block
@@ -732,8 +732,10 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
     __shared__ float4 xch[NT / 32][2];  // per item: its warps' totals, then partials
     const int H = f.H >> f.hs, warp = (int)(threadIdx.x >> 5), k = warp / W;
     const int item = blk * IPB + k;
+    // heads fastest: a block's items share their (batch, chunk) rows of dt
+    // and ddt, which are head-interleaved
     if (item < nfin)
-      finalize_item<NT>(f, item % f.nc, (item / f.nc) % H, item / (f.nc * H), warp % W, 1 + k,
+      finalize_item<NT>(f, (item / H) % f.nc, item % H, item / (f.nc * H), warp % W, 1 + k,
                         &xch[k * W][0]);
     // the last finalize block to finish also forms the parameter gradients
     // (each item's first lane wrote and fenced its partials)
