@@ -103,6 +103,33 @@ __device__ __forceinline__ void group_sync(int id) {
   asm volatile("bar.sync %0, 256;" ::"r"(id) : "memory");
 }
 
+// The persistent grid's split of the (batch, chunk, row tile, group) x head
+// items into contiguous ranges of equal cost: a head of row tile t costs its
+// 64-column panels, (L - 128 t) / 64, plus about two panels of fixed work
+// (state products, epilogue), so a CTA is not left with heavy-tile heads
+// only.  Returns the first item of range k of `parts`; range `parts` starts
+// at n_items.  Items run unit by unit, tile 0's groups before tile 1's, so
+// the cost is periodic in NLT * H items.
+template <int L>
+__device__ __forceinline__ int64_t dx_range_start(int k, int parts, int64_t n_items, int H) {
+  constexpr int NLT = L / 128, kOver = 2;
+  int64_t pc = 0;  // cost of one period (one chunk's tiles, all heads)
+#pragma unroll
+  for (int t = 0; t < NLT; ++t) pc += (int64_t)H * ((L - 128 * t) / 64 + kOver);
+  const int64_t periods = n_items / ((int64_t)NLT * H);
+  const int64_t target = (periods * pc * k) / parts;  // cost before range k
+  const int64_t q = target / pc;
+  int64_t rem = target - q * pc, i = q * NLT * H;
+#pragma unroll
+  for (int t = 0; t < NLT; ++t) {
+    const int64_t w = (L - 128 * t) / 64 + kOver;
+    if (rem <= (int64_t)H * w) return i + (rem + w - 1) / w;  // first item whose prefix reaches it
+    rem -= (int64_t)H * w;
+    i += H;
+  }
+  return i;
+}
+
 template <int N, int L>
 __global__ void __launch_bounds__(512, 1)
     k_scan_tc(const __grid_constant__ CUtensorMap mOut, const __grid_constant__ CUtensorMap mOp,
@@ -113,7 +140,7 @@ __global__ void __launch_bounds__(512, 1)
               const unsigned char* __restrict__ simg, const float* __restrict__ D,
               float* __restrict__ ddir, float* __restrict__ qrow,
               float* __restrict__ ddiag, int B_, int T, int H, int G, int nc, int hs,
-              int items_per_cta, int* status) {
+              int* status) {
   using SM = ScanSmem<N, L>;
   constexpr int LT = SM::kLT, NLT = L / LT;
   griddep_wait();  // the state images and vectors come from the previous kernels
@@ -131,8 +158,8 @@ __global__ void __launch_bounds__(512, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hpg = H / G;
   const int64_t n_items = (int64_t)B_ * nc * NLT * H;  // (batch, chunk, tile, group) x head
-  const int64_t it_begin = (int64_t)blockIdx.x * items_per_cta;
-  const int64_t it_end = min(n_items, it_begin + items_per_cta);
+  const int64_t it_begin = dx_range_start<L>(blockIdx.x, gridDim.x, n_items, H);
+  const int64_t it_end = dx_range_start<L>(blockIdx.x + 1, gridDim.x, n_items, H);
   const bf16* rowsrc = Bm;
   const bf16* colsrc = Cm;
 
@@ -758,14 +785,12 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
 }
 
 // ------------------------------------------------------------------ launch
-// Persistent scan kernels: one CTA per SM, each taking a contiguous range of
-// the (batch, chunk, row tile, group) x head items, so every SM gets the same
-// number of heads (+-1) whatever the shape.
-void scan_partition(const Dims& d, int sms, int* grid, int* per) {
+// The persistent dx kernel: one CTA per SM (at most one per item), each
+// taking a contiguous range of the (batch, chunk, row tile, group) x head
+// items of equal cost (dx_range_start).
+int scan_grid(const Dims& d, int sms) {
   const int64_t items = (int64_t)d.B * d.nc * (d.L / 128) * d.H;
-  const int64_t g = items < sms ? items : sms;
-  *per = (int)((items + g - 1) / g);
-  *grid = (int)((items + *per - 1) / *per);
+  return (int)(items < sms ? items : sms);
 }
 
 template <int N, int L, typename Tout>
@@ -810,8 +835,7 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     using SM = ScanSmem<N, L>;
     auto kern = k_scan_tc<N, L>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
-    int grid, per;
-    scan_partition(d, sms, &grid, &per);
+    const int grid = scan_grid(d, sms);
     CUtensorMap mDX, mDY, mXr;
     if (!make_y_map(&mDX, a.dx, d.H, d.T, d.B, 32) ||
         !make_tma_map(&mDY, dy, 64, d.H, d.T, d.B, 1, 128) ||
@@ -820,7 +844,7 @@ cudaError_t launch_tc_backward_nl(const Dims& d, const BwdArgs& a, const TcBwdWs
     SSD_LAUNCH("k_scan_tc_dx", s, launch_pdl(kern, dim3(grid), dim3(512), SM::kBytes, s,
         mDX, mDY, mXr, static_cast<const bf16*>(a.f.x), static_cast<const bf16*>(a.f.B), Cm, w.delta, w.acs,
         static_cast<const unsigned char*>(w.dSimg), a.f.D, w.ddir, w.qrow, w.ddiag, d.B, d.T,
-        d.H, d.G, d.nc, d.hs, per, status));
+        d.H, d.G, d.nc, d.hs, status));
   }
   const int nblk = w.nb.max();  // partial slots per row
   float* dCout = nblk == 1 ? a.dC : w.dCp;
